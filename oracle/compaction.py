@@ -1,0 +1,25 @@
+"""Keep-mask compaction (test infrastructure only).
+
+Collider abstract: the would-be sparse GEMM over all tokens becomes a
+"dimension-reduced dense GEMM" over the kept tokens.  The reduction needs the
+list of kept tokens; this is its plain definition: the ascending flat indices
+of the nonzero mask entries, the number of kept tokens before each sequence
+start, and the total.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def compact(keep: np.ndarray):
+    """keep: [B, T] (nonzero = kept).  Returns (idx int32 [n_kept], cu_kept
+    int32 [B+1], n_kept int).  idx is strictly increasing; cu_kept[b] is the
+    number of kept tokens in sequences 0..b-1."""
+    keep = np.asarray(keep)
+    B, T = keep.shape
+    flat = keep.reshape(-1) != 0
+    idx = np.flatnonzero(flat).astype(np.int32)
+    per_seq = flat.reshape(B, T).sum(axis=1)
+    cu = np.zeros(B + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(per_seq)
+    return idx, cu, int(idx.size)
