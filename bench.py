@@ -1,0 +1,398 @@
+"""Benchmark of the filtered decoder-block backward on one GB300.
+
+Workload: one TinyLlama-1.1B-shaped block (d_model 2048, 32 query / 4 kv heads
+of 64, SwiGLU 5632, RMSNorm, RoPE base 10000), batch 4 x 2048 tokens, causal;
+40% of each sequence filtered by the lowest Gumbel(0,1) scores; weights
+N(0, 0.02), block input and upstream gradient N(0, 1); all synthetic and
+seeded.  A step is the whole hot path: compaction of the keep-mask, gather of
+the kept rows, the dimension-reduced GEMMs, the filtered attention backward,
+the norm / activation / RoPE backward and the scatter of dx.
+
+Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+on the host cores instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "filtered-backward tokens/s, TFLOP/s vs bf16 TC peak, speedup vs unfiltered"
+WORKLOAD = "tinyllama_layer"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def config_dict(s, l2):
+    return {"workload": f"{WORKLOAD}: TinyLlama-1.1B-shaped decoder block backward, batch {s.B} x seq {s.T}, "
+                        f"d_model {s.D}, heads {s.H}/{s.Hkv}x{s.dh}, SwiGLU {s.F}, "
+                        f"{int(s.f * 100)}% tokens filtered per sequence (Gumbel scores)",
+            "global_batch": s.B, "seq_len": s.T, "filtered_fraction": s.f, "parallelism": "replicas",
+            "l2": l2}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work (counted over kept tokens only)
+def gemm_flops(s, nk):
+    p_lin = s.D * s.Nqkv + s.H * s.dh * s.D + s.D * s.Nup + s.F * s.D
+    return 4.0 * nk * p_lin
+
+
+def attn_flops(s, kept_per_seq):
+    return 10.0 * s.dh * s.H * sum(m * (m + 1) / 2 for m in kept_per_seq)
+
+
+# ---------------------------------------------------------------------------
+# synthetic saved activations: a dense bf16 forward on the GPU (input
+# preparation only, outside every timed region)
+def gpu_forward(s, w, x):
+    import torch
+    dev = x.device
+    M = s.M
+    f = lambda t: t.float()
+    xf = f(x)
+    rstd1 = torch.rsqrt(xf.pow(2).mean(-1) + s.eps)
+    a = (xf * rstd1[:, None] * f(w["norm1_w"])).bfloat16()
+    qkv = (f(a) @ f(w["w_qkv"])).bfloat16()
+    nq, nk = s.H * s.dh, s.Hkv * s.dh
+    pos = torch.arange(s.T, device=dev).repeat(s.B).double()
+    half = s.rotary_dim // 2
+    inv = s.rope_base ** (-(2.0 * torch.arange(half, device=dev, dtype=torch.float64)) / s.rotary_dim)
+    ang = pos[:, None] * inv[None, :]
+    cos, sin = torch.cos(ang).float()[:, None, :], torch.sin(ang).float()[:, None, :]
+
+    def rope(t, nh):
+        t = f(t).view(M, nh, s.dh)
+        x1, x2, rest = t[..., :half], t[..., half:s.rotary_dim], t[..., s.rotary_dim:]
+        return torch.cat([x1 * cos - x2 * sin, x2 * cos + x1 * sin, rest], -1).bfloat16()
+
+    q = rope(qkv[:, :nq], s.H)
+    k = rope(qkv[:, nq:nq + nk], s.Hkv)
+    v = qkv[:, nq + nk:].reshape(M, s.Hkv, s.dh)
+    qkv_rot = torch.cat([q.reshape(M, -1), k.reshape(M, -1), v.reshape(M, -1)], 1).contiguous()
+    o = torch.empty(M, s.H, s.dh, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(s.B, s.H, s.T, dtype=torch.float32, device=dev)
+    causal = torch.ones(s.T, s.T, dtype=torch.bool, device=dev).tril()
+    G = s.H // s.Hkv
+    for b in range(s.B):
+        rows = slice(b * s.T, (b + 1) * s.T)
+        for h in range(s.H):
+            S = f(q[rows, h]) @ f(k[rows, h // G]).T / math.sqrt(s.dh)
+            S = S.masked_fill(~causal, float("-inf"))
+            l = torch.logsumexp(S, -1)
+            o[rows, h] = (torch.exp(S - l[:, None]) @ f(v[rows, h // G])).bfloat16()
+            lse[b, h] = l
+    o = o.reshape(M, -1)
+    h_ = (xf + f(o) @ f(w["w_o"])).bfloat16()
+    rstd2 = torch.rsqrt(f(h_).pow(2).mean(-1) + s.eps)
+    bn = (f(h_) * rstd2[:, None] * f(w["norm2_w"])).bfloat16()
+    gu = (f(bn) @ f(w["w_up"])).bfloat16()
+    g_, u_ = f(gu[:, :s.F]), f(gu[:, s.F:])
+    sact = (g_ * torch.sigmoid(g_) * u_).bfloat16()
+    return dict(x=x, a=a, rstd1=rstd1, qkv=qkv_rot, o=o, lse=lse, h=h_, b=bn, rstd2=rstd2, up=gu, s=sact)
+
+
+# ---------------------------------------------------------------------------
+class Clocks:
+    """nvidia-smi samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.p = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        if self.p is not None:
+            self.p.terminate()
+            self.p.wait(timeout=10)
+            self.f.close()
+
+    def summary(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [x for x in sm if x > 0.5 * max(sm)] or sm
+        return {"sm_mhz": float(np.median(loaded)), "sm_max_mhz": float(max(smax)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ---------------------------------------------------------------------------
+def cpu_baseline(s, budget_s=20.0):
+    """The fp64 oracle, as it stands, on one sequence of the workload."""
+    from oracle import block as ob
+    one = s.with_(B=1)
+    w = workloads.layer_weights(s)
+    t = workloads.layer_inputs(s)
+    T = s.T
+    x, dout, keep = t["x"][:T], t["dout"][:T], t["keep"][:1]
+    _, saved = ob.block_forward(x, w, one, round_saved=True)
+    t0 = time.perf_counter()
+    ob.block_backward(dout, saved, w, one, keep)
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    return {"value": T / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"1 of {s.B} sequences ({T} tokens, {int(keep.sum())} kept), fp64 numpy, "
+                      f"backward only, {dt:.1f} s"}
+
+
+def run_reference(args):
+    s = workloads.WORKLOADS[WORKLOAD]
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    times = []
+    cb = None
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(s)
+        if i >= args.warmup:
+            times.append(s.T / r["value"])
+            cb = r
+    sec = float(np.mean(times))
+    val = s.T / sec
+    cb = dict(cb, value=val)
+    print(json.dumps({"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+                      "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                      "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+                      "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                      "config": config_dict(s, "n/a (CPU)"), "cpu_baseline": cb,
+                      "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                              "d2h_bytes_per_step": 0}}))
+
+
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import sparse_backward_gemm_gb300 as cl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    s = workloads.WORKLOADS[WORKLOAD]
+    M = s.M
+
+    # ---- inputs (seeded, synthetic) -------------------------------------
+    wn = workloads.layer_weights(s)
+    tn = workloads.layer_inputs(s)
+    W = {k: torch.from_numpy(v).to(dev).bfloat16() for k, v in wn.items()}
+    x = torch.from_numpy(tn["x"]).to(dev).bfloat16()
+    dout = torch.from_numpy(tn["dout"]).to(dev).bfloat16()
+    masks = {"filtered": torch.from_numpy(tn["keep"]).to(dev),
+             "unfiltered": torch.ones(s.B, s.T, dtype=torch.uint8, device=dev)}
+    with torch.no_grad():
+        saved = gpu_forward(s, W, x)
+    torch.cuda.synchronize()
+
+    desc = cl.LayerDesc(arch=cl.ARCH_LLAMA, B=s.B, T=s.T, D=s.D, H=s.H, Hkv=s.Hkv, dh=s.dh, F=s.F,
+                        rotary_dim=s.rotary_dim, rope_base=s.rope_base, norm=cl.NORM_RMS, eps=s.eps,
+                        act=cl.ACT_SWIGLU)
+    weights = cl.LayerWeights(**{k: W[k].data_ptr() for k in ("norm1_w", "w_qkv", "w_o", "norm2_w", "w_up",
+                                                               "w_down")})
+    sv = cl.LayerSaved(**{k: saved[k].data_ptr() for k in saved})
+    gshapes = dict(dnorm1_w=(s.D,), dw_qkv=(s.D, s.Nqkv), dw_o=(s.H * s.dh, s.D), dnorm2_w=(s.D,),
+                   dw_up=(s.D, s.Nup), dw_down=(s.F, s.D))
+    G = {k: torch.empty(v, dtype=torch.float32, device=dev) for k, v in gshapes.items()}
+    dx = torch.empty(M, s.D, dtype=torch.bfloat16, device=dev)
+    grads = cl.LayerGrads(dx=dx.data_ptr(), **{k: v.data_ptr() for k, v in G.items()})
+    ws = torch.empty(cl.collider_layer_workspace_size(desc), dtype=torch.uint8, device=dev)
+    idx = torch.empty(M, dtype=torch.int32, device=dev)
+    cu = torch.empty(s.B + 1, dtype=torch.int32, device=dev)
+    nk = torch.empty(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(mask):
+        cl.collider_compact(mask, s.B, s.T, idx, cu, nk, None, stream)
+        cl.collider_layer_bwd(desc, weights, sv, dout, cl.ROWS_FULL, idx, cu, nk, grads, cl.ROWS_FULL, ws, stream)
+
+    def timed(mask, K, Wm):
+        for _ in range(Wm):
+            step(mask)
+        cl.collider_check(stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        cl.collider_launch_count(1)
+        for e0, e1 in ev:
+            flush.fill_(1)   # evict L2 between steps
+            e0.record(stream)
+            step(mask)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        launches = cl.collider_launch_count(1)
+        if world > 1:
+            dist.barrier()
+        cl.collider_check(stream)
+        ms = [a.elapsed_time(b) for a, b in ev]
+        return float(np.mean(ms)), launches
+
+    # ---- main timed region (filtered) with clock sampling ----------------
+    with Clocks(local) as clk:
+        ms_f, launches = timed(masks["filtered"], args.steps, args.warmup)
+    clocks = clk.summary()
+    ms_u, _ = timed(masks["unfiltered"], args.steps, args.warmup)
+    if world > 1:
+        t = torch.tensor([ms_f, ms_u], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_f, ms_u = t.tolist()
+
+    # ---- per-kernel times from the library profiler (separate pass) ------
+    n_kept = int(tn["keep"].sum())
+    kept_per_seq = tn["keep"].sum(axis=1).tolist()
+    cl.collider_profile_enable(1)
+    for _ in range(args.steps):
+        flush.fill_(1)
+        step(masks["filtered"])
+    torch.cuda.synchronize()
+    cl.collider_profile_enable(0)
+    per = {}
+    gemm_ms, gemm_fl = 0.0, 0.0
+    for i in range(cl.collider_profile_count()):
+        name, (m, n, k, dyn), ms = cl.collider_profile_get(i)
+        d = per.setdefault(name, [0, 0.0])
+        d[0] += 1
+        d[1] += ms
+        if name == "tc_gemm":
+            mm = n_kept if dyn == 1 else m
+            kk = n_kept if dyn == 2 else k
+            gemm_ms += ms
+            gemm_fl += 2.0 * mm * n * kk
+    peaks, src = measured_peaks()
+    achieved = gemm_fl / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else 0.0
+    step_ms_prof = sum(v[1] for v in per.values()) / args.steps
+
+    # ---- end to end through the C ABI with host buffers ------------------
+    host_in = {k: v.cpu().pin_memory() for k, v in saved.items()}
+    host_dout = dout.cpu().pin_memory()
+    host_mask = masks["filtered"].cpu().pin_memory()
+    dev_in = {k: torch.empty_like(v) for k, v in saved.items()}
+    dev_dout = torch.empty_like(dout)
+    dev_mask = torch.empty_like(masks["filtered"])
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in G.items()}
+    host_dx = torch.empty(dx.shape, dtype=dx.dtype).pin_memory()
+    sv_e2e = cl.LayerSaved(**{k: dev_in[k].data_ptr() for k in dev_in})
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values()) + host_dout.numel() * 2 + host_mask.numel()
+    d2h = sum(v.numel() * 4 for v in G.values()) + dx.numel() * 2
+
+    def e2e_step():
+        for k in host_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        dev_dout.copy_(host_dout, non_blocking=True)
+        dev_mask.copy_(host_mask, non_blocking=True)
+        cl.collider_compact(dev_mask, s.B, s.T, idx, cu, nk, None, stream)
+        cl.collider_layer_bwd(desc, weights, sv_e2e, dev_dout, cl.ROWS_FULL, idx, cu, nk, grads, cl.ROWS_FULL, ws,
+                              stream)
+        for k in G:
+            host_out[k].copy_(G[k], non_blocking=True)
+        host_dx.copy_(dx, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = t.item()
+
+    if rank == 0:
+        tokens = s.M * world
+        line = {
+            "metric": METRIC, "value": tokens / (ms_f * 1e-3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_f, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_dict(s, "flushed: 256 MB device write before every timed step, outside its events"),
+            "kept_tokens": n_kept,
+            "tflops": (gemm_flops(s, n_kept) + attn_flops(s, kept_per_seq)) / (ms_f * 1e-3) / 1e12,
+            "unfiltered_ms_per_step": ms_u, "speedup_vs_unfiltered": ms_u / ms_f,
+            "roofline": {"bound": "tensor", "kernel": "tc_gemm (tcgen05 bf16 GEMM, all launches of a step)",
+                         "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": achieved / peaks["bf16_tflops"], "peak_source": f"bf16_tflops ({src})",
+                         "traffic": None, "gemm_ms_per_step": gemm_ms / args.steps,
+                         "step_ms_profiled": step_ms_prof},
+            "kernels_ms_per_step": {k: round(v[1] / args.steps, 4) for k, v in sorted(per.items())},
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(s)
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)

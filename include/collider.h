@@ -1,0 +1,311 @@
+/*
+ * libcollider -- filtered transformer backward on one GB300 (sm_103a).
+ *
+ * The method ("Enhancing Token Filtering Efficiency in Large Language Model
+ * Training with Collider", arXiv 2502.00340):
+ *   - the forward stays dense; a token filter marks each token kept or
+ *     filtered and drops the loss of filtered tokens (Fig. 2b);
+ *   - in backward, the activations and output gradients of filtered tokens
+ *     are dropped in EVERY layer, not only at the loss (abstract; TL;DR
+ *     "backward activation filtering across all layers");
+ *   - inside attention the softmax of filtered tokens is filtered as well, so
+ *     that G_V -- and the activations used for the Q and K gradients -- stay
+ *     sparse (Fig. 3, Fig. 5);
+ *   - each would-be sparse GEMM runs as a dimension-reduced dense GEMM over
+ *     the kept rows only (abstract).
+ *
+ * Conventions shared by every entry point
+ *   Ownership   The caller owns every buffer and the stream.  Pointers are
+ *               DEVICE pointers unless a parameter says otherwise.  Entry
+ *               points allocate no device memory, except that the first call
+ *               on a device allocates a 256-byte status word for that device.
+ *               Scratch comes from the caller's workspace `ws` (`ws_bytes`
+ *               long, 256-byte aligned), sized by the *_workspace_size calls.
+ *   Asynchrony  Every call enqueues work on `stream` (a cudaStream_t, may be
+ *               NULL for the legacy default stream) and returns without
+ *               synchronising.  n_kept stays on the device.
+ *   Errors      Argument errors are detected on the host and returned at
+ *               once; nothing is enqueued then.  A CUDA launch error is
+ *               COLLIDER_ERR_CUDA.  Every wait inside a kernel is bounded;
+ *               a wait that runs out sets the device status word, the kernel
+ *               returns early, and collider_check() reports
+ *               COLLIDER_ERR_TIMEOUT.  collider_last_error() gives a
+ *               thread-local message for the last failing call.  No C++
+ *               exception crosses this interface.
+ *   Layouts     Row-major.  Tokens are M = B*T rows in sequence order
+ *               (token t of sequence b is row b*T + t).  Linear weights are
+ *               stored [in, out] (Y = X.W).  bf16 = IEEE bfloat16 storage,
+ *               f32 = IEEE binary32.  "FULL" token rows means one row per
+ *               token (M rows; filtered rows of an output are written 0);
+ *               "COMPACT" means one row per kept token, in kept order
+ *               (n_kept rows, row r is token idx[r]).  COMPACT outputs are
+ *               written with zero rows from n_kept up to the next multiple
+ *               of 128 (within the M-row capacity).
+ *   Keep-mask   uint8 [B, T]; nonzero = kept.
+ */
+#ifndef COLLIDER_H
+#define COLLIDER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  COLLIDER_OK = 0,
+  COLLIDER_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, workspace too small */
+  COLLIDER_ERR_UNSUPPORTED = 2, /* shape or option this build does not handle */
+  COLLIDER_ERR_CUDA = 3,        /* a CUDA call failed (incl. an earlier asynchronous error) */
+  COLLIDER_ERR_TIMEOUT = 4      /* a bounded in-kernel wait ran out (see collider_check) */
+} collider_status;
+
+typedef enum { COLLIDER_F32 = 0, COLLIDER_BF16 = 1 } collider_dtype;
+typedef enum { COLLIDER_ROWS_FULL = 0, COLLIDER_ROWS_COMPACT = 1 } collider_rows;
+typedef enum { COLLIDER_ARCH_LLAMA = 0, COLLIDER_ARCH_PHI = 1 } collider_arch;
+typedef enum { COLLIDER_NORM_RMS = 0, COLLIDER_NORM_LAYER = 1 } collider_norm;
+typedef enum { COLLIDER_ACT_SWIGLU = 0, COLLIDER_ACT_GELU_TANH = 1 } collider_act;
+
+/* ------------------------------------------------------------------------ */
+/* Status                                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* Message describing the last failing call made by this host thread
+ * ("" if none).  The string stays valid until the thread's next call. */
+const char* collider_last_error(void);
+
+/* Synchronises `stream`, then reports (and clears) the device status word:
+ * COLLIDER_ERR_TIMEOUT if a kernel's bounded wait ran out since the last
+ * check, COLLIDER_ERR_CUDA if the stream holds an asynchronous CUDA error. */
+collider_status collider_check(void* stream);
+
+/* Number of kernels this library has launched on the calling host thread
+ * since the last reset (reset=1 returns the count and zeroes it). */
+long long collider_launch_count(int reset);
+
+/* Launch profiler (per host thread).  While enabled, every kernel launch of
+ * the library is bracketed by a pair of CUDA events recorded on the launch
+ * stream.  collider_profile_enable(1) clears earlier records and turns
+ * recording on; (0) turns it off and keeps the records.  collider_profile_get
+ * returns record i: the kernel's name (static string), for GEMM launches
+ * mnk_dyn = {M, N, K, dyn} (dyn 1: M is the device-resident kept count, 2: K
+ * is; all 0 for other kernels), and the elapsed milliseconds between the two
+ * events (waits for them).  Returns -1 for an index out of range. */
+int collider_profile_enable(int on);
+int collider_profile_count(void);
+int collider_profile_get(int i, const char** name, long long* mnk_dyn, float* ms);
+
+/* ------------------------------------------------------------------------ */
+/* a1. Compaction  (abstract: the dimension-reduced GEMM runs over the kept  */
+/*     tokens; this is the index list it runs over)                          */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes collider_compact needs for B*T tokens (0 when B*T <=
+ * 4,194,304: a single thread block scans the mask). */
+size_t collider_compact_workspace_size(int B, int T);
+
+/* mask [B,T] u8 -> idx i32 [capacity B*T] (ascending flat indices of kept
+ * tokens, first n_kept entries written), cu_kept i32 [B+1] (kept tokens
+ * before sequence b; cu_kept[B] = n_kept), n_kept i32 [1].  All device.
+ * Bit-exact; deterministic.  B >= 1, T >= 1, B*T < 2^31. */
+collider_status collider_compact(const uint8_t* mask, int B, int T, int32_t* idx,
+                                 int32_t* cu_kept, int32_t* n_kept, void* ws,
+                                 size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* a2. Row gather / scatter (abstract: activations of filtered tokens are    */
+/*     filtered across all layers)                                           */
+/* ------------------------------------------------------------------------ */
+
+/* dst[r, :] = src[idx[r], :] for r < n_kept; dst rows n_kept .. next
+ * multiple of 128 (below M) are zeroed.  row_bytes, src_ld_bytes and
+ * dst_ld_bytes are multiples of 16 and both pointers 16-byte aligned.  src
+ * has M rows, dst has room for M rows. */
+collider_status collider_gather_rows(const void* src, size_t src_ld_bytes, void* dst,
+                                     size_t dst_ld_bytes, size_t row_bytes, int M,
+                                     const int32_t* idx, const int32_t* n_kept, void* stream);
+
+/* full[t, :] = compact[r, :] where idx[r] == t, and full[t, :] = 0 for every
+ * filtered token t < M.  Same alignment rules as collider_gather_rows. */
+collider_status collider_scatter_rows(const void* compact, size_t compact_ld_bytes, void* full,
+                                      size_t full_ld_bytes, size_t row_bytes, int M,
+                                      const int32_t* idx, const int32_t* n_kept, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* a3/a4. Linear backward (abstract: sparse GEMM -> dimension-reduced dense  */
+/*        GEMM)                                                              */
+/* ------------------------------------------------------------------------ */
+
+/* Y = X.W (+b) with X [M,K], W [K,N] (stored [in=K, out=N]), dY [M,N] rows:
+ *   dX_k = dY_k . W^T        (only kept rows; filtered rows of a FULL dX = 0)
+ *   dW   = X_k^T . dY_k      ([K,N] f32, overwritten)
+ *   db   = column sums of dY_k ([N] f32, overwritten; may be NULL)
+ * dtype COLLIDER_F32: X, W, dY, dX are f32 and the arithmetic is f32 FMA
+ * (no TF32).  COLLIDER_BF16: X, W, dY, dX are bf16, products accumulate in
+ * f32 on the tensor cores.  x_rows / dy_rows say whether X and dY hold M
+ * (FULL, read through idx) or n_kept (COMPACT) rows; dx_rows likewise for
+ * the output.  dX may be NULL (skip), dW may be NULL (skip).
+ * bf16 needs K % 8 == 0 and N % 8 == 0 and 16-byte aligned pointers.
+ * Workspace: collider_linear_workspace_size(). */
+size_t collider_linear_workspace_size(collider_dtype dtype, int M, int K, int N);
+collider_status collider_linear_bwd(collider_dtype dtype, int M, int K, int N,
+                                    const void* X, collider_rows x_rows, const void* W,
+                                    const void* dY, collider_rows dy_rows,
+                                    const int32_t* idx, const int32_t* n_kept,
+                                    void* dX, collider_rows dx_rows, float* dW, float* db,
+                                    void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* a7/a8. Attention backward over the compacted sequences (Figs. 3 and 5)    */
+/* ------------------------------------------------------------------------ */
+
+/* Causal (or not) GQA attention backward with filtered probabilities:
+ *   P_ij  = exp(S_ij - lse_i), S = Q K^T * scale, on pairs with pos_j <= pos_i
+ *           inside one sequence (original positions; P is not renormalised)
+ *   P'_ij = P_ij for kept i and kept j, else 0
+ *   dV = P'^T dO;  dP = dO V^T;  D_i = sum_j P'_ij dP_ij;
+ *   dS = P' * (dP - D);  dQ = dS K * scale;  dK = dS^T Q * scale
+ * summed over each group of H/Hkv query heads for dK and dV (query head h
+ * reads kv head h*Hkv/H).
+ * Q [rows, H, dh], K and V [rows, Hkv, dh], dO [rows, H, dh], all bf16 with
+ * row strides q_ld, kv_ld, do_ld (elements); `rows` is M (in_rows FULL, read
+ * through idx) or n_kept (COMPACT).  O is not read (D is taken over P', not
+ * from the forward output) and may be NULL.  lse f32 [B, H, T] (natural
+ * log, from the dense forward).  Outputs dQ [*, H, dh], dK, dV [*, Hkv, dh]
+ * bf16 with the same row strides as the inputs, FULL or COMPACT per
+ * out_rows.  rotary_dim > 0 additionally applies the RoPE backward
+ * (rotate-half pairing on the first rotary_dim dims, angle pos*base^(-2i/r))
+ * to dQ and dK so they are gradients with respect to the pre-rotation q, k.
+ * dh in {64, 128}; H % Hkv == 0.  Workspace: collider_attn_workspace_size(). */
+size_t collider_attn_workspace_size(int B, int T, int H, int Hkv, int dh);
+collider_status collider_attn_bwd(int B, int T, int H, int Hkv, int dh, int causal, float scale,
+                                  int rotary_dim, float rope_base,
+                                  const void* Q, const void* K, const void* V, const void* O,
+                                  const void* dO, int q_ld, int kv_ld, int do_ld,
+                                  collider_rows in_rows, const float* lse,
+                                  const int32_t* idx, const int32_t* cu_kept,
+                                  const int32_t* n_kept, void* dQ, void* dK, void* dV,
+                                  collider_rows out_rows, void* ws, size_t ws_bytes,
+                                  void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Whole decoder block                                                       */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  int arch;          /* collider_arch: LLAMA (sequential, SwiGLU) or PHI (parallel block) */
+  int B, T;          /* batch, sequence length */
+  int D;             /* model width */
+  int H, Hkv, dh;    /* query heads, kv heads, head dim (64 or 128) */
+  int F;             /* MLP hidden width */
+  int rotary_dim;    /* RoPE dims per head (== dh for full, 32 for Phi-style partial) */
+  float rope_base;
+  int norm;          /* collider_norm */
+  float eps;         /* norm epsilon (informational: the saved rstd already includes it) */
+  int act;           /* collider_act: SWIGLU (llama) or GELU_TANH (phi) */
+  int qkv_bias, out_bias, mlp_bias; /* which bias gradients to produce */
+} collider_layer_desc;
+
+/* Weights the backward reads (bf16).  Biases and LayerNorm beta are not
+ * read by the backward.  w_up is [D, 2F] = [gate | up] for SwiGLU and
+ * [D, F] (fc1) for GELU; w_down [F, D]; w_qkv [D, (H+2Hkv)dh] with columns
+ * [q heads | k heads | v heads]; w_o [H*dh, D]. norm2_w unused for PHI. */
+typedef struct {
+  const void* norm1_w;
+  const void* w_qkv;
+  const void* w_o;
+  const void* norm2_w;
+  const void* w_up;
+  const void* w_down;
+} collider_layer_weights;
+
+/* Saved forward activations, FULL rows (M = B*T), bf16 unless noted:
+ *   x [M,D] block input; a [M,D] = norm1(x); mean1 f32 [M] (LayerNorm only);
+ *   rstd1 f32 [M]; qkv [M,(H+2Hkv)dh] with q and k AFTER RoPE; o [M,H*dh]
+ *   attention output; lse f32 [B,H,T].
+ *   LLAMA: h [M,D] = x + attn; b [M,D] = norm2(h); rstd2 f32 [M];
+ *          up [M,2F] = [g | u]; s [M,F] = silu(g)*u.
+ *   PHI:   up [M,F] = fc1 output before GELU; h, b, rstd2, s unused. */
+typedef struct {
+  const void* x;
+  const void* a;
+  const float* mean1;
+  const float* rstd1;
+  const void* qkv;
+  const void* o;
+  const float* lse;
+  const void* h;
+  const void* b;
+  const float* rstd2;
+  const void* up;
+  const void* s;
+} collider_layer_saved;
+
+/* Gradients (all overwritten).  dx bf16 [M or n_kept, D] per dx_rows; every
+ * other gradient f32 with its weight's shape.  Pointers for gradients the
+ * block does not have (e.g. dnorm1_b for RMSNorm, biases when the desc says
+ * none) are ignored and may be NULL. */
+typedef struct {
+  void* dx;
+  float* dnorm1_w;
+  float* dnorm1_b;
+  float* dw_qkv;
+  float* db_qkv;
+  float* dw_o;
+  float* db_o;
+  float* dnorm2_w;
+  float* dw_up;
+  float* db_up;
+  float* dw_down;
+  float* db_down;
+} collider_layer_grads;
+
+/* Filtered backward of one block: dOut (FULL or COMPACT rows, bf16 [*, D])
+ * -> every gradient of the block.  Gathers the kept rows of the saved set,
+ * runs the dimension-reduced GEMMs, the filtered attention backward, the
+ * norm/activation/RoPE backward and the bias/norm-weight column sums on
+ * kept rows only.  Deterministic except dQ (accumulated with f32 atomics
+ * inside the attention backward).  Workspace: collider_layer_workspace_size. */
+size_t collider_layer_workspace_size(const collider_layer_desc* desc);
+collider_status collider_layer_bwd(const collider_layer_desc* desc,
+                                   const collider_layer_weights* w,
+                                   const collider_layer_saved* saved,
+                                   const void* dOut, collider_rows dout_rows,
+                                   const int32_t* idx, const int32_t* cu_kept,
+                                   const int32_t* n_kept, const collider_layer_grads* grads,
+                                   collider_rows dx_rows, void* ws, size_t ws_bytes,
+                                   void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Whole stack: embedding -> L blocks -> final RMSNorm -> LM head -> CE      */
+/* ------------------------------------------------------------------------ */
+
+/* Loss = mean over kept tokens of cross-entropy(logits_t, targets_t) (the
+ * token filter drops the loss of filtered tokens, Fig. 2b).  The same keep
+ * mask applies in every block.  Inputs (FULL rows): logits bf16 [M,V] (saved
+ * by the forward), targets i32 [M], ids i32 [M] (input token ids), y bf16
+ * [M,D] final-norm output, xL bf16 [M,D] final-norm input, rstdf f32 [M],
+ * normf_w bf16 [D], w_lm bf16 [D,V]; per-block weights and saved sets
+ * (arrays of L, block 0 first).  Outputs: the weight gradients of each block
+ * in grads[l] (grads[l].dx is not used: gradients between blocks stay in the
+ * workspace, COMPACT), dnormf_w f32 [D], dw_lm f32 [D,V], dE f32 [V,D] (rows
+ * of token ids never seen at a kept position are 0).  LLAMA blocks, D <= 2048,
+ * V % 8 == 0.  Workspace: collider_stack_workspace_size. */
+size_t collider_stack_workspace_size(const collider_layer_desc* desc, int L, int V);
+collider_status collider_stack_bwd(const collider_layer_desc* desc, int L, int V,
+                                   const collider_layer_weights* w,
+                                   const collider_layer_saved* saved,
+                                   const void* logits, const int32_t* targets,
+                                   const int32_t* ids, const void* y, const void* xL,
+                                   const float* rstdf, const void* normf_w, const void* w_lm,
+                                   const int32_t* idx, const int32_t* cu_kept,
+                                   const int32_t* n_kept, const collider_layer_grads* grads,
+                                   float* dnormf_w, float* dw_lm, float* dE, void* ws,
+                                   size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* COLLIDER_H */

@@ -1,0 +1,847 @@
+// C ABI of libcollider: argument checks, status reporting, workspace carving,
+// the launch profiler, and the orchestration of the filtered backward of a
+// decoder block and of a decoder stack (Collider, arXiv 2502.00340: activations
+// and gradients of filtered tokens are dropped in every layer, the attention
+// probabilities are filtered, and each GEMM runs dimension-reduced over the
+// kept rows).
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/collider.h"
+#include "internal.h"
+
+namespace collider {
+
+// ---------------------------------------------------------------------------
+// thread-local error message, launch count, profiler
+namespace {
+thread_local std::string g_msg;
+thread_local long long g_launches = 0;
+
+struct ProfRec {
+  const char* name;
+  long long m, n, k;
+  int dyn;
+  cudaEvent_t e0, e1;
+};
+thread_local bool g_prof_on = false;
+thread_local std::vector<ProfRec> g_prof;
+thread_local std::vector<cudaEvent_t> g_event_pool;
+thread_local size_t g_event_used = 0;
+thread_local cudaStream_t g_prof_stream = nullptr;
+
+cudaEvent_t next_event() {
+  if (g_event_used == g_event_pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    g_event_pool.push_back(e);
+  }
+  return g_event_pool[g_event_used++];
+}
+
+collider_status fail(collider_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_msg = buf;
+  return s;
+}
+
+collider_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(COLLIDER_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+// per-device status word and SM count
+struct DevInfo {
+  DevStatus* st = nullptr;
+  int num_sms = 0;
+};
+std::mutex g_dev_mu;
+DevInfo g_dev[64];
+
+collider_status make_ctx(void* stream, Ctx* c) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(COLLIDER_ERR_UNSUPPORTED, "device ordinal %d >= 64", dev);
+  // an asynchronous error from earlier work is reported first
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "earlier asynchronous error");
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.st) {
+    void* p = nullptr;
+    e = cudaMalloc(&p, 256);
+    if (e != cudaSuccess) return cuda_fail(e, "status word allocation");
+    e = cudaMemset(p, 0, 256);
+    if (e != cudaSuccess) return cuda_fail(e, "status word reset");
+    d.st = static_cast<DevStatus*>(p);
+    e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "SM count");
+  }
+  c->stream = static_cast<cudaStream_t>(stream);
+  c->st = d.st;
+  c->num_sms = d.num_sms;
+  return COLLIDER_OK;
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+size_t up256(size_t b) { return (b + 255) & ~size_t(255); }
+long long pad128(long long m) { return (m + 127) & ~127ll; }
+
+// bump allocator over the caller's workspace
+struct Carver {
+  char* base;
+  size_t size;
+  size_t used = 0;
+  bool dry;  // sizing pass
+  template <typename T>
+  T* take(size_t count) {
+    size_t b = up256(count * sizeof(T));
+    T* p = dry ? nullptr : reinterpret_cast<T*>(base + used);
+    used += b;
+    return p;
+  }
+};
+
+#define CK(expr)                                      \
+  do {                                                \
+    cudaError_t _e = (expr);                          \
+    if (_e != cudaSuccess) return cuda_fail(_e, #expr); \
+  } while (0)
+
+}  // namespace
+
+void count_launch(int n) { g_launches += n; }
+
+void prof_begin(const Ctx& c, const char* name, long long m, long long n, long long k, int dyn) {
+  if (!g_prof_on) return;
+  ProfRec r{name, m, n, k, dyn, next_event(), next_event()};
+  if (r.e0) cudaEventRecord(r.e0, c.stream);
+  g_prof.push_back(r);
+  g_prof_stream = c.stream;
+}
+void prof_end(const Ctx& c) {
+  if (!g_prof_on || g_prof.empty()) return;
+  if (g_prof.back().e1) cudaEventRecord(g_prof.back().e1, c.stream);
+}
+
+}  // namespace collider
+
+using namespace collider;
+
+// ===========================================================================
+// status / profiling
+// ===========================================================================
+extern "C" const char* collider_last_error(void) { return g_msg.c_str(); }
+
+extern "C" long long collider_launch_count(int reset) {
+  long long n = g_launches;
+  if (reset) g_launches = 0;
+  return n;
+}
+
+extern "C" collider_status collider_check(void* stream) {
+  Ctx c;
+  collider_status s = make_ctx(stream, &c);
+  if (s != COLLIDER_OK) return s;
+  cudaError_t e = cudaStreamSynchronize(c.stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  DevStatus h{};
+  e = cudaMemcpy(&h, c.st, sizeof h, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (h.code == 0) return COLLIDER_OK;
+  cudaMemset(c.st, 0, sizeof(DevStatus));
+  if (h.code == kErrTimeout)
+    return fail(COLLIDER_ERR_TIMEOUT, "a bounded in-kernel wait ran out (site %u, block %u)", h.site, h.block);
+  return fail(COLLIDER_ERR_INVALID_ARG, "a kernel skipped an index outside its buffer (site %u, block %u)", h.site,
+              h.block);
+}
+
+// Profiler: record a CUDA event pair around every kernel launch of this host
+// thread while enabled.  collider_profile_enable(1) clears earlier records.
+extern "C" int collider_profile_enable(int on) {
+  g_prof_on = on != 0;
+  if (on) {
+    g_prof.clear();
+    g_event_used = 0;
+  }
+  return 0;
+}
+
+extern "C" int collider_profile_count(void) { return static_cast<int>(g_prof.size()); }
+
+// Record i: kernel name, GEMM extents (0 for other kernels), and elapsed ms.
+// Synchronises the recorded events.
+extern "C" int collider_profile_get(int i, const char** name, long long* mnk_dyn, float* ms) {
+  if (i < 0 || i >= static_cast<int>(g_prof.size())) return -1;
+  const ProfRec& r = g_prof[i];
+  if (name) *name = r.name;
+  if (mnk_dyn) {
+    mnk_dyn[0] = r.m; mnk_dyn[1] = r.n; mnk_dyn[2] = r.k; mnk_dyn[3] = r.dyn;
+  }
+  if (ms) {
+    *ms = -1.f;
+    if (r.e0 && r.e1 && cudaEventSynchronize(r.e1) == cudaSuccess) cudaEventElapsedTime(ms, r.e0, r.e1);
+  }
+  return 0;
+}
+
+// ===========================================================================
+// a1 compaction
+// ===========================================================================
+extern "C" size_t collider_compact_workspace_size(int B, int T) {
+  if (B < 1 || T < 1) return 0;
+  return compact_ws_bytes((long long)B * T);
+}
+
+extern "C" collider_status collider_compact(const uint8_t* mask, int B, int T, int32_t* idx, int32_t* cu_kept,
+                                            int32_t* n_kept, void* ws, size_t ws_bytes, void* stream) {
+  if (!mask || !idx || !cu_kept || !n_kept) return fail(COLLIDER_ERR_INVALID_ARG, "collider_compact: null pointer");
+  if (B < 1 || T < 1 || (long long)B * T >= (1ll << 31))
+    return fail(COLLIDER_ERR_INVALID_ARG, "collider_compact: need B, T >= 1 and B*T < 2^31 (B=%d, T=%d)", B, T);
+  const size_t need = compact_ws_bytes((long long)B * T);
+  if (need && (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255)))
+    return fail(COLLIDER_ERR_INVALID_ARG, "collider_compact: needs %zu bytes of 256-aligned workspace", need);
+  Ctx c;
+  collider_status s = make_ctx(stream, &c);
+  if (s != COLLIDER_OK) return s;
+  CK(launch_compact(c, mask, B, T, idx, cu_kept, n_kept, ws));
+  return COLLIDER_OK;
+}
+
+// ===========================================================================
+// a2 gather / scatter
+// ===========================================================================
+extern "C" collider_status collider_gather_rows(const void* src, size_t src_ld_bytes, void* dst,
+                                                size_t dst_ld_bytes, size_t row_bytes, int M, const int32_t* idx,
+                                                const int32_t* n_kept, void* stream) {
+  if (!src || !dst || !idx || !n_kept) return fail(COLLIDER_ERR_INVALID_ARG, "collider_gather_rows: null pointer");
+  if (M < 0 || row_bytes == 0 || row_bytes % 16 || src_ld_bytes % 16 || dst_ld_bytes % 16 || !al16(src) ||
+      !al16(dst) || row_bytes > src_ld_bytes || row_bytes > dst_ld_bytes || row_bytes > (1u << 30))
+    return fail(COLLIDER_ERR_INVALID_ARG, "collider_gather_rows: rows and pointers must be 16-byte multiples");
+  Ctx c;
+  collider_status s = make_ctx(stream, &c);
+  if (s != COLLIDER_OK) return s;
+  GatherJob j{static_cast<const char*>(src), static_cast<char*>(dst), (long long)src_ld_bytes,
+              (long long)dst_ld_bytes, (int)row_bytes, 0};
+  CK(launch_gather(c, &j, 1, M, idx, n_kept));
+  return COLLIDER_OK;
+}
+
+extern "C" collider_status collider_scatter_rows(const void* compact, size_t compact_ld_bytes, void* full,
+                                                 size_t full_ld_bytes, size_t row_bytes, int M,
+                                                 const int32_t* idx, const int32_t* n_kept, void* stream) {
+  if (!compact || !full || !idx || !n_kept)
+    return fail(COLLIDER_ERR_INVALID_ARG, "collider_scatter_rows: null pointer");
+  if (M < 0 || row_bytes == 0 || row_bytes % 16 || compact_ld_bytes % 16 || full_ld_bytes % 16 || !al16(compact) ||
+      !al16(full) || row_bytes > compact_ld_bytes || row_bytes > full_ld_bytes || row_bytes > (1u << 30))
+    return fail(COLLIDER_ERR_INVALID_ARG, "collider_scatter_rows: rows and pointers must be 16-byte multiples");
+  Ctx c;
+  collider_status s = make_ctx(stream, &c);
+  if (s != COLLIDER_OK) return s;
+  CK(launch_scatter(c, static_cast<const char*>(compact), (long long)compact_ld_bytes, static_cast<char*>(full),
+                    (long long)full_ld_bytes, (int)row_bytes, M, idx, n_kept));
+  return COLLIDER_OK;
+}
+
+// ===========================================================================
+// a3/a4 linear backward
+// ===========================================================================
+namespace {
+size_t linear_carve(Carver& cv, collider_dtype dt, int M, int K, int N, bool x_full, bool dy_full, bool dx_full,
+                    void** xk, void** dyk, void** dxk, float** part) {
+  const long long Mp = pad128(M);
+  *xk = *dyk = *dxk = nullptr;
+  (void)x_full; (void)dy_full;
+  if (dt == COLLIDER_BF16) {
+    // kept rows of X and dY, zero-padded to 128 rows (also for COMPACT inputs,
+    // so the padding rows the reduction reads are exactly zero)
+    *xk = cv.take<__nv_bfloat16>((size_t)Mp * K);
+    *dyk = cv.take<__nv_bfloat16>((size_t)Mp * N);
+    if (dx_full) *dxk = cv.take<__nv_bfloat16>((size_t)Mp * K);
+  }
+  *part = cv.take<float>(colsum_part_floats(M, N));
+  return cv.used;
+}
+}  // namespace
+
+extern "C" size_t collider_linear_workspace_size(collider_dtype dtype, int M, int K, int N) {
+  if (M < 0 || K < 1 || N < 1) return 0;
+  Carver cv{nullptr, 0, 0, true};
+  void *a, *b, *d;
+  float* p;
+  return linear_carve(cv, dtype, M, K, N, true, true, true, &a, &b, &d, &p);
+}
+
+extern "C" collider_status collider_linear_bwd(collider_dtype dtype, int M, int K, int N, const void* X,
+                                               collider_rows x_rows, const void* W, const void* dY,
+                                               collider_rows dy_rows, const int32_t* idx, const int32_t* n_kept,
+                                               void* dX, collider_rows dx_rows, float* dW, float* db, void* ws,
+                                               size_t ws_bytes, void* stream) {
+  if (dtype != COLLIDER_F32 && dtype != COLLIDER_BF16)
+    return fail(COLLIDER_ERR_UNSUPPORTED, "collider_linear_bwd: dtype %d", (int)dtype);
+  if (M < 0 || K < 1 || N < 1) return fail(COLLIDER_ERR_INVALID_ARG, "collider_linear_bwd: bad sizes");
+  if (!idx || !n_kept || !dY) return fail(COLLIDER_ERR_INVALID_ARG, "collider_linear_bwd: null idx/n_kept/dY");
+  if (dX && !W) return fail(COLLIDER_ERR_INVALID_ARG, "collider_linear_bwd: dX needs W");
+  if (dW && !X) return fail(COLLIDER_ERR_INVALID_ARG, "collider_linear_bwd: dW needs X");
+  const bool x_full = x_rows == COLLIDER_ROWS_FULL, dy_full = dy_rows == COLLIDER_ROWS_FULL,
+             dx_full = dx_rows == COLLIDER_ROWS_FULL;
+  if (dtype == COLLIDER_BF16) {
+    if (K % 8 || N % 8) return fail(COLLIDER_ERR_UNSUPPORTED, "collider_linear_bwd: bf16 needs K, N % 8 == 0");
+    if (!al16(X) || !al16(W) || !al16(dY) || !al16(dX) || !al16(dW) || !al16(db))
+      return fail(COLLIDER_ERR_INVALID_ARG, "collider_linear_bwd: bf16 pointers must be 16-byte aligned");
+  } else if (db && (N % 8 || !al16(dY) || !al16(db))) {
+    return fail(COLLIDER_ERR_UNSUPPORTED, "collider_linear_bwd: f32 db needs N %% 8 == 0 and 16-byte alignment");
+  }
+  Carver cv{static_cast<char*>(ws), ws_bytes, 0, false};
+  void *xk, *dyk, *dxk;
+  float* part;
+  Carver dry{nullptr, 0, 0, true};
+  void *t0, *t1, *t2;
+  float* t3;
+  const size_t need = linear_carve(dry, dtype, M, K, N, x_full && dW, dy_full, dx_full && dX, &t0, &t1, &t2, &t3);
+  if (need > ws_bytes || (ws && (reinterpret_cast<uintptr_t>(ws) & 255)) || (need && !ws))
+    return fail(COLLIDER_ERR_INVALID_ARG, "collider_linear_bwd: needs %zu bytes of 256-aligned workspace", need);
+  linear_carve(cv, dtype, M, K, N, x_full && dW, dy_full, dx_full && dX, &xk, &dyk, &dxk, &part);
+  Ctx c;
+  collider_status s = make_ctx(stream, &c);
+  if (s != COLLIDER_OK) return s;
+  if (M == 0) return COLLIDER_OK;
+
+  if (dtype == COLLIDER_F32) {
+    const float* Xf = static_cast<const float*>(X);
+    const float* Wf = static_cast<const float*>(W);
+    const float* dYf = static_cast<const float*>(dY);
+    if (dX) {
+      // filtered rows of a FULL dX (and padding rows of a COMPACT one) are 0
+      CK(cudaMemsetAsync(dX, 0, (size_t)M * K * sizeof(float), c.stream));
+      SimtGemm g{};
+      g.M = M; g.N = K; g.K = N;
+      g.A = dYf; g.lda = N; g.a_trans = 0; g.a_gather = dy_full;
+      g.B = Wf; g.ldb = N; g.b_trans = 0; g.b_gather = 0;
+      g.C = static_cast<float*>(dX); g.ldc = K; g.c_scatter = dx_full;
+      g.idx = idx; g.n_kept = n_kept; g.dyn = 1;
+      CK(launch_simt_gemm(c, g));
+    }
+    if (dW) {
+      SimtGemm g{};
+      g.M = K; g.N = N; g.K = M;
+      g.A = Xf; g.lda = K; g.a_trans = 1; g.a_gather = x_full;
+      g.B = dYf; g.ldb = N; g.b_trans = 1; g.b_gather = dy_full;
+      g.C = dW; g.ldc = N; g.c_scatter = 0;
+      g.idx = idx; g.n_kept = n_kept; g.dyn = 2;
+      CK(launch_simt_gemm(c, g));
+    }
+    if (db) CK(launch_colsum(c, dY, 0, N, M, N, dy_full ? idx : nullptr, n_kept, part, db));
+    return COLLIDER_OK;
+  }
+
+  // bf16: compact operands (zero-padded to 128 rows), tcgen05 GEMMs
+  const __nv_bfloat16* Xk = static_cast<const __nv_bfloat16*>(X);
+  const __nv_bfloat16* dYk = static_cast<const __nv_bfloat16*>(dY);
+  {
+    const GatherJob jx{static_cast<const char*>(X), static_cast<char*>(xk), (long long)K * 2, (long long)K * 2,
+                       K * 2, 0};
+    const GatherJob jy{static_cast<const char*>(dY), static_cast<char*>(dyk), (long long)N * 2, (long long)N * 2,
+                       N * 2, 0};
+    if (dW) CK(launch_gather(c, &jx, 1, M, x_full ? idx : nullptr, n_kept));
+    CK(launch_gather(c, &jy, 1, M, dy_full ? idx : nullptr, n_kept));
+    if (dW) Xk = static_cast<const __nv_bfloat16*>(xk);
+    dYk = static_cast<const __nv_bfloat16*>(dyk);
+  }
+  if (dX) {
+    TcGemm g{};
+    g.M = M; g.N = K; g.K = N;
+    g.A = dYk; g.lda = N; g.a_mn_major = 0; g.a_rows = M;
+    g.B = W; g.ldb = N; g.b_mn_major = 0; g.b_rows = K;
+    g.C = dx_full ? dxk : dX; g.ldc = K; g.c_bf16 = 1; g.zero_pad = 1;
+    g.n_kept = n_kept; g.dyn = 1;
+    CK(launch_tc_gemm(c, g));
+    if (dx_full) CK(launch_scatter(c, static_cast<const char*>(dxk), (long long)K * 2, static_cast<char*>(dX),
+                                   (long long)K * 2, K * 2, M, idx, n_kept));
+  }
+  if (dW) {
+    TcGemm g{};
+    g.M = K; g.N = N; g.K = M;
+    g.A = Xk; g.lda = K; g.a_mn_major = 1; g.a_rows = M;
+    g.B = dYk; g.ldb = N; g.b_mn_major = 1; g.b_rows = M;
+    g.C = dW; g.ldc = N; g.c_bf16 = 0;
+    g.n_kept = n_kept; g.dyn = 2;
+    CK(launch_tc_gemm(c, g));
+  }
+  if (db) CK(launch_colsum(c, dYk, 1, N, M, N, nullptr, n_kept, part, db));
+  return COLLIDER_OK;
+}
+
+// ===========================================================================
+// a7/a8 attention backward
+// ===========================================================================
+namespace {
+struct AttnScratch {
+  float* dq_acc;
+  float* Dvec;
+  float* lse2;
+  float2* rope;
+};
+void attn_carve(Carver& cv, int B, int T, int H, int dh, AttnScratch* a) {
+  const size_t M = (size_t)B * T;
+  a->dq_acc = cv.take<float>(M * H * dh);
+  a->Dvec = cv.take<float>(M * H);
+  a->lse2 = cv.take<float>(M * H);
+  a->rope = cv.take<float2>((size_t)T * (dh / 2));
+}
+}  // namespace
+
+extern "C" size_t collider_attn_workspace_size(int B, int T, int H, int Hkv, int dh) {
+  if (B < 1 || T < 1 || H < 1 || Hkv < 1 || dh < 1) return 0;
+  Carver cv{nullptr, 0, 0, true};
+  AttnScratch a;
+  attn_carve(cv, B, T, H, dh, &a);
+  const size_t Mp = pad128((long long)B * T);
+  cv.take<__nv_bfloat16>(Mp * H * dh * 2);          // compact Q, dO (FULL inputs)
+  cv.take<__nv_bfloat16>(Mp * Hkv * dh * 2);        // compact K, V
+  cv.take<__nv_bfloat16>(Mp * (H + 2 * Hkv) * dh);  // compact dQ, dK, dV (FULL outputs)
+  return cv.used;
+}
+
+extern "C" collider_status collider_attn_bwd(int B, int T, int H, int Hkv, int dh, int causal, float scale,
+                                             int rotary_dim, float rope_base, const void* Q, const void* K,
+                                             const void* V, const void* O, const void* dO, int q_ld, int kv_ld,
+                                             int do_ld, collider_rows in_rows, const float* lse,
+                                             const int32_t* idx, const int32_t* cu_kept, const int32_t* n_kept,
+                                             void* dQ, void* dK, void* dV, collider_rows out_rows, void* ws,
+                                             size_t ws_bytes, void* stream) {
+  (void)O;
+  if (!Q || !K || !V || !dO || !lse || !idx || !cu_kept || !n_kept || !dQ || !dK || !dV)
+    return fail(COLLIDER_ERR_INVALID_ARG, "collider_attn_bwd: null pointer");
+  if (B < 1 || T < 1 || H < 1 || Hkv < 1 || H % Hkv || (long long)B * T >= (1ll << 31))
+    return fail(COLLIDER_ERR_INVALID_ARG, "collider_attn_bwd: bad B/T/H/Hkv");
+  if (dh != 64 && dh != 128) return fail(COLLIDER_ERR_UNSUPPORTED, "collider_attn_bwd: dh must be 64 or 128");
+  if (rotary_dim < 0 || rotary_dim > dh || rotary_dim % 16)
+    return fail(COLLIDER_ERR_UNSUPPORTED, "collider_attn_bwd: rotary_dim must be a multiple of 16 <= dh");
+  if (q_ld < H * dh || kv_ld < Hkv * dh || do_ld < H * dh || q_ld % 8 || kv_ld % 8 || do_ld % 8)
+    return fail(COLLIDER_ERR_INVALID_ARG, "collider_attn_bwd: row strides too small or not multiples of 8");
+  if (!al16(Q) || !al16(K) || !al16(V) || !al16(dO) || !al16(dQ) || !al16(dK) || !al16(dV))
+    return fail(COLLIDER_ERR_INVALID_ARG, "collider_attn_bwd: pointers must be 16-byte aligned");
+  const size_t need = collider_attn_workspace_size(B, T, H, Hkv, dh);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255))
+    return fail(COLLIDER_ERR_INVALID_ARG, "collider_attn_bwd: needs %zu bytes of 256-aligned workspace", need);
+  Ctx c;
+  collider_status s = make_ctx(stream, &c);
+  if (s != COLLIDER_OK) return s;
+  const int M = B * T;
+  const long long Mp = pad128(M);
+  Carver cv{static_cast<char*>(ws), ws_bytes, 0, false};
+  AttnScratch sc;
+  attn_carve(cv, B, T, H, dh, &sc);
+  auto* cq = cv.take<__nv_bfloat16>((size_t)Mp * H * dh);
+  auto* cdo = cv.take<__nv_bfloat16>((size_t)Mp * H * dh);
+  auto* ck = cv.take<__nv_bfloat16>((size_t)Mp * Hkv * dh);
+  auto* cvv = cv.take<__nv_bfloat16>((size_t)Mp * Hkv * dh);
+  auto* cdq = cv.take<__nv_bfloat16>((size_t)Mp * H * dh);
+  auto* cdk = cv.take<__nv_bfloat16>((size_t)Mp * Hkv * dh);
+  auto* cdv = cv.take<__nv_bfloat16>((size_t)Mp * Hkv * dh);
+
+  AttnArgs a{};
+  a.B = B; a.T = T; a.H = H; a.Hkv = Hkv; a.dh = dh; a.causal = causal; a.scale = scale;
+  a.rotary_dim = rotary_dim; a.rope_base = rope_base;
+  a.lse = lse; a.idx = idx; a.cu_kept = cu_kept; a.n_kept = n_kept;
+  a.dq_acc = sc.dq_acc; a.Dvec = sc.Dvec; a.lse_k = sc.lse2; a.rope = sc.rope; a.M = M;
+  if (in_rows == COLLIDER_ROWS_FULL) {
+    GatherJob j[4] = {
+        {static_cast<const char*>(Q), reinterpret_cast<char*>(cq), (long long)q_ld * 2, (long long)H * dh * 2,
+         H * dh * 2, 0},
+        {static_cast<const char*>(dO), reinterpret_cast<char*>(cdo), (long long)do_ld * 2, (long long)H * dh * 2,
+         H * dh * 2, 0},
+        {static_cast<const char*>(K), reinterpret_cast<char*>(ck), (long long)kv_ld * 2, (long long)Hkv * dh * 2,
+         Hkv * dh * 2, 0},
+        {static_cast<const char*>(V), reinterpret_cast<char*>(cvv), (long long)kv_ld * 2, (long long)Hkv * dh * 2,
+         Hkv * dh * 2, 0}};
+    CK(launch_gather(c, j, 4, M, idx, n_kept));
+    a.q = cq; a.dO = cdo; a.k = ck; a.v = cvv;
+    a.q_ld = (long long)H * dh; a.do_ld = (long long)H * dh; a.kv_ld = (long long)Hkv * dh;
+  } else {
+    a.q = static_cast<const __nv_bfloat16*>(Q); a.k = static_cast<const __nv_bfloat16*>(K);
+    a.v = static_cast<const __nv_bfloat16*>(V); a.dO = static_cast<const __nv_bfloat16*>(dO);
+    a.q_ld = q_ld; a.kv_ld = kv_ld; a.do_ld = do_ld;
+  }
+  const bool out_full = out_rows == COLLIDER_ROWS_FULL;
+  if (out_full) {
+    a.dq = cdq; a.dk = cdk; a.dv = cdv;
+    a.dq_ld = (long long)H * dh; a.dkv_ld = (long long)Hkv * dh;
+  } else {
+    // COMPACT outputs use the input strides: dQ with q_ld, dK and dV with kv_ld
+    a.dq = static_cast<__nv_bfloat16*>(dQ); a.dk = static_cast<__nv_bfloat16*>(dK);
+    a.dv = static_cast<__nv_bfloat16*>(dV);
+    a.dq_ld = q_ld; a.dkv_ld = kv_ld;
+  }
+  CK(launch_attn_bwd(c, a));
+  if (out_full) {
+    CK(launch_scatter(c, reinterpret_cast<const char*>(cdq), (long long)H * dh * 2, static_cast<char*>(dQ),
+                      (long long)q_ld * 2, H * dh * 2, M, idx, n_kept));
+    CK(launch_scatter(c, reinterpret_cast<const char*>(cdk), (long long)Hkv * dh * 2, static_cast<char*>(dK),
+                      (long long)kv_ld * 2, Hkv * dh * 2, M, idx, n_kept));
+    CK(launch_scatter(c, reinterpret_cast<const char*>(cdv), (long long)Hkv * dh * 2, static_cast<char*>(dV),
+                      (long long)kv_ld * 2, Hkv * dh * 2, M, idx, n_kept));
+  }
+  return COLLIDER_OK;
+}
+
+// ===========================================================================
+// whole block
+// ===========================================================================
+namespace {
+
+struct LayerBufs {
+  __nv_bfloat16 *dout_k, *s_k, *b_k, *o_k, *a_k, *qkv_k;  // gathered (s_k holds gelu(f1) for phi)
+  __nv_bfloat16 *ds_k, *dgu_k, *dh_k, *do_k, *dqkv_k, *dx_k;
+  float *db_k, *da_k;
+  float* norm_part;
+  float* col_part;
+  AttnScratch at;
+};
+
+collider_status check_desc(const collider_layer_desc* d) {
+  if (!d) return fail(COLLIDER_ERR_INVALID_ARG, "null layer desc");
+  if (d->arch != COLLIDER_ARCH_LLAMA && d->arch != COLLIDER_ARCH_PHI)
+    return fail(COLLIDER_ERR_UNSUPPORTED, "arch %d", d->arch);
+  if (d->B < 1 || d->T < 1 || (long long)d->B * d->T >= (1ll << 31))
+    return fail(COLLIDER_ERR_INVALID_ARG, "bad B/T");
+  if (d->H < 1 || d->Hkv < 1 || d->H % d->Hkv) return fail(COLLIDER_ERR_INVALID_ARG, "bad head counts");
+  if (d->dh != 64 && d->dh != 128) return fail(COLLIDER_ERR_UNSUPPORTED, "head dim %d", d->dh);
+  if (d->D % 64 || d->F % 64 || d->D > 4096)
+    return fail(COLLIDER_ERR_UNSUPPORTED, "D and F must be multiples of 64, D <= 4096");
+  if (d->rotary_dim < 0 || d->rotary_dim > d->dh || d->rotary_dim % 16)
+    return fail(COLLIDER_ERR_UNSUPPORTED, "rotary_dim must be a multiple of 16 <= dh");
+  const bool llama = d->arch == COLLIDER_ARCH_LLAMA;
+  if (llama && (d->norm != COLLIDER_NORM_RMS || d->act != COLLIDER_ACT_SWIGLU))
+    return fail(COLLIDER_ERR_UNSUPPORTED, "llama blocks use RMSNorm + SwiGLU");
+  if (!llama && (d->norm != COLLIDER_NORM_LAYER || d->act != COLLIDER_ACT_GELU_TANH))
+    return fail(COLLIDER_ERR_UNSUPPORTED, "phi blocks use LayerNorm + GELU-tanh");
+  return COLLIDER_OK;
+}
+
+void layer_carve(Carver& cv, const collider_layer_desc* d, LayerBufs* L) {
+  const size_t Mp = pad128((long long)d->B * d->T);
+  const size_t D = d->D, F = d->F, Hd = (size_t)d->H * d->dh, Nqkv = (size_t)(d->H + 2 * d->Hkv) * d->dh;
+  const bool llama = d->arch == COLLIDER_ARCH_LLAMA;
+  const size_t Nup = llama ? 2 * F : F;
+  L->dout_k = cv.take<__nv_bfloat16>(Mp * D);
+  L->s_k = cv.take<__nv_bfloat16>(Mp * F);
+  L->b_k = llama ? cv.take<__nv_bfloat16>(Mp * D) : nullptr;
+  L->o_k = cv.take<__nv_bfloat16>(Mp * Hd);
+  L->a_k = cv.take<__nv_bfloat16>(Mp * D);
+  L->qkv_k = cv.take<__nv_bfloat16>(Mp * Nqkv);
+  L->ds_k = cv.take<__nv_bfloat16>(Mp * F);
+  L->dgu_k = cv.take<__nv_bfloat16>(Mp * Nup);
+  L->dh_k = llama ? cv.take<__nv_bfloat16>(Mp * D) : nullptr;
+  L->do_k = cv.take<__nv_bfloat16>(Mp * Hd);
+  L->dqkv_k = cv.take<__nv_bfloat16>(Mp * Nqkv);
+  L->dx_k = cv.take<__nv_bfloat16>(Mp * D);
+  L->db_k = llama ? cv.take<float>(Mp * D) : nullptr;
+  L->da_k = cv.take<float>(Mp * D);
+  L->norm_part = cv.take<float>(norm_part_floats((int)Mp, (int)D));
+  size_t cp = colsum_part_floats((int)Mp, (int)std::max(Nqkv, std::max(Nup, D)));
+  L->col_part = cv.take<float>(cp);
+  attn_carve(cv, d->B, d->T, d->H, d->dh, &L->at);
+}
+
+// C (bf16 or f32, COMPACT [Mk, N]) = A_k [Mk, K] . W^T with W stored [N, K]
+cudaError_t gemm_dx(const Ctx& c, int M, int N, int K, const void* A, const void* W, void* C, int c_bf16,
+                    int accumulate, const int32_t* n_kept) {
+  TcGemm g{};
+  g.M = M; g.N = N; g.K = K;
+  g.A = A; g.lda = K; g.a_mn_major = 0; g.a_rows = pad128(M);
+  g.B = W; g.ldb = K; g.b_mn_major = 0; g.b_rows = N;
+  g.C = C; g.ldc = N; g.c_bf16 = c_bf16; g.accumulate = accumulate; g.zero_pad = 1;
+  g.n_kept = n_kept; g.dyn = 1;
+  return launch_tc_gemm(c, g);
+}
+
+// dW [Kin, Nout] f32 = X_k^T dY_k, X_k [Mk, Kin], dY_k [Mk, Nout] (both COMPACT, zero-padded)
+cudaError_t gemm_dw(const Ctx& c, int M, int Kin, int Nout, const void* Xk, long long ldx, const void* dYk,
+                    long long ldy, float* dW, const int32_t* n_kept) {
+  TcGemm g{};
+  g.M = Kin; g.N = Nout; g.K = M;
+  g.A = Xk; g.lda = ldx; g.a_mn_major = 1; g.a_rows = pad128(M);
+  g.B = dYk; g.ldb = ldy; g.b_mn_major = 1; g.b_rows = pad128(M);
+  g.C = dW; g.ldc = Nout; g.c_bf16 = 0;
+  g.n_kept = n_kept; g.dyn = 2;
+  return launch_tc_gemm(c, g);
+}
+
+collider_status layer_bwd_impl(const Ctx& c, const collider_layer_desc* d, const collider_layer_weights* w,
+                               const collider_layer_saved* sv, const void* dOut, bool dout_full,
+                               const int32_t* idx, const int32_t* cu_kept, const int32_t* n_kept,
+                               const collider_layer_grads* g, bool dx_full, LayerBufs& L) {
+  const int M = d->B * d->T;
+  const int D = d->D, F = d->F, H = d->H, Hkv = d->Hkv, dh = d->dh;
+  const int Hd = H * dh, Nqkv = (H + 2 * Hkv) * dh;
+  const bool llama = d->arch == COLLIDER_ARCH_LLAMA;
+  const int Nup = llama ? 2 * F : F;
+
+  // 1. gather the kept rows of dOut and of the saved GEMM operands
+  {
+    GatherJob j[6];
+    int n = 0;
+    j[n++] = GatherJob{static_cast<const char*>(dOut), reinterpret_cast<char*>(L.dout_k), (long long)D * 2,
+                       (long long)D * 2, D * 2, 0};
+    if (llama) {
+      j[n++] = GatherJob{static_cast<const char*>(sv->s), reinterpret_cast<char*>(L.s_k), (long long)F * 2,
+                         (long long)F * 2, F * 2, 0};
+      j[n++] = GatherJob{static_cast<const char*>(sv->b), reinterpret_cast<char*>(L.b_k), (long long)D * 2,
+                         (long long)D * 2, D * 2, 0};
+    } else {
+      j[n++] = GatherJob{static_cast<const char*>(sv->up), reinterpret_cast<char*>(L.s_k), (long long)F * 2,
+                         (long long)F * 2, F * 2, 1};   // gelu(f1)
+    }
+    j[n++] = GatherJob{static_cast<const char*>(sv->o), reinterpret_cast<char*>(L.o_k), (long long)Hd * 2,
+                       (long long)Hd * 2, Hd * 2, 0};
+    j[n++] = GatherJob{static_cast<const char*>(sv->a), reinterpret_cast<char*>(L.a_k), (long long)D * 2,
+                       (long long)D * 2, D * 2, 0};
+    j[n++] = GatherJob{static_cast<const char*>(sv->qkv), reinterpret_cast<char*>(L.qkv_k), (long long)Nqkv * 2,
+                       (long long)Nqkv * 2, Nqkv * 2, 0};
+    if (dout_full) {
+      CK(launch_gather(c, j, n, M, idx, n_kept));
+    } else {
+      CK(launch_gather(c, j, 1, M, nullptr, n_kept));   // COMPACT dOut: copy + zero padding
+      CK(launch_gather(c, j + 1, n - 1, M, idx, n_kept));
+    }
+  }
+
+  // 2. MLP
+  const __nv_bfloat16* dres = L.dout_k;   // gradient flowing along the residual into the attention half
+  if (llama) {
+    CK(gemm_dx(c, M, F, D, L.dout_k, w->w_down, L.ds_k, 1, 0, n_kept));               // ds = dOut W_down^T
+    CK(gemm_dw(c, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept));               // dW_down = s^T dOut
+    CK(launch_swiglu_bwd(c, L.ds_k, 1, F, static_cast<const __nv_bfloat16*>(sv->up), L.dgu_k, M, idx, n_kept));
+    CK(gemm_dx(c, M, D, Nup, L.dgu_k, w->w_up, L.db_k, 0, 0, n_kept));                // db = dgu W_up^T
+    CK(gemm_dw(c, M, D, Nup, L.b_k, D, L.dgu_k, Nup, g->dw_up, n_kept));              // dW_up = b^T dgu
+    NormBwdArgs nb{};
+    nb.layer_norm = 0; nb.M = M; nb.D = D;
+    nb.dy1 = L.db_k; nb.res = L.dout_k; nb.res_ld = D;
+    nb.x = static_cast<const __nv_bfloat16*>(sv->h); nb.rstd = sv->rstd2;
+    nb.gamma = static_cast<const __nv_bfloat16*>(w->norm2_w);
+    nb.out = L.dh_k; nb.dgamma = g->dnorm2_w; nb.part = L.norm_part; nb.idx = idx; nb.n_kept = n_kept;
+    CK(launch_norm_bwd(c, nb));                                                          // dh = dOut + norm2'
+    dres = L.dh_k;
+  } else {
+    CK(gemm_dx(c, M, F, D, L.dout_k, w->w_down, L.ds_k, 1, 0, n_kept));               // df2 = dOut W2^T
+    CK(gemm_dw(c, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept));               // dW2 = gelu(f1)^T dOut
+    if (d->mlp_bias && g->db_down)
+      CK(launch_colsum(c, L.dout_k, 1, D, M, D, nullptr, n_kept, L.col_part, g->db_down));
+    CK(launch_gelu_bwd(c, L.ds_k, 1, F, static_cast<const __nv_bfloat16*>(sv->up), L.dgu_k, M, idx, n_kept));
+    CK(gemm_dw(c, M, D, F, L.a_k, D, L.dgu_k, F, g->dw_up, n_kept));                  // dW1 = a^T df1
+    if (d->mlp_bias && g->db_up)
+      CK(launch_colsum(c, L.dgu_k, 1, F, M, F, nullptr, n_kept, L.col_part, g->db_up));
+    CK(gemm_dx(c, M, D, F, L.dgu_k, w->w_up, L.da_k, 0, 0, n_kept));                  // da = df1 W1^T
+  }
+
+  // 3. attention output projection
+  CK(gemm_dx(c, M, Hd, D, dres, w->w_o, L.do_k, 1, 0, n_kept));                       // do = dh W_o^T
+  CK(gemm_dw(c, M, Hd, D, L.o_k, Hd, dres, D, g->dw_o, n_kept));                      // dW_o = o^T dh
+  if (d->out_bias && g->db_o) CK(launch_colsum(c, dres, 1, D, M, D, nullptr, n_kept, L.col_part, g->db_o));
+
+  // 4. filtered attention backward (+ RoPE backward) straight into dqkv_k
+  {
+    AttnArgs a{};
+    a.B = d->B; a.T = d->T; a.H = H; a.Hkv = Hkv; a.dh = dh; a.causal = 1;
+    a.scale = 1.0f / sqrtf((float)dh);
+    a.rotary_dim = d->rotary_dim; a.rope_base = d->rope_base;
+    a.q = L.qkv_k; a.k = L.qkv_k + Hd; a.v = L.qkv_k + Hd + Hkv * dh; a.dO = L.do_k;
+    a.q_ld = Nqkv; a.kv_ld = Nqkv; a.do_ld = Hd;
+    a.lse = sv->lse; a.idx = idx; a.cu_kept = cu_kept; a.n_kept = n_kept;
+    a.dq = L.dqkv_k; a.dk = L.dqkv_k + Hd; a.dv = L.dqkv_k + Hd + Hkv * dh;
+    a.dq_ld = Nqkv; a.dkv_ld = Nqkv;
+    a.dq_acc = L.at.dq_acc; a.Dvec = L.at.Dvec; a.lse_k = L.at.lse2; a.rope = L.at.rope; a.M = M;
+    CK(launch_attn_bwd(c, a));
+  }
+
+  // 5. QKV projection
+  CK(gemm_dw(c, M, D, Nqkv, L.a_k, D, L.dqkv_k, Nqkv, g->dw_qkv, n_kept));           // dW_qkv = a^T dqkv
+  if (d->qkv_bias && g->db_qkv)
+    CK(launch_colsum(c, L.dqkv_k, 1, Nqkv, M, Nqkv, nullptr, n_kept, L.col_part, g->db_qkv));
+  CK(gemm_dx(c, M, D, Nqkv, L.dqkv_k, w->w_qkv, L.da_k, 0, llama ? 0 : 1, n_kept));  // da (+)= dqkv W_qkv^T
+
+  // 6. input norm backward + residual, then back to FULL rows if asked
+  __nv_bfloat16* dxk = dx_full ? L.dx_k : static_cast<__nv_bfloat16*>(g->dx);
+  {
+    NormBwdArgs nb{};
+    nb.layer_norm = llama ? 0 : 1; nb.M = M; nb.D = D;
+    nb.dy1 = L.da_k; nb.res = dres; nb.res_ld = D;
+    nb.x = static_cast<const __nv_bfloat16*>(sv->x); nb.mean = sv->mean1; nb.rstd = sv->rstd1;
+    nb.gamma = static_cast<const __nv_bfloat16*>(w->norm1_w);
+    nb.out = dxk; nb.dgamma = g->dnorm1_w; nb.dbeta = g->dnorm1_b; nb.part = L.norm_part;
+    nb.idx = idx; nb.n_kept = n_kept;
+    CK(launch_norm_bwd(c, nb));
+  }
+  if (dx_full)
+    CK(launch_scatter(c, reinterpret_cast<const char*>(L.dx_k), (long long)D * 2, static_cast<char*>(g->dx),
+                      (long long)D * 2, D * 2, M, idx, n_kept));
+  return COLLIDER_OK;
+}
+
+collider_status check_layer_ptrs(const collider_layer_desc* d, const collider_layer_weights* w,
+                                 const collider_layer_saved* sv, const collider_layer_grads* g, bool need_dx) {
+  if (!w || !sv || !g) return fail(COLLIDER_ERR_INVALID_ARG, "null weights/saved/grads struct");
+  const bool llama = d->arch == COLLIDER_ARCH_LLAMA;
+  const void* req[] = {w->norm1_w, w->w_qkv, w->w_o, w->w_up, w->w_down, sv->x, sv->a, sv->rstd1, sv->qkv,
+                       sv->o, sv->lse, sv->up, g->dnorm1_w, g->dw_qkv, g->dw_o, g->dw_up, g->dw_down};
+  for (const void* p : req)
+    if (!p) return fail(COLLIDER_ERR_INVALID_ARG, "a required weight/saved/gradient pointer is null");
+  if (need_dx && !g->dx) return fail(COLLIDER_ERR_INVALID_ARG, "grads->dx is null");
+  if (llama && (!w->norm2_w || !sv->h || !sv->b || !sv->rstd2 || !sv->s || !g->dnorm2_w))
+    return fail(COLLIDER_ERR_INVALID_ARG, "llama block needs norm2_w, h, b, rstd2, s and dnorm2_w");
+  if (!llama && (!sv->mean1 || !g->dnorm1_b))
+    return fail(COLLIDER_ERR_INVALID_ARG, "phi block needs mean1 and dnorm1_b");
+  const void* al[] = {w->norm1_w, w->w_qkv, w->w_o, w->w_up, w->w_down, w->norm2_w, sv->x, sv->a, sv->qkv,
+                      sv->o, sv->h, sv->b, sv->up, sv->s, g->dx, g->dw_qkv, g->dw_o, g->dw_up, g->dw_down,
+                      g->dnorm1_w, g->dnorm1_b, g->dnorm2_w, g->db_qkv, g->db_o, g->db_up, g->db_down};
+  for (const void* p : al)
+    if (!al16(p)) return fail(COLLIDER_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  return COLLIDER_OK;
+}
+
+}  // namespace
+
+extern "C" size_t collider_layer_workspace_size(const collider_layer_desc* d) {
+  if (check_desc(d) != COLLIDER_OK) return 0;
+  Carver cv{nullptr, 0, 0, true};
+  LayerBufs L;
+  layer_carve(cv, d, &L);
+  return cv.used;
+}
+
+extern "C" collider_status collider_layer_bwd(const collider_layer_desc* d, const collider_layer_weights* w,
+                                              const collider_layer_saved* sv, const void* dOut,
+                                              collider_rows dout_rows, const int32_t* idx, const int32_t* cu_kept,
+                                              const int32_t* n_kept, const collider_layer_grads* g,
+                                              collider_rows dx_rows, void* ws, size_t ws_bytes, void* stream) {
+  collider_status s = check_desc(d);
+  if (s != COLLIDER_OK) return s;
+  if (!dOut || !idx || !cu_kept || !n_kept || !al16(dOut))
+    return fail(COLLIDER_ERR_INVALID_ARG, "collider_layer_bwd: null or misaligned dOut/idx/cu_kept/n_kept");
+  s = check_layer_ptrs(d, w, sv, g, true);
+  if (s != COLLIDER_OK) return s;
+  const size_t need = collider_layer_workspace_size(d);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255))
+    return fail(COLLIDER_ERR_INVALID_ARG, "collider_layer_bwd: needs %zu bytes of 256-aligned workspace", need);
+  Ctx c;
+  s = make_ctx(stream, &c);
+  if (s != COLLIDER_OK) return s;
+  Carver cv{static_cast<char*>(ws), ws_bytes, 0, false};
+  LayerBufs L;
+  layer_carve(cv, d, &L);
+  return layer_bwd_impl(c, d, w, sv, dOut, dout_rows == COLLIDER_ROWS_FULL, idx, cu_kept, n_kept, g,
+                        dx_rows == COLLIDER_ROWS_FULL, L);
+}
+
+// ===========================================================================
+// whole stack
+// ===========================================================================
+namespace {
+struct StackBufs {
+  __nv_bfloat16 *dz_k, *y_k, *dy_k, *dxa, *dxb;
+  float* dyf_k;
+  float* part;
+};
+void stack_carve(Carver& cv, const collider_layer_desc* d, int V, StackBufs* S) {
+  const size_t Mp = pad128((long long)d->B * d->T);
+  S->dz_k = cv.take<__nv_bfloat16>(Mp * V);
+  S->y_k = cv.take<__nv_bfloat16>(Mp * d->D);
+  S->dyf_k = cv.take<float>(Mp * d->D);
+  S->dy_k = nullptr;
+  S->dxa = cv.take<__nv_bfloat16>(Mp * d->D);
+  S->dxb = cv.take<__nv_bfloat16>(Mp * d->D);
+  S->part = cv.take<float>(norm_part_floats((int)Mp, d->D));
+}
+}  // namespace
+
+extern "C" size_t collider_stack_workspace_size(const collider_layer_desc* d, int L, int V) {
+  if (check_desc(d) != COLLIDER_OK || L < 1 || V < 8) return 0;
+  Carver cv{nullptr, 0, 0, true};
+  StackBufs S;
+  stack_carve(cv, d, V, &S);
+  LayerBufs LB;
+  layer_carve(cv, d, &LB);
+  return cv.used;
+}
+
+extern "C" collider_status collider_stack_bwd(const collider_layer_desc* d, int nL, int V,
+                                              const collider_layer_weights* w, const collider_layer_saved* sv,
+                                              const void* logits, const int32_t* targets, const int32_t* ids,
+                                              const void* y, const void* xL, const float* rstdf, const void* normf_w,
+                                              const void* w_lm, const int32_t* idx, const int32_t* cu_kept,
+                                              const int32_t* n_kept, const collider_layer_grads* grads,
+                                              float* dnormf_w, float* dw_lm, float* dE, void* ws, size_t ws_bytes,
+                                              void* stream) {
+  collider_status s = check_desc(d);
+  if (s != COLLIDER_OK) return s;
+  if (d->arch != COLLIDER_ARCH_LLAMA) return fail(COLLIDER_ERR_UNSUPPORTED, "collider_stack_bwd: llama blocks only");
+  if (nL < 1 || V < 8 || V % 8) return fail(COLLIDER_ERR_INVALID_ARG, "collider_stack_bwd: L >= 1, V % 8 == 0");
+  if (d->D > 2048) return fail(COLLIDER_ERR_UNSUPPORTED, "collider_stack_bwd: D <= 2048");
+  if (!w || !sv || !grads || !logits || !targets || !ids || !y || !xL || !rstdf || !normf_w || !w_lm || !idx ||
+      !cu_kept || !n_kept || !dnormf_w || !dw_lm || !dE)
+    return fail(COLLIDER_ERR_INVALID_ARG, "collider_stack_bwd: null pointer");
+  if (!al16(logits) || !al16(y) || !al16(xL) || !al16(normf_w) || !al16(w_lm) || !al16(dnormf_w) || !al16(dw_lm) ||
+      !al16(dE))
+    return fail(COLLIDER_ERR_INVALID_ARG, "collider_stack_bwd: pointers must be 16-byte aligned");
+  for (int l = 0; l < nL; ++l) {
+    s = check_layer_ptrs(d, &w[l], &sv[l], &grads[l], false);
+    if (s != COLLIDER_OK) return s;
+  }
+  const size_t need = collider_stack_workspace_size(d, nL, V);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255))
+    return fail(COLLIDER_ERR_INVALID_ARG, "collider_stack_bwd: needs %zu bytes of 256-aligned workspace", need);
+  Ctx c;
+  s = make_ctx(stream, &c);
+  if (s != COLLIDER_OK) return s;
+  Carver cv{static_cast<char*>(ws), ws_bytes, 0, false};
+  StackBufs S;
+  stack_carve(cv, d, V, &S);
+  LayerBufs LB;
+  layer_carve(cv, d, &LB);
+  const int M = d->B * d->T, D = d->D;
+
+  // LM head: dz = (softmax(z) - onehot) / n_kept on kept rows
+  CK(launch_ce_bwd(c, static_cast<const __nv_bfloat16*>(logits), targets, V, M, idx, n_kept, S.dz_k));
+  {
+    GatherJob j{static_cast<const char*>(y), reinterpret_cast<char*>(S.y_k), (long long)D * 2, (long long)D * 2,
+                D * 2, 0};
+    CK(launch_gather(c, &j, 1, M, idx, n_kept));
+  }
+  CK(gemm_dw(c, M, D, V, S.y_k, D, S.dz_k, V, dw_lm, n_kept));            // dW_lm = y^T dz
+  CK(gemm_dx(c, M, D, V, S.dz_k, w_lm, S.dyf_k, 0, 0, n_kept));           // dy = dz W_lm^T
+  {
+    NormBwdArgs nb{};
+    nb.layer_norm = 0; nb.M = M; nb.D = D;
+    nb.dy1 = S.dyf_k; nb.res = nullptr;
+    nb.x = static_cast<const __nv_bfloat16*>(xL); nb.rstd = rstdf;
+    nb.gamma = static_cast<const __nv_bfloat16*>(normf_w);
+    nb.out = S.dxa; nb.dgamma = dnormf_w; nb.part = S.part; nb.idx = idx; nb.n_kept = n_kept;
+    CK(launch_norm_bwd(c, nb));
+  }
+  // blocks, last to first, staying COMPACT between blocks
+  __nv_bfloat16* cur = S.dxa;
+  __nv_bfloat16* nxt = S.dxb;
+  for (int l = nL - 1; l >= 0; --l) {
+    collider_layer_grads gl = grads[l];
+    gl.dx = nxt;
+    s = layer_bwd_impl(c, d, &w[l], &sv[l], cur, false, idx, cu_kept, n_kept, &gl, false, LB);
+    if (s != COLLIDER_OK) return s;
+    std::swap(cur, nxt);
+  }
+  // embedding gradient
+  CK(cudaMemsetAsync(dE, 0, (size_t)V * D * sizeof(float), c.stream));
+  CK(launch_embed_bwd(c, cur, D, D, ids, V, M, idx, n_kept, dE));
+  return COLLIDER_OK;
+}

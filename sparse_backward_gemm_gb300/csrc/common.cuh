@@ -1,0 +1,105 @@
+// Shared device helpers for libcollider kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace collider {
+
+// ---------------------------------------------------------------------------
+// device status word: kernels record the first failure here (host reads it
+// in collider_check).  Codes:
+constexpr unsigned kErrTimeout = 1u;  // a bounded wait ran out
+constexpr unsigned kErrBadIndex = 2u; // an index outside its buffer was seen and skipped
+
+struct DevStatus {
+  unsigned code;   // first error code (0 = ok)
+  unsigned site;   // which wait / check gave up
+  unsigned block;  // blockIdx.x of the reporter
+  unsigned pad;
+};
+
+__device__ __forceinline__ void report_error(DevStatus* st, unsigned code, unsigned site) {
+  if (st != nullptr && atomicCAS(&st->code, 0u, code) == 0u) {
+    st->site = site;
+    st->block = blockIdx.x;
+  }
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait budget for any spin inside a kernel: generous against any legitimate
+// wait (kernels here run for at most milliseconds), short enough that a
+// broken pipeline gives the GPU back within seconds.
+constexpr uint64_t kWaitBudgetNs = 2000000000ull;  // 2 s
+
+// ---------------------------------------------------------------------------
+// small math / conversion helpers
+__device__ __forceinline__ float bf2f(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ __nv_bfloat16 f2bf(float v) { return __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float* f) {
+  uint4 u;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return u;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Block-wide sum for blockDim.x a multiple of 32 (<= 1024); every thread
+// gets the result.  `red` must hold 32 floats of shared memory.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = (lane < nw) ? red[lane] : 0.f;
+  return warp_sum(t);
+}
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_max(v);
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = (lane < nw) ? red[lane] : -INFINITY;
+  return warp_max(t);
+}
+
+// Rows a COMPACT buffer must hold valid data or zeros for: n_kept rounded up
+// to the GEMM tile height, capped at the buffer capacity.
+__device__ __forceinline__ int padded_rows(int n, int cap) {
+  int p = (n + 127) & ~127;
+  return p < cap ? p : cap;
+}
+
+}  // namespace collider

@@ -1,0 +1,173 @@
+// Keep-mask compaction: the ascending list of kept tokens that every
+// dimension-reduced dense GEMM of the filtered backward runs over (Collider,
+// abstract).  Warp ballots + popcounts give each thread's offset; no atomics,
+// so the list is bit-exact and deterministic.
+#include "internal.h"
+
+namespace collider {
+
+namespace {
+
+constexpr int kThreads = 1024;          // one block of 32 warps
+constexpr int kTokPerThread = 16;       // one 16-byte mask load per thread
+constexpr int kChunk = kThreads * kTokPerThread;  // tokens per block pass
+
+// 16 mask bytes starting at `start` -> bit i set if token start+i is kept.
+__device__ __forceinline__ uint32_t load_bits(const uint8_t* mask, long long start, long long M) {
+  uint32_t bits = 0;
+  if (start + kTokPerThread <= M && ((reinterpret_cast<uintptr_t>(mask + start) & 15) == 0)) {
+    uint4 v = *reinterpret_cast<const uint4*>(mask + start);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        if ((w[j] >> (8 * b)) & 0xffu) bits |= 1u << (4 * j + b);
+  } else {
+    for (int i = 0; i < kTokPerThread; ++i)
+      if (start + i < M && mask[start + i] != 0) bits |= 1u << i;
+  }
+  return bits;
+}
+
+// Exclusive block scan of one int per thread (kThreads threads).  Returns the
+// exclusive prefix; *total gets the block sum.  `ws` holds 32 ints.
+__device__ __forceinline__ int block_excl_scan(int v, int* ws, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) ws[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = ws[lane];
+    int s = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    ws[lane] = s - w;          // exclusive prefix of warp totals
+    if (lane == 31) ws[32] = s;
+  }
+  __syncthreads();
+  int r = ws[warp] + x - v;
+  *total = ws[32];
+  __syncthreads();
+  return r;
+}
+
+// Writes the indices of the kept tokens in `bits` (16 tokens from `start`)
+// at idx[off...], and cu_kept[b] for every sequence start inside the span.
+__device__ __forceinline__ void emit(uint32_t bits, long long start, int off, int B, int T,
+                                     int32_t* idx, int32_t* cu_kept, long long M) {
+  // sequence starts b*T inside [start, start+16)
+  long long b = (start + T - 1) / T;
+  for (; b < B && b * (long long)T < start + kTokPerThread && b * (long long)T < M; ++b) {
+    int within = (int)(b * (long long)T - start);
+    cu_kept[b] = off + __popc(bits & ((1u << within) - 1u));
+  }
+  int o = off;
+  while (bits) {
+    int i = __ffs(bits) - 1;
+    idx[o++] = (int32_t)(start + i);
+    bits &= bits - 1;
+  }
+}
+
+// Whole mask in one block: loops over kChunk-token passes.
+__global__ void __launch_bounds__(kThreads) compact_one_block(const uint8_t* __restrict__ mask, int B,
+                                                              int T, int32_t* __restrict__ idx,
+                                                              int32_t* __restrict__ cu_kept,
+                                                              int32_t* __restrict__ n_kept) {
+  __shared__ int ws[33];
+  const long long M = (long long)B * T;
+  int carry = 0;
+  for (long long base = 0; base < M; base += kChunk) {
+    long long start = base + (long long)threadIdx.x * kTokPerThread;
+    uint32_t bits = (start < M) ? load_bits(mask, start, M) : 0u;
+    int total;
+    int off = carry + block_excl_scan(__popc(bits), ws, &total);
+    if (start < M) emit(bits, start, off, B, T, idx, cu_kept, M);
+    carry += total;
+  }
+  if (threadIdx.x == 0) {
+    cu_kept[B] = carry;
+    n_kept[0] = carry;
+  }
+}
+
+// Multi-block path, pass 1: kept count per kChunk-token chunk.
+__global__ void __launch_bounds__(kThreads) compact_count(const uint8_t* __restrict__ mask, long long M,
+                                                          int* __restrict__ counts) {
+  __shared__ int ws[33];
+  long long start = (long long)blockIdx.x * kChunk + (long long)threadIdx.x * kTokPerThread;
+  uint32_t bits = (start < M) ? load_bits(mask, start, M) : 0u;
+  int total;
+  block_excl_scan(__popc(bits), ws, &total);
+  if (threadIdx.x == 0) counts[blockIdx.x] = total;
+}
+
+// Pass 2 (one block): exclusive scan of the chunk counts, in place.
+__global__ void __launch_bounds__(kThreads) compact_scan(int* __restrict__ counts, int nchunks, int B,
+                                                         int32_t* __restrict__ cu_kept,
+                                                         int32_t* __restrict__ n_kept) {
+  __shared__ int ws[33];
+  int carry = 0;
+  for (int base = 0; base < nchunks; base += kThreads) {
+    int i = base + threadIdx.x;
+    int v = (i < nchunks) ? counts[i] : 0;
+    int total;
+    int e = block_excl_scan(v, ws, &total);
+    if (i < nchunks) counts[i] = carry + e;
+    carry += total;
+  }
+  if (threadIdx.x == 0) {
+    cu_kept[B] = carry;
+    n_kept[0] = carry;
+  }
+}
+
+// Pass 3: each chunk writes its kept indices at its scanned offset.
+__global__ void __launch_bounds__(kThreads) compact_write(const uint8_t* __restrict__ mask, int B, int T,
+                                                          const int* __restrict__ offsets,
+                                                          int32_t* __restrict__ idx,
+                                                          int32_t* __restrict__ cu_kept) {
+  __shared__ int ws[33];
+  const long long M = (long long)B * T;
+  long long start = (long long)blockIdx.x * kChunk + (long long)threadIdx.x * kTokPerThread;
+  uint32_t bits = (start < M) ? load_bits(mask, start, M) : 0u;
+  int total;
+  int off = offsets[blockIdx.x] + block_excl_scan(__popc(bits), ws, &total);
+  if (start < M) emit(bits, start, off, B, T, idx, cu_kept, M);
+}
+
+}  // namespace
+
+size_t compact_ws_bytes(long long M) {
+  if (M <= kCompactOneBlockMax) return 0;
+  long long nchunks = (M + kChunk - 1) / kChunk;
+  return (size_t)((nchunks * sizeof(int) + 255) & ~255ll);
+}
+
+cudaError_t launch_compact(const Ctx& c, const uint8_t* mask, int B, int T, int32_t* idx,
+                           int32_t* cu_kept, int32_t* n_kept, void* ws) {
+  long long M = (long long)B * T;
+  if (M <= kCompactOneBlockMax) {
+    compact_one_block<<<1, kThreads, 0, c.stream>>>(mask, B, T, idx, cu_kept, n_kept);
+    count_launch();
+    return cudaGetLastError();
+  }
+  int nchunks = (int)((M + kChunk - 1) / kChunk);
+  int* counts = static_cast<int*>(ws);
+  compact_count<<<nchunks, kThreads, 0, c.stream>>>(mask, M, counts);
+  compact_scan<<<1, kThreads, 0, c.stream>>>(counts, nchunks, B, cu_kept, n_kept);
+  compact_write<<<nchunks, kThreads, 0, c.stream>>>(mask, B, T, counts, idx, cu_kept);
+  count_launch(3);
+  return cudaGetLastError();
+}
+
+}  // namespace collider

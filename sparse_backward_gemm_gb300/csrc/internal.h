@@ -1,0 +1,165 @@
+// Internal launcher interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace collider {
+
+// Per-call launch context.
+struct Ctx {
+  cudaStream_t stream;
+  DevStatus* st;   // device status word of the current device
+  int num_sms;
+};
+
+// Launch accounting (per host thread) and optional per-kernel event timing.
+void count_launch(int n = 1);
+// Kernel timing hooks used by the profiler: bracket a launch with events when
+// profiling is on.  `name` must be a string literal; m, n, k, dyn describe a
+// GEMM launch (dyn: which extent is the device-resident kept count).
+void prof_begin(const Ctx& c, const char* name, long long m = 0, long long n = 0, long long k = 0,
+                int dyn = 0);
+void prof_end(const Ctx& c);
+
+// ---- compaction ------------------------------------------------------------
+constexpr long long kCompactOneBlockMax = 4194304;  // 2^22 tokens: one block scans it all
+size_t compact_ws_bytes(long long M);
+cudaError_t launch_compact(const Ctx& c, const uint8_t* mask, int B, int T, int32_t* idx,
+                           int32_t* cu_kept, int32_t* n_kept, void* ws);
+
+// ---- row kernels (rows.cu) -------------------------------------------------
+struct GatherJob {
+  const char* src;
+  char* dst;
+  long long src_ld;   // bytes
+  long long dst_ld;   // bytes
+  int row_bytes;      // multiple of 16
+  int op;             // 0 copy, 1 gelu_tanh(bf16 row) -> bf16
+};
+constexpr int kMaxGatherJobs = 8;
+// idx may be null: identity (copy the first n_kept rows, zero the padding).
+cudaError_t launch_gather(const Ctx& c, const GatherJob* jobs, int njobs, int M, const int32_t* idx,
+                          const int32_t* n_kept);
+cudaError_t launch_scatter(const Ctx& c, const char* compact, long long compact_ld, char* full,
+                           long long full_ld, int row_bytes, int M, const int32_t* idx,
+                           const int32_t* n_kept);
+
+// Column sums over the first n_kept rows of a COMPACT matrix X [rows, N] (bf16
+// or f32), deterministic: per-row-block partials in `part` then a fixed-order
+// reduction.  Writes out[N] f32.  part needs colsum_part_floats(M, N) floats.
+// When gidx is non-null, row r is read at row gidx[r] (FULL storage).
+size_t colsum_part_floats(int M, int N);
+cudaError_t launch_colsum(const Ctx& c, const void* X, int x_is_bf16, long long ld, int M, int N,
+                          const int32_t* gidx, const int32_t* n_kept, float* part, float* out);
+
+// Norm backward on kept rows, plus residual:
+//   out[r] = res[r] + norm_bwd(dy1[r] (+ dy2[r]))   (COMPACT rows, bf16 out)
+// x, mean, rstd are FULL rows read through idx.  gamma bf16 [D].
+// dgamma (and dbeta for LayerNorm) f32 [D] via deterministic partials.
+struct NormBwdArgs {
+  int layer_norm;       // 0 RMSNorm, 1 LayerNorm
+  int M, D;
+  const float* dy1;     // COMPACT f32 [*, D]
+  const float* dy2;     // optional second COMPACT f32 input, summed
+  const __nv_bfloat16* res;  // COMPACT bf16 residual gradient (may be null)
+  long long res_ld;
+  const __nv_bfloat16* x;    // FULL bf16 [M, D]
+  const float* mean;    // FULL f32 [M] (LayerNorm)
+  const float* rstd;    // FULL f32 [M]
+  const __nv_bfloat16* gamma;
+  __nv_bfloat16* out;   // COMPACT bf16 [*, D]
+  float* dgamma;
+  float* dbeta;         // LayerNorm only
+  float* part;          // scratch: norm_part_floats(M, D)
+  const int32_t* idx;
+  const int32_t* n_kept;
+};
+size_t norm_part_floats(int M, int D);
+cudaError_t launch_norm_bwd(const Ctx& c, const NormBwdArgs& a);
+
+// SwiGLU backward: dgu[r] = [ds*u*sig(g)*(1+g*(1-sig(g))) | ds*silu(g)]
+// ds COMPACT (bf16 or f32) [*, F]; gu FULL bf16 [M, 2F] via idx; dgu COMPACT bf16 [*, 2F].
+cudaError_t launch_swiglu_bwd(const Ctx& c, const void* ds, int ds_is_bf16, int F,
+                              const __nv_bfloat16* gu, __nv_bfloat16* dgu, int M,
+                              const int32_t* idx, const int32_t* n_kept);
+// GELU-tanh backward: df1[r] = df2[r] * gelu'(f1[idx[r]]); df2 COMPACT, f1 FULL.
+cudaError_t launch_gelu_bwd(const Ctx& c, const void* df2, int df2_is_bf16, int F,
+                            const __nv_bfloat16* f1, __nv_bfloat16* df1, int M,
+                            const int32_t* idx, const int32_t* n_kept);
+
+// LM head: dz[r] = (softmax(z[idx[r]]) - onehot(targets[idx[r]])) / n_kept, bf16 COMPACT.
+cudaError_t launch_ce_bwd(const Ctx& c, const __nv_bfloat16* logits, const int32_t* targets, int V,
+                          int M, const int32_t* idx, const int32_t* n_kept, __nv_bfloat16* dz);
+// Embedding gradient: dE[v] = sum of dx rows of kept tokens with id v (ascending
+// kept order, deterministic); rows of unseen ids zeroed by the caller.
+cudaError_t launch_embed_bwd(const Ctx& c, const __nv_bfloat16* dx, long long ld, int D,
+                             const int32_t* ids, int V, int M, const int32_t* idx,
+                             const int32_t* n_kept, float* dE);
+
+// ---- fp32 SIMT GEMM (gemm_simt.cu) -----------------------------------------
+// C[m, n] = sum_k A(m, k) * B(k, n), f32 FMA.  Operands addressed by
+//   A(m,k) = A[rowA(m) * lda + k]     (a_trans = 0)   or  A[rowA(k) * lda + m] (a_trans = 1)
+//   B(k,n) = B[n * ldb + k]           (b_trans = 0)   or  B[rowB(k) * ldb + n] (b_trans = 1)
+// where row maps go through idx when the *_gather flag is set.  The dynamic
+// extent (n_kept) limits M (dyn = 1) or K (dyn = 2).  When c_scatter is set,
+// output row m is stored at row idx[m].
+struct SimtGemm {
+  int M, N, K;
+  const float* A; long long lda; int a_trans, a_gather;
+  const float* B; long long ldb; int b_trans, b_gather;
+  float* C; long long ldc; int c_scatter;
+  const int32_t* idx;
+  const int32_t* n_kept;
+  int dyn;
+};
+cudaError_t launch_simt_gemm(const Ctx& c, const SimtGemm& g);
+
+// ---- bf16 tcgen05 GEMM (gemm_tc.cu) ----------------------------------------
+// C[m, n] (+)= sum_k A(m,k) B(n,k), bf16 operands through TMA, f32 in TMEM.
+//   A: a_mn_major = 0 -> stored [M rows, K] (K contiguous), else [K rows, M].
+//   B: b_mn_major = 0 -> stored [N rows, K], else [K rows, N].
+// dyn = 1: M is limited by *n_kept (rows beyond are not computed; rows from
+// n_kept up to the next multiple of 128 are written 0 when zero_pad).
+// dyn = 2: K is limited by *n_kept (operand rows beyond must be 0 or finite
+// and are multiplied by 0-padded rows of the other operand -- callers keep
+// COMPACT buffers zero-padded to 128 rows).
+enum TcEpilogue { kEpiStore = 0 };
+struct TcGemm {
+  int M, N, K;
+  const void* A; long long lda; int a_mn_major;  // lda in elements
+  long long a_rows;   // rows of A's storage (M or K capacity)
+  const void* B; long long ldb; int b_mn_major;
+  long long b_rows;
+  void* C; long long ldc; int c_bf16; int accumulate; int zero_pad;
+  const int32_t* n_kept; int dyn;
+  int bn;             // 128 or 256 (0 = choose)
+};
+cudaError_t launch_tc_gemm(const Ctx& c, const TcGemm& g);
+bool tc_gemm_supported(const TcGemm& g);
+
+// ---- attention backward (attn.cu) ------------------------------------------
+struct AttnArgs {
+  int B, T, H, Hkv, dh, causal;
+  float scale;
+  int rotary_dim; float rope_base;
+  const __nv_bfloat16* q; const __nv_bfloat16* k; const __nv_bfloat16* v;   // COMPACT rows
+  const __nv_bfloat16* dO;
+  long long q_ld, kv_ld, do_ld;        // elements
+  const float* lse;                    // [B, H, T] (FULL positions)
+  const int32_t* idx; const int32_t* cu_kept; const int32_t* n_kept;
+  __nv_bfloat16* dq; __nv_bfloat16* dk; __nv_bfloat16* dv;   // COMPACT rows, same strides as inputs
+  long long dq_ld, dkv_ld;
+  float* dq_acc;   // scratch f32 [M, H, dh]
+  float* Dvec;     // scratch f32 [H, M]
+  float* lse_k;    // scratch f32 [H, M] (lse gathered to kept order, pre-scaled)
+  float2* rope;    // scratch [T, rotary_dim/2] (cos, sin)
+  int M;
+};
+size_t attn_ws_bytes(int B, int T, int H, int Hkv, int dh);
+cudaError_t launch_attn_bwd(const Ctx& c, const AttnArgs& a);
+
+}  // namespace collider

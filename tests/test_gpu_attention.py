@@ -1,0 +1,96 @@
+"""GPU parity: filtered attention backward (Figs. 3 and 5) against the fp64
+oracle, with and without the RoPE backward, GQA and MHA, head dims 64/128."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import ops
+from oracle.attention import attention_forward, filtered_attention_backward
+
+pytestmark = pytest.mark.gpu
+
+gu = pytest.importorskip("gpu_util")
+cl = gu.cl
+
+
+def _case(B, T, H, Hkv, dh, f, mask, seed, qk_std=1.0):
+    rng = np.random.default_rng(seed)
+    R = workloads.bf16_representable
+    q = R(rng.normal(size=(B * T, H, dh)) * qk_std)
+    k = R(rng.normal(size=(B * T, Hkv, dh)) * qk_std)
+    v = R(rng.normal(size=(B * T, Hkv, dh)))
+    dO = R(rng.normal(size=(B * T, H, dh)))
+    keep = workloads.keep_mask(B, T, f, mask, seed)
+    scale = 1 / math.sqrt(dh)
+    _, lse = attention_forward(q, k, v, B, T, scale)
+    lse = lse.astype(np.float32)
+    return q, k, v, dO, lse, keep, scale
+
+
+@pytest.mark.parametrize("B,T,H,Hkv,dh,f,mask,rot", [
+    (2, 200, 4, 2, 64, 0.4, "gumbel", 64),     # GQA, ragged sequence lengths
+    (1, 300, 2, 1, 128, 0.4, "gumbel", 128),   # head dim 128
+    (2, 130, 2, 2, 64, 0.6, "span", 32),       # MHA, partial rotary, span mask
+    (1, 64, 2, 2, 64, 0.0, "gumbel", 0),       # nothing filtered, no RoPE
+    (3, 100, 4, 1, 64, 0.2, "gumbel", 16),
+])
+@pytest.mark.parametrize("rows", ["full", "compact"])
+def test_attention_backward(B, T, H, Hkv, dh, f, mask, rot, rows):
+    q, k, v, dO, lse, keep, scale = _case(B, T, H, Hkv, dh, f, mask, seed=T + H + dh, qk_std=1.5)
+    M = B * T
+    idx, cu, nk = gu.compact(keep)
+    n = int(keep.sum())
+    kept = np.flatnonzero(keep.reshape(-1))
+    full = rows == "full"
+    pick = (lambda a: a) if full else (lambda a: np.concatenate([a[kept], np.zeros((M - n,) + a.shape[1:])]))
+    Qd, Kd, Vd, dOd = (gu.bf16(pick(a).reshape(M, -1)) for a in (q, k, v, dO))
+    dQ = torch.full((M, H * dh), float("nan"), dtype=torch.bfloat16, device=gu.DEV)
+    dK = torch.full((M, Hkv * dh), float("nan"), dtype=torch.bfloat16, device=gu.DEV)
+    dV = torch.full((M, Hkv * dh), float("nan"), dtype=torch.bfloat16, device=gu.DEV)
+    ws = torch.empty(cl.collider_attn_workspace_size(B, T, H, Hkv, dh), dtype=torch.uint8, device=gu.DEV)
+    mode = cl.ROWS_FULL if full else cl.ROWS_COMPACT
+    cl.collider_attn_bwd(B, T, H, Hkv, dh, 1, scale, rot, 10000.0, Qd, Kd, Vd, None, dOd, H * dh, Hkv * dh,
+                         H * dh, mode, gu.f32(lse), idx, cu, nk, dQ, dK, dV, mode, ws)
+    cl.collider_check()
+    rq, rk, rv = filtered_attention_backward(q, k, v, dO, lse, keep, scale)
+    pos = np.tile(np.arange(T), B)
+    if rot:
+        rq = ops.rope_backward(rq, pos, rot, 10000.0)
+        rk = ops.rope_backward(rk, pos, rot, 10000.0)
+    for got, ref, nh in ((dQ, rq, H), (dK, rk, Hkv), (dV, rv, Hkv)):
+        g = gu.host(got).reshape(M, nh, dh)
+        if not full:
+            g, ref = g[:n], ref[kept]
+            pad = min(-(-n // 128) * 128, M)
+            assert np.all(gu.host(got)[n:pad] == 0)
+        else:
+            assert np.all(g[keep.reshape(-1) == 0] == 0)
+        assert gu.rel_err(g, ref) <= 2e-2
+
+
+def test_attention_ignores_filtered_rows():
+    B, T, H, Hkv, dh = 2, 160, 4, 2, 64
+    q, k, v, dO, lse, keep, scale = _case(B, T, H, Hkv, dh, 0.4, "gumbel", seed=11)
+    M = B * T
+    idx, cu, nk = gu.compact(keep)
+    km = keep.reshape(-1) == 0
+    outs = []
+    for poison in (False, True):
+        arrs = [a.copy() for a in (q, k, v, dO)]
+        l2 = lse.copy()
+        if poison:
+            for a in arrs:
+                a[km] = np.nan
+            l2[np.broadcast_to((keep == 0)[:, None, :], l2.shape)] = np.inf
+        Qd, Kd, Vd, dOd = (gu.bf16(a.reshape(M, -1)) for a in arrs)
+        res = [torch.zeros((M, n * dh), dtype=torch.bfloat16, device=gu.DEV) for n in (H, Hkv, Hkv)]
+        ws = torch.empty(cl.collider_attn_workspace_size(B, T, H, Hkv, dh), dtype=torch.uint8, device=gu.DEV)
+        cl.collider_attn_bwd(B, T, H, Hkv, dh, 1, scale, 64, 10000.0, Qd, Kd, Vd, None, dOd, H * dh, Hkv * dh,
+                             H * dh, cl.ROWS_FULL, gu.f32(l2), idx, cu, nk, *res, cl.ROWS_FULL, ws)
+        torch.cuda.synchronize()
+        outs.append([r.cpu() for r in res])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b) and torch.isfinite(a.float()).all()
