@@ -39,6 +39,9 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--case", default="layer", choices=["layer", "gemm", "attn"],
+                   help="layer: the benchmark; gemm / attn: one kernel family on a small input "
+                        "(larger than L2) for profiler captures")
     return p.parse_args()
 
 
@@ -390,9 +393,67 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_case(args):
+    """One kernel family alone, for profiler captures: prints per-launch times."""
+    import torch
+    import sparse_backward_gemm_gb300 as cl
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    s = workloads.WORKLOADS[WORKLOAD]
+    keep = workloads.keep_mask(s.B, s.T, s.f, s.mask, s.seed_base)
+    mask = torch.from_numpy(keep).to(dev)
+    M = s.M
+    idx = torch.empty(M, dtype=torch.int32, device=dev)
+    cu = torch.empty(s.B + 1, dtype=torch.int32, device=dev)
+    nk = torch.empty(1, dtype=torch.int32, device=dev)
+    cl.collider_compact(mask, s.B, s.T, idx, cu, nk)
+    g = torch.Generator(device=dev).manual_seed(1)
+    rnd = lambda *shape: torch.randn(*shape, device=dev, generator=g).bfloat16()
+    if args.case == "gemm":
+        # MLP down-projection of the workload: dX [Mk, F] and dW [F, D] over the kept rows
+        K, N = s.F, s.D
+        X, W, dY = rnd(M, K), (rnd(K, N) * 0.02).bfloat16(), rnd(M, N)
+        dX = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+        dW = torch.empty(K, N, dtype=torch.float32, device=dev)
+        ws = torch.empty(cl.collider_linear_workspace_size(cl.BF16, M, K, N), dtype=torch.uint8, device=dev)
+        call = lambda: cl.collider_linear_bwd(cl.BF16, M, K, N, X, cl.ROWS_FULL, W, dY, cl.ROWS_FULL, idx, nk, dX,
+                                              cl.ROWS_COMPACT, dW, None, ws)
+        flops = {"tc_gemm": 2.0 * int(keep.sum()) * K * N}
+    else:
+        H, Hkv, dh = s.H, s.Hkv, s.dh
+        Q, Kt, V, dO = rnd(M, H * dh), rnd(M, Hkv * dh), rnd(M, Hkv * dh), rnd(M, H * dh)
+        lse = (torch.rand(s.B, s.H, s.T, device=dev, generator=g) * 4 + 2).float()
+        out = [torch.empty(M, n * dh, dtype=torch.bfloat16, device=dev) for n in (H, Hkv, Hkv)]
+        ws = torch.empty(cl.collider_attn_workspace_size(s.B, s.T, H, Hkv, dh), dtype=torch.uint8, device=dev)
+        call = lambda: cl.collider_attn_bwd(s.B, s.T, H, Hkv, dh, 1, dh ** -0.5, dh, s.rope_base, Q, Kt, V, None,
+                                            dO, H * dh, Hkv * dh, H * dh, cl.ROWS_FULL, lse, idx, cu, nk, *out,
+                                            cl.ROWS_COMPACT, ws)
+        flops = {"attn_main": attn_flops(s, keep.sum(axis=1).tolist())}
+    for _ in range(args.warmup):
+        call()
+    cl.collider_check()
+    cl.collider_profile_enable(1)
+    for _ in range(args.steps):
+        call()
+    torch.cuda.synchronize()
+    cl.collider_profile_enable(0)
+    cl.collider_check()
+    per = {}
+    for i in range(cl.collider_profile_count()):
+        name, _, ms = cl.collider_profile_get(i)
+        per.setdefault(name, []).append(ms)
+    res = {k: {"launches_per_call": len(v) // args.steps, "ms_per_call": sum(v) / args.steps} for k, v in per.items()}
+    for k, fl in flops.items():
+        if k in res:
+            res[k]["tflops"] = fl / (res[k]["ms_per_call"] * 1e-3) / 1e12
+    print(json.dumps({"case": args.case, "kernels": res}))
+
+
 if __name__ == "__main__":
     a = parse()
     if a.impl == "reference":
         run_reference(a)
+    elif a.case != "layer":
+        run_case(a)
     else:
         run_ours(a)

@@ -233,7 +233,7 @@ extern "C" collider_status collider_gather_rows(const void* src, size_t src_ld_b
   if (s != COLLIDER_OK) return s;
   GatherJob j{static_cast<const char*>(src), static_cast<char*>(dst), (long long)src_ld_bytes,
               (long long)dst_ld_bytes, (int)row_bytes, 0};
-  CK(launch_gather(c, &j, 1, M, idx, n_kept));
+  CK(launch_gather(c, &j, 1, M, M, idx, n_kept));
   return COLLIDER_OK;
 }
 
@@ -353,8 +353,8 @@ extern "C" collider_status collider_linear_bwd(collider_dtype dtype, int M, int 
                        K * 2, 0};
     const GatherJob jy{static_cast<const char*>(dY), static_cast<char*>(dyk), (long long)N * 2, (long long)N * 2,
                        N * 2, 0};
-    if (dW) CK(launch_gather(c, &jx, 1, M, x_full ? idx : nullptr, n_kept));
-    CK(launch_gather(c, &jy, 1, M, dy_full ? idx : nullptr, n_kept));
+    if (dW) CK(launch_gather(c, &jx, 1, M, pad128(M), x_full ? idx : nullptr, n_kept));
+    CK(launch_gather(c, &jy, 1, M, pad128(M), dy_full ? idx : nullptr, n_kept));
     if (dW) Xk = static_cast<const __nv_bfloat16*>(xk);
     dYk = static_cast<const __nv_bfloat16*>(dyk);
   }
@@ -363,7 +363,7 @@ extern "C" collider_status collider_linear_bwd(collider_dtype dtype, int M, int 
     g.M = M; g.N = K; g.K = N;
     g.A = dYk; g.lda = N; g.a_mn_major = 0; g.a_rows = M;
     g.B = W; g.ldb = N; g.b_mn_major = 0; g.b_rows = K;
-    g.C = dx_full ? dxk : dX; g.ldc = K; g.c_bf16 = 1; g.zero_pad = 1;
+    g.C = dx_full ? dxk : dX; g.ldc = K; g.c_bf16 = 1; g.zero_pad = 1; g.c_rows = dx_full ? pad128(M) : M;
     g.n_kept = n_kept; g.dyn = 1;
     CK(launch_tc_gemm(c, g));
     if (dx_full) CK(launch_scatter(c, static_cast<const char*>(dxk), (long long)K * 2, static_cast<char*>(dX),
@@ -456,6 +456,7 @@ extern "C" collider_status collider_attn_bwd(int B, int T, int H, int Hkv, int d
   a.rotary_dim = rotary_dim; a.rope_base = rope_base;
   a.lse = lse; a.idx = idx; a.cu_kept = cu_kept; a.n_kept = n_kept;
   a.dq_acc = sc.dq_acc; a.Dvec = sc.Dvec; a.lse_k = sc.lse2; a.rope = sc.rope; a.M = M;
+  a.cap = out_rows == COLLIDER_ROWS_FULL ? Mp : M;
   if (in_rows == COLLIDER_ROWS_FULL) {
     GatherJob j[4] = {
         {static_cast<const char*>(Q), reinterpret_cast<char*>(cq), (long long)q_ld * 2, (long long)H * dh * 2,
@@ -466,7 +467,7 @@ extern "C" collider_status collider_attn_bwd(int B, int T, int H, int Hkv, int d
          Hkv * dh * 2, 0},
         {static_cast<const char*>(V), reinterpret_cast<char*>(cvv), (long long)kv_ld * 2, (long long)Hkv * dh * 2,
          Hkv * dh * 2, 0}};
-    CK(launch_gather(c, j, 4, M, idx, n_kept));
+    CK(launch_gather(c, j, 4, M, Mp, idx, n_kept));
     a.q = cq; a.dO = cdo; a.k = ck; a.v = cvv;
     a.q_ld = (long long)H * dh; a.do_ld = (long long)H * dh; a.kv_ld = (long long)Hkv * dh;
   } else {
@@ -562,7 +563,7 @@ cudaError_t gemm_dx(const Ctx& c, int M, int N, int K, const void* A, const void
   g.M = M; g.N = N; g.K = K;
   g.A = A; g.lda = K; g.a_mn_major = 0; g.a_rows = pad128(M);
   g.B = W; g.ldb = K; g.b_mn_major = 0; g.b_rows = N;
-  g.C = C; g.ldc = N; g.c_bf16 = c_bf16; g.accumulate = accumulate; g.zero_pad = 1;
+  g.C = C; g.ldc = N; g.c_bf16 = c_bf16; g.accumulate = accumulate; g.zero_pad = 1; g.c_rows = pad128(M);
   g.n_kept = n_kept; g.dyn = 1;
   return launch_tc_gemm(c, g);
 }
@@ -611,10 +612,10 @@ collider_status layer_bwd_impl(const Ctx& c, const collider_layer_desc* d, const
     j[n++] = GatherJob{static_cast<const char*>(sv->qkv), reinterpret_cast<char*>(L.qkv_k), (long long)Nqkv * 2,
                        (long long)Nqkv * 2, Nqkv * 2, 0};
     if (dout_full) {
-      CK(launch_gather(c, j, n, M, idx, n_kept));
+      CK(launch_gather(c, j, n, M, pad128(M), idx, n_kept));
     } else {
-      CK(launch_gather(c, j, 1, M, nullptr, n_kept));   // COMPACT dOut: copy + zero padding
-      CK(launch_gather(c, j + 1, n - 1, M, idx, n_kept));
+      CK(launch_gather(c, j, 1, M, pad128(M), nullptr, n_kept));   // COMPACT dOut: copy + zero padding
+      CK(launch_gather(c, j + 1, n - 1, M, pad128(M), idx, n_kept));
     }
   }
 
@@ -623,7 +624,8 @@ collider_status layer_bwd_impl(const Ctx& c, const collider_layer_desc* d, const
   if (llama) {
     CK(gemm_dx(c, M, F, D, L.dout_k, w->w_down, L.ds_k, 1, 0, n_kept));               // ds = dOut W_down^T
     CK(gemm_dw(c, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept));               // dW_down = s^T dOut
-    CK(launch_swiglu_bwd(c, L.ds_k, 1, F, static_cast<const __nv_bfloat16*>(sv->up), L.dgu_k, M, idx, n_kept));
+    CK(launch_swiglu_bwd(c, L.ds_k, 1, F, static_cast<const __nv_bfloat16*>(sv->up), L.dgu_k, M, pad128(M), idx,
+                         n_kept));
     CK(gemm_dx(c, M, D, Nup, L.dgu_k, w->w_up, L.db_k, 0, 0, n_kept));                // db = dgu W_up^T
     CK(gemm_dw(c, M, D, Nup, L.b_k, D, L.dgu_k, Nup, g->dw_up, n_kept));              // dW_up = b^T dgu
     NormBwdArgs nb{};
@@ -631,7 +633,7 @@ collider_status layer_bwd_impl(const Ctx& c, const collider_layer_desc* d, const
     nb.dy1 = L.db_k; nb.res = L.dout_k; nb.res_ld = D;
     nb.x = static_cast<const __nv_bfloat16*>(sv->h); nb.rstd = sv->rstd2;
     nb.gamma = static_cast<const __nv_bfloat16*>(w->norm2_w);
-    nb.out = L.dh_k; nb.dgamma = g->dnorm2_w; nb.part = L.norm_part; nb.idx = idx; nb.n_kept = n_kept;
+    nb.out = L.dh_k; nb.cap = pad128(M); nb.dgamma = g->dnorm2_w; nb.part = L.norm_part; nb.idx = idx; nb.n_kept = n_kept;
     CK(launch_norm_bwd(c, nb));                                                          // dh = dOut + norm2'
     dres = L.dh_k;
   } else {
@@ -639,7 +641,8 @@ collider_status layer_bwd_impl(const Ctx& c, const collider_layer_desc* d, const
     CK(gemm_dw(c, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept));               // dW2 = gelu(f1)^T dOut
     if (d->mlp_bias && g->db_down)
       CK(launch_colsum(c, L.dout_k, 1, D, M, D, nullptr, n_kept, L.col_part, g->db_down));
-    CK(launch_gelu_bwd(c, L.ds_k, 1, F, static_cast<const __nv_bfloat16*>(sv->up), L.dgu_k, M, idx, n_kept));
+    CK(launch_gelu_bwd(c, L.ds_k, 1, F, static_cast<const __nv_bfloat16*>(sv->up), L.dgu_k, M, pad128(M), idx,
+                       n_kept));
     CK(gemm_dw(c, M, D, F, L.a_k, D, L.dgu_k, F, g->dw_up, n_kept));                  // dW1 = a^T df1
     if (d->mlp_bias && g->db_up)
       CK(launch_colsum(c, L.dgu_k, 1, F, M, F, nullptr, n_kept, L.col_part, g->db_up));
@@ -663,6 +666,7 @@ collider_status layer_bwd_impl(const Ctx& c, const collider_layer_desc* d, const
     a.dq = L.dqkv_k; a.dk = L.dqkv_k + Hd; a.dv = L.dqkv_k + Hd + Hkv * dh;
     a.dq_ld = Nqkv; a.dkv_ld = Nqkv;
     a.dq_acc = L.at.dq_acc; a.Dvec = L.at.Dvec; a.lse_k = L.at.lse2; a.rope = L.at.rope; a.M = M;
+    a.cap = pad128(M);
     CK(launch_attn_bwd(c, a));
   }
 
@@ -680,7 +684,7 @@ collider_status layer_bwd_impl(const Ctx& c, const collider_layer_desc* d, const
     nb.dy1 = L.da_k; nb.res = dres; nb.res_ld = D;
     nb.x = static_cast<const __nv_bfloat16*>(sv->x); nb.mean = sv->mean1; nb.rstd = sv->rstd1;
     nb.gamma = static_cast<const __nv_bfloat16*>(w->norm1_w);
-    nb.out = dxk; nb.dgamma = g->dnorm1_w; nb.dbeta = g->dnorm1_b; nb.part = L.norm_part;
+    nb.out = dxk; nb.cap = dx_full ? pad128(M) : M; nb.dgamma = g->dnorm1_w; nb.dbeta = g->dnorm1_b; nb.part = L.norm_part;
     nb.idx = idx; nb.n_kept = n_kept;
     CK(launch_norm_bwd(c, nb));
   }
@@ -813,11 +817,11 @@ extern "C" collider_status collider_stack_bwd(const collider_layer_desc* d, int 
   const int M = d->B * d->T, D = d->D;
 
   // LM head: dz = (softmax(z) - onehot) / n_kept on kept rows
-  CK(launch_ce_bwd(c, static_cast<const __nv_bfloat16*>(logits), targets, V, M, idx, n_kept, S.dz_k));
+  CK(launch_ce_bwd(c, static_cast<const __nv_bfloat16*>(logits), targets, V, M, pad128(M), idx, n_kept, S.dz_k));
   {
     GatherJob j{static_cast<const char*>(y), reinterpret_cast<char*>(S.y_k), (long long)D * 2, (long long)D * 2,
                 D * 2, 0};
-    CK(launch_gather(c, &j, 1, M, idx, n_kept));
+    CK(launch_gather(c, &j, 1, M, pad128(M), idx, n_kept));
   }
   CK(gemm_dw(c, M, D, V, S.y_k, D, S.dz_k, V, dw_lm, n_kept));            // dW_lm = y^T dz
   CK(gemm_dx(c, M, D, V, S.dz_k, w_lm, S.dyf_k, 0, 0, n_kept));           // dy = dz W_lm^T
@@ -827,7 +831,7 @@ extern "C" collider_status collider_stack_bwd(const collider_layer_desc* d, int 
     nb.dy1 = S.dyf_k; nb.res = nullptr;
     nb.x = static_cast<const __nv_bfloat16*>(xL); nb.rstd = rstdf;
     nb.gamma = static_cast<const __nv_bfloat16*>(normf_w);
-    nb.out = S.dxa; nb.dgamma = dnormf_w; nb.part = S.part; nb.idx = idx; nb.n_kept = n_kept;
+    nb.out = S.dxa; nb.cap = pad128(M); nb.dgamma = dnormf_w; nb.part = S.part; nb.idx = idx; nb.n_kept = n_kept;
     CK(launch_norm_bwd(c, nb));
   }
   // blocks, last to first, staying COMPACT between blocks

@@ -89,6 +89,7 @@ struct AttnK {
   float* lse2;       // [H, M]  lse * log2(e), kept order
   const float2* rope;  // [T, rot_half] (cos, sin)
   int M;
+  long long cap;     // row capacity of dq, dk, dv
   DevStatus* st;
 };
 
@@ -439,7 +440,7 @@ __global__ void __launch_bounds__(128) attn_main_kernel(AttnK p) {
 // finalize: dQ = scale * acc, RoPE backward, bf16; zero rows n_kept..pad of dQ, dK, dV
 __global__ void attn_finalize_kernel(AttnK p, int DH) {
   const int nk = *p.n_kept;
-  const int pad = padded_rows(nk, p.M);
+  const int pad = padded_rows(nk, p.cap);
   const int rh = p.rot_half;
   const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   const long long stride = (long long)gridDim.x * blockDim.x;
@@ -549,7 +550,7 @@ cudaError_t launch_attn_bwd(const Ctx& c, const AttnArgs& a) {
   k.lse = a.lse; k.idx = a.idx; k.cu_kept = a.cu_kept; k.n_kept = a.n_kept;
   k.dq = a.dq; k.dk = a.dk; k.dv = a.dv; k.dq_ld = a.dq_ld; k.dkv_ld = a.dkv_ld;
   k.dq_acc = a.dq_acc; k.Dvec = a.Dvec; k.lse2 = a.lse_k;
-  k.M = a.M; k.st = c.st;
+  k.M = a.M; k.cap = a.cap > 0 ? a.cap : a.M; k.st = c.st;
   k.rope = a.rope;
   if (a.dh == 64) return run<64>(c, k, a.rope_base);
   if (a.dh == 128) return run<128>(c, k, a.rope_base);

@@ -97,9 +97,9 @@ __device__ __forceinline__ float block_max(float v, float* red) {
 
 // Rows a COMPACT buffer must hold valid data or zeros for: n_kept rounded up
 // to the GEMM tile height, capped at the buffer capacity.
-__device__ __forceinline__ int padded_rows(int n, int cap) {
-  int p = (n + 127) & ~127;
-  return p < cap ? p : cap;
+__device__ __forceinline__ int padded_rows(int n, long long cap) {
+  long long p = ((long long)n + 127) & ~127ll;
+  return (int)(p < cap ? p : cap);
 }
 
 }  // namespace collider

@@ -36,6 +36,7 @@ struct TcParams {
   int c_bf16;
   int accumulate;
   int zero_pad;
+  long long c_rows;
   DevStatus* st;
 };
 
@@ -285,7 +286,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int m0 = (tile % m_tiles) * BM, n0 = (tile / m_tiles) * BN;
       const int row = m0 + q * 32 + lane;
       const bool row_ok = row < M;
-      const bool row_zero = !row_ok && p.zero_pad && row < padded_rows(M, p.M);
+      const bool row_zero = !row_ok && p.zero_pad && row < padded_rows(M, p.c_rows);
       for (int c = 0; c < BN; c += 32) {
         float v[32];
         if (num_kb > 0) {
@@ -408,7 +409,8 @@ cudaError_t launch_tc_gemm(const Ctx& c, const TcGemm& g) {
   ok = ok && (g.b_mn_major ? make_map(&mb, g.B, g.N, g.b_rows, g.ldb, 64)
                            : make_map(&mb, g.B, g.K, g.b_rows, g.ldb, bn));
   if (!ok) return cudaErrorInvalidValue;
-  TcParams p{g.M, g.N, g.K, g.dyn, g.n_kept, g.C, g.ldc, g.c_bf16, g.accumulate, g.zero_pad, c.st};
+  TcParams p{g.M, g.N, g.K, g.dyn, g.n_kept, g.C, g.ldc, g.c_bf16, g.accumulate, g.zero_pad,
+             g.c_rows > 0 ? g.c_rows : g.M, c.st};
   prof_begin(c, "tc_gemm", g.M, g.N, g.K, g.dyn);
   cudaError_t e;
   const int key = (bn == 256 ? 4 : 0) | (g.a_mn_major ? 2 : 0) | (g.b_mn_major ? 1 : 0);

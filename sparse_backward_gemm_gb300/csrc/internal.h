@@ -42,7 +42,8 @@ struct GatherJob {
 };
 constexpr int kMaxGatherJobs = 8;
 // idx may be null: identity (copy the first n_kept rows, zero the padding).
-cudaError_t launch_gather(const Ctx& c, const GatherJob* jobs, int njobs, int M, const int32_t* idx,
+// cap: row capacity of every dst (rows n_kept .. min(next multiple of 128, cap) are zeroed).
+cudaError_t launch_gather(const Ctx& c, const GatherJob* jobs, int njobs, int M, long long cap, const int32_t* idx,
                           const int32_t* n_kept);
 cudaError_t launch_scatter(const Ctx& c, const char* compact, long long compact_ld, char* full,
                            long long full_ld, int row_bytes, int M, const int32_t* idx,
@@ -72,6 +73,7 @@ struct NormBwdArgs {
   const float* rstd;    // FULL f32 [M]
   const __nv_bfloat16* gamma;
   __nv_bfloat16* out;   // COMPACT bf16 [*, D]
+  long long cap;        // row capacity of out (zero padding stops there)
   float* dgamma;
   float* dbeta;         // LayerNorm only
   float* part;          // scratch: norm_part_floats(M, D)
@@ -84,16 +86,17 @@ cudaError_t launch_norm_bwd(const Ctx& c, const NormBwdArgs& a);
 // SwiGLU backward: dgu[r] = [ds*u*sig(g)*(1+g*(1-sig(g))) | ds*silu(g)]
 // ds COMPACT (bf16 or f32) [*, F]; gu FULL bf16 [M, 2F] via idx; dgu COMPACT bf16 [*, 2F].
 cudaError_t launch_swiglu_bwd(const Ctx& c, const void* ds, int ds_is_bf16, int F,
-                              const __nv_bfloat16* gu, __nv_bfloat16* dgu, int M,
+                              const __nv_bfloat16* gu, __nv_bfloat16* dgu, int M, long long cap,
                               const int32_t* idx, const int32_t* n_kept);
 // GELU-tanh backward: df1[r] = df2[r] * gelu'(f1[idx[r]]); df2 COMPACT, f1 FULL.
 cudaError_t launch_gelu_bwd(const Ctx& c, const void* df2, int df2_is_bf16, int F,
-                            const __nv_bfloat16* f1, __nv_bfloat16* df1, int M,
+                            const __nv_bfloat16* f1, __nv_bfloat16* df1, int M, long long cap,
                             const int32_t* idx, const int32_t* n_kept);
 
 // LM head: dz[r] = (softmax(z[idx[r]]) - onehot(targets[idx[r]])) / n_kept, bf16 COMPACT.
 cudaError_t launch_ce_bwd(const Ctx& c, const __nv_bfloat16* logits, const int32_t* targets, int V,
-                          int M, const int32_t* idx, const int32_t* n_kept, __nv_bfloat16* dz);
+                          int M, long long cap, const int32_t* idx, const int32_t* n_kept,
+                          __nv_bfloat16* dz);
 // Embedding gradient: dE[v] = sum of dx rows of kept tokens with id v (ascending
 // kept order, deterministic); rows of unseen ids zeroed by the caller.
 cudaError_t launch_embed_bwd(const Ctx& c, const __nv_bfloat16* dx, long long ld, int D,
@@ -135,6 +138,7 @@ struct TcGemm {
   const void* B; long long ldb; int b_mn_major;
   long long b_rows;
   void* C; long long ldc; int c_bf16; int accumulate; int zero_pad;
+  long long c_rows;   // row capacity of C (zero padding stops there)
   const int32_t* n_kept; int dyn;
   int bn;             // 128 or 256 (0 = choose)
 };
@@ -158,6 +162,7 @@ struct AttnArgs {
   float* lse_k;    // scratch f32 [H, M] (lse gathered to kept order, pre-scaled)
   float2* rope;    // scratch [T, rotary_dim/2] (cos, sin)
   int M;
+  long long cap;   // row capacity of dq, dk, dv (zero padding stops there)
 };
 size_t attn_ws_bytes(int B, int T, int H, int Hkv, int dh);
 cudaError_t launch_attn_bwd(const Ctx& c, const AttnArgs& a);

@@ -47,11 +47,12 @@ struct GatherBatch {
   GatherJob j[kMaxGatherJobs];
 };
 
-__global__ void __launch_bounds__(256) gather_kernel(GatherBatch jb, int M, const int32_t* __restrict__ idx,
+__global__ void __launch_bounds__(256) gather_kernel(GatherBatch jb, int M, long long cap,
+                                                     const int32_t* __restrict__ idx,
                                                      const int32_t* __restrict__ n_kept, DevStatus* st) {
   const GatherJob J = jb.j[blockIdx.y];
   const int nk = *n_kept;
-  const int pad = padded_rows(nk, M);
+  const int pad = padded_rows(nk, cap);
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
   const int vecs = J.row_bytes >> 4;
@@ -150,108 +151,111 @@ __global__ void __launch_bounds__(256) colsum_reduce_kernel(const float* __restr
 }
 
 // ---------------------------------------------------------------------------
-// norm backward (+ residual) on kept rows
-constexpr int kNormRows = 16;
-constexpr int kNormThreads = 256;
-constexpr int kNormMaxIt = 2;   // D <= 2 * 256 * 8 = 4096
+// norm backward (+ residual) on kept rows: one warp per row, two passes over
+// the row (the second re-reads it from L1/L2).  dgamma / dbeta partials go to
+// a per-warp shared-memory row and are summed over the warps in a fixed order,
+// so the result is deterministic.
+constexpr int kNormWarps = 4;
+constexpr int kNormRowsPerWarp = 8;
+constexpr int kNormRows = kNormWarps * kNormRowsPerWarp;   // rows per block (one partial row each)
 
-__global__ void __launch_bounds__(kNormThreads) norm_bwd_kernel(NormBwdArgs a, DevStatus* st) {
-  __shared__ float red[32];
-  const int nk = *a.n_kept;
-  const int pad = padded_rows(nk, a.M);
-  const int r0 = blockIdx.x * kNormRows;
-  if (r0 >= pad) return;
+__global__ void __launch_bounds__(kNormWarps * 32) norm_bwd_kernel(NormBwdArgs a, DevStatus* st) {
+  extern __shared__ float sp[];   // [kNormWarps][nsets][D]
+  const int nsets = a.layer_norm ? 2 : 1;
   const int D = a.D;
-  float dg[kNormMaxIt][8], db[kNormMaxIt][8];
-#pragma unroll
-  for (int j = 0; j < kNormMaxIt; ++j)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) dg[j][i] = db[j][i] = 0.f;
-  for (int r = r0; r < min(r0 + kNormRows, pad); ++r) {
-    if (r >= nk) {   // zero padding rows
-      for (int c = threadIdx.x * 8; c < D; c += kNormThreads * 8)
-        *reinterpret_cast<uint4*>(a.out + (long long)r * D + c) = make_uint4(0, 0, 0, 0);
+  const int nk = *a.n_kept;
+  const int pad = padded_rows(nk, a.cap);
+  const int rb = blockIdx.x * kNormRows;
+  if (rb >= pad) return;
+  for (int i = threadIdx.x; i < kNormWarps * nsets * D; i += blockDim.x) sp[i] = 0.f;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* mine = sp + warp * nsets * D;
+  const int r0 = rb + warp * kNormRowsPerWarp;
+  for (int i = 0; i < kNormRowsPerWarp; ++i) {
+    const int r = r0 + i;
+    if (r >= pad) break;
+    __nv_bfloat16* orow = a.out + (long long)r * D;
+    if (r >= nk) {
+      for (int c = lane * 8; c < D; c += 256) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
       continue;
     }
     const int t = a.idx[r];
     if ((unsigned)t >= (unsigned)a.M) {
-      if (threadIdx.x == 0) report_error(st, kErrBadIndex, 200);
+      if (lane == 0) report_error(st, kErrBadIndex, 200);
       continue;
     }
     const float rstd = a.rstd[t];
     const float mu = a.layer_norm ? a.mean[t] : 0.f;
-    float g[kNormMaxIt][8], xh[kNormMaxIt][8], dyv[kNormMaxIt][8];
+    const float* dy1 = a.dy1 + (long long)r * D;
+    const float* dy2 = a.dy2 ? a.dy2 + (long long)r * D : nullptr;
+    const __nv_bfloat16* xr = a.x + (long long)t * D;
     float s_gx = 0.f, s_g = 0.f;
+    for (int c = lane * 8; c < D; c += 256) {
+      float dy[8], xv[8], gm[8];
+      load8(dy1, 0, c, dy);
+      if (dy2) {
+        float d2[8];
+        load8(dy2, 0, c, d2);
 #pragma unroll
-    for (int j = 0; j < kNormMaxIt; ++j) {
-      const int c = (threadIdx.x + j * kNormThreads) * 8;
-      if (c < D) {
-        float dy[8], xv[8], gm[8];
-        load8(a.dy1, 0, (long long)r * D + c, dy);
-        if (a.dy2) {
-          float d2[8];
-          load8(a.dy2, 0, (long long)r * D + c, d2);
+        for (int k = 0; k < 8; ++k) dy[k] += d2[k];
+      }
+      load8(xr, 1, c, xv);
+      load8(a.gamma, 1, c, gm);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) dy[i] += d2[i];
-        }
-        load8(a.x, 1, (long long)t * D + c, xv);
-        load8(a.gamma, 1, c, gm);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          dyv[j][i] = dy[i];
-          xh[j][i] = (xv[i] - mu) * rstd;
-          g[j][i] = dy[i] * gm[i];
-          s_gx += g[j][i] * xh[j][i];
-          s_g += g[j][i];
-        }
+      for (int k = 0; k < 8; ++k) {
+        const float g = dy[k] * gm[k];
+        s_gx += g * (xv[k] - mu) * rstd;
+        s_g += g;
       }
     }
-    s_gx = block_sum(s_gx, red) / (float)D;
-    if (a.layer_norm) s_g = block_sum(s_g, red) / (float)D;
+    s_gx = warp_sum(s_gx) / (float)D;
+    s_g = a.layer_norm ? warp_sum(s_g) / (float)D : 0.f;
+    for (int c = lane * 8; c < D; c += 256) {
+      float dy[8], xv[8], gm[8], o[8];
+      load8(dy1, 0, c, dy);
+      if (dy2) {
+        float d2[8];
+        load8(dy2, 0, c, d2);
 #pragma unroll
-    for (int j = 0; j < kNormMaxIt; ++j) {
-      const int c = (threadIdx.x + j * kNormThreads) * 8;
-      if (c < D) {
-        float o[8], rs[8];
-        if (a.res) load8(a.res, 1, (long long)r * a.res_ld + c, rs);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float v = g[j][i] - xh[j][i] * s_gx;
-          if (a.layer_norm) v -= s_g;
-          o[i] = rstd * v + (a.res ? rs[i] : 0.f);
-          dg[j][i] += dyv[j][i] * xh[j][i];
-          db[j][i] += dyv[j][i];
-        }
-        *reinterpret_cast<uint4*>(a.out + (long long)r * D + c) = pack8(o);
+        for (int k = 0; k < 8; ++k) dy[k] += d2[k];
       }
+      load8(xr, 1, c, xv);
+      load8(a.gamma, 1, c, gm);
+      if (a.res) {
+        load8(a.res, 1, (long long)r * a.res_ld + c, o);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) o[k] = 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float xh = (xv[k] - mu) * rstd;
+        o[k] += rstd * (dy[k] * gm[k] - xh * s_gx - s_g);
+        mine[c + k] += dy[k] * xh;
+        if (nsets == 2) mine[D + c + k] += dy[k];
+      }
+      *reinterpret_cast<uint4*>(orow + c) = pack8(o);
     }
   }
-  // partials for dgamma (set 0) and dbeta (set 1): layout [part][set][D]
-  const int nsets = a.layer_norm ? 2 : 1;
+  __syncthreads();
+  float* part = a.part + (long long)blockIdx.x * nsets * D;
+  for (int i = threadIdx.x; i < nsets * D; i += blockDim.x) {
+    float v = 0.f;
 #pragma unroll
-  for (int j = 0; j < kNormMaxIt; ++j) {
-    const int c = (threadIdx.x + j * kNormThreads) * 8;
-    if (c < D) {
-      float4* p = reinterpret_cast<float4*>(a.part + ((long long)blockIdx.x * nsets) * D + c);
-      p[0] = make_float4(dg[j][0], dg[j][1], dg[j][2], dg[j][3]);
-      p[1] = make_float4(dg[j][4], dg[j][5], dg[j][6], dg[j][7]);
-      if (nsets == 2) {
-        float4* q = reinterpret_cast<float4*>(a.part + ((long long)blockIdx.x * nsets + 1) * D + c);
-        q[0] = make_float4(db[j][0], db[j][1], db[j][2], db[j][3]);
-        q[1] = make_float4(db[j][4], db[j][5], db[j][6], db[j][7]);
-      }
-    }
+    for (int w = 0; w < kNormWarps; ++w) v += sp[w * nsets * D + i];
+    part[i] = v;
   }
 }
 
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const void* __restrict__ ds, int ds_bf16, int F,
                                                          const __nv_bfloat16* __restrict__ gu,
-                                                         __nv_bfloat16* __restrict__ dgu, int M,
+                                                         __nv_bfloat16* __restrict__ dgu, int M, long long cap,
                                                          const int32_t* __restrict__ idx,
                                                          const int32_t* __restrict__ n_kept, DevStatus* st) {
   const int nk = *n_kept;
-  const int pad = padded_rows(nk, M);
+  const int pad = padded_rows(nk, cap);
   const int vpr = F >> 3;   // 8-wide vectors per row
   const long long total = (long long)pad * vpr;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
@@ -282,11 +286,11 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const void* __restrict_
 
 __global__ void __launch_bounds__(256) gelu_bwd_kernel(const void* __restrict__ df2, int df2_bf16, int F,
                                                        const __nv_bfloat16* __restrict__ f1,
-                                                       __nv_bfloat16* __restrict__ df1, int M,
+                                                       __nv_bfloat16* __restrict__ df1, int M, long long cap,
                                                        const int32_t* __restrict__ idx,
                                                        const int32_t* __restrict__ n_kept, DevStatus* st) {
   const int nk = *n_kept;
-  const int pad = padded_rows(nk, M);
+  const int pad = padded_rows(nk, cap);
   const int vpr = F >> 3;
   const long long total = (long long)pad * vpr;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
@@ -310,12 +314,12 @@ constexpr int kCeThreads = 512;
 
 __global__ void __launch_bounds__(kCeThreads) ce_bwd_kernel(const __nv_bfloat16* __restrict__ z,
                                                             const int32_t* __restrict__ targets, int V, int M,
-                                                            const int32_t* __restrict__ idx,
+                                                            long long cap, const int32_t* __restrict__ idx,
                                                             const int32_t* __restrict__ n_kept,
                                                             __nv_bfloat16* __restrict__ dz, DevStatus* st) {
   __shared__ float red[32];
   const int nk = *n_kept;
-  const int pad = padded_rows(nk, M);
+  const int pad = padded_rows(nk, cap);
   const int r = blockIdx.x;
   if (r >= pad) return;
   __nv_bfloat16* o = dz + (long long)r * V;
@@ -422,16 +426,16 @@ inline int grid_rows(const Ctx& c, long long rows, int per_block) {
 
 }  // namespace
 
-cudaError_t launch_gather(const Ctx& c, const GatherJob* jobs, int njobs, int M, const int32_t* idx,
-                          const int32_t* n_kept) {
+cudaError_t launch_gather(const Ctx& c, const GatherJob* jobs, int njobs, int M, long long cap,
+                          const int32_t* idx, const int32_t* n_kept) {
   if (njobs <= 0) return cudaSuccess;
   GatherBatch b{};
   for (int i = 0; i < njobs; ++i) b.j[i] = jobs[i];
-  dim3 grid(grid_rows(c, M, 8), njobs);
+  dim3 grid(grid_rows(c, cap, 8), njobs);
   double bytes = 0;
   for (int i = 0; i < njobs; ++i) bytes += 2.0 * jobs[i].row_bytes;  // per kept row
   prof_begin(c, "gather_rows");
-  gather_kernel<<<grid, 256, 0, c.stream>>>(b, M, idx, n_kept, c.st);
+  gather_kernel<<<grid, 256, 0, c.stream>>>(b, M, cap, idx, n_kept, c.st);
   prof_end(c);
   count_launch();
   return cudaGetLastError();
@@ -466,11 +470,21 @@ cudaError_t launch_colsum(const Ctx& c, const void* X, int x_is_bf16, long long 
 size_t norm_part_floats(int M, int D) { return (size_t)((M + kNormRows - 1) / kNormRows) * 2 * (size_t)D; }
 
 cudaError_t launch_norm_bwd(const Ctx& c, const NormBwdArgs& a) {
-  int grid = (a.M + kNormRows - 1) / kNormRows;
-  prof_begin(c, "norm_bwd");
-  norm_bwd_kernel<<<grid, kNormThreads, 0, c.stream>>>(a, c.st);
-  // partials are laid out [part][set][D] with set 0 = dgamma, set 1 = dbeta
   const int nsets = a.layer_norm ? 2 : 1;
+  const size_t smem = (size_t)kNormWarps * nsets * a.D * sizeof(float);
+  static int seen[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !seen[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(norm_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kNormWarps * 2 * 4096 * (int)sizeof(float));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) seen[dev] = 1;
+  }
+  const int grid = (int)((a.cap + kNormRows - 1) / kNormRows);
+  prof_begin(c, "norm_bwd");
+  norm_bwd_kernel<<<grid, kNormWarps * 32, smem, c.stream>>>(a, c.st);
+  // partials are laid out [block][set][D] with set 0 = dgamma, set 1 = dbeta
   const int g = (a.D + 255) / 256;
   colsum_reduce_kernel<<<g, 256, 0, c.stream>>>(a.part, a.D, (long long)nsets * a.D, kNormRows, a.n_kept,
                                                 a.dgamma);
@@ -483,29 +497,29 @@ cudaError_t launch_norm_bwd(const Ctx& c, const NormBwdArgs& a) {
 }
 
 cudaError_t launch_swiglu_bwd(const Ctx& c, const void* ds, int ds_is_bf16, int F, const __nv_bfloat16* gu,
-                              __nv_bfloat16* dgu, int M, const int32_t* idx, const int32_t* n_kept) {
+                              __nv_bfloat16* dgu, int M, long long cap, const int32_t* idx, const int32_t* n_kept) {
   prof_begin(c, "swiglu_bwd");
-  swiglu_bwd_kernel<<<grid_rows(c, (long long)M * (F / 8), 256), 256, 0, c.stream>>>(ds, ds_is_bf16, F, gu, dgu,
-                                                                                     M, idx, n_kept, c.st);
+  swiglu_bwd_kernel<<<grid_rows(c, cap * (F / 8), 256), 256, 0, c.stream>>>(ds, ds_is_bf16, F, gu, dgu, M, cap,
+                                                                            idx, n_kept, c.st);
   prof_end(c);
   count_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_gelu_bwd(const Ctx& c, const void* df2, int df2_is_bf16, int F, const __nv_bfloat16* f1,
-                            __nv_bfloat16* df1, int M, const int32_t* idx, const int32_t* n_kept) {
+                            __nv_bfloat16* df1, int M, long long cap, const int32_t* idx, const int32_t* n_kept) {
   prof_begin(c, "gelu_bwd");
-  gelu_bwd_kernel<<<grid_rows(c, (long long)M * (F / 8), 256), 256, 0, c.stream>>>(df2, df2_is_bf16, F, f1, df1,
-                                                                                   M, idx, n_kept, c.st);
+  gelu_bwd_kernel<<<grid_rows(c, cap * (F / 8), 256), 256, 0, c.stream>>>(df2, df2_is_bf16, F, f1, df1, M, cap,
+                                                                          idx, n_kept, c.st);
   prof_end(c);
   count_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_ce_bwd(const Ctx& c, const __nv_bfloat16* logits, const int32_t* targets, int V, int M,
-                          const int32_t* idx, const int32_t* n_kept, __nv_bfloat16* dz) {
+                          long long cap, const int32_t* idx, const int32_t* n_kept, __nv_bfloat16* dz) {
   prof_begin(c, "ce_bwd");
-  ce_bwd_kernel<<<M, kCeThreads, 0, c.stream>>>(logits, targets, V, M, idx, n_kept, dz, c.st);
+  ce_bwd_kernel<<<(int)cap, kCeThreads, 0, c.stream>>>(logits, targets, V, M, cap, idx, n_kept, dz, c.st);
   prof_end(c);
   count_launch();
   return cudaGetLastError();
