@@ -113,6 +113,27 @@ collider_status collider_compact(const uint8_t* mask, int B, int T, int32_t* idx
                                  int32_t* cu_kept, int32_t* n_kept, void* ws,
                                  size_t ws_bytes, void* stream);
 
+/* Compaction that allocates nothing, for callers that cannot allocate device
+ * memory: programs whose device memory is handed out by their own pool
+ * allocator (a raw cudaMalloc would bypass it, or fail once the pool has
+ * reserved the device), and latency-critical paths, since cudaMalloc and
+ * cudaFree can synchronise the device.  The pages have no counterpart: this is
+ * an interface convenience, not part of the method.
+ * Same arguments and results as collider_compact (bit-identical), without the
+ * workspace.  Its scratch (one int per 16,384 tokens) is a fixed 256 KB array
+ * of device memory inside the library, held by every device that loads the
+ * library until the process exits; so B*T may be at most 1,073,741,824
+ * (2^30) tokens, and larger sizes return COLLIDER_ERR_INVALID_ARG.  All calls
+ * share that array: calls whose work can overlap on the GPU (different
+ * streams without ordering between them) race and must be serialised by the
+ * caller; calls on one stream are fine.  The first call on each device looks
+ * up the array's device address (cudaGetSymbolAddress, with that device
+ * current); make that first call before any stream capture.  Nothing is
+ * allocated, and no earlier call's contents need clearing: every entry a call
+ * reads is written by that call first. */
+collider_status collider_compact_noalloc(const uint8_t* mask, int B, int T, int32_t* idx,
+                                         int32_t* cu_kept, int32_t* n_kept, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* a2. Row gather / scatter (abstract: activations of filtered tokens are    */
 /*     filtered across all layers)                                           */

@@ -19,7 +19,7 @@ __all__ = [
     "LayerDesc", "LayerWeights", "LayerSaved", "LayerGrads", "EXPORTED",
     "collider_last_error", "collider_check", "collider_launch_count",
     "collider_profile_enable", "collider_profile_count", "collider_profile_get",
-    "collider_compact_workspace_size", "collider_compact", "collider_gather_rows",
+    "collider_compact_workspace_size", "collider_compact", "collider_compact_noalloc", "collider_gather_rows",
     "collider_scatter_rows", "collider_linear_workspace_size", "collider_linear_bwd",
     "collider_attn_workspace_size", "collider_attn_bwd", "collider_layer_workspace_size",
     "collider_layer_bwd", "collider_stack_workspace_size", "collider_stack_bwd",
@@ -76,6 +76,7 @@ _SIGS = {
     "collider_profile_get": (I, [I, C.POINTER(C.c_char_p), C.POINTER(C.c_longlong), C.POINTER(C.c_float)]),
     "collider_compact_workspace_size": (SZ, [I, I]),
     "collider_compact": (I, [P, I, I, P, P, P, P, SZ, P]),
+    "collider_compact_noalloc": (I, [P, I, I, P, P, P, P]),
     "collider_gather_rows": (I, [P, SZ, P, SZ, SZ, I, P, P, P]),
     "collider_scatter_rows": (I, [P, SZ, P, SZ, SZ, I, P, P, P]),
     "collider_linear_workspace_size": (SZ, [I, I, I, I]),
@@ -180,6 +181,13 @@ def collider_compact_workspace_size(B: int, T: int) -> int:
 def collider_compact(mask, B, T, idx, cu_kept, n_kept, ws=None, stream=None) -> None:
     _check(lib().collider_compact(_ptr(mask), B, T, _ptr(idx), _ptr(cu_kept), _ptr(n_kept), _ptr(ws),
                                   _nbytes(ws), _stream(stream)))
+
+
+def collider_compact_noalloc(mask, B, T, idx, cu_kept, n_kept, stream=None) -> None:
+    """collider_compact without a workspace and without any allocation (scratch
+    is a fixed array inside the library; B*T <= 2^30)."""
+    _check(lib().collider_compact_noalloc(_ptr(mask), B, T, _ptr(idx), _ptr(cu_kept), _ptr(n_kept),
+                                          _stream(stream)))
 
 
 def collider_gather_rows(src, src_ld_bytes, dst, dst_ld_bytes, row_bytes, M, idx, n_kept, stream=None) -> None:

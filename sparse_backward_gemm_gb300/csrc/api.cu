@@ -122,6 +122,8 @@ struct Carver {
 
 void count_launch(int n) { g_launches += n; }
 
+void set_last_error(const char* msg) { g_msg = msg; }
+
 void prof_begin(const Ctx& c, const char* name, long long m, long long n, long long k, int dyn) {
   if (!g_prof_on) return;
   ProfRec r{name, m, n, k, dyn, next_event(), next_event()};

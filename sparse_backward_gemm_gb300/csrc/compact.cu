@@ -171,3 +171,76 @@ cudaError_t launch_compact(const Ctx& c, const uint8_t* mask, int B, int T, int3
 }
 
 }  // namespace collider
+
+// ===========================================================================
+// collider_compact_noalloc: the same compaction for callers that cannot
+// allocate device memory (see include/collider.h).  It always takes the
+// three-kernel path, with the per-chunk counts in a fixed array of device
+// memory that belongs to this library and lives as long as the process.
+// ===========================================================================
+#include <mutex>
+
+#include "../../include/collider.h"
+
+namespace collider {
+namespace {
+
+// One int per 16,384-token chunk: 65,536 chunks cover 2^30 tokens.  256 KB,
+// held by every device that loads the library, until the process exits.
+constexpr long long kNoAllocMaxChunks = 65536;
+constexpr long long kNoAllocMaxTokens = kNoAllocMaxChunks * kChunk;
+static __device__ __align__(256) int g_noalloc_counts[kNoAllocMaxChunks];
+
+std::mutex g_noalloc_mu;
+int* g_noalloc_addr[64] = {nullptr};   // device address of g_noalloc_counts, per device
+
+collider_status noalloc_fail(collider_status s, const char* m) {
+  set_last_error(m);
+  return s;
+}
+
+}  // namespace
+}  // namespace collider
+
+extern "C" collider_status collider_compact_noalloc(const uint8_t* mask, int B, int T, int32_t* idx,
+                                                    int32_t* cu_kept, int32_t* n_kept, void* stream) {
+  using namespace collider;
+  if (!mask || !idx || !cu_kept || !n_kept)
+    return noalloc_fail(COLLIDER_ERR_INVALID_ARG, "collider_compact_noalloc: null pointer");
+  if (B < 1 || T < 1)
+    return noalloc_fail(COLLIDER_ERR_INVALID_ARG, "collider_compact_noalloc: need B >= 1 and T >= 1");
+  const long long M = (long long)B * T;
+  if (M > kNoAllocMaxTokens)
+    return noalloc_fail(COLLIDER_ERR_INVALID_ARG,
+                        "collider_compact_noalloc: B*T exceeds its fixed limit of 1073741824 tokens "
+                        "(use collider_compact with a workspace)");
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    return noalloc_fail(COLLIDER_ERR_CUDA, "collider_compact_noalloc: no current CUDA device");
+  if (cudaGetLastError() != cudaSuccess)
+    return noalloc_fail(COLLIDER_ERR_CUDA, "collider_compact_noalloc: earlier asynchronous CUDA error");
+  int* counts = nullptr;
+  {
+    // first call on this device: look up the device address of the array
+    // (host code cannot use the array's name as a device pointer)
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_counts) != cudaSuccess || !p)
+        return noalloc_fail(COLLIDER_ERR_CUDA, "collider_compact_noalloc: cudaGetSymbolAddress failed");
+      g_noalloc_addr[dev] = static_cast<int*>(p);
+    }
+    counts = g_noalloc_addr[dev];
+  }
+  // every entry read below is written by compact_count first, so nothing
+  // left over from an earlier call needs clearing
+  const int nchunks = (int)((M + kChunk - 1) / kChunk);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  compact_count<<<nchunks, kThreads, 0, s>>>(mask, M, counts);
+  compact_scan<<<1, kThreads, 0, s>>>(counts, nchunks, B, cu_kept, n_kept);
+  compact_write<<<nchunks, kThreads, 0, s>>>(mask, B, T, counts, idx, cu_kept);
+  count_launch(3);
+  if (cudaGetLastError() != cudaSuccess)
+    return noalloc_fail(COLLIDER_ERR_CUDA, "collider_compact_noalloc: kernel launch failed");
+  return COLLIDER_OK;
+}

@@ -18,6 +18,8 @@ struct Ctx {
 
 // Launch accounting (per host thread) and optional per-kernel event timing.
 void count_launch(int n = 1);
+// Message returned by collider_last_error() on this host thread.
+void set_last_error(const char* msg);
 // Kernel timing hooks used by the profiler: bracket a launch with events when
 // profiling is on.  `name` must be a string literal; m, n, k, dyn describe a
 // GEMM launch (dyn: which extent is the device-resident kept count).
