@@ -311,6 +311,7 @@ def run_ours(args):
     cl.collider_profile_enable(0)
     per = {}
     gemm_ms, gemm_fl = 0.0, 0.0
+    gemm_shapes = {}
     for i in range(cl.collider_profile_count()):
         name, (m, n, k, dyn), ms = cl.collider_profile_get(i)
         d = per.setdefault(name, [0, 0.0])
@@ -321,6 +322,9 @@ def run_ours(args):
             kk = n_kept if dyn == 2 else k
             gemm_ms += ms
             gemm_fl += 2.0 * mm * n * kk
+            key = f"{mm}x{n}x{kk}" + ("" if dyn != 2 else " (dW)")
+            e = gemm_shapes.setdefault(key, [0.0, 2.0 * mm * n * kk])
+            e[0] += ms / args.steps
     peaks, src = measured_peaks()
     achieved = gemm_fl / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else 0.0
     step_ms_prof = sum(v[1] for v in per.values()) / args.steps
@@ -381,6 +385,8 @@ def run_ours(args):
                          "traffic": None, "gemm_ms_per_step": gemm_ms / args.steps,
                          "step_ms_profiled": step_ms_prof},
             "kernels_ms_per_step": {k: round(v[1] / args.steps, 4) for k, v in sorted(per.items())},
+            "gemms": {k: {"ms": round(v[0], 4), "tflops": round(v[1] / (v[0] * 1e-3) / 1e12, 1)}
+                      for k, v in gemm_shapes.items()},
             "gpu_launches": launches,
             "clocks": clocks,
             "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,

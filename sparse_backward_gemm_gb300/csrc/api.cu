@@ -259,6 +259,9 @@ extern "C" collider_status collider_scatter_rows(const void* compact, size_t com
 // a3/a4 linear backward
 // ===========================================================================
 namespace {
+// stream-K per-tile counters for GEMMs with row extents <= m and columns <= n
+long long sk_counter_cap(long long m, long long n) { return ((m + 127) / 128) * ((n + 127) / 128); }
+
 size_t linear_carve(Carver& cv, collider_dtype dt, int M, int K, int N, bool x_full, bool dy_full, bool dx_full,
                     void** xk, void** dyk, void** dxk, float** part) {
   const long long Mp = pad128(M);
@@ -272,6 +275,10 @@ size_t linear_carve(Carver& cv, collider_dtype dt, int M, int K, int N, bool x_f
     if (dx_full) *dxk = cv.take<__nv_bfloat16>((size_t)Mp * K);
   }
   *part = cv.take<float>(colsum_part_floats(M, N));
+  if (dt == COLLIDER_BF16) {
+    cv.take<float>(kSkPartialFloats);
+    cv.take<int>(sk_counter_cap(std::max<long long>(M, K), std::max(K, N)));
+  }
   return cv.used;
 }
 }  // namespace
@@ -318,6 +325,15 @@ extern "C" collider_status collider_linear_bwd(collider_dtype dtype, int M, int 
   collider_status s = make_ctx(stream, &c);
   if (s != COLLIDER_OK) return s;
   if (M == 0) return COLLIDER_OK;
+  float* sk_partial = nullptr;
+  int* sk_counters = nullptr;
+  const long long sk_cap = sk_counter_cap(std::max<long long>(M, K), std::max(K, N));
+  if (dtype == COLLIDER_BF16) {
+    // the stream-K scratch sits at the end of the carve (see linear_carve)
+    sk_counters = reinterpret_cast<int*>(static_cast<char*>(ws) + need - up256(sk_cap * sizeof(int)));
+    sk_partial = reinterpret_cast<float*>(reinterpret_cast<char*>(sk_counters) - up256(kSkPartialFloats * 4));
+    CK(cudaMemsetAsync(sk_counters, 0, sk_cap * sizeof(int), c.stream));
+  }
 
   if (dtype == COLLIDER_F32) {
     const float* Xf = static_cast<const float*>(X);
@@ -367,6 +383,7 @@ extern "C" collider_status collider_linear_bwd(collider_dtype dtype, int M, int 
     g.B = W; g.ldb = N; g.b_mn_major = 0; g.b_rows = K;
     g.C = dx_full ? dxk : dX; g.ldc = K; g.c_bf16 = 1; g.zero_pad = 1; g.c_rows = dx_full ? pad128(M) : M;
     g.n_kept = n_kept; g.dyn = 1;
+    g.partial = sk_partial; g.counters = sk_counters; g.counter_cap = sk_cap;
     CK(launch_tc_gemm(c, g));
     if (dx_full) CK(launch_scatter(c, static_cast<const char*>(dxk), (long long)K * 2, static_cast<char*>(dX),
                                    (long long)K * 2, K * 2, M, idx, n_kept));
@@ -378,6 +395,7 @@ extern "C" collider_status collider_linear_bwd(collider_dtype dtype, int M, int 
     g.B = dYk; g.ldb = N; g.b_mn_major = 1; g.b_rows = M;
     g.C = dW; g.ldc = N; g.c_bf16 = 0;
     g.n_kept = n_kept; g.dyn = 2;
+    g.partial = sk_partial; g.counters = sk_counters; g.counter_cap = sk_cap;
     CK(launch_tc_gemm(c, g));
   }
   if (db) CK(launch_colsum(c, dYk, 1, N, M, N, nullptr, n_kept, part, db));
@@ -390,13 +408,17 @@ extern "C" collider_status collider_linear_bwd(collider_dtype dtype, int M, int 
 namespace {
 struct AttnScratch {
   float* dq_acc;
+  float* dk_acc;
+  float* dv_acc;
   float* Dvec;
   float* lse2;
   float2* rope;
 };
-void attn_carve(Carver& cv, int B, int T, int H, int dh, AttnScratch* a) {
+void attn_carve(Carver& cv, int B, int T, int H, int Hkv, int dh, AttnScratch* a) {
   const size_t M = (size_t)B * T;
   a->dq_acc = cv.take<float>(M * H * dh);
+  a->dk_acc = cv.take<float>(M * Hkv * dh);
+  a->dv_acc = cv.take<float>(M * Hkv * dh);
   a->Dvec = cv.take<float>(M * H);
   a->lse2 = cv.take<float>(M * H);
   a->rope = cv.take<float2>((size_t)T * (dh / 2));
@@ -407,7 +429,7 @@ extern "C" size_t collider_attn_workspace_size(int B, int T, int H, int Hkv, int
   if (B < 1 || T < 1 || H < 1 || Hkv < 1 || dh < 1) return 0;
   Carver cv{nullptr, 0, 0, true};
   AttnScratch a;
-  attn_carve(cv, B, T, H, dh, &a);
+  attn_carve(cv, B, T, H, Hkv, dh, &a);
   const size_t Mp = pad128((long long)B * T);
   cv.take<__nv_bfloat16>(Mp * H * dh * 2);          // compact Q, dO (FULL inputs)
   cv.take<__nv_bfloat16>(Mp * Hkv * dh * 2);        // compact K, V
@@ -444,7 +466,7 @@ extern "C" collider_status collider_attn_bwd(int B, int T, int H, int Hkv, int d
   const long long Mp = pad128(M);
   Carver cv{static_cast<char*>(ws), ws_bytes, 0, false};
   AttnScratch sc;
-  attn_carve(cv, B, T, H, dh, &sc);
+  attn_carve(cv, B, T, H, Hkv, dh, &sc);
   auto* cq = cv.take<__nv_bfloat16>((size_t)Mp * H * dh);
   auto* cdo = cv.take<__nv_bfloat16>((size_t)Mp * H * dh);
   auto* ck = cv.take<__nv_bfloat16>((size_t)Mp * Hkv * dh);
@@ -458,6 +480,8 @@ extern "C" collider_status collider_attn_bwd(int B, int T, int H, int Hkv, int d
   a.rotary_dim = rotary_dim; a.rope_base = rope_base;
   a.lse = lse; a.idx = idx; a.cu_kept = cu_kept; a.n_kept = n_kept;
   a.dq_acc = sc.dq_acc; a.Dvec = sc.Dvec; a.lse_k = sc.lse2; a.rope = sc.rope; a.M = M;
+  a.dk_acc = sc.dk_acc; a.dv_acc = sc.dv_acc;
+  a.in_cap = in_rows == COLLIDER_ROWS_FULL ? Mp : M;
   a.cap = out_rows == COLLIDER_ROWS_FULL ? Mp : M;
   if (in_rows == COLLIDER_ROWS_FULL) {
     GatherJob j[4] = {
@@ -510,6 +534,9 @@ struct LayerBufs {
   float *db_k, *da_k;
   float* norm_part;
   float* col_part;
+  float* sk_partial;
+  int* sk_counters;
+  long long sk_cap;
   AttnScratch at;
 };
 
@@ -555,13 +582,23 @@ void layer_carve(Carver& cv, const collider_layer_desc* d, LayerBufs* L) {
   L->norm_part = cv.take<float>(norm_part_floats((int)Mp, (int)D));
   size_t cp = colsum_part_floats((int)Mp, (int)std::max(Nqkv, std::max(Nup, D)));
   L->col_part = cv.take<float>(cp);
-  attn_carve(cv, d->B, d->T, d->H, d->dh, &L->at);
+  attn_carve(cv, d->B, d->T, d->H, d->Hkv, d->dh, &L->at);
+  L->sk_partial = cv.take<float>(kSkPartialFloats);
+  const long long mmax = std::max<long long>((long long)Mp, std::max(D, F));
+  L->sk_cap = sk_counter_cap(mmax, std::max<long long>(std::max(Nqkv, Nup), std::max(D, F)));
+  L->sk_counters = cv.take<int>(L->sk_cap);
 }
+
+// stream-K scratch shared by the GEMMs of one call (they run in stream order)
+thread_local float* g_sk_partial = nullptr;
+thread_local int* g_sk_counters = nullptr;
+thread_local long long g_sk_cap = 0;
 
 // C (bf16 or f32, COMPACT [Mk, N]) = A_k [Mk, K] . W^T with W stored [N, K]
 cudaError_t gemm_dx(const Ctx& c, int M, int N, int K, const void* A, const void* W, void* C, int c_bf16,
                     int accumulate, const int32_t* n_kept) {
   TcGemm g{};
+  g.partial = g_sk_partial; g.counters = g_sk_counters; g.counter_cap = g_sk_cap;
   g.M = M; g.N = N; g.K = K;
   g.A = A; g.lda = K; g.a_mn_major = 0; g.a_rows = pad128(M);
   g.B = W; g.ldb = K; g.b_mn_major = 0; g.b_rows = N;
@@ -574,6 +611,7 @@ cudaError_t gemm_dx(const Ctx& c, int M, int N, int K, const void* A, const void
 cudaError_t gemm_dw(const Ctx& c, int M, int Kin, int Nout, const void* Xk, long long ldx, const void* dYk,
                     long long ldy, float* dW, const int32_t* n_kept) {
   TcGemm g{};
+  g.partial = g_sk_partial; g.counters = g_sk_counters; g.counter_cap = g_sk_cap;
   g.M = Kin; g.N = Nout; g.K = M;
   g.A = Xk; g.lda = ldx; g.a_mn_major = 1; g.a_rows = pad128(M);
   g.B = dYk; g.ldb = ldy; g.b_mn_major = 1; g.b_rows = pad128(M);
@@ -591,6 +629,10 @@ collider_status layer_bwd_impl(const Ctx& c, const collider_layer_desc* d, const
   const int Hd = H * dh, Nqkv = (H + 2 * Hkv) * dh;
   const bool llama = d->arch == COLLIDER_ARCH_LLAMA;
   const int Nup = llama ? 2 * F : F;
+  g_sk_partial = L.sk_partial;
+  g_sk_counters = L.sk_counters;
+  g_sk_cap = L.sk_cap;
+  CK(cudaMemsetAsync(L.sk_counters, 0, L.sk_cap * sizeof(int), c.stream));
 
   // 1. gather the kept rows of dOut and of the saved GEMM operands
   {
@@ -668,6 +710,7 @@ collider_status layer_bwd_impl(const Ctx& c, const collider_layer_desc* d, const
     a.dq = L.dqkv_k; a.dk = L.dqkv_k + Hd; a.dv = L.dqkv_k + Hd + Hkv * dh;
     a.dq_ld = Nqkv; a.dkv_ld = Nqkv;
     a.dq_acc = L.at.dq_acc; a.Dvec = L.at.Dvec; a.lse_k = L.at.lse2; a.rope = L.at.rope; a.M = M;
+    a.dk_acc = L.at.dk_acc; a.dv_acc = L.at.dv_acc; a.in_cap = pad128(M);
     a.cap = pad128(M);
     CK(launch_attn_bwd(c, a));
   }
@@ -817,6 +860,10 @@ extern "C" collider_status collider_stack_bwd(const collider_layer_desc* d, int 
   LayerBufs LB;
   layer_carve(cv, d, &LB);
   const int M = d->B * d->T, D = d->D;
+  g_sk_partial = LB.sk_partial;
+  g_sk_counters = LB.sk_counters;
+  g_sk_cap = LB.sk_cap;
+  CK(cudaMemsetAsync(LB.sk_counters, 0, LB.sk_cap * sizeof(int), c.stream));
 
   // LM head: dz = (softmax(z) - onehot) / n_kept on kept rows
   CK(launch_ce_bwd(c, static_cast<const __nv_bfloat16*>(logits), targets, V, M, pad128(M), idx, n_kept, S.dz_k));

@@ -17,6 +17,7 @@
 // backward, bf16, zero padding rows).  Tensor-core math is mma.sync
 // m16n8k16 bf16 with f32 accumulation.
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace collider {
 
@@ -85,6 +86,9 @@ struct AttnK {
   __nv_bfloat16 *dq, *dk, *dv;
   long long dq_ld, dkv_ld;
   float* dq_acc;     // [M, H, DH]
+  float* dk_acc;     // [M, Hkv, DH]  (tcgen05 path: dK, dV reduced here, then finalized)
+  float* dv_acc;
+  int kv_acc;        // 1: dK / dV come from dk_acc / dv_acc
   float* Dvec;       // [H, M]
   float* lse2;       // [H, M]  lse * log2(e), kept order
   const float2* rope;  // [T, rot_half] (cos, sin)
@@ -108,6 +112,15 @@ __global__ void attn_prep_kernel(AttnK p, int DH, float rope_base, float2* rope)
   const long long nacc = (long long)nk * p.H * DH / 4;
   float4* acc4 = reinterpret_cast<float4*>(p.dq_acc);
   for (long long e = tid; e < nacc; e += stride) acc4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (p.kv_acc) {
+    const long long nkv = (long long)nk * p.Hkv * DH / 4;
+    float4* k4 = reinterpret_cast<float4*>(p.dk_acc);
+    float4* v4 = reinterpret_cast<float4*>(p.dv_acc);
+    for (long long e = tid; e < nkv; e += stride) {
+      k4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+      v4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
   if (p.rot_half > 0) {
     const int rd = 2 * p.rot_half;
     for (long long e = tid; e < (long long)p.T * p.rot_half; e += stride) {
@@ -437,44 +450,54 @@ __global__ void __launch_bounds__(128) attn_main_kernel(AttnK p) {
 }
 
 // ---------------------------------------------------------------------------
-// finalize: dQ = scale * acc, RoPE backward, bf16; zero rows n_kept..pad of dQ, dK, dV
+// finalize: gradients from the f32 accumulators, times `scale`, RoPE backward
+// where asked, to bf16; zero rows n_kept..pad of dQ, dK, dV.
+// One thread per (row, head, column pair): the rotary pair (i, i + r/2) for
+// i < r/2, else two adjacent pass-through columns.
+__device__ __forceinline__ void finalize_pair(const float* a, __nv_bfloat16* o, int c, int DH, int rh,
+                                              const float2* rope_row, float scale) {
+  const int per_head = DH / 2;
+  if (rh == 0) {
+    o[c] = f2bf(a[c] * scale);
+    o[c + per_head] = f2bf(a[c + per_head] * scale);
+  } else if (c < rh) {
+    const float2 cs = rope_row[c];
+    const float d1 = a[c] * scale, d2 = a[c + rh] * scale;
+    o[c] = f2bf(d1 * cs.x + d2 * cs.y);
+    o[c + rh] = f2bf(d2 * cs.x - d1 * cs.y);
+  } else {
+    const int cc = 2 * rh + 2 * (c - rh);
+    if (cc < DH) {
+      o[cc] = f2bf(a[cc] * scale);
+      o[cc + 1] = f2bf(a[cc + 1] * scale);
+    }
+  }
+}
+
 __global__ void attn_finalize_kernel(AttnK p, int DH) {
   const int nk = *p.n_kept;
   const int pad = padded_rows(nk, p.cap);
   const int rh = p.rot_half;
   const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   const long long stride = (long long)gridDim.x * blockDim.x;
-  // one thread per (row, head, column pair (c, c+half) or single column beyond the rotary dims)
-  const int per_head = DH / 2;   // each thread handles columns c and c + DH/2
-  const long long total = (long long)nk * p.H * per_head;
-  for (long long e = tid; e < total; e += stride) {
-    const int c = (int)(e % per_head);
-    const int h = (int)((e / per_head) % p.H);
-    const int r = (int)(e / ((long long)per_head * p.H));
-    const float* a = p.dq_acc + ((long long)r * p.H + h) * DH;
-    __nv_bfloat16* o = p.dq + (long long)r * p.dq_ld + h * DH;
-    // handle the pair (c, c + DH/2) when RoPE is off or for the pass-through
-    // dims; with RoPE pair (i, i + rh) for i < rh
-    if (rh == 0) {
-      o[c] = f2bf(a[c] * p.scale);
-      o[c + per_head] = f2bf(a[c + per_head] * p.scale);
-    } else {
-      // map thread c in [0, DH/2) to: rotary pair i = c if c < rh, else two
-      // pass-through columns starting at 2*rh + 2*(c - rh)
-      if (c < rh) {
-        const int pos = p.idx[r] % p.T;
-        const float2 cs = p.rope[(long long)pos * rh + c];
-        const float d1 = a[c] * p.scale, d2 = a[c + rh] * p.scale;
-        o[c] = f2bf(d1 * cs.x + d2 * cs.y);
-        o[c + rh] = f2bf(d2 * cs.x - d1 * cs.y);
-      } else {
-        const int cc = 2 * rh + 2 * (c - rh);
-        if (cc < DH) {
-          o[cc] = f2bf(a[cc] * p.scale);
-          o[cc + 1] = f2bf(a[cc + 1] * p.scale);
-        }
-      }
-    }
+  const int per_head = DH / 2;
+  const long long tq = (long long)nk * p.H * per_head;
+  const long long tk = p.kv_acc ? (long long)nk * p.Hkv * per_head : 0;
+  for (long long e = tid; e < tq + 2 * tk; e += stride) {
+    long long f = e;
+    int which = 0;   // 0 dQ, 1 dK, 2 dV
+    if (f >= tq) { f -= tq; which = 1 + (int)(f / tk); f %= tk; }
+    const int nh = which == 0 ? p.H : p.Hkv;
+    const int c = (int)(f % per_head);
+    const int h = (int)((f / per_head) % nh);
+    const int r = (int)(f / ((long long)per_head * nh));
+    const float* acc = which == 0 ? p.dq_acc : (which == 1 ? p.dk_acc : p.dv_acc);
+    const float* a = acc + ((long long)r * nh + h) * DH;
+    __nv_bfloat16* o = which == 0 ? p.dq + (long long)r * p.dq_ld + h * DH
+                                  : (which == 1 ? p.dk : p.dv) + (long long)r * p.dkv_ld + h * DH;
+    const int use_rh = which == 2 ? 0 : rh;
+    const float2* rope_row = use_rh ? p.rope + (long long)(p.idx[r] % p.T) * rh : nullptr;
+    finalize_pair(a, o, c, DH, use_rh, rope_row, which == 2 ? 1.f : p.scale);
   }
   // zero padding rows
   const long long zq = (long long)(pad - nk) * p.H * DH, zk = (long long)(pad - nk) * p.Hkv * DH;
@@ -491,12 +514,544 @@ __global__ void attn_finalize_kernel(AttnK p, int DH) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// tcgen05 main pass, head dim 64.  One CTA per work item (sequence, kv head,
+// 128 keys, a chunk of hc query heads of the group); items are numbered key
+// block first, so the heavy (early) key blocks start first.
+//   warp 0      TMA: K, V once; Q_i, dO_i per iteration (2 stages)
+//   warp 1      TMEM owner; one lane issues the MMAs:
+//                 S^T = K Q^T, dP^T = V dO^T           (M 128 keys, N 128 queries)
+//                 dV += P^T dO, dK += dS^T Q           (M 128 keys, N 64)
+//                 dQ  = dS K                           (M 128 queries, N 64)
+//   warps 2-5   one key row per thread: P^T, dS^T from TMEM -> bf16 -> shared
+//   warps 6-9   one query row per thread: dQ from TMEM -> shared -> TMA
+//               reduce-add into the f32 dQ accumulator; at the end dK, dV
+//               likewise into their accumulators
+// TMEM columns: S^T 0-127, dP^T 128-255, dV 256-319, dK 320-383, dQ 384-447.
+namespace tcattn {
+constexpr int kQ = 128, kK = 128, kD = 64;
+constexpr uint32_t kTile = kQ * kD * 2;                 // 16 KB: 128 rows x 128 bytes
+constexpr uint32_t OFF_K = 0, OFF_V = kTile, OFF_Q = 2 * kTile, OFF_DO = 4 * kTile, OFF_P = 6 * kTile,
+                   OFF_DS = 8 * kTile, OFF_ST = 10 * kTile, OFF_LD = 12 * kTile, OFF_BAR = 12 * kTile + 2048;
+constexpr size_t kSmem = 1024 + OFF_BAR + 256;
+constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 320, TM_DQ = 384;
+constexpr int kThreads = 320;
+}  // namespace tcattn
+
+struct MainTc {
+  int B, T, H, Hkv, G, hc, nhc, nkb, causal;
+  float scale_log2;
+  const int32_t* cu_kept;
+  const float* lse2;
+  const float* Dvec;
+  long long M;
+  DevStatus* st;
+};
+
+__global__ void __launch_bounds__(tcattn::kThreads, 1)
+    attn_main_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                        const __grid_constant__ CUtensorMap tmdQ, const __grid_constant__ CUtensorMap tmdK,
+                        const __grid_constant__ CUtensorMap tmdV, MainTc p) {
+  using namespace tc;
+  using namespace tcattn;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int per_j = p.B * p.Hkv * p.nhc;
+  const int j = blockIdx.x / per_j;
+  const int rem = blockIdx.x % per_j;
+  const int b = rem / (p.Hkv * p.nhc);
+  const int hk = (rem / p.nhc) % p.Hkv;
+  const int hci = rem % p.nhc;
+  const int s0 = p.cu_kept[b], len = p.cu_kept[b + 1] - s0;
+  const int j0 = j * kK;
+  if (j0 >= len) return;   // uniform: nothing initialised yet
+  const int nqb = (len + kQ - 1) / kQ;
+  const int i_start = p.causal ? j : 0;
+  const int nq_head = nqb - i_start;
+  const int n_iter = p.hc * nq_head;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  const uint32_t b_kv = smem_u32(bars + 0), b_qfull = smem_u32(bars + 1), b_qempty = smem_u32(bars + 3),
+                 b_sfull = smem_u32(bars + 5), b_pfull = smem_u32(bars + 6), b_pempty = smem_u32(bars + 7),
+                 b_dqfull = smem_u32(bars + 8), b_dqempty = smem_u32(bars + 9), b_kvready = smem_u32(bars + 10),
+                 b_qready = smem_u32(bars + 11);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* sL = reinterpret_cast<float*>(sm + OFF_LD);   // [2][128]
+  float* sD = sL + 256;                                // [2][128]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(b_kv, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(b_qfull + 8 * s, 1);
+      mbar_init(b_qempty + 8 * s, 1);
+    }
+    mbar_init(b_sfull, 1);
+    mbar_init(b_pfull, 128);
+    mbar_init(b_pempty, 1);
+    mbar_init(b_dqfull, 1);
+    mbar_init(b_dqempty, 128);
+    mbar_init(b_kvready, 1);
+    mbar_init(b_qready, 1);
+    mbar_init(b_qready + 8, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint32_t sbase = smem_u32(sm);
+  // The consumer groups below synchronise with named barriers, so they must
+  // leave together: their waits give up only on their own timeout, which every
+  // thread of the group reaches on the same barrier phase.
+  volatile int no_abort = 0;
+
+  if (warp == 0) {
+    // ---------------- TMA producer (lane 0) + tile finishing (whole warp) ----------------
+    // A tile may reach past its sequence into rows that hold anything; rows
+    // past the sequence are zeroed in shared memory before the MMAs see the
+    // tile (a masked probability of 0 times a non-finite row would leak).
+    auto zero_rows = [&](uint32_t off, int from) {
+      for (int i = lane; i < (128 - from) * 8; i += 32)
+        *reinterpret_cast<uint4*>(sm + off + (from + i / 8) * 128 + (i % 8) * 16) = make_uint4(0, 0, 0, 0);
+    };
+    auto issue = [&](int it) -> bool {
+      const int st = it & 1, use = it >> 1;
+      if (!mbar_wait(b_qempty + 8 * st, (use & 1) ^ 1, abort_flag, p.st, 20)) return false;
+      const int h = hk * p.G + hci * p.hc + it / nq_head;
+      const int i0 = (i_start + it % nq_head) * kQ;
+      mbar_expect_tx(b_qfull + 8 * st, 2 * kTile);
+      tma_load_2d(sbase + OFF_Q + st * kTile, &tmQ, b_qfull + 8 * st, h * kD, s0 + i0);
+      tma_load_2d(sbase + OFF_DO + st * kTile, &tmdO, b_qfull + 8 * st, h * kD, s0 + i0);
+      return true;
+    };
+    const int krows = min(kK, len - j0);
+    bool ok = true;
+    if (lane == 0) {
+      mbar_expect_tx(b_kv, 2 * kTile);
+      tma_load_2d(sbase + OFF_K, &tmK, b_kv, hk * kD, s0 + j0);
+      tma_load_2d(sbase + OFF_V, &tmV, b_kv, hk * kD, s0 + j0);
+    }
+    if (mbar_wait(b_kv, 0, &no_abort, p.st, 28)) {
+      if (krows < kK) {
+        zero_rows(OFF_K, krows);
+        zero_rows(OFF_V, krows);
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_kvready);
+    } else {
+      ok = false;
+    }
+    if (lane == 0 && ok && n_iter > 0) ok = issue(0);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    for (int it = 0; ok && it < n_iter; ++it) {
+      const int st = it & 1, use = it >> 1;
+      int nxt = 1;
+      if (lane == 0 && it + 1 < n_iter) nxt = issue(it + 1) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, nxt, 0)) break;
+      if (!mbar_wait(b_qfull + 8 * st, use & 1, &no_abort, p.st, 29)) break;
+      const int i0 = (i_start + it % nq_head) * kQ;
+      const int qrows = min(kQ, len - i0);
+      if (qrows < kQ) {
+        zero_rows(OFF_Q + st * kTile, qrows);
+        zero_rows(OFF_DO + st * kTile, qrows);
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_qready + 8 * st);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t id_kv = idesc_bf16(128, 64, false, true);
+      constexpr uint32_t id_q = idesc_bf16(128, 64, true, true);
+      bool ok = mbar_wait(b_kvready, 0, abort_flag, p.st, 21);
+      for (int it = 0; ok && it < n_iter; ++it) {
+        const int st = it & 1, use = it >> 1;
+        if (!mbar_wait(b_qready + 8 * st, use & 1, abort_flag, p.st, 22)) break;
+        fence_after();
+        const uint32_t sq = sbase + OFF_Q + st * kTile, sdo = sbase + OFF_DO + st * kTile;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_bf16(tbase + TM_S, sdesc(sbase + OFF_K + kk * 32, 16, 1024), sdesc(sq + kk * 32, 16, 1024), id_s,
+                   kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_bf16(tbase + TM_DP, sdesc(sbase + OFF_V + kk * 32, 16, 1024), sdesc(sdo + kk * 32, 16, 1024), id_s,
+                   kk > 0);
+        mma_commit(b_sfull);
+        if (!mbar_wait(b_pfull, it & 1, abort_flag, p.st, 23)) break;
+        if (it > 0 && !mbar_wait(b_dqempty, (it - 1) & 1, abort_flag, p.st, 24)) break;
+        fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kQ / 16; ++kk) {   // k = queries
+          const uint32_t pa = sbase + OFF_P + (kk >> 2) * kTile + (kk & 3) * 32;
+          mma_bf16(tbase + TM_DV, sdesc(pa, 16, 1024), sdesc(sdo + kk * 2048, 8192, 1024), id_kv,
+                   (it > 0) || (kk > 0));
+        }
+#pragma unroll
+        for (int kk = 0; kk < kQ / 16; ++kk) {
+          const uint32_t da = sbase + OFF_DS + (kk >> 2) * kTile + (kk & 3) * 32;
+          mma_bf16(tbase + TM_DK, sdesc(da, 16, 1024), sdesc(sq + kk * 2048, 8192, 1024), id_kv,
+                   (it > 0) || (kk > 0));
+        }
+#pragma unroll
+        for (int kk = 0; kk < kK / 16; ++kk)     // k = keys; dS read MN-major from the dS^T tile
+          mma_bf16(tbase + TM_DQ, sdesc(sbase + OFF_DS + kk * 2048, kTile, 1024),
+                   sdesc(sbase + OFF_K + kk * 2048, 8192, 1024), id_q, kk > 0);
+        mma_commit(b_dqfull);
+        mma_commit(b_qempty + 8 * st);
+        mma_commit(b_pempty);
+      }
+    }
+  } else if (warp < 6) {
+    // ---------------- softmax warps: one key row per thread ----------------
+    const int t = threadIdx.x - 64;
+    const int q = warp & 3;
+    const int kr = q * 32 + lane;
+    const int key = j0 + kr;
+    const bool kvalid = key < len;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    for (int it = 0; it < n_iter; ++it) {
+      const int h = hk * p.G + hci * p.hc + it / nq_head;
+      const int i0 = (i_start + it % nq_head) * kQ;
+      const int qrows = min(kQ, len - i0);
+      const int buf = it & 1;
+      sL[buf * 128 + t] = (t < qrows) ? p.lse2[(long long)h * p.M + s0 + i0 + t] : 0.f;
+      sD[buf * 128 + t] = (t < qrows) ? p.Dvec[(long long)h * p.M + s0 + i0 + t] : 0.f;
+      named_bar(1, 128);
+      if (!mbar_wait(b_sfull, it & 1, &no_abort, p.st, 25)) break;
+      if (it > 0 && !mbar_wait(b_pempty, (it - 1) & 1, &no_abort, p.st, 26)) break;
+      fence_after();
+      const float* L = sL + buf * 128;
+      const float* Dd = sD + buf * 128;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float sv[32], dv[32];
+        tmem_ld32(tbase + lane_off + TM_S + c * 32, sv);
+        tmem_ld32(tbase + lane_off + TM_DP + c * 32, dv);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int qi = c * 32 + e;
+          const bool valid = kvalid && qi < qrows && (!p.causal || key <= i0 + qi);
+          const float pv = valid ? exp2f(sv[e] * p.scale_log2 - L[qi]) : 0.f;
+          sv[e] = pv;
+          dv[e] = valid ? pv * (dv[e] - Dd[qi]) : 0.f;
+        }
+        const uint32_t sub = (c >> 1) * kTile + kr * 128;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const uint32_t phys = ((((c & 1) * 4 + g) ^ (kr & 7)) * 16);
+          *reinterpret_cast<uint4*>(sm + OFF_P + sub + phys) = pack8(sv + 8 * g);
+          *reinterpret_cast<uint4*>(sm + OFF_DS + sub + phys) = pack8(dv + 8 * g);
+        }
+      }
+      fence_before();
+      fence_async_smem();
+      mbar_arrive(b_pfull);
+    }
+  } else {
+    // ---------------- dQ / dK / dV epilogue: one row per thread ----------------
+    const int t = threadIdx.x - 192;
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t stage = sbase + OFF_ST;
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int h = hk * p.G + hci * p.hc + it / nq_head;
+      const int i0 = (i_start + it % nq_head) * kQ;
+      if (!mbar_wait(b_dqfull, it & 1, &no_abort, p.st, 27)) { ok = false; break; }
+      fence_after();
+      float v[64];
+      tmem_ld32(tbase + lane_off + TM_DQ, v);
+      tmem_ld32(tbase + lane_off + TM_DQ + 32, v + 32);
+      fence_before();
+      mbar_arrive(b_dqempty);
+      if (t == 0) bulk_wait_read_all();
+      named_bar(2, 128);
+#pragma unroll
+      for (int half = 0; half < 2; ++half)
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const uint32_t phys = ((g ^ (r & 7)) * 16);
+          *reinterpret_cast<float4*>(sm + OFF_ST + half * kTile + r * 128 + phys) =
+              make_float4(v[half * 32 + 4 * g], v[half * 32 + 4 * g + 1], v[half * 32 + 4 * g + 2],
+                          v[half * 32 + 4 * g + 3]);
+        }
+      fence_async_smem();
+      named_bar(2, 128);
+      if (t == 0) {
+        tma_reduce_add_2d(&tmdQ, stage, h * kD, s0 + i0);
+        tma_reduce_add_2d(&tmdQ, stage + kTile, h * kD + 32, s0 + i0);
+        bulk_commit();
+      }
+    }
+    if (ok) {
+      // every MMA has completed (the last dQ commit covers them all): drain dK, dV
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        float v[64];
+        const uint32_t col = which == 0 ? TM_DK : TM_DV;
+        tmem_ld32(tbase + lane_off + col, v);
+        tmem_ld32(tbase + lane_off + col + 32, v + 32);
+        if (t == 0) bulk_wait_read_all();
+        named_bar(2, 128);
+#pragma unroll
+        for (int half = 0; half < 2; ++half)
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const uint32_t phys = ((g ^ (r & 7)) * 16);
+            *reinterpret_cast<float4*>(sm + OFF_ST + half * kTile + r * 128 + phys) =
+                make_float4(v[half * 32 + 4 * g], v[half * 32 + 4 * g + 1], v[half * 32 + 4 * g + 2],
+                            v[half * 32 + 4 * g + 3]);
+          }
+        fence_async_smem();
+        named_bar(2, 128);
+        if (t == 0) {
+          const CUtensorMap* m = which == 0 ? &tmdK : &tmdV;
+          tma_reduce_add_2d(m, stage, hk * kD, s0 + j0);
+          tma_reduce_add_2d(m, stage + kTile, hk * kD + 32, s0 + j0);
+          bulk_commit();
+        }
+      }
+    }
+    if (t == 0) bulk_wait_all();
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 D pre-pass, head dim 64.  One CTA per (sequence, query head, 128
+// queries): O' = sum over kept causal keys of P V, D = rowsum(dO * O').
+//   warp 0     TMA: Q, dO once; K_j, V_j per key block (2 stages)
+//   warp 1     TMEM owner; one lane issues S_j = Q K_j^T (into one of two
+//              TMEM buffers, so S_{j+1} overlaps the softmax of block j) and
+//              O' += P_j V_j
+//   warps 2-5  one query row per thread: P_j from TMEM -> bf16 -> shared;
+//              at the end D from O' (TMEM) and dO (shared)
+// TMEM columns: S buffers 0-127 and 128-255, O' 256-319.
+namespace tcdprep {
+constexpr int kQ = 128, kK = 128, kD = 64;
+constexpr uint32_t kTile = 16384;
+constexpr uint32_t OFF_Q = 0, OFF_DO = kTile, OFF_K = 2 * kTile, OFF_V = 4 * kTile, OFF_P = 6 * kTile,
+                   OFF_BAR = 10 * kTile;
+constexpr size_t kSmem = 1024 + OFF_BAR + 256;
+constexpr uint32_t TM_S = 0, TM_O = 256;
+constexpr int kThreads = 192;
+}  // namespace tcdprep
+
+struct DprepTc {
+  int B, T, H, G, causal, nqb;
+  float scale_log2;
+  const int32_t* cu_kept;
+  const float* lse2;
+  float* Dvec;
+  long long M;
+  DevStatus* st;
+};
+
+__global__ void __launch_bounds__(tcdprep::kThreads, 1)
+    attn_dprep_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                         DprepTc p) {
+  using namespace tc;
+  using namespace tcdprep;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // items: query block descending (most key blocks first), then sequence, head
+  const int per_i = p.B * p.H;
+  const int ib = p.nqb - 1 - (int)(blockIdx.x / per_i);
+  const int b = (blockIdx.x % per_i) / p.H;
+  const int h = blockIdx.x % p.H;
+  const int s0 = p.cu_kept[b], len = p.cu_kept[b + 1] - s0;
+  const int i0 = ib * kQ;
+  if (i0 >= len) return;
+  const int hk = h / p.G;
+  const int nj = p.causal ? ib + 1 : (len + kK - 1) / kK;
+  const int qrows = min(kQ, len - i0);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  const uint32_t b_q = smem_u32(bars + 0), b_kvfull = smem_u32(bars + 1), b_kvempty = smem_u32(bars + 3),
+                 b_sfull = smem_u32(bars + 5), b_pfull = smem_u32(bars + 7), b_pempty = smem_u32(bars + 8),
+                 b_ofull = smem_u32(bars + 10), b_kvready = smem_u32(bars + 11);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(b_q, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(b_kvfull + 8 * s, 1);
+      mbar_init(b_kvempty + 8 * s, 1);
+      mbar_init(b_sfull + 8 * s, 1);
+      mbar_init(b_pempty + 8 * s, 1);
+    }
+    mbar_init(b_pfull, 128);
+    mbar_init(b_ofull, 1);
+    mbar_init(b_kvready, 1);
+    mbar_init(b_kvready + 8, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint32_t sbase = smem_u32(sm);
+  volatile int no_abort = 0;
+
+  if (warp == 0) {
+    // TMA producer (lane 0); the whole warp zeroes K / V rows past the
+    // sequence before the MMAs read a block (0 * non-finite would leak)
+    auto issue = [&](int j) -> bool {
+      const int st = j & 1, use = j >> 1;
+      if (!mbar_wait(b_kvempty + 8 * st, (use & 1) ^ 1, abort_flag, p.st, 40)) return false;
+      mbar_expect_tx(b_kvfull + 8 * st, 2 * kTile);
+      tma_load_2d(sbase + OFF_K + st * 2 * kTile, &tmK, b_kvfull + 8 * st, hk * kD, s0 + j * kK);
+      tma_load_2d(sbase + OFF_K + st * 2 * kTile + kTile, &tmV, b_kvfull + 8 * st, hk * kD, s0 + j * kK);
+      return true;
+    };
+    int ok = 1;
+    if (lane == 0) {
+      mbar_expect_tx(b_q, 2 * kTile);
+      tma_load_2d(sbase + OFF_Q, &tmQ, b_q, h * kD, s0 + i0);
+      tma_load_2d(sbase + OFF_DO, &tmdO, b_q, h * kD, s0 + i0);
+      ok = issue(0) ? 1 : 0;
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    // Block j is released to the MMA before block j+1 is requested: requesting
+    // j+1 waits for the P V of block j-1, which the MMA issues only after
+    // S_j, i.e. after block j is released.
+    for (int j = 0; ok && j < nj; ++j) {
+      const int st = j & 1, use = j >> 1;
+      if (!mbar_wait(b_kvfull + 8 * st, use & 1, &no_abort, p.st, 47)) break;
+      const int krows = min(kK, len - j * kK);
+      if (krows < kK) {
+        const uint32_t base = OFF_K + st * 2 * kTile;
+        for (int i = lane; i < (kK - krows) * 8; i += 32) {
+          const uint32_t off = (krows + i / 8) * 128 + (i % 8) * 16;
+          *reinterpret_cast<uint4*>(sm + base + off) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(sm + base + kTile + off) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_kvready + 8 * st);
+      int nxt = 1;
+      if (lane == 0 && j + 1 < nj) nxt = issue(j + 1) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, nxt, 0)) break;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t id_o = idesc_bf16(128, 64, false, true);
+      bool ok = mbar_wait(b_q, 0, abort_flag, p.st, 41);
+      // O' += P_{jj} V_{jj} for the block whose P the softmax has finished
+      auto pv = [&](int jj) -> bool {
+        const int st = jj & 1;
+        if (!mbar_wait(b_pfull, jj & 1, abort_flag, p.st, 42)) return false;
+        fence_after();
+        const uint32_t sv = sbase + OFF_K + st * 2 * kTile + kTile;
+#pragma unroll
+        for (int kk = 0; kk < kK / 16; ++kk) {
+          const uint32_t pa = sbase + OFF_P + st * 2 * kTile + (kk >> 2) * kTile + (kk & 3) * 32;
+          mma_bf16(tbase + TM_O, sdesc(pa, 16, 1024), sdesc(sv + kk * 2048, 8192, 1024), id_o, (jj > 0) || (kk > 0));
+        }
+        mma_commit(b_kvempty + 8 * st);
+        mma_commit(b_pempty + 8 * st);
+        return true;
+      };
+      for (int j = 0; ok && j < nj; ++j) {
+        const int st = j & 1, use = j >> 1;
+        if (!mbar_wait(b_kvready + 8 * st, use & 1, abort_flag, p.st, 43)) { ok = false; break; }
+        fence_after();
+        const uint32_t sk = sbase + OFF_K + st * 2 * kTile;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_bf16(tbase + TM_S + st * 128, sdesc(sbase + OFF_Q + kk * 32, 16, 1024), sdesc(sk + kk * 32, 16, 1024),
+                   id_s, kk > 0);
+        mma_commit(b_sfull + 8 * st);
+        if (j > 0 && !pv(j - 1)) { ok = false; break; }
+      }
+      if (ok && pv(nj - 1)) mma_commit(b_ofull);
+    }
+  } else {
+    // softmax: one query row per thread
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const float L = (r < qrows) ? p.lse2[(long long)h * p.M + s0 + i0 + r] : 0.f;
+    bool ok = true;
+    for (int j = 0; j < nj; ++j) {
+      const int st = j & 1, use = j >> 1;
+      if (!mbar_wait(b_sfull + 8 * st, use & 1, &no_abort, p.st, 44)) { ok = false; break; }
+      if (j >= 2 && !mbar_wait(b_pempty + 8 * st, (use - 1) & 1, &no_abort, p.st, 45)) { ok = false; break; }
+      fence_after();
+      const int j0 = j * kK;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float sv[32];
+        tmem_ld32(tbase + lane_off + TM_S + st * 128 + c * 32, sv);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int kj = j0 + c * 32 + e;
+          const bool valid = r < qrows && kj < len && (!p.causal || kj <= i0 + r);
+          sv[e] = valid ? exp2f(sv[e] * p.scale_log2 - L) : 0.f;
+        }
+        const uint32_t sub = st * 2 * kTile + (c >> 1) * kTile + r * 128;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const uint32_t phys = ((((c & 1) * 4 + g) ^ (r & 7)) * 16);
+          *reinterpret_cast<uint4*>(sm + OFF_P + sub + phys) = pack8(sv + 8 * g);
+        }
+      }
+      fence_before();
+      fence_async_smem();
+      mbar_arrive(b_pfull);
+    }
+    if (ok && mbar_wait(b_ofull, 0, &no_abort, p.st, 46)) {
+      fence_after();
+      float o[64];
+      tmem_ld32(tbase + lane_off + TM_O, o);
+      tmem_ld32(tbase + lane_off + TM_O + 32, o + 32);
+      float d = 0.f;
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        float x[8];
+        unpack8(*reinterpret_cast<const uint4*>(sm + OFF_DO + r * 128 + ((g ^ (r & 7)) * 16)), x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) d += x[e] * o[8 * g + e];
+      }
+      if (r < qrows) p.Dvec[(long long)h * p.M + s0 + i0 + r] = d;
+    }
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
 template <int DH>
-cudaError_t run(const Ctx& c, const AttnK& k, float rope_base) {
+cudaError_t run(const Ctx& c, const AttnK& k, float rope_base, const AttnArgs& a) {
   constexpr int LD = Tile<DH>::kLd;
   const size_t smem_prep = 4 * kBlk * LD * sizeof(__nv_bfloat16);
   const size_t smem_main = 4 * kBlk * LD * sizeof(__nv_bfloat16) + kBlk * (kBlk + 8) * sizeof(__nv_bfloat16) +
                            2 * kBlk * sizeof(float);
+  const bool use_tc = (DH == 64) && k.kv_acc;
   static int seen[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -506,6 +1061,12 @@ cudaError_t run(const Ctx& c, const AttnK& k, float rope_base) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_main_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(smem_main));
+    if (e == cudaSuccess && DH == 64)
+      e = cudaFuncSetAttribute(attn_main_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(tcattn::kSmem));
+    if (e == cudaSuccess && DH == 64)
+      e = cudaFuncSetAttribute(attn_dprep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(tcdprep::kSmem));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) seen[dev] = 1;
   }
@@ -513,12 +1074,45 @@ cudaError_t run(const Ctx& c, const AttnK& k, float rope_base) {
   prof_begin(c, "attn_prep");
   attn_prep_kernel<<<c.num_sms * 4, 256, 0, c.stream>>>(k, DH, rope_base, const_cast<float2*>(k.rope));
   prof_end(c);
-  prof_begin(c, "attn_dprep");
-  attn_dprep_kernel<DH><<<k.B * k.H * nb, 128, smem_prep, c.stream>>>(k);
-  prof_end(c);
-  prof_begin(c, "attn_main");
-  attn_main_kernel<DH><<<k.B * k.Hkv * nb, 128, smem_main, c.stream>>>(k);
-  prof_end(c);
+  if (!use_tc) {
+    prof_begin(c, "attn_dprep");
+    attn_dprep_kernel<DH><<<k.B * k.H * nb, 128, smem_prep, c.stream>>>(k);
+    prof_end(c);
+  }
+  if (use_tc) {
+    // work items: (key block, sequence, kv head, chunk of hc query heads)
+    const int nkb = (k.T + tcattn::kK - 1) / tcattn::kK;
+    int hc = k.G;
+    while (hc > 1 && hc % 2 == 0 && (long long)k.B * k.Hkv * nkb * (k.G / hc) < 3LL * c.num_sms) hc /= 2;
+    MainTc m{};
+    m.B = k.B; m.T = k.T; m.H = k.H; m.Hkv = k.Hkv; m.G = k.G; m.hc = hc; m.nhc = k.G / hc; m.nkb = nkb;
+    m.causal = k.causal; m.scale_log2 = k.scale_log2; m.cu_kept = k.cu_kept; m.lse2 = k.lse2; m.Dvec = k.Dvec;
+    m.M = k.M; m.st = c.st;
+    CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
+    bool ok = make_tensor_map(&tq, k.q, false, (long long)k.H * DH, a.in_cap, k.q_ld, 64, 128) &&
+              make_tensor_map(&tk, k.k, false, (long long)k.Hkv * DH, a.in_cap, k.kv_ld, 64, 128) &&
+              make_tensor_map(&tv, k.v, false, (long long)k.Hkv * DH, a.in_cap, k.kv_ld, 64, 128) &&
+              make_tensor_map(&tdo, k.dO, false, (long long)k.H * DH, a.in_cap, k.do_ld, 64, 128) &&
+              make_tensor_map(&tdq, k.dq_acc, true, (long long)k.H * DH, k.M, (long long)k.H * DH, 32, 128) &&
+              make_tensor_map(&tdk, k.dk_acc, true, (long long)k.Hkv * DH, k.M, (long long)k.Hkv * DH, 32, 128) &&
+              make_tensor_map(&tdv, k.dv_acc, true, (long long)k.Hkv * DH, k.M, (long long)k.Hkv * DH, 32, 128);
+    if (!ok) return cudaErrorInvalidValue;
+    DprepTc dp{};
+    dp.B = k.B; dp.T = k.T; dp.H = k.H; dp.G = k.G; dp.causal = k.causal; dp.nqb = nkb;
+    dp.scale_log2 = k.scale_log2; dp.cu_kept = k.cu_kept; dp.lse2 = k.lse2; dp.Dvec = k.Dvec; dp.M = k.M;
+    dp.st = c.st;
+    prof_begin(c, "attn_dprep_tc");
+    attn_dprep_tc_kernel<<<k.B * k.H * nkb, tcdprep::kThreads, tcdprep::kSmem, c.stream>>>(tq, tk, tv, tdo, dp);
+    prof_end(c);
+    prof_begin(c, "attn_main_tc");
+    attn_main_tc_kernel<<<k.B * k.Hkv * nkb * m.nhc, tcattn::kThreads, tcattn::kSmem, c.stream>>>(
+        tq, tk, tv, tdo, tdq, tdk, tdv, m);
+    prof_end(c);
+  } else {
+    prof_begin(c, "attn_main");
+    attn_main_kernel<DH><<<k.B * k.Hkv * nb, 128, smem_main, c.stream>>>(k);
+    prof_end(c);
+  }
   prof_begin(c, "attn_finalize");
   attn_finalize_kernel<<<c.num_sms * 4, 256, 0, c.stream>>>(k, DH);
   prof_end(c);
@@ -533,6 +1127,8 @@ size_t attn_ws_bytes(int B, int T, int H, int Hkv, int dh) {
   size_t b = 0;
   auto add = [&](size_t n) { b += (n + 255) & ~size_t(255); };
   add(M * H * dh * sizeof(float));      // dq_acc
+  add(M * Hkv * dh * sizeof(float));    // dk_acc
+  add(M * Hkv * dh * sizeof(float));    // dv_acc
   add(M * H * sizeof(float));           // Dvec
   add(M * H * sizeof(float));           // lse2
   add((size_t)T * (dh / 2) * sizeof(float2));   // RoPE table
@@ -552,8 +1148,10 @@ cudaError_t launch_attn_bwd(const Ctx& c, const AttnArgs& a) {
   k.dq_acc = a.dq_acc; k.Dvec = a.Dvec; k.lse2 = a.lse_k;
   k.M = a.M; k.cap = a.cap > 0 ? a.cap : a.M; k.st = c.st;
   k.rope = a.rope;
-  if (a.dh == 64) return run<64>(c, k, a.rope_base);
-  if (a.dh == 128) return run<128>(c, k, a.rope_base);
+  k.dk_acc = a.dk_acc; k.dv_acc = a.dv_acc;
+  k.kv_acc = (a.dh == 64 && a.dk_acc && a.dv_acc && a.in_cap > 0) ? 1 : 0;
+  if (a.dh == 64) return run<64>(c, k, a.rope_base, a);
+  if (a.dh == 128) return run<128>(c, k, a.rope_base, a);
   return cudaErrorInvalidValue;
 }
 

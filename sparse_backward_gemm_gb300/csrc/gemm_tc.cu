@@ -12,12 +12,11 @@
 // into a double-buffered TMEM accumulator; four epilogue warps drain TMEM
 // with tcgen05.ld while the next tile's MMAs run.  Persistent grid (one CTA
 // per SM); every mbarrier wait is bounded.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
+#include <cstdlib>
 #include <mutex>
 
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace collider {
 
@@ -37,108 +36,17 @@ struct TcParams {
   int accumulate;
   int zero_pad;
   long long c_rows;
+  float* partial;    // stream-K: [2 * gridDim.x][BM][BN] f32 partial tiles (null: whole tiles only)
+  int* counters;     // stream-K: per-tile arrival counts, zero on entry and left zero
   DevStatus* st;
 };
 
-// ---------------------------------------------------------------------------
-// PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait for the phase with the given parity to complete.  Returns
-// false when the budget ran out (recorded in the status word) or another role
-// of this CTA already gave up.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                       DevStatus* st, unsigned site) {
-  if (mbar_try(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t n = 1;; ++n) {
-    if (mbar_try(bar, parity)) return true;
-    if ((n & 63) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitBudgetNs) {
-        report_error(st, kErrTimeout, site);
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// tcgen05 shared-memory matrix descriptor, 128-byte swizzle, sm_100 version.
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
-  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
-         (static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16) |
-         (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accum) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
+using namespace tc;
 
 // instruction descriptor: f32 accumulate, bf16 A and B, M = 128, N = BN
 template <int BN, bool A_MN, bool B_MN>
 __device__ __forceinline__ constexpr uint32_t make_idesc() {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
-         (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+  return idesc_bf16(BM, BN, A_MN, B_MN);
 }
 
 template <int BN>
@@ -151,6 +59,82 @@ struct TcCfg {
   static constexpr size_t kSmem = 1024 + kStages * kStageBytes + 256;
 };
 
+// Work split.  Stream-K (partial != null): the num_tiles * num_kb (tile,
+// k-slice) iterations are cut into gridDim.x equal contiguous ranges, so every
+// CTA gets the same work whatever the tile count; a tile cut between CTAs is
+// finished by whichever of them arrives last, summing the partial tiles in
+// CTA order (deterministic).  Otherwise whole tiles round-robin.
+struct Split {
+  int m_tiles, num_tiles, num_kb;
+  long long total;
+  bool sk;
+  int G;   // CTAs sharing the work: min(grid, total), so that no range is empty
+  __device__ long long begin(int c) const { return sk ? (long long)c * total / G : 0; }
+  // the CTA whose range holds iteration x
+  __device__ int owner(long long x) const { return (int)(((x + 1) * (long long)G - 1) / total); }
+  __device__ int slot(int c, int t) const { return 2 * c + (t == (int)(begin(c) / num_kb) ? 0 : 1); }
+};
+
+// Iterates this CTA's segments: (tile, first k-slice, end k-slice).
+struct SegIter {
+  const Split& sp;
+  long long it, end;   // stream-K
+  int tile;            // whole-tile mode
+  __device__ SegIter(const Split& s) : sp(s) {
+    if (sp.sk) {
+      if ((int)blockIdx.x < sp.G) {
+        it = sp.begin(blockIdx.x);
+        end = (long long)(blockIdx.x + 1) * sp.total / sp.G;
+      } else {
+        it = end = 0;
+      }
+    } else {
+      tile = blockIdx.x;
+    }
+  }
+  __device__ bool next(int& t, int& k0, int& k1) {
+    if (sp.sk) {
+      if (it >= end) return false;
+      t = (int)(it / sp.num_kb);
+      k0 = (int)(it % sp.num_kb);
+      const long long lim = k0 + (end - it);
+      k1 = lim < sp.num_kb ? (int)lim : sp.num_kb;
+      it += k1 - k0;
+      return true;
+    }
+    if (tile >= sp.num_tiles) return false;
+    t = tile;
+    k0 = 0;
+    k1 = sp.num_kb;
+    tile += gridDim.x;
+    return true;
+  }
+};
+
+// Store 32 consecutive columns of one output row (bf16 or f32, optional
+// accumulate into C, zero rows past the kept count up to the padding).
+__device__ __forceinline__ void store32(const TcParams& p, int row, int col, bool row_ok, float* v) {
+  if (p.c_bf16) {
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.C) + (long long)row * p.ldc + col;
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      if (col + 8 * g + 8 <= p.N) *reinterpret_cast<uint4*>(out + 8 * g) = pack8(v + 8 * g);
+  } else {
+    float* out = static_cast<float*>(p.C) + (long long)row * p.ldc + col;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      if (col + 4 * g + 4 <= p.N) {
+        float4 o = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+        if (p.accumulate && row_ok) {
+          float4 old = *reinterpret_cast<const float4*>(out + 4 * g);
+          o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
+        }
+        *reinterpret_cast<float4*>(out + 4 * g) = o;
+      }
+    }
+  }
+}
+
 template <int BN, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcParams p) {
@@ -161,6 +145,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::kStageBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S), tfull0 = smem_u32(bars + 2 * S),
                  tempty0 = smem_u32(bars + 2 * S + 2);
 
@@ -172,9 +157,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (p.dyn == 1) M = min(M, nk);
     else K = min(K, nk);
   }
-  const int m_tiles = (M + BM - 1) / BM, n_tiles = (p.N + BN - 1) / BN;
-  const int num_tiles = m_tiles * n_tiles;
-  const int num_kb = (K + BK - 1) / BK;
+  Split sp;
+  sp.m_tiles = (M + BM - 1) / BM;
+  sp.num_tiles = sp.m_tiles * ((p.N + BN - 1) / BN);
+  sp.num_kb = (K + BK - 1) / BK;
+  sp.total = (long long)sp.num_tiles * sp.num_kb;
+  sp.sk = p.partial != nullptr && sp.total > 0;
+  sp.G = (int)(sp.total < (long long)gridDim.x ? sp.total : (long long)gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -190,47 +179,63 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
   }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(Cfg::kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  tc_fence_before();
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+  fence_before();
   __syncthreads();
-  tc_fence_after();
+  fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
+  if (sp.num_kb == 0) {
+    // empty reduction (nothing kept): the output is zero
+    if (warp >= 2) {
+      const int q = warp & 3;
+      for (int t = blockIdx.x; t < sp.num_tiles; t += gridDim.x) {
+        const int m0 = (t % sp.m_tiles) * BM, n0 = (t / sp.m_tiles) * BN;
+        const int row = m0 + q * 32 + lane;
+        const bool row_ok = row < M;
+        if (!(row_ok || (p.zero_pad && row < padded_rows(M, p.c_rows)))) continue;
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          store32(p, row, n0 + c, row_ok, v);
+        }
+      }
+    }
+  } else if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;   // stages with copies issued, and the phase parity armed
-      for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
-        const int m0 = (tile % m_tiles) * BM, n0 = (tile / m_tiles) * BN;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.st, 1)) break;
+      SegIter si(sp);
+      int t, k0, k1;
+      while (!*abort_flag && si.next(t, k0, k1)) {
+        const int m0 = (t % sp.m_tiles) * BM, n0 = (t / sp.m_tiles) * BN;
+        bool ok = true;
+        for (int kb = k0; kb < k1; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.st, 1)) { ok = false; break; }
           const uint32_t fb = full0 + 8 * stage;
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           mbar_expect_tx(fb, Cfg::kStageBytes);
           const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes), sb = sa + Cfg::kABytes;
-          const int k0 = kb * BK;
+          const int kx = kb * BK;
           if (!A_MN) {
-            tma_load_2d(sa, &tmA, fb, k0, m0);
+            tma_load_2d(sa, &tmA, fb, kx, m0);
           } else {
-            tma_load_2d(sa, &tmA, fb, m0, k0);
-            tma_load_2d(sa + 8192, &tmA, fb, m0 + 64, k0);
+            tma_load_2d(sa, &tmA, fb, m0, kx);
+            tma_load_2d(sa + 8192, &tmA, fb, m0 + 64, kx);
           }
           if (!B_MN) {
-            tma_load_2d(sb, &tmB, fb, k0, n0);
+            tma_load_2d(sb, &tmB, fb, kx, n0);
           } else {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + 8192 * j, &tmB, fb, n0 + 64 * j, k0);
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + 8192 * j, &tmB, fb, n0 + 64 * j, kx);
           }
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
+        if (!ok) break;
       }
       if (*abort_flag) {
         // another role gave up: let this thread's copies still in flight land
@@ -249,88 +254,123 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       constexpr uint32_t idesc = make_idesc<BN, A_MN, B_MN>();
       int stage = 0;
       uint32_t phase = 0;
-      int it = 0;
-      for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x, ++it) {
-        const int acc = it & 1;
-        const uint32_t aph = (it >> 1) & 1;
+      int seg = 0;
+      SegIter si(sp);
+      int t, k0, k1;
+      while (!*abort_flag && si.next(t, k0, k1)) {
+        const int acc = seg & 1;
+        const uint32_t aph = (seg >> 1) & 1;
         if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1u, abort_flag, p.st, 2)) break;
-        tc_fence_after();
+        fence_after();
         const uint32_t d = tmem_base + acc * BN;
         bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = k0; kb < k1; ++kb) {
           if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.st, 3)) { ok = false; break; }
-          tc_fence_after();
+          fence_after();
           const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes), sb = sa + Cfg::kABytes;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = A_MN ? sdesc(sa + kk * 2048, 8192, 1024) : sdesc(sa + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc(sb + kk * 2048, 8192, 1024) : sdesc(sb + kk * 32, 16, 1024);
-            mma_bf16(d, ad, bd, idesc, (kb | kk) != 0);
+            mma_bf16(d, ad, bd, idesc, (kb > k0) || (kk > 0));
           }
           mma_commit(empty0 + 8 * stage);
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
         mma_commit(tfull0 + 8 * acc);
+        ++seg;
       }
     }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
+    // Timeout-only waits: the group synchronises with a named barrier, so all
+    // 128 threads leave together.
+    volatile int no_abort = 0;
     const int q = warp & 3;   // TMEM lane quadrant this warp may access
-    int it = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
-      const int acc = it & 1;
-      const uint32_t aph = (it >> 1) & 1;
-      if (!mbar_wait(tfull0 + 8 * acc, aph, abort_flag, p.st, 4)) break;
-      tc_fence_after();
-      const int m0 = (tile % m_tiles) * BM, n0 = (tile / m_tiles) * BN;
-      const int row = m0 + q * 32 + lane;
+    const int et = threadIdx.x - 64;
+    int seg = 0;
+    SegIter si(sp);
+    int t, k0, k1;
+    while (si.next(t, k0, k1)) {
+      const int acc = seg & 1;
+      const uint32_t aph = (seg >> 1) & 1;
+      if (!mbar_wait(tfull0 + 8 * acc, aph, &no_abort, p.st, 4)) break;
+      fence_after();
+      const int m0 = (t % sp.m_tiles) * BM, n0 = (t / sp.m_tiles) * BN;
+      const int rl = q * 32 + lane;
+      const int row = m0 + rl;
       const bool row_ok = row < M;
       const bool row_zero = !row_ok && p.zero_pad && row < padded_rows(M, p.c_rows);
-      for (int c = 0; c < BN; c += 32) {
-        float v[32];
-        if (num_kb > 0) {
-          tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c, v);
-        } else {
+      const uint32_t tcol = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      if (!sp.sk || (k0 == 0 && k1 == sp.num_kb)) {
+        // whole tile: straight to the output
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld32(tcol + c, v);
+          if (!(row_ok || row_zero)) continue;
+          if (row_zero) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          }
+          store32(p, row, n0 + c, row_ok, v);
         }
-        if (!(row_ok || row_zero)) continue;
-        if (row_zero) {
+        fence_before();
+        mbar_arrive(tempty0 + 8 * acc);
+      } else {
+        // part of a tile: park it, and finish the tile if this CTA is the last
+        float* mine = p.partial + ((long long)sp.slot(blockIdx.x, t) * BM + rl) * BN;
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld32(tcol + c, v);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          for (int i = 0; i < 32; i += 4)
+            __stcg(reinterpret_cast<float4*>(mine + c + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
         }
-        const int col = n0 + c;
-        if (p.c_bf16) {
-          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.C) + (long long)row * p.ldc + col;
+        fence_before();
+        mbar_arrive(tempty0 + 8 * acc);
+        __threadfence();
+        named_bar(1, 128);
+        const long long x0 = (long long)t * sp.num_kb;
+        const int c_first = sp.owner(x0), c_last = sp.owner(x0 + sp.num_kb - 1);
+        if (et == 0) {
+          const int old = atomicAdd(p.counters + t, 1);
+          const int last = old == c_last - c_first;
+          if (last) p.counters[t] = 0;
+          *last_flag = last;
+        }
+        named_bar(1, 128);
+        if (*last_flag && (row_ok || row_zero)) {
+          __threadfence();
+          for (int c = 0; c < BN; c += 32) {
+            float v[32];
 #pragma unroll
-          for (int g = 0; g < 4; ++g)
-            if (col + 8 * g + 8 <= p.N) *reinterpret_cast<uint4*>(out + 8 * g) = pack8(v + 8 * g);
-        } else {
-          float* out = static_cast<float*>(p.C) + (long long)row * p.ldc + col;
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            for (int cc = c_first; cc <= c_last; ++cc) {
+              const float* src = p.partial + ((long long)sp.slot(cc, t) * BM + rl) * BN + c;
 #pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            if (col + 4 * g + 4 <= p.N) {
-              float4 o = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-              if (p.accumulate && row_ok) {
-                float4 old = *reinterpret_cast<const float4*>(out + 4 * g);
-                o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
+              for (int i = 0; i < 32; i += 4) {
+                const float4 w = __ldcg(reinterpret_cast<const float4*>(src + i));
+                v[i] += w.x; v[i + 1] += w.y; v[i + 2] += w.z; v[i + 3] += w.w;
               }
-              *reinterpret_cast<float4*>(out + 4 * g) = o;
             }
+            if (row_zero) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            }
+            store32(p, row, n0 + c, row_ok, v);
           }
         }
+        named_bar(1, 128);   // last_flag is reused by the next segment
       }
-      tc_fence_before();
-      mbar_arrive(tempty0 + 8 * acc);
+      ++seg;
     }
   }
-  tc_fence_before();
+  fence_before();
   __syncthreads();
   if (warp == 1) {
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(Cfg::kTmemCols)
-                 : "memory");
+    fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
   }
 }
 
@@ -350,19 +390,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// 2-D bf16 tensor map over a row-major [rows, inner] matrix with leading
-// dimension ld (elements); box {64, box_rows}; 128-byte swizzle; zero fill.
 bool make_map(CUtensorMap* m, const void* base, long long inner, long long rows, long long ld, int box_rows) {
-  auto enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1u, 1u};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return make_tensor_map(m, base, false, inner, rows, ld, 64, box_rows);
 }
 
 template <int BN, bool A_MN, bool B_MN>
@@ -381,13 +410,34 @@ cudaError_t launch_variant(const Ctx& c, const TcGemm& g, const CUtensorMap& ma,
     if (dev >= 0 && dev < 64) seen[dev] = 1;
   }
   const long long tiles = ((long long)(g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
-  int grid = static_cast<int>(tiles < c.num_sms ? tiles : c.num_sms);
+  int grid;
+  if (p.partial) {
+    grid = c.num_sms < kSkMaxCtas ? c.num_sms : kSkMaxCtas;   // stream-K: one CTA per SM
+  } else {
+    grid = static_cast<int>(tiles < c.num_sms ? tiles : c.num_sms);
+  }
   if (grid < 1) grid = 1;
   tc_gemm_kernel<BN, A_MN, B_MN><<<grid, kTcThreads, Cfg::kSmem, c.stream>>>(ma, mb, p);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+bool make_tensor_map(CUtensorMap* m, const void* base, bool f32, long long inner, long long rows, long long ld,
+                     int box_inner, int box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  const int esz = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esz};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 bool tc_gemm_supported(const TcGemm& g) {
   if (g.N % 8 || g.K % 8 || g.M % 8) return false;
@@ -409,8 +459,15 @@ cudaError_t launch_tc_gemm(const Ctx& c, const TcGemm& g) {
   ok = ok && (g.b_mn_major ? make_map(&mb, g.B, g.N, g.b_rows, g.ldb, 64)
                            : make_map(&mb, g.B, g.K, g.b_rows, g.ldb, bn));
   if (!ok) return cudaErrorInvalidValue;
+  const long long max_tiles = ((long long)(g.M + BM - 1) / BM) * ((g.N + bn - 1) / bn);
+  // COLLIDER_GEMM_STREAMK=0 turns the stream-K split off (whole tiles only)
+  static const int sk_env = [] {
+    const char* e = getenv("COLLIDER_GEMM_STREAMK");
+    return e ? atoi(e) : 1;
+  }();
+  const bool sk = sk_env != 0 && g.partial && g.counters && max_tiles <= g.counter_cap;
   TcParams p{g.M, g.N, g.K, g.dyn, g.n_kept, g.C, g.ldc, g.c_bf16, g.accumulate, g.zero_pad,
-             g.c_rows > 0 ? g.c_rows : g.M, c.st};
+             g.c_rows > 0 ? g.c_rows : g.M, sk ? g.partial : nullptr, sk ? g.counters : nullptr, c.st};
   prof_begin(c, "tc_gemm", g.M, g.N, g.K, g.dyn);
   cudaError_t e;
   const int key = (bn == 256 ? 4 : 0) | (g.a_mn_major ? 2 : 0) | (g.b_mn_major ? 1 : 0);

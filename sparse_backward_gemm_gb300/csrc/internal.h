@@ -143,7 +143,15 @@ struct TcGemm {
   long long c_rows;   // row capacity of C (zero padding stops there)
   const int32_t* n_kept; int dyn;
   int bn;             // 128 or 256 (0 = choose)
+  // stream-K scratch (both null: whole tiles only).  partial holds
+  // kSkMaxCtas * 2 tiles of 128 x 256 f32; counters hold counter_cap ints,
+  // zero before the launch (the kernel leaves them zero).
+  float* partial;
+  int* counters;
+  long long counter_cap;
 };
+constexpr int kSkMaxCtas = 256;
+constexpr size_t kSkPartialFloats = (size_t)kSkMaxCtas * 2 * 128 * 256;
 cudaError_t launch_tc_gemm(const Ctx& c, const TcGemm& g);
 bool tc_gemm_supported(const TcGemm& g);
 
@@ -160,6 +168,9 @@ struct AttnArgs {
   __nv_bfloat16* dq; __nv_bfloat16* dk; __nv_bfloat16* dv;   // COMPACT rows, same strides as inputs
   long long dq_ld, dkv_ld;
   float* dq_acc;   // scratch f32 [M, H, dh]
+  float* dk_acc;   // scratch f32 [M, Hkv, dh] (tcgen05 path)
+  float* dv_acc;
+  long long in_cap;  // row capacity of the COMPACT q/k/v/dO buffers (TMA extent)
   float* Dvec;     // scratch f32 [H, M]
   float* lse_k;    // scratch f32 [H, M] (lse gathered to kept order, pre-scaled)
   float2* rope;    // scratch [T, rotary_dim/2] (cos, sin)

@@ -151,30 +151,30 @@ __global__ void __launch_bounds__(256) colsum_reduce_kernel(const float* __restr
 }
 
 // ---------------------------------------------------------------------------
-// norm backward (+ residual) on kept rows: one warp per row, two passes over
-// the row (the second re-reads it from L1/L2).  dgamma / dbeta partials go to
-// a per-warp shared-memory row and are summed over the warps in a fixed order,
-// so the result is deterministic.
-constexpr int kNormWarps = 4;
-constexpr int kNormRowsPerWarp = 8;
-constexpr int kNormRows = kNormWarps * kNormRowsPerWarp;   // rows per block (one partial row each)
+// norm backward (+ residual) on kept rows.
+//   rows:    one warp per row, two passes over the row (the second re-reads it
+//            from L1/L2): out = res + rstd * (g - xh * mean(g xh) [- mean(g)])
+//   columns: dgamma = sum_r dy xh, dbeta = sum_r dy, as per-64-row partials
+//            (thread = 8 columns) then a fixed-order reduction: deterministic.
+constexpr int kNormWarps = 8;
+constexpr int kNormColRows = 64;
 
-__global__ void __launch_bounds__(kNormWarps * 32) norm_bwd_kernel(NormBwdArgs a, DevStatus* st) {
-  extern __shared__ float sp[];   // [kNormWarps][nsets][D]
-  const int nsets = a.layer_norm ? 2 : 1;
+__device__ __forceinline__ void norm_dy8(const NormBwdArgs& a, long long off, float* dy) {
+  load8(a.dy1, 0, off, dy);
+  if (a.dy2) {
+    float d2[8];
+    load8(a.dy2, 0, off, d2);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) dy[k] += d2[k];
+  }
+}
+
+__global__ void __launch_bounds__(kNormWarps * 32) norm_rows_kernel(NormBwdArgs a, DevStatus* st) {
   const int D = a.D;
   const int nk = *a.n_kept;
   const int pad = padded_rows(nk, a.cap);
-  const int rb = blockIdx.x * kNormRows;
-  if (rb >= pad) return;
-  for (int i = threadIdx.x; i < kNormWarps * nsets * D; i += blockDim.x) sp[i] = 0.f;
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* mine = sp + warp * nsets * D;
-  const int r0 = rb + warp * kNormRowsPerWarp;
-  for (int i = 0; i < kNormRowsPerWarp; ++i) {
-    const int r = r0 + i;
-    if (r >= pad) break;
+  const int lane = threadIdx.x & 31;
+  for (int r = blockIdx.x * kNormWarps + (threadIdx.x >> 5); r < pad; r += gridDim.x * kNormWarps) {
     __nv_bfloat16* orow = a.out + (long long)r * D;
     if (r >= nk) {
       for (int c = lane * 8; c < D; c += 256) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
@@ -187,19 +187,11 @@ __global__ void __launch_bounds__(kNormWarps * 32) norm_bwd_kernel(NormBwdArgs a
     }
     const float rstd = a.rstd[t];
     const float mu = a.layer_norm ? a.mean[t] : 0.f;
-    const float* dy1 = a.dy1 + (long long)r * D;
-    const float* dy2 = a.dy2 ? a.dy2 + (long long)r * D : nullptr;
     const __nv_bfloat16* xr = a.x + (long long)t * D;
     float s_gx = 0.f, s_g = 0.f;
     for (int c = lane * 8; c < D; c += 256) {
       float dy[8], xv[8], gm[8];
-      load8(dy1, 0, c, dy);
-      if (dy2) {
-        float d2[8];
-        load8(dy2, 0, c, d2);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) dy[k] += d2[k];
-      }
+      norm_dy8(a, (long long)r * D + c, dy);
       load8(xr, 1, c, xv);
       load8(a.gamma, 1, c, gm);
 #pragma unroll
@@ -213,13 +205,7 @@ __global__ void __launch_bounds__(kNormWarps * 32) norm_bwd_kernel(NormBwdArgs a
     s_g = a.layer_norm ? warp_sum(s_g) / (float)D : 0.f;
     for (int c = lane * 8; c < D; c += 256) {
       float dy[8], xv[8], gm[8], o[8];
-      load8(dy1, 0, c, dy);
-      if (dy2) {
-        float d2[8];
-        load8(dy2, 0, c, d2);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) dy[k] += d2[k];
-      }
+      norm_dy8(a, (long long)r * D + c, dy);
       load8(xr, 1, c, xv);
       load8(a.gamma, 1, c, gm);
       if (a.res) {
@@ -229,22 +215,42 @@ __global__ void __launch_bounds__(kNormWarps * 32) norm_bwd_kernel(NormBwdArgs a
         for (int k = 0; k < 8; ++k) o[k] = 0.f;
       }
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float xh = (xv[k] - mu) * rstd;
-        o[k] += rstd * (dy[k] * gm[k] - xh * s_gx - s_g);
-        mine[c + k] += dy[k] * xh;
-        if (nsets == 2) mine[D + c + k] += dy[k];
-      }
+      for (int k = 0; k < 8; ++k) o[k] += rstd * (dy[k] * gm[k] - (xv[k] - mu) * rstd * s_gx - s_g);
       *reinterpret_cast<uint4*>(orow + c) = pack8(o);
     }
   }
-  __syncthreads();
-  float* part = a.part + (long long)blockIdx.x * nsets * D;
-  for (int i = threadIdx.x; i < nsets * D; i += blockDim.x) {
-    float v = 0.f;
+}
+
+__global__ void __launch_bounds__(256) norm_cols_kernel(NormBwdArgs a) {
+  const int nk = *a.n_kept;
+  const int r0 = blockIdx.y * kNormColRows;
+  if (r0 >= nk) return;
+  const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (c >= a.D) return;
+  float dg[8] = {0, 0, 0, 0, 0, 0, 0, 0}, db[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  const int r1 = min(nk, r0 + kNormColRows);
+  for (int r = r0; r < r1; ++r) {
+    const int t = a.idx[r];
+    if ((unsigned)t >= (unsigned)a.M) continue;   // reported by the row kernel
+    const float rstd = a.rstd[t];
+    const float mu = a.layer_norm ? a.mean[t] : 0.f;
+    float dy[8], xv[8];
+    norm_dy8(a, (long long)r * a.D + c, dy);
+    load8(a.x, 1, (long long)t * a.D + c, xv);
 #pragma unroll
-    for (int w = 0; w < kNormWarps; ++w) v += sp[w * nsets * D + i];
-    part[i] = v;
+    for (int k = 0; k < 8; ++k) {
+      dg[k] += dy[k] * (xv[k] - mu) * rstd;
+      db[k] += dy[k];
+    }
+  }
+  const int nsets = a.layer_norm ? 2 : 1;
+  float4* p = reinterpret_cast<float4*>(a.part + ((long long)blockIdx.y * nsets) * a.D + c);
+  p[0] = make_float4(dg[0], dg[1], dg[2], dg[3]);
+  p[1] = make_float4(dg[4], dg[5], dg[6], dg[7]);
+  if (nsets == 2) {
+    float4* q = reinterpret_cast<float4*>(a.part + ((long long)blockIdx.y * nsets + 1) * a.D + c);
+    q[0] = make_float4(db[0], db[1], db[2], db[3]);
+    q[1] = make_float4(db[4], db[5], db[6], db[7]);
   }
 }
 
@@ -467,31 +473,24 @@ cudaError_t launch_colsum(const Ctx& c, const void* X, int x_is_bf16, long long 
   return cudaGetLastError();
 }
 
-size_t norm_part_floats(int M, int D) { return (size_t)((M + kNormRows - 1) / kNormRows) * 2 * (size_t)D; }
+size_t norm_part_floats(int M, int D) {
+  return (size_t)((M + kNormColRows - 1) / kNormColRows) * 2 * (size_t)D;
+}
 
 cudaError_t launch_norm_bwd(const Ctx& c, const NormBwdArgs& a) {
   const int nsets = a.layer_norm ? 2 : 1;
-  const size_t smem = (size_t)kNormWarps * nsets * a.D * sizeof(float);
-  static int seen[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !seen[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(norm_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kNormWarps * 2 * 4096 * (int)sizeof(float));
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) seen[dev] = 1;
-  }
-  const int grid = (int)((a.cap + kNormRows - 1) / kNormRows);
   prof_begin(c, "norm_bwd");
-  norm_bwd_kernel<<<grid, kNormWarps * 32, smem, c.stream>>>(a, c.st);
-  // partials are laid out [block][set][D] with set 0 = dgamma, set 1 = dbeta
+  norm_rows_kernel<<<grid_rows(c, a.cap, kNormWarps), kNormWarps * 32, 0, c.stream>>>(a, c.st);
+  norm_cols_kernel<<<dim3((a.D / 8 + 255) / 256, (unsigned)((a.cap + kNormColRows - 1) / kNormColRows)), 256, 0,
+                     c.stream>>>(a);
+  // partials are laid out [part][set][D] with set 0 = dgamma, set 1 = dbeta
   const int g = (a.D + 255) / 256;
-  colsum_reduce_kernel<<<g, 256, 0, c.stream>>>(a.part, a.D, (long long)nsets * a.D, kNormRows, a.n_kept,
+  colsum_reduce_kernel<<<g, 256, 0, c.stream>>>(a.part, a.D, (long long)nsets * a.D, kNormColRows, a.n_kept,
                                                 a.dgamma);
   if (a.layer_norm)
-    colsum_reduce_kernel<<<g, 256, 0, c.stream>>>(a.part + a.D, a.D, (long long)nsets * a.D, kNormRows, a.n_kept,
-                                                  a.dbeta);
-  count_launch(1 + nsets);
+    colsum_reduce_kernel<<<g, 256, 0, c.stream>>>(a.part + a.D, a.D, (long long)nsets * a.D, kNormColRows,
+                                                  a.n_kept, a.dbeta);
+  count_launch(2 + nsets);
   prof_end(c);
   return cudaGetLastError();
 }

@@ -36,6 +36,7 @@ def _case(B, T, H, Hkv, dh, f, mask, seed, qk_std=1.0):
     (2, 130, 2, 2, 64, 0.6, "span", 32),       # MHA, partial rotary, span mask
     (1, 64, 2, 2, 64, 0.0, "gumbel", 0),       # nothing filtered, no RoPE
     (3, 100, 4, 1, 64, 0.2, "gumbel", 16),
+    (1, 1100, 8, 2, 64, 0.3, "gumbel", 64),    # many key / query blocks per sequence
 ])
 @pytest.mark.parametrize("rows", ["full", "compact"])
 def test_attention_backward(B, T, H, Hkv, dh, f, mask, rot, rows):
