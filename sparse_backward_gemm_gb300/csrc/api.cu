@@ -595,14 +595,19 @@ thread_local int* g_sk_counters = nullptr;
 thread_local long long g_sk_cap = 0;
 
 // C (bf16 or f32, COMPACT [Mk, N]) = A_k [Mk, K] . W^T with W stored [N, K]
+// (epi: a fused activation backward, reading FULL rows of aux through idx)
 cudaError_t gemm_dx(const Ctx& c, int M, int N, int K, const void* A, const void* W, void* C, int c_bf16,
-                    int accumulate, const int32_t* n_kept) {
+                    int accumulate, const int32_t* n_kept, int epi = kEpiStore, const void* aux = nullptr,
+                    const int32_t* idx = nullptr) {
   TcGemm g{};
   g.partial = g_sk_partial; g.counters = g_sk_counters; g.counter_cap = g_sk_cap;
+  g.epi = epi; g.aux = static_cast<const __nv_bfloat16*>(aux); g.idx = idx; g.aux_rows = M;
+  g.aux_ld = epi == kEpiSwiGLU ? 2LL * N : N;
   g.M = M; g.N = N; g.K = K;
   g.A = A; g.lda = K; g.a_mn_major = 0; g.a_rows = pad128(M);
   g.B = W; g.ldb = K; g.b_mn_major = 0; g.b_rows = N;
-  g.C = C; g.ldc = N; g.c_bf16 = c_bf16; g.accumulate = accumulate; g.zero_pad = 1; g.c_rows = pad128(M);
+  g.C = C; g.ldc = epi == kEpiSwiGLU ? 2LL * N : N; g.c_bf16 = c_bf16; g.accumulate = accumulate; g.zero_pad = 1;
+  g.c_rows = pad128(M);
   g.n_kept = n_kept; g.dyn = 1;
   return launch_tc_gemm(c, g);
 }

@@ -523,8 +523,9 @@ __global__ void attn_finalize_kernel(AttnK p, int DH) {
 //                 S^T = K Q^T, dP^T = V dO^T           (M 128 keys, N 128 queries)
 //                 dV += P^T dO, dK += dS^T Q           (M 128 keys, N 64)
 //                 dQ  = dS K                           (M 128 queries, N 64)
-//   warps 2-5   one key row per thread: P^T, dS^T from TMEM -> bf16 -> shared
-//   warps 6-9   one query row per thread: dQ from TMEM -> shared -> TMA
+//   warps 2-9   one key row and 64 of the 128 queries per thread: P^T, dS^T
+//               from TMEM -> bf16 -> shared
+//   warps 10-13 one query row per thread: dQ from TMEM -> shared -> TMA
 //               reduce-add into the f32 dQ accumulator; at the end dK, dV
 //               likewise into their accumulators
 // TMEM columns: S^T 0-127, dP^T 128-255, dV 256-319, dK 320-383, dQ 384-447.
@@ -535,7 +536,8 @@ constexpr uint32_t OFF_K = 0, OFF_V = kTile, OFF_Q = 2 * kTile, OFF_DO = 4 * kTi
                    OFF_DS = 8 * kTile, OFF_ST = 10 * kTile, OFF_LD = 12 * kTile, OFF_BAR = 12 * kTile + 2048;
 constexpr size_t kSmem = 1024 + OFF_BAR + 256;
 constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 320, TM_DQ = 384;
-constexpr int kThreads = 320;
+constexpr int kSoftWarps = 8;                       // two per TMEM lane quadrant
+constexpr int kThreads = 32 * (2 + kSoftWarps + 4);
 }  // namespace tcattn
 
 struct MainTc {
@@ -589,7 +591,7 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       mbar_init(b_qempty + 8 * s, 1);
     }
     mbar_init(b_sfull, 1);
-    mbar_init(b_pfull, 128);
+    mbar_init(b_pfull, 32 * kSoftWarps);
     mbar_init(b_pempty, 1);
     mbar_init(b_dqfull, 1);
     mbar_init(b_dqempty, 128);
@@ -710,39 +712,54 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
         mma_commit(b_pempty);
       }
     }
-  } else if (warp < 6) {
-    // ---------------- softmax warps: one key row per thread ----------------
-    const int t = threadIdx.x - 64;
+  } else if (warp < 2 + kSoftWarps) {
+    // ---------------- softmax warps: one key row, 64 queries per thread ----------------
+    const int t = threadIdx.x - 64;             // 0..255
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;           // which 64 queries of the block
     const int kr = q * 32 + lane;
     const int key = j0 + kr;
     const bool kvalid = key < len;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    for (int it = 0; it < n_iter; ++it) {
+    // lse (threads 0-127) and D (threads 128-255) of the block after the
+    // current one are fetched one iteration early, so the global-load latency
+    // hides behind the current block
+    auto fetch = [&](int it) -> float {
       const int h = hk * p.G + hci * p.hc + it / nq_head;
+      const int i0 = (i_start + it % nq_head) * kQ;
+      const int qq = t & 127;
+      if (qq >= min(kQ, len - i0)) return 0.f;
+      const float* src = t < 128 ? p.lse2 : p.Dvec;
+      return src[(long long)h * p.M + s0 + i0 + qq];
+    };
+    float nxt = n_iter > 0 ? fetch(0) : 0.f;
+    for (int it = 0; it < n_iter; ++it) {
       const int i0 = (i_start + it % nq_head) * kQ;
       const int qrows = min(kQ, len - i0);
       const int buf = it & 1;
-      sL[buf * 128 + t] = (t < qrows) ? p.lse2[(long long)h * p.M + s0 + i0 + t] : 0.f;
-      sD[buf * 128 + t] = (t < qrows) ? p.Dvec[(long long)h * p.M + s0 + i0 + t] : 0.f;
-      named_bar(1, 128);
+      (t < 128 ? sL : sD)[buf * 128 + (t & 127)] = nxt;
+      if (it + 1 < n_iter) nxt = fetch(it + 1);
+      named_bar(1, 32 * kSoftWarps);
       if (!mbar_wait(b_sfull, it & 1, &no_abort, p.st, 25)) break;
       if (it > 0 && !mbar_wait(b_pempty, (it - 1) & 1, &no_abort, p.st, 26)) break;
       fence_after();
       const float* L = sL + buf * 128;
       const float* Dd = sD + buf * 128;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * half + cc;            // 32-query chunk
+        uint32_t sr[32], dr[32];
+        tmem_ld32_async(tbase + lane_off + TM_S + c * 32, sr);
+        tmem_ld32_async(tbase + lane_off + TM_DP + c * 32, dr);
+        tmem_wait_ld();
         float sv[32], dv[32];
-        tmem_ld32(tbase + lane_off + TM_S + c * 32, sv);
-        tmem_ld32(tbase + lane_off + TM_DP + c * 32, dv);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int qi = c * 32 + e;
           const bool valid = kvalid && qi < qrows && (!p.causal || key <= i0 + qi);
-          const float pv = valid ? exp2f(sv[e] * p.scale_log2 - L[qi]) : 0.f;
+          const float pv = valid ? exp2_approx(__uint_as_float(sr[e]) * p.scale_log2 - L[qi]) : 0.f;
           sv[e] = pv;
-          dv[e] = valid ? pv * (dv[e] - Dd[qi]) : 0.f;
+          dv[e] = valid ? pv * (__uint_as_float(dr[e]) - Dd[qi]) : 0.f;
         }
         const uint32_t sub = (c >> 1) * kTile + kr * 128;
 #pragma unroll
@@ -758,7 +775,7 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
     }
   } else {
     // ---------------- dQ / dK / dV epilogue: one row per thread ----------------
-    const int t = threadIdx.x - 192;
+    const int t = threadIdx.x - 32 * (2 + kSoftWarps);
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
@@ -839,17 +856,21 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
 //   warp 1     TMEM owner; one lane issues S_j = Q K_j^T (into one of two
 //              TMEM buffers, so S_{j+1} overlaps the softmax of block j) and
 //              O' += P_j V_j
-//   warps 2-5  one query row per thread: P_j from TMEM -> bf16 -> shared;
-//              at the end D from O' (TMEM) and dO (shared)
+//   warps 2-9  one query row and 64 of the 128 keys per thread: P_j from
+//              TMEM -> bf16 -> shared; at the end D from O' (TMEM) and dO
+//              (shared), each half of the row's columns summed separately
 // TMEM columns: S buffers 0-127 and 128-255, O' 256-319.
 namespace tcdprep {
 constexpr int kQ = 128, kK = 128, kD = 64;
 constexpr uint32_t kTile = 16384;
-constexpr uint32_t OFF_Q = 0, OFF_DO = kTile, OFF_K = 2 * kTile, OFF_V = 4 * kTile, OFF_P = 6 * kTile,
-                   OFF_BAR = 10 * kTile;
-constexpr size_t kSmem = 1024 + OFF_BAR + 256;
+constexpr int kKV = 3;                                   // K/V stages
+constexpr uint32_t OFF_Q = 0, OFF_DO = kTile, OFF_K = 2 * kTile, OFF_P = OFF_K + kKV * 2 * kTile,
+                   OFF_BAR = OFF_P + 4 * kTile;
+constexpr uint32_t OFF_PART = OFF_BAR + 256;              // [2][128] f32 partial dot products
+constexpr size_t kSmem = 1024 + OFF_PART + 1024;
 constexpr uint32_t TM_S = 0, TM_O = 256;
-constexpr int kThreads = 192;
+constexpr int kSoftWarps = 8;                                // two per TMEM lane quadrant
+constexpr int kThreads = 32 * (2 + kSoftWarps);
 }  // namespace tcdprep
 
 struct DprepTc {
@@ -883,24 +904,26 @@ __global__ void __launch_bounds__(tcdprep::kThreads, 1)
   const int qrows = min(kQ, len - i0);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-  const uint32_t b_q = smem_u32(bars + 0), b_kvfull = smem_u32(bars + 1), b_kvempty = smem_u32(bars + 3),
-                 b_sfull = smem_u32(bars + 5), b_pfull = smem_u32(bars + 7), b_pempty = smem_u32(bars + 8),
-                 b_ofull = smem_u32(bars + 10), b_kvready = smem_u32(bars + 11);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+  // kv_full/kv_empty/kv_ready: one per K/V stage; s_full/p_empty: one per S / P buffer
+  const uint32_t b_q = smem_u32(bars + 0), b_kvfull = smem_u32(bars + 1), b_kvempty = smem_u32(bars + 4),
+                 b_kvready = smem_u32(bars + 7), b_sfull = smem_u32(bars + 10), b_pempty = smem_u32(bars + 12),
+                 b_pfull = smem_u32(bars + 14), b_ofull = smem_u32(bars + 15);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(b_q, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kKV; ++s) {
       mbar_init(b_kvfull + 8 * s, 1);
       mbar_init(b_kvempty + 8 * s, 1);
+      mbar_init(b_kvready + 8 * s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(b_sfull + 8 * s, 1);
       mbar_init(b_pempty + 8 * s, 1);
     }
-    mbar_init(b_pfull, 128);
+    mbar_init(b_pfull, 32 * kSoftWarps);
     mbar_init(b_ofull, 1);
-    mbar_init(b_kvready, 1);
-    mbar_init(b_kvready + 8, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -916,7 +939,7 @@ __global__ void __launch_bounds__(tcdprep::kThreads, 1)
     // TMA producer (lane 0); the whole warp zeroes K / V rows past the
     // sequence before the MMAs read a block (0 * non-finite would leak)
     auto issue = [&](int j) -> bool {
-      const int st = j & 1, use = j >> 1;
+      const int st = j % kKV, use = j / kKV;
       if (!mbar_wait(b_kvempty + 8 * st, (use & 1) ^ 1, abort_flag, p.st, 40)) return false;
       mbar_expect_tx(b_kvfull + 8 * st, 2 * kTile);
       tma_load_2d(sbase + OFF_K + st * 2 * kTile, &tmK, b_kvfull + 8 * st, hk * kD, s0 + j * kK);
@@ -931,11 +954,14 @@ __global__ void __launch_bounds__(tcdprep::kThreads, 1)
       ok = issue(0) ? 1 : 0;
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    // Block j is released to the MMA before block j+1 is requested: requesting
-    // j+1 waits for the P V of block j-1, which the MMA issues only after
-    // S_j, i.e. after block j is released.
+    // With three stages block j+1 can be requested before block j is
+    // released: the request waits for the P V of block j-2, which the MMA
+    // issues once block j-1 is released.
     for (int j = 0; ok && j < nj; ++j) {
-      const int st = j & 1, use = j >> 1;
+      const int st = j % kKV, use = j / kKV;
+      int nxt = 1;
+      if (lane == 0 && j + 1 < nj) nxt = issue(j + 1) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, nxt, 0)) break;
       if (!mbar_wait(b_kvfull + 8 * st, use & 1, &no_abort, p.st, 47)) break;
       const int krows = min(kK, len - j * kK);
       if (krows < kK) {
@@ -949,9 +975,6 @@ __global__ void __launch_bounds__(tcdprep::kThreads, 1)
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_kvready + 8 * st);
-      int nxt = 1;
-      if (lane == 0 && j + 1 < nj) nxt = issue(j + 1) ? 1 : 0;
-      if (!__shfl_sync(0xffffffffu, nxt, 0)) break;
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -960,36 +983,37 @@ __global__ void __launch_bounds__(tcdprep::kThreads, 1)
       bool ok = mbar_wait(b_q, 0, abort_flag, p.st, 41);
       // O' += P_{jj} V_{jj} for the block whose P the softmax has finished
       auto pv = [&](int jj) -> bool {
-        const int st = jj & 1;
+        const int kst = jj % kKV, pb = jj & 1;
         if (!mbar_wait(b_pfull, jj & 1, abort_flag, p.st, 42)) return false;
         fence_after();
-        const uint32_t sv = sbase + OFF_K + st * 2 * kTile + kTile;
+        const uint32_t sv = sbase + OFF_K + kst * 2 * kTile + kTile;
 #pragma unroll
         for (int kk = 0; kk < kK / 16; ++kk) {
-          const uint32_t pa = sbase + OFF_P + st * 2 * kTile + (kk >> 2) * kTile + (kk & 3) * 32;
+          const uint32_t pa = sbase + OFF_P + pb * 2 * kTile + (kk >> 2) * kTile + (kk & 3) * 32;
           mma_bf16(tbase + TM_O, sdesc(pa, 16, 1024), sdesc(sv + kk * 2048, 8192, 1024), id_o, (jj > 0) || (kk > 0));
         }
-        mma_commit(b_kvempty + 8 * st);
-        mma_commit(b_pempty + 8 * st);
+        mma_commit(b_kvempty + 8 * kst);
+        mma_commit(b_pempty + 8 * pb);
         return true;
       };
       for (int j = 0; ok && j < nj; ++j) {
-        const int st = j & 1, use = j >> 1;
-        if (!mbar_wait(b_kvready + 8 * st, use & 1, abort_flag, p.st, 43)) { ok = false; break; }
+        const int kst = j % kKV, kuse = j / kKV, sb = j & 1;
+        if (!mbar_wait(b_kvready + 8 * kst, kuse & 1, abort_flag, p.st, 43)) { ok = false; break; }
         fence_after();
-        const uint32_t sk = sbase + OFF_K + st * 2 * kTile;
+        const uint32_t sk = sbase + OFF_K + kst * 2 * kTile;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
-          mma_bf16(tbase + TM_S + st * 128, sdesc(sbase + OFF_Q + kk * 32, 16, 1024), sdesc(sk + kk * 32, 16, 1024),
+          mma_bf16(tbase + TM_S + sb * 128, sdesc(sbase + OFF_Q + kk * 32, 16, 1024), sdesc(sk + kk * 32, 16, 1024),
                    id_s, kk > 0);
-        mma_commit(b_sfull + 8 * st);
+        mma_commit(b_sfull + 8 * sb);
         if (j > 0 && !pv(j - 1)) { ok = false; break; }
       }
       if (ok && pv(nj - 1)) mma_commit(b_ofull);
     }
   } else {
-    // softmax: one query row per thread
+    // softmax: one query row, 64 of the 128 keys of a block per thread
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const float L = (r < qrows) ? p.lse2[(long long)h * p.M + s0 + i0 + r] : 0.f;
@@ -1000,15 +1024,19 @@ __global__ void __launch_bounds__(tcdprep::kThreads, 1)
       if (j >= 2 && !mbar_wait(b_pempty + 8 * st, (use - 1) & 1, &no_abort, p.st, 45)) { ok = false; break; }
       fence_after();
       const int j0 = j * kK;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      uint32_t sr[64];
+      tmem_ld32_async(tbase + lane_off + TM_S + st * 128 + half * 64, sr);
+      tmem_ld32_async(tbase + lane_off + TM_S + st * 128 + half * 64 + 32, sr + 32);
+      tmem_wait_ld();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * half + cc;
         float sv[32];
-        tmem_ld32(tbase + lane_off + TM_S + st * 128 + c * 32, sv);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int kj = j0 + c * 32 + e;
           const bool valid = r < qrows && kj < len && (!p.causal || kj <= i0 + r);
-          sv[e] = valid ? exp2f(sv[e] * p.scale_log2 - L) : 0.f;
+          sv[e] = valid ? exp2_approx(__uint_as_float(sr[cc * 32 + e]) * p.scale_log2 - L) : 0.f;
         }
         const uint32_t sub = st * 2 * kTile + (c >> 1) * kTile + r * 128;
 #pragma unroll
@@ -1021,21 +1049,26 @@ __global__ void __launch_bounds__(tcdprep::kThreads, 1)
       fence_async_smem();
       mbar_arrive(b_pfull);
     }
+    float* part = reinterpret_cast<float*>(sm + OFF_PART);
+    float d = 0.f;
     if (ok && mbar_wait(b_ofull, 0, &no_abort, p.st, 46)) {
       fence_after();
-      float o[64];
-      tmem_ld32(tbase + lane_off + TM_O, o);
-      tmem_ld32(tbase + lane_off + TM_O + 32, o + 32);
-      float d = 0.f;
+      float o[32];
+      tmem_ld32(tbase + lane_off + TM_O + half * 32, o);
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
+      for (int g = 0; g < 4; ++g) {
         float x[8];
-        unpack8(*reinterpret_cast<const uint4*>(sm + OFF_DO + r * 128 + ((g ^ (r & 7)) * 16)), x);
+        const int chunk = half * 4 + g;
+        unpack8(*reinterpret_cast<const uint4*>(sm + OFF_DO + r * 128 + ((chunk ^ (r & 7)) * 16)), x);
 #pragma unroll
         for (int e = 0; e < 8; ++e) d += x[e] * o[8 * g + e];
       }
-      if (r < qrows) p.Dvec[(long long)h * p.M + s0 + i0 + r] = d;
+    } else {
+      ok = false;
     }
+    part[half * 128 + r] = d;
+    named_bar(1, 32 * kSoftWarps);
+    if (ok && half == 0 && r < qrows) p.Dvec[(long long)h * p.M + s0 + i0 + r] = d + part[128 + r];
   }
   fence_before();
   __syncthreads();

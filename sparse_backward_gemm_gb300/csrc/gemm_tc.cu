@@ -38,6 +38,12 @@ struct TcParams {
   long long c_rows;
   float* partial;    // stream-K: [2 * gridDim.x][BM][BN] f32 partial tiles (null: whole tiles only)
   int* counters;     // stream-K: per-tile arrival counts, zero on entry and left zero
+  int split_mode;    // 0 whole tiles, 1 stream-K, 2 hybrid (see Split)
+  int epi;           // TcEpilogue
+  const __nv_bfloat16* aux;
+  long long aux_ld;
+  const int32_t* idx;
+  int aux_rows;
   DevStatus* st;
 };
 
@@ -59,61 +65,134 @@ struct TcCfg {
   static constexpr size_t kSmem = 1024 + kStages * kStageBytes + 256;
 };
 
-// Work split.  Stream-K (partial != null): the num_tiles * num_kb (tile,
-// k-slice) iterations are cut into gridDim.x equal contiguous ranges, so every
-// CTA gets the same work whatever the tile count; a tile cut between CTAs is
-// finished by whichever of them arrives last, summing the partial tiles in
-// CTA order (deterministic).  Otherwise whole tiles round-robin.
+// Work split.
+//   whole tiles  (mode 0): tiles round-robin over the CTAs.
+//   stream-K     (mode 1): the num_tiles * num_kb (tile, k-slice) iterations
+//                are cut into equal contiguous ranges, one per CTA.
+//   hybrid       (mode 2): whole tiles round-robin for all but the last full
+//                wave, stream-K over the remaining tiles (between one and two
+//                waves' worth), so the tail wave is as full as the others
+//                while the bulk keeps the round-robin tile order.
+// A tile cut between CTAs is finished by whichever of them arrives last,
+// summing the partial tiles in CTA order (deterministic).
 struct Split {
   int m_tiles, num_tiles, num_kb;
-  long long total;
+  int dp_tiles;        // tiles handled whole, round-robin, first
+  long long total;     // stream-K iterations (over tiles dp_tiles..num_tiles-1)
   bool sk;
-  int G;   // CTAs sharing the work: min(grid, total), so that no range is empty
-  __device__ long long begin(int c) const { return sk ? (long long)c * total / G : 0; }
-  // the CTA whose range holds iteration x
+  int G;               // CTAs sharing the stream-K part: min(grid, total), no empty range
+  __device__ long long begin(int c) const { return (long long)c * total / G; }
+  // the CTA whose range holds stream-K iteration x
   __device__ int owner(long long x) const { return (int)(((x + 1) * (long long)G - 1) / total); }
-  __device__ int slot(int c, int t) const { return 2 * c + (t == (int)(begin(c) / num_kb) ? 0 : 1); }
+  __device__ int slot(int c, int t) const {
+    return 2 * c + (t == dp_tiles + (int)(begin(c) / num_kb) ? 0 : 1);
+  }
+  __device__ void init(int mode, bool have_scratch) {
+    total = 0;
+    sk = false;
+    dp_tiles = num_tiles;
+    G = gridDim.x;
+    if (!have_scratch || mode == 0 || num_kb == 0) return;
+    const int grid = gridDim.x;
+    const int waves = num_tiles / grid, rem = num_tiles % grid;
+    if (mode == 2) {
+      if (rem == 0) return;
+      dp_tiles = waves >= 1 ? (waves - 1) * grid : 0;
+    } else {
+      dp_tiles = 0;
+    }
+    total = (long long)(num_tiles - dp_tiles) * num_kb;
+    sk = total > 0;
+    G = (int)(total < (long long)grid ? total : (long long)grid);
+  }
 };
 
 // Iterates this CTA's segments: (tile, first k-slice, end k-slice).
 struct SegIter {
   const Split& sp;
-  long long it, end;   // stream-K
-  int tile;            // whole-tile mode
+  int tile;            // whole-tile phase
+  long long it, end;   // stream-K phase (relative iterations)
   __device__ SegIter(const Split& s) : sp(s) {
-    if (sp.sk) {
-      if ((int)blockIdx.x < sp.G) {
-        it = sp.begin(blockIdx.x);
-        end = (long long)(blockIdx.x + 1) * sp.total / sp.G;
-      } else {
-        it = end = 0;
-      }
+    tile = blockIdx.x;
+    if (sp.sk && (int)blockIdx.x < sp.G) {
+      it = sp.begin(blockIdx.x);
+      end = (long long)(blockIdx.x + 1) * sp.total / sp.G;
     } else {
-      tile = blockIdx.x;
+      it = end = 0;
     }
   }
   __device__ bool next(int& t, int& k0, int& k1) {
-    if (sp.sk) {
-      if (it >= end) return false;
-      t = (int)(it / sp.num_kb);
-      k0 = (int)(it % sp.num_kb);
-      const long long lim = k0 + (end - it);
-      k1 = lim < sp.num_kb ? (int)lim : sp.num_kb;
-      it += k1 - k0;
+    if (tile < sp.dp_tiles) {
+      t = tile;
+      k0 = 0;
+      k1 = sp.num_kb;
+      tile += gridDim.x;
       return true;
     }
-    if (tile >= sp.num_tiles) return false;
-    t = tile;
-    k0 = 0;
-    k1 = sp.num_kb;
-    tile += gridDim.x;
+    if (it >= end) return false;
+    t = sp.dp_tiles + (int)(it / sp.num_kb);
+    k0 = (int)(it % sp.num_kb);
+    const long long lim = k0 + (end - it);
+    k1 = lim < sp.num_kb ? (int)lim : sp.num_kb;
+    it += k1 - k0;
     return true;
   }
 };
 
+__device__ __forceinline__ float sigmoid_dev(float x) { return 1.f / (1.f + __expf(-x)); }
+__device__ __forceinline__ float gelu_tanh_grad_dev(float x) {
+  const float c = 0.7978845608028654f, a = 0.044715f;
+  const float t = tanhf(c * (x + a * x * x * x));
+  return 0.5f * (1.f + t) + 0.5f * x * (1.f - t * t) * c * (1.f + 3.f * a * x * x);
+}
+
 // Store 32 consecutive columns of one output row (bf16 or f32, optional
-// accumulate into C, zero rows past the kept count up to the padding).
+// accumulate into C, zero rows past the kept count up to the padding, fused
+// activation backward).
 __device__ __forceinline__ void store32(const TcParams& p, int row, int col, bool row_ok, float* v) {
+  if (p.epi != kEpiStore) {
+    // activation backward on the kept row: the saved pre-activations are read
+    // through the kept-row index (padding rows stay zero)
+    const int N = p.N;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.C) + (long long)row * p.ldc + col;
+    float o1[32], o2[32];
+    if (row_ok) {
+      const int t = p.idx[row];
+      const bool in = (unsigned)t < (unsigned)p.aux_rows;
+      if (!in) report_error(p.st, kErrBadIndex, 10);
+      const __nv_bfloat16* a = p.aux + (long long)(in ? t : 0) * p.aux_ld + col;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float x[8], u[8];
+        if (col + 8 * g + 8 <= N) {
+          unpack8(*reinterpret_cast<const uint4*>(a + 8 * g), x);
+          if (p.epi == kEpiSwiGLU) unpack8(*reinterpret_cast<const uint4*>(a + N + 8 * g), u);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float d = in ? v[8 * g + e] : 0.f;
+          if (p.epi == kEpiSwiGLU) {
+            const float sg = sigmoid_dev(x[e]);
+            o1[8 * g + e] = d * u[e] * sg * (1.f + x[e] * (1.f - sg));
+            o2[8 * g + e] = d * x[e] * sg;
+          } else {
+            o1[8 * g + e] = d * gelu_tanh_grad_dev(x[e]);
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o1[i] = o2[i] = 0.f;
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      if (col + 8 * g + 8 <= N) {
+        *reinterpret_cast<uint4*>(out + 8 * g) = pack8(o1 + 8 * g);
+        if (p.epi == kEpiSwiGLU) *reinterpret_cast<uint4*>(out + N + 8 * g) = pack8(o2 + 8 * g);
+      }
+    }
+    return;
+  }
   if (p.c_bf16) {
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.C) + (long long)row * p.ldc + col;
 #pragma unroll
@@ -161,9 +240,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   sp.m_tiles = (M + BM - 1) / BM;
   sp.num_tiles = sp.m_tiles * ((p.N + BN - 1) / BN);
   sp.num_kb = (K + BK - 1) / BK;
-  sp.total = (long long)sp.num_tiles * sp.num_kb;
-  sp.sk = p.partial != nullptr && sp.total > 0;
-  sp.G = (int)(sp.total < (long long)gridDim.x ? sp.total : (long long)gridDim.x);
+  sp.init(p.split_mode, p.partial != nullptr);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -303,7 +380,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool row_ok = row < M;
       const bool row_zero = !row_ok && p.zero_pad && row < padded_rows(M, p.c_rows);
       const uint32_t tcol = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      if (!sp.sk || (k0 == 0 && k1 == sp.num_kb)) {
+      if (k0 == 0 && k1 == sp.num_kb) {
         // whole tile: straight to the output
         for (int c = 0; c < BN; c += 32) {
           float v[32];
@@ -331,7 +408,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_arrive(tempty0 + 8 * acc);
         __threadfence();
         named_bar(1, 128);
-        const long long x0 = (long long)t * sp.num_kb;
+        const long long x0 = (long long)(t - sp.dp_tiles) * sp.num_kb;
         const int c_first = sp.owner(x0), c_last = sp.owner(x0 + sp.num_kb - 1);
         if (et == 0) {
           const int old = atomicAdd(p.counters + t, 1);
@@ -460,14 +537,20 @@ cudaError_t launch_tc_gemm(const Ctx& c, const TcGemm& g) {
                            : make_map(&mb, g.B, g.K, g.b_rows, g.ldb, bn));
   if (!ok) return cudaErrorInvalidValue;
   const long long max_tiles = ((long long)(g.M + BM - 1) / BM) * ((g.N + bn - 1) / bn);
-  // COLLIDER_GEMM_STREAMK=0 turns the stream-K split off (whole tiles only)
-  static const int sk_env = [] {
+  // Work split.  Measured on the block shapes: whole tiles keep the operands'
+  // L2 locality and win except for long reductions over a static K (>= 128
+  // k-slices), where stream-K's even split pays for its fix-up.
+  // COLLIDER_GEMM_STREAMK=0/1/2 forces whole tiles / stream-K / hybrid.
+  static const int split_env = [] {
     const char* e = getenv("COLLIDER_GEMM_STREAMK");
-    return e ? atoi(e) : 1;
+    return e ? atoi(e) : -1;
   }();
-  const bool sk = sk_env != 0 && g.partial && g.counters && max_tiles <= g.counter_cap;
+  int split = split_env;
+  if (split < 0) split = (g.dyn != 2 && g.K / BK >= 128) ? 1 : 0;
+  const bool sk = split != 0 && g.partial && g.counters && max_tiles <= g.counter_cap;
   TcParams p{g.M, g.N, g.K, g.dyn, g.n_kept, g.C, g.ldc, g.c_bf16, g.accumulate, g.zero_pad,
-             g.c_rows > 0 ? g.c_rows : g.M, sk ? g.partial : nullptr, sk ? g.counters : nullptr, c.st};
+             g.c_rows > 0 ? g.c_rows : g.M, sk ? g.partial : nullptr, sk ? g.counters : nullptr,
+             split, g.epi, g.aux, g.aux_ld, g.idx, g.aux_rows, c.st};
   prof_begin(c, "tc_gemm", g.M, g.N, g.K, g.dyn);
   cudaError_t e;
   const int key = (bn == 256 ? 4 : 0) | (g.a_mn_major ? 2 : 0) | (g.b_mn_major ? 1 : 0);
