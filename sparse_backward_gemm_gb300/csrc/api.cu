@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -589,6 +590,60 @@ void layer_carve(Carver& cv, const collider_layer_desc* d, LayerBufs* L) {
   L->sk_counters = cv.take<int>(L->sk_cap);
 }
 
+// The weight-gradient GEMMs of a block depend on nothing the block computes
+// after their inputs, so they run on a second stream (one per host thread and
+// device), forked from and joined back into the caller's stream with events:
+// they fill the SMs the input-gradient chain leaves idle (GEMM tail waves,
+// attention, row kernels).  No host synchronisation.
+struct Side {
+  cudaStream_t s = nullptr;
+  cudaEvent_t ev[8] = {};
+};
+thread_local Side g_side[64];
+
+// COLLIDER_SIDE_STREAM=0 keeps every launch on the caller's stream (used to
+// time kernels one at a time); read at every call.
+bool side_enabled() {
+  const char* e = getenv("COLLIDER_SIDE_STREAM");
+  return !(e && e[0] == '0');
+}
+
+collider_status side_ctx(const Ctx& c, Ctx* c2, Side** sd) {
+  if (!side_enabled()) {
+    *c2 = c;
+    *sd = nullptr;
+    return COLLIDER_OK;
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  Side& S = g_side[dev & 63];
+  if (!S.s) {
+    e = cudaStreamCreateWithFlags(&S.s, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return cuda_fail(e, "side stream");
+    for (auto& ev : S.ev) {
+      e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+      if (e != cudaSuccess) return cuda_fail(e, "side stream event");
+    }
+  }
+  *c2 = c;
+  c2->stream = S.s;
+  *sd = &S;
+  return COLLIDER_OK;
+}
+// side stream waits for everything enqueued on the caller's stream so far
+cudaError_t fork_side(const Ctx& c, Side* S, int k) {
+  if (!S) return cudaSuccess;
+  cudaError_t e = cudaEventRecord(S->ev[k], c.stream);
+  return e == cudaSuccess ? cudaStreamWaitEvent(S->s, S->ev[k], 0) : e;
+}
+// caller's stream waits for everything enqueued on the side stream so far
+cudaError_t join_side(const Ctx& c, Side* S, int k) {
+  if (!S) return cudaSuccess;
+  cudaError_t e = cudaEventRecord(S->ev[k], S->s);
+  return e == cudaSuccess ? cudaStreamWaitEvent(c.stream, S->ev[k], 0) : e;
+}
+
 // stream-K scratch shared by the GEMMs of one call (they run in stream order)
 thread_local float* g_sk_partial = nullptr;
 thread_local int* g_sk_counters = nullptr;
@@ -613,10 +668,11 @@ cudaError_t gemm_dx(const Ctx& c, int M, int N, int K, const void* A, const void
 }
 
 // dW [Kin, Nout] f32 = X_k^T dY_k, X_k [Mk, Kin], dY_k [Mk, Nout] (both COMPACT, zero-padded)
+// (runs on the side stream, concurrently with the caller's stream: it must not
+// use the shared stream-K scratch)
 cudaError_t gemm_dw(const Ctx& c, int M, int Kin, int Nout, const void* Xk, long long ldx, const void* dYk,
                     long long ldy, float* dW, const int32_t* n_kept) {
   TcGemm g{};
-  g.partial = g_sk_partial; g.counters = g_sk_counters; g.counter_cap = g_sk_cap;
   g.M = Kin; g.N = Nout; g.K = M;
   g.A = Xk; g.lda = ldx; g.a_mn_major = 1; g.a_rows = pad128(M);
   g.B = dYk; g.ldb = ldy; g.b_mn_major = 1; g.b_rows = pad128(M);
@@ -638,6 +694,12 @@ collider_status layer_bwd_impl(const Ctx& c, const collider_layer_desc* d, const
   g_sk_counters = L.sk_counters;
   g_sk_cap = L.sk_cap;
   CK(cudaMemsetAsync(L.sk_counters, 0, L.sk_cap * sizeof(int), c.stream));
+  Ctx cs;
+  Side* side = nullptr;
+  {
+    collider_status st = side_ctx(c, &cs, &side);
+    if (st != COLLIDER_OK) return st;
+  }
 
   // 1. gather the kept rows of dOut and of the saved GEMM operands
   {
@@ -671,12 +733,14 @@ collider_status layer_bwd_impl(const Ctx& c, const collider_layer_desc* d, const
   // 2. MLP
   const __nv_bfloat16* dres = L.dout_k;   // gradient flowing along the residual into the attention half
   if (llama) {
+    CK(fork_side(c, side, 0));
+    CK(gemm_dw(cs, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept));              // dW_down = s^T dOut
     CK(gemm_dx(c, M, F, D, L.dout_k, w->w_down, L.ds_k, 1, 0, n_kept));               // ds = dOut W_down^T
-    CK(gemm_dw(c, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept));               // dW_down = s^T dOut
     CK(launch_swiglu_bwd(c, L.ds_k, 1, F, static_cast<const __nv_bfloat16*>(sv->up), L.dgu_k, M, pad128(M), idx,
                          n_kept));
+    CK(fork_side(c, side, 1));
+    CK(gemm_dw(cs, M, D, Nup, L.b_k, D, L.dgu_k, Nup, g->dw_up, n_kept));             // dW_up = b^T dgu
     CK(gemm_dx(c, M, D, Nup, L.dgu_k, w->w_up, L.db_k, 0, 0, n_kept));                // db = dgu W_up^T
-    CK(gemm_dw(c, M, D, Nup, L.b_k, D, L.dgu_k, Nup, g->dw_up, n_kept));              // dW_up = b^T dgu
     NormBwdArgs nb{};
     nb.layer_norm = 0; nb.M = M; nb.D = D;
     nb.dy1 = L.db_k; nb.res = L.dout_k; nb.res_ld = D;
@@ -686,21 +750,24 @@ collider_status layer_bwd_impl(const Ctx& c, const collider_layer_desc* d, const
     CK(launch_norm_bwd(c, nb));                                                          // dh = dOut + norm2'
     dres = L.dh_k;
   } else {
+    CK(fork_side(c, side, 0));
+    CK(gemm_dw(cs, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept));              // dW2 = gelu(f1)^T dOut
     CK(gemm_dx(c, M, F, D, L.dout_k, w->w_down, L.ds_k, 1, 0, n_kept));               // df2 = dOut W2^T
-    CK(gemm_dw(c, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept));               // dW2 = gelu(f1)^T dOut
     if (d->mlp_bias && g->db_down)
       CK(launch_colsum(c, L.dout_k, 1, D, M, D, nullptr, n_kept, L.col_part, g->db_down));
     CK(launch_gelu_bwd(c, L.ds_k, 1, F, static_cast<const __nv_bfloat16*>(sv->up), L.dgu_k, M, pad128(M), idx,
                        n_kept));
-    CK(gemm_dw(c, M, D, F, L.a_k, D, L.dgu_k, F, g->dw_up, n_kept));                  // dW1 = a^T df1
+    CK(fork_side(c, side, 1));
+    CK(gemm_dw(cs, M, D, F, L.a_k, D, L.dgu_k, F, g->dw_up, n_kept));                 // dW1 = a^T df1
     if (d->mlp_bias && g->db_up)
       CK(launch_colsum(c, L.dgu_k, 1, F, M, F, nullptr, n_kept, L.col_part, g->db_up));
     CK(gemm_dx(c, M, D, F, L.dgu_k, w->w_up, L.da_k, 0, 0, n_kept));                  // da = df1 W1^T
   }
 
   // 3. attention output projection
+  CK(fork_side(c, side, 2));
+  CK(gemm_dw(cs, M, Hd, D, L.o_k, Hd, dres, D, g->dw_o, n_kept));                     // dW_o = o^T dh
   CK(gemm_dx(c, M, Hd, D, dres, w->w_o, L.do_k, 1, 0, n_kept));                       // do = dh W_o^T
-  CK(gemm_dw(c, M, Hd, D, L.o_k, Hd, dres, D, g->dw_o, n_kept));                      // dW_o = o^T dh
   if (d->out_bias && g->db_o) CK(launch_colsum(c, dres, 1, D, M, D, nullptr, n_kept, L.col_part, g->db_o));
 
   // 4. filtered attention backward (+ RoPE backward) straight into dqkv_k
@@ -721,9 +788,10 @@ collider_status layer_bwd_impl(const Ctx& c, const collider_layer_desc* d, const
   }
 
   // 5. QKV projection
-  CK(gemm_dw(c, M, D, Nqkv, L.a_k, D, L.dqkv_k, Nqkv, g->dw_qkv, n_kept));           // dW_qkv = a^T dqkv
+  CK(fork_side(c, side, 3));
+  CK(gemm_dw(cs, M, D, Nqkv, L.a_k, D, L.dqkv_k, Nqkv, g->dw_qkv, n_kept));          // dW_qkv = a^T dqkv
   if (d->qkv_bias && g->db_qkv)
-    CK(launch_colsum(c, L.dqkv_k, 1, Nqkv, M, Nqkv, nullptr, n_kept, L.col_part, g->db_qkv));
+    CK(launch_colsum(cs, L.dqkv_k, 1, Nqkv, M, Nqkv, nullptr, n_kept, L.col_part, g->db_qkv));
   CK(gemm_dx(c, M, D, Nqkv, L.dqkv_k, w->w_qkv, L.da_k, 0, llama ? 0 : 1, n_kept));  // da (+)= dqkv W_qkv^T
 
   // 6. input norm backward + residual, then back to FULL rows if asked
@@ -741,6 +809,7 @@ collider_status layer_bwd_impl(const Ctx& c, const collider_layer_desc* d, const
   if (dx_full)
     CK(launch_scatter(c, reinterpret_cast<const char*>(L.dx_k), (long long)D * 2, static_cast<char*>(g->dx),
                       (long long)D * 2, D * 2, M, idx, n_kept));
+  CK(join_side(c, side, 4));   // the weight gradients are done when the caller's stream is
   return COLLIDER_OK;
 }
 
@@ -877,7 +946,14 @@ extern "C" collider_status collider_stack_bwd(const collider_layer_desc* d, int 
                 D * 2, 0};
     CK(launch_gather(c, &j, 1, M, pad128(M), idx, n_kept));
   }
-  CK(gemm_dw(c, M, D, V, S.y_k, D, S.dz_k, V, dw_lm, n_kept));            // dW_lm = y^T dz
+  {
+    Ctx cs;
+    Side* side = nullptr;
+    s = side_ctx(c, &cs, &side);
+    if (s != COLLIDER_OK) return s;
+    CK(fork_side(c, side, 5));
+    CK(gemm_dw(cs, M, D, V, S.y_k, D, S.dz_k, V, dw_lm, n_kept));         // dW_lm = y^T dz (side stream;
+  }                                                                        // joined by the last block)
   CK(gemm_dx(c, M, D, V, S.dz_k, w_lm, S.dyf_k, 0, 0, n_kept));           // dy = dz W_lm^T
   {
     NormBwdArgs nb{};

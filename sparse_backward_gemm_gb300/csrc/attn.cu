@@ -122,12 +122,21 @@ __global__ void attn_prep_kernel(AttnK p, int DH, float rope_base, float2* rope)
     }
   }
   if (p.rot_half > 0) {
+    // theta_i = base^(-2i/r) once per block in fp64; the angle pos * theta_i
+    // and its reduction mod 2 pi in fp64, then sin / cos of the reduced angle
+    __shared__ double inv[256];
     const int rd = 2 * p.rot_half;
+    for (int i = threadIdx.x; i < p.rot_half && i < 256; i += blockDim.x)
+      inv[i] = pow((double)rope_base, -(2.0 * i) / (double)rd);
+    __syncthreads();
+    const double two_pi = 6.283185307179586476925;
     for (long long e = tid; e < (long long)p.T * p.rot_half; e += stride) {
       const int pos = (int)(e / p.rot_half), i = (int)(e % p.rot_half);
-      const double inv = pow((double)rope_base, -(2.0 * i) / (double)rd);
-      const double ang = (double)pos * inv;
-      rope[e] = make_float2((float)cos(ang), (float)sin(ang));
+      const double ang = (double)pos * inv[i];
+      const float red = (float)(ang - rint(ang / two_pi) * two_pi);
+      float sn, cs;
+      sincosf(red, &sn, &cs);
+      rope[e] = make_float2(cs, sn);
     }
   }
 }
@@ -454,23 +463,37 @@ __global__ void __launch_bounds__(128) attn_main_kernel(AttnK p) {
 // where asked, to bf16; zero rows n_kept..pad of dQ, dK, dV.
 // One thread per (row, head, column pair): the rotary pair (i, i + r/2) for
 // i < r/2, else two adjacent pass-through columns.
-__device__ __forceinline__ void finalize_pair(const float* a, __nv_bfloat16* o, int c, int DH, int rh,
+// One unit of work = 8 columns of one (row, head): the rotary pairs
+// (c..c+7, c+r/2..c+r/2+7) for c < r/2, else 8 pass-through columns.
+__device__ __forceinline__ void load8f(const float* a, float* v) {
+  const float4 x = *reinterpret_cast<const float4*>(a), y = *reinterpret_cast<const float4*>(a + 4);
+  v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w; v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+}
+
+__device__ __forceinline__ void finalize_unit(const float* a, __nv_bfloat16* o, int u, int rh,
                                               const float2* rope_row, float scale) {
-  const int per_head = DH / 2;
-  if (rh == 0) {
-    o[c] = f2bf(a[c] * scale);
-    o[c + per_head] = f2bf(a[c + per_head] * scale);
-  } else if (c < rh) {
-    const float2 cs = rope_row[c];
-    const float d1 = a[c] * scale, d2 = a[c + rh] * scale;
-    o[c] = f2bf(d1 * cs.x + d2 * cs.y);
-    o[c + rh] = f2bf(d2 * cs.x - d1 * cs.y);
-  } else {
-    const int cc = 2 * rh + 2 * (c - rh);
-    if (cc < DH) {
-      o[cc] = f2bf(a[cc] * scale);
-      o[cc + 1] = f2bf(a[cc + 1] * scale);
+  const int pairs = rh / 8;
+  if (u < pairs) {
+    const int c = 8 * u;
+    float d1[8], d2[8], o1[8], o2[8];
+    load8f(a + c, d1);
+    load8f(a + c + rh, d2);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float2 cs = rope_row[c + e];
+      const float x1 = d1[e] * scale, x2 = d2[e] * scale;
+      o1[e] = x1 * cs.x + x2 * cs.y;
+      o2[e] = x2 * cs.x - x1 * cs.y;
     }
+    *reinterpret_cast<uint4*>(o + c) = pack8(o1);
+    *reinterpret_cast<uint4*>(o + c + rh) = pack8(o2);
+  } else {
+    const int c = 2 * rh + 8 * (u - pairs);
+    float d[8];
+    load8f(a + c, d);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) d[e] *= scale;
+    *reinterpret_cast<uint4*>(o + c) = pack8(d);
   }
 }
 
@@ -480,37 +503,44 @@ __global__ void attn_finalize_kernel(AttnK p, int DH) {
   const int rh = p.rot_half;
   const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   const long long stride = (long long)gridDim.x * blockDim.x;
-  const int per_head = DH / 2;
-  const long long tq = (long long)nk * p.H * per_head;
-  const long long tk = p.kv_acc ? (long long)nk * p.Hkv * per_head : 0;
-  for (long long e = tid; e < tq + 2 * tk; e += stride) {
+  const int units = rh / 8 + (DH - 2 * rh) / 8;            // per (row, head)
+  const long long tq = (long long)nk * p.H * units;
+  const long long tk = p.kv_acc ? (long long)nk * p.Hkv * units : 0;
+  const int vunits = DH / 8;                                // dV: no rotation
+  const long long tv = p.kv_acc ? (long long)nk * p.Hkv * vunits : 0;
+  for (long long e = tid; e < tq + tk + tv; e += stride) {
     long long f = e;
     int which = 0;   // 0 dQ, 1 dK, 2 dV
-    if (f >= tq) { f -= tq; which = 1 + (int)(f / tk); f %= tk; }
+    if (f >= tq) {
+      f -= tq;
+      which = 1;
+      if (f >= tk) { f -= tk; which = 2; }
+    }
     const int nh = which == 0 ? p.H : p.Hkv;
-    const int c = (int)(f % per_head);
-    const int h = (int)((f / per_head) % nh);
-    const int r = (int)(f / ((long long)per_head * nh));
+    const int per = which == 2 ? vunits : units;
+    const int u = (int)(f % per);
+    const int h = (int)((f / per) % nh);
+    const int r = (int)(f / ((long long)per * nh));
     const float* acc = which == 0 ? p.dq_acc : (which == 1 ? p.dk_acc : p.dv_acc);
     const float* a = acc + ((long long)r * nh + h) * DH;
     __nv_bfloat16* o = which == 0 ? p.dq + (long long)r * p.dq_ld + h * DH
                                   : (which == 1 ? p.dk : p.dv) + (long long)r * p.dkv_ld + h * DH;
     const int use_rh = which == 2 ? 0 : rh;
     const float2* rope_row = use_rh ? p.rope + (long long)(p.idx[r] % p.T) * rh : nullptr;
-    finalize_pair(a, o, c, DH, use_rh, rope_row, which == 2 ? 1.f : p.scale);
+    finalize_unit(a, o, u, use_rh, rope_row, which == 2 ? 1.f : p.scale);
   }
-  // zero padding rows
-  const long long zq = (long long)(pad - nk) * p.H * DH, zk = (long long)(pad - nk) * p.Hkv * DH;
+  // zero padding rows, 16 bytes at a time
+  const int qv = p.H * DH / 8, kvv = p.Hkv * DH / 8;
+  const long long zq = (long long)(pad - nk) * qv, zk = (long long)(pad - nk) * kvv;
   for (long long e = tid; e < zq; e += stride) {
-    const int r = nk + (int)(e / ((long long)p.H * DH));
-    const int c = (int)(e % ((long long)p.H * DH));
-    p.dq[(long long)r * p.dq_ld + c] = f2bf(0.f);
+    const int r = nk + (int)(e / qv);
+    *reinterpret_cast<uint4*>(p.dq + (long long)r * p.dq_ld + 8 * (e % qv)) = make_uint4(0, 0, 0, 0);
   }
   for (long long e = tid; e < zk; e += stride) {
-    const int r = nk + (int)(e / ((long long)p.Hkv * DH));
-    const int c = (int)(e % ((long long)p.Hkv * DH));
-    p.dk[(long long)r * p.dkv_ld + c] = f2bf(0.f);
-    p.dv[(long long)r * p.dkv_ld + c] = f2bf(0.f);
+    const int r = nk + (int)(e / kvv);
+    const long long off = (long long)r * p.dkv_ld + 8 * (e % kvv);
+    *reinterpret_cast<uint4*>(p.dk + off) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(p.dv + off) = make_uint4(0, 0, 0, 0);
   }
 }
 
@@ -745,6 +775,8 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       fence_after();
       const float* L = sL + buf * 128;
       const float* Dd = sD + buf * 128;
+      // a full block strictly below the diagonal needs no masking
+      const bool interior = (!p.causal || i0 > j0) && qrows == kQ && len - j0 >= kK;
 #pragma unroll 1
       for (int cc = 0; cc < 2; ++cc) {
         const int c = 2 * half + cc;            // 32-query chunk
@@ -753,13 +785,23 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
         tmem_ld32_async(tbase + lane_off + TM_DP + c * 32, dr);
         tmem_wait_ld();
         float sv[32], dv[32];
+        if (interior) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int qi = c * 32 + e;
-          const bool valid = kvalid && qi < qrows && (!p.causal || key <= i0 + qi);
-          const float pv = valid ? exp2_approx(__uint_as_float(sr[e]) * p.scale_log2 - L[qi]) : 0.f;
-          sv[e] = pv;
-          dv[e] = valid ? pv * (__uint_as_float(dr[e]) - Dd[qi]) : 0.f;
+          for (int e = 0; e < 32; ++e) {
+            const int qi = c * 32 + e;
+            const float pv = exp2_approx(__uint_as_float(sr[e]) * p.scale_log2 - L[qi]);
+            sv[e] = pv;
+            dv[e] = pv * (__uint_as_float(dr[e]) - Dd[qi]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int qi = c * 32 + e;
+            const bool valid = kvalid && qi < qrows && (!p.causal || key <= i0 + qi);
+            const float pv = valid ? exp2_approx(__uint_as_float(sr[e]) * p.scale_log2 - L[qi]) : 0.f;
+            sv[e] = pv;
+            dv[e] = valid ? pv * (__uint_as_float(dr[e]) - Dd[qi]) : 0.f;
+          }
         }
         const uint32_t sub = (c >> 1) * kTile + kr * 128;
 #pragma unroll
@@ -1028,15 +1070,22 @@ __global__ void __launch_bounds__(tcdprep::kThreads, 1)
       tmem_ld32_async(tbase + lane_off + TM_S + st * 128 + half * 64, sr);
       tmem_ld32_async(tbase + lane_off + TM_S + st * 128 + half * 64 + 32, sr + 32);
       tmem_wait_ld();
+      // a full key block strictly before the query block needs no masking
+      const bool interior = (!p.causal || j0 + kK <= i0) && qrows == kQ && len - j0 >= kK;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int c = 2 * half + cc;
         float sv[32];
+        if (interior) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int kj = j0 + c * 32 + e;
-          const bool valid = r < qrows && kj < len && (!p.causal || kj <= i0 + r);
-          sv[e] = valid ? exp2_approx(__uint_as_float(sr[cc * 32 + e]) * p.scale_log2 - L) : 0.f;
+          for (int e = 0; e < 32; ++e) sv[e] = exp2_approx(__uint_as_float(sr[cc * 32 + e]) * p.scale_log2 - L);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int kj = j0 + c * 32 + e;
+            const bool valid = r < qrows && kj < len && (!p.causal || kj <= i0 + r);
+            sv[e] = valid ? exp2_approx(__uint_as_float(sr[cc * 32 + e]) * p.scale_log2 - L) : 0.f;
+          }
         }
         const uint32_t sub = st * 2 * kTile + (c >> 1) * kTile + r * 128;
 #pragma unroll
