@@ -65,7 +65,14 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherBatch jb, int M, long
         continue;
       }
       const uint4* s = reinterpret_cast<const uint4*>(J.src + (long long)t * J.src_ld);
-      for (int v = lane; v < vecs; v += 32) {
+      int v = lane;
+      // four 16-byte loads in flight per lane before their stores
+      for (; v + 96 < vecs; v += 128) {
+        uint4 x0 = s[v], x1 = s[v + 32], x2 = s[v + 64], x3 = s[v + 96];
+        if (J.op == 1) { x0 = gelu8(x0); x1 = gelu8(x1); x2 = gelu8(x2); x3 = gelu8(x3); }
+        d[v] = x0; d[v + 32] = x1; d[v + 64] = x2; d[v + 96] = x3;
+      }
+      for (; v < vecs; v += 32) {
         uint4 x = s[v];
         if (J.op == 1) x = gelu8(x);
         d[v] = x;
@@ -111,7 +118,7 @@ __global__ void __launch_bounds__(256) scatter_kernel(const char* __restrict__ c
 
 // ---------------------------------------------------------------------------
 // column sums: pass 1 over blocks of kColRows rows, pass 2 fixed-order reduce
-constexpr int kColRows = 64;
+constexpr int kColRows = 16;
 
 __global__ void __launch_bounds__(256) colsum_part_kernel(const void* __restrict__ X, int is_bf16, long long ld,
                                                           int N, const int32_t* __restrict__ gidx,
@@ -137,17 +144,28 @@ __global__ void __launch_bounds__(256) colsum_part_kernel(const void* __restrict
 }
 
 // out[c] = sum over partial rows i < ceil(n_kept / rows_per_part) of
-// part[i * stride + c], in ascending i (deterministic)
+// part[i * stride + c].  A block covers 32 columns with 8 row groups: group g
+// sums rows g, g+8, ... in ascending order, then the 8 group sums are added
+// in group order -- a fixed summation order, so the result is deterministic.
 __global__ void __launch_bounds__(256) colsum_reduce_kernel(const float* __restrict__ part, int N, long long stride,
                                                             int rows_per_part, const int32_t* __restrict__ n_kept,
                                                             float* __restrict__ out) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= N) return;
+  __shared__ float acc[8][33];
+  const int cl = threadIdx.x & 31, g = threadIdx.x >> 5;
+  const int c = blockIdx.x * 32 + cl;
   const int nk = *n_kept;
   const int nparts = (nk + rows_per_part - 1) / rows_per_part;
   float s = 0.f;
-  for (int i = 0; i < nparts; ++i) s += part[(long long)i * stride + c];
-  out[c] = s;
+  if (c < N)
+    for (int i = g; i < nparts; i += 8) s += part[(long long)i * stride + c];
+  acc[g][cl] = s;
+  __syncthreads();
+  if (g == 0 && c < N) {
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t += acc[k][cl];
+    out[c] = t;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -157,7 +175,7 @@ __global__ void __launch_bounds__(256) colsum_reduce_kernel(const float* __restr
 //   columns: dgamma = sum_r dy xh, dbeta = sum_r dy, as per-64-row partials
 //            (thread = 8 columns) then a fixed-order reduction: deterministic.
 constexpr int kNormWarps = 8;
-constexpr int kNormColRows = 64;
+constexpr int kNormColRows = 16;
 
 __device__ __forceinline__ void norm_dy8(const NormBwdArgs& a, long long off, float* dy) {
   load8(a.dy1, 0, off, dy);
@@ -467,7 +485,7 @@ cudaError_t launch_colsum(const Ctx& c, const void* X, int x_is_bf16, long long 
   dim3 g1((N / 8 + 255) / 256, (M + kColRows - 1) / kColRows);
   prof_begin(c, "colsum");
   colsum_part_kernel<<<g1, 256, 0, c.stream>>>(X, x_is_bf16, ld, N, gidx, n_kept, part);
-  colsum_reduce_kernel<<<(N + 255) / 256, 256, 0, c.stream>>>(part, N, N, kColRows, n_kept, out);
+  colsum_reduce_kernel<<<(N + 31) / 32, 256, 0, c.stream>>>(part, N, N, kColRows, n_kept, out);
   prof_end(c);
   count_launch(2);
   return cudaGetLastError();
@@ -484,7 +502,7 @@ cudaError_t launch_norm_bwd(const Ctx& c, const NormBwdArgs& a) {
   norm_cols_kernel<<<dim3((a.D / 8 + 255) / 256, (unsigned)((a.cap + kNormColRows - 1) / kNormColRows)), 256, 0,
                      c.stream>>>(a);
   // partials are laid out [part][set][D] with set 0 = dgamma, set 1 = dbeta
-  const int g = (a.D + 255) / 256;
+  const int g = (a.D + 31) / 32;
   colsum_reduce_kernel<<<g, 256, 0, c.stream>>>(a.part, a.D, (long long)nsets * a.D, kNormColRows, a.n_kept,
                                                 a.dgamma);
   if (a.layer_norm)
