@@ -168,6 +168,18 @@ class Clocks:
                 "samples": len(sm)}
 
 
+def max_over_ranks(vals, device):
+    """Element-wise max over all ranks (the slowest replica sets the job time);
+    identity outside a multi-rank run."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in vals]
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def measured_peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
@@ -295,10 +307,7 @@ def run_ours(args):
         ms_f, launches = timed(masks["filtered"], args.steps, args.warmup)
     clocks = clk.summary()
     ms_u, _ = timed(masks["unfiltered"], args.steps, args.warmup)
-    if world > 1:
-        t = torch.tensor([ms_f, ms_u], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_f, ms_u = t.tolist()
+    ms_f, ms_u = max_over_ranks([ms_f, ms_u], dev)
 
     # ---- per-kernel times from the library profiler (separate pass) ------
     # The weight-gradient GEMMs normally overlap the rest of the step on a
@@ -371,10 +380,7 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = t.item()
+    e2e_ms = max_over_ranks([e2e_ms], dev)[0]
 
     if rank == 0:
         tokens = s.M * world

@@ -101,6 +101,15 @@ int collider_profile_get(int i, const char** name, long long* mnk_dyn, float* ms
 /*     tokens; this is the index list it runs over)                          */
 /* ------------------------------------------------------------------------ */
 
+/* The token filter's decision (Fig. 2b: the filter drops the loss of the
+ * tokens it filters), from per-token scores: in every sequence the n_filter
+ * lowest scores are filtered -- equal scores lower position first, NaN above
+ * every number, -0.0 equal to +0.0 -- and mask[b, t] = 1 for the kept tokens.
+ * scores f32 [B, T], mask u8 [B, T], both device.  Bit-exact, deterministic.
+ * 0 <= n_filter <= T.  The scoring model itself is outside this library. */
+collider_status collider_select_keep(const float* scores, int B, int T, int n_filter, uint8_t* mask,
+                                     void* stream);
+
 /* Workspace bytes collider_compact needs for B*T tokens (0 when B*T <=
  * 4,194,304: a single thread block scans the mask). */
 size_t collider_compact_workspace_size(int B, int T);

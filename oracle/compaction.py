@@ -1,4 +1,4 @@
-"""Keep-mask compaction (test infrastructure only).
+"""Keep-mask selection and compaction (test infrastructure only).
 
 Collider abstract: the would-be sparse GEMM over all tokens becomes a
 "dimension-reduced dense GEMM" over the kept tokens.  The reduction needs the
@@ -23,3 +23,20 @@ def compact(keep: np.ndarray):
     cu = np.zeros(B + 1, dtype=np.int32)
     cu[1:] = np.cumsum(per_seq)
     return idx, cu, int(idx.size)
+
+
+def select_keep(scores: np.ndarray, n_filter: int) -> np.ndarray:
+    """The token filter's decision from per-token scores (Fig. 2b: the loss of
+    the filtered tokens is dropped): in every sequence the n_filter lowest
+    scores are filtered, equal scores filtered lower position first; NaN
+    scores order above every number.  scores [B, T]; returns uint8 [B, T],
+    1 = kept."""
+    scores = np.asarray(scores, dtype=np.float32)
+    B, T = scores.shape
+    keep = np.ones((B, T), dtype=np.uint8)
+    pos = np.arange(T)
+    for b in range(B):
+        s = np.where(scores[b] == 0, np.float32(0), scores[b])   # -0.0 ties with +0.0
+        order = np.lexsort((pos, s))                            # NaN sorts last
+        keep[b, order[:n_filter]] = 0
+    return keep

@@ -19,7 +19,8 @@ __all__ = [
     "LayerDesc", "LayerWeights", "LayerSaved", "LayerGrads", "EXPORTED",
     "collider_last_error", "collider_check", "collider_launch_count",
     "collider_profile_enable", "collider_profile_count", "collider_profile_get",
-    "collider_compact_workspace_size", "collider_compact", "collider_compact_noalloc", "collider_gather_rows",
+    "collider_select_keep", "collider_compact_workspace_size", "collider_compact", "collider_compact_noalloc",
+    "collider_gather_rows",
     "collider_scatter_rows", "collider_linear_workspace_size", "collider_linear_bwd",
     "collider_attn_workspace_size", "collider_attn_bwd", "collider_layer_workspace_size",
     "collider_layer_bwd", "collider_stack_workspace_size", "collider_stack_bwd",
@@ -74,6 +75,7 @@ _SIGS = {
     "collider_profile_enable": (I, [I]),
     "collider_profile_count": (I, []),
     "collider_profile_get": (I, [I, C.POINTER(C.c_char_p), C.POINTER(C.c_longlong), C.POINTER(C.c_float)]),
+    "collider_select_keep": (I, [P, I, I, I, P, P]),
     "collider_compact_workspace_size": (SZ, [I, I]),
     "collider_compact": (I, [P, I, I, P, P, P, P, SZ, P]),
     "collider_compact_noalloc": (I, [P, I, I, P, P, P, P]),
@@ -172,6 +174,10 @@ def collider_profile_get(i: int):
     if lib().collider_profile_get(i, C.byref(name), mnk, C.byref(ms)) != 0:
         raise IndexError(i)
     return name.value.decode(), tuple(mnk), ms.value
+
+
+def collider_select_keep(scores, B, T, n_filter, mask, stream=None) -> None:
+    _check(lib().collider_select_keep(_ptr(scores), B, T, n_filter, _ptr(mask), _stream(stream)))
 
 
 def collider_compact_workspace_size(B: int, T: int) -> int:

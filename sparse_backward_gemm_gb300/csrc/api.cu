@@ -199,8 +199,20 @@ extern "C" int collider_profile_get(int i, const char** name, long long* mnk_dyn
 }
 
 // ===========================================================================
-// a1 compaction
+// token filter decision and a1 compaction
 // ===========================================================================
+extern "C" collider_status collider_select_keep(const float* scores, int B, int T, int n_filter, uint8_t* mask,
+                                                void* stream) {
+  if (!scores || !mask) return fail(COLLIDER_ERR_INVALID_ARG, "collider_select_keep: null pointer");
+  if (B < 1 || T < 1 || (long long)B * T >= (1ll << 31) || n_filter < 0 || n_filter > T)
+    return fail(COLLIDER_ERR_INVALID_ARG, "collider_select_keep: need B, T >= 1, B*T < 2^31, 0 <= n_filter <= T");
+  Ctx c;
+  collider_status s = make_ctx(stream, &c);
+  if (s != COLLIDER_OK) return s;
+  CK(launch_select_keep(c, scores, B, T, n_filter, mask));
+  return COLLIDER_OK;
+}
+
 extern "C" size_t collider_compact_workspace_size(int B, int T) {
   if (B < 1 || T < 1) return 0;
   return compact_ws_bytes((long long)B * T);

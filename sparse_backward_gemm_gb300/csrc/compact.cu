@@ -145,7 +145,87 @@ __global__ void __launch_bounds__(kThreads) compact_write(const uint8_t* __restr
   if (start < M) emit(bits, start, off, B, T, idx, cu_kept, M);
 }
 
+// ---------------------------------------------------------------------------
+// Token filter decision from scores (Collider Fig. 2b: the loss of the
+// filtered tokens is dropped): per sequence the n lowest scores are filtered,
+// equal scores lower position first, NaN above every number.  Keys
+// (ordered score bits << 32 | position) are unique, so the n-th smallest key
+// X splits the sequence exactly: filtered iff key <= X.  X is found by a radix
+// select, 8 bits per pass from the top, one block per sequence.
+__device__ __forceinline__ uint32_t order_key(float x) {
+  if (x != x) return 0xFFFFFFFFu;
+  if (x == 0.f) x = 0.f;   // -0.0 ties with +0.0
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(kThreads) select_keep_kernel(const float* __restrict__ scores, int T, int n,
+                                                               uint8_t* __restrict__ mask) {
+  __shared__ unsigned hist[256];
+  __shared__ unsigned long long s_prefix;
+  __shared__ unsigned s_k;
+  const float* sc = scores + (long long)blockIdx.x * T;
+  uint8_t* mk = mask + (long long)blockIdx.x * T;
+  if (n <= 0 || n >= T) {
+    for (int i = threadIdx.x; i < T; i += blockDim.x) mk[i] = n <= 0 ? 1 : 0;
+    return;
+  }
+  unsigned long long prefix = 0, himask = 0;
+  unsigned k = (unsigned)n;   // rank (1-based) of X among the keys sharing `prefix`
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < T; i += blockDim.x) {
+      const unsigned long long key = ((unsigned long long)order_key(sc[i]) << 32) | (unsigned)i;
+      if ((key & himask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      // warp 0: lane l owns bins 8l..8l+7; find the bin where the running count reaches k
+      const int l = threadIdx.x;
+      unsigned c[8], tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) { c[j] = hist[8 * l + j]; tot += c[j]; }
+      unsigned incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (l >= o) incl += y;
+      }
+      const unsigned excl = incl - tot;
+      const unsigned hit = __ballot_sync(0xffffffffu, excl < k && incl >= k);
+      if (l == __ffs(hit) - 1) {
+        unsigned cum = excl;
+        int d = 0;
+        for (; d < 7; ++d) {
+          if (cum + c[d] >= k) break;
+          cum += c[d];
+        }
+        s_k = k - cum;
+        s_prefix = prefix | ((unsigned long long)(8 * l + d) << shift);
+      }
+    }
+    __syncthreads();
+    k = s_k;
+    prefix = s_prefix;
+    himask |= 0xFFull << shift;
+    __syncthreads();
+  }
+  for (int i = threadIdx.x; i < T; i += blockDim.x) {
+    const unsigned long long key = ((unsigned long long)order_key(sc[i]) << 32) | (unsigned)i;
+    mk[i] = key > prefix ? 1 : 0;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_select_keep(const Ctx& c, const float* scores, int B, int T, int n_filter, uint8_t* mask) {
+  prof_begin(c, "select_keep");
+  select_keep_kernel<<<B, kThreads, 0, c.stream>>>(scores, T, n_filter, mask);
+  prof_end(c);
+  count_launch();
+  return cudaGetLastError();
+}
 
 size_t compact_ws_bytes(long long M) {
   if (M <= kCompactOneBlockMax) return 0;

@@ -27,7 +27,8 @@ void prof_begin(const Ctx& c, const char* name, long long m = 0, long long n = 0
                 int dyn = 0);
 void prof_end(const Ctx& c);
 
-// ---- compaction ------------------------------------------------------------
+// ---- keep-mask selection and compaction -------------------------------------
+cudaError_t launch_select_keep(const Ctx& c, const float* scores, int B, int T, int n_filter, uint8_t* mask);
 constexpr long long kCompactOneBlockMax = 4194304;  // 2^22 tokens: one block scans it all
 size_t compact_ws_bytes(long long M);
 cudaError_t launch_compact(const Ctx& c, const uint8_t* mask, int B, int T, int32_t* idx,

@@ -96,3 +96,24 @@ def test_argument_errors_are_reported():
     with pytest.raises(cl.ColliderError, match="INVALID_ARG"):
         cl.collider_gather_rows(t, 16, t, 16, 8, 4, t, t)     # row_bytes not a multiple of 16
     cl.collider_check()
+
+
+@pytest.mark.parametrize("B,T,n", [(4, 2048, 819), (1, 8192, 3276), (3, 100, 0), (3, 100, 100), (2, 5000, 1),
+                                   (5, 33, 17)])
+def test_select_keep_matches_oracle(B, T, n):
+    from oracle.compaction import select_keep
+    rng = np.random.default_rng(B * T + n)
+    s = rng.gumbel(size=(B, T)).astype(np.float32)
+    s[:, ::7] = np.round(s[:, ::7])                 # plenty of ties
+    s[0, 3 % T] = np.nan
+    s[-1, 5 % T] = -0.0
+    s[-1, 6 % T] = 0.0
+    s[0, 1 % T] = -np.inf
+    mask = torch.full((B, T), 7, dtype=torch.uint8, device=gu.DEV)
+    cl.collider_select_keep(torch.from_numpy(s).to(gu.DEV), B, T, n, mask)
+    torch.cuda.synchronize()
+    assert np.array_equal(mask.cpu().numpy(), select_keep(s, n))
+    # scores -> mask -> kept-index list, end to end on the device
+    idx, cu, nk = gu.compact(mask.cpu().numpy())
+    ri, rc, rn = oracle_compact(select_keep(s, n))
+    assert int(nk.item()) == rn and np.array_equal(idx[:rn].cpu().numpy(), ri)

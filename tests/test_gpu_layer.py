@@ -145,3 +145,26 @@ def test_small_stack():
             if k == "dx":
                 continue
             assert gu.rel_err(got[k], v) <= 2e-2, (l, k, gu.rel_err(got[k], v))
+
+
+def test_loss_only_filtering_baseline():
+    """The prior art Collider improves on (Fig. 2b / Fig. 3): only the loss of
+    filtered tokens is dropped.  On the library that is the dense backward (an
+    all-kept mask) of the masked upstream gradient; it must match the oracle's
+    loss-only backward, and gradients then do reach filtered rows."""
+    s = SMALL["llama"]
+    w = workloads.layer_weights(s)
+    t = workloads.layer_inputs(s)
+    keep = t["keep"]
+    km = keep.reshape(-1) != 0
+    _, saved = ob.block_forward(t["x"], w, s, round_saved=True)
+    dmask = np.where(km[:, None], t["dout"], 0.0)
+    ref = ob.block_backward(dmask, saved, w, s, keep, filter_activations=False)
+    L = gu.DeviceLayer(s, w, saved)
+    idx, cu, nk = gu.compact(np.ones_like(keep))
+    L.run(gu.bf16(dmask), idx, cu, nk)
+    got = L.results()
+    cl.collider_check()
+    for k in ref:
+        assert gu.rel_err(got[k], ref[k]) <= 2e-2, k
+    assert np.abs(got["dx"][~km]).max() > 0

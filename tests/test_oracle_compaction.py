@@ -70,3 +70,42 @@ def test_mask_generators_filter_exact_count():
             assert (m.sum(axis=1) == 200 - nf).all()
     # floor, not round: 40% of 128 -> 51 filtered, 77 kept
     assert workloads.n_filtered(128, 0.4) == 51
+
+
+def _brute_select(scores, n):
+    B, T = scores.shape
+    keep = np.ones((B, T), np.uint8)
+    for b in range(B):
+        def key(p):
+            v = float(scores[b, p])
+            return (1, 0.0, p) if v != v else (0, v, p)    # NaN after every number
+        for p in sorted(range(T), key=key)[:n]:
+            keep[b, p] = 0
+    return keep
+
+
+def test_select_keep_hand_example():
+    from oracle.compaction import select_keep
+    # scores of one sequence; filter the 3 lowest: -2.0 (pos 4), then the two
+    # 0.5s -- equal, so the lower position (1) goes before (3) -- nothing else
+    s = np.array([[1.0, 0.5, 7.0, 0.5, -2.0, 0.5]], np.float32)
+    assert select_keep(s, 3).tolist() == [[1, 0, 1, 0, 0, 1]]
+    assert select_keep(s, 0).tolist() == [[1] * 6]
+    assert select_keep(s, 6).tolist() == [[0] * 6]
+
+
+def test_select_keep_brute_force():
+    from oracle.compaction import select_keep
+    rng = np.random.default_rng(5)
+    s = rng.integers(-3, 4, size=(3, 40)).astype(np.float32)      # many ties
+    s[0, 5] = np.nan
+    s[1, 7] = -0.0
+    s[1, 8] = 0.0
+    s[2, :3] = np.inf
+    for n in (0, 1, 13, 39, 40):
+        assert np.array_equal(select_keep(s, n), _brute_select(s, n))
+    # matches the generator's Gumbel rule on the same scores
+    g = np.random.Generator(np.random.PCG64(123)).gumbel(size=(2, 64))
+    import workloads
+    want = workloads.gumbel_keep_mask(2, 64, 0.4, 123)
+    assert np.array_equal(select_keep(g.astype(np.float32), workloads.n_filtered(64, 0.4)), want)
