@@ -77,6 +77,8 @@ struct TcCfg {
 // summing the partial tiles in CTA order (deterministic).
 struct Split {
   int m_tiles, num_tiles, num_kb;
+  int m_units;         // tile rows of the schedule: m_tiles, or pairs of them for a CTA pair
+  int unit0, ustride;  // whole-tile phase: first tile and stride (per CTA, or per CTA pair)
   int dp_tiles;        // tiles handled whole, round-robin, first
   long long total;     // stream-K iterations (over tiles dp_tiles..num_tiles-1)
   bool sk;
@@ -113,7 +115,7 @@ struct SegIter {
   int tile;            // whole-tile phase
   long long it, end;   // stream-K phase (relative iterations)
   __device__ SegIter(const Split& s) : sp(s) {
-    tile = blockIdx.x;
+    tile = sp.unit0;
     if (sp.sk && (int)blockIdx.x < sp.G) {
       it = sp.begin(blockIdx.x);
       end = (long long)(blockIdx.x + 1) * sp.total / sp.G;
@@ -126,7 +128,7 @@ struct SegIter {
       t = tile;
       k0 = 0;
       k1 = sp.num_kb;
-      tile += gridDim.x;
+      tile += sp.ustride;
       return true;
     }
     if (it >= end) return false;
@@ -214,7 +216,12 @@ __device__ __forceinline__ void store32(const TcParams& p, int row, int col, boo
   }
 }
 
-template <int BN, bool A_MN, bool B_MN>
+// PAIR: the grid is made of 2-CTA clusters.  Both CTAs of a pair work on the
+// same column tile and on adjacent 128-row tiles; each loads half of the B
+// tile and multicasts it to both, so every SM reads 2/3 of the operand bytes
+// from L2 that a lone CTA reads.  A stage is released to either producer only
+// when both MMAs have consumed it (the empty barrier counts two commits).
+template <int BN, bool A_MN, bool B_MN, bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcParams p) {
   using Cfg = TcCfg<BN>;
@@ -236,16 +243,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (p.dyn == 1) M = min(M, nk);
     else K = min(K, nk);
   }
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
   Split sp;
   sp.m_tiles = (M + BM - 1) / BM;
-  sp.num_tiles = sp.m_tiles * ((p.N + BN - 1) / BN);
+  sp.m_units = PAIR ? (sp.m_tiles + 1) / 2 : sp.m_tiles;
+  sp.num_tiles = sp.m_units * ((p.N + BN - 1) / BN);
   sp.num_kb = (K + BK - 1) / BK;
-  sp.init(p.split_mode, p.partial != nullptr);
+  sp.unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  sp.ustride = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  sp.init(PAIR ? 0 : p.split_mode, !PAIR && p.partial != nullptr);
+  // tile t -> this CTA's output origin
+  auto origin = [&](int t, int& m0, int& n0) {
+    const int mu = t % sp.m_units;
+    m0 = (PAIR ? 2 * mu + rank : mu) * BM;
+    n0 = (t / sp.m_units) * BN;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, PAIR ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
@@ -259,6 +276,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
   fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();   // the peer's barriers exist before any multicast reaches them
   fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -266,8 +284,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // empty reduction (nothing kept): the output is zero
     if (warp >= 2) {
       const int q = warp & 3;
-      for (int t = blockIdx.x; t < sp.num_tiles; t += gridDim.x) {
-        const int m0 = (t % sp.m_tiles) * BM, n0 = (t / sp.m_tiles) * BN;
+      for (int t = sp.unit0; t < sp.num_tiles; t += sp.ustride) {
+        int m0, n0;
+        origin(t, m0, n0);
         const int row = m0 + q * 32 + lane;
         const bool row_ok = row < M;
         if (!(row_ok || (p.zero_pad && row < padded_rows(M, p.c_rows)))) continue;
@@ -288,7 +307,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       SegIter si(sp);
       int t, k0, k1;
       while (!*abort_flag && si.next(t, k0, k1)) {
-        const int m0 = (t % sp.m_tiles) * BM, n0 = (t / sp.m_tiles) * BN;
+        int m0, n0;
+        origin(t, m0, n0);
         bool ok = true;
         for (int kb = k0; kb < k1; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.st, 1)) { ok = false; break; }
@@ -304,7 +324,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tma_load_2d(sa, &tmA, fb, m0, kx);
             tma_load_2d(sa + 8192, &tmA, fb, m0 + 64, kx);
           }
-          if (!B_MN) {
+          if (PAIR) {
+            // this CTA's half of B, to both CTAs of the pair
+            if (!B_MN) {
+              tma_load_2d_mc(sb + rank * (Cfg::kBBytes / 2), &tmB, fb, kx, n0 + rank * (BN / 2), 3);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BN / 128; ++j) {
+                const int c = rank * (BN / 128) + j;
+                tma_load_2d_mc(sb + 8192 * c, &tmB, fb, n0 + 64 * c, kx, 3);
+              }
+            }
+          } else if (!B_MN) {
             tma_load_2d(sb, &tmB, fb, kx, n0);
           } else {
 #pragma unroll
@@ -313,6 +344,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
+      }
+      if (PAIR && !*abort_flag) {
+        // both MMAs release every stage (their commits land in this CTA's
+        // empty barriers) before this CTA may leave the cluster
+        for (int i = 0; i < S; ++i) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.st, 5)) break;
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
       }
       if (*abort_flag) {
         // another role gave up: let this thread's copies still in flight land
@@ -351,7 +390,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint64_t bd = B_MN ? sdesc(sb + kk * 2048, 8192, 1024) : sdesc(sb + kk * 32, 16, 1024);
             mma_bf16(d, ad, bd, idesc, (kb > k0) || (kk > 0));
           }
-          mma_commit(empty0 + 8 * stage);
+          if (PAIR) mma_commit_mc(empty0 + 8 * stage, 3);
+          else mma_commit(empty0 + 8 * stage);
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -374,7 +414,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t aph = (seg >> 1) & 1;
       if (!mbar_wait(tfull0 + 8 * acc, aph, &no_abort, p.st, 4)) break;
       fence_after();
-      const int m0 = (t % sp.m_tiles) * BM, n0 = (t / sp.m_tiles) * BN;
+      int m0, n0;
+      origin(t, m0, n0);
       const int rl = q * 32 + lane;
       const int row = m0 + rl;
       const bool row_ok = row < M;
@@ -445,6 +486,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();
   if (warp == 1) {
     fence_after();
     tmem_dealloc(tmem_base, Cfg::kTmemCols);
@@ -471,22 +513,64 @@ bool make_map(CUtensorMap* m, const void* base, long long inner, long long rows,
   return make_tensor_map(m, base, false, inner, rows, ld, 64, box_rows);
 }
 
-template <int BN, bool A_MN, bool B_MN>
+template <int BN, bool A_MN, bool B_MN, bool PAIR>
 cudaError_t launch_variant(const Ctx& c, const TcGemm& g, const CUtensorMap& ma, const CUtensorMap& mb,
                            const TcParams& p) {
   using Cfg = TcCfg<BN>;
-  // the shared-memory opt-in is a per-device function attribute: set it the
-  // first time each device uses this variant
-  static int seen[64] = {0};
+  auto kern = tc_gemm_kernel<BN, A_MN, B_MN, PAIR>;
+  // Per-device set-up, the first time each device uses this variant: the
+  // shared-memory opt-in (a function attribute), and for the pair variant
+  // how many 2-CTA clusters fit on the GPU at once (a persistent grid larger
+  // than that would run its last clusters in a second wave).
+  static int max_pairs[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !seen[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, A_MN, B_MN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Cfg::kSmem));
+  const bool cache = dev >= 0 && dev < 64;
+  int pairs_fit = cache ? max_pairs[dev] : 0;
+  if (pairs_fit == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Cfg::kSmem));
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) seen[dev] = 1;
+    pairs_fit = c.num_sms / 2;
+    if (PAIR) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2 * pairs_fit);
+      cfg.blockDim = dim3(kTcThreads);
+      cfg.dynamicSmemBytes = Cfg::kSmem;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      if (n < 1) return cudaErrorNotSupported;
+      pairs_fit = n < pairs_fit ? n : pairs_fit;
+    }
+    if (cache) max_pairs[dev] = pairs_fit;
   }
-  const long long tiles = ((long long)(g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
+  const long long m_tiles = (g.M + BM - 1) / BM, n_tiles = (g.N + BN - 1) / BN;
+  if (PAIR) {
+    const long long units = (m_tiles + 1) / 2 * n_tiles;
+    const int pairs = static_cast<int>(units < pairs_fit ? (units < 1 ? 1 : units) : pairs_fit);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmem;
+    cfg.stream = c.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, ma, mb, p);
+  }
+  const long long tiles = m_tiles * n_tiles;
   int grid;
   if (p.partial) {
     grid = c.num_sms < kSkMaxCtas ? c.num_sms : kSkMaxCtas;   // stream-K: one CTA per SM
@@ -494,7 +578,7 @@ cudaError_t launch_variant(const Ctx& c, const TcGemm& g, const CUtensorMap& ma,
     grid = static_cast<int>(tiles < c.num_sms ? tiles : c.num_sms);
   }
   if (grid < 1) grid = 1;
-  tc_gemm_kernel<BN, A_MN, B_MN><<<grid, kTcThreads, Cfg::kSmem, c.stream>>>(ma, mb, p);
+  kern<<<grid, kTcThreads, Cfg::kSmem, c.stream>>>(ma, mb, p);
   return cudaGetLastError();
 }
 
@@ -529,14 +613,7 @@ cudaError_t launch_tc_gemm(const Ctx& c, const TcGemm& g) {
     const long long t256 = ((long long)(g.M + BM - 1) / BM) * ((g.N + 255) / 256);
     bn = (t256 >= c.num_sms || g.N % 256 == 0) && g.N >= 256 ? 256 : 128;
   }
-  CUtensorMap ma, mb;
-  // A: K-major [M rows, K] or MN-major [K rows, M]
-  bool ok = g.a_mn_major ? make_map(&ma, g.A, g.M, g.a_rows, g.lda, 64)
-                         : make_map(&ma, g.A, g.K, g.a_rows, g.lda, BM);
-  ok = ok && (g.b_mn_major ? make_map(&mb, g.B, g.N, g.b_rows, g.ldb, 64)
-                           : make_map(&mb, g.B, g.K, g.b_rows, g.ldb, bn));
-  if (!ok) return cudaErrorInvalidValue;
-  const long long max_tiles = ((long long)(g.M + BM - 1) / BM) * ((g.N + bn - 1) / bn);
+  if (g.a_mn_major != g.b_mn_major) return cudaErrorNotSupported;   // dX: both K-major; dW: both MN-major
   // Work split.  Measured on the block shapes: whole tiles keep the operands'
   // L2 locality and win except for long reductions over a static K (>= 128
   // k-slices), where stream-K's even split pays for its fix-up.
@@ -545,24 +622,41 @@ cudaError_t launch_tc_gemm(const Ctx& c, const TcGemm& g) {
     const char* e = getenv("COLLIDER_GEMM_STREAMK");
     return e ? atoi(e) : -1;
   }();
+  // CTA pairs sharing B tiles, for every whole-tile launch: measured 4-7%
+  // faster than lone CTAs on each of the block's GEMMs (stream-K launches
+  // stay lone CTAs).  COLLIDER_GEMM_PAIR=0 turns them off.
+  static const int pair_env = [] {
+    const char* e = getenv("COLLIDER_GEMM_PAIR");
+    return e ? atoi(e) : -1;
+  }();
+  const long long max_tiles = ((long long)(g.M + BM - 1) / BM) * ((g.N + bn - 1) / bn);
   int split = split_env;
   if (split < 0) split = (g.dyn != 2 && g.K / BK >= 128) ? 1 : 0;
   const bool sk = split != 0 && g.partial && g.counters && max_tiles <= g.counter_cap;
+  const bool pair = !sk && pair_env != 0;
+  CUtensorMap ma, mb;
+  // A: K-major [M rows, K] or MN-major [K rows, M]; B: K-major [N rows, K]
+  // (half the tile's rows per box for a pair) or MN-major [K rows, N]
+  bool ok = g.a_mn_major ? make_map(&ma, g.A, g.M, g.a_rows, g.lda, 64)
+                         : make_map(&ma, g.A, g.K, g.a_rows, g.lda, BM);
+  ok = ok && (g.b_mn_major ? make_map(&mb, g.B, g.N, g.b_rows, g.ldb, 64)
+                           : make_map(&mb, g.B, g.K, g.b_rows, g.ldb, pair ? bn / 2 : bn));
+  if (!ok) return cudaErrorInvalidValue;
   TcParams p{g.M, g.N, g.K, g.dyn, g.n_kept, g.C, g.ldc, g.c_bf16, g.accumulate, g.zero_pad,
              g.c_rows > 0 ? g.c_rows : g.M, sk ? g.partial : nullptr, sk ? g.counters : nullptr,
              split, g.epi, g.aux, g.aux_ld, g.idx, g.aux_rows, c.st};
   prof_begin(c, "tc_gemm", g.M, g.N, g.K, g.dyn);
   cudaError_t e;
-  const int key = (bn == 256 ? 4 : 0) | (g.a_mn_major ? 2 : 0) | (g.b_mn_major ? 1 : 0);
+  const int key = (bn == 256 ? 4 : 0) | (g.a_mn_major ? 2 : 0) | (pair ? 1 : 0);
   switch (key) {
-    case 0: e = launch_variant<128, false, false>(c, g, ma, mb, p); break;
-    case 3: e = launch_variant<128, true, true>(c, g, ma, mb, p); break;
-    case 4: e = launch_variant<256, false, false>(c, g, ma, mb, p); break;
-    case 7: e = launch_variant<256, true, true>(c, g, ma, mb, p); break;
-    case 1: e = launch_variant<128, false, true>(c, g, ma, mb, p); break;
-    case 2: e = launch_variant<128, true, false>(c, g, ma, mb, p); break;
-    case 5: e = launch_variant<256, false, true>(c, g, ma, mb, p); break;
-    default: e = launch_variant<256, true, false>(c, g, ma, mb, p); break;
+    case 0: e = launch_variant<128, false, false, false>(c, g, ma, mb, p); break;
+    case 1: e = launch_variant<128, false, false, true>(c, g, ma, mb, p); break;
+    case 2: e = launch_variant<128, true, true, false>(c, g, ma, mb, p); break;
+    case 3: e = launch_variant<128, true, true, true>(c, g, ma, mb, p); break;
+    case 4: e = launch_variant<256, false, false, false>(c, g, ma, mb, p); break;
+    case 5: e = launch_variant<256, false, false, true>(c, g, ma, mb, p); break;
+    case 6: e = launch_variant<256, true, true, false>(c, g, ma, mb, p); break;
+    default: e = launch_variant<256, true, true, true>(c, g, ma, mb, p); break;
   }
   prof_end(c);
   count_launch();
