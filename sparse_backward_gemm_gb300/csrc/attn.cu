@@ -604,11 +604,12 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
   const int n_iter = p.hc * nq_head;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  // [2] = one per query half (sfull, pfull, pempty) or per stage (qfull, qempty, qready)
   const uint32_t b_kv = smem_u32(bars + 0), b_qfull = smem_u32(bars + 1), b_qempty = smem_u32(bars + 3),
-                 b_sfull = smem_u32(bars + 5), b_pfull = smem_u32(bars + 6), b_pempty = smem_u32(bars + 7),
-                 b_dqfull = smem_u32(bars + 8), b_dqempty = smem_u32(bars + 9), b_kvready = smem_u32(bars + 10),
-                 b_qready = smem_u32(bars + 11);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+                 b_sfull = smem_u32(bars + 5), b_pfull = smem_u32(bars + 7), b_pempty = smem_u32(bars + 9),
+                 b_dqfull = smem_u32(bars + 11), b_dqempty = smem_u32(bars + 12), b_kvready = smem_u32(bars + 13),
+                 b_qready = smem_u32(bars + 14);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* sL = reinterpret_cast<float*>(sm + OFF_LD);   // [2][128]
   float* sD = sL + 256;                                // [2][128]
@@ -620,9 +621,11 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       mbar_init(b_qfull + 8 * s, 1);
       mbar_init(b_qempty + 8 * s, 1);
     }
-    mbar_init(b_sfull, 1);
-    mbar_init(b_pfull, 32 * kSoftWarps);
-    mbar_init(b_pempty, 1);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(b_sfull + 8 * g, 1);
+      mbar_init(b_pfull + 8 * g, 16 * kSoftWarps);
+      mbar_init(b_pempty + 8 * g, 1);
+    }
     mbar_init(b_dqfull, 1);
     mbar_init(b_dqempty, 128);
     mbar_init(b_kvready, 1);
@@ -679,13 +682,14 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
     } else {
       ok = false;
     }
+    // Block it+1 is loaded once block it is handed over: the MMA thread asks
+    // for block it+1 before it frees the stage that block it+1 reuses (the dQ
+    // of block it-1 frees it), so the hand-over of block it must not wait on
+    // that stage.
     if (lane == 0 && ok && n_iter > 0) ok = issue(0);
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     for (int it = 0; ok && it < n_iter; ++it) {
       const int st = it & 1, use = it >> 1;
-      int nxt = 1;
-      if (lane == 0 && it + 1 < n_iter) nxt = issue(it + 1) ? 1 : 0;
-      if (!__shfl_sync(0xffffffffu, nxt, 0)) break;
       if (!mbar_wait(b_qfull + 8 * st, use & 1, &no_abort, p.st, 29)) break;
       const int i0 = (i_start + it % nq_head) * kQ;
       const int qrows = min(kQ, len - i0);
@@ -696,70 +700,105 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_qready + 8 * st);
+      int nxt = 1;
+      if (lane == 0 && it + 1 < n_iter) nxt = issue(it + 1) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, nxt, 0)) break;
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);
+      // Query half g of iteration it has its own S^T / dP^T columns in TMEM
+      // (buffer g) and its own P^T / dS^T tile in shared memory, so the MMAs
+      // of one half run while the softmax warps of the other half work:
+      //   S, dP (it, 0) | S, dP (it, 1) | [P(it, 0)] dV, dK (it, 0) | S, dP (it+1, 0)
+      //   | [P(it, 1)] dV, dK (it, 1) | dQ (it) | S, dP (it+1, 1) | ...
+      constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);
       constexpr uint32_t id_kv = idesc_bf16(128, 64, false, true);
       constexpr uint32_t id_q = idesc_bf16(128, 64, true, true);
-      bool ok = mbar_wait(b_kvready, 0, abort_flag, p.st, 21);
-      for (int it = 0; ok && it < n_iter; ++it) {
-        const int st = it & 1, use = it >> 1;
-        if (!mbar_wait(b_qready + 8 * st, use & 1, abort_flag, p.st, 22)) break;
-        fence_after();
+      auto sdp = [&](int it, int g) {   // S^T, dP^T of half g: M 128 keys, N 64 queries
+        const int st = it & 1;
+        const uint32_t sq = sbase + OFF_Q + st * kTile + g * (kTile / 2),
+                       sdo = sbase + OFF_DO + st * kTile + g * (kTile / 2);
+        const uint32_t ts = tbase + TM_S + g * 128, tdp = ts + 64;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_bf16(ts, sdesc(sbase + OFF_K + kk * 32, 16, 1024), sdesc(sq + kk * 32, 16, 1024), id_s, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_bf16(tdp, sdesc(sbase + OFF_V + kk * 32, 16, 1024), sdesc(sdo + kk * 32, 16, 1024), id_s, kk > 0);
+        mma_commit(b_sfull + 8 * g);
+      };
+      auto dvdk = [&](int it, int g) {  // dV += P^T dO, dK += dS^T Q over the 64 queries of half g
+        const int st = it & 1;
         const uint32_t sq = sbase + OFF_Q + st * kTile, sdo = sbase + OFF_DO + st * kTile;
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_bf16(tbase + TM_S, sdesc(sbase + OFF_K + kk * 32, 16, 1024), sdesc(sq + kk * 32, 16, 1024), id_s,
-                   kk > 0);
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int kk = 4 * g + k4;
+          mma_bf16(tbase + TM_DV, sdesc(sbase + OFF_P + g * kTile + k4 * 32, 16, 1024),
+                   sdesc(sdo + kk * 2048, 8192, 1024), id_kv, (it > 0) || (kk > 0));
+        }
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_bf16(tbase + TM_DP, sdesc(sbase + OFF_V + kk * 32, 16, 1024), sdesc(sdo + kk * 32, 16, 1024), id_s,
-                   kk > 0);
-        mma_commit(b_sfull);
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int kk = 4 * g + k4;
+          mma_bf16(tbase + TM_DK, sdesc(sbase + OFF_DS + g * kTile + k4 * 32, 16, 1024),
+                   sdesc(sq + kk * 2048, 8192, 1024), id_kv, (it > 0) || (kk > 0));
+        }
+      };
+      bool ok = mbar_wait(b_kvready, 0, abort_flag, p.st, 21);
+      if (ok && n_iter > 0) {
+        ok = mbar_wait(b_qready, 0, abort_flag, p.st, 22);
+        if (ok) {
+          fence_after();
+          sdp(0, 0);
+          sdp(0, 1);
+        }
+      }
+      for (int it = 0; ok && it < n_iter; ++it) {
+        const int st = it & 1;
+        const bool more = it + 1 < n_iter;
         if (!mbar_wait(b_pfull, it & 1, abort_flag, p.st, 23)) break;
+        fence_after();
+        dvdk(it, 0);
+        if (more) {
+          if (!mbar_wait(b_qready + 8 * ((it + 1) & 1), ((it + 1) >> 1) & 1, abort_flag, p.st, 22)) break;
+          fence_after();
+          sdp(it + 1, 0);
+        }
+        if (!mbar_wait(b_pfull + 8, it & 1, abort_flag, p.st, 23)) break;
         if (it > 0 && !mbar_wait(b_dqempty, (it - 1) & 1, abort_flag, p.st, 24)) break;
         fence_after();
+        dvdk(it, 1);
 #pragma unroll
-        for (int kk = 0; kk < kQ / 16; ++kk) {   // k = queries
-          const uint32_t pa = sbase + OFF_P + (kk >> 2) * kTile + (kk & 3) * 32;
-          mma_bf16(tbase + TM_DV, sdesc(pa, 16, 1024), sdesc(sdo + kk * 2048, 8192, 1024), id_kv,
-                   (it > 0) || (kk > 0));
-        }
-#pragma unroll
-        for (int kk = 0; kk < kQ / 16; ++kk) {
-          const uint32_t da = sbase + OFF_DS + (kk >> 2) * kTile + (kk & 3) * 32;
-          mma_bf16(tbase + TM_DK, sdesc(da, 16, 1024), sdesc(sq + kk * 2048, 8192, 1024), id_kv,
-                   (it > 0) || (kk > 0));
-        }
-#pragma unroll
-        for (int kk = 0; kk < kK / 16; ++kk)     // k = keys; dS read MN-major from the dS^T tile
+        for (int kk = 0; kk < kK / 16; ++kk)     // k = keys; dS read MN-major from the dS^T tiles
           mma_bf16(tbase + TM_DQ, sdesc(sbase + OFF_DS + kk * 2048, kTile, 1024),
                    sdesc(sbase + OFF_K + kk * 2048, 8192, 1024), id_q, kk > 0);
         mma_commit(b_dqfull);
         mma_commit(b_qempty + 8 * st);
         mma_commit(b_pempty);
+        mma_commit(b_pempty + 8);
+        if (more) sdp(it + 1, 1);
       }
     }
   } else if (warp < 2 + kSoftWarps) {
     // ---------------- softmax warps: one key row, 64 queries per thread ----------------
-    const int t = threadIdx.x - 64;             // 0..255
+    // Warps 2-5 own query half 0 of every block, warps 6-9 half 1; the two
+    // groups run independently, each on its own TMEM buffer and P/dS tile.
+    const int g = (warp - 2) >> 2;              // query half
+    const int tg = threadIdx.x - 64 - 128 * g;  // 0..127 within the group
     const int q = warp & 3;
-    const int half = (warp - 2) >> 2;           // which 64 queries of the block
     const int kr = q * 32 + lane;
     const int key = j0 + kr;
     const bool kvalid = key < len;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    // lse (threads 0-127) and D (threads 128-255) of the block after the
-    // current one are fetched one iteration early, so the global-load latency
-    // hides behind the current block
+    // lse (tg 0-63) and D (tg 64-127) of this half's queries for the block
+    // after the current one are fetched one iteration early, so the
+    // global-load latency hides behind the current block
     auto fetch = [&](int it) -> float {
       const int h = hk * p.G + hci * p.hc + it / nq_head;
       const int i0 = (i_start + it % nq_head) * kQ;
-      const int qq = t & 127;
+      const int qq = 64 * g + (tg & 63);
       if (qq >= min(kQ, len - i0)) return 0.f;
-      const float* src = t < 128 ? p.lse2 : p.Dvec;
+      const float* src = tg < 64 ? p.lse2 : p.Dvec;
       return src[(long long)h * p.M + s0 + i0 + qq];
     };
     float nxt = n_iter > 0 ? fetch(0) : 0.f;
@@ -767,53 +806,65 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       const int i0 = (i_start + it % nq_head) * kQ;
       const int qrows = min(kQ, len - i0);
       const int buf = it & 1;
-      (t < 128 ? sL : sD)[buf * 128 + (t & 127)] = nxt;
+      (tg < 64 ? sL : sD)[buf * 128 + 64 * g + (tg & 63)] = nxt;
       if (it + 1 < n_iter) nxt = fetch(it + 1);
-      named_bar(1, 32 * kSoftWarps);
-      if (!mbar_wait(b_sfull, it & 1, &no_abort, p.st, 25)) break;
-      if (it > 0 && !mbar_wait(b_pempty, (it - 1) & 1, &no_abort, p.st, 26)) break;
+      named_bar(1 + 2 * g, 128);
+      if (!mbar_wait(b_sfull + 8 * g, it & 1, &no_abort, p.st, 25)) break;
       fence_after();
       const float* L = sL + buf * 128;
       const float* Dd = sD + buf * 128;
-      // a full block strictly below the diagonal needs no masking
-      const bool interior = (!p.causal || i0 > j0) && qrows == kQ && len - j0 >= kK;
-#pragma unroll 1
+      // a full half-block strictly below the diagonal needs no masking
+      const bool interior = (!p.causal || i0 > j0) && qrows >= 64 * (g + 1) && len - j0 >= kK;
+      uint32_t pk[2][16], dk[2][16];   // bf16 pairs of P^T and dS^T for the 64 queries
+#pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        const int c = 2 * half + cc;            // 32-query chunk
+        const uint32_t col = TM_S + g * 128 + cc * 32;
         uint32_t sr[32], dr[32];
-        tmem_ld32_async(tbase + lane_off + TM_S + c * 32, sr);
-        tmem_ld32_async(tbase + lane_off + TM_DP + c * 32, dr);
+        tmem_ld32_async(tbase + lane_off + col, sr);
+        tmem_ld32_async(tbase + lane_off + col + 64, dr);
         tmem_wait_ld();
-        float sv[32], dv[32];
         if (interior) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int qi = c * 32 + e;
-            const float pv = exp2_approx(__uint_as_float(sr[e]) * p.scale_log2 - L[qi]);
-            sv[e] = pv;
-            dv[e] = pv * (__uint_as_float(dr[e]) - Dd[qi]);
+          for (int e = 0; e < 16; ++e) {
+            const int qi = 64 * g + cc * 32 + 2 * e;
+            const float p0 = exp2_approx(__uint_as_float(sr[2 * e]) * p.scale_log2 - L[qi]);
+            const float p1 = exp2_approx(__uint_as_float(sr[2 * e + 1]) * p.scale_log2 - L[qi + 1]);
+            pk[cc][e] = pack_bf16x2(p0, p1);
+            dk[cc][e] = pack_bf16x2(p0 * (__uint_as_float(dr[2 * e]) - Dd[qi]),
+                                    p1 * (__uint_as_float(dr[2 * e + 1]) - Dd[qi + 1]));
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int qi = c * 32 + e;
-            const bool valid = kvalid && qi < qrows && (!p.causal || key <= i0 + qi);
-            const float pv = valid ? exp2_approx(__uint_as_float(sr[e]) * p.scale_log2 - L[qi]) : 0.f;
-            sv[e] = pv;
-            dv[e] = valid ? pv * (__uint_as_float(dr[e]) - Dd[qi]) : 0.f;
+          for (int e = 0; e < 16; ++e) {
+            float pv[2], dv[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const int qi = 64 * g + cc * 32 + 2 * e + k;
+              const bool valid = kvalid && qi < qrows && (!p.causal || key <= i0 + qi);
+              pv[k] = valid ? exp2_approx(__uint_as_float(sr[2 * e + k]) * p.scale_log2 - L[qi]) : 0.f;
+              dv[k] = valid ? pv[k] * (__uint_as_float(dr[2 * e + k]) - Dd[qi]) : 0.f;
+            }
+            pk[cc][e] = pack_bf16x2(pv[0], pv[1]);
+            dk[cc][e] = pack_bf16x2(dv[0], dv[1]);
           }
         }
-        const uint32_t sub = (c >> 1) * kTile + kr * 128;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const uint32_t phys = ((((c & 1) * 4 + g) ^ (kr & 7)) * 16);
-          *reinterpret_cast<uint4*>(sm + OFF_P + sub + phys) = pack8(sv + 8 * g);
-          *reinterpret_cast<uint4*>(sm + OFF_DS + sub + phys) = pack8(dv + 8 * g);
-        }
       }
+      // the P/dS tile of this half is free once dQ of the previous block is done
+      if (it > 0 && !mbar_wait(b_pempty + 8 * g, (it - 1) & 1, &no_abort, p.st, 26)) break;
+      const uint32_t rowoff = g * kTile + kr * 128;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t phys = (((cc * 4 + u) ^ (kr & 7)) * 16);
+          *reinterpret_cast<uint4*>(sm + OFF_P + rowoff + phys) =
+              make_uint4(pk[cc][4 * u], pk[cc][4 * u + 1], pk[cc][4 * u + 2], pk[cc][4 * u + 3]);
+          *reinterpret_cast<uint4*>(sm + OFF_DS + rowoff + phys) =
+              make_uint4(dk[cc][4 * u], dk[cc][4 * u + 1], dk[cc][4 * u + 2], dk[cc][4 * u + 3]);
+        }
       fence_before();
       fence_async_smem();
-      mbar_arrive(b_pfull);
+      mbar_arrive(b_pfull + 8 * g);
     }
   } else {
     // ---------------- dQ / dK / dV epilogue: one row per thread ----------------
