@@ -64,6 +64,11 @@ struct TcCfg {
   static constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators
   static constexpr size_t kSmem = 1024 + kStages * kStageBytes + 256;
 };
+// 2-SM mode (BN = 256): a stage holds this CTA's 128 x 64 A slice and half of
+// the 256 x 64 B slice, 32 KB, so seven stages fit
+constexpr int kTwoStages = 7;
+constexpr uint32_t kTwoStageBytes = BM * BK * 2 + 128 * BK * 2;
+constexpr size_t kTwoSmem = 1024 + kTwoStages * kTwoStageBytes + 256;
 
 // Work split.
 //   whole tiles  (mode 0): tiles round-robin over the CTAs.
@@ -216,19 +221,30 @@ __device__ __forceinline__ void store32(const TcParams& p, int row, int col, boo
   }
 }
 
-// PAIR: the grid is made of 2-CTA clusters.  Both CTAs of a pair work on the
-// same column tile and on adjacent 128-row tiles; each loads half of the B
-// tile and multicasts it to both, so every SM reads 2/3 of the operand bytes
-// from L2 that a lone CTA reads.  A stage is released to either producer only
-// when both MMAs have consumed it (the empty barrier counts two commits).
-template <int BN, bool A_MN, bool B_MN, bool PAIR>
+// MODE 0: lone CTAs.  MODE 1 and 2: the grid is made of 2-CTA clusters; both
+// CTAs of a pair work on the same column tile and on adjacent 128-row tiles.
+//   MODE 1: each CTA loads half of the B tile and multicasts it to both, so
+//           every SM reads 2/3 of the operand bytes from L2 that a lone CTA
+//           reads.  A stage is released to either producer only when both
+//           MMAs have consumed it (the empty barrier counts two commits).
+//   MODE 2 (BN = 256): 2-SM MMAs.  Each CTA loads its A tile and half of the
+//           B tile into its own shared memory only (32 KB a stage instead of
+//           48), every copy counted on the even CTA's full barrier; the even
+//           CTA issues one 256 x 256 MMA over both CTAs' tiles, writing each
+//           CTA's 128 rows into that CTA's TMEM; its commits reach both CTAs'
+//           empty and TMEM-full barriers, and both epilogues release the
+//           accumulator on the even CTA's TMEM-empty barrier.
+template <int BN, bool A_MN, bool B_MN, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcParams p) {
   using Cfg = TcCfg<BN>;
-  constexpr int S = Cfg::kStages;
+  constexpr bool PAIR = MODE != 0, TWO = MODE == 2;
+  static_assert(!TWO || BN == 256, "2-SM tiles are 256 x 256");
+  constexpr uint32_t kStageBytes = TWO ? kTwoStageBytes : Cfg::kStageBytes;
+  constexpr int S = TWO ? kTwoStages : Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * kStageBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
@@ -262,18 +278,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, PAIR ? 2 : 1);
+      mbar_init(empty0 + 8 * s, MODE == 1 ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 128);
+      mbar_init(tempty0 + 8 * a, TWO ? 256 : 128);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+  if (warp == 1) {
+    if (TWO) tmem_alloc_pair(smem_u32(tmem_slot), Cfg::kTmemCols);
+    else tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+  }
   fence_before();
   __syncthreads();
   if (PAIR) cluster_sync();   // the peer's barriers exist before any multicast reaches them
@@ -315,9 +334,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint32_t fb = full0 + 8 * stage;
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          mbar_expect_tx(fb, Cfg::kStageBytes);
-          const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes), sb = sa + Cfg::kABytes;
+          const uint32_t sa = smem_u32(smem + stage * kStageBytes), sb = sa + Cfg::kABytes;
           const int kx = kb * BK;
+          if (TWO) {
+            // both CTAs' copies are counted on the even CTA's full barrier
+            if (rank == 0) mbar_expect_tx(fb, 2 * kStageBytes);
+            const uint32_t lb = map_to_rank(fb, 0);
+            if (!A_MN) {
+              tma_load_2d_pair(sa, &tmA, lb, kx, m0);
+            } else {
+              tma_load_2d_pair(sa, &tmA, lb, m0, kx);
+              tma_load_2d_pair(sa + 8192, &tmA, lb, m0 + 64, kx);
+            }
+            if (!B_MN) {
+              tma_load_2d_pair(sb, &tmB, lb, kx, n0 + rank * (BN / 2));
+            } else {
+#pragma unroll
+              for (int j = 0; j < BN / 128; ++j) tma_load_2d_pair(sb + 8192 * j, &tmB, lb, n0 + rank * (BN / 2) + 64 * j, kx);
+            }
+            if (++stage == S) { stage = 0; phase ^= 1u; }
+            continue;
+          }
+          mbar_expect_tx(fb, kStageBytes);
           if (!A_MN) {
             tma_load_2d(sa, &tmA, fb, kx, m0);
           } else {
@@ -365,9 +403,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
-      constexpr uint32_t idesc = make_idesc<BN, A_MN, B_MN>();
+    if (lane == 0 && (!TWO || rank == 0)) {
+      // ---------------- MMA issuer (the even CTA of a pair in 2-SM mode) ----------------
+      constexpr uint32_t idesc = TWO ? idesc_bf16(2 * BM, BN, A_MN, B_MN) : make_idesc<BN, A_MN, B_MN>();
       int stage = 0;
       uint32_t phase = 0;
       int seg = 0;
@@ -383,24 +421,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int kb = k0; kb < k1; ++kb) {
           if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.st, 3)) { ok = false; break; }
           fence_after();
-          const uint32_t sa = smem_u32(smem + stage * Cfg::kStageBytes), sb = sa + Cfg::kABytes;
+          const uint32_t sa = smem_u32(smem + stage * kStageBytes), sb = sa + Cfg::kABytes;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = A_MN ? sdesc(sa + kk * 2048, 8192, 1024) : sdesc(sa + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc(sb + kk * 2048, 8192, 1024) : sdesc(sb + kk * 32, 16, 1024);
-            mma_bf16(d, ad, bd, idesc, (kb > k0) || (kk > 0));
+            if (TWO) mma_bf16_pair(d, ad, bd, idesc, (kb > k0) || (kk > 0));
+            else mma_bf16(d, ad, bd, idesc, (kb > k0) || (kk > 0));
           }
-          if (PAIR) mma_commit_mc(empty0 + 8 * stage, 3);
+          if (TWO) mma_commit_pair_mc(empty0 + 8 * stage, 3);
+          else if (PAIR) mma_commit_mc(empty0 + 8 * stage, 3);
           else mma_commit(empty0 + 8 * stage);
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        mma_commit(tfull0 + 8 * acc);
+        if (TWO) mma_commit_pair_mc(tfull0 + 8 * acc, 3);
+        else mma_commit(tfull0 + 8 * acc);
         ++seg;
       }
     }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
+    // the accumulator is handed back to the MMA issuer: in 2-SM mode on the
+    // even CTA's barrier, which counts both CTAs' epilogue threads
+    auto release_acc = [&](int acc) {
+      if (TWO) mbar_arrive_cluster(map_to_rank(tempty0 + 8 * acc, 0));
+      else mbar_arrive(tempty0 + 8 * acc);
+    };
     // Timeout-only waits: the group synchronises with a named barrier, so all
     // 128 threads leave together.
     volatile int no_abort = 0;
@@ -434,7 +481,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           store32(p, row, n0 + c, row_ok, v);
         }
         fence_before();
-        mbar_arrive(tempty0 + 8 * acc);
+        release_acc(acc);
       } else {
         // part of a tile: park it, and finish the tile if this CTA is the last
         float* mine = p.partial + ((long long)sp.slot(blockIdx.x, t) * BM + rl) * BN;
@@ -446,7 +493,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __stcg(reinterpret_cast<float4*>(mine + c + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
         }
         fence_before();
-        mbar_arrive(tempty0 + 8 * acc);
+        release_acc(acc);
         __threadfence();
         named_bar(1, 128);
         const long long x0 = (long long)(t - sp.dp_tiles) * sp.num_kb;
@@ -489,7 +536,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (PAIR) cluster_sync();
   if (warp == 1) {
     fence_after();
-    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    if (TWO) tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+    else tmem_dealloc(tmem_base, Cfg::kTmemCols);
   }
 }
 
@@ -513,11 +561,12 @@ bool make_map(CUtensorMap* m, const void* base, long long inner, long long rows,
   return make_tensor_map(m, base, false, inner, rows, ld, 64, box_rows);
 }
 
-template <int BN, bool A_MN, bool B_MN, bool PAIR>
+template <int BN, bool A_MN, bool B_MN, int MODE>
 cudaError_t launch_variant(const Ctx& c, const TcGemm& g, const CUtensorMap& ma, const CUtensorMap& mb,
                            const TcParams& p) {
-  using Cfg = TcCfg<BN>;
-  auto kern = tc_gemm_kernel<BN, A_MN, B_MN, PAIR>;
+  constexpr bool PAIR = MODE != 0;
+  constexpr size_t kSmemBytes = MODE == 2 ? kTwoSmem : TcCfg<BN>::kSmem;
+  auto kern = tc_gemm_kernel<BN, A_MN, B_MN, MODE>;
   // Per-device set-up, the first time each device uses this variant: the
   // shared-memory opt-in (a function attribute), and for the pair variant
   // how many 2-CTA clusters fit on the GPU at once (a persistent grid larger
@@ -529,7 +578,7 @@ cudaError_t launch_variant(const Ctx& c, const TcGemm& g, const CUtensorMap& ma,
   int pairs_fit = cache ? max_pairs[dev] : 0;
   if (pairs_fit == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(Cfg::kSmem));
+                                         static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
     pairs_fit = c.num_sms / 2;
     if (PAIR) {
@@ -541,7 +590,7 @@ cudaError_t launch_variant(const Ctx& c, const TcGemm& g, const CUtensorMap& ma,
       attr[0].val.clusterDim.z = 1;
       cfg.gridDim = dim3(2 * pairs_fit);
       cfg.blockDim = dim3(kTcThreads);
-      cfg.dynamicSmemBytes = Cfg::kSmem;
+      cfg.dynamicSmemBytes = kSmemBytes;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int n = 0;
@@ -564,7 +613,7 @@ cudaError_t launch_variant(const Ctx& c, const TcGemm& g, const CUtensorMap& ma,
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(2 * pairs);
     cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = Cfg::kSmem;
+    cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = c.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -578,7 +627,7 @@ cudaError_t launch_variant(const Ctx& c, const TcGemm& g, const CUtensorMap& ma,
     grid = static_cast<int>(tiles < c.num_sms ? tiles : c.num_sms);
   }
   if (grid < 1) grid = 1;
-  kern<<<grid, kTcThreads, Cfg::kSmem, c.stream>>>(ma, mb, p);
+  kern<<<grid, kTcThreads, kSmemBytes, c.stream>>>(ma, mb, p);
   return cudaGetLastError();
 }
 
@@ -622,9 +671,9 @@ cudaError_t launch_tc_gemm(const Ctx& c, const TcGemm& g) {
     const char* e = getenv("COLLIDER_GEMM_STREAMK");
     return e ? atoi(e) : -1;
   }();
-  // CTA pairs sharing B tiles, for every whole-tile launch: measured 4-7%
-  // faster than lone CTAs on each of the block's GEMMs (stream-K launches
-  // stay lone CTAs).  COLLIDER_GEMM_PAIR=0 turns them off.
+  // CTA pairs for every whole-tile launch (stream-K launches stay lone
+  // CTAs): 2-SM MMAs for 256-wide tiles, B multicast for 128-wide ones.
+  // COLLIDER_GEMM_PAIR=0 / 1 forces lone CTAs / B multicast everywhere.
   static const int pair_env = [] {
     const char* e = getenv("COLLIDER_GEMM_PAIR");
     return e ? atoi(e) : -1;
@@ -634,6 +683,7 @@ cudaError_t launch_tc_gemm(const Ctx& c, const TcGemm& g) {
   if (split < 0) split = (g.dyn != 2 && g.K / BK >= 128) ? 1 : 0;
   const bool sk = split != 0 && g.partial && g.counters && max_tiles <= g.counter_cap;
   const bool pair = !sk && pair_env != 0;
+  const int mode = !pair ? 0 : (bn == 256 && pair_env != 1 ? 2 : 1);
   CUtensorMap ma, mb;
   // A: K-major [M rows, K] or MN-major [K rows, M]; B: K-major [N rows, K]
   // (half the tile's rows per box for a pair) or MN-major [K rows, N]
@@ -647,16 +697,18 @@ cudaError_t launch_tc_gemm(const Ctx& c, const TcGemm& g) {
              split, g.epi, g.aux, g.aux_ld, g.idx, g.aux_rows, c.st};
   prof_begin(c, "tc_gemm", g.M, g.N, g.K, g.dyn);
   cudaError_t e;
-  const int key = (bn == 256 ? 4 : 0) | (g.a_mn_major ? 2 : 0) | (pair ? 1 : 0);
+  const int key = (bn == 256 ? 100 : 0) + (g.a_mn_major ? 10 : 0) + mode;
   switch (key) {
-    case 0: e = launch_variant<128, false, false, false>(c, g, ma, mb, p); break;
-    case 1: e = launch_variant<128, false, false, true>(c, g, ma, mb, p); break;
-    case 2: e = launch_variant<128, true, true, false>(c, g, ma, mb, p); break;
-    case 3: e = launch_variant<128, true, true, true>(c, g, ma, mb, p); break;
-    case 4: e = launch_variant<256, false, false, false>(c, g, ma, mb, p); break;
-    case 5: e = launch_variant<256, false, false, true>(c, g, ma, mb, p); break;
-    case 6: e = launch_variant<256, true, true, false>(c, g, ma, mb, p); break;
-    default: e = launch_variant<256, true, true, true>(c, g, ma, mb, p); break;
+    case 0: e = launch_variant<128, false, false, 0>(c, g, ma, mb, p); break;
+    case 1: e = launch_variant<128, false, false, 1>(c, g, ma, mb, p); break;
+    case 10: e = launch_variant<128, true, true, 0>(c, g, ma, mb, p); break;
+    case 11: e = launch_variant<128, true, true, 1>(c, g, ma, mb, p); break;
+    case 100: e = launch_variant<256, false, false, 0>(c, g, ma, mb, p); break;
+    case 101: e = launch_variant<256, false, false, 1>(c, g, ma, mb, p); break;
+    case 102: e = launch_variant<256, false, false, 2>(c, g, ma, mb, p); break;
+    case 110: e = launch_variant<256, true, true, 0>(c, g, ma, mb, p); break;
+    case 111: e = launch_variant<256, true, true, 1>(c, g, ma, mb, p); break;
+    default: e = launch_variant<256, true, true, 2>(c, g, ma, mb, p); break;
   }
   prof_end(c);
   count_launch();
