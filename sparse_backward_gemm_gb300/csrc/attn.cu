@@ -549,23 +549,25 @@ __global__ void attn_finalize_kernel(AttnK p, int DH) {
 // 128 keys, a chunk of hc query heads of the group); items are numbered key
 // block first, so the heavy (early) key blocks start first.
 //   warp 0      TMA: K, V once; Q_i, dO_i per iteration (2 stages)
-//   warp 1      TMEM owner; one lane issues the MMAs:
-//                 S^T = K Q^T, dP^T = V dO^T           (M 128 keys, N 128 queries)
-//                 dV += P^T dO, dK += dS^T Q           (M 128 keys, N 64)
-//                 dQ  = dS K                           (M 128 queries, N 64)
-//   warps 2-9   one key row and 64 of the 128 queries per thread: P^T, dS^T
-//               from TMEM -> bf16 -> shared
+//   warp 1      TMEM owner; one lane issues the MMAs, per 64-query half g:
+//                 S^T = K Q_g^T, dP^T = V dO_g^T       (M 128 keys, N 64 queries)
+//                 dV += P_g^T dO_g, dK += dS_g^T Q_g   (M 128 keys, N 64)
+//               and per block dQ = dS K                (M 128 queries, N 64)
+//   warps 2-5   query half 0, warps 6-9 query half 1: one key row and the
+//               half's 64 queries per thread: P^T, dS^T from TMEM -> bf16 ->
+//               shared
 //   warps 10-13 one query row per thread: dQ from TMEM -> shared -> TMA
 //               reduce-add into the f32 dQ accumulator; at the end dK, dV
 //               likewise into their accumulators
-// TMEM columns: S^T 0-127, dP^T 128-255, dV 256-319, dK 320-383, dQ 384-447.
+// TMEM columns: half 0 S^T 0-63, dP^T 64-127; half 1 S^T 128-191, dP^T
+// 192-255; dV 256-319, dK 320-383, dQ 384-447.
 namespace tcattn {
 constexpr int kQ = 128, kK = 128, kD = 64;
 constexpr uint32_t kTile = kQ * kD * 2;                 // 16 KB: 128 rows x 128 bytes
 constexpr uint32_t OFF_K = 0, OFF_V = kTile, OFF_Q = 2 * kTile, OFF_DO = 4 * kTile, OFF_P = 6 * kTile,
                    OFF_DS = 8 * kTile, OFF_ST = 10 * kTile, OFF_LD = 12 * kTile, OFF_BAR = 12 * kTile + 2048;
 constexpr size_t kSmem = 1024 + OFF_BAR + 256;
-constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 320, TM_DQ = 384;
+constexpr uint32_t TM_S = 0, TM_DV = 256, TM_DK = 320, TM_DQ = 384;
 constexpr int kSoftWarps = 8;                       // two per TMEM lane quadrant
 constexpr int kThreads = 32 * (2 + kSoftWarps + 4);
 }  // namespace tcattn
@@ -715,33 +717,41 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);
       constexpr uint32_t id_kv = idesc_bf16(128, 64, false, true);
       constexpr uint32_t id_q = idesc_bf16(128, 64, true, true);
+      // Shared-memory descriptors are built once; a k-step moves the start
+      // address (bits 0-13, in 16-byte units) by a constant: +2 (32 bytes)
+      // inside a K-major swizzle row, +128 (2 KB, 16 rows) down an MN-major tile.
+      const uint64_t d_k = sdesc(sbase + OFF_K, 16, 1024), d_v = sdesc(sbase + OFF_V, 16, 1024);
+      const uint64_t d_kmn = sdesc(sbase + OFF_K, 8192, 1024);            // K as the MN-major B of dQ
+      const uint64_t d_ds_mn = sdesc(sbase + OFF_DS, kTile, 1024);        // dS^T as the MN-major A of dQ
+      // per Q/dO stage (1 = the second stage, kTile bytes on); per P/dS half
+      const uint64_t d_q0 = sdesc(sbase + OFF_Q, 16, 1024), d_do0 = sdesc(sbase + OFF_DO, 16, 1024);
+      const uint64_t d_qmn0 = sdesc(sbase + OFF_Q, 8192, 1024), d_domn0 = sdesc(sbase + OFF_DO, 8192, 1024);
+      const uint64_t d_p0 = sdesc(sbase + OFF_P, 16, 1024), d_ds0 = sdesc(sbase + OFF_DS, 16, 1024);
+      constexpr uint64_t kTileStep = kTile / 16;   // one tile further on, in descriptor units
       auto sdp = [&](int it, int g) {   // S^T, dP^T of half g: M 128 keys, N 64 queries
         const int st = it & 1;
-        const uint32_t sq = sbase + OFF_Q + st * kTile + g * (kTile / 2),
-                       sdo = sbase + OFF_DO + st * kTile + g * (kTile / 2);
+        const uint64_t bq = d_q0 + st * kTileStep + g * (kTileStep / 2),
+                       bdo = d_do0 + st * kTileStep + g * (kTileStep / 2);
         const uint32_t ts = tbase + TM_S + g * 128, tdp = ts + 64;
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_bf16(ts, sdesc(sbase + OFF_K + kk * 32, 16, 1024), sdesc(sq + kk * 32, 16, 1024), id_s, kk > 0);
+        for (int kk = 0; kk < kD / 16; ++kk) mma_bf16(ts, d_k + 2 * kk, bq + 2 * kk, id_s, kk > 0);
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_bf16(tdp, sdesc(sbase + OFF_V + kk * 32, 16, 1024), sdesc(sdo + kk * 32, 16, 1024), id_s, kk > 0);
+        for (int kk = 0; kk < kD / 16; ++kk) mma_bf16(tdp, d_v + 2 * kk, bdo + 2 * kk, id_s, kk > 0);
         mma_commit(b_sfull + 8 * g);
       };
       auto dvdk = [&](int it, int g) {  // dV += P^T dO, dK += dS^T Q over the 64 queries of half g
         const int st = it & 1;
-        const uint32_t sq = sbase + OFF_Q + st * kTile, sdo = sbase + OFF_DO + st * kTile;
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
           const int kk = 4 * g + k4;
-          mma_bf16(tbase + TM_DV, sdesc(sbase + OFF_P + g * kTile + k4 * 32, 16, 1024),
-                   sdesc(sdo + kk * 2048, 8192, 1024), id_kv, (it > 0) || (kk > 0));
+          mma_bf16(tbase + TM_DV, d_p0 + g * kTileStep + 2 * k4, d_domn0 + st * kTileStep + 128 * kk, id_kv,
+                   (it > 0) || (kk > 0));
         }
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
           const int kk = 4 * g + k4;
-          mma_bf16(tbase + TM_DK, sdesc(sbase + OFF_DS + g * kTile + k4 * 32, 16, 1024),
-                   sdesc(sq + kk * 2048, 8192, 1024), id_kv, (it > 0) || (kk > 0));
+          mma_bf16(tbase + TM_DK, d_ds0 + g * kTileStep + 2 * k4, d_qmn0 + st * kTileStep + 128 * kk, id_kv,
+                   (it > 0) || (kk > 0));
         }
       };
       bool ok = mbar_wait(b_kvready, 0, abort_flag, p.st, 21);
@@ -768,12 +778,11 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
         if (it > 0 && !mbar_wait(b_dqempty, (it - 1) & 1, abort_flag, p.st, 24)) break;
         fence_after();
         dvdk(it, 1);
+        mma_commit(b_qempty + 8 * st);   // Q, dO of this block are read for the last time
 #pragma unroll
         for (int kk = 0; kk < kK / 16; ++kk)     // k = keys; dS read MN-major from the dS^T tiles
-          mma_bf16(tbase + TM_DQ, sdesc(sbase + OFF_DS + kk * 2048, kTile, 1024),
-                   sdesc(sbase + OFF_K + kk * 2048, 8192, 1024), id_q, kk > 0);
+          mma_bf16(tbase + TM_DQ, d_ds_mn + 128 * kk, d_kmn + 128 * kk, id_q, kk > 0);
         mma_commit(b_dqfull);
-        mma_commit(b_qempty + 8 * st);
         mma_commit(b_pempty);
         mma_commit(b_pempty + 8);
         if (more) sdp(it + 1, 1);
@@ -815,23 +824,25 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       const float* Dd = sD + buf * 128;
       // a full half-block strictly below the diagonal needs no masking
       const bool interior = (!p.causal || i0 > j0) && qrows >= 64 * (g + 1) && len - j0 >= kK;
-      uint32_t pk[2][16], dk[2][16];   // bf16 pairs of P^T and dS^T for the 64 queries
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
+      bool stop = false;
+      const uint32_t rowoff = g * kTile + kr * 128;
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {          // 32 queries at a time
         const uint32_t col = TM_S + g * 128 + cc * 32;
         uint32_t sr[32], dr[32];
         tmem_ld32_async(tbase + lane_off + col, sr);
         tmem_ld32_async(tbase + lane_off + col + 64, dr);
         tmem_wait_ld();
+        uint32_t pk[16], dk[16];   // bf16 pairs of P^T and dS^T
         if (interior) {
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int qi = 64 * g + cc * 32 + 2 * e;
             const float p0 = exp2_approx(__uint_as_float(sr[2 * e]) * p.scale_log2 - L[qi]);
             const float p1 = exp2_approx(__uint_as_float(sr[2 * e + 1]) * p.scale_log2 - L[qi + 1]);
-            pk[cc][e] = pack_bf16x2(p0, p1);
-            dk[cc][e] = pack_bf16x2(p0 * (__uint_as_float(dr[2 * e]) - Dd[qi]),
-                                    p1 * (__uint_as_float(dr[2 * e + 1]) - Dd[qi + 1]));
+            pk[e] = pack_bf16x2(p0, p1);
+            dk[e] = pack_bf16x2(p0 * (__uint_as_float(dr[2 * e]) - Dd[qi]),
+                                p1 * (__uint_as_float(dr[2 * e + 1]) - Dd[qi + 1]));
           }
         } else {
 #pragma unroll
@@ -844,24 +855,25 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
               pv[k] = valid ? exp2_approx(__uint_as_float(sr[2 * e + k]) * p.scale_log2 - L[qi]) : 0.f;
               dv[k] = valid ? pv[k] * (__uint_as_float(dr[2 * e + k]) - Dd[qi]) : 0.f;
             }
-            pk[cc][e] = pack_bf16x2(pv[0], pv[1]);
-            dk[cc][e] = pack_bf16x2(dv[0], dv[1]);
+            pk[e] = pack_bf16x2(pv[0], pv[1]);
+            dk[e] = pack_bf16x2(dv[0], dv[1]);
           }
         }
-      }
-      // the P/dS tile of this half is free once dQ of the previous block is done
-      if (it > 0 && !mbar_wait(b_pempty + 8 * g, (it - 1) & 1, &no_abort, p.st, 26)) break;
-      const uint32_t rowoff = g * kTile + kr * 128;
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc)
+        // the P/dS tile of this half is free once dQ of the previous block is done
+        if (cc == 0 && it > 0 && !mbar_wait(b_pempty + 8 * g, (it - 1) & 1, &no_abort, p.st, 26)) {
+          stop = true;
+          break;
+        }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const uint32_t phys = (((cc * 4 + u) ^ (kr & 7)) * 16);
           *reinterpret_cast<uint4*>(sm + OFF_P + rowoff + phys) =
-              make_uint4(pk[cc][4 * u], pk[cc][4 * u + 1], pk[cc][4 * u + 2], pk[cc][4 * u + 3]);
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
           *reinterpret_cast<uint4*>(sm + OFF_DS + rowoff + phys) =
-              make_uint4(dk[cc][4 * u], dk[cc][4 * u + 1], dk[cc][4 * u + 2], dk[cc][4 * u + 3]);
+              make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
         }
+      }
+      if (stop) break;
       fence_before();
       fence_async_smem();
       mbar_arrive(b_pfull + 8 * g);
