@@ -14,9 +14,11 @@ on the host cores instead, on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
+import re
 import subprocess
 import sys
 import time
@@ -51,6 +53,25 @@ def config_dict(s, l2):
                         f"{int(s.f * 100)}% tokens filtered per sequence (Gumbel scores)",
             "global_batch": s.B, "seq_len": s.T, "filtered_fraction": s.f, "parallelism": "replicas",
             "l2": l2}
+
+
+# ---------------------------------------------------------------------------
+GEMM_PROFILE = os.path.join(ROOT, "profiles", "tc_gemm_2sm_tinyllama_case.md")
+GEMM_SOURCE = os.path.join(ROOT, "sparse_backward_gemm_gb300", "csrc", "gemm_tc.cu")
+
+
+def gemm_traffic():
+    """DRAM bytes (read + write) of one step's GEMM launches, from the committed ncu summary,
+    as long as the GEMM source is still the one profiled; else None."""
+    try:
+        text = open(GEMM_PROFILE).read()
+        want = re.search(r"gemm_tc\.cu sha256: ([0-9a-f]+)", text).group(1)
+        nbytes = int(re.search(r"traffic_bytes_per_step: (\d+)", text).group(1))
+        with open(GEMM_SOURCE, "rb") as f:
+            have = hashlib.sha256(f.read()).hexdigest()
+    except (OSError, AttributeError, ValueError):
+        return None
+    return nbytes if have.startswith(want) else None
 
 
 # ---------------------------------------------------------------------------
@@ -395,7 +416,8 @@ def run_ours(args):
             "roofline": {"bound": "tensor", "kernel": "tc_gemm (tcgen05 bf16 GEMM, all launches of a step)",
                          "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": achieved / peaks["bf16_tflops"], "peak_source": f"bf16_tflops ({src})",
-                         "traffic": None, "gemm_ms_per_step": gemm_ms / args.steps,
+                         "traffic": gemm_traffic(), "traffic_unit": "bytes per step (8 launches), ncu cold-cache",
+                         "gemm_ms_per_step": gemm_ms / args.steps,
                          "timing": "per-launch CUDA events, every launch on one stream (serialised pass)",
                          "step_ms_serialised": step_ms_prof},
             "kernels_ms_per_step": {k: round(v[1] / args.steps, 4) for k, v in sorted(per.items())},
