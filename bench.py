@@ -41,6 +41,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--workload", default=WORKLOAD, choices=sorted(k for k in workloads.WORKLOADS if k.endswith("_layer")),
+                   help="block shape for --case gemm / attn")
     p.add_argument("--case", default="layer", choices=["layer", "gemm", "attn"],
                    help="layer: the benchmark; gemm / attn: one kernel family on a small input "
                         "(larger than L2) for profiler captures")
@@ -441,7 +443,7 @@ def run_case(args):
     import sparse_backward_gemm_gb300 as cl
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(0)
-    s = workloads.WORKLOADS[WORKLOAD]
+    s = workloads.WORKLOADS[args.workload]
     keep = workloads.keep_mask(s.B, s.T, s.f, s.mask, s.seed_base)
     mask = torch.from_numpy(keep).to(dev)
     M = s.M

@@ -955,28 +955,387 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// tcgen05 D pre-pass, head dim 64.  One CTA per (sequence, query head, 128
-// queries): O' = sum over kept causal keys of P V, D = rowsum(dO * O').
-//   warp 0     TMA: Q, dO once; K_j, V_j per key block (2 stages)
+// tcgen05 main pass, head dim 128.  One CTA per work item (128 kept keys,
+// sequence, kv head, a chunk of hc query heads), iterating over blocks of 64
+// queries.  The TMEM budget sets the shape: S^T and dP^T (64 columns each),
+// dV and dK (128 each) leave 64 columns, so dQ is formed transposed,
+// dQ^T = K^T dS^T (M = 128 head dims, N = 64 queries).
+//   warp 0      TMA: K, V once; Q_i, dO_i per iteration (2 stages)
+//   warp 1      TMEM owner; one lane issues the MMAs:
+//                 S^T = K Q^T, dP^T = V dO^T          (M 128 keys, N 64 queries)
+//                 dV += P^T dO, dK += dS^T Q          (M 128 keys, N 128)
+//                 dQ^T = K^T dS^T                     (M 128 head dims, N 64 queries)
+//   warps 2-9   one key row and 32 of the 64 queries per thread: P^T, dS^T
+//               from TMEM -> bf16 -> shared
+//   warps 10-13 one head-dim row of dQ^T per thread: TMEM -> shared (as dQ
+//               rows) -> TMA reduce-add into the f32 dQ accumulator; at the
+//               end dK, dV likewise, 64 columns at a time
+// Tiles are 64-column (128-byte) swizzle chunks.
+// TMEM columns: S^T 0-63, dP^T 64-127, dV 128-255, dK 256-383, dQ^T 384-447.
+namespace tcattn128 {
+constexpr int kQ = 64, kK = 128, kD = 128;
+constexpr uint32_t kKChunk = 16384;                 // 128 rows x 128 bytes
+constexpr uint32_t kQChunk = 8192;                  // 64 rows x 128 bytes
+constexpr uint32_t OFF_K = 0, OFF_V = 2 * kKChunk, OFF_Q = 4 * kKChunk, OFF_DO = OFF_Q + 4 * kQChunk,
+                   OFF_P = OFF_DO + 4 * kQChunk, OFF_DS = OFF_P + kKChunk, OFF_ST = OFF_DS + kKChunk,
+                   OFF_LD = OFF_ST + 2 * kKChunk, OFF_BAR = OFF_LD + 1024;
+constexpr size_t kSmem = 1024 + OFF_BAR + 256;
+constexpr uint32_t TM_S = 0, TM_DP = 64, TM_DV = 128, TM_DK = 256, TM_DQ = 384;
+constexpr int kSoftWarps = 8;                       // two per TMEM lane quadrant
+constexpr int kThreads = 32 * (2 + kSoftWarps + 4);
+static_assert(kSmem <= 232448, "shared memory");
+}  // namespace tcattn128
+
+__global__ void __launch_bounds__(tcattn128::kThreads, 1)
+    attn_main_tc128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                           const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                           const __grid_constant__ CUtensorMap tmdQ, const __grid_constant__ CUtensorMap tmdK,
+                           const __grid_constant__ CUtensorMap tmdV, MainTc p) {
+  using namespace tc;
+  using namespace tcattn128;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int per_j = p.B * p.Hkv * p.nhc;
+  const int j = blockIdx.x / per_j;
+  const int rem = blockIdx.x % per_j;
+  const int b = rem / (p.Hkv * p.nhc);
+  const int hk = (rem / p.nhc) % p.Hkv;
+  const int hci = rem % p.nhc;
+  const int s0 = p.cu_kept[b], len = p.cu_kept[b + 1] - s0;
+  const int j0 = j * kK;
+  if (j0 >= len) return;   // uniform: nothing initialised yet
+  const int nqb = (len + kQ - 1) / kQ;
+  const int i_start = p.causal ? j0 / kQ : 0;
+  const int nq_head = nqb - i_start;
+  const int n_iter = p.hc * nq_head;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  const uint32_t b_kv = smem_u32(bars + 0), b_qfull = smem_u32(bars + 1), b_qempty = smem_u32(bars + 3),
+                 b_sfull = smem_u32(bars + 5), b_pfull = smem_u32(bars + 6), b_pempty = smem_u32(bars + 7),
+                 b_dqfull = smem_u32(bars + 8), b_dqempty = smem_u32(bars + 9), b_kvready = smem_u32(bars + 10),
+                 b_qready = smem_u32(bars + 11);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* sL = reinterpret_cast<float*>(sm + OFF_LD);   // [2][64]
+  float* sD = sL + 128;                                // [2][64]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(b_kv, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(b_qfull + 8 * s, 1);
+      mbar_init(b_qempty + 8 * s, 1);
+      mbar_init(b_qready + 8 * s, 1);
+    }
+    mbar_init(b_sfull, 1);
+    mbar_init(b_pfull, 32 * kSoftWarps);
+    mbar_init(b_pempty, 1);
+    mbar_init(b_dqfull, 1);
+    mbar_init(b_dqempty, 128);
+    mbar_init(b_kvready, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint32_t sbase = smem_u32(sm);
+  // The consumer groups below synchronise with named barriers, so they must
+  // leave together: their waits give up only on their own timeout, which every
+  // thread of the group reaches on the same barrier phase.
+  volatile int no_abort = 0;
+
+  if (warp == 0) {
+    // ---------------- TMA producer (lane 0) + tile finishing (whole warp) ----------------
+    // rows past the sequence are zeroed in shared memory before the MMAs see
+    // a tile (a masked probability of 0 times a non-finite row would leak)
+    auto zero_rows = [&](uint32_t off, int rows, int from) {
+      for (int i = lane; i < (rows - from) * 8; i += 32)
+        *reinterpret_cast<uint4*>(sm + off + (from + i / 8) * 128 + (i % 8) * 16) = make_uint4(0, 0, 0, 0);
+    };
+    auto issue = [&](int it) -> bool {
+      const int st = it & 1, use = it >> 1;
+      if (!mbar_wait(b_qempty + 8 * st, (use & 1) ^ 1, abort_flag, p.st, 50)) return false;
+      const int h = hk * p.G + hci * p.hc + it / nq_head;
+      const int i0 = (i_start + it % nq_head) * kQ;
+      mbar_expect_tx(b_qfull + 8 * st, 4 * kQChunk);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        tma_load_2d(sbase + OFF_Q + st * 2 * kQChunk + c * kQChunk, &tmQ, b_qfull + 8 * st, h * kD + 64 * c, s0 + i0);
+        tma_load_2d(sbase + OFF_DO + st * 2 * kQChunk + c * kQChunk, &tmdO, b_qfull + 8 * st, h * kD + 64 * c,
+                    s0 + i0);
+      }
+      return true;
+    };
+    const int krows = min(kK, len - j0);
+    bool ok = true;
+    if (lane == 0) {
+      mbar_expect_tx(b_kv, 4 * kKChunk);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        tma_load_2d(sbase + OFF_K + c * kKChunk, &tmK, b_kv, hk * kD + 64 * c, s0 + j0);
+        tma_load_2d(sbase + OFF_V + c * kKChunk, &tmV, b_kv, hk * kD + 64 * c, s0 + j0);
+      }
+    }
+    if (mbar_wait(b_kv, 0, &no_abort, p.st, 58)) {
+      if (krows < kK)
+        for (int c = 0; c < 4; ++c) zero_rows(OFF_K + c * kKChunk, kK, krows);   // K chunks then V chunks
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_kvready);
+    } else {
+      ok = false;
+    }
+    // block it+1 is loaded once block it is handed over (the MMA thread frees
+    // the stage block it+1 reuses only after it has taken block it)
+    if (lane == 0 && ok && n_iter > 0) ok = issue(0);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    for (int it = 0; ok && it < n_iter; ++it) {
+      const int st = it & 1, use = it >> 1;
+      if (!mbar_wait(b_qfull + 8 * st, use & 1, &no_abort, p.st, 59)) break;
+      const int i0 = (i_start + it % nq_head) * kQ;
+      const int qrows = min(kQ, len - i0);
+      if (qrows < kQ)
+        for (int c = 0; c < 2; ++c) {
+          zero_rows(OFF_Q + st * 2 * kQChunk + c * kQChunk, kQ, qrows);
+          zero_rows(OFF_DO + st * 2 * kQChunk + c * kQChunk, kQ, qrows);
+        }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_qready + 8 * st);
+      int nxt = 1;
+      if (lane == 0 && it + 1 < n_iter) nxt = issue(it + 1) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, nxt, 0)) break;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t id_kv = idesc_bf16(128, 128, false, true);
+      constexpr uint32_t id_q = idesc_bf16(128, 64, true, true);
+      // descriptors built once; a k-step moves the start address by a constant
+      const uint64_t d_k = sdesc(sbase + OFF_K, 16, 1024), d_v = sdesc(sbase + OFF_V, 16, 1024);
+      const uint64_t d_q = sdesc(sbase + OFF_Q, 16, 1024), d_do = sdesc(sbase + OFF_DO, 16, 1024);
+      const uint64_t d_qmn = sdesc(sbase + OFF_Q, kQChunk, 1024), d_domn = sdesc(sbase + OFF_DO, kQChunk, 1024);
+      const uint64_t d_p = sdesc(sbase + OFF_P, 16, 1024), d_ds = sdesc(sbase + OFF_DS, 16, 1024);
+      const uint64_t d_kmn = sdesc(sbase + OFF_K, kKChunk, 1024);   // K^T: MN-major A, head-dim chunks
+      const uint64_t d_dsmn = sdesc(sbase + OFF_DS, kKChunk, 1024); // dS^T: MN-major B
+      constexpr uint64_t kQStep = 2 * kQChunk / 16, kKCh = kKChunk / 16, kQCh = kQChunk / 16;
+      bool ok = mbar_wait(b_kvready, 0, abort_flag, p.st, 51);
+      for (int it = 0; ok && it < n_iter; ++it) {
+        const int st = it & 1, use = it >> 1;
+        if (!mbar_wait(b_qready + 8 * st, use & 1, abort_flag, p.st, 52)) break;
+        fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {   // k = head dims: chunk kk / 4, 32 bytes a step inside it
+          const uint64_t ko = (kk >> 2) * kKCh + 2 * (kk & 3), qo = st * kQStep + (kk >> 2) * kQCh + 2 * (kk & 3);
+          mma_bf16(tbase + TM_S, d_k + ko, d_q + qo, id_s, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint64_t ko = (kk >> 2) * kKCh + 2 * (kk & 3), qo = st * kQStep + (kk >> 2) * kQCh + 2 * (kk & 3);
+          mma_bf16(tbase + TM_DP, d_v + ko, d_do + qo, id_s, kk > 0);
+        }
+        mma_commit(b_sfull);
+        if (!mbar_wait(b_pfull, it & 1, abort_flag, p.st, 53)) break;
+        if (it > 0 && !mbar_wait(b_dqempty, (it - 1) & 1, abort_flag, p.st, 54)) break;
+        fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kQ / 16; ++kk)     // k = queries, 16 rows (2 KB) a step
+          mma_bf16(tbase + TM_DV, d_p + 2 * kk, d_domn + st * kQStep + 128 * kk, id_kv, (it > 0) || (kk > 0));
+#pragma unroll
+        for (int kk = 0; kk < kQ / 16; ++kk)
+          mma_bf16(tbase + TM_DK, d_ds + 2 * kk, d_qmn + st * kQStep + 128 * kk, id_kv, (it > 0) || (kk > 0));
+        mma_commit(b_qempty + 8 * st);          // Q, dO of this block are read for the last time
+#pragma unroll
+        for (int kk = 0; kk < kK / 16; ++kk)     // k = keys, 16 rows (2 KB) a step
+          mma_bf16(tbase + TM_DQ, d_kmn + 128 * kk, d_dsmn + 128 * kk, id_q, kk > 0);
+        mma_commit(b_dqfull);
+        mma_commit(b_pempty);
+      }
+    }
+  } else if (warp < 2 + kSoftWarps) {
+    // ---------------- softmax warps: one key row, 32 queries per thread ----------------
+    const int g = (warp - 2) >> 2;              // which 32 queries of the block
+    const int tg = threadIdx.x - 64 - 128 * g;  // 0..127 within the group
+    const int q = warp & 3;
+    const int kr = q * 32 + lane;
+    const int key = j0 + kr;
+    const bool kvalid = key < len;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    // lse (tg 0-31) and D (tg 32-63) of this group's queries of the block
+    // after the current one are fetched one iteration early
+    auto fetch = [&](int it) -> float {
+      if (tg >= 64) return 0.f;
+      const int h = hk * p.G + hci * p.hc + it / nq_head;
+      const int i0 = (i_start + it % nq_head) * kQ;
+      const int qq = 32 * g + (tg & 31);
+      if (qq >= min(kQ, len - i0)) return 0.f;
+      const float* src = tg < 32 ? p.lse2 : p.Dvec;
+      return src[(long long)h * p.M + s0 + i0 + qq];
+    };
+    float nxt = n_iter > 0 ? fetch(0) : 0.f;
+    for (int it = 0; it < n_iter; ++it) {
+      const int i0 = (i_start + it % nq_head) * kQ;
+      const int qrows = min(kQ, len - i0);
+      const int buf = it & 1;
+      if (tg < 64) (tg < 32 ? sL : sD)[buf * 64 + 32 * g + (tg & 31)] = nxt;
+      if (it + 1 < n_iter) nxt = fetch(it + 1);
+      named_bar(1, 32 * kSoftWarps);
+      if (!mbar_wait(b_sfull, it & 1, &no_abort, p.st, 55)) break;
+      if (it > 0 && !mbar_wait(b_pempty, (it - 1) & 1, &no_abort, p.st, 56)) break;
+      fence_after();
+      const float* L = sL + buf * 64;
+      const float* Dd = sD + buf * 64;
+      // all 32 queries past the whole key block (and inside the sequence) need no mask
+      const bool interior = (!p.causal || i0 >= j0 + kK) && qrows >= 32 * (g + 1) && len - j0 >= kK;
+      uint32_t sr[32], dr[32];
+      tmem_ld32_async(tbase + lane_off + TM_S + 32 * g, sr);
+      tmem_ld32_async(tbase + lane_off + TM_DP + 32 * g, dr);
+      tmem_wait_ld();
+      uint32_t pk[16], dk[16];
+      if (interior) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int qi = 32 * g + 2 * e;
+          const float p0 = exp2_approx(__uint_as_float(sr[2 * e]) * p.scale_log2 - L[qi]);
+          const float p1 = exp2_approx(__uint_as_float(sr[2 * e + 1]) * p.scale_log2 - L[qi + 1]);
+          pk[e] = pack_bf16x2(p0, p1);
+          dk[e] = pack_bf16x2(p0 * (__uint_as_float(dr[2 * e]) - Dd[qi]),
+                              p1 * (__uint_as_float(dr[2 * e + 1]) - Dd[qi + 1]));
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float pv[2], dv[2];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int qi = 32 * g + 2 * e + k;
+            const bool valid = kvalid && qi < qrows && (!p.causal || key <= i0 + qi);
+            pv[k] = valid ? exp2_approx(__uint_as_float(sr[2 * e + k]) * p.scale_log2 - L[qi]) : 0.f;
+            dv[k] = valid ? pv[k] * (__uint_as_float(dr[2 * e + k]) - Dd[qi]) : 0.f;
+          }
+          pk[e] = pack_bf16x2(pv[0], pv[1]);
+          dk[e] = pack_bf16x2(dv[0], dv[1]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t phys = (((4 * g + u) ^ (kr & 7)) * 16);
+        *reinterpret_cast<uint4*>(sm + OFF_P + kr * 128 + phys) =
+            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        *reinterpret_cast<uint4*>(sm + OFF_DS + kr * 128 + phys) =
+            make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+      }
+      fence_before();
+      fence_async_smem();
+      mbar_arrive(b_pfull);
+    }
+  } else {
+    // ---------------- dQ / dK / dV epilogue ----------------
+    const int t = threadIdx.x - 32 * (2 + kSoftWarps);
+    const int q = warp & 3;
+    const int r = q * 32 + lane;                // TMEM lane: head dim (dQ^T) or key (dK, dV)
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t stage = sbase + OFF_ST;
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int h = hk * p.G + hci * p.hc + it / nq_head;
+      const int i0 = (i_start + it % nq_head) * kQ;
+      if (!mbar_wait(b_dqfull, it & 1, &no_abort, p.st, 57)) { ok = false; break; }
+      fence_after();
+      float v[64];                               // dQ[query c][head dim r], c = 0..63
+      tmem_ld32(tbase + lane_off + TM_DQ, v);
+      tmem_ld32(tbase + lane_off + TM_DQ + 32, v + 32);
+      fence_before();
+      mbar_arrive(b_dqempty);
+      if (t == 0) bulk_wait_read_all();
+      named_bar(2, 128);
+      // staging: four 32-column boxes of [64 query rows x 128 bytes]; head dim r
+      // sits in box q, column lane
+#pragma unroll
+      for (int c = 0; c < kQ; ++c) {
+        const uint32_t off = q * 8192 + c * 128 + ((((lane >> 2) ^ (c & 7)) * 16)) + (lane & 3) * 4;
+        *reinterpret_cast<float*>(sm + OFF_ST + off) = v[c];
+      }
+      fence_async_smem();
+      named_bar(2, 128);
+      if (t == 0) {
+#pragma unroll
+        for (int bx = 0; bx < 4; ++bx) tma_reduce_add_2d(&tmdQ, stage + bx * 8192, h * kD + 32 * bx, s0 + i0);
+        bulk_commit();
+      }
+    }
+    if (ok) {
+      // every MMA has completed (the last dQ commit covers them all): drain
+      // dK, dV 64 columns at a time through two [128 x 32] f32 boxes
+#pragma unroll 1
+      for (int pass = 0; pass < 4; ++pass) {
+        const uint32_t col = (pass < 2 ? TM_DK : TM_DV) + 64 * (pass & 1);
+        float v[64];
+        tmem_ld32(tbase + lane_off + col, v);
+        tmem_ld32(tbase + lane_off + col + 32, v + 32);
+        if (t == 0) bulk_wait_read_all();
+        named_bar(2, 128);
+#pragma unroll
+        for (int bx = 0; bx < 2; ++bx)
+#pragma unroll
+          for (int g8 = 0; g8 < 8; ++g8) {
+            const uint32_t phys = ((g8 ^ (r & 7)) * 16);
+            *reinterpret_cast<float4*>(sm + OFF_ST + bx * kKChunk + r * 128 + phys) =
+                make_float4(v[bx * 32 + 4 * g8], v[bx * 32 + 4 * g8 + 1], v[bx * 32 + 4 * g8 + 2],
+                            v[bx * 32 + 4 * g8 + 3]);
+          }
+        fence_async_smem();
+        named_bar(2, 128);
+        if (t == 0) {
+          const CUtensorMap* m = pass < 2 ? &tmdK : &tmdV;
+#pragma unroll
+          for (int bx = 0; bx < 2; ++bx)
+            tma_reduce_add_2d(m, stage + bx * kKChunk, hk * kD + 64 * (pass & 1) + 32 * bx, s0 + j0);
+          bulk_commit();
+        }
+      }
+    }
+    if (t == 0) bulk_wait_all();
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 D pre-pass, head dim 64 or 128.  One CTA per (sequence, query
+// head, 128 queries): O' = sum over kept causal keys of P V, D = rowsum(dO * O').
+// Q, K and V tiles are held as 64-column (128-byte) swizzle chunks.
+//   warp 0     TMA: Q once; K_j, V_j per key block (3 stages at head dim 64, 2 at 128)
 //   warp 1     TMEM owner; one lane issues S_j = Q K_j^T (into one of two
 //              TMEM buffers, so S_{j+1} overlaps the softmax of block j) and
 //              O' += P_j V_j
 //   warps 2-9  one query row and 64 of the 128 keys per thread: P_j from
 //              TMEM -> bf16 -> shared; at the end D from O' (TMEM) and dO
-//              (shared), each half of the row's columns summed separately
-// TMEM columns: S buffers 0-127 and 128-255, O' 256-319.
-namespace tcdprep {
-constexpr int kQ = 128, kK = 128, kD = 64;
-constexpr uint32_t kTile = 16384;
-constexpr int kKV = 3;                                   // K/V stages
-constexpr uint32_t OFF_Q = 0, OFF_DO = kTile, OFF_K = 2 * kTile, OFF_P = OFF_K + kKV * 2 * kTile,
-                   OFF_BAR = OFF_P + 4 * kTile;
-constexpr uint32_t OFF_PART = OFF_BAR + 256;              // [2][128] f32 partial dot products
-constexpr size_t kSmem = 1024 + OFF_PART + 1024;
-constexpr uint32_t TM_S = 0, TM_O = 256;
-constexpr int kSoftWarps = 8;                                // two per TMEM lane quadrant
-constexpr int kThreads = 32 * (2 + kSoftWarps);
-}  // namespace tcdprep
+//              (global), each half of the row's columns summed separately
+// TMEM columns: S buffers 0-127 and 128-255, O' from 256 (head-dim columns).
+template <int DH>
+struct DprepCfg {
+  static constexpr int kQ = 128, kK = 128, kD = DH, kCh = DH / 64;   // 64-column chunks
+  static constexpr uint32_t kTile = 16384;                           // 128 rows x 64 columns
+  static constexpr int kKV = DH == 64 ? 3 : 2;                       // K/V stages
+  static constexpr uint32_t kKVBytes = 2 * kCh * kTile;              // K and V of one stage
+  static constexpr uint32_t OFF_Q = 0, OFF_K = kCh * kTile, OFF_P = OFF_K + kKV * kKVBytes,
+                            OFF_BAR = OFF_P + 4 * kTile;
+  static constexpr uint32_t OFF_PART = OFF_BAR + 256;                // [2][128] f32 partial dot products
+  static constexpr size_t kSmem = 1024 + OFF_PART + 1024;
+  static constexpr uint32_t TM_S = 0, TM_O = 256;
+  static constexpr int kSoftWarps = 8;                               // two per TMEM lane quadrant
+  static constexpr int kThreads = 32 * (2 + kSoftWarps);
+  static_assert(kSmem <= 232448, "shared memory");
+};
 
 struct DprepTc {
   int B, T, H, G, causal, nqb;
@@ -984,16 +1343,22 @@ struct DprepTc {
   const int32_t* cu_kept;
   const float* lse2;
   float* Dvec;
+  const __nv_bfloat16* dO;   // COMPACT rows, head h at columns h * DH
+  long long do_ld;
   long long M;
   DevStatus* st;
 };
 
-__global__ void __launch_bounds__(tcdprep::kThreads, 1)
+template <int DH>
+__global__ void __launch_bounds__(DprepCfg<DH>::kThreads, 1)
     attn_dprep_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                         DprepTc p) {
+                         const __grid_constant__ CUtensorMap tmV, DprepTc p) {
   using namespace tc;
-  using namespace tcdprep;
+  using Cfg = DprepCfg<DH>;
+  constexpr int kQ = Cfg::kQ, kK = Cfg::kK, kD = Cfg::kD, kCh = Cfg::kCh, kKV = Cfg::kKV, kSoftWarps = Cfg::kSoftWarps;
+  constexpr uint32_t kTile = Cfg::kTile, kKVBytes = Cfg::kKVBytes, OFF_Q = Cfg::OFF_Q, OFF_K = Cfg::OFF_K,
+                     OFF_P = Cfg::OFF_P, OFF_BAR = Cfg::OFF_BAR, OFF_PART = Cfg::OFF_PART, TM_S = Cfg::TM_S,
+                     TM_O = Cfg::TM_O;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // items: query block descending (most key blocks first), then sequence, head
@@ -1046,56 +1411,68 @@ __global__ void __launch_bounds__(tcdprep::kThreads, 1)
     auto issue = [&](int j) -> bool {
       const int st = j % kKV, use = j / kKV;
       if (!mbar_wait(b_kvempty + 8 * st, (use & 1) ^ 1, abort_flag, p.st, 40)) return false;
-      mbar_expect_tx(b_kvfull + 8 * st, 2 * kTile);
-      tma_load_2d(sbase + OFF_K + st * 2 * kTile, &tmK, b_kvfull + 8 * st, hk * kD, s0 + j * kK);
-      tma_load_2d(sbase + OFF_K + st * 2 * kTile + kTile, &tmV, b_kvfull + 8 * st, hk * kD, s0 + j * kK);
+      mbar_expect_tx(b_kvfull + 8 * st, kKVBytes);
+      const uint32_t kb = sbase + OFF_K + st * kKVBytes;
+#pragma unroll
+      for (int c = 0; c < kCh; ++c) {
+        tma_load_2d(kb + c * kTile, &tmK, b_kvfull + 8 * st, hk * kD + 64 * c, s0 + j * kK);
+        tma_load_2d(kb + (kCh + c) * kTile, &tmV, b_kvfull + 8 * st, hk * kD + 64 * c, s0 + j * kK);
+      }
       return true;
     };
     int ok = 1;
     if (lane == 0) {
-      mbar_expect_tx(b_q, 2 * kTile);
-      tma_load_2d(sbase + OFF_Q, &tmQ, b_q, h * kD, s0 + i0);
-      tma_load_2d(sbase + OFF_DO, &tmdO, b_q, h * kD, s0 + i0);
+      mbar_expect_tx(b_q, kCh * kTile);
+#pragma unroll
+      for (int c = 0; c < kCh; ++c) tma_load_2d(sbase + OFF_Q + c * kTile, &tmQ, b_q, h * kD + 64 * c, s0 + i0);
       ok = issue(0) ? 1 : 0;
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
     // With three stages block j+1 can be requested before block j is
     // released: the request waits for the P V of block j-2, which the MMA
-    // issues once block j-1 is released.
+    // issues once block j-1 is released.  With two stages the request waits
+    // for the P V of block j-1, which the MMA issues only after it has taken
+    // block j, so block j is released first.
     for (int j = 0; ok && j < nj; ++j) {
       const int st = j % kKV, use = j / kKV;
       int nxt = 1;
-      if (lane == 0 && j + 1 < nj) nxt = issue(j + 1) ? 1 : 0;
-      if (!__shfl_sync(0xffffffffu, nxt, 0)) break;
+      if (kKV >= 3) {
+        if (lane == 0 && j + 1 < nj) nxt = issue(j + 1) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, nxt, 0)) break;
+      }
       if (!mbar_wait(b_kvfull + 8 * st, use & 1, &no_abort, p.st, 47)) break;
       const int krows = min(kK, len - j * kK);
       if (krows < kK) {
-        const uint32_t base = OFF_K + st * 2 * kTile;
+        const uint32_t base = OFF_K + st * kKVBytes;
         for (int i = lane; i < (kK - krows) * 8; i += 32) {
           const uint32_t off = (krows + i / 8) * 128 + (i % 8) * 16;
-          *reinterpret_cast<uint4*>(sm + base + off) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(sm + base + kTile + off) = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int c = 0; c < 2 * kCh; ++c) *reinterpret_cast<uint4*>(sm + base + c * kTile + off) = make_uint4(0, 0, 0, 0);
         }
       }
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_kvready + 8 * st);
+      if (kKV < 3) {
+        if (lane == 0 && j + 1 < nj) nxt = issue(j + 1) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, nxt, 0)) break;
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t id_o = idesc_bf16(128, 64, false, true);
+      constexpr uint32_t id_o = idesc_bf16(128, kD, false, true);
       bool ok = mbar_wait(b_q, 0, abort_flag, p.st, 41);
       // O' += P_{jj} V_{jj} for the block whose P the softmax has finished
       auto pv = [&](int jj) -> bool {
         const int kst = jj % kKV, pb = jj & 1;
         if (!mbar_wait(b_pfull, jj & 1, abort_flag, p.st, 42)) return false;
         fence_after();
-        const uint32_t sv = sbase + OFF_K + kst * 2 * kTile + kTile;
+        const uint32_t sv = sbase + OFF_K + kst * kKVBytes + kCh * kTile;
 #pragma unroll
-        for (int kk = 0; kk < kK / 16; ++kk) {
+        for (int kk = 0; kk < kK / 16; ++kk) {   // V as the MN-major B: head-dim chunks kTile apart
           const uint32_t pa = sbase + OFF_P + pb * 2 * kTile + (kk >> 2) * kTile + (kk & 3) * 32;
-          mma_bf16(tbase + TM_O, sdesc(pa, 16, 1024), sdesc(sv + kk * 2048, 8192, 1024), id_o, (jj > 0) || (kk > 0));
+          mma_bf16(tbase + TM_O, sdesc(pa, 16, 1024), sdesc(sv + kk * 2048, kTile, 1024), id_o, (jj > 0) || (kk > 0));
         }
         mma_commit(b_kvempty + 8 * kst);
         mma_commit(b_pempty + 8 * pb);
@@ -1105,11 +1482,13 @@ __global__ void __launch_bounds__(tcdprep::kThreads, 1)
         const int kst = j % kKV, kuse = j / kKV, sb = j & 1;
         if (!mbar_wait(b_kvready + 8 * kst, kuse & 1, abort_flag, p.st, 43)) { ok = false; break; }
         fence_after();
-        const uint32_t sk = sbase + OFF_K + kst * 2 * kTile;
+        const uint32_t sk = sbase + OFF_K + kst * kKVBytes;
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_bf16(tbase + TM_S + sb * 128, sdesc(sbase + OFF_Q + kk * 32, 16, 1024), sdesc(sk + kk * 32, 16, 1024),
-                   id_s, kk > 0);
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kTile + (kk & 3) * 32;
+          mma_bf16(tbase + TM_S + sb * 128, sdesc(sbase + OFF_Q + off, 16, 1024), sdesc(sk + off, 16, 1024), id_s,
+                   kk > 0);
+        }
         mma_commit(b_sfull + 8 * sb);
         if (j > 0 && !pv(j - 1)) { ok = false; break; }
       }
@@ -1122,6 +1501,15 @@ __global__ void __launch_bounds__(tcdprep::kThreads, 1)
     const int r = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const float L = (r < qrows) ? p.lse2[(long long)h * p.M + s0 + i0 + r] : 0.f;
+    // this thread's half of its dO row, loaded now so the latency hides behind the key loop
+    uint4 dov[kD / 16];
+#pragma unroll
+    for (int u = 0; u < kD / 16; ++u) {
+      dov[u] = make_uint4(0, 0, 0, 0);
+      if (r < qrows)
+        dov[u] = *reinterpret_cast<const uint4*>(p.dO + (long long)(s0 + i0 + r) * p.do_ld + h * kD + half * (kD / 2) +
+                                                 8 * u);
+    }
     bool ok = true;
     for (int j = 0; j < nj; ++j) {
       const int st = j & 1, use = j >> 1;
@@ -1165,15 +1553,19 @@ __global__ void __launch_bounds__(tcdprep::kThreads, 1)
     float d = 0.f;
     if (ok && mbar_wait(b_ofull, 0, &no_abort, p.st, 46)) {
       fence_after();
-      float o[32];
-      tmem_ld32(tbase + lane_off + TM_O + half * 32, o);
+      // this thread's half of the row: head-dim columns half * kD / 2 ..
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        float x[8];
-        const int chunk = half * 4 + g;
-        unpack8(*reinterpret_cast<const uint4*>(sm + OFF_DO + r * 128 + ((chunk ^ (r & 7)) * 16)), x);
+      for (int cc = 0; cc < kD / 64; ++cc) {
+        float o[32];
+        const int col = half * (kD / 2) + 32 * cc;
+        tmem_ld32(tbase + lane_off + TM_O + col, o);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) d += x[e] * o[8 * g + e];
+        for (int g = 0; g < 4; ++g) {
+          float x[8];
+          unpack8(dov[4 * cc + g], x);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) d += x[e] * o[8 * g + e];
+        }
       }
     } else {
       ok = false;
@@ -1196,7 +1588,7 @@ cudaError_t run(const Ctx& c, const AttnK& k, float rope_base, const AttnArgs& a
   const size_t smem_prep = 4 * kBlk * LD * sizeof(__nv_bfloat16);
   const size_t smem_main = 4 * kBlk * LD * sizeof(__nv_bfloat16) + kBlk * (kBlk + 8) * sizeof(__nv_bfloat16) +
                            2 * kBlk * sizeof(float);
-  const bool use_tc = (DH == 64) && k.kv_acc;
+  const bool use_tc = k.kv_acc;   // tcgen05 kernels for head dim 64 and 128
   static int seen[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1209,9 +1601,12 @@ cudaError_t run(const Ctx& c, const AttnK& k, float rope_base, const AttnArgs& a
     if (e == cudaSuccess && DH == 64)
       e = cudaFuncSetAttribute(attn_main_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(tcattn::kSmem));
-    if (e == cudaSuccess && DH == 64)
-      e = cudaFuncSetAttribute(attn_dprep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(tcdprep::kSmem));
+    if (e == cudaSuccess && DH == 128)
+      e = cudaFuncSetAttribute(attn_main_tc128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(tcattn128::kSmem));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_dprep_tc_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(DprepCfg<DH>::kSmem));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) seen[dev] = 1;
   }
@@ -1233,25 +1628,34 @@ cudaError_t run(const Ctx& c, const AttnK& k, float rope_base, const AttnArgs& a
     m.B = k.B; m.T = k.T; m.H = k.H; m.Hkv = k.Hkv; m.G = k.G; m.hc = hc; m.nhc = k.G / hc; m.nkb = nkb;
     m.causal = k.causal; m.scale_log2 = k.scale_log2; m.cu_kept = k.cu_kept; m.lse2 = k.lse2; m.Dvec = k.Dvec;
     m.M = k.M; m.st = c.st;
-    CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
-    bool ok = make_tensor_map(&tq, k.q, false, (long long)k.H * DH, a.in_cap, k.q_ld, 64, 128) &&
+    // Q / dO tiles: 128 query rows for head dim 64, 64 for head dim 128
+    constexpr int kQRows = DH == 64 ? tcattn::kQ : tcattn128::kQ;
+    CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv, tq_pre;
+    bool ok = make_tensor_map(&tq, k.q, false, (long long)k.H * DH, a.in_cap, k.q_ld, 64, kQRows) &&
+              make_tensor_map(&tq_pre, k.q, false, (long long)k.H * DH, a.in_cap, k.q_ld, 64, 128) &&
               make_tensor_map(&tk, k.k, false, (long long)k.Hkv * DH, a.in_cap, k.kv_ld, 64, 128) &&
               make_tensor_map(&tv, k.v, false, (long long)k.Hkv * DH, a.in_cap, k.kv_ld, 64, 128) &&
-              make_tensor_map(&tdo, k.dO, false, (long long)k.H * DH, a.in_cap, k.do_ld, 64, 128) &&
-              make_tensor_map(&tdq, k.dq_acc, true, (long long)k.H * DH, k.M, (long long)k.H * DH, 32, 128) &&
+              make_tensor_map(&tdo, k.dO, false, (long long)k.H * DH, a.in_cap, k.do_ld, 64, kQRows) &&
+              make_tensor_map(&tdq, k.dq_acc, true, (long long)k.H * DH, k.M, (long long)k.H * DH, 32, kQRows) &&
               make_tensor_map(&tdk, k.dk_acc, true, (long long)k.Hkv * DH, k.M, (long long)k.Hkv * DH, 32, 128) &&
               make_tensor_map(&tdv, k.dv_acc, true, (long long)k.Hkv * DH, k.M, (long long)k.Hkv * DH, 32, 128);
     if (!ok) return cudaErrorInvalidValue;
     DprepTc dp{};
     dp.B = k.B; dp.T = k.T; dp.H = k.H; dp.G = k.G; dp.causal = k.causal; dp.nqb = nkb;
     dp.scale_log2 = k.scale_log2; dp.cu_kept = k.cu_kept; dp.lse2 = k.lse2; dp.Dvec = k.Dvec; dp.M = k.M;
+    dp.dO = k.dO; dp.do_ld = k.do_ld;
     dp.st = c.st;
     prof_begin(c, "attn_dprep_tc");
-    attn_dprep_tc_kernel<<<k.B * k.H * nkb, tcdprep::kThreads, tcdprep::kSmem, c.stream>>>(tq, tk, tv, tdo, dp);
+    attn_dprep_tc_kernel<DH><<<k.B * k.H * nkb, DprepCfg<DH>::kThreads, DprepCfg<DH>::kSmem, c.stream>>>(tq_pre, tk,
+                                                                                                          tv, dp);
     prof_end(c);
     prof_begin(c, "attn_main_tc");
-    attn_main_tc_kernel<<<k.B * k.Hkv * nkb * m.nhc, tcattn::kThreads, tcattn::kSmem, c.stream>>>(
-        tq, tk, tv, tdo, tdq, tdk, tdv, m);
+    if (DH == 64)
+      attn_main_tc_kernel<<<k.B * k.Hkv * nkb * m.nhc, tcattn::kThreads, tcattn::kSmem, c.stream>>>(
+          tq, tk, tv, tdo, tdq, tdk, tdv, m);
+    else
+      attn_main_tc128_kernel<<<k.B * k.Hkv * nkb * m.nhc, tcattn128::kThreads, tcattn128::kSmem, c.stream>>>(
+          tq, tk, tv, tdo, tdq, tdk, tdv, m);
     prof_end(c);
   } else {
     prof_begin(c, "attn_main");
@@ -1294,7 +1698,7 @@ cudaError_t launch_attn_bwd(const Ctx& c, const AttnArgs& a) {
   k.M = a.M; k.cap = a.cap > 0 ? a.cap : a.M; k.st = c.st;
   k.rope = a.rope;
   k.dk_acc = a.dk_acc; k.dv_acc = a.dv_acc;
-  k.kv_acc = (a.dh == 64 && a.dk_acc && a.dv_acc && a.in_cap > 0) ? 1 : 0;
+  k.kv_acc = ((a.dh == 64 || a.dh == 128) && a.dk_acc && a.dv_acc && a.in_cap > 0) ? 1 : 0;
   if (a.dh == 64) return run<64>(c, k, a.rope_base, a);
   if (a.dh == 128) return run<128>(c, k, a.rope_base, a);
   return cudaErrorInvalidValue;

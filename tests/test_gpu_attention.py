@@ -33,6 +33,7 @@ def _case(B, T, H, Hkv, dh, f, mask, seed, qk_std=1.0):
 @pytest.mark.parametrize("B,T,H,Hkv,dh,f,mask,rot", [
     (2, 200, 4, 2, 64, 0.4, "gumbel", 64),     # GQA, ragged sequence lengths
     (1, 300, 2, 1, 128, 0.4, "gumbel", 128),   # head dim 128
+    (2, 700, 6, 2, 128, 0.4, "gumbel", 128),   # head dim 128, GQA 3, several 64-query blocks per key block
     (2, 130, 2, 2, 64, 0.6, "span", 32),       # MHA, partial rotary, span mask
     (1, 64, 2, 2, 64, 0.0, "gumbel", 0),       # nothing filtered, no RoPE
     (3, 100, 4, 1, 64, 0.2, "gumbel", 16),
