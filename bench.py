@@ -8,7 +8,11 @@ seeded.  A step is the whole hot path: compaction of the keep-mask, gather of
 the kept rows, the dimension-reduced GEMMs, the filtered attention backward,
 the norm / activation / RoPE backward and the scatter of dx.
 
-Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+Prints one JSON line (rank 0).  The headline numbers are the TinyLlama-shaped
+block's; "configs" adds the same filtered / unfiltered timing for the
+Qwen2.5-shaped block, the Phi-1.5-shaped block at 0/20/40/60% filtered (span
+masks) and the 22-block TinyLlama-shaped stack with its LM head
+(`--headline-only` skips them).  `--impl reference` times the fp64 CPU oracle
 on the host cores instead, on a bounded sample of the same workload.
 """
 from __future__ import annotations
@@ -41,6 +45,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--headline-only", action="store_true",
+                   help="time only the headline block (skip the other block shapes and the stack)")
     p.add_argument("--workload", default=WORKLOAD, choices=sorted(k for k in workloads.WORKLOADS if k.endswith("_layer")),
                    help="block shape for --case gemm / attn")
     p.add_argument("--case", default="layer", choices=["layer", "gemm", "attn"],
@@ -91,14 +97,29 @@ def attn_flops(s, kept_per_seq):
 # synthetic saved activations: a dense bf16 forward on the GPU (input
 # preparation only, outside every timed region)
 def gpu_forward(s, w, x):
+    """Dense forward of one block on the GPU with torch (input preparation, never
+    timed): the saved activations the backward reads, rounded to their storage
+    types.  Llama-style blocks (RMSNorm, GQA, RoPE, SwiGLU, optional QKV bias) and
+    Phi-style parallel blocks (LayerNorm, partial RoPE, GELU-tanh MLP, biases)."""
     import torch
     dev = x.device
     M = s.M
     f = lambda t: t.float()
+    mm = lambda a_, w_: (a_.bfloat16() @ w_.bfloat16()).float()   # bf16 tensor-core matmul
     xf = f(x)
-    rstd1 = torch.rsqrt(xf.pow(2).mean(-1) + s.eps)
-    a = (xf * rstd1[:, None] * f(w["norm1_w"])).bfloat16()
-    qkv = (f(a) @ f(w["w_qkv"])).bfloat16()
+    out = {}
+    if s.norm == "ln":
+        mean1 = xf.mean(-1)
+        rstd1 = torch.rsqrt((xf - mean1[:, None]).pow(2).mean(-1) + s.eps)
+        a = ((xf - mean1[:, None]) * rstd1[:, None] * f(w["norm1_w"]) + f(w["norm1_b"])).bfloat16()
+        out["mean1"] = mean1
+    else:
+        rstd1 = torch.rsqrt(xf.pow(2).mean(-1) + s.eps)
+        a = (xf * rstd1[:, None] * f(w["norm1_w"])).bfloat16()
+    qkv = mm(a, w["w_qkv"])
+    if "b_qkv" in w:
+        qkv = qkv + f(w["b_qkv"])
+    qkv = qkv.bfloat16()
     nq, nk = s.H * s.dh, s.Hkv * s.dh
     pos = torch.arange(s.T, device=dev).repeat(s.B).double()
     half = s.rotary_dim // 2
@@ -128,13 +149,143 @@ def gpu_forward(s, w, x):
             o[rows, h] = (torch.exp(S - l[:, None]) @ f(v[rows, h // G])).bfloat16()
             lse[b, h] = l
     o = o.reshape(M, -1)
-    h_ = (xf + f(o) @ f(w["w_o"])).bfloat16()
+    if s.arch == "phi":
+        f1 = mm(a, w["w_up"])
+        if "b_up" in w:
+            f1 = f1 + f(w["b_up"])
+        out.update(x=x, a=a, rstd1=rstd1, qkv=qkv_rot, o=o, lse=lse, up=f1.bfloat16())
+        return out
+    h_ = (xf + mm(o, w["w_o"])).bfloat16()
     rstd2 = torch.rsqrt(f(h_).pow(2).mean(-1) + s.eps)
     bn = (f(h_) * rstd2[:, None] * f(w["norm2_w"])).bfloat16()
-    gu = (f(bn) @ f(w["w_up"])).bfloat16()
+    gu = mm(bn, w["w_up"]).bfloat16()
     g_, u_ = f(gu[:, :s.F]), f(gu[:, s.F:])
     sact = (g_ * torch.sigmoid(g_) * u_).bfloat16()
-    return dict(x=x, a=a, rstd1=rstd1, qkv=qkv_rot, o=o, lse=lse, h=h_, b=bn, rstd2=rstd2, up=gu, s=sact)
+    out.update(x=x, a=a, rstd1=rstd1, qkv=qkv_rot, o=o, lse=lse, h=h_, b=bn, rstd2=rstd2, up=gu, s=sact)
+    return out
+
+
+def layer_desc(cl, s):
+    return cl.LayerDesc(arch=cl.ARCH_LLAMA if s.arch == "llama" else cl.ARCH_PHI, B=s.B, T=s.T, D=s.D, H=s.H,
+                        Hkv=s.Hkv, dh=s.dh, F=s.F, rotary_dim=s.rotary_dim, rope_base=s.rope_base,
+                        norm=cl.NORM_RMS if s.norm == "rms" else cl.NORM_LAYER, eps=s.eps,
+                        act=cl.ACT_SWIGLU if s.act == "swiglu" else cl.ACT_GELU_TANH, qkv_bias=int(s.qkv_bias),
+                        out_bias=int(s.out_bias), mlp_bias=int(s.mlp_bias))
+
+
+def grad_buffers(s, dev):
+    """f32 weight-gradient buffers of one block (the bias / beta ones where the shape has them)."""
+    import torch
+    shapes = dict(dnorm1_w=(s.D,), dw_qkv=(s.D, s.Nqkv), dw_o=(s.H * s.dh, s.D), dw_up=(s.D, s.Nup),
+                  dw_down=(s.F, s.D))
+    if s.norm == "ln":
+        shapes["dnorm1_b"] = (s.D,)
+    if s.arch == "llama":
+        shapes["dnorm2_w"] = (s.D,)
+    if s.qkv_bias:
+        shapes["db_qkv"] = (s.Nqkv,)
+    if s.out_bias:
+        shapes["db_o"] = (s.D,)
+    if s.mlp_bias:
+        shapes["db_up"] = (s.Nup,)
+        shapes["db_down"] = (s.D,)
+    return {k: torch.empty(v, dtype=torch.float32, device=dev) for k, v in shapes.items()}
+
+
+class Block:
+    """One block's synthetic inputs, saved activations, gradient buffers and
+    workspace on the GPU; step() runs compaction + the layer backward."""
+
+    def __init__(self, cl, s, dev):
+        import torch
+        self.cl, self.s = cl, s
+        wn = workloads.layer_weights(s)
+        tn = workloads.layer_inputs(s)
+        self.keep_np = tn["keep"]
+        self.W = {k: torch.from_numpy(v).to(dev).bfloat16() for k, v in wn.items()}
+        x = torch.from_numpy(tn["x"]).to(dev).bfloat16()
+        self.dout = torch.from_numpy(tn["dout"]).to(dev).bfloat16()
+        self.masks = {"filtered": torch.from_numpy(tn["keep"]).to(dev),
+                      "unfiltered": torch.ones(s.B, s.T, dtype=torch.uint8, device=dev)}
+        with torch.no_grad():
+            self.saved = gpu_forward(s, self.W, x)
+        self.desc = layer_desc(cl, s)
+        self.weights = cl.LayerWeights(**{k: self.W[k].data_ptr() for k in
+                                          ("norm1_w", "w_qkv", "w_o", "norm2_w", "w_up", "w_down") if k in self.W})
+        self.sv = cl.LayerSaved(**{k: v.data_ptr() for k, v in self.saved.items()})
+        self.G = grad_buffers(s, dev)
+        self.dx = torch.empty(s.M, s.D, dtype=torch.bfloat16, device=dev)
+        self.grads = cl.LayerGrads(dx=self.dx.data_ptr(), **{k: v.data_ptr() for k, v in self.G.items()})
+        self.ws = torch.empty(cl.collider_layer_workspace_size(self.desc), dtype=torch.uint8, device=dev)
+        self.idx = torch.empty(s.M, dtype=torch.int32, device=dev)
+        self.cu = torch.empty(s.B + 1, dtype=torch.int32, device=dev)
+        self.nk = torch.empty(1, dtype=torch.int32, device=dev)
+
+    def step(self, mask, stream, sv=None, dout=None):
+        cl, s = self.cl, self.s
+        cl.collider_compact(mask, s.B, s.T, self.idx, self.cu, self.nk, None, stream)
+        cl.collider_layer_bwd(self.desc, self.weights, self.sv if sv is None else sv,
+                              self.dout if dout is None else dout, cl.ROWS_FULL, self.idx, self.cu, self.nk,
+                              self.grads, cl.ROWS_FULL, self.ws, stream)
+
+
+class Stack:
+    """The 22-block stack: inputs and saved activations of every block (torch
+    forward on the GPU), LM head and embedding; step() runs compaction +
+    collider_stack_bwd."""
+
+    def __init__(self, cl, st, dev):
+        import torch
+        self.cl, self.st = cl, st
+        ls = st.layer
+        t = workloads.stack_tensors(st)
+        self.keep_np = t["keep"]
+        self.mask = torch.from_numpy(t["keep"]).to(dev)
+        self.mask_all = torch.ones_like(self.mask)
+        E = torch.from_numpy(t["E"]).to(dev).bfloat16()
+        ids = torch.from_numpy(t["ids"].astype(np.int64)).to(dev)
+        x = E[ids]
+        self.saved, self.Ws = [], []
+        with torch.no_grad():
+            for w in t["layers"]:
+                W = {k: torch.from_numpy(v).to(dev).bfloat16() for k, v in w.items()}
+                sv = gpu_forward(ls, W, x)
+                self.saved.append(sv)
+                self.Ws.append(W)
+                x = (sv["h"].float() + (sv["s"] @ W["w_down"]).float()).bfloat16()
+            xf = x.float()
+            self.rstdf = torch.rsqrt(xf.pow(2).mean(-1) + ls.eps)
+            self.nf = torch.from_numpy(t["normf_w"]).to(dev).bfloat16()
+            self.y = (xf * self.rstdf[:, None] * self.nf.float()).bfloat16()
+            self.wlm = torch.from_numpy(t["w_lm"]).to(dev).bfloat16()
+            self.z = (self.y @ self.wlm).bfloat16()
+        self.xL = x
+        self.desc = layer_desc(cl, ls)
+        L = st.L
+        self.Wc = (cl.LayerWeights * L)(*[cl.LayerWeights(**{k: W[k].data_ptr() for k in
+                                                              ("norm1_w", "w_qkv", "w_o", "norm2_w", "w_up", "w_down")})
+                                          for W in self.Ws])
+        self.Sc = (cl.LayerSaved * L)(*[cl.LayerSaved(**{k: v.data_ptr() for k, v in sv.items()}) for sv in self.saved])
+        self.G = [grad_buffers(ls, dev) for _ in range(L)]
+        self.Gc = (cl.LayerGrads * L)(*[cl.LayerGrads(dx=None, **{k: v.data_ptr() for k, v in g.items()})
+                                        for g in self.G])
+        self.targets = torch.from_numpy(t["targets"]).to(dev)
+        self.ids = torch.from_numpy(t["ids"]).to(dev)
+        self.dnf = torch.empty(ls.D, device=dev)
+        self.dlm = torch.empty(ls.D, st.V, device=dev)
+        self.dE = torch.empty(st.V, ls.D, device=dev)
+        self.ws = torch.empty(cl.collider_stack_workspace_size(self.desc, L, st.V), dtype=torch.uint8, device=dev)
+        self.idx = torch.empty(ls.M, dtype=torch.int32, device=dev)
+        self.cu = torch.empty(ls.B + 1, dtype=torch.int32, device=dev)
+        self.nk = torch.empty(1, dtype=torch.int32, device=dev)
+
+    def step(self, mask, stream):
+        cl, st = self.cl, self.st
+        ls = st.layer
+        cl.collider_compact(mask, ls.B, ls.T, self.idx, self.cu, self.nk, None, stream)
+        cl.collider_stack_bwd(self.desc, st.L, st.V, self.Wc, self.Sc, self.z, self.targets, self.ids, self.y,
+                              self.xL, self.rstdf, self.nf, self.wlm, self.idx, self.cu, self.nk, self.Gc, self.dnf,
+                              self.dlm, self.dE, self.ws, stream)
 
 
 # ---------------------------------------------------------------------------
@@ -269,43 +420,22 @@ def run_ours(args):
     s = workloads.WORKLOADS[WORKLOAD]
     M = s.M
 
-    # ---- inputs (seeded, synthetic) -------------------------------------
-    wn = workloads.layer_weights(s)
-    tn = workloads.layer_inputs(s)
-    W = {k: torch.from_numpy(v).to(dev).bfloat16() for k, v in wn.items()}
-    x = torch.from_numpy(tn["x"]).to(dev).bfloat16()
-    dout = torch.from_numpy(tn["dout"]).to(dev).bfloat16()
-    masks = {"filtered": torch.from_numpy(tn["keep"]).to(dev),
-             "unfiltered": torch.ones(s.B, s.T, dtype=torch.uint8, device=dev)}
-    with torch.no_grad():
-        saved = gpu_forward(s, W, x)
+    # ---- inputs (seeded, synthetic), saved activations by a torch forward ----
+    blk = Block(cl, s, dev)
+    tn = {"keep": blk.keep_np}
+    W, saved, dout, masks, G, dx = blk.W, blk.saved, blk.dout, blk.masks, blk.G, blk.dx
+    desc, weights, grads, ws, idx, cu, nk = blk.desc, blk.weights, blk.grads, blk.ws, blk.idx, blk.cu, blk.nk
     torch.cuda.synchronize()
-
-    desc = cl.LayerDesc(arch=cl.ARCH_LLAMA, B=s.B, T=s.T, D=s.D, H=s.H, Hkv=s.Hkv, dh=s.dh, F=s.F,
-                        rotary_dim=s.rotary_dim, rope_base=s.rope_base, norm=cl.NORM_RMS, eps=s.eps,
-                        act=cl.ACT_SWIGLU)
-    weights = cl.LayerWeights(**{k: W[k].data_ptr() for k in ("norm1_w", "w_qkv", "w_o", "norm2_w", "w_up",
-                                                               "w_down")})
-    sv = cl.LayerSaved(**{k: saved[k].data_ptr() for k in saved})
-    gshapes = dict(dnorm1_w=(s.D,), dw_qkv=(s.D, s.Nqkv), dw_o=(s.H * s.dh, s.D), dnorm2_w=(s.D,),
-                   dw_up=(s.D, s.Nup), dw_down=(s.F, s.D))
-    G = {k: torch.empty(v, dtype=torch.float32, device=dev) for k, v in gshapes.items()}
-    dx = torch.empty(M, s.D, dtype=torch.bfloat16, device=dev)
-    grads = cl.LayerGrads(dx=dx.data_ptr(), **{k: v.data_ptr() for k, v in G.items()})
-    ws = torch.empty(cl.collider_layer_workspace_size(desc), dtype=torch.uint8, device=dev)
-    idx = torch.empty(M, dtype=torch.int32, device=dev)
-    cu = torch.empty(s.B + 1, dtype=torch.int32, device=dev)
-    nk = torch.empty(1, dtype=torch.int32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def step(mask):
-        cl.collider_compact(mask, s.B, s.T, idx, cu, nk, None, stream)
-        cl.collider_layer_bwd(desc, weights, sv, dout, cl.ROWS_FULL, idx, cu, nk, grads, cl.ROWS_FULL, ws, stream)
+        blk.step(mask, stream)
 
-    def timed(mask, K, Wm):
+    def timed(mask, K, Wm, step_fn=None):
+        step_fn = step_fn or step
         for _ in range(Wm):
-            step(mask)
+            step_fn(mask)
         cl.collider_check(stream)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
         if world > 1:
@@ -315,7 +445,7 @@ def run_ours(args):
         for e0, e1 in ev:
             flush.fill_(1)   # evict L2 between steps
             e0.record(stream)
-            step(mask)
+            step_fn(mask)
             e1.record(stream)
         torch.cuda.synchronize()
         launches = cl.collider_launch_count(1)
@@ -405,6 +535,36 @@ def run_ours(args):
     e2e_ms = e0.elapsed_time(e1) / args.steps
     e2e_ms = max_over_ranks([e2e_ms], dev)[0]
 
+    # ---- the other block shapes and the 22-block stack (filtered vs unfiltered) ----
+    configs = {}
+    if not args.headline_only:
+        runs = [("qwen25_layer", workloads.WORKLOADS["qwen25_layer"])]
+        runs += [(f"phi15_layer f={f}", workloads.WORKLOADS["phi15_layer"].with_(f=f)) for f in (0.0, 0.2, 0.4, 0.6)]
+        del blk
+        torch.cuda.empty_cache()
+        for label, shp in runs:
+            b2 = Block(cl, shp, dev)
+            ms2f, _ = timed(b2.masks["filtered"], args.steps, args.warmup, lambda m: b2.step(m, stream))
+            ms2u, _ = timed(b2.masks["unfiltered"], args.steps, args.warmup, lambda m: b2.step(m, stream))
+            ms2f, ms2u = max_over_ranks([ms2f, ms2u], dev)
+            configs[label] = {"tokens_per_s": shp.M * world / (ms2f * 1e-3), "ms_per_step": ms2f,
+                              "unfiltered_ms_per_step": ms2u, "speedup_vs_unfiltered": ms2u / ms2f,
+                              "kept_tokens": int(b2.keep_np.sum()), "tokens": shp.M}
+            del b2
+            torch.cuda.empty_cache()
+        st = workloads.WORKLOADS["tinyllama_stack"]
+        stk = Stack(cl, st, dev)
+        K2 = max(2, args.steps // 4)
+        ms3f, _ = timed(stk.mask, K2, args.warmup, lambda m: stk.step(m, stream))
+        ms3u, _ = timed(stk.mask_all, K2, args.warmup, lambda m: stk.step(m, stream))
+        ms3f, ms3u = max_over_ranks([ms3f, ms3u], dev)
+        configs["tinyllama_stack (22 blocks + LM head)"] = {
+            "tokens_per_s": st.layer.M * world / (ms3f * 1e-3), "ms_per_step": ms3f, "unfiltered_ms_per_step": ms3u,
+            "speedup_vs_unfiltered": ms3u / ms3f, "kept_tokens": int(stk.keep_np.sum()), "tokens": st.layer.M,
+            "steps": K2}
+        del stk
+        torch.cuda.empty_cache()
+
     if rank == 0:
         tokens = s.M * world
         line = {
@@ -426,6 +586,7 @@ def run_ours(args):
             "gemms": {k: {"ms": round(v[0], 4), "tflops": round(v[1] / (v[0] * 1e-3) / 1e12, 1)}
                       for k, v in gemm_shapes.items()},
             "gpu_launches": launches,
+            "configs": configs,
             "clocks": clocks,
             "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
