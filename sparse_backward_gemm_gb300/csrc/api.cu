@@ -606,10 +606,14 @@ void layer_carve(Carver& cv, const collider_layer_desc* d, LayerBufs* L) {
 // after their inputs, so they run on a second stream (one per host thread and
 // device), forked from and joined back into the caller's stream with events:
 // they fill the SMs the input-gradient chain leaves idle (GEMM tail waves,
-// attention, row kernels).  No host synchronisation.
+// attention, row kernels).  The input-gradient chain itself runs on a
+// high-priority stream (forked from the caller's stream at the start of the
+// block, joined back at the end), so when CTAs of both wait for SMs the
+// chain's go first.  No host synchronisation.
 struct Side {
-  cudaStream_t s = nullptr;
-  cudaEvent_t ev[8] = {};
+  cudaStream_t s = nullptr;    // weight gradients, default priority
+  cudaStream_t hi = nullptr;   // input-gradient chain, highest priority
+  cudaEvent_t ev[10] = {};
 };
 thread_local Side g_side[64];
 
@@ -631,6 +635,11 @@ collider_status side_ctx(const Ctx& c, Ctx* c2, Side** sd) {
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   Side& S = g_side[dev & 63];
   if (!S.s) {
+    int least = 0, greatest = 0;
+    e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    if (e != cudaSuccess) return cuda_fail(e, "stream priority range");
+    e = cudaStreamCreateWithPriority(&S.hi, cudaStreamNonBlocking, greatest);
+    if (e != cudaSuccess) return cuda_fail(e, "high-priority stream");
     e = cudaStreamCreateWithFlags(&S.s, cudaStreamNonBlocking);
     if (e != cudaSuccess) return cuda_fail(e, "side stream");
     for (auto& ev : S.ev) {
@@ -642,6 +651,16 @@ collider_status side_ctx(const Ctx& c, Ctx* c2, Side** sd) {
   c2->stream = S.s;
   *sd = &S;
   return COLLIDER_OK;
+}
+// the high-priority stream waits for the caller's stream (event slot 8), and
+// the caller's stream waits for it at the end (slot 9)
+cudaError_t fork_hi(cudaStream_t caller, Side* S) {
+  cudaError_t e = cudaEventRecord(S->ev[8], caller);
+  return e == cudaSuccess ? cudaStreamWaitEvent(S->hi, S->ev[8], 0) : e;
+}
+cudaError_t join_hi(cudaStream_t caller, Side* S) {
+  cudaError_t e = cudaEventRecord(S->ev[9], S->hi);
+  return e == cudaSuccess ? cudaStreamWaitEvent(caller, S->ev[9], 0) : e;
 }
 // side stream waits for everything enqueued on the caller's stream so far
 cudaError_t fork_side(const Ctx& c, Side* S, int k) {
@@ -693,10 +712,23 @@ cudaError_t gemm_dw(const Ctx& c, int M, int Kin, int Nout, const void* Xk, long
   return launch_tc_gemm(c, g);
 }
 
-collider_status layer_bwd_impl(const Ctx& c, const collider_layer_desc* d, const collider_layer_weights* w,
+collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, const collider_layer_weights* w,
                                const collider_layer_saved* sv, const void* dOut, bool dout_full,
                                const int32_t* idx, const int32_t* cu_kept, const int32_t* n_kept,
                                const collider_layer_grads* g, bool dx_full, LayerBufs& L) {
+  // c: the context of the input-gradient chain (the high-priority stream when
+  // the side stream is on, else the caller's)
+  Ctx c = c_in;
+  Ctx cs;
+  Side* side = nullptr;
+  {
+    collider_status st = side_ctx(c_in, &cs, &side);
+    if (st != COLLIDER_OK) return st;
+  }
+  if (side) {
+    CK(fork_hi(c_in.stream, side));
+    c.stream = side->hi;
+  }
   const int M = d->B * d->T;
   const int D = d->D, F = d->F, H = d->H, Hkv = d->Hkv, dh = d->dh;
   const int Hd = H * dh, Nqkv = (H + 2 * Hkv) * dh;
@@ -706,12 +738,6 @@ collider_status layer_bwd_impl(const Ctx& c, const collider_layer_desc* d, const
   g_sk_counters = L.sk_counters;
   g_sk_cap = L.sk_cap;
   CK(cudaMemsetAsync(L.sk_counters, 0, L.sk_cap * sizeof(int), c.stream));
-  Ctx cs;
-  Side* side = nullptr;
-  {
-    collider_status st = side_ctx(c, &cs, &side);
-    if (st != COLLIDER_OK) return st;
-  }
 
   // 1. gather the kept rows of dOut and of the saved GEMM operands
   {
@@ -821,7 +847,8 @@ collider_status layer_bwd_impl(const Ctx& c, const collider_layer_desc* d, const
   if (dx_full)
     CK(launch_scatter(c, reinterpret_cast<const char*>(L.dx_k), (long long)D * 2, static_cast<char*>(g->dx),
                       (long long)D * 2, D * 2, M, idx, n_kept));
-  CK(join_side(c, side, 4));   // the weight gradients are done when the caller's stream is
+  CK(join_side(c, side, 4));   // the weight gradients are done when the chain is
+  if (side) CK(join_hi(c_in.stream, side));
   return COLLIDER_OK;
 }
 
