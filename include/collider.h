@@ -77,8 +77,18 @@ const char* collider_last_error(void);
 
 /* Synchronises `stream`, then reports (and clears) the device status word:
  * COLLIDER_ERR_TIMEOUT if a kernel's bounded wait ran out since the last
- * check, COLLIDER_ERR_CUDA if the stream holds an asynchronous CUDA error. */
+ * check, COLLIDER_ERR_INVALID_ARG if a kernel met a kept index outside its
+ * buffer (and skipped it), COLLIDER_ERR_CUDA if the stream holds an
+ * asynchronous CUDA error. */
 collider_status collider_check(void* stream);
+
+/* Self-test of the failure path (the pages have no counterpart): one thread
+ * waits on an mbarrier that nothing arrives on, through the same bounded wait
+ * every kernel of the library uses.  After about 2 s the wait gives up, the
+ * timeout (site 999) lands in the status word and the kernel returns; the
+ * next collider_check reports COLLIDER_ERR_TIMEOUT and clears the word, and
+ * the device stays usable.  Returns the launch status. */
+collider_status collider_selftest_wait_timeout(void* stream);
 
 /* Number of kernels this library has launched on the calling host thread
  * since the last reset (reset=1 returns the count and zeroes it). */

@@ -15,9 +15,10 @@ import os
 
 __all__ = [
     "ColliderError", "lib", "LIB_PATH", "ROWS_FULL", "ROWS_COMPACT", "F32", "BF16",
+    "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_TIMEOUT",
     "ARCH_LLAMA", "ARCH_PHI", "NORM_RMS", "NORM_LAYER", "ACT_SWIGLU", "ACT_GELU_TANH",
     "LayerDesc", "LayerWeights", "LayerSaved", "LayerGrads", "EXPORTED",
-    "collider_last_error", "collider_check", "collider_launch_count",
+    "collider_last_error", "collider_check", "collider_selftest_wait_timeout", "collider_launch_count",
     "collider_profile_enable", "collider_profile_count", "collider_profile_get",
     "collider_select_keep", "collider_compact_workspace_size", "collider_compact", "collider_compact_noalloc",
     "collider_gather_rows",
@@ -71,6 +72,7 @@ SZ = C.c_size_t
 _SIGS = {
     "collider_last_error": (C.c_char_p, []),
     "collider_check": (I, [P]),
+    "collider_selftest_wait_timeout": (I, [P]),
     "collider_launch_count": (C.c_longlong, [I]),
     "collider_profile_enable": (I, [I]),
     "collider_profile_count": (I, []),
@@ -152,6 +154,10 @@ def collider_last_error() -> str:
 
 def collider_check(stream=None) -> None:
     _check(lib().collider_check(_stream(stream)))
+
+
+def collider_selftest_wait_timeout(stream=None) -> None:
+    _check(lib().collider_selftest_wait_timeout(_stream(stream)))
 
 
 def collider_launch_count(reset: int = 0) -> int:

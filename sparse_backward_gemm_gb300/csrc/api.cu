@@ -16,6 +16,7 @@
 
 #include "../../include/collider.h"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace collider {
 
@@ -167,6 +168,30 @@ extern "C" collider_status collider_check(void* stream) {
     return fail(COLLIDER_ERR_TIMEOUT, "a bounded in-kernel wait ran out (site %u, block %u)", h.site, h.block);
   return fail(COLLIDER_ERR_INVALID_ARG, "a kernel skipped an index outside its buffer (site %u, block %u)", h.site,
               h.block);
+}
+
+namespace selftest {
+// one thread waits on an mbarrier nothing arrives on: the bounded wait runs out
+__global__ void wait_kernel(DevStatus* st) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(tc::smem_u32(&bar), 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tc::mbar_wait(tc::smem_u32(&bar), 0, &abort_flag, st, 999);
+  }
+}
+}  // namespace selftest
+
+extern "C" collider_status collider_selftest_wait_timeout(void* stream) {
+  Ctx c;
+  collider_status s = make_ctx(stream, &c);
+  if (s != COLLIDER_OK) return s;
+  selftest::wait_kernel<<<1, 32, 0, c.stream>>>(c.st);
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? COLLIDER_OK : cuda_fail(e, "self-test wait kernel");
 }
 
 // Profiler: record a CUDA event pair around every kernel launch of this host
