@@ -499,37 +499,71 @@ def run_ours(args):
     step_ms_prof = sum(v[1] for v in per.values()) / args.steps
 
     # ---- end to end through the C ABI with host buffers ------------------
+    # Every step copies its inputs (saved activations, dOut, keep-mask) from
+    # pinned host memory and its outputs (weight gradients, dx) back.  The
+    # copies are pipelined the way a training loop prefetches: the inputs of
+    # step i+1 go up on a copy stream while step i computes (two device input
+    # sets), and step i's outputs come down on a third stream while step i+1
+    # computes (two device output sets).  All copies sit inside the timed region.
     host_in = {k: v.cpu().pin_memory() for k, v in saved.items()}
     host_dout = dout.cpu().pin_memory()
     host_mask = masks["filtered"].cpu().pin_memory()
-    dev_in = {k: torch.empty_like(v) for k, v in saved.items()}
-    dev_dout = torch.empty_like(dout)
-    dev_mask = torch.empty_like(masks["filtered"])
     host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in G.items()}
     host_dx = torch.empty(dx.shape, dtype=dx.dtype).pin_memory()
-    sv_e2e = cl.LayerSaved(**{k: dev_in[k].data_ptr() for k in dev_in})
     h2d = sum(v.numel() * v.element_size() for v in host_in.values()) + host_dout.numel() * 2 + host_mask.numel()
     d2h = sum(v.numel() * 4 for v in G.values()) + dx.numel() * 2
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    sets = []
+    for _ in range(2):
+        din = {k: torch.empty_like(v) for k, v in saved.items()}
+        dgr = {k: torch.empty_like(v) for k, v in G.items()}
+        ddx = torch.empty_like(dx)
+        sets.append(dict(
+            din=din, dout=torch.empty_like(dout), mask=torch.empty_like(masks["filtered"]), G=dgr, dx=ddx,
+            sv=cl.LayerSaved(**{k: din[k].data_ptr() for k in din}),
+            grads=cl.LayerGrads(dx=ddx.data_ptr(), **{k: v.data_ptr() for k, v in dgr.items()}),
+            loaded=torch.cuda.Event(), computed=torch.cuda.Event(), drained=torch.cuda.Event()))
 
-    def e2e_step():
-        for k in host_in:
-            dev_in[k].copy_(host_in[k], non_blocking=True)
-        dev_dout.copy_(host_dout, non_blocking=True)
-        dev_mask.copy_(host_mask, non_blocking=True)
-        cl.collider_compact(dev_mask, s.B, s.T, idx, cu, nk, None, stream)
-        cl.collider_layer_bwd(desc, weights, sv_e2e, dev_dout, cl.ROWS_FULL, idx, cu, nk, grads, cl.ROWS_FULL, ws,
-                              stream)
-        for k in G:
-            host_out[k].copy_(G[k], non_blocking=True)
-        host_dx.copy_(dx, non_blocking=True)
+    def e2e_run(n):
+        up.wait_stream(stream)     # nothing of this run starts before the work already on the stream
+        down.wait_stream(stream)
 
-    for _ in range(args.warmup):
-        e2e_step()
+        def upload(i):
+            b_ = sets[i % 2]
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(b_["computed"])      # step i-2 is done reading this set
+                for k in host_in:
+                    b_["din"][k].copy_(host_in[k], non_blocking=True)
+                b_["dout"].copy_(host_dout, non_blocking=True)
+                b_["mask"].copy_(host_mask, non_blocking=True)
+                b_["loaded"].record(up)
+        upload(0)
+        for i in range(n):
+            b_ = sets[i % 2]
+            if i + 1 < n:
+                upload(i + 1)
+            stream.wait_event(b_["loaded"])
+            if i >= 2:
+                stream.wait_event(b_["drained"])                  # outputs of step i-2 are on the host
+            cl.collider_compact(b_["mask"], s.B, s.T, idx, cu, nk, None, stream)
+            cl.collider_layer_bwd(desc, weights, b_["sv"], b_["dout"], cl.ROWS_FULL, idx, cu, nk, b_["grads"],
+                                  cl.ROWS_FULL, ws, stream)
+            b_["computed"].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(b_["computed"])
+                for k in host_out:
+                    host_out[k].copy_(b_["G"][k], non_blocking=True)
+                host_dx.copy_(b_["dx"], non_blocking=True)
+                b_["drained"].record(down)
+        stream.wait_stream(down)
+        stream.wait_stream(up)
+
+    e2e_run(args.warmup)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    e2e_run(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
