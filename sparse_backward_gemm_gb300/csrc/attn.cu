@@ -942,31 +942,35 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// tcgen05 D pre-pass, head dim 64 or 128.  One CTA per (sequence, query
-// head, 128 queries): O' = sum over kept causal keys of P V, D = rowsum(dO * O').
-// Q, K and V tiles are held as 64-column (128-byte) swizzle chunks.
-//   warp 0     TMA: Q once; K_j, V_j per key block (3 stages at head dim 64, 2 at 128)
-//   warp 1     TMEM owner; one lane issues S_j = Q K_j^T (into one of two
-//              TMEM buffers, so S_{j+1} overlaps the softmax of block j) and
-//              O' += P_j V_j
-//   warps 2-9  one query row and 64 of the 128 keys per thread: P_j from
-//              TMEM -> bf16 -> shared; at the end D from O' (TMEM) and dO
+// tcgen05 D pre-pass, head dim 64 or 128.  One CTA per (sequence, 128 queries,
+// HPC query heads of one kv head): O'_h = sum over kept causal keys of P_h V,
+// D_h = rowsum(dO_h * O'_h).  With HPC > 1 the heads share each K/V block: it
+// is loaded once, and the HPC (head, key block) iterations run back to back
+// through the double-buffered S and P.  Tiles are 64-column (128-byte)
+// swizzle chunks.
+//   warp 0     TMA: the HPC Q tiles once; K_j, V_j per key block
+//   warp 1     TMEM owner; one lane issues S = Q_h K_j^T (into one of two TMEM
+//              buffers, so the next S overlaps the softmax of this one) and
+//              O'_h += P V_j
+//   warps 2-9  one query row and 64 of the 128 keys per thread: P from TMEM
+//              -> bf16 -> shared; at the end D_h from O'_h (TMEM) and dO_h
 //              (global), each half of the row's columns summed separately
-// TMEM columns: S buffers 0-127 and 128-255, O' from 256 (head-dim columns).
-template <int DH>
+// TMEM columns: S buffers 0-127 and 128-255, O'_h from 256 + h * head dim.
+template <int DH, int HPC>
 struct DprepCfg {
   static constexpr int kQ = 128, kK = 128, kD = DH, kCh = DH / 64;   // 64-column chunks
   static constexpr uint32_t kTile = 16384;                           // 128 rows x 64 columns
-  static constexpr int kKV = DH == 64 ? 3 : 2;                       // K/V stages
+  static constexpr int kKV = DH == 64 && HPC == 1 ? 3 : 2;           // K/V stages
   static constexpr uint32_t kKVBytes = 2 * kCh * kTile;              // K and V of one stage
-  static constexpr uint32_t OFF_Q = 0, OFF_K = kCh * kTile, OFF_P = OFF_K + kKV * kKVBytes,
+  static constexpr uint32_t OFF_Q = 0, OFF_K = HPC * kCh * kTile, OFF_P = OFF_K + kKV * kKVBytes,
                             OFF_BAR = OFF_P + 4 * kTile;
-  static constexpr uint32_t OFF_PART = OFF_BAR + 256;                // [2][128] f32 partial dot products
-  static constexpr size_t kSmem = 1024 + OFF_PART + 1024;
+  static constexpr uint32_t OFF_PART = OFF_BAR + 256;                // [HPC][2][128] f32 partial dot products
+  static constexpr size_t kSmem = 1024 + OFF_PART + HPC * 1024;
   static constexpr uint32_t TM_S = 0, TM_O = 256;
   static constexpr int kSoftWarps = 8;                               // two per TMEM lane quadrant
   static constexpr int kThreads = 32 * (2 + kSoftWarps);
   static_assert(kSmem <= 232448, "shared memory");
+  static_assert(TM_O + HPC * DH <= 512, "TMEM columns");
 };
 
 struct DprepTc {
@@ -981,28 +985,30 @@ struct DprepTc {
   DevStatus* st;
 };
 
-template <int DH>
-__global__ void __launch_bounds__(DprepCfg<DH>::kThreads, 1)
+template <int DH, int HPC>
+__global__ void __launch_bounds__(DprepCfg<DH, HPC>::kThreads, 1)
     attn_dprep_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, DprepTc p) {
   using namespace tc;
-  using Cfg = DprepCfg<DH>;
+  using Cfg = DprepCfg<DH, HPC>;
   constexpr int kQ = Cfg::kQ, kK = Cfg::kK, kD = Cfg::kD, kCh = Cfg::kCh, kKV = Cfg::kKV, kSoftWarps = Cfg::kSoftWarps;
   constexpr uint32_t kTile = Cfg::kTile, kKVBytes = Cfg::kKVBytes, OFF_Q = Cfg::OFF_Q, OFF_K = Cfg::OFF_K,
                      OFF_P = Cfg::OFF_P, OFF_BAR = Cfg::OFF_BAR, OFF_PART = Cfg::OFF_PART, TM_S = Cfg::TM_S,
                      TM_O = Cfg::TM_O;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // items: query block descending (most key blocks first), then sequence, head
-  const int per_i = p.B * p.H;
+  // items: query block descending (most key blocks first), then sequence, head group
+  const int ngroups = p.H / HPC;
+  const int per_i = p.B * ngroups;
   const int ib = p.nqb - 1 - (int)(blockIdx.x / per_i);
-  const int b = (blockIdx.x % per_i) / p.H;
-  const int h = blockIdx.x % p.H;
+  const int b = (blockIdx.x % per_i) / ngroups;
+  const int h0 = (blockIdx.x % ngroups) * HPC;   // the HPC heads share kv head h0 / G
   const int s0 = p.cu_kept[b], len = p.cu_kept[b + 1] - s0;
   const int i0 = ib * kQ;
   if (i0 >= len) return;
-  const int hk = h / p.G;
+  const int hk = h0 / p.G;
   const int nj = p.causal ? ib + 1 : (len + kK - 1) / kK;
+  const int n_it = nj * HPC;                     // iteration it: key block it / HPC, head it % HPC
   const int qrows = min(kQ, len - i0);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
@@ -1054,17 +1060,20 @@ __global__ void __launch_bounds__(DprepCfg<DH>::kThreads, 1)
     };
     int ok = 1;
     if (lane == 0) {
-      mbar_expect_tx(b_q, kCh * kTile);
+      mbar_expect_tx(b_q, HPC * kCh * kTile);
 #pragma unroll
-      for (int c = 0; c < kCh; ++c) tma_load_2d(sbase + OFF_Q + c * kTile, &tmQ, b_q, h * kD + 64 * c, s0 + i0);
+      for (int hh = 0; hh < HPC; ++hh)
+#pragma unroll
+        for (int c = 0; c < kCh; ++c)
+          tma_load_2d(sbase + OFF_Q + (hh * kCh + c) * kTile, &tmQ, b_q, (h0 + hh) * kD + 64 * c, s0 + i0);
       ok = issue(0) ? 1 : 0;
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
     // With three stages block j+1 can be requested before block j is
-    // released: the request waits for the P V of block j-2, which the MMA
-    // issues once block j-1 is released.  With two stages the request waits
-    // for the P V of block j-1, which the MMA issues only after it has taken
-    // block j, so block j is released first.
+    // released: the request waits for the last P V of block j-2, which the
+    // MMA issues once block j-1 is released.  With two stages the request
+    // waits for the last P V of block j-1, which the MMA issues only after it
+    // has taken block j, so block j is released first.
     for (int j = 0; ok && j < nj; ++j) {
       const int st = j % kKV, use = j / kKV;
       int nxt = 1;
@@ -1095,36 +1104,41 @@ __global__ void __launch_bounds__(DprepCfg<DH>::kThreads, 1)
       constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t id_o = idesc_bf16(128, kD, false, true);
       bool ok = mbar_wait(b_q, 0, abort_flag, p.st, 41);
-      // O' += P_{jj} V_{jj} for the block whose P the softmax has finished
-      auto pv = [&](int jj) -> bool {
-        const int kst = jj % kKV, pb = jj & 1;
-        if (!mbar_wait(b_pfull, jj & 1, abort_flag, p.st, 42)) return false;
+      // O'_h += P V_j for the iteration whose P the softmax has finished; the
+      // last head of a key block releases its K/V stage
+      auto pv = [&](int t) -> bool {
+        const int jj = t / HPC, hh = t % HPC;
+        const int kst = jj % kKV, pb = t & 1;
+        if (!mbar_wait(b_pfull, t & 1, abort_flag, p.st, 42)) return false;
         fence_after();
         const uint32_t sv = sbase + OFF_K + kst * kKVBytes + kCh * kTile;
 #pragma unroll
         for (int kk = 0; kk < kK / 16; ++kk) {   // V as the MN-major B: head-dim chunks kTile apart
           const uint32_t pa = sbase + OFF_P + pb * 2 * kTile + (kk >> 2) * kTile + (kk & 3) * 32;
-          mma_bf16(tbase + TM_O, sdesc(pa, 16, 1024), sdesc(sv + kk * 2048, kTile, 1024), id_o, (jj > 0) || (kk > 0));
+          mma_bf16(tbase + TM_O + hh * kD, sdesc(pa, 16, 1024), sdesc(sv + kk * 2048, kTile, 1024), id_o,
+                   (jj > 0) || (kk > 0));
         }
-        mma_commit(b_kvempty + 8 * kst);
+        if (hh == HPC - 1) mma_commit(b_kvempty + 8 * kst);
         mma_commit(b_pempty + 8 * pb);
         return true;
       };
-      for (int j = 0; ok && j < nj; ++j) {
-        const int kst = j % kKV, kuse = j / kKV, sb = j & 1;
-        if (!mbar_wait(b_kvready + 8 * kst, kuse & 1, abort_flag, p.st, 43)) { ok = false; break; }
-        fence_after();
-        const uint32_t sk = sbase + OFF_K + kst * kKVBytes;
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int j = it / HPC, hh = it % HPC;
+        const int kst = j % kKV, kuse = j / kKV, sb = it & 1;
+        if (hh == 0) {
+          if (!mbar_wait(b_kvready + 8 * kst, kuse & 1, abort_flag, p.st, 43)) { ok = false; break; }
+          fence_after();
+        }
+        const uint32_t sk = sbase + OFF_K + kst * kKVBytes, sq = sbase + OFF_Q + hh * kCh * kTile;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kTile + (kk & 3) * 32;
-          mma_bf16(tbase + TM_S + sb * 128, sdesc(sbase + OFF_Q + off, 16, 1024), sdesc(sk + off, 16, 1024), id_s,
-                   kk > 0);
+          mma_bf16(tbase + TM_S + sb * 128, sdesc(sq + off, 16, 1024), sdesc(sk + off, 16, 1024), id_s, kk > 0);
         }
         mma_commit(b_sfull + 8 * sb);
-        if (j > 0 && !pv(j - 1)) { ok = false; break; }
+        if (it > 0 && !pv(it - 1)) { ok = false; break; }
       }
-      if (ok && pv(nj - 1)) mma_commit(b_ofull);
+      if (ok && n_it > 0 && pv(n_it - 1)) mma_commit(b_ofull);
     }
   } else {
     // softmax: one query row, 64 of the 128 keys of a block per thread
@@ -1132,23 +1146,34 @@ __global__ void __launch_bounds__(DprepCfg<DH>::kThreads, 1)
     const int half = (warp - 2) >> 2;
     const int r = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    const float L = (r < qrows) ? p.lse2[(long long)h * p.M + s0 + i0 + r] : 0.f;
-    // this thread's half of its dO row, loaded now so the latency hides behind the key loop
-    uint4 dov[kD / 16];
+    float Lh[HPC];
 #pragma unroll
-    for (int u = 0; u < kD / 16; ++u) {
-      dov[u] = make_uint4(0, 0, 0, 0);
-      if (r < qrows)
-        dov[u] = *reinterpret_cast<const uint4*>(p.dO + (long long)(s0 + i0 + r) * p.do_ld + h * kD + half * (kD / 2) +
-                                                 8 * u);
+    for (int hh = 0; hh < HPC; ++hh) Lh[hh] = (r < qrows) ? p.lse2[(long long)(h0 + hh) * p.M + s0 + i0 + r] : 0.f;
+    // with one head, this thread's half of its dO row is loaded now so the
+    // latency hides behind the key loop; with several heads at the end
+    constexpr int kDoVec = HPC == 1 ? kD / 16 : 1;
+    uint4 dov[kDoVec];
+    if (HPC == 1) {
+#pragma unroll
+      for (int u = 0; u < kDoVec; ++u) {
+        dov[u] = make_uint4(0, 0, 0, 0);
+        if (r < qrows)
+          dov[u] = *reinterpret_cast<const uint4*>(p.dO + (long long)(s0 + i0 + r) * p.do_ld + h0 * kD +
+                                                   half * (kD / 2) + 8 * u);
+      }
     }
     bool ok = true;
-    for (int j = 0; j < nj; ++j) {
-      const int st = j & 1, use = j >> 1;
+    for (int it = 0; it < n_it; ++it) {
+      const int st = it & 1, use = it >> 1;
+      const int j = it / HPC, hh = it % HPC;
       if (!mbar_wait(b_sfull + 8 * st, use & 1, &no_abort, p.st, 44)) { ok = false; break; }
-      if (j >= 2 && !mbar_wait(b_pempty + 8 * st, (use - 1) & 1, &no_abort, p.st, 45)) { ok = false; break; }
+      if (it >= 2 && !mbar_wait(b_pempty + 8 * st, (use - 1) & 1, &no_abort, p.st, 45)) { ok = false; break; }
       fence_after();
       const int j0 = j * kK;
+      float L = Lh[0];
+#pragma unroll
+      for (int x = 1; x < HPC; ++x)
+        if (hh == x) L = Lh[x];
       uint32_t sr[64];
       tmem_ld32_async(tbase + lane_off + TM_S + st * 128 + half * 64, sr);
       tmem_ld32_async(tbase + lane_off + TM_S + st * 128 + half * 64 + 32, sr + 32);
@@ -1181,30 +1206,47 @@ __global__ void __launch_bounds__(DprepCfg<DH>::kThreads, 1)
       fence_async_smem();
       mbar_arrive(b_pfull);
     }
-    float* part = reinterpret_cast<float*>(sm + OFF_PART);
-    float d = 0.f;
+    float* part = reinterpret_cast<float*>(sm + OFF_PART);   // [HPC][2][128]
+    float d[HPC];
+#pragma unroll
+    for (int hh = 0; hh < HPC; ++hh) d[hh] = 0.f;
     if (ok && mbar_wait(b_ofull, 0, &no_abort, p.st, 46)) {
       fence_after();
-      // this thread's half of the row: head-dim columns half * kD / 2 ..
 #pragma unroll
-      for (int cc = 0; cc < kD / 64; ++cc) {
-        float o[32];
-        const int col = half * (kD / 2) + 32 * cc;
-        tmem_ld32(tbase + lane_off + TM_O + col, o);
+      for (int hh = 0; hh < HPC; ++hh) {
+        // this thread's half of the row: head-dim columns half * kD / 2 ..
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          float x[8];
-          unpack8(dov[4 * cc + g], x);
+        for (int cc = 0; cc < kD / 64; ++cc) {
+          float o[32];
+          const int col = half * (kD / 2) + 32 * cc;
+          tmem_ld32(tbase + lane_off + TM_O + hh * kD + col, o);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) d += x[e] * o[8 * g + e];
+          for (int g = 0; g < 4; ++g) {
+            float x[8];
+            if (HPC == 1) {
+              unpack8(dov[(4 * cc + g) % kDoVec], x);
+            } else {
+              uint4 u = make_uint4(0, 0, 0, 0);
+              if (r < qrows)
+                u = *reinterpret_cast<const uint4*>(p.dO + (long long)(s0 + i0 + r) * p.do_ld + (h0 + hh) * kD +
+                                                    col + 8 * g);
+              unpack8(u, x);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) d[hh] += x[e] * o[8 * g + e];
+          }
         }
       }
     } else {
       ok = false;
     }
-    part[half * 128 + r] = d;
+#pragma unroll
+    for (int hh = 0; hh < HPC; ++hh) part[(hh * 2 + half) * 128 + r] = d[hh];
     named_bar(1, 32 * kSoftWarps);
-    if (ok && half == 0 && r < qrows) p.Dvec[(long long)h * p.M + s0 + i0 + r] = d + part[128 + r];
+    if (ok && half == 0 && r < qrows)
+#pragma unroll
+      for (int hh = 0; hh < HPC; ++hh)
+        p.Dvec[(long long)(h0 + hh) * p.M + s0 + i0 + r] = d[hh] + part[(hh * 2 + 1) * 128 + r];
   }
   fence_before();
   __syncthreads();
@@ -1229,8 +1271,11 @@ cudaError_t run(const Ctx& c, const AttnK& k, float rope_base, const AttnArgs& a
       e = cudaFuncSetAttribute(attn_main_tc128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(tcattn128::kSmem));
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_dprep_tc_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(DprepCfg<DH>::kSmem));
+      e = cudaFuncSetAttribute(attn_dprep_tc_kernel<DH, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(DprepCfg<DH, 1>::kSmem));
+    if (e == cudaSuccess && DH == 64)
+      e = cudaFuncSetAttribute(attn_dprep_tc_kernel<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(DprepCfg<64, 4>::kSmem));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) seen[dev] = 1;
   }
@@ -1264,8 +1309,13 @@ cudaError_t run(const Ctx& c, const AttnK& k, float rope_base, const AttnArgs& a
     dp.dO = k.dO; dp.do_ld = k.do_ld;
     dp.st = c.st;
     prof_begin(c, "attn_dprep_tc");
-    attn_dprep_tc_kernel<DH><<<k.B * k.H * nkb, DprepCfg<DH>::kThreads, DprepCfg<DH>::kSmem, c.stream>>>(tq_pre, tk,
-                                                                                                          tv, dp);
+    // four query heads of one kv head per CTA share each K/V block (head dim 64, groups of 4+)
+    if (DH == 64 && k.G % 4 == 0)
+      attn_dprep_tc_kernel<64, 4><<<k.B * (k.H / 4) * nkb, DprepCfg<64, 4>::kThreads, DprepCfg<64, 4>::kSmem,
+                                    c.stream>>>(tq_pre, tk, tv, dp);
+    else
+      attn_dprep_tc_kernel<DH, 1><<<k.B * k.H * nkb, DprepCfg<DH, 1>::kThreads, DprepCfg<DH, 1>::kSmem, c.stream>>>(
+          tq_pre, tk, tv, dp);
     prof_end(c);
     prof_begin(c, "attn_main_tc");
     if (DH == 64)
