@@ -204,6 +204,7 @@ class Block:
         self.keep_np = tn["keep"]
         self.W = {k: torch.from_numpy(v).to(dev).bfloat16() for k, v in wn.items()}
         x = torch.from_numpy(tn["x"]).to(dev).bfloat16()
+        self.x = x
         self.dout = torch.from_numpy(tn["dout"]).to(dev).bfloat16()
         self.masks = {"filtered": torch.from_numpy(tn["keep"]).to(dev),
                       "unfiltered": torch.ones(s.B, s.T, dtype=torch.uint8, device=dev)}
@@ -220,6 +221,31 @@ class Block:
         self.idx = torch.empty(s.M, dtype=torch.int32, device=dev)
         self.cu = torch.empty(s.B + 1, dtype=torch.int32, device=dev)
         self.nk = torch.empty(1, dtype=torch.int32, device=dev)
+
+    def native_forward(self):
+        """Buffers for the library's own dense forward (collider_layer_fwd) of this
+        block; returns a function that runs it on a stream."""
+        import torch
+        cl, s, dev = self.cl, self.s, self.x.device
+        g = lambda k: self.W[k].data_ptr() if k in self.W else None
+        self.fw_params = cl.LayerParams(**{k: g(k) for k in ("norm1_w", "norm1_b", "w_qkv", "b_qkv", "w_o", "b_o",
+                                                             "norm2_w", "w_up", "b_up", "w_down", "b_down")})
+        bf = lambda *shp: torch.empty(shp, dtype=torch.bfloat16, device=dev)
+        f32 = lambda *shp: torch.empty(shp, dtype=torch.float32, device=dev)
+        t = dict(a=bf(s.M, s.D), rstd1=f32(s.M), qkv=bf(s.M, s.Nqkv), o=bf(s.M, s.H * s.dh),
+                 lse=f32(s.B, s.H, s.T), up=bf(s.M, s.Nup))
+        if s.arch == "llama":
+            t.update(h=bf(s.M, s.D), b=bf(s.M, s.D), rstd2=f32(s.M), s=bf(s.M, s.F))
+        else:
+            t["mean1"] = f32(s.M)
+        self.fw_t = t
+        self.fw_acts = cl.LayerActs(**{k: v.data_ptr() for k, v in t.items()})
+        self.fw_y = bf(s.M, s.D)
+        self.fw_ws = torch.empty(cl.collider_layer_fwd_workspace_size(self.desc), dtype=torch.uint8, device=dev)
+
+        def run(stream):
+            cl.collider_layer_fwd(self.desc, self.fw_params, self.x, self.fw_y, self.fw_acts, self.fw_ws, stream)
+        return run
 
     def step(self, mask, stream, sv=None, dout=None):
         cl, s = self.cl, self.s
@@ -569,6 +595,29 @@ def run_ours(args):
     e2e_ms = e0.elapsed_time(e1) / args.steps
     e2e_ms = max_over_ranks([e2e_ms], dev)[0]
 
+    # ---- the library's own dense forward of the same block ----------------
+    # (collider_layer_fwd: the producer of the saved set; not part of the
+    # filtered backward's step, reported beside it)
+    fwd_run = blk.native_forward()
+    ms_fwd, fwd_launches = timed(masks["filtered"], args.steps, args.warmup, lambda m: fwd_run(stream))
+    ms_fwd = max_over_ranks([ms_fwd], dev)[0]
+    cl.collider_profile_enable(1)
+    for _ in range(args.steps):
+        flush.fill_(1)
+        fwd_run(stream)
+    torch.cuda.synchronize()
+    cl.collider_profile_enable(0)
+    fwd_per, fwd_gemm_ms, fwd_gemm_fl = {}, 0.0, 0.0
+    for i in range(cl.collider_profile_count()):
+        name, (m, n, k, dyn), ms = cl.collider_profile_get(i)
+        fwd_per[name] = fwd_per.get(name, 0.0) + ms / args.steps
+        if name == "tc_gemm":
+            fwd_gemm_ms += ms / args.steps
+            fwd_gemm_fl += 2.0 * m * n * k
+    forward = {"ms_per_step": ms_fwd, "tokens_per_s": s.M * world / (ms_fwd * 1e-3), "gpu_launches": fwd_launches,
+               "gemm_tflops": fwd_gemm_fl / args.steps / (fwd_gemm_ms * 1e-3) / 1e12 if fwd_gemm_ms > 0 else None,
+               "kernels_ms_per_step": {k: round(v, 4) for k, v in sorted(fwd_per.items())}}
+
     # ---- the other block shapes and the 22-block stack (filtered vs unfiltered) ----
     configs = {}
     if not args.headline_only:
@@ -621,6 +670,7 @@ def run_ours(args):
                       for k, v in gemm_shapes.items()},
             "gpu_launches": launches,
             "configs": configs,
+            "forward": forward,
             "clocks": clocks,
             "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},

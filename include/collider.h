@@ -318,6 +318,67 @@ collider_status collider_layer_bwd(const collider_layer_desc* desc,
                                    void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Dense forward of one block (Fig. 2b: the forward stays dense; it saves    */
+/* what the filtered backward reads)                                         */
+/* ------------------------------------------------------------------------ */
+
+/* Every parameter of a block, bf16, layouts as collider_layer_weights.
+ * Biases are read only where the desc asks for them: b_qkv [(H+2Hkv)dh]
+ * (qkv_bias), b_o [D] (out_bias), b_up [F] and b_down [D] (mlp_bias, PHI
+ * only: LLAMA MLPs have no bias, as in the backward).  norm1_b is the
+ * LayerNorm beta (PHI). */
+typedef struct {
+  const void* norm1_w;
+  const void* norm1_b;
+  const void* w_qkv;
+  const void* b_qkv;
+  const void* w_o;
+  const void* b_o;
+  const void* norm2_w;
+  const void* w_up;
+  const void* b_up;
+  const void* w_down;
+  const void* b_down;
+} collider_layer_params;
+
+/* Where the forward writes the saved set: the buffers of collider_layer_saved
+ * without x (the block input), same shapes and types.  LLAMA writes a, rstd1,
+ * qkv, o, lse, h, b, rstd2, up, s (mean1 unused); PHI writes a, mean1, rstd1,
+ * qkv, o, lse, up (h, b, rstd2, s unused and may be NULL). */
+typedef struct {
+  void* a;
+  float* mean1;
+  float* rstd1;
+  void* qkv;
+  void* o;
+  float* lse;
+  void* h;
+  void* b;
+  float* rstd2;
+  void* up;
+  void* s;
+} collider_layer_acts;
+
+/* y = block(x) for all M = B*T tokens (x, y bf16 [M, D], FULL rows), causal
+ * attention inside each sequence of T tokens, and the saved set in `acts`:
+ *   LLAMA: a = RMSNorm1(x); qkv = rope(a W_qkv (+ b_qkv)); o = attn(qkv);
+ *          h = x + o W_o (+ b_o); b = RMSNorm2(h); up = b W_up = [g | u];
+ *          s = silu(g) u; y = h + s W_down
+ *   PHI:   a = LayerNorm(x); qkv, o as above (partial RoPE); up = a W1 + b1;
+ *          y = x + (o W_o + b_o) + (gelu_tanh(up) W2 + b2)
+ * Products accumulate in f32 (tcgen05 GEMMs; attention as two passes, the
+ * log-sum-exp of each query row then O = exp(S - lse) V); each saved tensor
+ * is rounded to its storage type once, and the projection sums (with their
+ * bias) are rounded to bf16 before RoPE, the activation and the second norm.
+ * lse is the natural-log log-sum-exp of the scaled logits, [B, H, T].
+ * Pointers 16-byte aligned; workspace (256-byte aligned) of
+ * collider_layer_fwd_workspace_size bytes.  Asynchronous on the stream. */
+size_t collider_layer_fwd_workspace_size(const collider_layer_desc* desc);
+collider_status collider_layer_fwd(const collider_layer_desc* desc, const collider_layer_params* w,
+                                   const void* x, void* y, const collider_layer_acts* acts,
+                                   void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Whole stack: embedding -> L blocks -> final RMSNorm -> LM head -> CE      */
 /* ------------------------------------------------------------------------ */
 

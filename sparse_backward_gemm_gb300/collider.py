@@ -17,14 +17,15 @@ __all__ = [
     "ColliderError", "lib", "LIB_PATH", "ROWS_FULL", "ROWS_COMPACT", "F32", "BF16",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_TIMEOUT",
     "ARCH_LLAMA", "ARCH_PHI", "NORM_RMS", "NORM_LAYER", "ACT_SWIGLU", "ACT_GELU_TANH",
-    "LayerDesc", "LayerWeights", "LayerSaved", "LayerGrads", "EXPORTED",
+    "LayerDesc", "LayerWeights", "LayerSaved", "LayerGrads", "LayerParams", "LayerActs", "EXPORTED",
     "collider_last_error", "collider_check", "collider_selftest_wait_timeout", "collider_launch_count",
     "collider_profile_enable", "collider_profile_count", "collider_profile_get",
     "collider_select_keep", "collider_compact_workspace_size", "collider_compact", "collider_compact_noalloc",
     "collider_gather_rows",
     "collider_scatter_rows", "collider_linear_workspace_size", "collider_linear_bwd",
     "collider_attn_workspace_size", "collider_attn_bwd", "collider_layer_workspace_size",
-    "collider_layer_bwd", "collider_stack_workspace_size", "collider_stack_bwd",
+    "collider_layer_bwd", "collider_layer_fwd_workspace_size", "collider_layer_fwd",
+    "collider_stack_workspace_size", "collider_stack_bwd",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcollider.so")
@@ -65,6 +66,16 @@ class LayerGrads(C.Structure):
                                           "db_o", "dnorm2_w", "dw_up", "db_up", "dw_down", "db_down")]
 
 
+class LayerParams(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("norm1_w", "norm1_b", "w_qkv", "b_qkv", "w_o", "b_o", "norm2_w",
+                                          "w_up", "b_up", "w_down", "b_down")]
+
+
+class LayerActs(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("a", "mean1", "rstd1", "qkv", "o", "lse", "h", "b", "rstd2", "up",
+                                          "s")]
+
+
 P = C.c_void_p
 I = C.c_int
 SZ = C.c_size_t
@@ -91,6 +102,9 @@ _SIGS = {
     "collider_layer_workspace_size": (SZ, [C.POINTER(LayerDesc)]),
     "collider_layer_bwd": (I, [C.POINTER(LayerDesc), C.POINTER(LayerWeights), C.POINTER(LayerSaved), P, I,
                                P, P, P, C.POINTER(LayerGrads), I, P, SZ, P]),
+    "collider_layer_fwd_workspace_size": (SZ, [C.POINTER(LayerDesc)]),
+    "collider_layer_fwd": (I, [C.POINTER(LayerDesc), C.POINTER(LayerParams), P, P, C.POINTER(LayerActs), P, SZ,
+                               P]),
     "collider_stack_workspace_size": (SZ, [C.POINTER(LayerDesc), I, I]),
     "collider_stack_bwd": (I, [C.POINTER(LayerDesc), I, I, C.POINTER(LayerWeights), C.POINTER(LayerSaved),
                                P, P, P, P, P, P, P, P, P, P, P, C.POINTER(LayerGrads), P, P, P, P, SZ, P]),
@@ -244,6 +258,15 @@ def collider_layer_bwd(desc, weights, saved, dOut, dout_rows, idx, cu_kept, n_ke
                        stream=None) -> None:
     _check(lib().collider_layer_bwd(C.byref(desc), C.byref(weights), C.byref(saved), _ptr(dOut), dout_rows,
                                     _ptr(idx), _ptr(cu_kept), _ptr(n_kept), C.byref(grads), dx_rows, _ptr(ws),
+                                    _nbytes(ws), _stream(stream)))
+
+
+def collider_layer_fwd_workspace_size(desc: LayerDesc) -> int:
+    return lib().collider_layer_fwd_workspace_size(C.byref(desc))
+
+
+def collider_layer_fwd(desc, params, x, y, acts, ws, stream=None) -> None:
+    _check(lib().collider_layer_fwd(C.byref(desc), C.byref(params), _ptr(x), _ptr(y), C.byref(acts), _ptr(ws),
                                     _nbytes(ws), _stream(stream)))
 
 

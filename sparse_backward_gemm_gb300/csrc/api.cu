@@ -933,6 +933,152 @@ extern "C" collider_status collider_layer_bwd(const collider_layer_desc* d, cons
 }
 
 // ===========================================================================
+// dense forward of one block
+// ===========================================================================
+namespace {
+
+struct FwdBufs {
+  float *qkv_acc, *attn_acc, *up_acc, *mlp_acc;   // f32 projection outputs [M, N]
+  __nv_bfloat16* act;   // PHI: gelu(f1) [M, F]
+  float* lse2;          // [H, M]
+  float2* rope;         // [T, rotary_dim / 2]
+  int32_t* cu;          // [B + 1]
+};
+
+void fwd_carve(Carver& cv, const collider_layer_desc* d, FwdBufs* f) {
+  const size_t M = (size_t)d->B * d->T;
+  const size_t D = d->D, F = d->F, Nqkv = (size_t)(d->H + 2 * d->Hkv) * d->dh;
+  const bool llama = d->arch == COLLIDER_ARCH_LLAMA;
+  f->qkv_acc = cv.take<float>(M * Nqkv);
+  f->attn_acc = cv.take<float>(M * D);
+  f->up_acc = cv.take<float>(M * (llama ? 2 * F : F));
+  f->mlp_acc = cv.take<float>(M * D);
+  f->act = llama ? nullptr : cv.take<__nv_bfloat16>(M * F);
+  f->lse2 = cv.take<float>(M * d->H);
+  f->rope = cv.take<float2>((size_t)d->T * (d->rotary_dim > 0 ? d->rotary_dim / 2 : 1));
+  f->cu = cv.take<int32_t>((size_t)d->B + 1);
+}
+
+// C [M, N] f32 = A [M, K] . W with W stored [K, N] (the MN-major B operand)
+cudaError_t gemm_fwd(const Ctx& c, int M, int K, int N, const void* A, const void* W, float* C) {
+  TcGemm g{};
+  g.M = M; g.N = N; g.K = K;
+  g.A = A; g.lda = K; g.a_mn_major = 0; g.a_rows = M;
+  g.B = W; g.ldb = N; g.b_mn_major = 1; g.b_rows = K;
+  g.C = C; g.ldc = N; g.c_bf16 = 0; g.c_rows = M;
+  return launch_tc_gemm(c, g);
+}
+
+collider_status layer_fwd_impl(const Ctx& c, const collider_layer_desc* d, const collider_layer_params* w,
+                               const void* x_, void* y_, const collider_layer_acts* ac, FwdBufs& F) {
+  using bf = __nv_bfloat16;
+  const int M = d->B * d->T;
+  const int D = d->D, Ff = d->F, H = d->H, Hkv = d->Hkv, dh = d->dh;
+  const int Hd = H * dh, Nqkv = (H + 2 * Hkv) * dh;
+  const bool llama = d->arch == COLLIDER_ARCH_LLAMA;
+  const bf* x = static_cast<const bf*>(x_);
+  auto B16 = [](const void* p) { return static_cast<const bf*>(p); };
+  const bf* b_qkv = d->qkv_bias ? B16(w->b_qkv) : nullptr;
+  const bf* b_o = d->out_bias ? B16(w->b_o) : nullptr;
+  const bf* b_up = (!llama && d->mlp_bias) ? B16(w->b_up) : nullptr;
+  const bf* b_down = (!llama && d->mlp_bias) ? B16(w->b_down) : nullptr;
+  bf* a = static_cast<bf*>(ac->a);
+  bf* qkv = static_cast<bf*>(ac->qkv);
+  bf* o = static_cast<bf*>(ac->o);
+
+  // 1. input norm
+  NormFwdArgs n1{};
+  n1.layer_norm = llama ? 0 : 1; n1.M = M; n1.D = D; n1.eps = d->eps; n1.x = x;
+  n1.gamma = B16(w->norm1_w); n1.beta = llama ? nullptr : B16(w->norm1_b);
+  n1.out = a; n1.mean = llama ? nullptr : ac->mean1; n1.rstd = ac->rstd1;
+  CK(launch_norm_fwd(c, n1));
+  // 2. QKV projection, bias and RoPE
+  CK(gemm_fwd(c, M, D, Nqkv, a, w->w_qkv, F.qkv_acc));
+  const int rot_half = d->rotary_dim / 2;
+  CK(launch_rope_table(c, d->T, rot_half, d->rope_base, F.rope));
+  CK(launch_qkv_rope_fwd(c, M, Nqkv, H + Hkv, dh, rot_half, d->T, F.qkv_acc, b_qkv, F.rope, qkv));
+  // 3. causal attention over every sequence
+  CK(launch_iota_cu(c, d->B, d->T, F.cu));
+  {
+    AttnFwdArgs at{};
+    at.B = d->B; at.T = d->T; at.H = H; at.Hkv = Hkv; at.dh = dh; at.scale = 1.0f / sqrtf((float)dh);
+    at.q = qkv; at.k = qkv + Hd; at.v = qkv + Hd + Hkv * dh; at.q_ld = Nqkv; at.kv_ld = Nqkv;
+    at.o = o; at.o_ld = Hd; at.lse = ac->lse; at.lse2 = F.lse2; at.cu = F.cu; at.M = M;
+    CK(launch_attn_fwd(c, at));
+  }
+  // 4. output projection, then the MLP
+  CK(gemm_fwd(c, M, Hd, D, o, w->w_o, F.attn_acc));
+  bf* y = static_cast<bf*>(y_);
+  if (llama) {
+    NormFwdArgs n2{};
+    n2.layer_norm = 0; n2.M = M; n2.D = D; n2.eps = d->eps; n2.x = x;
+    n2.add = F.attn_acc; n2.add_ld = D; n2.add_bias = b_o; n2.sum_out = static_cast<bf*>(ac->h);
+    n2.gamma = B16(w->norm2_w); n2.out = static_cast<bf*>(ac->b); n2.rstd = ac->rstd2;
+    CK(launch_norm_fwd(c, n2));                                                    // h = x + attn, b = norm2(h)
+    CK(gemm_fwd(c, M, D, 2 * Ff, ac->b, w->w_up, F.up_acc));                        // [g | u] = b W_up
+    CK(launch_act_fwd(c, 0, M, Ff, F.up_acc, nullptr, static_cast<bf*>(ac->up), static_cast<bf*>(ac->s)));
+    CK(gemm_fwd(c, M, Ff, D, ac->s, w->w_down, F.mlp_acc));                         // s W_down
+    CK(launch_residual_out(c, M, D, static_cast<const bf*>(ac->h), F.mlp_acc, nullptr, nullptr, nullptr, y));
+  } else {
+    CK(gemm_fwd(c, M, D, Ff, a, w->w_up, F.up_acc));                                // f1 = a W1 (+ b1)
+    CK(launch_act_fwd(c, 1, M, Ff, F.up_acc, b_up, static_cast<bf*>(ac->up), F.act));
+    CK(gemm_fwd(c, M, Ff, D, F.act, w->w_down, F.mlp_acc));                         // gelu(f1) W2
+    CK(launch_residual_out(c, M, D, x, F.attn_acc, b_o, F.mlp_acc, b_down, y));
+  }
+  return COLLIDER_OK;
+}
+
+collider_status check_fwd_ptrs(const collider_layer_desc* d, const collider_layer_params* w, const void* x,
+                               const void* y, const collider_layer_acts* ac) {
+  if (!w || !ac || !x || !y) return fail(COLLIDER_ERR_INVALID_ARG, "null params/acts/x/y");
+  const bool llama = d->arch == COLLIDER_ARCH_LLAMA;
+  const void* req[] = {w->norm1_w, w->w_qkv, w->w_o, w->w_up, w->w_down, ac->a, ac->rstd1, ac->qkv, ac->o,
+                       ac->lse, ac->up};
+  for (const void* p : req)
+    if (!p) return fail(COLLIDER_ERR_INVALID_ARG, "a required parameter or saved-set pointer is null");
+  if (llama && (!w->norm2_w || !ac->h || !ac->b || !ac->rstd2 || !ac->s))
+    return fail(COLLIDER_ERR_INVALID_ARG, "llama block needs norm2_w, h, b, rstd2 and s");
+  if (!llama && (!w->norm1_b || !ac->mean1))
+    return fail(COLLIDER_ERR_INVALID_ARG, "phi block needs norm1_b and mean1");
+  if ((d->qkv_bias && !w->b_qkv) || (d->out_bias && !w->b_o) || (!llama && d->mlp_bias && (!w->b_up || !w->b_down)))
+    return fail(COLLIDER_ERR_INVALID_ARG, "a bias the desc asks for is null");
+  const void* al[] = {x, y, w->norm1_w, w->norm1_b, w->w_qkv, w->b_qkv, w->w_o, w->b_o, w->norm2_w, w->w_up,
+                      w->b_up, w->w_down, w->b_down, ac->a, ac->qkv, ac->o, ac->h, ac->b, ac->up, ac->s};
+  for (const void* p : al)
+    if (!al16(p)) return fail(COLLIDER_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  return COLLIDER_OK;
+}
+
+}  // namespace
+
+extern "C" size_t collider_layer_fwd_workspace_size(const collider_layer_desc* d) {
+  if (check_desc(d) != COLLIDER_OK) return 0;
+  Carver cv{nullptr, 0, 0, true};
+  FwdBufs f;
+  fwd_carve(cv, d, &f);
+  return cv.used;
+}
+
+extern "C" collider_status collider_layer_fwd(const collider_layer_desc* d, const collider_layer_params* w,
+                                              const void* x, void* y, const collider_layer_acts* acts, void* ws,
+                                              size_t ws_bytes, void* stream) {
+  collider_status s = check_desc(d);
+  if (s != COLLIDER_OK) return s;
+  s = check_fwd_ptrs(d, w, x, y, acts);
+  if (s != COLLIDER_OK) return s;
+  const size_t need = collider_layer_fwd_workspace_size(d);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255))
+    return fail(COLLIDER_ERR_INVALID_ARG, "collider_layer_fwd: needs %zu bytes of 256-aligned workspace", need);
+  Ctx c;
+  s = make_ctx(stream, &c);
+  if (s != COLLIDER_OK) return s;
+  Carver cv{static_cast<char*>(ws), ws_bytes, 0, false};
+  FwdBufs f;
+  fwd_carve(cv, d, &f);
+  return layer_fwd_impl(c, d, w, x, y, acts, f);
+}
+
+// ===========================================================================
 // whole stack
 // ===========================================================================
 namespace {

@@ -23,6 +23,7 @@ namespace collider {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 struct AttnK {
   int B, T, H, Hkv, G, causal;
@@ -45,6 +46,29 @@ struct AttnK {
   long long cap;     // row capacity of dq, dk, dv
   DevStatus* st;
 };
+
+// ---------------------------------------------------------------------------
+// RoPE table [T, rot_half] of (cos, sin): theta_i = base^(-2i/r) once per
+// block in fp64; the angle pos * theta_i and its reduction mod 2 pi in fp64,
+// then sin / cos of the reduced angle.  Called by every thread of the block
+// (rot_half <= 256).
+__device__ __forceinline__ void fill_rope_table(int T, int rot_half, float rope_base, float2* rope, long long tid,
+                                                long long stride) {
+  __shared__ double inv[256];
+  const int rd = 2 * rot_half;
+  for (int i = threadIdx.x; i < rot_half && i < 256; i += blockDim.x)
+    inv[i] = pow((double)rope_base, -(2.0 * i) / (double)rd);
+  __syncthreads();
+  const double two_pi = 6.283185307179586476925;
+  for (long long e = tid; e < (long long)T * rot_half; e += stride) {
+    const int pos = (int)(e / rot_half), i = (int)(e % rot_half);
+    const double ang = (double)pos * inv[i];
+    const float red = (float)(ang - rint(ang / two_pi) * two_pi);
+    float sn, cs;
+    sincosf(red, &sn, &cs);
+    rope[e] = make_float2(cs, sn);
+  }
+}
 
 // ---------------------------------------------------------------------------
 // prep: lse in kept order (log2 units), dQ accumulator reset, RoPE table
@@ -70,24 +94,12 @@ __global__ void attn_prep_kernel(AttnK p, int DH, float rope_base, float2* rope)
       v4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
-  if (p.rot_half > 0) {
-    // theta_i = base^(-2i/r) once per block in fp64; the angle pos * theta_i
-    // and its reduction mod 2 pi in fp64, then sin / cos of the reduced angle
-    __shared__ double inv[256];
-    const int rd = 2 * p.rot_half;
-    for (int i = threadIdx.x; i < p.rot_half && i < 256; i += blockDim.x)
-      inv[i] = pow((double)rope_base, -(2.0 * i) / (double)rd);
-    __syncthreads();
-    const double two_pi = 6.283185307179586476925;
-    for (long long e = tid; e < (long long)p.T * p.rot_half; e += stride) {
-      const int pos = (int)(e / p.rot_half), i = (int)(e % p.rot_half);
-      const double ang = (double)pos * inv[i];
-      const float red = (float)(ang - rint(ang / two_pi) * two_pi);
-      float sn, cs;
-      sincosf(red, &sn, &cs);
-      rope[e] = make_float2(cs, sn);
-    }
-  }
+  if (p.rot_half > 0) fill_rope_table(p.T, p.rot_half, rope_base, rope, tid, stride);
+}
+
+__global__ void rope_table_kernel(int T, int rot_half, float rope_base, float2* rope) {
+  fill_rope_table(T, rot_half, rope_base, rope, blockIdx.x * (long long)blockDim.x + threadIdx.x,
+                  (long long)gridDim.x * blockDim.x);
 }
 
 // ---------------------------------------------------------------------------
@@ -956,7 +968,16 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
 //              -> bf16 -> shared; at the end D_h from O'_h (TMEM) and dO_h
 //              (global), each half of the row's columns summed separately
 // TMEM columns: S buffers 0-127 and 128-255, O'_h from 256 + h * head dim.
-template <int DH, int HPC>
+//
+// The same pipeline also serves the dense attention forward over whole
+// sequences (every token kept), as two passes (MODE):
+//   2  log-sum-exp: S = Q_h K_j^T only (no V); each thread keeps a running
+//      max and sum of exp2 over its 64 keys, the two halves of a row are
+//      merged at the end -> lse (log2 units for pass 1, natural log [B,H,T])
+//   1  output: exactly the D pre-pass's O'_h with the lse of pass 2, so
+//      O'_h = softmax(Q_h K^T scale) V; written as bf16 instead of D.
+// MODE 0 is the D pre-pass of the backward.
+template <int DH, int HPC, int MODE = 0>
 struct DprepCfg {
   static constexpr int kQ = 128, kK = 128, kD = DH, kCh = DH / 64;   // 64-column chunks
   static constexpr uint32_t kTile = 16384;                           // 128 rows x 64 columns
@@ -965,7 +986,7 @@ struct DprepCfg {
   static constexpr uint32_t OFF_Q = 0, OFF_K = HPC * kCh * kTile, OFF_P = OFF_K + kKV * kKVBytes,
                             OFF_BAR = OFF_P + 4 * kTile;
   static constexpr uint32_t OFF_PART = OFF_BAR + 256;                // [HPC][2][128] f32 partial dot products
-  static constexpr size_t kSmem = 1024 + OFF_PART + HPC * 1024;
+  static constexpr size_t kSmem = 1024 + OFF_PART + HPC * 1024;   // MODE 2 merges in the (unused) P tiles
   static constexpr uint32_t TM_S = 0, TM_O = 256;
   static constexpr int kSoftWarps = 8;                               // two per TMEM lane quadrant
   static constexpr int kThreads = 32 * (2 + kSoftWarps);
@@ -983,14 +1004,18 @@ struct DprepTc {
   long long do_ld;
   long long M;
   DevStatus* st;
+  // forward passes (every token kept: row s0 + i is position i)
+  __nv_bfloat16* O;          // MODE 1: attention output rows, head h at columns h * DH
+  long long o_ld;
+  float* lse2_out;           // MODE 2: [H, M] log2 units
+  float* lse_out;            // MODE 2: [B, H, T] natural log
 };
 
-template <int DH, int HPC>
-__global__ void __launch_bounds__(DprepCfg<DH, HPC>::kThreads, 1)
-    attn_dprep_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                         const __grid_constant__ CUtensorMap tmV, DprepTc p) {
+template <int DH, int HPC, int MODE>
+__device__ __forceinline__ void dprep_body(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                           const DprepTc& p) {
   using namespace tc;
-  using Cfg = DprepCfg<DH, HPC>;
+  using Cfg = DprepCfg<DH, HPC, MODE>;
   constexpr int kQ = Cfg::kQ, kK = Cfg::kK, kD = Cfg::kD, kCh = Cfg::kCh, kKV = Cfg::kKV, kSoftWarps = Cfg::kSoftWarps;
   constexpr uint32_t kTile = Cfg::kTile, kKVBytes = Cfg::kKVBytes, OFF_Q = Cfg::OFF_Q, OFF_K = Cfg::OFF_K,
                      OFF_P = Cfg::OFF_P, OFF_BAR = Cfg::OFF_BAR, OFF_PART = Cfg::OFF_PART, TM_S = Cfg::TM_S,
@@ -1012,11 +1037,16 @@ __global__ void __launch_bounds__(DprepCfg<DH, HPC>::kThreads, 1)
   const int qrows = min(kQ, len - i0);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-  // kv_full/kv_empty/kv_ready: one per K/V stage; s_full/p_empty: one per S / P buffer
+  // kv_full/kv_empty/kv_ready: one per K/V stage; s_full/p_full/p_empty: one
+  // per S / P buffer.  Every barrier's next phase needs the waiter to have
+  // seen the previous one (p_full of iteration t+2 needs p_empty of t, which
+  // the MMA commits only after its wait on p_full of t), so no parity wait can
+  // miss a phase.  A single p_full for both buffers would not have that: the
+  // softmax could finish iterations t and t+1 before the MMA looks at t.
   const uint32_t b_q = smem_u32(bars + 0), b_kvfull = smem_u32(bars + 1), b_kvempty = smem_u32(bars + 4),
                  b_kvready = smem_u32(bars + 7), b_sfull = smem_u32(bars + 10), b_pempty = smem_u32(bars + 12),
-                 b_pfull = smem_u32(bars + 14), b_ofull = smem_u32(bars + 15);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+                 b_pfull = smem_u32(bars + 14), b_ofull = smem_u32(bars + 16);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -1029,8 +1059,8 @@ __global__ void __launch_bounds__(DprepCfg<DH, HPC>::kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(b_sfull + 8 * s, 1);
       mbar_init(b_pempty + 8 * s, 1);
+      mbar_init(b_pfull + 8 * s, 32 * kSoftWarps);
     }
-    mbar_init(b_pfull, 32 * kSoftWarps);
     mbar_init(b_ofull, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1049,12 +1079,13 @@ __global__ void __launch_bounds__(DprepCfg<DH, HPC>::kThreads, 1)
     auto issue = [&](int j) -> bool {
       const int st = j % kKV, use = j / kKV;
       if (!mbar_wait(b_kvempty + 8 * st, (use & 1) ^ 1, abort_flag, p.st, 40)) return false;
-      mbar_expect_tx(b_kvfull + 8 * st, kKVBytes);
+      mbar_expect_tx(b_kvfull + 8 * st, MODE == 2 ? kCh * kTile : kKVBytes);   // the lse pass reads no V
       const uint32_t kb = sbase + OFF_K + st * kKVBytes;
 #pragma unroll
       for (int c = 0; c < kCh; ++c) {
         tma_load_2d(kb + c * kTile, &tmK, b_kvfull + 8 * st, hk * kD + 64 * c, s0 + j * kK);
-        tma_load_2d(kb + (kCh + c) * kTile, &tmV, b_kvfull + 8 * st, hk * kD + 64 * c, s0 + j * kK);
+        if (MODE != 2)
+          tma_load_2d(kb + (kCh + c) * kTile, &tmV, b_kvfull + 8 * st, hk * kD + 64 * c, s0 + j * kK);
       }
       return true;
     };
@@ -1109,14 +1140,16 @@ __global__ void __launch_bounds__(DprepCfg<DH, HPC>::kThreads, 1)
       auto pv = [&](int t) -> bool {
         const int jj = t / HPC, hh = t % HPC;
         const int kst = jj % kKV, pb = t & 1;
-        if (!mbar_wait(b_pfull, t & 1, abort_flag, p.st, 42)) return false;
+        if (!mbar_wait(b_pfull + 8 * pb, (t >> 1) & 1, abort_flag, p.st, 42)) return false;
         fence_after();
         const uint32_t sv = sbase + OFF_K + kst * kKVBytes + kCh * kTile;
+        if (MODE != 2) {   // the lse pass only releases the buffers
 #pragma unroll
-        for (int kk = 0; kk < kK / 16; ++kk) {   // V as the MN-major B: head-dim chunks kTile apart
-          const uint32_t pa = sbase + OFF_P + pb * 2 * kTile + (kk >> 2) * kTile + (kk & 3) * 32;
-          mma_bf16(tbase + TM_O + hh * kD, sdesc(pa, 16, 1024), sdesc(sv + kk * 2048, kTile, 1024), id_o,
-                   (jj > 0) || (kk > 0));
+          for (int kk = 0; kk < kK / 16; ++kk) {   // V as the MN-major B: head-dim chunks kTile apart
+            const uint32_t pa = sbase + OFF_P + pb * 2 * kTile + (kk >> 2) * kTile + (kk & 3) * 32;
+            mma_bf16(tbase + TM_O + hh * kD, sdesc(pa, 16, 1024), sdesc(sv + kk * 2048, kTile, 1024), id_o,
+                     (jj > 0) || (kk > 0));
+          }
         }
         if (hh == HPC - 1) mma_commit(b_kvempty + 8 * kst);
         mma_commit(b_pempty + 8 * pb);
@@ -1148,12 +1181,20 @@ __global__ void __launch_bounds__(DprepCfg<DH, HPC>::kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     float Lh[HPC];
 #pragma unroll
-    for (int hh = 0; hh < HPC; ++hh) Lh[hh] = (r < qrows) ? p.lse2[(long long)(h0 + hh) * p.M + s0 + i0 + r] : 0.f;
+    for (int hh = 0; hh < HPC; ++hh)
+      Lh[hh] = (MODE != 2 && r < qrows) ? p.lse2[(long long)(h0 + hh) * p.M + s0 + i0 + r] : 0.f;
+    // lse pass: running max and sum of exp2 (log2 units) per head
+    float mrun[HPC], lrun[HPC];
+#pragma unroll
+    for (int hh = 0; hh < HPC; ++hh) {
+      mrun[hh] = -INFINITY;
+      lrun[hh] = 0.f;
+    }
     // with one head, this thread's half of its dO row is loaded now so the
     // latency hides behind the key loop; with several heads at the end
     constexpr int kDoVec = HPC == 1 ? kD / 16 : 1;
     uint4 dov[kDoVec];
-    if (HPC == 1) {
+    if (HPC == 1 && MODE == 0) {
 #pragma unroll
       for (int u = 0; u < kDoVec; ++u) {
         dov[u] = make_uint4(0, 0, 0, 0);
@@ -1180,8 +1221,35 @@ __global__ void __launch_bounds__(DprepCfg<DH, HPC>::kThreads, 1)
       tmem_wait_ld();
       // a full key block strictly before the query block needs no masking
       const bool interior = (!p.causal || j0 + kK <= i0) && qrows == kQ && len - j0 >= kK;
+      if (MODE == 2) {
+        // keys j0 + half * 64 + e of this row, e < 64
+        float xv[64];
+        float bm = -INFINITY;
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
+        for (int e = 0; e < 64; ++e) {
+          const int kj = j0 + half * 64 + e;
+          const bool valid = interior || (r < qrows && kj < len && (!p.causal || kj <= i0 + r));
+          xv[e] = valid ? __uint_as_float(sr[e]) * p.scale_log2 : -INFINITY;
+          bm = fmaxf(bm, xv[e]);
+        }
+        float m = mrun[0], l = lrun[0];
+#pragma unroll
+        for (int x = 1; x < HPC; ++x)
+          if (hh == x) { m = mrun[x]; l = lrun[x]; }
+        const float mn = fmaxf(m, bm);
+        if (mn != -INFINITY) {
+          float acc = 0.f;
+#pragma unroll
+          for (int e = 0; e < 64; ++e) acc += exp2_approx(xv[e] - mn);
+          l = l * exp2_approx(m - mn) + acc;
+          m = mn;
+        }
+#pragma unroll
+        for (int x = 0; x < HPC; ++x)
+          if (hh == x) { mrun[x] = m; lrun[x] = l; }
+      }
+#pragma unroll
+      for (int cc = 0; cc < (MODE == 2 ? 0 : 2); ++cc) {
         const int c = 2 * half + cc;
         float sv[32];
         if (interior) {
@@ -1204,13 +1272,57 @@ __global__ void __launch_bounds__(DprepCfg<DH, HPC>::kThreads, 1)
       }
       fence_before();
       fence_async_smem();
-      mbar_arrive(b_pfull);
+      mbar_arrive(b_pfull + 8 * st);
     }
     float* part = reinterpret_cast<float*>(sm + OFF_PART);   // [HPC][2][128]
+    if (MODE == 1) {
+      // the attention output: this thread's half of the row's head-dim columns
+      if (ok && mbar_wait(b_ofull, 0, &no_abort, p.st, 48)) {
+        fence_after();
+#pragma unroll
+        for (int hh = 0; hh < HPC; ++hh) {
+#pragma unroll
+          for (int cc = 0; cc < kD / 64; ++cc) {
+            float o[32];
+            const int col = half * (kD / 2) + 32 * cc;
+            tmem_ld32(tbase + lane_off + TM_O + hh * kD + col, o);
+            if (r < qrows) {
+              __nv_bfloat16* dst = p.O + (long long)(s0 + i0 + r) * p.o_ld + (h0 + hh) * kD + col;
+#pragma unroll
+              for (int g = 0; g < 4; ++g) *reinterpret_cast<uint4*>(dst + 8 * g) = pack8(o + 8 * g);
+            }
+          }
+        }
+      }
+    } else if (MODE == 2) {
+      // merge the two halves of each row: lse2 = max + log2(sum exp2(x - max))
+      if (!(ok && mbar_wait(b_ofull, 0, &no_abort, p.st, 49))) ok = false;
+      float* pm = reinterpret_cast<float*>(sm + OFF_P);   // no P tile is written in this pass
+      float* pl = pm + HPC * 256;
+#pragma unroll
+      for (int hh = 0; hh < HPC; ++hh) {
+        pm[(hh * 2 + half) * 128 + r] = mrun[hh];
+        pl[(hh * 2 + half) * 128 + r] = lrun[hh];
+      }
+      named_bar(1, 32 * kSoftWarps);
+      if (ok && half == 0 && r < qrows) {
+#pragma unroll
+        for (int hh = 0; hh < HPC; ++hh) {
+          const float m1 = pm[(hh * 2 + 1) * 128 + r], l1 = pl[(hh * 2 + 1) * 128 + r];
+          const float mm = fmaxf(mrun[hh], m1);
+          const float lsum = lrun[hh] * exp2f(mrun[hh] - mm) + l1 * exp2f(m1 - mm);
+          const float lse2 = mm + log2f(lsum);
+          p.lse2_out[(long long)(h0 + hh) * p.M + s0 + i0 + r] = lse2;
+          p.lse_out[((long long)b * p.H + h0 + hh) * p.T + i0 + r] = lse2 * kLn2;
+        }
+      }
+    }
     float d[HPC];
 #pragma unroll
     for (int hh = 0; hh < HPC; ++hh) d[hh] = 0.f;
-    if (ok && mbar_wait(b_ofull, 0, &no_abort, p.st, 46)) {
+    if (MODE != 0) {
+      // the forward passes are done
+    } else if (ok && mbar_wait(b_ofull, 0, &no_abort, p.st, 46)) {
       fence_after();
 #pragma unroll
       for (int hh = 0; hh < HPC; ++hh) {
@@ -1240,13 +1352,15 @@ __global__ void __launch_bounds__(DprepCfg<DH, HPC>::kThreads, 1)
     } else {
       ok = false;
     }
+    if (MODE == 0) {
 #pragma unroll
-    for (int hh = 0; hh < HPC; ++hh) part[(hh * 2 + half) * 128 + r] = d[hh];
-    named_bar(1, 32 * kSoftWarps);
-    if (ok && half == 0 && r < qrows)
+      for (int hh = 0; hh < HPC; ++hh) part[(hh * 2 + half) * 128 + r] = d[hh];
+      named_bar(1, 32 * kSoftWarps);
+      if (ok && half == 0 && r < qrows)
 #pragma unroll
-      for (int hh = 0; hh < HPC; ++hh)
-        p.Dvec[(long long)(h0 + hh) * p.M + s0 + i0 + r] = d[hh] + part[(hh * 2 + 1) * 128 + r];
+        for (int hh = 0; hh < HPC; ++hh)
+          p.Dvec[(long long)(h0 + hh) * p.M + s0 + i0 + r] = d[hh] + part[(hh * 2 + 1) * 128 + r];
+    }
   }
   fence_before();
   __syncthreads();
@@ -1254,6 +1368,29 @@ __global__ void __launch_bounds__(DprepCfg<DH, HPC>::kThreads, 1)
     fence_after();
     tmem_dealloc(tbase, 512);
   }
+}
+
+template <int DH, int HPC>
+__global__ void __launch_bounds__(DprepCfg<DH, HPC>::kThreads, 1)
+    attn_dprep_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, DprepTc p) {
+  dprep_body<DH, HPC, 0>(tmQ, tmK, tmV, p);
+}
+
+// dense forward, pass 1: log-sum-exp of every query row
+template <int DH, int HPC>
+__global__ void __launch_bounds__(DprepCfg<DH, HPC, 2>::kThreads, 1)
+    attn_fwd_lse_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, DprepTc p) {
+  dprep_body<DH, HPC, 2>(tmQ, tmK, tmV, p);
+}
+
+// dense forward, pass 2: O = exp(S - lse) V
+template <int DH, int HPC>
+__global__ void __launch_bounds__(DprepCfg<DH, HPC, 1>::kThreads, 1)
+    attn_fwd_o_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, DprepTc p) {
+  dprep_body<DH, HPC, 1>(tmQ, tmK, tmV, p);
 }
 
 template <int DH>
@@ -1333,7 +1470,78 @@ cudaError_t run(const Ctx& c, const AttnK& k, float rope_base, const AttnArgs& a
   return cudaGetLastError();
 }
 
+template <int DH>
+cudaError_t run_fwd(const Ctx& c, const AttnFwdArgs& a) {
+  static int seen[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !seen[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_lse_kernel<DH, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(DprepCfg<DH, 1, 2>::kSmem));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_fwd_o_kernel<DH, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(DprepCfg<DH, 1, 1>::kSmem));
+    if (e == cudaSuccess && DH == 64)
+      e = cudaFuncSetAttribute(attn_fwd_lse_kernel<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(DprepCfg<64, 4, 2>::kSmem));
+    if (e == cudaSuccess && DH == 64)
+      e = cudaFuncSetAttribute(attn_fwd_o_kernel<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(DprepCfg<64, 4, 1>::kSmem));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) seen[dev] = 1;
+  }
+  const int G = a.H / a.Hkv;
+  CUtensorMap tq, tk, tv;
+  bool ok = make_tensor_map(&tq, a.q, false, (long long)a.H * DH, a.M, a.q_ld, 64, 128) &&
+            make_tensor_map(&tk, a.k, false, (long long)a.Hkv * DH, a.M, a.kv_ld, 64, 128) &&
+            make_tensor_map(&tv, a.v, false, (long long)a.Hkv * DH, a.M, a.kv_ld, 64, 128);
+  if (!ok) return cudaErrorInvalidValue;
+  DprepTc dp{};
+  dp.B = a.B; dp.T = a.T; dp.H = a.H; dp.G = G; dp.causal = 1; dp.nqb = (a.T + 127) / 128;
+  dp.scale_log2 = a.scale * kLog2e; dp.cu_kept = a.cu; dp.lse2 = a.lse2; dp.M = a.M; dp.st = c.st;
+  dp.O = a.o; dp.o_ld = a.o_ld; dp.lse2_out = a.lse2; dp.lse_out = a.lse;
+  const bool multi = DH == 64 && G % 4 == 0;   // four query heads of a kv group per CTA
+  const int grid = a.B * (multi ? a.H / 4 : a.H) * dp.nqb;
+  prof_begin(c, "attn_fwd_lse");
+  if (multi)
+    attn_fwd_lse_kernel<64, 4><<<grid, DprepCfg<64, 4, 2>::kThreads, DprepCfg<64, 4, 2>::kSmem, c.stream>>>(
+        tq, tk, tv, dp);
+  else
+    attn_fwd_lse_kernel<DH, 1><<<grid, DprepCfg<DH, 1, 2>::kThreads, DprepCfg<DH, 1, 2>::kSmem, c.stream>>>(
+        tq, tk, tv, dp);
+  prof_end(c);
+  prof_begin(c, "attn_fwd_o");
+  if (multi)
+    attn_fwd_o_kernel<64, 4><<<grid, DprepCfg<64, 4, 1>::kThreads, DprepCfg<64, 4, 1>::kSmem, c.stream>>>(
+        tq, tk, tv, dp);
+  else
+    attn_fwd_o_kernel<DH, 1><<<grid, DprepCfg<DH, 1, 1>::kThreads, DprepCfg<DH, 1, 1>::kSmem, c.stream>>>(
+        tq, tk, tv, dp);
+  prof_end(c);
+  count_launch(2);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_rope_table(const Ctx& c, int T, int rot_half, float rope_base, float2* rope) {
+  if (rot_half <= 0) return cudaSuccess;
+  if (rot_half > 256) return cudaErrorInvalidValue;
+  const long long n = (long long)T * rot_half;
+  const long long want = (n + 255) / 256, cap = (long long)c.num_sms * 4;
+  const int grid = (int)(want < cap ? want : cap);
+  rope_table_kernel<<<grid, 256, 0, c.stream>>>(T, rot_half, rope_base, rope);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_fwd(const Ctx& c, const AttnFwdArgs& a) {
+  if (a.H < 1 || a.Hkv < 1 || a.H % a.Hkv || a.B < 1 || a.T < 1 || !a.cu || !a.lse || !a.lse2 || !a.o)
+    return cudaErrorInvalidValue;
+  if (a.dh == 64) return run_fwd<64>(c, a);
+  if (a.dh == 128) return run_fwd<128>(c, a);
+  return cudaErrorInvalidValue;
+}
 
 size_t attn_ws_bytes(int B, int T, int H, int Hkv, int dh) {
   const size_t M = (size_t)B * T;

@@ -6,7 +6,9 @@
 //                          (K-major); the M extent is n_kept (device-resident)
 //   dW   = X_k^T . dY_k -> A = X_k [Mk, in], B = dY_k [Mk, out], both
 //                          MN-major; the reduction extent is n_kept
-// Both run here: TMA (cp.async.bulk.tensor, 128-byte swizzle) stages
+// The dense forward's Y = X . W (A = X K-major, B = W [in, out] MN-major)
+// uses the same kernel with static extents.
+// All run here: TMA (cp.async.bulk.tensor, 128-byte swizzle) stages
 // 128 x 64 A tiles and BN x 64 B tiles through a multi-stage shared-memory
 // ring; one thread issues tcgen05.mma (kind::f16, bf16 in, f32 accumulate)
 // into a double-buffered TMEM accumulator; four epilogue warps drain TMEM
@@ -662,7 +664,8 @@ cudaError_t launch_tc_gemm(const Ctx& c, const TcGemm& g) {
     const long long t256 = ((long long)(g.M + BM - 1) / BM) * ((g.N + 255) / 256);
     bn = (t256 >= c.num_sms || g.N % 256 == 0) && g.N >= 256 ? 256 : 128;
   }
-  if (g.a_mn_major != g.b_mn_major) return cudaErrorNotSupported;   // dX: both K-major; dW: both MN-major
+  // dX: both K-major; dW: both MN-major; the forward's Y = X W: A K-major, B MN-major
+  if (g.a_mn_major && !g.b_mn_major) return cudaErrorNotSupported;
   // Work split.  Measured on the block shapes: whole tiles keep the operands'
   // L2 locality and win except for long reductions over a static K (>= 128
   // k-slices), where stream-K's even split pays for its fix-up.
@@ -697,17 +700,22 @@ cudaError_t launch_tc_gemm(const Ctx& c, const TcGemm& g) {
              split, g.epi, g.aux, g.aux_ld, g.idx, g.aux_rows, c.st};
   prof_begin(c, "tc_gemm", g.M, g.N, g.K, g.dyn);
   cudaError_t e;
-  const int key = (bn == 256 ? 100 : 0) + (g.a_mn_major ? 10 : 0) + mode;
+  const int key = (bn == 256 ? 100 : 0) + (g.a_mn_major ? 10 : (g.b_mn_major ? 20 : 0)) + mode;
   switch (key) {
     case 0: e = launch_variant<128, false, false, 0>(c, g, ma, mb, p); break;
     case 1: e = launch_variant<128, false, false, 1>(c, g, ma, mb, p); break;
     case 10: e = launch_variant<128, true, true, 0>(c, g, ma, mb, p); break;
     case 11: e = launch_variant<128, true, true, 1>(c, g, ma, mb, p); break;
+    case 20: e = launch_variant<128, false, true, 0>(c, g, ma, mb, p); break;
+    case 21: e = launch_variant<128, false, true, 1>(c, g, ma, mb, p); break;
     case 100: e = launch_variant<256, false, false, 0>(c, g, ma, mb, p); break;
     case 101: e = launch_variant<256, false, false, 1>(c, g, ma, mb, p); break;
     case 102: e = launch_variant<256, false, false, 2>(c, g, ma, mb, p); break;
     case 110: e = launch_variant<256, true, true, 0>(c, g, ma, mb, p); break;
     case 111: e = launch_variant<256, true, true, 1>(c, g, ma, mb, p); break;
+    case 120: e = launch_variant<256, false, true, 0>(c, g, ma, mb, p); break;
+    case 121: e = launch_variant<256, false, true, 1>(c, g, ma, mb, p); break;
+    case 122: e = launch_variant<256, false, true, 2>(c, g, ma, mb, p); break;
     default: e = launch_variant<256, true, true, 2>(c, g, ma, mb, p); break;
   }
   prof_end(c);

@@ -192,4 +192,56 @@ struct AttnArgs {
 size_t attn_ws_bytes(int B, int T, int H, int Hkv, int dh);
 cudaError_t launch_attn_bwd(const Ctx& c, const AttnArgs& a);
 
+// ---- dense forward of one block (attn.cu, fwd.cu) ---------------------------
+// Causal GQA attention over whole sequences (every token kept), two passes:
+// the log-sum-exp of every query row, then O = exp(S - lse) V.
+struct AttnFwdArgs {
+  int B, T, H, Hkv, dh;
+  float scale;
+  const __nv_bfloat16* q; const __nv_bfloat16* k; const __nv_bfloat16* v;   // FULL rows [M, ...]
+  long long q_ld, kv_ld;   // elements
+  __nv_bfloat16* o; long long o_ld;    // [M, H*dh]
+  float* lse;    // out: [B, H, T] natural log
+  float* lse2;   // scratch [H, M] (log2 units)
+  const int32_t* cu;   // [B+1] = b*T
+  int M;
+};
+cudaError_t launch_attn_fwd(const Ctx& c, const AttnFwdArgs& a);
+// RoPE table [T, rot_half] of (cos, sin), the same values the backward uses.
+cudaError_t launch_rope_table(const Ctx& c, int T, int rot_half, float rope_base, float2* rope);
+
+// Norm forward, one row per CTA (D a multiple of 8, D <= 4096):
+//   v = x, or bf16(x + add + add_bias) (written to sum_out when given);
+//   out = bf16(norm(v) * gamma (+ beta));  mean (LayerNorm) and rstd f32.
+struct NormFwdArgs {
+  int layer_norm;   // 0 RMSNorm, 1 LayerNorm
+  int M, D;
+  float eps;
+  const __nv_bfloat16* x;
+  const float* add; long long add_ld;   // optional f32 [M, D]
+  const __nv_bfloat16* add_bias;        // optional bf16 [D] (with add)
+  __nv_bfloat16* sum_out;               // optional bf16 [M, D]
+  const __nv_bfloat16* gamma;
+  const __nv_bfloat16* beta;            // LayerNorm
+  __nv_bfloat16* out;
+  float* mean;                          // LayerNorm
+  float* rstd;
+};
+cudaError_t launch_norm_fwd(const Ctx& c, const NormFwdArgs& a);
+// qkv = bf16(acc + bias), then the first rot_heads heads (q then k) rotated on
+// their first 2*rot_half dims at position row % T; [M, N] f32 -> bf16.
+cudaError_t launch_qkv_rope_fwd(const Ctx& c, int M, int N, int rot_heads, int dh, int rot_half, int T,
+                                const float* acc, const __nv_bfloat16* bias, const float2* rope,
+                                __nv_bfloat16* qkv);
+// gelu == 0: up = bf16(acc + bias) [M, 2F] = [g | u], act = bf16(silu(g) u) [M, F]
+// gelu == 1: up = bf16(acc + bias) [M, F],            act = bf16(gelu_tanh(up)) [M, F]
+cudaError_t launch_act_fwd(const Ctx& c, int gelu, int M, int F, const float* acc, const __nv_bfloat16* bias,
+                           __nv_bfloat16* up, __nv_bfloat16* act);
+// y = bf16(res + acc1 (+ bias1) (+ acc2 (+ bias2))), all [M, D]
+cudaError_t launch_residual_out(const Ctx& c, int M, int D, const __nv_bfloat16* res, const float* acc1,
+                                const __nv_bfloat16* bias1, const float* acc2, const __nv_bfloat16* bias2,
+                                __nv_bfloat16* y);
+// cu[b] = b * T for b <= B
+cudaError_t launch_iota_cu(const Ctx& c, int B, int T, int32_t* cu);
+
 }  // namespace collider

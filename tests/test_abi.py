@@ -47,8 +47,42 @@ def test_sizing_calls(lib):
                       act=lib.ACT_SWIGLU)
     n = lib.collider_layer_workspace_size(d)
     assert 100 << 20 < n < 4 << 30
+    # the dense forward's scratch: four f32 projection outputs, lse, RoPE table
+    nf = lib.collider_layer_fwd_workspace_size(d)
+    M = s.B * s.T
+    f32_acc = 4 * M * (s.Nqkv + 2 * s.D + 2 * s.F)
+    assert f32_acc <= nf < f32_acc + (16 << 20)
     d.dh = 96            # unsupported head dim -> 0
     assert lib.collider_layer_workspace_size(d) == 0
+    assert lib.collider_layer_fwd_workspace_size(d) == 0
+
+
+def test_forward_argument_errors_need_no_gpu(lib):
+    """Argument errors come back synchronously, before any CUDA call."""
+    import workloads
+    s = workloads.WORKLOADS["phi15_layer"]
+    d = lib.LayerDesc(arch=lib.ARCH_PHI, B=s.B, T=s.T, D=s.D, H=s.H, Hkv=s.Hkv, dh=s.dh, F=s.F,
+                      rotary_dim=s.rotary_dim, rope_base=s.rope_base, norm=lib.NORM_LAYER, eps=s.eps,
+                      act=lib.ACT_GELU_TANH, qkv_bias=1, out_bias=1, mlp_bias=1)
+    fake = 1 << 20   # never dereferenced: validation fails first
+    params = lib.LayerParams(norm1_w=fake, norm1_b=fake, w_qkv=fake, b_qkv=fake, w_o=fake, b_o=None,
+                             w_up=fake, b_up=fake, w_down=fake, b_down=fake)
+    acts = lib.LayerActs(a=fake, mean1=fake, rstd1=fake, qkv=fake, o=fake, lse=fake, up=fake)
+    with pytest.raises(lib.ColliderError) as e:      # b_o missing although out_bias is set
+        lib.collider_layer_fwd(d, params, fake, fake, acts, None, stream=0)
+    assert e.value.status == lib.ERR_INVALID_ARG and "bias" in str(e.value)
+    params.b_o = fake + 8                           # misaligned
+    with pytest.raises(lib.ColliderError) as e:
+        lib.collider_layer_fwd(d, params, fake, fake, acts, None, stream=0)
+    assert e.value.status == lib.ERR_INVALID_ARG and "aligned" in str(e.value)
+    params.b_o = fake
+    with pytest.raises(lib.ColliderError) as e:      # no workspace
+        lib.collider_layer_fwd(d, params, fake, fake, acts, None, stream=0)
+    assert e.value.status == lib.ERR_INVALID_ARG and "workspace" in str(e.value)
+    d.act = lib.ACT_SWIGLU                          # phi blocks use GELU
+    with pytest.raises(lib.ColliderError) as e:
+        lib.collider_layer_fwd(d, params, fake, fake, acts, None, stream=0)
+    assert e.value.status == lib.ERR_UNSUPPORTED
 
 
 def test_binding_has_no_fallback(lib):
