@@ -20,7 +20,6 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import re
 import subprocess
@@ -96,75 +95,6 @@ def attn_flops(s, kept_per_seq):
 # ---------------------------------------------------------------------------
 # synthetic saved activations: a dense bf16 forward on the GPU (input
 # preparation only, outside every timed region)
-def gpu_forward(s, w, x):
-    """Dense forward of one block on the GPU with torch (input preparation, never
-    timed): the saved activations the backward reads, rounded to their storage
-    types.  Llama-style blocks (RMSNorm, GQA, RoPE, SwiGLU, optional QKV bias) and
-    Phi-style parallel blocks (LayerNorm, partial RoPE, GELU-tanh MLP, biases)."""
-    import torch
-    dev = x.device
-    M = s.M
-    f = lambda t: t.float()
-    mm = lambda a_, w_: (a_.bfloat16() @ w_.bfloat16()).float()   # bf16 tensor-core matmul
-    xf = f(x)
-    out = {}
-    if s.norm == "ln":
-        mean1 = xf.mean(-1)
-        rstd1 = torch.rsqrt((xf - mean1[:, None]).pow(2).mean(-1) + s.eps)
-        a = ((xf - mean1[:, None]) * rstd1[:, None] * f(w["norm1_w"]) + f(w["norm1_b"])).bfloat16()
-        out["mean1"] = mean1
-    else:
-        rstd1 = torch.rsqrt(xf.pow(2).mean(-1) + s.eps)
-        a = (xf * rstd1[:, None] * f(w["norm1_w"])).bfloat16()
-    qkv = mm(a, w["w_qkv"])
-    if "b_qkv" in w:
-        qkv = qkv + f(w["b_qkv"])
-    qkv = qkv.bfloat16()
-    nq, nk = s.H * s.dh, s.Hkv * s.dh
-    pos = torch.arange(s.T, device=dev).repeat(s.B).double()
-    half = s.rotary_dim // 2
-    inv = s.rope_base ** (-(2.0 * torch.arange(half, device=dev, dtype=torch.float64)) / s.rotary_dim)
-    ang = pos[:, None] * inv[None, :]
-    cos, sin = torch.cos(ang).float()[:, None, :], torch.sin(ang).float()[:, None, :]
-
-    def rope(t, nh):
-        t = f(t).view(M, nh, s.dh)
-        x1, x2, rest = t[..., :half], t[..., half:s.rotary_dim], t[..., s.rotary_dim:]
-        return torch.cat([x1 * cos - x2 * sin, x2 * cos + x1 * sin, rest], -1).bfloat16()
-
-    q = rope(qkv[:, :nq], s.H)
-    k = rope(qkv[:, nq:nq + nk], s.Hkv)
-    v = qkv[:, nq + nk:].reshape(M, s.Hkv, s.dh)
-    qkv_rot = torch.cat([q.reshape(M, -1), k.reshape(M, -1), v.reshape(M, -1)], 1).contiguous()
-    o = torch.empty(M, s.H, s.dh, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(s.B, s.H, s.T, dtype=torch.float32, device=dev)
-    causal = torch.ones(s.T, s.T, dtype=torch.bool, device=dev).tril()
-    G = s.H // s.Hkv
-    for b in range(s.B):
-        rows = slice(b * s.T, (b + 1) * s.T)
-        for h in range(s.H):
-            S = f(q[rows, h]) @ f(k[rows, h // G]).T / math.sqrt(s.dh)
-            S = S.masked_fill(~causal, float("-inf"))
-            l = torch.logsumexp(S, -1)
-            o[rows, h] = (torch.exp(S - l[:, None]) @ f(v[rows, h // G])).bfloat16()
-            lse[b, h] = l
-    o = o.reshape(M, -1)
-    if s.arch == "phi":
-        f1 = mm(a, w["w_up"])
-        if "b_up" in w:
-            f1 = f1 + f(w["b_up"])
-        out.update(x=x, a=a, rstd1=rstd1, qkv=qkv_rot, o=o, lse=lse, up=f1.bfloat16())
-        return out
-    h_ = (xf + mm(o, w["w_o"])).bfloat16()
-    rstd2 = torch.rsqrt(f(h_).pow(2).mean(-1) + s.eps)
-    bn = (f(h_) * rstd2[:, None] * f(w["norm2_w"])).bfloat16()
-    gu = mm(bn, w["w_up"]).bfloat16()
-    g_, u_ = f(gu[:, :s.F]), f(gu[:, s.F:])
-    sact = (g_ * torch.sigmoid(g_) * u_).bfloat16()
-    out.update(x=x, a=a, rstd1=rstd1, qkv=qkv_rot, o=o, lse=lse, h=h_, b=bn, rstd2=rstd2, up=gu, s=sact)
-    return out
-
-
 def layer_desc(cl, s):
     return cl.LayerDesc(arch=cl.ARCH_LLAMA if s.arch == "llama" else cl.ARCH_PHI, B=s.B, T=s.T, D=s.D, H=s.H,
                         Hkv=s.Hkv, dh=s.dh, F=s.F, rotary_dim=s.rotary_dim, rope_base=s.rope_base,
@@ -192,9 +122,40 @@ def grad_buffers(s, dev):
     return {k: torch.empty(v, dtype=torch.float32, device=dev) for k, v in shapes.items()}
 
 
+class NativeForward:
+    """The library's dense forward of one block (collider_layer_fwd): parameter
+    struct, the saved-set buffers it writes, y and its workspace."""
+
+    def __init__(self, cl, s, W, desc, dev):
+        import torch
+        self.cl, self.s, self.desc = cl, s, desc
+        g = lambda k: W[k].data_ptr() if k in W else None
+        self.params = cl.LayerParams(**{k: g(k) for k in ("norm1_w", "norm1_b", "w_qkv", "b_qkv", "w_o", "b_o",
+                                                          "norm2_w", "w_up", "b_up", "w_down", "b_down")})
+        bf = lambda *shp: torch.empty(shp, dtype=torch.bfloat16, device=dev)
+        f32 = lambda *shp: torch.empty(shp, dtype=torch.float32, device=dev)
+        t = dict(a=bf(s.M, s.D), rstd1=f32(s.M), qkv=bf(s.M, s.Nqkv), o=bf(s.M, s.H * s.dh),
+                 lse=f32(s.B, s.H, s.T), up=bf(s.M, s.Nup))
+        if s.arch == "llama":
+            t.update(h=bf(s.M, s.D), b=bf(s.M, s.D), rstd2=f32(s.M), s=bf(s.M, s.F))
+        else:
+            t["mean1"] = f32(s.M)
+        self.t = t
+        self.acts = cl.LayerActs(**{k: v.data_ptr() for k, v in t.items()})
+        self.y = bf(s.M, s.D)
+        self.ws = torch.empty(cl.collider_layer_fwd_workspace_size(desc), dtype=torch.uint8, device=dev)
+
+    def run(self, x, stream=None):
+        self.cl.collider_layer_fwd(self.desc, self.params, x, self.y, self.acts, self.ws, stream)
+
+    def saved(self, x) -> dict:
+        return dict(x=x, **self.t)
+
+
 class Block:
-    """One block's synthetic inputs, saved activations, gradient buffers and
-    workspace on the GPU; step() runs compaction + the layer backward."""
+    """One block's synthetic inputs, saved activations (written by the library's
+    own dense forward), gradient buffers and workspace on the GPU; step() runs
+    compaction + the layer backward."""
 
     def __init__(self, cl, s, dev):
         import torch
@@ -208,9 +169,10 @@ class Block:
         self.dout = torch.from_numpy(tn["dout"]).to(dev).bfloat16()
         self.masks = {"filtered": torch.from_numpy(tn["keep"]).to(dev),
                       "unfiltered": torch.ones(s.B, s.T, dtype=torch.uint8, device=dev)}
-        with torch.no_grad():
-            self.saved = gpu_forward(s, self.W, x)
         self.desc = layer_desc(cl, s)
+        self.fwd = NativeForward(cl, s, self.W, self.desc, dev)
+        self.fwd.run(x)
+        self.saved = self.fwd.saved(x)
         self.weights = cl.LayerWeights(**{k: self.W[k].data_ptr() for k in
                                           ("norm1_w", "w_qkv", "w_o", "norm2_w", "w_up", "w_down") if k in self.W})
         self.sv = cl.LayerSaved(**{k: v.data_ptr() for k, v in self.saved.items()})
@@ -222,31 +184,6 @@ class Block:
         self.cu = torch.empty(s.B + 1, dtype=torch.int32, device=dev)
         self.nk = torch.empty(1, dtype=torch.int32, device=dev)
 
-    def native_forward(self):
-        """Buffers for the library's own dense forward (collider_layer_fwd) of this
-        block; returns a function that runs it on a stream."""
-        import torch
-        cl, s, dev = self.cl, self.s, self.x.device
-        g = lambda k: self.W[k].data_ptr() if k in self.W else None
-        self.fw_params = cl.LayerParams(**{k: g(k) for k in ("norm1_w", "norm1_b", "w_qkv", "b_qkv", "w_o", "b_o",
-                                                             "norm2_w", "w_up", "b_up", "w_down", "b_down")})
-        bf = lambda *shp: torch.empty(shp, dtype=torch.bfloat16, device=dev)
-        f32 = lambda *shp: torch.empty(shp, dtype=torch.float32, device=dev)
-        t = dict(a=bf(s.M, s.D), rstd1=f32(s.M), qkv=bf(s.M, s.Nqkv), o=bf(s.M, s.H * s.dh),
-                 lse=f32(s.B, s.H, s.T), up=bf(s.M, s.Nup))
-        if s.arch == "llama":
-            t.update(h=bf(s.M, s.D), b=bf(s.M, s.D), rstd2=f32(s.M), s=bf(s.M, s.F))
-        else:
-            t["mean1"] = f32(s.M)
-        self.fw_t = t
-        self.fw_acts = cl.LayerActs(**{k: v.data_ptr() for k, v in t.items()})
-        self.fw_y = bf(s.M, s.D)
-        self.fw_ws = torch.empty(cl.collider_layer_fwd_workspace_size(self.desc), dtype=torch.uint8, device=dev)
-
-        def run(stream):
-            cl.collider_layer_fwd(self.desc, self.fw_params, self.x, self.fw_y, self.fw_acts, self.fw_ws, stream)
-        return run
-
     def step(self, mask, stream, sv=None, dout=None):
         cl, s = self.cl, self.s
         cl.collider_compact(mask, s.B, s.T, self.idx, self.cu, self.nk, None, stream)
@@ -256,9 +193,9 @@ class Block:
 
 
 class Stack:
-    """The 22-block stack: inputs and saved activations of every block (torch
-    forward on the GPU), LM head and embedding; step() runs compaction +
-    collider_stack_bwd."""
+    """The 22-block stack: inputs and saved activations of every block (the
+    library's dense forward, block by block), LM head and embedding; step() runs
+    compaction + collider_stack_bwd."""
 
     def __init__(self, cl, st, dev):
         import torch
@@ -272,13 +209,16 @@ class Stack:
         ids = torch.from_numpy(t["ids"].astype(np.int64)).to(dev)
         x = E[ids]
         self.saved, self.Ws = [], []
+        self.desc = layer_desc(cl, ls)
         with torch.no_grad():
             for w in t["layers"]:
                 W = {k: torch.from_numpy(v).to(dev).bfloat16() for k, v in w.items()}
-                sv = gpu_forward(ls, W, x)
-                self.saved.append(sv)
+                fw = NativeForward(cl, ls, W, self.desc, dev)
+                fw.run(x)
+                self.saved.append(fw.saved(x))
                 self.Ws.append(W)
-                x = (sv["h"].float() + (sv["s"] @ W["w_down"]).float()).bfloat16()
+                x = fw.y
+                fw.ws = None   # the workspace is not kept per block
             xf = x.float()
             self.rstdf = torch.rsqrt(xf.pow(2).mean(-1) + ls.eps)
             self.nf = torch.from_numpy(t["normf_w"]).to(dev).bfloat16()
@@ -286,7 +226,6 @@ class Stack:
             self.wlm = torch.from_numpy(t["w_lm"]).to(dev).bfloat16()
             self.z = (self.y @ self.wlm).bfloat16()
         self.xL = x
-        self.desc = layer_desc(cl, ls)
         L = st.L
         self.Wc = (cl.LayerWeights * L)(*[cl.LayerWeights(**{k: W[k].data_ptr() for k in
                                                               ("norm1_w", "w_qkv", "w_o", "norm2_w", "w_up", "w_down")})
@@ -446,7 +385,7 @@ def run_ours(args):
     s = workloads.WORKLOADS[WORKLOAD]
     M = s.M
 
-    # ---- inputs (seeded, synthetic), saved activations by a torch forward ----
+    # ---- inputs (seeded, synthetic), saved activations by the library's forward ----
     blk = Block(cl, s, dev)
     tn = {"keep": blk.keep_np}
     W, saved, dout, masks, G, dx = blk.W, blk.saved, blk.dout, blk.masks, blk.G, blk.dx
@@ -598,7 +537,7 @@ def run_ours(args):
     # ---- the library's own dense forward of the same block ----------------
     # (collider_layer_fwd: the producer of the saved set; not part of the
     # filtered backward's step, reported beside it)
-    fwd_run = blk.native_forward()
+    fwd_run = lambda st_: blk.fwd.run(blk.x, st_)
     ms_fwd, fwd_launches = timed(masks["filtered"], args.steps, args.warmup, lambda m: fwd_run(stream))
     ms_fwd = max_over_ranks([ms_fwd], dev)[0]
     cl.collider_profile_enable(1)

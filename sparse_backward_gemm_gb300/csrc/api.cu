@@ -951,7 +951,7 @@ void fwd_carve(Carver& cv, const collider_layer_desc* d, FwdBufs* f) {
   const bool llama = d->arch == COLLIDER_ARCH_LLAMA;
   f->qkv_acc = cv.take<float>(M * Nqkv);
   f->attn_acc = cv.take<float>(M * D);
-  f->up_acc = cv.take<float>(M * (llama ? 2 * F : F));
+  f->up_acc = llama ? nullptr : cv.take<float>(M * F);   // LLAMA's GEMM writes the saved bf16 up itself
   f->mlp_acc = cv.take<float>(M * D);
   f->act = llama ? nullptr : cv.take<__nv_bfloat16>(M * F);
   f->lse2 = cv.take<float>(M * d->H);
@@ -959,13 +959,14 @@ void fwd_carve(Carver& cv, const collider_layer_desc* d, FwdBufs* f) {
   f->cu = cv.take<int32_t>((size_t)d->B + 1);
 }
 
-// C [M, N] f32 = A [M, K] . W with W stored [K, N] (the MN-major B operand)
-cudaError_t gemm_fwd(const Ctx& c, int M, int K, int N, const void* A, const void* W, float* C) {
+// C [M, N] = A [M, K] . W with W stored [K, N] (the MN-major B operand); C is
+// f32, or bf16 (rounded once, in the epilogue) when c_bf16
+cudaError_t gemm_fwd(const Ctx& c, int M, int K, int N, const void* A, const void* W, void* C, int c_bf16 = 0) {
   TcGemm g{};
   g.M = M; g.N = N; g.K = K;
   g.A = A; g.lda = K; g.a_mn_major = 0; g.a_rows = M;
   g.B = W; g.ldb = N; g.b_mn_major = 1; g.b_rows = K;
-  g.C = C; g.ldc = N; g.c_bf16 = 0; g.c_rows = M;
+  g.C = C; g.ldc = N; g.c_bf16 = c_bf16; g.c_rows = M;
   return launch_tc_gemm(c, g);
 }
 
@@ -992,11 +993,12 @@ collider_status layer_fwd_impl(const Ctx& c, const collider_layer_desc* d, const
   n1.gamma = B16(w->norm1_w); n1.beta = llama ? nullptr : B16(w->norm1_b);
   n1.out = a; n1.mean = llama ? nullptr : ac->mean1; n1.rstd = ac->rstd1;
   CK(launch_norm_fwd(c, n1));
-  // 2. QKV projection, bias and RoPE
-  CK(gemm_fwd(c, M, D, Nqkv, a, w->w_qkv, F.qkv_acc));
+  // 2. QKV projection, bias and RoPE (without a bias the GEMM rounds to bf16 itself)
+  const int qkv16 = b_qkv ? 0 : 1;
+  CK(gemm_fwd(c, M, D, Nqkv, a, w->w_qkv, F.qkv_acc, qkv16));
   const int rot_half = d->rotary_dim / 2;
   CK(launch_rope_table(c, d->T, rot_half, d->rope_base, F.rope));
-  CK(launch_qkv_rope_fwd(c, M, Nqkv, H + Hkv, dh, rot_half, d->T, F.qkv_acc, b_qkv, F.rope, qkv));
+  CK(launch_qkv_rope_fwd(c, M, Nqkv, H + Hkv, dh, rot_half, d->T, F.qkv_acc, qkv16, b_qkv, F.rope, qkv));
   // 3. causal attention over every sequence
   CK(launch_iota_cu(c, d->B, d->T, F.cu));
   {
@@ -1015,8 +1017,8 @@ collider_status layer_fwd_impl(const Ctx& c, const collider_layer_desc* d, const
     n2.add = F.attn_acc; n2.add_ld = D; n2.add_bias = b_o; n2.sum_out = static_cast<bf*>(ac->h);
     n2.gamma = B16(w->norm2_w); n2.out = static_cast<bf*>(ac->b); n2.rstd = ac->rstd2;
     CK(launch_norm_fwd(c, n2));                                                    // h = x + attn, b = norm2(h)
-    CK(gemm_fwd(c, M, D, 2 * Ff, ac->b, w->w_up, F.up_acc));                        // [g | u] = b W_up
-    CK(launch_act_fwd(c, 0, M, Ff, F.up_acc, nullptr, static_cast<bf*>(ac->up), static_cast<bf*>(ac->s)));
+    CK(gemm_fwd(c, M, D, 2 * Ff, ac->b, w->w_up, ac->up, 1));                       // [g | u] = b W_up (bf16)
+    CK(launch_swiglu_fwd(c, M, Ff, static_cast<const bf*>(ac->up), static_cast<bf*>(ac->s)));
     CK(gemm_fwd(c, M, Ff, D, ac->s, w->w_down, F.mlp_acc));                         // s W_down
     CK(launch_residual_out(c, M, D, static_cast<const bf*>(ac->h), F.mlp_acc, nullptr, nullptr, nullptr, y));
   } else {

@@ -1222,25 +1222,42 @@ __device__ __forceinline__ void dprep_body(const CUtensorMap& tmQ, const CUtenso
       // a full key block strictly before the query block needs no masking
       const bool interior = (!p.causal || j0 + kK <= i0) && qrows == kQ && len - j0 >= kK;
       if (MODE == 2) {
-        // keys j0 + half * 64 + e of this row, e < 64
-        float xv[64];
-        float bm = -INFINITY;
+        // keys j0 + half * 64 + e of this row, e < 64.  The block maximum is
+        // taken on the raw scores (scaling by c > 0 is monotone, so max(S) c
+        // = max(S c) exactly) and each exponent is one fma; eight independent
+        // partial maxima and sums keep the dependency chains short.
+        float sv[64], bm8[8], a8[8];
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          const int kj = j0 + half * 64 + e;
-          const bool valid = interior || (r < qrows && kj < len && (!p.causal || kj <= i0 + r));
-          xv[e] = valid ? __uint_as_float(sr[e]) * p.scale_log2 : -INFINITY;
-          bm = fmaxf(bm, xv[e]);
+        for (int q8 = 0; q8 < 8; ++q8) {
+          bm8[q8] = -INFINITY;
+          a8[q8] = 0.f;
         }
+        if (interior) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            sv[e] = __uint_as_float(sr[e]);
+            bm8[e & 7] = fmaxf(bm8[e & 7], sv[e]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            const int kj = j0 + half * 64 + e;
+            const bool valid = r < qrows && kj < len && (!p.causal || kj <= i0 + r);
+            sv[e] = valid ? __uint_as_float(sr[e]) : -INFINITY;
+            bm8[e & 7] = fmaxf(bm8[e & 7], sv[e]);
+          }
+        }
+        const float bm = fmaxf(fmaxf(fmaxf(bm8[0], bm8[1]), fmaxf(bm8[2], bm8[3])),
+                               fmaxf(fmaxf(bm8[4], bm8[5]), fmaxf(bm8[6], bm8[7]))) * p.scale_log2;
         float m = mrun[0], l = lrun[0];
 #pragma unroll
         for (int x = 1; x < HPC; ++x)
           if (hh == x) { m = mrun[x]; l = lrun[x]; }
         const float mn = fmaxf(m, bm);
         if (mn != -INFINITY) {
-          float acc = 0.f;
 #pragma unroll
-          for (int e = 0; e < 64; ++e) acc += exp2_approx(xv[e] - mn);
+          for (int e = 0; e < 64; ++e) a8[e & 7] += exp2_approx(fmaf(sv[e], p.scale_log2, -mn));
+          const float acc = ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
           l = l * exp2_approx(m - mn) + acc;
           m = mn;
         }

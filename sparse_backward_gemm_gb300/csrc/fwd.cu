@@ -90,23 +90,46 @@ __global__ void __launch_bounds__(kNormThreads) norm_fwd_kernel(NormFwdArgs a) {
 // for the rotated heads and d < r (r = 2 * rot_half) it pairs with d +- r/2:
 //   d <  r/2:  x_d c - x_{d+r/2} s        d >= r/2:  x_d c + x_{d-r/2} s
 // with (c, s) of angle pos * base^(-2i/r), i = d mod r/2.
-__global__ void qkv_rope_kernel(int N, int rot_heads, int dh, int rot_half, int T, const float* acc,
+// The projection arrives as f32 (plus bias, rounded here) or already as bf16.
+template <bool IN_BF16>
+__global__ void qkv_rope_kernel(int N, int rot_heads, int dh, int rot_half, int T, const void* acc,
                                 const __nv_bfloat16* bias, const float2* rope, __nv_bfloat16* qkv) {
   const int row = blockIdx.x;
   const int pos = row % T;
-  const float* in = acc + (long long)row * N;
+  const float* in = static_cast<const float*>(acc) + (long long)row * N;
+  const __nv_bfloat16* in16 = static_cast<const __nv_bfloat16*>(acc) + (long long)row * N;
+  auto value = [&](int j) {
+    return IN_BF16 ? __bfloat162float(in16[j]) : bf16_round(in[j] + (bias ? __bfloat162float(bias[j]) : 0.f));
+  };
   __nv_bfloat16* out = qkv + (long long)row * N;
   for (int j = threadIdx.x; j < N; j += blockDim.x) {
-    float x = bf16_round(in[j] + (bias ? __bfloat162float(bias[j]) : 0.f));
+    float x = value(j);
     const int head = j / dh, d = j % dh;
     if (head < rot_heads && d < 2 * rot_half) {
       const bool lo = d < rot_half;
       const int jp = lo ? j + rot_half : j - rot_half;
-      const float y = bf16_round(in[jp] + (bias ? __bfloat162float(bias[jp]) : 0.f));
+      const float y = value(jp);
       const float2 cs = rope[(long long)pos * rot_half + (lo ? d : d - rot_half)];
       x = lo ? x * cs.x - y * cs.y : x * cs.x + y * cs.y;
     }
     out[j] = __float2bfloat16_rn(x);
+  }
+}
+
+// SwiGLU from the saved bf16 [g | u] (the GEMM wrote it rounded): s = bf16(silu(g) u).
+__global__ void swiglu_fwd_kernel(int M, int F, const __nv_bfloat16* up, __nv_bfloat16* act) {
+  const int nch = F / 8;
+  const long long total = (long long)M * nch;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    const int row = (int)(e / nch), c = 8 * (int)(e % nch);
+    const __nv_bfloat16* in = up + (long long)row * 2 * F;
+    float g[8], u[8], o[8];
+    unpack8(*reinterpret_cast<const uint4*>(in + c), g);
+    unpack8(*reinterpret_cast<const uint4*>(in + F + c), u);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = g[i] / (1.f + expf(-g[i])) * u[i];
+    *reinterpret_cast<uint4*>(act + (long long)row * F + c) = pack8(o);
   }
 }
 
@@ -199,12 +222,15 @@ cudaError_t launch_norm_fwd(const Ctx& c, const NormFwdArgs& a) {
 }
 
 cudaError_t launch_qkv_rope_fwd(const Ctx& c, int M, int N, int rot_heads, int dh, int rot_half, int T,
-                                const float* acc, const __nv_bfloat16* bias, const float2* rope,
+                                const void* acc, int acc_bf16, const __nv_bfloat16* bias, const float2* rope,
                                 __nv_bfloat16* qkv) {
   if (M <= 0) return cudaSuccess;
-  if (rot_half > 0 && !rope) return cudaErrorInvalidValue;
+  if ((rot_half > 0 && !rope) || (acc_bf16 && bias)) return cudaErrorInvalidValue;
   prof_begin(c, "qkv_rope_fwd");
-  qkv_rope_kernel<<<M, 256, 0, c.stream>>>(N, rot_heads, dh, rot_half, T, acc, bias, rope, qkv);
+  if (acc_bf16)
+    qkv_rope_kernel<true><<<M, 256, 0, c.stream>>>(N, rot_heads, dh, rot_half, T, acc, nullptr, rope, qkv);
+  else
+    qkv_rope_kernel<false><<<M, 256, 0, c.stream>>>(N, rot_heads, dh, rot_half, T, acc, bias, rope, qkv);
   prof_end(c);
   count_launch();
   return cudaGetLastError();
@@ -216,6 +242,16 @@ cudaError_t launch_act_fwd(const Ctx& c, int gelu, int M, int F, const float* ac
   if (M <= 0) return cudaSuccess;
   prof_begin(c, "act_fwd");
   act_fwd_kernel<<<grid_for(c, (long long)M * (F / 8)), 256, 0, c.stream>>>(gelu, M, F, acc, bias, up, act);
+  prof_end(c);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_fwd(const Ctx& c, int M, int F, const __nv_bfloat16* up, __nv_bfloat16* act) {
+  if (F % 8) return cudaErrorInvalidValue;
+  if (M <= 0) return cudaSuccess;
+  prof_begin(c, "act_fwd");
+  swiglu_fwd_kernel<<<grid_for(c, (long long)M * (F / 8)), 256, 0, c.stream>>>(M, F, up, act);
   prof_end(c);
   count_launch();
   return cudaGetLastError();

@@ -229,14 +229,17 @@ struct NormFwdArgs {
 };
 cudaError_t launch_norm_fwd(const Ctx& c, const NormFwdArgs& a);
 // qkv = bf16(acc + bias), then the first rot_heads heads (q then k) rotated on
-// their first 2*rot_half dims at position row % T; [M, N] f32 -> bf16.
+// their first 2*rot_half dims at position row % T; [M, N] f32 (acc_bf16 = 0)
+// or bf16 already rounded (acc_bf16 = 1, no bias) -> bf16.
 cudaError_t launch_qkv_rope_fwd(const Ctx& c, int M, int N, int rot_heads, int dh, int rot_half, int T,
-                                const float* acc, const __nv_bfloat16* bias, const float2* rope,
+                                const void* acc, int acc_bf16, const __nv_bfloat16* bias, const float2* rope,
                                 __nv_bfloat16* qkv);
 // gelu == 0: up = bf16(acc + bias) [M, 2F] = [g | u], act = bf16(silu(g) u) [M, F]
 // gelu == 1: up = bf16(acc + bias) [M, F],            act = bf16(gelu_tanh(up)) [M, F]
 cudaError_t launch_act_fwd(const Ctx& c, int gelu, int M, int F, const float* acc, const __nv_bfloat16* bias,
                            __nv_bfloat16* up, __nv_bfloat16* act);
+// act = bf16(silu(g) u) from the bf16 up [M, 2F] = [g | u]
+cudaError_t launch_swiglu_fwd(const Ctx& c, int M, int F, const __nv_bfloat16* up, __nv_bfloat16* act);
 // y = bf16(res + acc1 (+ bias1) (+ acc2 (+ bias2))), all [M, D]
 cudaError_t launch_residual_out(const Ctx& c, int M, int D, const __nv_bfloat16* res, const float* acc1,
                                 const __nv_bfloat16* bias1, const float* acc2, const __nv_bfloat16* bias2,

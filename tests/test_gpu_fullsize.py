@@ -59,7 +59,7 @@ def test_full_size_phi_ratio_sweep(f):
 
 def _gpu_stack_forward(st, t):
     """Dense bf16 stack forward with torch on the GPU (input preparation)."""
-    import bench
+    from torch_forward import gpu_forward
     ls = st.layer
     dev = torch.device(gu.DEV)
     E = torch.from_numpy(t["E"]).to(dev).bfloat16()
@@ -68,7 +68,7 @@ def _gpu_stack_forward(st, t):
     blocks, Ws = [], []
     for w in t["layers"]:
         W = {k: torch.from_numpy(v).to(dev).bfloat16() for k, v in w.items()}
-        sv = bench.gpu_forward(ls, W, x)
+        sv = gpu_forward(ls, W, x)
         blocks.append(sv)
         Ws.append(W)
         xf = sv["h"].float() + sv["s"].float() @ W["w_down"].float()
