@@ -93,8 +93,8 @@ def attn_flops(s, kept_per_seq):
 
 
 # ---------------------------------------------------------------------------
-# synthetic saved activations: a dense bf16 forward on the GPU (input
-# preparation only, outside every timed region)
+# synthetic saved activations: the library's own dense forward on the GPU
+# (input preparation, outside the backward's timed region)
 def layer_desc(cl, s):
     return cl.LayerDesc(arch=cl.ARCH_LLAMA if s.arch == "llama" else cl.ARCH_PHI, B=s.B, T=s.T, D=s.D, H=s.H,
                         Hkv=s.Hkv, dh=s.dh, F=s.F, rotary_dim=s.rotary_dim, rope_base=s.rope_base,
