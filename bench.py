@@ -12,8 +12,10 @@ Prints one JSON line (rank 0).  The headline numbers are the TinyLlama-shaped
 block's; "configs" adds the same filtered / unfiltered timing for the
 Qwen2.5-shaped block, the Phi-1.5-shaped block at 0/20/40/60% filtered (span
 masks) and the 22-block TinyLlama-shaped stack with its LM head
-(`--headline-only` skips them).  `--impl reference` times the fp64 CPU oracle
-on the host cores instead, on a bounded sample of the same workload.
+(`--headline-only` skips them); "forward" times the library's dense forward of
+the headline block (collider_layer_fwd, which also writes every saved set the
+bench uses).  `--impl reference` times the fp64 CPU oracle on the host cores
+instead, on a bounded sample of the same workload.
 """
 from __future__ import annotations
 
