@@ -371,8 +371,12 @@ typedef struct {
  * is rounded to its storage type once, and the projection sums (with their
  * bias) are rounded to bf16 before RoPE, the activation and the second norm.
  * lse is the natural-log log-sum-exp of the scaled logits, [B, H, T].
- * Pointers 16-byte aligned; workspace (256-byte aligned) of
- * collider_layer_fwd_workspace_size bytes.  Asynchronous on the stream. */
+ * x stays part of the saved set, so y must not alias x; the acts buffers are
+ * distinct from each other and from x and y.  Pointers 16-byte aligned;
+ * workspace (256-byte aligned) of collider_layer_fwd_workspace_size bytes.
+ * Deterministic (no atomics).  Asynchronous on the stream; errors as for
+ * collider_layer_bwd (arguments synchronously, kernel-side failures through
+ * collider_check). */
 size_t collider_layer_fwd_workspace_size(const collider_layer_desc* desc);
 collider_status collider_layer_fwd(const collider_layer_desc* desc, const collider_layer_params* w,
                                    const void* x, void* y, const collider_layer_acts* acts,

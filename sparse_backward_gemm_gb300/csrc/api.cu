@@ -1033,6 +1033,7 @@ collider_status layer_fwd_impl(const Ctx& c, const collider_layer_desc* d, const
 collider_status check_fwd_ptrs(const collider_layer_desc* d, const collider_layer_params* w, const void* x,
                                const void* y, const collider_layer_acts* ac) {
   if (!w || !ac || !x || !y) return fail(COLLIDER_ERR_INVALID_ARG, "null params/acts/x/y");
+  if (x == y) return fail(COLLIDER_ERR_INVALID_ARG, "y must not alias x (x is part of the saved set)");
   const bool llama = d->arch == COLLIDER_ARCH_LLAMA;
   const void* req[] = {w->norm1_w, w->w_qkv, w->w_o, w->w_up, w->w_down, ac->a, ac->rstd1, ac->qkv, ac->o,
                        ac->lse, ac->up};

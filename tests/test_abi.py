@@ -71,19 +71,22 @@ def test_forward_argument_errors_need_no_gpu(lib):
                              w_up=fake, b_up=fake, w_down=fake, b_down=fake)
     acts = lib.LayerActs(a=fake, mean1=fake, rstd1=fake, qkv=fake, o=fake, lse=fake, up=fake)
     with pytest.raises(lib.ColliderError) as e:      # b_o missing although out_bias is set
-        lib.collider_layer_fwd(d, params, fake, fake, acts, None, stream=0)
+        lib.collider_layer_fwd(d, params, fake, fake + 4096, acts, None, stream=0)
     assert e.value.status == lib.ERR_INVALID_ARG and "bias" in str(e.value)
     params.b_o = fake + 8                           # misaligned
     with pytest.raises(lib.ColliderError) as e:
-        lib.collider_layer_fwd(d, params, fake, fake, acts, None, stream=0)
+        lib.collider_layer_fwd(d, params, fake, fake + 4096, acts, None, stream=0)
     assert e.value.status == lib.ERR_INVALID_ARG and "aligned" in str(e.value)
     params.b_o = fake
     with pytest.raises(lib.ColliderError) as e:      # no workspace
-        lib.collider_layer_fwd(d, params, fake, fake, acts, None, stream=0)
+        lib.collider_layer_fwd(d, params, fake, fake + 4096, acts, None, stream=0)
     assert e.value.status == lib.ERR_INVALID_ARG and "workspace" in str(e.value)
+    with pytest.raises(lib.ColliderError) as e:      # y aliasing x
+        lib.collider_layer_fwd(d, params, fake, fake, acts, None, stream=0)
+    assert e.value.status == lib.ERR_INVALID_ARG and "alias" in str(e.value)
     d.act = lib.ACT_SWIGLU                          # phi blocks use GELU
     with pytest.raises(lib.ColliderError) as e:
-        lib.collider_layer_fwd(d, params, fake, fake, acts, None, stream=0)
+        lib.collider_layer_fwd(d, params, fake, fake + 4096, acts, None, stream=0)
     assert e.value.status == lib.ERR_UNSUPPORTED
 
 
