@@ -26,6 +26,7 @@ import os
 import re
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -265,7 +266,9 @@ class Clocks:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.p = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        # raw samples (the JSON line carries their summary); COLLIDER_CLOCKS_DIR keeps them
+        self.path = os.path.join(os.environ.get("COLLIDER_CLOCKS_DIR", tempfile.gettempdir()),
+                                 f"collider_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
