@@ -15,6 +15,9 @@ those rows cannot leak), and inside attention the recomputed probabilities
 are zeroed at filtered query rows and key columns (P') before they are used
 for G_V, dP's correction term D and G_Q, G_K.  It never compacts: the
 dimension-reduced dense GEMM of the CUDA path must reach the same numbers.
+The block's dense forward (Fig. 2b: the forward is not filtered), with each
+saved tensor rounded to its storage type, is also the reference for the
+library's own forward.
 
 Modules:
   compaction  keep-mask -> ascending kept index list, per-sequence offsets
