@@ -15,6 +15,10 @@
 // group's query heads; head dim 64 and 128 have their own kernels), and a
 // finalize pass (scale, RoPE backward, bf16, zero padding rows).  dQ, dK and
 // dV are summed in f32 by TMA bulk reduce-adds.
+//
+// The dense forward's attention (every token kept) reuses the D pre-pass
+// pipeline in two passes: the log-sum-exp of each query row, then
+// O = exp(S - lse) V.
 #include "internal.h"
 #include "tc_ptx.cuh"
 
