@@ -1,0 +1,25 @@
+"""Host logic of bench.py that needs no GPU: the GEMM traffic figure is taken
+from the committed ncu summary only while the profiled GEMM source is
+unchanged."""
+import hashlib
+import os
+
+import bench
+
+
+def test_gemm_traffic_tracks_the_profiled_source(tmp_path, monkeypatch):
+    text = open(bench.GEMM_PROFILE).read()
+    want = text.split("gemm_tc.cu sha256: ")[1].split()[0]
+    have = hashlib.sha256(open(bench.GEMM_SOURCE, "rb").read()).hexdigest()
+    # the committed summary was captured on the committed source
+    assert have.startswith(want)
+    n = bench.gemm_traffic()
+    assert isinstance(n, int) and 500e6 < n < 1.5e9
+    # any edit of the kernel source invalidates the figure
+    edited = tmp_path / "gemm_tc.cu"
+    edited.write_bytes(open(bench.GEMM_SOURCE, "rb").read() + b"\n// edited\n")
+    monkeypatch.setattr(bench, "GEMM_SOURCE", str(edited))
+    assert bench.gemm_traffic() is None
+    monkeypatch.setattr(bench, "GEMM_SOURCE", os.path.join(str(tmp_path), "missing.cu"))
+    assert bench.gemm_traffic() is None
+
