@@ -1,23 +1,32 @@
 """Models of the mbarrier protocols of the tcgen05 attention kernels
 (sparse_backward_gemm_gb300/csrc/attn.cu), checked on the CPU.
 
-Each role of a kernel (TMA producer, MMA issuer, softmax groups, epilogue) is
-written as its sequence of waits and arrivals; an event is (barrier, phase).
-Two properties are checked for every sequence length:
+Each role of a kernel (TMA producer, MMA issuer, softmax warps, epilogue
+warps) is written as its sequence of operations on (barrier, phase) events:
+  sig     a single-arrival completion (a TMA transaction, a tcgen05.commit,
+          a one-thread arrive)
+  arrive  one of several arrivals a phase needs (warps of a group); the
+          phase completes when every listed arriver has arrived
+  wait    block until the phase has completed
+Three properties are checked for every sequence length:
   * no deadlock: run to quiescence, every role finishes;
-  * no missed phase: every wait is a parity wait, so a wait for phase k of a
-    barrier must never find phase k+1 already complete (the parity would read
-    as "not yet" and the wait would run out).  With the waiting role frozen
-    just before that wait and every other role run as far as it can, phase
-    k+1 of that barrier must not complete.
-The models restate the kernels' orders by hand; a change of a kernel's
-protocol must be mirrored here.
+  * no missed phase: every mbarrier wait is a parity wait, so a wait for
+    phase k must never find phase k+1 already complete (the parity would
+    read as "not yet" and the wait would run out);
+  * no overrun: an arriver must never arrive for phase k+1 of a barrier
+    while another arriver's arrival for phase k is still pending (the early
+    arrival would be counted toward phase k and complete it too soon).
+Both hazards are checked by freezing one role just before the operation in
+question while every other role runs as far as it can.  Warps are modelled
+one by one where a barrier counts several of them; a named barrier (bar.sync)
+is an arrive followed by a wait.  The models restate the kernels' orders by
+hand; a change of a kernel's protocol must be mirrored here.
 """
 import pytest
 
 
-def _fixpoint(roles, frozen=None, frozen_pos=None):
-    sig = set()
+def _run(roles, arrivers, frozen=None, frozen_pos=None):
+    done, arrived = set(), set()
     pcs = {r: 0 for r in roles}
     changed = True
     while changed:
@@ -27,27 +36,36 @@ def _fixpoint(roles, frozen=None, frozen_pos=None):
             while pcs[r] < lim:
                 kind, ev = ops[pcs[r]]
                 if kind == "sig":
-                    sig.add(ev)
-                elif ev not in sig:
+                    done.add(ev)
+                elif kind == "arrive":
+                    bar, k = ev
+                    arrived.add((bar, k, r))
+                    if all((bar, k, a) in arrived for a in arrivers[bar]):
+                        done.add(ev)
+                elif ev not in done:
                     break
                 pcs[r] += 1
                 changed = True
-    return sig, pcs
+    return done, arrived, pcs
 
 
-def check(roles):
-    """Returns (roles that cannot finish, waits that can miss a phase)."""
-    _, pcs = _fixpoint(roles)
+def check(model):
+    """Returns (roles that cannot finish, waits that can miss a phase, arrivals that can overrun)."""
+    roles, arrivers = model
+    _, _, pcs = _run(roles, arrivers)
     dead = [r for r in roles if pcs[r] < len(roles[r])]
-    missed = []
+    missed, overrun = [], []
     for r, ops in roles.items():
-        for pos, (kind, ev) in enumerate(ops):
-            if kind == "wait":
-                bar, k = ev
-                sig, _ = _fixpoint(roles, r, pos)
-                if (bar, k + 1) in sig:
-                    missed.append((r, pos, ev))
-    return dead, missed
+        for pos, (kind, (bar, k)) in enumerate(ops):
+            if kind == "wait" and not (isinstance(bar, tuple) and bar[0] == "nb"):
+                done, _, _ = _run(roles, arrivers, r, pos)
+                if (bar, k + 1) in done:
+                    missed.append((r, pos, (bar, k)))
+            if kind == "arrive":
+                _, arrived, _ = _run(roles, arrivers, r, pos)
+                if any((bar, k + 1, a) in arrived for a in arrivers[bar] if a != r):
+                    overrun.append((r, pos, (bar, k)))
+    return dead, missed, overrun
 
 
 def ring(name, i, n):
@@ -55,13 +73,14 @@ def ring(name, i, n):
     return ((name, i % n), i // n)
 
 
-def dprep(nj, n_stages, heads, split_pfull=True):
+def dprep(nj, n_stages, heads, split_pfull=True, warps=2):
     """D pre-pass (and the forward's two passes, which run the same protocol):
     nj key blocks, K/V ring of n_stages, `heads` query heads per CTA, S and P
-    double-buffered."""
+    double-buffered; the softmax warps arrive on P-full without a named
+    barrier between iterations."""
     n_it = nj * heads
     pfull = (lambda t: ring("pfull", t, 2)) if split_pfull else (lambda t: ("pfull", t))
-    prod, mma, soft = [], [], []
+    prod, mma = [], []
 
     def issue(j):
         if j >= n_stages:
@@ -94,14 +113,20 @@ def dprep(nj, n_stages, heads, split_pfull=True):
     if n_it:
         pv(n_it - 1)
         mma.append(("sig", ("ofull", 0)))
-    for it in range(n_it):
-        soft.append(("wait", ring("sfull", it, 2)))
-        if it >= 2:
-            soft.append(("wait", ring("pempty", it - 2, 2)))
-        soft.append(("sig", pfull(it)))
-    if n_it:
-        soft.append(("wait", ("ofull", 0)))
-    return {"producer": prod, "mma": mma, "softmax": soft}
+    roles = {"producer": prod, "mma": mma}
+    soft_names = [f"softmax{w}" for w in range(warps)]
+    for name in soft_names:
+        soft = []
+        for it in range(n_it):
+            soft.append(("wait", ring("sfull", it, 2)))
+            if it >= 2:
+                soft.append(("wait", ring("pempty", it - 2, 2)))
+            soft.append(("arrive", pfull(it)))
+        if n_it:
+            soft.append(("wait", ("ofull", 0)))
+        roles[name] = soft
+    bars = [("pfull", 0), ("pfull", 1)] if split_pfull else ["pfull"]
+    return roles, {b: soft_names for b in bars}
 
 
 def _q_producer(n):
@@ -123,8 +148,23 @@ def _q_producer(n):
     return prod
 
 
-def main64(n):
-    """Main pass, head dim 64: two query halves with their own S/dP and P/dS buffers."""
+def _epilogue(n, roles, arrivers, warps=2):
+    """dQ drain: wait dQ-full, arrive dQ-empty, two named barriers per block."""
+    names = [f"epilogue{w}" for w in range(warps)]
+    for name in names:
+        ops = []
+        for it in range(n):
+            ops += [("wait", ("dqfull", it)), ("arrive", ("dqempty", it)),
+                    ("arrive", (("nb", "epi"), 2 * it)), ("wait", (("nb", "epi"), 2 * it)),
+                    ("arrive", (("nb", "epi"), 2 * it + 1)), ("wait", (("nb", "epi"), 2 * it + 1))]
+        roles[name] = ops
+    arrivers["dqempty"] = names
+    arrivers[("nb", "epi")] = names
+
+
+def main64(n, warps=2):
+    """Main pass, head dim 64: two query halves, each with its own S/dP buffer,
+    P/dS tile and group of softmax warps (a named barrier per block)."""
     mma = [("wait", ("kvready", 0))]
     if n:
         mma += [("wait", ring("qready", 0, 2)), ("sig", (("sfull", 0), 0)), ("sig", (("sfull", 1), 0))]
@@ -141,55 +181,68 @@ def main64(n):
         if more:
             mma.append(("sig", (("sfull", 1), it + 1)))
     roles = {"producer": _q_producer(n), "mma": mma}
+    arrivers = {}
     for g in (0, 1):
-        soft = []
-        for it in range(n):
-            soft.append(("wait", (("sfull", g), it)))
-            if it > 0:
-                soft.append(("wait", (("pempty", g), it - 1)))
-            soft.append(("sig", (("pfull", g), it)))
-        roles[f"softmax{g}"] = soft
-    roles["epilogue"] = [op for it in range(n) for op in (("wait", ("dqfull", it)), ("sig", ("dqempty", it)))]
-    return roles
+        names = [f"softmax{g}.{w}" for w in range(warps)]
+        for name in names:
+            ops = []
+            for it in range(n):
+                ops += [("arrive", (("nb", g), it)), ("wait", (("nb", g), it)), ("wait", (("sfull", g), it))]
+                if it > 0:
+                    ops.append(("wait", (("pempty", g), it - 1)))
+                ops.append(("arrive", (("pfull", g), it)))
+            roles[name] = ops
+        arrivers[("pfull", g)] = names
+        arrivers[("nb", g)] = names
+    _epilogue(n, roles, arrivers)
+    return roles, arrivers
 
 
-def main128(n):
-    """Main pass, head dim 128: one S/dP buffer, one P/dS tile."""
+def main128(n, warps=2):
+    """Main pass, head dim 128: one S/dP buffer, one P/dS tile, the softmax
+    warps meet at a named barrier per block."""
     mma = [("wait", ("kvready", 0))]
     for it in range(n):
         mma += [("wait", ring("qready", it, 2)), ("sig", ("sfull", it)), ("wait", ("pfull", it))]
         if it > 0:
             mma.append(("wait", ("dqempty", it - 1)))
         mma += [("sig", ring("qempty", it, 2)), ("sig", ("dqfull", it)), ("sig", ("pempty", it))]
-    soft = []
-    for it in range(n):
-        soft.append(("wait", ("sfull", it)))
-        if it > 0:
-            soft.append(("wait", ("pempty", it - 1)))
-        soft.append(("sig", ("pfull", it)))
-    epi = [op for it in range(n) for op in (("wait", ("dqfull", it)), ("sig", ("dqempty", it)))]
-    return {"producer": _q_producer(n), "mma": mma, "softmax": soft, "epilogue": epi}
+    roles = {"producer": _q_producer(n), "mma": mma}
+    names = [f"softmax{w}" for w in range(warps)]
+    for name in names:
+        ops = []
+        for it in range(n):
+            ops += [("arrive", (("nb", "soft"), it)), ("wait", (("nb", "soft"), it)), ("wait", ("sfull", it))]
+            if it > 0:
+                ops.append(("wait", ("pempty", it - 1)))
+            ops.append(("arrive", ("pfull", it)))
+        roles[name] = ops
+    arrivers = {"pfull": names, ("nb", "soft"): names}
+    _epilogue(n, roles, arrivers)
+    return roles, arrivers
 
 
 @pytest.mark.parametrize("n_stages,heads", [(3, 1), (2, 1), (2, 4)])
 def test_dprep_protocol(n_stages, heads):
-    for nj in range(0, 10):
-        dead, missed = check(dprep(nj, n_stages, heads))
-        assert not dead and not missed, (nj, dead, missed[:3])
+    for nj in range(0, 9):
+        dead, missed, overrun = check(dprep(nj, n_stages, heads))
+        assert not dead and not missed and not overrun, (nj, dead, missed[:3], overrun[:3])
 
 
 @pytest.mark.parametrize("fn", [main64, main128])
 def test_main_protocols(fn):
-    for n in range(0, 12):
-        dead, missed = check(fn(n))
-        assert not dead and not missed, (n, dead, missed[:3])
+    for n in range(0, 10):
+        dead, missed, overrun = check(fn(n))
+        assert not dead and not missed and not overrun, (n, dead, missed[:3], overrun[:3])
 
 
-def test_single_p_full_barrier_can_miss_a_phase():
-    """The check finds the flaw the D pre-pass once had: one P-full barrier for
-    both P buffers lets the softmax finish iterations t and t+1 before the MMA
-    thread looks at t."""
+def test_single_p_full_barrier_is_unsafe():
+    """The check finds the flaw the D pre-pass once had.  With one P-full
+    barrier for both P buffers, the softmax can finish iterations t and t+1
+    before the MMA thread looks at t (a missed phase).  And one warp can
+    arrive for t+1 before another has arrived for t (an overrun)."""
     for n_stages, heads in [(3, 1), (2, 4)]:
-        dead, missed = check(dprep(4, n_stages, heads, split_pfull=False))
+        dead, missed, overrun = check(dprep(4, n_stages, heads, split_pfull=False))
         assert not dead
         assert any(ev[0] == "pfull" for _, _, ev in missed)
+        assert any(ev[0] == "pfull" for _, _, ev in overrun)
