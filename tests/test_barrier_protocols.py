@@ -1,5 +1,7 @@
-"""Models of the mbarrier protocols of the tcgen05 attention kernels
-(sparse_backward_gemm_gb300/csrc/attn.cu), checked on the CPU.
+"""Models of the mbarrier protocols of the tcgen05 kernels, checked on the
+CPU: the attention kernels (sparse_backward_gemm_gb300/csrc/attn.cu) and the
+GEMM in its three forms (lone CTAs, B-multicast pairs, 2-SM pairs;
+sparse_backward_gemm_gb300/csrc/gemm_tc.cu).
 
 Each role of a kernel (TMA producer, MMA issuer, softmax warps, epilogue
 warps) is written as its sequence of operations on (barrier, phase) events:
@@ -246,3 +248,77 @@ def test_single_p_full_barrier_is_unsafe():
         assert not dead
         assert any(ev[0] == "pfull" for _, _, ev in missed)
         assert any(ev[0] == "pfull" for _, _, ev in overrun)
+
+
+# ---------------------------------------------------------------------------
+# tcgen05 GEMM (sparse_backward_gemm_gb300/csrc/gemm_tc.cu): an S-stage ring
+# of shared-memory stages, a double-buffered TMEM accumulator, epilogue warps
+# that release it.  `tiles` whole tiles of `kb` k-blocks each.
+def gemm(mode, tiles, kb, S, warps=2):
+    G = tiles * kb
+    roles, arrivers = {}, {}
+    ctas = ["A"] if mode == 0 else ["A", "B"]
+    for c in ctas:
+        ops = []
+        for g in range(G):
+            if g >= S:
+                ops.append(("wait", ring(("empty", c), g - S, S)))
+            if mode == 0:
+                ops.append(("sig", ring(("full", c), g, S)))
+            elif mode == 1:
+                # its A tile and its B half land in its own stage; the B half also in the peer's
+                ops += [("arrive", ring(("full", x), g, S)) for x in ctas]
+            else:
+                # every copy of both CTAs is counted on the even CTA's full barrier
+                ops.append(("arrive", ring(("full", "A"), g, S)))
+        if mode != 0:
+            # a pair member leaves only after both MMAs released every stage it loaded
+            ops += [("wait", ring(("empty", c), g, S)) for g in range(max(0, G - S), G)]
+        roles[f"producer{c}"] = ops
+    if mode == 1:
+        for x in ctas:
+            for s in range(S):
+                arrivers[(("full", x), s)] = [f"producer{c}" for c in ctas]
+                arrivers[(("empty", x), s)] = [f"mma{c}" for c in ctas]
+    if mode == 2:
+        for s in range(S):
+            arrivers[(("full", "A"), s)] = [f"producer{c}" for c in ctas]
+    issuers = ctas if mode != 2 else ["A"]     # 2-SM: the even CTA issues for both
+    for c in issuers:
+        ops = []
+        for t in range(tiles):
+            if t >= 2:
+                ops.append(("wait", ring(("tempty", c), t - 2, 2)))
+            for k in range(kb):
+                g = t * kb + k
+                ops.append(("wait", ring(("full", c), g, S)))
+                if mode == 0:
+                    ops.append(("sig", ring(("empty", c), g, S)))
+                elif mode == 1:
+                    ops += [("arrive", ring(("empty", x), g, S)) for x in ctas]   # commit to both CTAs
+                else:
+                    ops += [("sig", ring(("empty", x), g, S)) for x in ctas]
+            ops += [("sig", ring(("tfull", x), t, 2)) for x in (ctas if mode == 2 else [c])]
+        roles[f"mma{c}"] = ops
+    epi_names = {c: [f"epilogue{c}.{w}" for w in range(warps)] for c in ctas}
+    for c in ctas:
+        owner = "A" if mode == 2 else c          # 2-SM: both epilogues release on the even CTA
+        for name in epi_names[c]:
+            ops = []
+            for t in range(tiles):
+                ops += [("wait", ring(("tfull", c), t, 2)), ("arrive", ring(("tempty", owner), t, 2))]
+            roles[name] = ops
+    for c in issuers:
+        names = [n for x in ctas for n in epi_names[x]] if mode == 2 else epi_names[c]
+        for a in range(2):
+            arrivers[(("tempty", c), a)] = names
+    return roles, arrivers
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_gemm_protocols(mode):
+    for tiles in range(0, 5):
+        for kb in (1, 2, 5):
+            for S in (2, 3, 7):
+                dead, missed, overrun = check(gemm(mode, tiles, kb, S))
+                assert not dead and not missed and not overrun, (mode, tiles, kb, S, dead, missed[:2], overrun[:2])
