@@ -322,3 +322,18 @@ def test_gemm_protocols(mode):
             for S in (2, 3, 7):
                 dead, missed, overrun = check(gemm(mode, tiles, kb, S))
                 assert not dead and not missed and not overrun, (mode, tiles, kb, S, dead, missed[:2], overrun[:2])
+
+
+def test_checker_catches_planted_gemm_flaws():
+    """Dropping a wait from a correct model must be caught."""
+    # the MMA issuer no longer waits for the epilogues to release the accumulator
+    roles, arrivers = gemm(2, 4, 2, 3)
+    roles["mmaA"] = [op for op in roles["mmaA"] if not (op[0] == "wait" and op[1][0][0][0] == "tempty")]
+    dead, missed, overrun = check((roles, arrivers))
+    assert missed and overrun
+    # the producers no longer wait for a stage to be consumed
+    roles, arrivers = gemm(1, 3, 2, 2)
+    for c in "AB":
+        roles[f"producer{c}"] = [op for op in roles[f"producer{c}"] if op[0] != "wait"]
+    dead, missed, overrun = check((roles, arrivers))
+    assert missed and overrun
