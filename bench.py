@@ -324,6 +324,60 @@ def max_over_ranks(vals, device):
     return t.tolist()
 
 
+def profile_pass(cl, step_fn, steps, warmup, flush, n_kept):
+    """Per-launch event times of `steps` steps, every launch on one stream
+    (the library's profiler; the weight-gradient side stream is off so no
+    kernel shares the GPU with another).  Returns per-kernel [launches, ms]
+    summed over the steps, the GEMM launches' algorithmic FLOPs and time, and
+    a per-shape GEMM table (ms per step)."""
+    import torch
+    os.environ["COLLIDER_SIDE_STREAM"] = "0"
+    try:
+        for _ in range(warmup):
+            step_fn()
+        cl.collider_profile_enable(1)
+        for _ in range(steps):
+            flush.fill_(1)
+            step_fn()
+        torch.cuda.synchronize()
+        cl.collider_profile_enable(0)
+    finally:
+        os.environ["COLLIDER_SIDE_STREAM"] = "1"
+    per, shapes = {}, {}
+    gemm_ms, gemm_fl = 0.0, 0.0
+    for i in range(cl.collider_profile_count()):
+        name, (m, n, k, dyn), ms = cl.collider_profile_get(i)
+        d = per.setdefault(name, [0, 0.0])
+        d[0] += 1
+        d[1] += ms
+        if name == "tc_gemm":
+            mm = n_kept if dyn == 1 else m
+            kk = n_kept if dyn == 2 else k
+            gemm_ms += ms
+            gemm_fl += 2.0 * mm * n * kk
+            key = f"{mm}x{n}x{kk}" + ("" if dyn != 2 else " (dW)")
+            e = shapes.setdefault(key, [0.0, 2.0 * mm * n * kk])
+            e[0] += ms / steps
+    return per, gemm_ms, gemm_fl, shapes
+
+
+def attn_roofline(per, steps, fl_per_step, peak, src):
+    """The attention backward's main pass (and with its D' pre-pass) against
+    the bf16 tensor peak: 5-unit algorithmic FLOPs over event time."""
+    main = per.get("attn_main_tc", [0, 0.0])[1] / steps
+    pre = per.get("attn_dprep_tc", [0, 0.0])[1] / steps
+    if main <= 0:
+        return None
+    a_main = fl_per_step / (main * 1e-3) / 1e12
+    a_both = fl_per_step / ((main + pre) * 1e-3) / 1e12
+    return {"bound": "tensor", "kernel": "attn_main_tc (tcgen05 filtered attention backward, main pass)",
+            "achieved": a_main, "peak": peak, "unit": "TFLOP/s", "frac": a_main / peak,
+            "peak_source": f"bf16_tflops ({src})", "traffic": None,
+            "ms_per_step": main, "prepass_ms_per_step": pre,
+            "frac_with_prepass": a_both / peak,
+            "flops": "5 matmul units over the kept causal pairs: 10*dh*H*sum_b m_b(m_b+1)/2 per step"}
+
+
 def measured_peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
@@ -438,32 +492,8 @@ def run_ours(args):
     # every launch on one stream, so no kernel shares the GPU with another.
     n_kept = int(tn["keep"].sum())
     kept_per_seq = tn["keep"].sum(axis=1).tolist()
-    os.environ["COLLIDER_SIDE_STREAM"] = "0"
-    for _ in range(args.warmup):
-        step(masks["filtered"])
-    cl.collider_profile_enable(1)
-    for _ in range(args.steps):
-        flush.fill_(1)
-        step(masks["filtered"])
-    torch.cuda.synchronize()
-    cl.collider_profile_enable(0)
-    os.environ["COLLIDER_SIDE_STREAM"] = "1"
-    per = {}
-    gemm_ms, gemm_fl = 0.0, 0.0
-    gemm_shapes = {}
-    for i in range(cl.collider_profile_count()):
-        name, (m, n, k, dyn), ms = cl.collider_profile_get(i)
-        d = per.setdefault(name, [0, 0.0])
-        d[0] += 1
-        d[1] += ms
-        if name == "tc_gemm":
-            mm = n_kept if dyn == 1 else m
-            kk = n_kept if dyn == 2 else k
-            gemm_ms += ms
-            gemm_fl += 2.0 * mm * n * kk
-            key = f"{mm}x{n}x{kk}" + ("" if dyn != 2 else " (dW)")
-            e = gemm_shapes.setdefault(key, [0.0, 2.0 * mm * n * kk])
-            e[0] += ms / args.steps
+    per, gemm_ms, gemm_fl, gemm_shapes = profile_pass(cl, lambda: step(masks["filtered"]), args.steps,
+                                                      args.warmup, flush, n_kept)
     peaks, src = measured_peaks()
     achieved = gemm_fl / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else 0.0
     step_ms_prof = sum(v[1] for v in per.values()) / args.steps
@@ -581,14 +611,30 @@ def run_ours(args):
             torch.cuda.empty_cache()
         st = workloads.WORKLOADS["tinyllama_stack"]
         stk = Stack(cl, st, dev)
-        K2 = max(2, args.steps // 4)
+        K2 = max(10, args.steps // 2)
         ms3f, _ = timed(stk.mask, K2, args.warmup, lambda m: stk.step(m, stream))
         ms3u, _ = timed(stk.mask_all, K2, args.warmup, lambda m: stk.step(m, stream))
         ms3f, ms3u = max_over_ranks([ms3f, ms3u], dev)
+        # serialised profiler pass over the whole stack: GEMM and attention
+        # fractions of the largest workload
+        nk3 = int(stk.keep_np.sum())
+        sp, sg_ms, sg_fl, sg_shapes = profile_pass(cl, lambda: stk.step(stk.mask, stream), 3, 1, flush, nk3)
+        s_att = attn_roofline(sp, 3, st.L * attn_flops(st.layer, stk.keep_np.sum(axis=1).tolist()),
+                              peaks["bf16_tflops"], src)
+        s_ach = sg_fl / (sg_ms * 1e-3) / 1e12 if sg_ms > 0 else 0.0
         configs["tinyllama_stack (22 blocks + LM head)"] = {
             "tokens_per_s": st.layer.M * world / (ms3f * 1e-3), "ms_per_step": ms3f, "unfiltered_ms_per_step": ms3u,
-            "speedup_vs_unfiltered": ms3u / ms3f, "kept_tokens": int(stk.keep_np.sum()), "tokens": st.layer.M,
-            "steps": K2}
+            "speedup_vs_unfiltered": ms3u / ms3f, "kept_tokens": nk3, "tokens": st.layer.M,
+            "steps": K2,
+            "roofline": {
+                "gemm": {"bound": "tensor", "kernel": "tc_gemm (all launches of a step: 22 blocks + LM head)",
+                         "achieved": s_ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": s_ach / peaks["bf16_tflops"], "ms_per_step": sg_ms / 3,
+                         "launches_per_step": sp.get("tc_gemm", [0, 0])[0] // 3},
+                "attention": s_att,
+                "step_ms_serialised": sum(v[1] for v in sp.values()) / 3,
+                "kernels_ms_per_step": {k: round(v[1] / 3, 4) for k, v in sorted(sp.items())},
+                "timing": "per-launch CUDA events, every launch on one stream (serialised pass, 3 steps)"}}
         del stk
         torch.cuda.empty_cache()
 
@@ -608,7 +654,11 @@ def run_ours(args):
                          "traffic": gemm_traffic(), "traffic_unit": "bytes per step (8 launches), ncu cold-cache",
                          "gemm_ms_per_step": gemm_ms / args.steps,
                          "timing": "per-launch CUDA events, every launch on one stream (serialised pass)",
-                         "step_ms_serialised": step_ms_prof},
+                         "step_ms_serialised": step_ms_prof,
+                         "attention": attn_roofline(per, args.steps, attn_flops(s, kept_per_seq),
+                                                    peaks["bf16_tflops"], src),
+                         "speedup_vs_unfiltered": ms_u / ms_f, "unfiltered_ms_per_step": ms_u,
+                         "stack": (configs.get("tinyllama_stack (22 blocks + LM head)") or {}).get("roofline")},
             "kernels_ms_per_step": {k: round(v[1] / args.steps, 4) for k, v in sorted(per.items())},
             "gemms": {k: {"ms": round(v[0], 4), "tflops": round(v[1] / (v[0] * 1e-3) / 1e12, 1)}
                       for k, v in gemm_shapes.items()},

@@ -6,8 +6,7 @@
  *   - the forward stays dense; a token filter marks each token kept or
  *     filtered and drops the loss of filtered tokens (Fig. 2b);
  *   - in backward, the activations and output gradients of filtered tokens
- *     are dropped in EVERY layer, not only at the loss (abstract; TL;DR
- *     "backward activation filtering across all layers");
+ *     are dropped in EVERY layer, not only at the loss (abstract; TL;DR);
  *   - inside attention the softmax of filtered tokens is filtered as well, so
  *     that G_V -- and the activations used for the Q and K gradients -- stay
  *     sparse (Fig. 3, Fig. 5);
@@ -147,15 +146,18 @@ collider_status collider_compact(const uint8_t* mask, int B, int T, int32_t* idx
  * streams without ordering between them) race and must be serialised by the
  * caller; calls on one stream are fine.  The first call on each device looks
  * up the array's device address (cudaGetSymbolAddress, with that device
- * current); make that first call before any stream capture.  Nothing is
- * allocated, and no earlier call's contents need clearing: every entry a call
- * reads is written by that call first. */
+ * current) and keeps it for the life of the process; make that first call
+ * before any stream capture.  The kept address belongs to the device's primary
+ * context: do not call this after cudaDeviceReset on that device, or with
+ * another (non-primary) context current.  Nothing is allocated, and no earlier
+ * call's contents need clearing: every entry a call reads is written by that
+ * call first. */
 collider_status collider_compact_noalloc(const uint8_t* mask, int B, int T, int32_t* idx,
                                          int32_t* cu_kept, int32_t* n_kept, void* stream);
 
 /* ------------------------------------------------------------------------ */
-/* a2. Row gather / scatter (abstract: activations of filtered tokens are    */
-/*     filtered across all layers)                                           */
+/* a2. Row gather / scatter (abstract: the activations of filtered tokens   */
+/*     are dropped in every layer)                                           */
 /* ------------------------------------------------------------------------ */
 
 /* dst[r, :] = src[idx[r], :] for r < n_kept; dst rows n_kept .. next

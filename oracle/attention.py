@@ -51,7 +51,25 @@ def attention_forward(q, k, v, B, T, scale, causal=True):
     return o, lse
 
 
-def filtered_attention_backward(q, k, v, dO, lse, keep, scale, causal=True, zero_p=True):
+def _head_backward(task):
+    """One (sequence, query head): the filtered backward of that head alone.
+    Returns its dQ rows and its contributions to dK, dV of the head's kv head."""
+    Q, K, V, G, lse_row, mi, causal, zero_p, scale = task
+    T = mi.size
+    pos = np.arange(T)
+    allowed = (pos[None, :] <= pos[:, None]) if causal else np.ones((T, T), dtype=bool)
+    pair = np.outer(mi, mi) if zero_p else np.ones((T, T), dtype=bool)
+    S = (Q @ K.T) * scale
+    P = np.where(allowed, np.exp(np.where(allowed, S, 0.0) - lse_row[:, None]), 0.0)
+    Pf = np.where(pair, P, 0.0)                 # P'
+    dv = Pf.T @ G                               # G_V
+    dP = G @ V.T
+    D = np.sum(Pf * dP, axis=1)                 # over the filtered P'
+    dS = Pf * (dP - D[:, None])
+    return (dS @ K) * scale, (dS.T @ Q) * scale, dv
+
+
+def filtered_attention_backward(q, k, v, dO, lse, keep, scale, causal=True, zero_p=True, pool=None):
     """Collider attention backward, full-size and masked.
 
     keep: [B, T] keep-mask.  Rows of q, k, v, dO of filtered tokens are
@@ -60,6 +78,9 @@ def filtered_attention_backward(q, k, v, dO, lse, keep, scale, causal=True, zero
     the softmax of filtered tokens is left as the dense forward made it (K, V
     of filtered tokens kept, P not zeroed), only the upstream gradient rows
     are filtered, and G_V picks up rows at filtered tokens.
+    pool: an optional process pool (anything with ``map``) over which the
+    independent (sequence, head) computations are spread; the results are
+    summed in the same order either way.
     Returns dq [M, H, dh], dk and dv [M, Hkv, dh].
     """
     keep = np.asarray(keep) != 0
@@ -76,22 +97,14 @@ def filtered_attention_backward(q, k, v, dO, lse, keep, scale, causal=True, zero
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
-    pos = np.arange(T)
-    allowed = (pos[None, :] <= pos[:, None]) if causal else np.ones((T, T), dtype=bool)
     for b in range(B):
         rows = slice(b * T, (b + 1) * T)
-        mi = keep[b]
-        pair = np.outer(mi, mi) if zero_p else np.ones((T, T), dtype=bool)
-        for h in range(H):
+        tasks = [(q[rows, h, :], k[rows, _kv_head(h, H, Hkv), :], v[rows, _kv_head(h, H, Hkv), :],
+                  dO[rows, h, :], lse[b, h, :], keep[b], causal, zero_p, scale) for h in range(H)]
+        outs = (pool.map if pool is not None else map)(_head_backward, tasks)
+        for h, (dq_h, dk_h, dv_h) in enumerate(outs):
             hk = _kv_head(h, H, Hkv)
-            Q, K, V, G = q[rows, h, :], k[rows, hk, :], v[rows, hk, :], dO[rows, h, :]
-            S = (Q @ K.T) * scale
-            P = np.where(allowed, np.exp(np.where(allowed, S, 0.0) - lse[b, h, :, None]), 0.0)
-            Pf = np.where(pair, P, 0.0)                 # P'
-            dv[rows, hk, :] += Pf.T @ G                 # G_V
-            dP = G @ V.T
-            D = np.sum(Pf * dP, axis=1)                 # over the filtered P'
-            dS = Pf * (dP - D[:, None])
-            dq[rows, h, :] = (dS @ K) * scale
-            dk[rows, hk, :] += (dS.T @ Q) * scale
+            dq[rows, h, :] = dq_h
+            dk[rows, hk, :] += dk_h
+            dv[rows, hk, :] += dv_h
     return dq, dk, dv

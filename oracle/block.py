@@ -1,7 +1,7 @@
 """Decoder block: dense forward (producing the saved set) and Collider's
 filtered backward, float64 (test infrastructure only).
 
-Collider (abstract; TL;DR "backward activation filtering across all layers")
+Collider (abstract; TL;DR: activation filtering in the backward of every layer)
 keeps the forward dense and, in backward, drops the activations and output
 gradients of filtered tokens in every layer.  Here that is done full-size:
 every saved row and every incoming-gradient row of a filtered token is
@@ -99,7 +99,7 @@ def block_forward(x, w, s, round_saved=True):
     return out, sv
 
 
-def block_backward(dout, saved, w, s, keep, filter_activations=True):
+def block_backward(dout, saved, w, s, keep, filter_activations=True, pool=None):
     """Collider filtered backward of one block, full-size and masked.
 
     keep: [B, T] keep-mask.  Returns a dict of gradients: dx [M, D] (filtered
@@ -108,6 +108,7 @@ def block_backward(dout, saved, w, s, keep, filter_activations=True):
     filter_activations=False is the prior art Collider improves on (Fig. 2b,
     Fig. 3): only the loss of filtered tokens is dropped, the saved
     activations and the softmax stay dense, so gradients reach filtered rows.
+    pool: optional process pool for the attention's (sequence, head) loop.
     """
     keep = np.asarray(keep) != 0
     km = keep.reshape(-1)
@@ -161,9 +162,9 @@ def block_backward(dout, saved, w, s, keep, filter_activations=True):
     do = (dattn @ f64(w["w_o"]).T).reshape(M, s.H, s.dh)
     q, k, v = _split_qkv(qkv, s)
     if filter_activations:
-        dq, dk, dv = filtered_attention_backward(q, k, v, do, lse, keep, scale)
+        dq, dk, dv = filtered_attention_backward(q, k, v, do, lse, keep, scale, pool=pool)
     else:
-        dq, dk, dv = filtered_attention_backward(q, k, v, do, lse, np.ones_like(keep), scale)
+        dq, dk, dv = filtered_attention_backward(q, k, v, do, lse, np.ones_like(keep), scale, pool=pool)
     dq = ops.rope_backward(dq, pos, s.rotary_dim, s.rope_base)
     dk = ops.rope_backward(dk, pos, s.rotary_dim, s.rope_base)
     dqkv = np.concatenate([dq.reshape(M, -1), dk.reshape(M, -1), dv.reshape(M, -1)], axis=1)

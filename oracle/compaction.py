@@ -1,7 +1,7 @@
 """Keep-mask selection and compaction (test infrastructure only).
 
-Collider abstract: the would-be sparse GEMM over all tokens becomes a
-"dimension-reduced dense GEMM" over the kept tokens.  The reduction needs the
+Collider abstract: the would-be sparse GEMM over all tokens is rewritten as a
+dense GEMM whose token dimension is cut down to the kept tokens.  That needs the
 list of kept tokens; this is its plain definition: the ascending flat indices
 of the nonzero mask entries, the number of kept tokens before each sequence
 start, and the total.

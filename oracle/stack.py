@@ -31,10 +31,16 @@ def stack_forward(ids, E, layers, normf_w, w_lm, ls, round_saved=True):
     return z, dict(blocks=blocks, xL=x, rstdf=rstd, y=y)
 
 
-def stack_backward(z, targets, ids, saved, layers, normf_w, w_lm, ls, V, keep, filter_activations=True):
+def stack_backward(z, targets, ids, saved, layers, normf_w, w_lm, ls, V, keep, filter_activations=True,
+                   pool=None, on_block=None):
     """Filtered backward of the whole stack.  Returns dict with dz-derived
     dw_lm [D, V], dnormf_w [D], dE [V, D] and per-block gradient dicts
-    (``blocks``, input order), plus dx0 (gradient at the embedding output)."""
+    (``blocks``, input order), plus dx0 (gradient at the embedding output).
+    ``saved["blocks"]`` is indexed once per block, top block first, so it may
+    produce each block's saved set on demand.  pool: optional process pool
+    for the attention loop.  on_block(l, grads), if given, receives each
+    block's gradients as soon as they exist, and only dx is kept between
+    blocks (the per-block dicts are then not returned)."""
     keep = np.asarray(keep) != 0
     km = keep.reshape(-1)
     Z = (lambda t: ops.rows_where(km, t)) if filter_activations else \
@@ -50,9 +56,12 @@ def stack_backward(z, targets, ids, saved, layers, normf_w, w_lm, ls, V, keep, f
     grads = [None] * len(layers)
     for l in reversed(range(len(layers))):
         g = block_backward(dx, saved["blocks"][l], layers[l], ls, keep,
-                           filter_activations=filter_activations)
+                           filter_activations=filter_activations, pool=pool)
         dx = g["dx"]
-        grads[l] = g
+        if on_block is not None:
+            on_block(l, g)
+        else:
+            grads[l] = g
     out["blocks"] = grads
     out["dx0"] = dx
     dE = np.zeros((V, dx.shape[1]))

@@ -258,6 +258,7 @@ cudaError_t launch_compact(const Ctx& c, const uint8_t* mask, int B, int T, int3
 // three-kernel path, with the per-chunk counts in a fixed array of device
 // memory that belongs to this library and lives as long as the process.
 // ===========================================================================
+#include <cstdio>
 #include <mutex>
 
 #include "../../include/collider.h"
@@ -279,6 +280,13 @@ collider_status noalloc_fail(collider_status s, const char* m) {
   return s;
 }
 
+collider_status noalloc_cuda_fail(cudaError_t e, const char* where) {
+  char buf[256];
+  snprintf(buf, sizeof buf, "collider_compact_noalloc: %s: %s", where, cudaGetErrorString(e));
+  set_last_error(buf);
+  return COLLIDER_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace collider
 
@@ -295,10 +303,12 @@ extern "C" collider_status collider_compact_noalloc(const uint8_t* mask, int B, 
                         "collider_compact_noalloc: B*T exceeds its fixed limit of 1073741824 tokens "
                         "(use collider_compact with a workspace)");
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-    return noalloc_fail(COLLIDER_ERR_CUDA, "collider_compact_noalloc: no current CUDA device");
-  if (cudaGetLastError() != cudaSuccess)
-    return noalloc_fail(COLLIDER_ERR_CUDA, "collider_compact_noalloc: earlier asynchronous CUDA error");
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return noalloc_cuda_fail(e, "no current CUDA device");
+  if (dev < 0 || dev >= 64)
+    return noalloc_fail(COLLIDER_ERR_UNSUPPORTED, "collider_compact_noalloc: device ordinal >= 64");
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return noalloc_cuda_fail(e, "earlier asynchronous CUDA error");
   int* counts = nullptr;
   {
     // first call on this device: look up the device address of the array
@@ -306,8 +316,9 @@ extern "C" collider_status collider_compact_noalloc(const uint8_t* mask, int B, 
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     if (!g_noalloc_addr[dev]) {
       void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_noalloc_counts) != cudaSuccess || !p)
-        return noalloc_fail(COLLIDER_ERR_CUDA, "collider_compact_noalloc: cudaGetSymbolAddress failed");
+      e = cudaGetSymbolAddress(&p, g_noalloc_counts);
+      if (e != cudaSuccess) return noalloc_cuda_fail(e, "cudaGetSymbolAddress");
+      if (!p) return noalloc_fail(COLLIDER_ERR_CUDA, "collider_compact_noalloc: cudaGetSymbolAddress gave null");
       g_noalloc_addr[dev] = static_cast<int*>(p);
     }
     counts = g_noalloc_addr[dev];
@@ -320,7 +331,7 @@ extern "C" collider_status collider_compact_noalloc(const uint8_t* mask, int B, 
   compact_scan<<<1, kThreads, 0, s>>>(counts, nchunks, B, cu_kept, n_kept);
   compact_write<<<nchunks, kThreads, 0, s>>>(mask, B, T, counts, idx, cu_kept);
   count_launch(3);
-  if (cudaGetLastError() != cudaSuccess)
-    return noalloc_fail(COLLIDER_ERR_CUDA, "collider_compact_noalloc: kernel launch failed");
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return noalloc_cuda_fail(e, "kernel launch");
   return COLLIDER_OK;
 }

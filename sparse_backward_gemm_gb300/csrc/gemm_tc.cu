@@ -223,24 +223,23 @@ __device__ __forceinline__ void store32(const TcParams& p, int row, int col, boo
   }
 }
 
-// MODE 0: lone CTAs.  MODE 1 and 2: the grid is made of 2-CTA clusters; both
-// CTAs of a pair work on the same column tile and on adjacent 128-row tiles.
-//   MODE 1: each CTA loads half of the B tile and multicasts it to both, so
-//           every SM reads 2/3 of the operand bytes from L2 that a lone CTA
-//           reads.  A stage is released to either producer only when both
-//           MMAs have consumed it (the empty barrier counts two commits).
-//   MODE 2 (BN = 256): 2-SM MMAs.  Each CTA loads its A tile and half of the
-//           B tile into its own shared memory only (32 KB a stage instead of
-//           48), every copy counted on the even CTA's full barrier; the even
-//           CTA issues one 256 x 256 MMA over both CTAs' tiles, writing each
-//           CTA's 128 rows into that CTA's TMEM; its commits reach both CTAs'
-//           empty and TMEM-full barriers, and both epilogues release the
-//           accumulator on the even CTA's TMEM-empty barrier.
+// MODE 0: lone CTAs.
+// MODE 2 (BN = 256): the grid is made of 2-CTA clusters; both CTAs of a pair
+//           work on the same column tile and on adjacent 128-row tiles, with
+//           2-SM MMAs.  Each CTA loads its A tile and half of the B tile into
+//           its own shared memory only (32 KB a stage instead of 48), every
+//           copy counted on the even CTA's full barrier; the even CTA issues
+//           one 256 x 256 MMA over both CTAs' tiles, writing each CTA's 128
+//           rows into that CTA's TMEM; its commits reach both CTAs' empty and
+//           TMEM-full barriers, and both epilogues release the accumulator on
+//           the even CTA's TMEM-empty barrier.  No copy is multicast: each CTA
+//           loads only what lands in its own shared memory.
 template <int BN, bool A_MN, bool B_MN, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcParams p) {
   using Cfg = TcCfg<BN>;
-  constexpr bool PAIR = MODE != 0, TWO = MODE == 2;
+  static_assert(MODE == 0 || MODE == 2, "lone CTAs or 2-SM pairs");
+  constexpr bool PAIR = MODE == 2, TWO = MODE == 2;
   static_assert(!TWO || BN == 256, "2-SM tiles are 256 x 256");
   constexpr uint32_t kStageBytes = TWO ? kTwoStageBytes : Cfg::kStageBytes;
   constexpr int S = TWO ? kTwoStages : Cfg::kStages;
@@ -280,7 +279,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, MODE == 1 ? 2 : 1);
+      mbar_init(empty0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
@@ -297,7 +296,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   fence_before();
   __syncthreads();
-  if (PAIR) cluster_sync();   // the peer's barriers exist before any multicast reaches them
+  if (PAIR) cluster_sync();   // the peer's barriers exist before any copy or commit reaches them
   fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -364,18 +363,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tma_load_2d(sa, &tmA, fb, m0, kx);
             tma_load_2d(sa + 8192, &tmA, fb, m0 + 64, kx);
           }
-          if (PAIR) {
-            // this CTA's half of B, to both CTAs of the pair
-            if (!B_MN) {
-              tma_load_2d_mc(sb + rank * (Cfg::kBBytes / 2), &tmB, fb, kx, n0 + rank * (BN / 2), 3);
-            } else {
-#pragma unroll
-              for (int j = 0; j < BN / 128; ++j) {
-                const int c = rank * (BN / 128) + j;
-                tma_load_2d_mc(sb + 8192 * c, &tmB, fb, n0 + 64 * c, kx, 3);
-              }
-            }
-          } else if (!B_MN) {
+          if (!B_MN) {
             tma_load_2d(sb, &tmB, fb, kx, n0);
           } else {
 #pragma unroll
@@ -432,7 +420,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             else mma_bf16(d, ad, bd, idesc, (kb > k0) || (kk > 0));
           }
           if (TWO) mma_commit_pair_mc(empty0 + 8 * stage, 3);
-          else if (PAIR) mma_commit_mc(empty0 + 8 * stage, 3);
           else mma_commit(empty0 + 8 * stage);
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
@@ -566,7 +553,7 @@ bool make_map(CUtensorMap* m, const void* base, long long inner, long long rows,
 template <int BN, bool A_MN, bool B_MN, int MODE>
 cudaError_t launch_variant(const Ctx& c, const TcGemm& g, const CUtensorMap& ma, const CUtensorMap& mb,
                            const TcParams& p) {
-  constexpr bool PAIR = MODE != 0;
+  constexpr bool PAIR = MODE == 2;
   constexpr size_t kSmemBytes = MODE == 2 ? kTwoSmem : TcCfg<BN>::kSmem;
   auto kern = tc_gemm_kernel<BN, A_MN, B_MN, MODE>;
   // Per-device set-up, the first time each device uses this variant: the
@@ -674,9 +661,9 @@ cudaError_t launch_tc_gemm(const Ctx& c, const TcGemm& g) {
     const char* e = getenv("COLLIDER_GEMM_STREAMK");
     return e ? atoi(e) : -1;
   }();
-  // CTA pairs for every whole-tile launch (stream-K launches stay lone
-  // CTAs): 2-SM MMAs for 256-wide tiles, B multicast for 128-wide ones.
-  // COLLIDER_GEMM_PAIR=0 / 1 forces lone CTAs / B multicast everywhere.
+  // 2-SM pairs for every whole-tile launch of 256-wide tiles; 128-wide tiles
+  // and stream-K launches run as lone CTAs.  COLLIDER_GEMM_PAIR=0 forces lone
+  // CTAs everywhere.
   static const int pair_env = [] {
     const char* e = getenv("COLLIDER_GEMM_PAIR");
     return e ? atoi(e) : -1;
@@ -685,8 +672,8 @@ cudaError_t launch_tc_gemm(const Ctx& c, const TcGemm& g) {
   int split = split_env;
   if (split < 0) split = (g.dyn != 2 && g.K / BK >= 128) ? 1 : 0;
   const bool sk = split != 0 && g.partial && g.counters && max_tiles <= g.counter_cap;
-  const bool pair = !sk && pair_env != 0;
-  const int mode = !pair ? 0 : (bn == 256 && pair_env != 1 ? 2 : 1);
+  const bool pair = !sk && pair_env != 0 && bn == 256;
+  const int mode = pair ? 2 : 0;
   CUtensorMap ma, mb;
   // A: K-major [M rows, K] or MN-major [K rows, M]; B: K-major [N rows, K]
   // (half the tile's rows per box for a pair) or MN-major [K rows, N]
@@ -703,20 +690,15 @@ cudaError_t launch_tc_gemm(const Ctx& c, const TcGemm& g) {
   const int key = (bn == 256 ? 100 : 0) + (g.a_mn_major ? 10 : (g.b_mn_major ? 20 : 0)) + mode;
   switch (key) {
     case 0: e = launch_variant<128, false, false, 0>(c, g, ma, mb, p); break;
-    case 1: e = launch_variant<128, false, false, 1>(c, g, ma, mb, p); break;
     case 10: e = launch_variant<128, true, true, 0>(c, g, ma, mb, p); break;
-    case 11: e = launch_variant<128, true, true, 1>(c, g, ma, mb, p); break;
     case 20: e = launch_variant<128, false, true, 0>(c, g, ma, mb, p); break;
-    case 21: e = launch_variant<128, false, true, 1>(c, g, ma, mb, p); break;
     case 100: e = launch_variant<256, false, false, 0>(c, g, ma, mb, p); break;
-    case 101: e = launch_variant<256, false, false, 1>(c, g, ma, mb, p); break;
     case 102: e = launch_variant<256, false, false, 2>(c, g, ma, mb, p); break;
     case 110: e = launch_variant<256, true, true, 0>(c, g, ma, mb, p); break;
-    case 111: e = launch_variant<256, true, true, 1>(c, g, ma, mb, p); break;
     case 120: e = launch_variant<256, false, true, 0>(c, g, ma, mb, p); break;
-    case 121: e = launch_variant<256, false, true, 1>(c, g, ma, mb, p); break;
     case 122: e = launch_variant<256, false, true, 2>(c, g, ma, mb, p); break;
-    default: e = launch_variant<256, true, true, 2>(c, g, ma, mb, p); break;
+    case 112: e = launch_variant<256, true, true, 2>(c, g, ma, mb, p); break;
+    default: e = cudaErrorNotSupported; break;
   }
   prof_end(c);
   count_launch();

@@ -61,16 +61,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
-// The same tile delivered to every CTA of the cluster named in cta_mask, at
-// this CTA's shared-memory offsets of dst and bar in each of them.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
-                                               uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
-}
 // Copy into this CTA's shared memory whose completion is counted on `bar`, an
 // mbarrier in either CTA of the pair (a shared::cluster address, see
 // map_to_rank); for kernels whose tensor-core work is issued by CTA pairs.
@@ -180,14 +170,6 @@ __device__ __forceinline__ void tmem_alloc_pair(uint32_t slot_smem, uint32_t col
 }
 __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t cols) {
   asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
-}
-
-// the same arrival on `bar` at this offset in every CTA of cta_mask
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   bar),
-               "h"(cta_mask)
-               : "memory");
 }
 
 // 32 consecutive f32 columns of this thread's TMEM lane (warp-collective)

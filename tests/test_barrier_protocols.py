@@ -1,6 +1,6 @@
 """Models of the mbarrier protocols of the tcgen05 kernels, checked on the
 CPU: the attention kernels (sparse_backward_gemm_gb300/csrc/attn.cu) and the
-GEMM in its three forms (lone CTAs, B-multicast pairs, 2-SM pairs;
+GEMM in its two forms (lone CTAs, 2-SM pairs;
 sparse_backward_gemm_gb300/csrc/gemm_tc.cu).
 
 Each role of a kernel (TMA producer, MMA issuer, softmax warps, epilogue
@@ -265,9 +265,6 @@ def gemm(mode, tiles, kb, S, warps=2):
                 ops.append(("wait", ring(("empty", c), g - S, S)))
             if mode == 0:
                 ops.append(("sig", ring(("full", c), g, S)))
-            elif mode == 1:
-                # its A tile and its B half land in its own stage; the B half also in the peer's
-                ops += [("arrive", ring(("full", x), g, S)) for x in ctas]
             else:
                 # every copy of both CTAs is counted on the even CTA's full barrier
                 ops.append(("arrive", ring(("full", "A"), g, S)))
@@ -275,11 +272,6 @@ def gemm(mode, tiles, kb, S, warps=2):
             # a pair member leaves only after both MMAs released every stage it loaded
             ops += [("wait", ring(("empty", c), g, S)) for g in range(max(0, G - S), G)]
         roles[f"producer{c}"] = ops
-    if mode == 1:
-        for x in ctas:
-            for s in range(S):
-                arrivers[(("full", x), s)] = [f"producer{c}" for c in ctas]
-                arrivers[(("empty", x), s)] = [f"mma{c}" for c in ctas]
     if mode == 2:
         for s in range(S):
             arrivers[(("full", "A"), s)] = [f"producer{c}" for c in ctas]
@@ -294,8 +286,6 @@ def gemm(mode, tiles, kb, S, warps=2):
                 ops.append(("wait", ring(("full", c), g, S)))
                 if mode == 0:
                     ops.append(("sig", ring(("empty", c), g, S)))
-                elif mode == 1:
-                    ops += [("arrive", ring(("empty", x), g, S)) for x in ctas]   # commit to both CTAs
                 else:
                     ops += [("sig", ring(("empty", x), g, S)) for x in ctas]
             ops += [("sig", ring(("tfull", x), t, 2)) for x in (ctas if mode == 2 else [c])]
@@ -315,7 +305,7 @@ def gemm(mode, tiles, kb, S, warps=2):
     return roles, arrivers
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("mode", [0, 2])
 def test_gemm_protocols(mode):
     for tiles in range(0, 5):
         for kb in (1, 2, 5):
@@ -332,7 +322,7 @@ def test_checker_catches_planted_gemm_flaws():
     dead, missed, overrun = check((roles, arrivers))
     assert missed and overrun
     # the producers no longer wait for a stage to be consumed
-    roles, arrivers = gemm(1, 3, 2, 2)
+    roles, arrivers = gemm(2, 3, 2, 2)
     for c in "AB":
         roles[f"producer{c}"] = [op for op in roles[f"producer{c}"] if op[0] != "wait"]
     dead, missed, overrun = check((roles, arrivers))

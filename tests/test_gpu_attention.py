@@ -16,7 +16,7 @@ gu = pytest.importorskip("gpu_util")
 cl = gu.cl
 
 
-def _case(B, T, H, Hkv, dh, f, mask, seed, qk_std=1.0):
+def _case(B, T, H, Hkv, dh, f, mask, seed, qk_std=1.0, causal=True):
     rng = np.random.default_rng(seed)
     R = workloads.bf16_representable
     q = R(rng.normal(size=(B * T, H, dh)) * qk_std)
@@ -25,7 +25,7 @@ def _case(B, T, H, Hkv, dh, f, mask, seed, qk_std=1.0):
     dO = R(rng.normal(size=(B * T, H, dh)))
     keep = workloads.keep_mask(B, T, f, mask, seed)
     scale = 1 / math.sqrt(dh)
-    _, lse = attention_forward(q, k, v, B, T, scale)
+    _, lse = attention_forward(q, k, v, B, T, scale, causal=causal)
     lse = lse.astype(np.float32)
     return q, k, v, dO, lse, keep, scale
 
@@ -96,3 +96,28 @@ def test_attention_ignores_filtered_rows():
         outs.append([r.cpu() for r in res])
     for a, b in zip(*outs):
         assert torch.equal(a, b) and torch.isfinite(a.float()).all()
+
+
+@pytest.mark.parametrize("B,T,H,Hkv,dh", [(2, 300, 4, 2, 64), (1, 260, 2, 1, 128)])
+def test_attention_backward_non_causal(B, T, H, Hkv, dh):
+    """causal=0: every kept query attends to every kept key of its sequence
+    (the lse comes from a non-causal dense forward)."""
+    q, k, v, dO, lse, keep, scale = _case(B, T, H, Hkv, dh, 0.4, "gumbel", seed=5 + T, qk_std=1.2, causal=False)
+    M = B * T
+    idx, cu, nk = gu.compact(keep)
+    Qd, Kd, Vd, dOd = (gu.bf16(a.reshape(M, -1)) for a in (q, k, v, dO))
+    dQ = torch.full((M, H * dh), float("nan"), dtype=torch.bfloat16, device=gu.DEV)
+    dK = torch.full((M, Hkv * dh), float("nan"), dtype=torch.bfloat16, device=gu.DEV)
+    dV = torch.full((M, Hkv * dh), float("nan"), dtype=torch.bfloat16, device=gu.DEV)
+    ws = torch.empty(cl.collider_attn_workspace_size(B, T, H, Hkv, dh), dtype=torch.uint8, device=gu.DEV)
+    cl.collider_attn_bwd(B, T, H, Hkv, dh, 0, scale, dh, 10000.0, Qd, Kd, Vd, None, dOd, H * dh, Hkv * dh,
+                         H * dh, cl.ROWS_FULL, gu.f32(lse), idx, cu, nk, dQ, dK, dV, cl.ROWS_FULL, ws)
+    cl.collider_check()
+    rq, rk, rv = filtered_attention_backward(q, k, v, dO, lse, keep, scale, causal=False)
+    pos = np.tile(np.arange(T), B)
+    rq = ops.rope_backward(rq, pos, dh, 10000.0)
+    rk = ops.rope_backward(rk, pos, dh, 10000.0)
+    for got, ref, nh in ((dQ, rq, H), (dK, rk, Hkv), (dV, rv, Hkv)):
+        g = gu.host(got).reshape(M, nh, dh)
+        assert np.all(g[keep.reshape(-1) == 0] == 0)
+        assert gu.rel_err(g, ref) <= 2e-2

@@ -4,11 +4,15 @@ step).
 
 Single blocks (TinyLlama-, Qwen2.5- and Phi-1.5-shaped) are compared with the
 fp64 oracle element by element over every output tensor.  The 22-block stack
-at 8192 tokens is too large for the oracle as a whole: its LM head, final norm
-and last block are checked against the oracle, the rest by properties that hold
-at any size (finite, filtered rows zero, reproducible weight gradients,
-embedding rows only at kept token ids).
+at 8192 tokens is compared whole: the oracle's stack backward runs from the
+loss down through every block to the embedding gradient, on the same saved
+activations (a plain torch bf16 forward on the GPU, independent of the library),
+and every block's weight gradients, the final norm's, the LM head's and dE are
+compared element by element.  The oracle's attention loop is spread over a
+spawned process pool so the comparison takes minutes, not an hour.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -16,6 +20,7 @@ import torch
 import workloads
 from oracle import block as ob
 from oracle import ops
+from oracle import stack as ost
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -82,6 +87,45 @@ def _gpu_stack_forward(st, t):
     return blocks, Ws, x, rstd, y, z, nf, wlm
 
 
+class _SavedFromDevice:
+    """The stack's saved sets, copied to the host one block at a time when the
+    oracle asks for them (the oracle's stack backward indexes each block once)."""
+
+    def __init__(self, blocks):
+        self.blocks = blocks
+
+    def __getitem__(self, l):
+        sv = {k: gu.host(v) for k, v in self.blocks[l].items()}
+        sv["gu"] = sv.pop("up")       # the oracle names the saved [gate | up] projection "gu"
+        return sv
+
+    def __len__(self):
+        return len(self.blocks)
+
+
+def _oracle_pool():
+    """Spawned worker processes for the oracle's (sequence, head) loop, one
+    BLAS thread each, as many as the host's cores and memory allow (a worker
+    holds a few 8192 x 8192 fp64 arrays at a time)."""
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0))
+    try:
+        avail_gb = int([l for l in open("/proc/meminfo") if l.startswith("MemAvailable")][0].split()[1]) / 2**20
+    except (OSError, IndexError, ValueError):
+        avail_gb = 32.0
+    n = int(max(1, min(cores, 16, (avail_gb - 24) // 4)))
+    saved = {k: os.environ.get(k) for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")}
+    os.environ.update({k: "1" for k in saved})
+    try:
+        return mp.get_context("spawn").Pool(n)
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
 def test_full_size_stack():
     st = workloads.WORKLOADS["tinyllama_stack"]
     ls = st.layer
@@ -118,34 +162,32 @@ def test_full_size_stack():
     dlm1, dnf1, dE1, g1 = run()
     dlm2, dnf2, dE2, g2 = run()
     km = t["keep"].reshape(-1) != 0
-    # properties at full size
     for a in [dlm1, dnf1, dE1] + [v for g in g1 for v in g.values()]:
         assert np.all(np.isfinite(a))
-    # bit-reproducible where no attention reduce-add lies upstream: the LM
-    # head, the final norm and the MLP / output projection of the last block;
-    # below that the f32 reduce order of dQ, dK, dV varies run to run
-    assert np.array_equal(dlm1, dlm2) and np.array_equal(dnf1, dnf2)
-    for k in ("dw_down", "dw_up", "dnorm2_w", "dw_o"):
-        assert np.array_equal(g1[-1][k], g2[-1][k]), k
-    for l, (la, lb) in enumerate(zip(g1, g2)):
-        for k in la:
-            e = gu.rel_err(la[k], lb[k])
-            assert e <= 5e-2, (l, k, e)
     seen = set(np.flatnonzero(np.abs(dE1).sum(1)).tolist())
     assert seen <= set(t["ids"][km].tolist())
 
-    # the oracle on the LM head, final norm and last block
-    zk = gu.host(z)
-    dz = ops.ce_backward(zk, t["targets"], km)
-    yk = np.where(km[:, None], gu.host(y), 0.0)
-    assert gu.rel_err(dlm1, yk.T @ dz) <= 2e-2
-    dy = dz @ gu.host(wlm).T
-    dx22, dnf_ref = ops.rmsnorm_backward(dy, np.where(km[:, None], gu.host(xL), 0.0),
-                                         np.where(km, gu.host(rstdf), 0.0), gu.host(nf))
-    assert gu.rel_err(dnf1, dnf_ref) <= 2e-2
-    last = {k: gu.host(v) for k, v in blocks[-1].items()}
-    last["gu"] = last.pop("up")       # the oracle names the saved [gate | up] projection "gu"
-    wl = {k: v.astype(np.float64) for k, v in t["layers"][-1].items()}
-    ref = ob.block_backward(dx22, last, wl, ls, t["keep"])
-    for k in ("dw_down", "dw_up", "dnorm2_w", "dw_o", "dw_qkv", "dnorm1_w"):
-        assert gu.rel_err(g1[-1][k], ref[k]) <= 2e-2, k
+    # the oracle: the whole stack, chained from the loss with its own gradients
+    errs = {}
+
+    def on_block(l, ref):
+        for k in g1[l]:
+            errs[(l, k)] = gu.rel_err(g1[l][k], ref[k])
+
+    saved = dict(blocks=_SavedFromDevice(blocks), xL=gu.host(xL), rstdf=gu.host(rstdf), y=gu.host(y))
+    with _oracle_pool() as pool:
+        ref = ost.stack_backward(gu.host(z), t["targets"], t["ids"], saved, t["layers"], t["normf_w"], t["w_lm"],
+                                 ls, V, t["keep"], pool=pool, on_block=on_block)
+    errs[("head", "dw_lm")] = gu.rel_err(dlm1, ref["dw_lm"])
+    errs[("head", "dnormf_w")] = gu.rel_err(dnf1, ref["dnormf_w"])
+    errs[("embed", "dE")] = gu.rel_err(dE1, ref["dE"])
+    assert len(errs) == 6 * L + 3
+    worst = max(errs.items(), key=lambda kv: kv[1])
+    print(f"full-size stack: worst max|err|/max|ref| = {worst[1]:.3e} at {worst[0]}")
+    bad = {k: v for k, v in errs.items() if v > 2e-2}
+    assert not bad, bad
+    # run to run: every reduction of the path has a fixed order
+    assert np.array_equal(dlm1, dlm2) and np.array_equal(dnf1, dnf2) and np.array_equal(dE1, dE2)
+    for l, (la, lb) in enumerate(zip(g1, g2)):
+        for k in la:
+            assert np.array_equal(la[k], lb[k]), (l, k)

@@ -105,13 +105,16 @@ def test_block_nan_poison_and_determinism():
     Lb = gu.DeviceLayer(s, w, bad)
     Lb.run(gu.bf16(d2), idx, cu, nk)
     b = Lb.results()
-    for k in a:
-        assert np.all(np.isfinite(b[k])), k
-        if k != "dx":
-            # weight gradients do not depend on dQ's atomic summation order only through dx
-            pass
-    for k in ("dw_down", "dw_up", "dnorm2_w", "dw_o"):
-        assert np.array_equal(a[k], a2[k]) and np.array_equal(a[k], b[k]), k
+    cl.collider_check()
+    # NaN / Inf in filtered rows reaches no output: every output of the
+    # poisoned run matches the oracle (which saw the clean inputs) and is
+    # bit-identical to the clean run, filtered rows of dx included
+    assert set(b) == set(ref) == set(a)
+    for k in ref:
+        assert gu.rel_err(b[k], ref[k]) <= 2e-2, (k, gu.rel_err(b[k], ref[k]))
+        assert np.array_equal(a[k], a2[k]), k
+        assert np.array_equal(a[k], b[k]), k
+    assert np.all(b["dx"][km] == 0)
 
 
 def test_small_stack():

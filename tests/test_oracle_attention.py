@@ -140,3 +140,19 @@ def test_fig3_ablation_leaves_gv_dense():
     filt = keep.reshape(-1) == 0
     assert np.all(np.abs(dv[filt]).max(axis=(1, 2)) > 0)      # G_V no longer sparse
     assert np.all(dvf[filt] == 0)
+
+
+def test_process_pool_gives_the_sequential_result():
+    """Spreading the (sequence, head) loop over a spawned process pool (as the
+    full-size stack comparison does) sums the same terms in the same order."""
+    import multiprocessing as mp
+    rng = np.random.default_rng(3)
+    B, T, H, Hkv, dh = 2, 24, 4, 2, 8
+    q, k, v, dO = (rng.normal(size=(B * T, n, dh)) for n in (H, Hkv, Hkv, H))
+    keep = (rng.random((B, T)) > 0.4).astype(np.uint8)
+    _, lse = attention_forward(q, k, v, B, T, 0.35)
+    seq = filtered_attention_backward(q, k, v, dO, lse, keep, 0.35)
+    with mp.get_context("spawn").Pool(2) as pool:
+        par = filtered_attention_backward(q, k, v, dO, lse, keep, 0.35, pool=pool)
+    for a, b in zip(seq, par):
+        assert np.allclose(a, b, rtol=1e-13, atol=1e-13)

@@ -225,3 +225,32 @@ def test_stack_invariants():
     g0 = ost.stack_backward(z, t["targets"], t["ids"], saved, layers, t["normf_w"], w_lm, ls, st.V,
                             np.zeros_like(keep))
     assert np.all(g0["dw_lm"] == 0) and np.all(g0["dE"] == 0)
+
+
+def test_stack_streamed_blocks_and_pool_give_the_same_gradients():
+    """The full-size stack comparison hands the oracle its saved sets one block
+    at a time, takes each block's gradients through on_block, and spreads the
+    attention loop over a spawned pool; none of that changes the result."""
+    import multiprocessing as mp
+    st = STACK
+    ls = st.layer
+    t, layers, E, w_lm, keep = _stack_case(st)
+    z, saved = ost.stack_forward(t["ids"], E, layers, t["normf_w"], w_lm, ls, round_saved=True)
+    g = ost.stack_backward(z, t["targets"], t["ids"], saved, layers, t["normf_w"], w_lm, ls, st.V, keep)
+    asked = []
+
+    class Lazy:
+        def __getitem__(self, l):
+            asked.append(l)
+            return saved["blocks"][l]
+
+    got = {}
+    with mp.get_context("spawn").Pool(2) as pool:
+        g2 = ost.stack_backward(z, t["targets"], t["ids"], dict(saved, blocks=Lazy()), layers, t["normf_w"],
+                                w_lm, ls, st.V, keep, pool=pool, on_block=lambda l, gb: got.setdefault(l, gb))
+    assert asked == list(reversed(range(st.L)))
+    for k in ("dw_lm", "dnormf_w", "dE", "dx0"):
+        assert _rel(g[k], g2[k]) < 1e-13, k
+    for l in range(st.L):
+        for k, v in g["blocks"][l].items():
+            assert _rel(v, got[l][k]) < 1e-13, (l, k)
