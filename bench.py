@@ -170,8 +170,9 @@ class Block:
         x = torch.from_numpy(tn["x"]).to(dev).bfloat16()
         self.x = x
         self.dout = torch.from_numpy(tn["dout"]).to(dev).bfloat16()
-        self.masks = {"filtered": torch.from_numpy(tn["keep"]).to(dev),
-                      "unfiltered": torch.ones(s.B, s.T, dtype=torch.uint8, device=dev)}
+        # "unfiltered" is the dense backward: the library's NULL-index call,
+        # which reads FULL rows in place (no compaction, gather or scatter)
+        self.masks = {"filtered": torch.from_numpy(tn["keep"]).to(dev), "unfiltered": None}
         self.desc = layer_desc(cl, s)
         self.fwd = NativeForward(cl, s, self.W, self.desc, dev)
         self.fwd.run(x)
@@ -188,10 +189,14 @@ class Block:
         self.nk = torch.empty(1, dtype=torch.int32, device=dev)
 
     def step(self, mask, stream, sv=None, dout=None):
+        """mask None: the unfiltered dense backward (no compaction, NULL index)."""
         cl, s = self.cl, self.s
-        cl.collider_compact(mask, s.B, s.T, self.idx, self.cu, self.nk, None, stream)
+        index = (None, None, None)
+        if mask is not None:
+            cl.collider_compact(mask, s.B, s.T, self.idx, self.cu, self.nk, None, stream)
+            index = (self.idx, self.cu, self.nk)
         cl.collider_layer_bwd(self.desc, self.weights, self.sv if sv is None else sv,
-                              self.dout if dout is None else dout, cl.ROWS_FULL, self.idx, self.cu, self.nk,
+                              self.dout if dout is None else dout, cl.ROWS_FULL, *index,
                               self.grads, cl.ROWS_FULL, self.ws, stream)
 
 
@@ -207,7 +212,7 @@ class Stack:
         t = workloads.stack_tensors(st)
         self.keep_np = t["keep"]
         self.mask = torch.from_numpy(t["keep"]).to(dev)
-        self.mask_all = torch.ones_like(self.mask)
+        self.mask_all = None   # the unfiltered dense backward: the NULL-index call
         E = torch.from_numpy(t["E"]).to(dev).bfloat16()
         ids = torch.from_numpy(t["ids"].astype(np.int64)).to(dev)
         x = E[ids]
@@ -248,11 +253,15 @@ class Stack:
         self.nk = torch.empty(1, dtype=torch.int32, device=dev)
 
     def step(self, mask, stream):
+        """mask None: the unfiltered dense backward (no compaction, NULL index)."""
         cl, st = self.cl, self.st
         ls = st.layer
-        cl.collider_compact(mask, ls.B, ls.T, self.idx, self.cu, self.nk, None, stream)
+        index = (None, None, None)
+        if mask is not None:
+            cl.collider_compact(mask, ls.B, ls.T, self.idx, self.cu, self.nk, None, stream)
+            index = (self.idx, self.cu, self.nk)
         cl.collider_stack_bwd(self.desc, st.L, st.V, self.Wc, self.Sc, self.z, self.targets, self.ids, self.y,
-                              self.xL, self.rstdf, self.nf, self.wlm, self.idx, self.cu, self.nk, self.Gc, self.dnf,
+                              self.xL, self.rstdf, self.nf, self.wlm, *index, self.Gc, self.dnf,
                               self.dlm, self.dE, self.ws, stream)
 
 

@@ -219,7 +219,9 @@ collider_status collider_linear_bwd(collider_dtype dtype, int M, int K, int N,
  * out_rows.  rotary_dim > 0 additionally applies the RoPE backward
  * (rotate-half pairing on the first rotary_dim dims, angle pos*base^(-2i/r))
  * to dQ and dK so they are gradients with respect to the pre-rotation q, k.
- * dh in {64, 128}; H % Hkv == 0.  Workspace: collider_attn_workspace_size(). */
+ * dh in {64, 128}; H % Hkv == 0.  Bit-identical from run to run: dQ tiles
+ * are added in key-block order, each dK / dV tile gets at most two additions.
+ * Workspace: collider_attn_workspace_size(). */
 size_t collider_attn_workspace_size(int B, int T, int H, int Hkv, int dh);
 collider_status collider_attn_bwd(int B, int T, int H, int Hkv, int dh, int causal, float scale,
                                   int rotary_dim, float rope_base,
@@ -307,8 +309,18 @@ typedef struct {
  * -> every gradient of the block.  Gathers the kept rows of the saved set,
  * runs the dimension-reduced GEMMs, the filtered attention backward, the
  * norm/activation/RoPE backward and the bias/norm-weight column sums on
- * kept rows only.  Deterministic except dQ (accumulated with f32 atomics
- * inside the attention backward).  Workspace: collider_layer_workspace_size. */
+ * kept rows only.  Every output is bit-identical from run to run: each
+ * weight-gradient tile has one owner with a fixed reduction order, column
+ * sums reduce fixed partials in a fixed order, and inside the attention
+ * backward dQ tiles are added in key-block order and dK / dV get at most two
+ * additions each.
+ * idx, cu_kept and n_kept all NULL: every token is kept, and this is the
+ * unfiltered dense backward (the baseline the filtered one is measured
+ * against): dOut and the saved rows are read where they are, nothing is
+ * gathered, dx is written in place (dout_rows / dx_rows do not matter, the
+ * COMPACT rows being the FULL rows); the library writes the identity index
+ * into its workspace for the kernels that read one.  Giving only some of the
+ * three is COLLIDER_ERR_INVALID_ARG.  Workspace: collider_layer_workspace_size. */
 size_t collider_layer_workspace_size(const collider_layer_desc* desc);
 collider_status collider_layer_bwd(const collider_layer_desc* desc,
                                    const collider_layer_weights* w,
@@ -398,7 +410,10 @@ collider_status collider_layer_fwd(const collider_layer_desc* desc, const collid
  * in grads[l] (grads[l].dx is not used: gradients between blocks stay in the
  * workspace, COMPACT), dnormf_w f32 [D], dw_lm f32 [D,V], dE f32 [V,D] (rows
  * of token ids never seen at a kept position are 0).  LLAMA blocks, D <= 2048,
- * V % 8 == 0.  Workspace: collider_stack_workspace_size. */
+ * V % 8 == 0.  idx, cu_kept and n_kept all NULL: every token is kept -- the
+ * unfiltered dense backward, as for collider_layer_bwd (the saved rows and y
+ * are read in place, nothing is gathered).  Workspace:
+ * collider_stack_workspace_size. */
 size_t collider_stack_workspace_size(const collider_layer_desc* desc, int L, int V);
 collider_status collider_stack_bwd(const collider_layer_desc* desc, int L, int V,
                                    const collider_layer_weights* w,

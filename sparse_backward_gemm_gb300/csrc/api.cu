@@ -451,6 +451,7 @@ struct AttnScratch {
   float* Dvec;
   float* lse2;
   float2* rope;
+  int* order;   // work-item ticket + the dQ accumulation turn of every (sequence, head, query block)
 };
 void attn_carve(Carver& cv, int B, int T, int H, int Hkv, int dh, AttnScratch* a) {
   const size_t M = (size_t)B * T;
@@ -460,6 +461,7 @@ void attn_carve(Carver& cv, int B, int T, int H, int Hkv, int dh, AttnScratch* a
   a->Dvec = cv.take<float>(M * H);
   a->lse2 = cv.take<float>(M * H);
   a->rope = cv.take<float2>((size_t)T * (dh / 2));
+  a->order = cv.take<int>(attn_order_ints(B, T, H));
 }
 }  // namespace
 
@@ -518,7 +520,7 @@ extern "C" collider_status collider_attn_bwd(int B, int T, int H, int Hkv, int d
   a.rotary_dim = rotary_dim; a.rope_base = rope_base;
   a.lse = lse; a.idx = idx; a.cu_kept = cu_kept; a.n_kept = n_kept;
   a.dq_acc = sc.dq_acc; a.Dvec = sc.Dvec; a.lse_k = sc.lse2; a.rope = sc.rope; a.M = M;
-  a.dk_acc = sc.dk_acc; a.dv_acc = sc.dv_acc;
+  a.dk_acc = sc.dk_acc; a.dv_acc = sc.dv_acc; a.order = sc.order;
   a.in_cap = in_rows == COLLIDER_ROWS_FULL ? Mp : M;
   a.cap = out_rows == COLLIDER_ROWS_FULL ? Mp : M;
   if (in_rows == COLLIDER_ROWS_FULL) {
@@ -572,10 +574,13 @@ struct LayerBufs {
   float *db_k, *da_k;
   float* norm_part;
   float* col_part;
-  float* sk_partial;
+  float* sk_partial;     // stream-K scratch of the input-gradient chain's GEMMs
   int* sk_counters;
+  float* sk_partial_w;   // and of the weight-gradient GEMMs (side stream, concurrent)
+  int* sk_counters_w;
   long long sk_cap;
   AttnScratch at;
+  int32_t *id_idx, *id_cu, *id_nk;   // the identity index of a dense (every token kept) call
 };
 
 collider_status check_desc(const collider_layer_desc* d) {
@@ -625,6 +630,11 @@ void layer_carve(Carver& cv, const collider_layer_desc* d, LayerBufs* L) {
   const long long mmax = std::max<long long>((long long)Mp, std::max(D, F));
   L->sk_cap = sk_counter_cap(mmax, std::max<long long>(std::max(Nqkv, Nup), std::max(D, F)));
   L->sk_counters = cv.take<int>(L->sk_cap);
+  L->sk_partial_w = cv.take<float>(kSkPartialFloats);
+  L->sk_counters_w = cv.take<int>(L->sk_cap);
+  L->id_idx = cv.take<int32_t>((size_t)d->B * d->T);
+  L->id_cu = cv.take<int32_t>((size_t)d->B + 1);
+  L->id_nk = cv.take<int32_t>(1);
 }
 
 // The weight-gradient GEMMs of a block depend on nothing the block computes
@@ -700,22 +710,26 @@ cudaError_t join_side(const Ctx& c, Side* S, int k) {
   return e == cudaSuccess ? cudaStreamWaitEvent(c.stream, S->ev[k], 0) : e;
 }
 
-// stream-K scratch shared by the GEMMs of one call (they run in stream order)
+// stream-K scratch shared by the GEMMs of one call that run in stream order:
+// one set for the input-gradient chain, one for the weight-gradient GEMMs
+// (which run concurrently with it on the side stream)
 thread_local float* g_sk_partial = nullptr;
 thread_local int* g_sk_counters = nullptr;
+thread_local float* g_sk_partial_w = nullptr;
+thread_local int* g_sk_counters_w = nullptr;
 thread_local long long g_sk_cap = 0;
 
 // C (bf16 or f32, COMPACT [Mk, N]) = A_k [Mk, K] . W^T with W stored [N, K]
 // (epi: a fused activation backward, reading FULL rows of aux through idx)
 cudaError_t gemm_dx(const Ctx& c, int M, int N, int K, const void* A, const void* W, void* C, int c_bf16,
                     int accumulate, const int32_t* n_kept, int epi = kEpiStore, const void* aux = nullptr,
-                    const int32_t* idx = nullptr) {
+                    const int32_t* idx = nullptr, long long a_rows = -1) {
   TcGemm g{};
   g.partial = g_sk_partial; g.counters = g_sk_counters; g.counter_cap = g_sk_cap;
   g.epi = epi; g.aux = static_cast<const __nv_bfloat16*>(aux); g.idx = idx; g.aux_rows = M;
   g.aux_ld = epi == kEpiSwiGLU ? 2LL * N : N;
   g.M = M; g.N = N; g.K = K;
-  g.A = A; g.lda = K; g.a_mn_major = 0; g.a_rows = pad128(M);
+  g.A = A; g.lda = K; g.a_mn_major = 0; g.a_rows = a_rows > 0 ? a_rows : pad128(M);
   g.B = W; g.ldb = K; g.b_mn_major = 0; g.b_rows = N;
   g.C = C; g.ldc = epi == kEpiSwiGLU ? 2LL * N : N; g.c_bf16 = c_bf16; g.accumulate = accumulate; g.zero_pad = 1;
   g.c_rows = pad128(M);
@@ -723,24 +737,29 @@ cudaError_t gemm_dx(const Ctx& c, int M, int N, int K, const void* A, const void
   return launch_tc_gemm(c, g);
 }
 
-// dW [Kin, Nout] f32 = X_k^T dY_k, X_k [Mk, Kin], dY_k [Mk, Nout] (both COMPACT, zero-padded)
-// (runs on the side stream, concurrently with the caller's stream: it must not
-// use the shared stream-K scratch)
+// dW [Kin, Nout] f32 = X_k^T dY_k, X_k [Mk, Kin], dY_k [Mk, Nout] (both COMPACT, zero-padded,
+// or -- a dense call -- the caller's M rows: rows = M, the TMA fills past them with zeros)
+// (runs on the side stream, concurrently with the caller's stream: it uses the
+// weight-gradient GEMMs' own stream-K scratch)
 cudaError_t gemm_dw(const Ctx& c, int M, int Kin, int Nout, const void* Xk, long long ldx, const void* dYk,
-                    long long ldy, float* dW, const int32_t* n_kept) {
+                    long long ldy, float* dW, const int32_t* n_kept, long long rows = -1) {
   TcGemm g{};
+  g.partial = g_sk_partial_w; g.counters = g_sk_counters_w; g.counter_cap = g_sk_cap;
   g.M = Kin; g.N = Nout; g.K = M;
-  g.A = Xk; g.lda = ldx; g.a_mn_major = 1; g.a_rows = pad128(M);
-  g.B = dYk; g.ldb = ldy; g.b_mn_major = 1; g.b_rows = pad128(M);
+  g.A = Xk; g.lda = ldx; g.a_mn_major = 1; g.a_rows = rows > 0 ? rows : pad128(M);
+  g.B = dYk; g.ldb = ldy; g.b_mn_major = 1; g.b_rows = rows > 0 ? rows : pad128(M);
   g.C = dW; g.ldc = Nout; g.c_bf16 = 0;
   g.n_kept = n_kept; g.dyn = 2;
   return launch_tc_gemm(c, g);
 }
 
+// dense: every token is kept (idx, cu_kept, n_kept are the identity index the
+// caller made with launch_identity_index into L.id_*): the saved rows and dOut
+// are read where they are, nothing is gathered, and dx is written in place.
 collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, const collider_layer_weights* w,
                                const collider_layer_saved* sv, const void* dOut, bool dout_full,
                                const int32_t* idx, const int32_t* cu_kept, const int32_t* n_kept,
-                               const collider_layer_grads* g, bool dx_full, LayerBufs& L) {
+                               const collider_layer_grads* g, bool dx_full, LayerBufs& L, bool dense = false) {
   // c: the context of the input-gradient chain (the high-priority stream when
   // the side stream is on, else the caller's)
   Ctx c = c_in;
@@ -759,13 +778,34 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
   const int Hd = H * dh, Nqkv = (H + 2 * Hkv) * dh;
   const bool llama = d->arch == COLLIDER_ARCH_LLAMA;
   const int Nup = llama ? 2 * F : F;
+  // (the stream-K counters were zeroed by the entry point; kernels leave them zero)
   g_sk_partial = L.sk_partial;
   g_sk_counters = L.sk_counters;
+  g_sk_partial_w = L.sk_partial_w;
+  g_sk_counters_w = L.sk_counters_w;
   g_sk_cap = L.sk_cap;
-  CK(cudaMemsetAsync(L.sk_counters, 0, L.sk_cap * sizeof(int), c.stream));
 
+  // row extent of the GEMM / attention operands: COMPACT buffers are padded
+  // to whole 128-row tiles; a dense call reads the caller's M rows in place
+  const long long in_rows = dense ? (long long)M : pad128(M);
+  using bfp = __nv_bfloat16*;
+  if (dense) {
+    L.dout_k = bfp(dOut);
+    L.b_k = llama ? bfp(sv->b) : nullptr;
+    L.o_k = bfp(sv->o);
+    L.a_k = bfp(sv->a);
+    L.qkv_k = bfp(sv->qkv);
+    if (llama) {
+      L.s_k = bfp(sv->s);
+    } else {
+      // not a gather: gelu(f1) of every row, which the GEMM needs as an operand
+      GatherJob j{static_cast<const char*>(sv->up), reinterpret_cast<char*>(L.s_k), (long long)F * 2,
+                  (long long)F * 2, F * 2, 1};
+      CK(launch_gather(c, &j, 1, M, pad128(M), nullptr, n_kept));
+    }
+  }
   // 1. gather the kept rows of dOut and of the saved GEMM operands
-  {
+  if (!dense) {
     GatherJob j[6];
     int n = 0;
     j[n++] = GatherJob{static_cast<const char*>(dOut), reinterpret_cast<char*>(L.dout_k), (long long)D * 2,
@@ -797,12 +837,13 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
   const __nv_bfloat16* dres = L.dout_k;   // gradient flowing along the residual into the attention half
   if (llama) {
     CK(fork_side(c, side, 0));
-    CK(gemm_dw(cs, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept));              // dW_down = s^T dOut
-    CK(gemm_dx(c, M, F, D, L.dout_k, w->w_down, L.ds_k, 1, 0, n_kept));               // ds = dOut W_down^T
+    CK(gemm_dw(cs, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept, in_rows));     // dW_down = s^T dOut
+    CK(gemm_dx(c, M, F, D, L.dout_k, w->w_down, L.ds_k, 1, 0, n_kept, kEpiStore, nullptr, nullptr,
+               in_rows));                                                              // ds = dOut W_down^T
     CK(launch_swiglu_bwd(c, L.ds_k, 1, F, static_cast<const __nv_bfloat16*>(sv->up), L.dgu_k, M, pad128(M), idx,
                          n_kept));
     CK(fork_side(c, side, 1));
-    CK(gemm_dw(cs, M, D, Nup, L.b_k, D, L.dgu_k, Nup, g->dw_up, n_kept));             // dW_up = b^T dgu
+    CK(gemm_dw(cs, M, D, Nup, L.b_k, D, L.dgu_k, Nup, g->dw_up, n_kept, in_rows));    // dW_up = b^T dgu
     CK(gemm_dx(c, M, D, Nup, L.dgu_k, w->w_up, L.db_k, 0, 0, n_kept));                // db = dgu W_up^T
     NormBwdArgs nb{};
     nb.layer_norm = 0; nb.M = M; nb.D = D;
@@ -814,14 +855,15 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
     dres = L.dh_k;
   } else {
     CK(fork_side(c, side, 0));
-    CK(gemm_dw(cs, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept));              // dW2 = gelu(f1)^T dOut
-    CK(gemm_dx(c, M, F, D, L.dout_k, w->w_down, L.ds_k, 1, 0, n_kept));               // df2 = dOut W2^T
+    CK(gemm_dw(cs, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept, in_rows));     // dW2 = gelu(f1)^T dOut
+    CK(gemm_dx(c, M, F, D, L.dout_k, w->w_down, L.ds_k, 1, 0, n_kept, kEpiStore, nullptr, nullptr,
+               in_rows));                                                              // df2 = dOut W2^T
     if (d->mlp_bias && g->db_down)
       CK(launch_colsum(c, L.dout_k, 1, D, M, D, nullptr, n_kept, L.col_part, g->db_down));
     CK(launch_gelu_bwd(c, L.ds_k, 1, F, static_cast<const __nv_bfloat16*>(sv->up), L.dgu_k, M, pad128(M), idx,
                        n_kept));
     CK(fork_side(c, side, 1));
-    CK(gemm_dw(cs, M, D, F, L.a_k, D, L.dgu_k, F, g->dw_up, n_kept));                 // dW1 = a^T df1
+    CK(gemm_dw(cs, M, D, F, L.a_k, D, L.dgu_k, F, g->dw_up, n_kept, in_rows));        // dW1 = a^T df1
     if (d->mlp_bias && g->db_up)
       CK(launch_colsum(c, L.dgu_k, 1, F, M, F, nullptr, n_kept, L.col_part, g->db_up));
     CK(gemm_dx(c, M, D, F, L.dgu_k, w->w_up, L.da_k, 0, 0, n_kept));                  // da = df1 W1^T
@@ -829,8 +871,9 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
 
   // 3. attention output projection
   CK(fork_side(c, side, 2));
-  CK(gemm_dw(cs, M, Hd, D, L.o_k, Hd, dres, D, g->dw_o, n_kept));                     // dW_o = o^T dh
-  CK(gemm_dx(c, M, Hd, D, dres, w->w_o, L.do_k, 1, 0, n_kept));                       // do = dh W_o^T
+  CK(gemm_dw(cs, M, Hd, D, L.o_k, Hd, dres, D, g->dw_o, n_kept, in_rows));            // dW_o = o^T dh
+  CK(gemm_dx(c, M, Hd, D, dres, w->w_o, L.do_k, 1, 0, n_kept, kEpiStore, nullptr, nullptr,
+             in_rows));                                                                // do = dh W_o^T
   if (d->out_bias && g->db_o) CK(launch_colsum(c, dres, 1, D, M, D, nullptr, n_kept, L.col_part, g->db_o));
 
   // 4. filtered attention backward (+ RoPE backward) straight into dqkv_k
@@ -845,19 +888,20 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
     a.dq = L.dqkv_k; a.dk = L.dqkv_k + Hd; a.dv = L.dqkv_k + Hd + Hkv * dh;
     a.dq_ld = Nqkv; a.dkv_ld = Nqkv;
     a.dq_acc = L.at.dq_acc; a.Dvec = L.at.Dvec; a.lse_k = L.at.lse2; a.rope = L.at.rope; a.M = M;
-    a.dk_acc = L.at.dk_acc; a.dv_acc = L.at.dv_acc; a.in_cap = pad128(M);
+    a.dk_acc = L.at.dk_acc; a.dv_acc = L.at.dv_acc; a.order = L.at.order; a.in_cap = in_rows;
     a.cap = pad128(M);
     CK(launch_attn_bwd(c, a));
   }
 
   // 5. QKV projection
   CK(fork_side(c, side, 3));
-  CK(gemm_dw(cs, M, D, Nqkv, L.a_k, D, L.dqkv_k, Nqkv, g->dw_qkv, n_kept));          // dW_qkv = a^T dqkv
+  CK(gemm_dw(cs, M, D, Nqkv, L.a_k, D, L.dqkv_k, Nqkv, g->dw_qkv, n_kept, in_rows)); // dW_qkv = a^T dqkv
   if (d->qkv_bias && g->db_qkv)
     CK(launch_colsum(cs, L.dqkv_k, 1, Nqkv, M, Nqkv, nullptr, n_kept, L.col_part, g->db_qkv));
   CK(gemm_dx(c, M, D, Nqkv, L.dqkv_k, w->w_qkv, L.da_k, 0, llama ? 0 : 1, n_kept));  // da (+)= dqkv W_qkv^T
 
   // 6. input norm backward + residual, then back to FULL rows if asked
+  if (dense) dx_full = false;   // every token kept: the COMPACT rows are the FULL rows
   __nv_bfloat16* dxk = dx_full ? L.dx_k : static_cast<__nv_bfloat16*>(g->dx);
   {
     NormBwdArgs nb{};
@@ -915,8 +959,10 @@ extern "C" collider_status collider_layer_bwd(const collider_layer_desc* d, cons
                                               collider_rows dx_rows, void* ws, size_t ws_bytes, void* stream) {
   collider_status s = check_desc(d);
   if (s != COLLIDER_OK) return s;
-  if (!dOut || !idx || !cu_kept || !n_kept || !al16(dOut))
-    return fail(COLLIDER_ERR_INVALID_ARG, "collider_layer_bwd: null or misaligned dOut/idx/cu_kept/n_kept");
+  const bool dense = !idx && !cu_kept && !n_kept;   // every token kept: the unfiltered dense backward
+  if (!dOut || !al16(dOut) || (!dense && (!idx || !cu_kept || !n_kept)))
+    return fail(COLLIDER_ERR_INVALID_ARG,
+                "collider_layer_bwd: null or misaligned dOut, or only some of idx/cu_kept/n_kept given");
   s = check_layer_ptrs(d, w, sv, g, true);
   if (s != COLLIDER_OK) return s;
   const size_t need = collider_layer_workspace_size(d);
@@ -928,6 +974,14 @@ extern "C" collider_status collider_layer_bwd(const collider_layer_desc* d, cons
   Carver cv{static_cast<char*>(ws), ws_bytes, 0, false};
   LayerBufs L;
   layer_carve(cv, d, &L);
+  // stream-K counters start at zero (every GEMM leaves them zero); zeroed here,
+  // on the caller's stream, before any work of this call is forked off it
+  CK(cudaMemsetAsync(L.sk_counters, 0, L.sk_cap * sizeof(int), c.stream));
+  CK(cudaMemsetAsync(L.sk_counters_w, 0, L.sk_cap * sizeof(int), c.stream));
+  if (dense) {
+    CK(launch_identity_index(c, d->B, d->T, L.id_idx, L.id_cu, L.id_nk));
+    return layer_bwd_impl(c, d, w, sv, dOut, true, L.id_idx, L.id_cu, L.id_nk, g, true, L, true);
+  }
   return layer_bwd_impl(c, d, w, sv, dOut, dout_rows == COLLIDER_ROWS_FULL, idx, cu_kept, n_kept, g,
                         dx_rows == COLLIDER_ROWS_FULL, L);
 }
@@ -1125,8 +1179,9 @@ extern "C" collider_status collider_stack_bwd(const collider_layer_desc* d, int 
   if (d->arch != COLLIDER_ARCH_LLAMA) return fail(COLLIDER_ERR_UNSUPPORTED, "collider_stack_bwd: llama blocks only");
   if (nL < 1 || V < 8 || V % 8) return fail(COLLIDER_ERR_INVALID_ARG, "collider_stack_bwd: L >= 1, V % 8 == 0");
   if (d->D > 2048) return fail(COLLIDER_ERR_UNSUPPORTED, "collider_stack_bwd: D <= 2048");
-  if (!w || !sv || !grads || !logits || !targets || !ids || !y || !xL || !rstdf || !normf_w || !w_lm || !idx ||
-      !cu_kept || !n_kept || !dnormf_w || !dw_lm || !dE)
+  const bool dense = !idx && !cu_kept && !n_kept;   // every token kept: the unfiltered dense backward
+  if (!w || !sv || !grads || !logits || !targets || !ids || !y || !xL || !rstdf || !normf_w || !w_lm ||
+      (!dense && (!idx || !cu_kept || !n_kept)) || !dnormf_w || !dw_lm || !dE)
     return fail(COLLIDER_ERR_INVALID_ARG, "collider_stack_bwd: null pointer");
   if (!al16(logits) || !al16(y) || !al16(xL) || !al16(normf_w) || !al16(w_lm) || !al16(dnormf_w) || !al16(dw_lm) ||
       !al16(dE))
@@ -1149,15 +1204,26 @@ extern "C" collider_status collider_stack_bwd(const collider_layer_desc* d, int 
   const int M = d->B * d->T, D = d->D;
   g_sk_partial = LB.sk_partial;
   g_sk_counters = LB.sk_counters;
+  g_sk_partial_w = LB.sk_partial_w;
+  g_sk_counters_w = LB.sk_counters_w;
   g_sk_cap = LB.sk_cap;
   CK(cudaMemsetAsync(LB.sk_counters, 0, LB.sk_cap * sizeof(int), c.stream));
+  CK(cudaMemsetAsync(LB.sk_counters_w, 0, LB.sk_cap * sizeof(int), c.stream));
+  if (dense) {
+    CK(launch_identity_index(c, d->B, d->T, LB.id_idx, LB.id_cu, LB.id_nk));
+    idx = LB.id_idx;
+    cu_kept = LB.id_cu;
+    n_kept = LB.id_nk;
+  }
 
   // LM head: dz = (softmax(z) - onehot) / n_kept on kept rows
   CK(launch_ce_bwd(c, static_cast<const __nv_bfloat16*>(logits), targets, V, M, pad128(M), idx, n_kept, S.dz_k));
-  {
+  const __nv_bfloat16* yk = static_cast<const __nv_bfloat16*>(y);   // a dense call reads y in place
+  if (!dense) {
     GatherJob j{static_cast<const char*>(y), reinterpret_cast<char*>(S.y_k), (long long)D * 2, (long long)D * 2,
                 D * 2, 0};
     CK(launch_gather(c, &j, 1, M, pad128(M), idx, n_kept));
+    yk = S.y_k;
   }
   {
     Ctx cs;
@@ -1165,8 +1231,9 @@ extern "C" collider_status collider_stack_bwd(const collider_layer_desc* d, int 
     s = side_ctx(c, &cs, &side);
     if (s != COLLIDER_OK) return s;
     CK(fork_side(c, side, 5));
-    CK(gemm_dw(cs, M, D, V, S.y_k, D, S.dz_k, V, dw_lm, n_kept));         // dW_lm = y^T dz (side stream;
-  }                                                                        // joined by the last block)
+    CK(gemm_dw(cs, M, D, V, yk, D, S.dz_k, V, dw_lm, n_kept,             // dW_lm = y^T dz (side stream;
+               dense ? (long long)M : -1));                                // joined by the last block)
+  }
   CK(gemm_dx(c, M, D, V, S.dz_k, w_lm, S.dyf_k, 0, 0, n_kept));           // dy = dz W_lm^T
   {
     NormBwdArgs nb{};
@@ -1183,7 +1250,7 @@ extern "C" collider_status collider_stack_bwd(const collider_layer_desc* d, int 
   for (int l = nL - 1; l >= 0; --l) {
     collider_layer_grads gl = grads[l];
     gl.dx = nxt;
-    s = layer_bwd_impl(c, d, &w[l], &sv[l], cur, false, idx, cu_kept, n_kept, &gl, false, LB);
+    s = layer_bwd_impl(c, d, &w[l], &sv[l], cur, false, idx, cu_kept, n_kept, &gl, false, LB, dense);
     if (s != COLLIDER_OK) return s;
     std::swap(cur, nxt);
   }

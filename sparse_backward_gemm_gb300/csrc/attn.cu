@@ -46,6 +46,7 @@ struct AttnK {
   float* Dvec;       // [H, M]
   float* lse2;       // [H, M]  lse * log2(e), kept order
   const float2* rope;  // [T, rot_half] (cos, sin)
+  int* order;        // [1 + B * H * ceil(T / 64)]: work-item ticket, dQ accumulation turns
   int M;
   long long cap;     // row capacity of dq, dk, dv
   DevStatus* st;
@@ -98,6 +99,9 @@ __global__ void attn_prep_kernel(AttnK p, int DH, float rope_base, float2* rope)
       v4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
+  // work-item ticket and dQ turns start at zero
+  const long long nord = (long long)attn_order_ints(p.B, p.T, p.H);
+  for (long long e = tid; e < nord; e += stride) p.order[e] = 0;
   if (p.rot_half > 0) fill_rope_table(p.T, p.rot_half, rope_base, rope, tid, stride);
 }
 
@@ -199,21 +203,28 @@ __global__ void attn_finalize_kernel(AttnK p, int DH) {
 //   warp 0      TMA: K, V once; Q_i, dO_i per iteration (2 stages)
 //   warp 1      TMEM owner; one lane issues the MMAs, per 64-query half g:
 //                 S^T = K Q_g^T, dP^T = V dO_g^T       (M 128 keys, N 64 queries)
-//                 dV += P_g^T dO_g, dK += dS_g^T Q_g   (M 128 keys, N 64)
+//                 dV += P_g^T dO_g, dK += dS_g^T Q_g   (M 128 keys, N 64; A
+//                                                       = P^T, dS^T from TMEM)
 //               and per block dQ = dS K                (M 128 queries, N 64)
 //   warps 2-5   query half 0, warps 6-9 query half 1: one key row and the
 //               half's 64 queries per thread: P^T, dS^T from TMEM -> bf16 ->
-//               shared
+//               back into TMEM over the consumed S^T / dP^T columns; dS^T
+//               also to shared (double-buffered by block) for dQ
 //   warps 10-13 one query row per thread: dQ from TMEM -> shared -> TMA
 //               reduce-add into the f32 dQ accumulator; at the end dK, dV
 //               likewise into their accumulators
-// TMEM columns: half 0 S^T 0-63, dP^T 64-127; half 1 S^T 128-191, dP^T
-// 192-255; dV 256-319, dK 320-383, dQ 384-447.
+// TMEM columns: half 0 S^T 0-63 (P^T in 0-31 once formed), dP^T 64-127
+// (dS^T in 64-95); half 1 S^T 128-191, dP^T 192-255; dV 256-319, dK
+// 320-383, dQ 384-447 and 448-511 (double-buffered by block).
+// P never goes through shared memory and dS has a buffer per block parity,
+// so a softmax half never waits for the previous block's dQ: only for the
+// dQ two blocks back, long done.
 namespace tcattn {
 constexpr int kQ = 128, kK = 128, kD = 64;
 constexpr uint32_t kTile = kQ * kD * 2;                 // 16 KB: 128 rows x 128 bytes
-constexpr uint32_t OFF_K = 0, OFF_V = kTile, OFF_Q = 2 * kTile, OFF_DO = 4 * kTile, OFF_P = 6 * kTile,
-                   OFF_DS = 8 * kTile, OFF_ST = 10 * kTile, OFF_LD = 12 * kTile, OFF_BAR = 12 * kTile + 2048;
+// dS^T buffers: two (block parity), each two halves of one kTile
+constexpr uint32_t OFF_K = 0, OFF_V = kTile, OFF_Q = 2 * kTile, OFF_DO = 4 * kTile, OFF_DS = 6 * kTile,
+                   OFF_ST = 10 * kTile, OFF_LD = 12 * kTile, OFF_BAR = 12 * kTile + 2048;
 constexpr size_t kSmem = 1024 + OFF_BAR + 256;
 constexpr uint32_t TM_S = 0, TM_DV = 256, TM_DK = 320, TM_DQ = 384;
 constexpr int kSoftWarps = 8;                       // two per TMEM lane quadrant
@@ -227,8 +238,46 @@ struct MainTc {
   const float* lse2;
   const float* Dvec;
   long long M;
+  int* order;        // [0]: next work item; then the dQ turn of (sequence, head, query block)
+  int nqb_max;       // query blocks per sequence at most (turn array stride)
   DevStatus* st;
 };
+
+// Work items are taken in ticket order, so an item only ever waits (for its
+// dQ turn) on items that hold smaller tickets: items already running or done.
+__device__ __forceinline__ int take_item(int* ticket) {
+  __shared__ int s_item;
+  if (threadIdx.x == 0) s_item = atomicAdd(ticket, 1);
+  __syncthreads();
+  return s_item;
+}
+
+// Adds this key block's dQ tile of (sequence b, head h, query block ib) into
+// the f32 accumulator in key-block order, so the sum is the same every run:
+// wait until the key blocks before this one (0 .. j-1) have added theirs,
+// then issue the TMA reduce-add(s).  The turn is passed on lazily: the next
+// call (or dq_turn_flush at the end) waits for this add to complete and then
+// releases it, so the issuing thread never stalls on its own add.  A wait
+// that runs out is recorded (COLLIDER_ERR_TIMEOUT) and the chain goes on
+// unordered rather than stall.  One thread; `pending` carries the turn to pass.
+__device__ __forceinline__ void dq_turn_flush(int*& pending, int j) {
+  if (!pending) return;
+  tc::bulk_wait_all();              // the previous add has completed
+  tc::fence_proxy_async_global();
+  tc::release_turn(pending, j + 1);
+  pending = nullptr;
+}
+template <typename Issue>
+__device__ __forceinline__ void ordered_dq_add(const MainTc& p, int b, int h, int ib, int j, bool& broken,
+                                               int*& pending, unsigned site, Issue issue) {
+  dq_turn_flush(pending, j);
+  int* turn = p.order + 1 + ((long long)b * p.H + h) * p.nqb_max + ib;
+  if (!broken && !tc::wait_turn(turn, j, p.st, site)) broken = true;
+  tc::fence_proxy_async_global();
+  issue();
+  tc::bulk_commit();
+  pending = turn;
+}
 
 __global__ void __launch_bounds__(tcattn::kThreads, 1)
     attn_main_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -239,9 +288,10 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
   using namespace tcattn;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int item = take_item(p.order);
   const int per_j = p.B * p.Hkv * p.nhc;
-  const int j = blockIdx.x / per_j;
-  const int rem = blockIdx.x % per_j;
+  const int j = item / per_j;
+  const int rem = item % per_j;
   const int b = rem / (p.Hkv * p.nhc);
   const int hk = (rem / p.nhc) % p.Hkv;
   const int hci = rem % p.nhc;
@@ -254,12 +304,14 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
   const int n_iter = p.hc * nq_head;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-  // [2] = one per query half (sfull, pfull, pempty) or per stage (qfull, qempty, qready)
+  // [2] = one per query half (sfull, pfull), per Q/dO stage (qfull, qempty,
+  // qready), or per block parity (dsempty: the dS^T buffer; dqfull, dqempty:
+  // the dQ accumulator)
   const uint32_t b_kv = smem_u32(bars + 0), b_qfull = smem_u32(bars + 1), b_qempty = smem_u32(bars + 3),
-                 b_sfull = smem_u32(bars + 5), b_pfull = smem_u32(bars + 7), b_pempty = smem_u32(bars + 9),
-                 b_dqfull = smem_u32(bars + 11), b_dqempty = smem_u32(bars + 12), b_kvready = smem_u32(bars + 13),
-                 b_qready = smem_u32(bars + 14);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+                 b_sfull = smem_u32(bars + 5), b_pfull = smem_u32(bars + 7), b_dsempty = smem_u32(bars + 9),
+                 b_dqfull = smem_u32(bars + 11), b_dqempty = smem_u32(bars + 13), b_kvready = smem_u32(bars + 15),
+                 b_qready = smem_u32(bars + 16);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* sL = reinterpret_cast<float*>(sm + OFF_LD);   // [2][128]
   float* sD = sL + 256;                                // [2][128]
@@ -274,10 +326,10 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
     for (int g = 0; g < 2; ++g) {
       mbar_init(b_sfull + 8 * g, 1);
       mbar_init(b_pfull + 8 * g, 16 * kSoftWarps);
-      mbar_init(b_pempty + 8 * g, 1);
+      mbar_init(b_dsempty + 8 * g, 1);
+      mbar_init(b_dqfull + 8 * g, 1);
+      mbar_init(b_dqempty + 8 * g, 128);
     }
-    mbar_init(b_dqfull, 1);
-    mbar_init(b_dqempty, 128);
     mbar_init(b_kvready, 1);
     mbar_init(b_qready, 1);
     mbar_init(b_qready + 8, 1);
@@ -307,8 +359,8 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
     auto issue = [&](int it) -> bool {
       const int st = it & 1, use = it >> 1;
       if (!mbar_wait(b_qempty + 8 * st, (use & 1) ^ 1, abort_flag, p.st, 20)) return false;
-      const int h = hk * p.G + hci * p.hc + it / nq_head;
-      const int i0 = (i_start + it % nq_head) * kQ;
+      const int h = hk * p.G + hci * p.hc + it % p.hc;
+      const int i0 = (nqb - 1 - it / p.hc) * kQ;
       mbar_expect_tx(b_qfull + 8 * st, 2 * kTile);
       tma_load_2d(sbase + OFF_Q + st * kTile, &tmQ, b_qfull + 8 * st, h * kD, s0 + i0);
       tma_load_2d(sbase + OFF_DO + st * kTile, &tmdO, b_qfull + 8 * st, h * kD, s0 + i0);
@@ -341,7 +393,7 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
     for (int it = 0; ok && it < n_iter; ++it) {
       const int st = it & 1, use = it >> 1;
       if (!mbar_wait(b_qfull + 8 * st, use & 1, &no_abort, p.st, 29)) break;
-      const int i0 = (i_start + it % nq_head) * kQ;
+      const int i0 = (nqb - 1 - it / p.hc) * kQ;
       const int qrows = min(kQ, len - i0);
       if (qrows < kQ) {
         zero_rows(OFF_Q + st * kTile, qrows);
@@ -358,10 +410,12 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
       // Query half g of iteration it has its own S^T / dP^T columns in TMEM
-      // (buffer g) and its own P^T / dS^T tile in shared memory, so the MMAs
-      // of one half run while the softmax warps of the other half work:
+      // (buffer g), where its P^T lands too, so the MMAs of one half run while
+      // the softmax warps of the other half work:
       //   S, dP (it, 0) | S, dP (it, 1) | [P(it, 0)] dV, dK (it, 0) | S, dP (it+1, 0)
       //   | [P(it, 1)] dV, dK (it, 1) | dQ (it) | S, dP (it+1, 1) | ...
+      // MMAs issued by this thread run in issue order, so S (it+1, g) cannot
+      // overwrite P (it, g) before dV (it, g) has read it.
       constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);
       constexpr uint32_t id_kv = idesc_bf16(128, 64, false, true);
       constexpr uint32_t id_q = idesc_bf16(128, 64, true, true);
@@ -371,10 +425,9 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       const uint64_t d_k = sdesc(sbase + OFF_K, 16, 1024), d_v = sdesc(sbase + OFF_V, 16, 1024);
       const uint64_t d_kmn = sdesc(sbase + OFF_K, 8192, 1024);            // K as the MN-major B of dQ
       const uint64_t d_ds_mn = sdesc(sbase + OFF_DS, kTile, 1024);        // dS^T as the MN-major A of dQ
-      // per Q/dO stage (1 = the second stage, kTile bytes on); per P/dS half
+      // per Q/dO stage (1 = the second stage, kTile bytes on); per dS buffer and half
       const uint64_t d_q0 = sdesc(sbase + OFF_Q, 16, 1024), d_do0 = sdesc(sbase + OFF_DO, 16, 1024);
       const uint64_t d_qmn0 = sdesc(sbase + OFF_Q, 8192, 1024), d_domn0 = sdesc(sbase + OFF_DO, 8192, 1024);
-      const uint64_t d_p0 = sdesc(sbase + OFF_P, 16, 1024), d_ds0 = sdesc(sbase + OFF_DS, 16, 1024);
       constexpr uint64_t kTileStep = kTile / 16;   // one tile further on, in descriptor units
       auto sdp = [&](int it, int g) {   // S^T, dP^T of half g: M 128 keys, N 64 queries
         const int st = it & 1;
@@ -392,14 +445,16 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
           const int kk = 4 * g + k4;
-          mma_bf16(tbase + TM_DV, d_p0 + g * kTileStep + 2 * k4, d_domn0 + st * kTileStep + 128 * kk, id_kv,
-                   (it > 0) || (kk > 0));
+          // P^T of this half: 64 queries = 32 columns of packed bf16 pairs, 8 per k-step
+          mma_bf16_ts(tbase + TM_DV, tbase + TM_S + g * 128 + 8 * k4, d_domn0 + st * kTileStep + 128 * kk, id_kv,
+                      (it > 0) || (kk > 0));
         }
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
           const int kk = 4 * g + k4;
-          mma_bf16(tbase + TM_DK, d_ds0 + g * kTileStep + 2 * k4, d_qmn0 + st * kTileStep + 128 * kk, id_kv,
-                   (it > 0) || (kk > 0));
+          // dS^T of this half, packed over the first 32 dP^T columns
+          mma_bf16_ts(tbase + TM_DK, tbase + TM_S + g * 128 + 64 + 8 * k4, d_qmn0 + st * kTileStep + 128 * kk,
+                      id_kv, (it > 0) || (kk > 0));
         }
       };
       bool ok = mbar_wait(b_kvready, 0, abort_flag, p.st, 21);
@@ -412,7 +467,7 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
         }
       }
       for (int it = 0; ok && it < n_iter; ++it) {
-        const int st = it & 1;
+        const int st = it & 1, a = it & 1, use = it >> 1;
         const bool more = it + 1 < n_iter;
         if (!mbar_wait(b_pfull, it & 1, abort_flag, p.st, 23)) break;
         fence_after();
@@ -423,16 +478,17 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
           sdp(it + 1, 0);
         }
         if (!mbar_wait(b_pfull + 8, it & 1, abort_flag, p.st, 23)) break;
-        if (it > 0 && !mbar_wait(b_dqempty, (it - 1) & 1, abort_flag, p.st, 24)) break;
         fence_after();
         dvdk(it, 1);
         mma_commit(b_qempty + 8 * st);   // Q, dO of this block are read for the last time
+        // dQ accumulator a was drained of block it-2
+        if (use > 0 && !mbar_wait(b_dqempty + 8 * a, (use - 1) & 1, abort_flag, p.st, 24)) break;
+        fence_after();
 #pragma unroll
         for (int kk = 0; kk < kK / 16; ++kk)     // k = keys; dS read MN-major from the dS^T tiles
-          mma_bf16(tbase + TM_DQ, d_ds_mn + 128 * kk, d_kmn + 128 * kk, id_q, kk > 0);
-        mma_commit(b_dqfull);
-        mma_commit(b_pempty);
-        mma_commit(b_pempty + 8);
+          mma_bf16(tbase + TM_DQ + 64 * a, d_ds_mn + 2 * a * kTileStep + 128 * kk, d_kmn + 128 * kk, id_q, kk > 0);
+        mma_commit(b_dqfull + 8 * a);
+        mma_commit(b_dsempty + 8 * a);   // dS^T buffer a is read for the last time
         if (more) sdp(it + 1, 1);
       }
     }
@@ -451,8 +507,8 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
     // after the current one are fetched one iteration early, so the
     // global-load latency hides behind the current block
     auto fetch = [&](int it) -> float {
-      const int h = hk * p.G + hci * p.hc + it / nq_head;
-      const int i0 = (i_start + it % nq_head) * kQ;
+      const int h = hk * p.G + hci * p.hc + it % p.hc;
+      const int i0 = (nqb - 1 - it / p.hc) * kQ;
       const int qq = 64 * g + (tg & 63);
       if (qq >= min(kQ, len - i0)) return 0.f;
       const float* src = tg < 64 ? p.lse2 : p.Dvec;
@@ -460,7 +516,7 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
     };
     float nxt = n_iter > 0 ? fetch(0) : 0.f;
     for (int it = 0; it < n_iter; ++it) {
-      const int i0 = (i_start + it % nq_head) * kQ;
+      const int i0 = (nqb - 1 - it / p.hc) * kQ;
       const int qrows = min(kQ, len - i0);
       const int buf = it & 1;
       (tg < 64 ? sL : sD)[buf * 128 + 64 * g + (tg & 63)] = nxt;
@@ -507,21 +563,24 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
             dk[e] = pack_bf16x2(dv[0], dv[1]);
           }
         }
-        // the P/dS tile of this half is free once dQ of the previous block is done
-        if (cc == 0 && it > 0 && !mbar_wait(b_pempty + 8 * g, (it - 1) & 1, &no_abort, p.st, 26)) {
+        // P^T and dS^T into TMEM over S^T / dP^T columns this thread has read
+        // already (the chunk cc of 32 queries packs into 16 columns, at 16 cc)
+        tmem_st16(tbase + lane_off + TM_S + g * 128 + 16 * cc, pk);
+        tmem_st16(tbase + lane_off + TM_S + g * 128 + 64 + 16 * cc, dk);
+        // dS^T buffer (it & 1) is free once dQ of block it-2 has read it
+        if (cc == 0 && it >= 2 && !mbar_wait(b_dsempty + 8 * (it & 1), ((it >> 1) - 1) & 1, &no_abort, p.st, 26)) {
           stop = true;
           break;
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const uint32_t phys = (((cc * 4 + u) ^ (kr & 7)) * 16);
-          *reinterpret_cast<uint4*>(sm + OFF_P + rowoff + phys) =
-              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-          *reinterpret_cast<uint4*>(sm + OFF_DS + rowoff + phys) =
+          *reinterpret_cast<uint4*>(sm + OFF_DS + (it & 1) * 2 * kTile + rowoff + phys) =
               make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
         }
       }
       if (stop) break;
+      tmem_wait_st();
       fence_before();
       fence_async_smem();
       mbar_arrive(b_pfull + 8 * g);
@@ -533,17 +592,19 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
     const int r = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t stage = sbase + OFF_ST;
-    bool ok = true;
+    bool ok = true, chain_broken = false;
+    int* dq_pending = nullptr;   // the dQ turn this thread still has to pass on
     for (int it = 0; it < n_iter; ++it) {
-      const int h = hk * p.G + hci * p.hc + it / nq_head;
-      const int i0 = (i_start + it % nq_head) * kQ;
-      if (!mbar_wait(b_dqfull, it & 1, &no_abort, p.st, 27)) { ok = false; break; }
+      const int h = hk * p.G + hci * p.hc + it % p.hc;
+      const int i0 = (nqb - 1 - it / p.hc) * kQ;
+      const int a = it & 1;
+      if (!mbar_wait(b_dqfull + 8 * a, (it >> 1) & 1, &no_abort, p.st, 27)) { ok = false; break; }
       fence_after();
       float v[64];
-      tmem_ld32(tbase + lane_off + TM_DQ, v);
-      tmem_ld32(tbase + lane_off + TM_DQ + 32, v + 32);
+      tmem_ld32(tbase + lane_off + TM_DQ + 64 * a, v);
+      tmem_ld32(tbase + lane_off + TM_DQ + 64 * a + 32, v + 32);
       fence_before();
-      mbar_arrive(b_dqempty);
+      mbar_arrive(b_dqempty + 8 * a);
       if (t == 0) bulk_wait_read_all();
       named_bar(2, 128);
 #pragma unroll
@@ -557,12 +618,13 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
         }
       fence_async_smem();
       named_bar(2, 128);
-      if (t == 0) {
-        tma_reduce_add_2d(&tmdQ, stage, h * kD, s0 + i0);
-        tma_reduce_add_2d(&tmdQ, stage + kTile, h * kD + 32, s0 + i0);
-        bulk_commit();
-      }
+      if (t == 0)
+        ordered_dq_add(p, b, h, i0 / kQ, j, chain_broken, dq_pending, 30, [&] {
+          tma_reduce_add_2d(&tmdQ, stage, h * kD, s0 + i0);
+          tma_reduce_add_2d(&tmdQ, stage + kTile, h * kD + 32, s0 + i0);
+        });
     }
+    if (t == 0) dq_turn_flush(dq_pending, j);   // pass the last turn on, even after a failure
     if (ok) {
       // every MMA has completed (the last dQ commit covers them all): drain dK, dV
 #pragma unroll 1
@@ -611,21 +673,29 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
 //   warp 0      TMA: K, V once; Q_i, dO_i per iteration (2 stages)
 //   warp 1      TMEM owner; one lane issues the MMAs:
 //                 S^T = K Q^T, dP^T = V dO^T          (M 128 keys, N 64 queries)
-//                 dV += P^T dO, dK += dS^T Q          (M 128 keys, N 128)
+//                 dV += P^T dO, dK += dS^T Q          (M 128 keys, N 128; A
+//                                                      = P^T, dS^T from TMEM)
 //                 dQ^T = K^T dS^T                     (M 128 head dims, N 64 queries)
+//               in the order S, dP (it) | dV, dK (it) | S, dP (it+1) | dQ^T (it),
+//               so the softmax of block it+1 overlaps dQ^T of block it
 //   warps 2-9   one key row and 32 of the 64 queries per thread: P^T, dS^T
-//               from TMEM -> bf16 -> shared
+//               from TMEM -> bf16 -> back into TMEM over the consumed S^T /
+//               dP^T columns; dS^T also to shared (double-buffered by block)
+//               for dQ^T
 //   warps 10-13 one head-dim row of dQ^T per thread: TMEM -> shared (as dQ
 //               rows) -> TMA reduce-add into the f32 dQ accumulator; at the
 //               end dK, dV likewise, 64 columns at a time
 // Tiles are 64-column (128-byte) swizzle chunks.
-// TMEM columns: S^T 0-63, dP^T 64-127, dV 128-255, dK 256-383, dQ^T 384-447.
+// TMEM columns: S^T 0-63 (P^T of queries 32 g .. 32 g + 31 in 32 g .. 32 g +
+// 15), dP^T 64-127 (dS^T likewise from 64), dV 128-255, dK 256-383, dQ^T
+// 384-447.
 namespace tcattn128 {
 constexpr int kQ = 64, kK = 128, kD = 128;
 constexpr uint32_t kKChunk = 16384;                 // 128 rows x 128 bytes
 constexpr uint32_t kQChunk = 8192;                  // 64 rows x 128 bytes
+// dS^T: two buffers (block parity) of one kKChunk
 constexpr uint32_t OFF_K = 0, OFF_V = 2 * kKChunk, OFF_Q = 4 * kKChunk, OFF_DO = OFF_Q + 4 * kQChunk,
-                   OFF_P = OFF_DO + 4 * kQChunk, OFF_DS = OFF_P + kKChunk, OFF_ST = OFF_DS + kKChunk,
+                   OFF_DS = OFF_DO + 4 * kQChunk, OFF_ST = OFF_DS + 2 * kKChunk,
                    OFF_LD = OFF_ST + 2 * kKChunk, OFF_BAR = OFF_LD + 1024;
 constexpr size_t kSmem = 1024 + OFF_BAR + 256;
 constexpr uint32_t TM_S = 0, TM_DP = 64, TM_DV = 128, TM_DK = 256, TM_DQ = 384;
@@ -643,9 +713,10 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
   using namespace tcattn128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int item = take_item(p.order);
   const int per_j = p.B * p.Hkv * p.nhc;
-  const int j = blockIdx.x / per_j;
-  const int rem = blockIdx.x % per_j;
+  const int j = item / per_j;
+  const int rem = item % per_j;
   const int b = rem / (p.Hkv * p.nhc);
   const int hk = (rem / p.nhc) % p.Hkv;
   const int hci = rem % p.nhc;
@@ -659,10 +730,10 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   const uint32_t b_kv = smem_u32(bars + 0), b_qfull = smem_u32(bars + 1), b_qempty = smem_u32(bars + 3),
-                 b_sfull = smem_u32(bars + 5), b_pfull = smem_u32(bars + 6), b_pempty = smem_u32(bars + 7),
-                 b_dqfull = smem_u32(bars + 8), b_dqempty = smem_u32(bars + 9), b_kvready = smem_u32(bars + 10),
-                 b_qready = smem_u32(bars + 11);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+                 b_sfull = smem_u32(bars + 5), b_pfull = smem_u32(bars + 6), b_dsempty = smem_u32(bars + 7),
+                 b_dqfull = smem_u32(bars + 9), b_dqempty = smem_u32(bars + 10), b_kvready = smem_u32(bars + 11),
+                 b_qready = smem_u32(bars + 12);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* sL = reinterpret_cast<float*>(sm + OFF_LD);   // [2][64]
   float* sD = sL + 128;                                // [2][64]
@@ -677,7 +748,8 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
     }
     mbar_init(b_sfull, 1);
     mbar_init(b_pfull, 32 * kSoftWarps);
-    mbar_init(b_pempty, 1);
+    mbar_init(b_dsempty, 1);
+    mbar_init(b_dsempty + 8, 1);
     mbar_init(b_dqfull, 1);
     mbar_init(b_dqempty, 128);
     mbar_init(b_kvready, 1);
@@ -706,8 +778,8 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
     auto issue = [&](int it) -> bool {
       const int st = it & 1, use = it >> 1;
       if (!mbar_wait(b_qempty + 8 * st, (use & 1) ^ 1, abort_flag, p.st, 50)) return false;
-      const int h = hk * p.G + hci * p.hc + it / nq_head;
-      const int i0 = (i_start + it % nq_head) * kQ;
+      const int h = hk * p.G + hci * p.hc + it % p.hc;
+      const int i0 = (nqb - 1 - it / p.hc) * kQ;
       mbar_expect_tx(b_qfull + 8 * st, 4 * kQChunk);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -743,7 +815,7 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
     for (int it = 0; ok && it < n_iter; ++it) {
       const int st = it & 1, use = it >> 1;
       if (!mbar_wait(b_qfull + 8 * st, use & 1, &no_abort, p.st, 59)) break;
-      const int i0 = (i_start + it % nq_head) * kQ;
+      const int i0 = (nqb - 1 - it / p.hc) * kQ;
       const int qrows = min(kQ, len - i0);
       if (qrows < kQ)
         for (int c = 0; c < 2; ++c) {
@@ -767,15 +839,11 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
       const uint64_t d_k = sdesc(sbase + OFF_K, 16, 1024), d_v = sdesc(sbase + OFF_V, 16, 1024);
       const uint64_t d_q = sdesc(sbase + OFF_Q, 16, 1024), d_do = sdesc(sbase + OFF_DO, 16, 1024);
       const uint64_t d_qmn = sdesc(sbase + OFF_Q, kQChunk, 1024), d_domn = sdesc(sbase + OFF_DO, kQChunk, 1024);
-      const uint64_t d_p = sdesc(sbase + OFF_P, 16, 1024), d_ds = sdesc(sbase + OFF_DS, 16, 1024);
       const uint64_t d_kmn = sdesc(sbase + OFF_K, kKChunk, 1024);   // K^T: MN-major A, head-dim chunks
-      const uint64_t d_dsmn = sdesc(sbase + OFF_DS, kKChunk, 1024); // dS^T: MN-major B
+      const uint64_t d_dsmn = sdesc(sbase + OFF_DS, kKChunk, 1024); // dS^T: MN-major B (buffer 0)
       constexpr uint64_t kQStep = 2 * kQChunk / 16, kKCh = kKChunk / 16, kQCh = kQChunk / 16;
-      bool ok = mbar_wait(b_kvready, 0, abort_flag, p.st, 51);
-      for (int it = 0; ok && it < n_iter; ++it) {
-        const int st = it & 1, use = it >> 1;
-        if (!mbar_wait(b_qready + 8 * st, use & 1, abort_flag, p.st, 52)) break;
-        fence_after();
+      auto sdp = [&](int it) {   // S^T, dP^T: M 128 keys, N 64 queries
+        const int st = it & 1;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {   // k = head dims: chunk kk / 4, 32 bytes a step inside it
           const uint64_t ko = (kk >> 2) * kKCh + 2 * (kk & 3), qo = st * kQStep + (kk >> 2) * kQCh + 2 * (kk & 3);
@@ -787,21 +855,44 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
           mma_bf16(tbase + TM_DP, d_v + ko, d_do + qo, id_s, kk > 0);
         }
         mma_commit(b_sfull);
+      };
+      bool ok = mbar_wait(b_kvready, 0, abort_flag, p.st, 51);
+      if (ok && n_iter > 0) {
+        ok = mbar_wait(b_qready, 0, abort_flag, p.st, 52);
+        if (ok) {
+          fence_after();
+          sdp(0);
+        }
+      }
+      for (int it = 0; ok && it < n_iter; ++it) {
+        const int st = it & 1, buf = it & 1;
         if (!mbar_wait(b_pfull, it & 1, abort_flag, p.st, 53)) break;
+        fence_after();
+        // P^T / dS^T of queries 16 kk .. 16 kk + 15: 8 packed columns, the
+        // first 16 of each 32-query group's 32
+#pragma unroll
+        for (int kk = 0; kk < kQ / 16; ++kk)     // k = queries, 16 rows (2 KB) a step
+          mma_bf16_ts(tbase + TM_DV, tbase + TM_S + 32 * (kk >> 1) + 8 * (kk & 1),
+                      d_domn + st * kQStep + 128 * kk, id_kv, (it > 0) || (kk > 0));
+#pragma unroll
+        for (int kk = 0; kk < kQ / 16; ++kk)
+          mma_bf16_ts(tbase + TM_DK, tbase + TM_DP + 32 * (kk >> 1) + 8 * (kk & 1),
+                      d_qmn + st * kQStep + 128 * kk, id_kv, (it > 0) || (kk > 0));
+        mma_commit(b_qempty + 8 * st);          // Q, dO of this block are read for the last time
+        // S, dP of the next block overwrite P, dS of this one, which the MMAs
+        // above (issued first, run first) have read
+        if (it + 1 < n_iter) {
+          if (!mbar_wait(b_qready + 8 * ((it + 1) & 1), ((it + 1) >> 1) & 1, abort_flag, p.st, 52)) break;
+          fence_after();
+          sdp(it + 1);
+        }
         if (it > 0 && !mbar_wait(b_dqempty, (it - 1) & 1, abort_flag, p.st, 54)) break;
         fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kQ / 16; ++kk)     // k = queries, 16 rows (2 KB) a step
-          mma_bf16(tbase + TM_DV, d_p + 2 * kk, d_domn + st * kQStep + 128 * kk, id_kv, (it > 0) || (kk > 0));
-#pragma unroll
-        for (int kk = 0; kk < kQ / 16; ++kk)
-          mma_bf16(tbase + TM_DK, d_ds + 2 * kk, d_qmn + st * kQStep + 128 * kk, id_kv, (it > 0) || (kk > 0));
-        mma_commit(b_qempty + 8 * st);          // Q, dO of this block are read for the last time
-#pragma unroll
         for (int kk = 0; kk < kK / 16; ++kk)     // k = keys, 16 rows (2 KB) a step
-          mma_bf16(tbase + TM_DQ, d_kmn + 128 * kk, d_dsmn + 128 * kk, id_q, kk > 0);
+          mma_bf16(tbase + TM_DQ, d_kmn + 128 * kk, d_dsmn + buf * kKCh + 128 * kk, id_q, kk > 0);
         mma_commit(b_dqfull);
-        mma_commit(b_pempty);
+        mma_commit(b_dsempty + 8 * buf);        // dS^T buffer buf is read for the last time
       }
     }
   } else if (warp < 2 + kSoftWarps) {
@@ -817,8 +908,8 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
     // after the current one are fetched one iteration early
     auto fetch = [&](int it) -> float {
       if (tg >= 64) return 0.f;
-      const int h = hk * p.G + hci * p.hc + it / nq_head;
-      const int i0 = (i_start + it % nq_head) * kQ;
+      const int h = hk * p.G + hci * p.hc + it % p.hc;
+      const int i0 = (nqb - 1 - it / p.hc) * kQ;
       const int qq = 32 * g + (tg & 31);
       if (qq >= min(kQ, len - i0)) return 0.f;
       const float* src = tg < 32 ? p.lse2 : p.Dvec;
@@ -826,14 +917,15 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
     };
     float nxt = n_iter > 0 ? fetch(0) : 0.f;
     for (int it = 0; it < n_iter; ++it) {
-      const int i0 = (i_start + it % nq_head) * kQ;
+      const int i0 = (nqb - 1 - it / p.hc) * kQ;
       const int qrows = min(kQ, len - i0);
       const int buf = it & 1;
       if (tg < 64) (tg < 32 ? sL : sD)[buf * 64 + 32 * g + (tg & 31)] = nxt;
       if (it + 1 < n_iter) nxt = fetch(it + 1);
       named_bar(1, 32 * kSoftWarps);
       if (!mbar_wait(b_sfull, it & 1, &no_abort, p.st, 55)) break;
-      if (it > 0 && !mbar_wait(b_pempty, (it - 1) & 1, &no_abort, p.st, 56)) break;
+      // dS^T buffer (it & 1) is free once dQ^T of block it-2 has read it
+      if (it >= 2 && !mbar_wait(b_dsempty + 8 * (it & 1), ((it >> 1) - 1) & 1, &no_abort, p.st, 56)) break;
       fence_after();
       const float* L = sL + buf * 64;
       const float* Dd = sD + buf * 64;
@@ -869,14 +961,17 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
           dk[e] = pack_bf16x2(dv[0], dv[1]);
         }
       }
+      // P^T, dS^T into TMEM over this group's S^T / dP^T columns (read above;
+      // the other group's 32 columns are not touched)
+      tmem_st16(tbase + lane_off + TM_S + 32 * g, pk);
+      tmem_st16(tbase + lane_off + TM_DP + 32 * g, dk);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const uint32_t phys = (((4 * g + u) ^ (kr & 7)) * 16);
-        *reinterpret_cast<uint4*>(sm + OFF_P + kr * 128 + phys) =
-            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-        *reinterpret_cast<uint4*>(sm + OFF_DS + kr * 128 + phys) =
+        *reinterpret_cast<uint4*>(sm + OFF_DS + (it & 1) * kKChunk + kr * 128 + phys) =
             make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
       }
+      tmem_wait_st();
       fence_before();
       fence_async_smem();
       mbar_arrive(b_pfull);
@@ -888,10 +983,11 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
     const int r = q * 32 + lane;                // TMEM lane: head dim (dQ^T) or key (dK, dV)
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t stage = sbase + OFF_ST;
-    bool ok = true;
+    bool ok = true, chain_broken = false;
+    int* dq_pending = nullptr;   // the dQ turn this thread still has to pass on
     for (int it = 0; it < n_iter; ++it) {
-      const int h = hk * p.G + hci * p.hc + it / nq_head;
-      const int i0 = (i_start + it % nq_head) * kQ;
+      const int h = hk * p.G + hci * p.hc + it % p.hc;
+      const int i0 = (nqb - 1 - it / p.hc) * kQ;
       if (!mbar_wait(b_dqfull, it & 1, &no_abort, p.st, 57)) { ok = false; break; }
       fence_after();
       float v[64];                               // dQ[query c][head dim r], c = 0..63
@@ -910,12 +1006,13 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
       }
       fence_async_smem();
       named_bar(2, 128);
-      if (t == 0) {
+      if (t == 0)
+        ordered_dq_add(p, b, h, i0 / kQ, j, chain_broken, dq_pending, 60, [&] {
 #pragma unroll
-        for (int bx = 0; bx < 4; ++bx) tma_reduce_add_2d(&tmdQ, stage + bx * 8192, h * kD + 32 * bx, s0 + i0);
-        bulk_commit();
-      }
+          for (int bx = 0; bx < 4; ++bx) tma_reduce_add_2d(&tmdQ, stage + bx * 8192, h * kD + 32 * bx, s0 + i0);
+        });
     }
+    if (t == 0) dq_turn_flush(dq_pending, j);   // pass the last turn on, even after a failure
     if (ok) {
       // every MMA has completed (the last dQ commit covers them all): drain
       // dK, dV 64 columns at a time through two [128 x 32] f32 boxes
@@ -969,9 +1066,12 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
 //              buffers, so the next S overlaps the softmax of this one) and
 //              O'_h += P V_j
 //   warps 2-9  one query row and 64 of the 128 keys per thread: P from TMEM
-//              -> bf16 -> shared; at the end D_h from O'_h (TMEM) and dO_h
-//              (global), each half of the row's columns summed separately
-// TMEM columns: S buffers 0-127 and 128-255, O'_h from 256 + h * head dim.
+//              -> bf16 -> back into TMEM, over the first 32 of the 64 S
+//              columns the thread has read (so O'_h += P V_j reads A from
+//              TMEM); at the end D_h from O'_h (TMEM) and dO_h (global), each
+//              half of the row's columns summed separately
+// TMEM columns: S buffers 0-127 and 128-255 (P of keys 0-63 in 0-31 and of
+// keys 64-127 in 64-95 of its buffer), O'_h from 256 + h * head dim.
 //
 // The same pipeline also serves the dense attention forward over whole
 // sequences (every token kept), as two passes (MODE):
@@ -1150,9 +1250,9 @@ __device__ __forceinline__ void dprep_body(const CUtensorMap& tmQ, const CUtenso
         if (MODE != 2) {   // the lse pass only releases the buffers
 #pragma unroll
           for (int kk = 0; kk < kK / 16; ++kk) {   // V as the MN-major B: head-dim chunks kTile apart
-            const uint32_t pa = sbase + OFF_P + pb * 2 * kTile + (kk >> 2) * kTile + (kk & 3) * 32;
-            mma_bf16(tbase + TM_O + hh * kD, sdesc(pa, 16, 1024), sdesc(sv + kk * 2048, kTile, 1024), id_o,
-                     (jj > 0) || (kk > 0));
+            // P of keys 16 kk .. 16 kk + 15: 8 columns, in the half (kk / 4) of the S buffer
+            const uint32_t pa = tbase + TM_S + pb * 128 + 64 * (kk >> 2) + 8 * (kk & 3);
+            mma_bf16_ts(tbase + TM_O + hh * kD, pa, sdesc(sv + kk * 2048, kTile, 1024), id_o, (jj > 0) || (kk > 0));
           }
         }
         if (hh == HPC - 1) mma_commit(b_kvempty + 8 * kst);
@@ -1284,15 +1384,15 @@ __device__ __forceinline__ void dprep_body(const CUtensorMap& tmQ, const CUtenso
             sv[e] = valid ? exp2_approx(__uint_as_float(sr[cc * 32 + e]) * p.scale_log2 - L) : 0.f;
           }
         }
-        const uint32_t sub = st * 2 * kTile + (c >> 1) * kTile + r * 128;
+        // these 32 keys' P, packed in pairs: 16 columns of this half's first 32
+        // (every S column of the half is in registers already)
+        uint32_t pk[16];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const uint32_t phys = ((((c & 1) * 4 + g) ^ (r & 7)) * 16);
-          *reinterpret_cast<uint4*>(sm + OFF_P + sub + phys) = pack8(sv + 8 * g);
-        }
+        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(sv[2 * e], sv[2 * e + 1]);
+        tmem_st16(tbase + lane_off + TM_S + st * 128 + half * 64 + 16 * cc, pk);
       }
+      tmem_wait_st();
       fence_before();
-      fence_async_smem();
       mbar_arrive(b_pfull + 8 * st);
     }
     float* part = reinterpret_cast<float*>(sm + OFF_PART);   // [HPC][2][128]
@@ -1441,14 +1541,18 @@ cudaError_t run(const Ctx& c, const AttnK& k, float rope_base, const AttnArgs& a
   attn_prep_kernel<<<c.num_sms * 4, 256, 0, c.stream>>>(k, DH, rope_base, const_cast<float2*>(k.rope));
   prof_end(c);
   {
-    // work items: (key block, sequence, kv head, chunk of hc query heads)
+    // work items: (key block, sequence, kv head, chunk of hc query heads).
+    // The group's heads are split in at most two chunks: a key block's dK
+    // and dV then get at most two reduce-adds into a zeroed accumulator, and
+    // 0 + a + b = 0 + b + a exactly, so they are the same every run.
     const int nkb = (k.T + tcattn::kK - 1) / tcattn::kK;
     int hc = k.G;
-    while (hc > 1 && hc % 2 == 0 && (long long)k.B * k.Hkv * nkb * (k.G / hc) < 3LL * c.num_sms) hc /= 2;
+    if (hc % 2 == 0 && (long long)k.B * k.Hkv * nkb < 3LL * c.num_sms) hc /= 2;
     MainTc m{};
     m.B = k.B; m.T = k.T; m.H = k.H; m.Hkv = k.Hkv; m.G = k.G; m.hc = hc; m.nhc = k.G / hc; m.nkb = nkb;
     m.causal = k.causal; m.scale_log2 = k.scale_log2; m.cu_kept = k.cu_kept; m.lse2 = k.lse2; m.Dvec = k.Dvec;
     m.M = k.M; m.st = c.st;
+    m.order = k.order; m.nqb_max = (k.T + 63) / 64;
     // Q / dO tiles: 128 query rows for head dim 64, 64 for head dim 128
     constexpr int kQRows = DH == 64 ? tcattn::kQ : tcattn128::kQ;
     CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv, tq_pre;
@@ -1564,20 +1668,6 @@ cudaError_t launch_attn_fwd(const Ctx& c, const AttnFwdArgs& a) {
   return cudaErrorInvalidValue;
 }
 
-size_t attn_ws_bytes(int B, int T, int H, int Hkv, int dh) {
-  const size_t M = (size_t)B * T;
-  size_t b = 0;
-  auto add = [&](size_t n) { b += (n + 255) & ~size_t(255); };
-  add(M * H * dh * sizeof(float));      // dq_acc
-  add(M * Hkv * dh * sizeof(float));    // dk_acc
-  add(M * Hkv * dh * sizeof(float));    // dv_acc
-  add(M * H * sizeof(float));           // Dvec
-  add(M * H * sizeof(float));           // lse2
-  add((size_t)T * (dh / 2) * sizeof(float2));   // RoPE table
-  (void)Hkv;
-  return b;
-}
-
 cudaError_t launch_attn_bwd(const Ctx& c, const AttnArgs& a) {
   AttnK k{};
   k.B = a.B; k.T = a.T; k.H = a.H; k.Hkv = a.Hkv; k.G = a.H / a.Hkv; k.causal = a.causal;
@@ -1590,8 +1680,10 @@ cudaError_t launch_attn_bwd(const Ctx& c, const AttnArgs& a) {
   k.dq_acc = a.dq_acc; k.Dvec = a.Dvec; k.lse2 = a.lse_k;
   k.M = a.M; k.cap = a.cap > 0 ? a.cap : a.M; k.st = c.st;
   k.rope = a.rope;
+  k.order = a.order;
   k.dk_acc = a.dk_acc; k.dv_acc = a.dv_acc;
   k.kv_acc = ((a.dh == 64 || a.dh == 128) && a.dk_acc && a.dv_acc && a.in_cap > 0) ? 1 : 0;
+  if (!a.order) return cudaErrorInvalidValue;
   if (a.dh == 64) return run<64>(c, k, a.rope_base, a);
   if (a.dh == 128) return run<128>(c, k, a.rope_base, a);
   return cudaErrorInvalidValue;

@@ -204,6 +204,16 @@ __global__ void iota_cu_kernel(int B, int T, int32_t* cu) {
   for (int b = threadIdx.x; b <= B; b += blockDim.x) cu[b] = b * T;
 }
 
+// every token kept: idx[i] = i, cu[b] = b*T, n_kept = B*T
+__global__ void identity_index_kernel(int B, int T, int32_t* idx, int32_t* cu, int32_t* nk) {
+  const long long M = (long long)B * T;
+  const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = tid; i < M; i += stride) idx[i] = (int32_t)i;
+  for (long long b = tid; b <= B; b += stride) cu[b] = (int32_t)(b * T);
+  if (tid == 0) nk[0] = (int32_t)M;
+}
+
 int grid_for(const Ctx& c, long long work) {
   const long long want = (work + 255) / 256, cap = (long long)c.num_sms * 8;
   return (int)(want < 1 ? 1 : (want < cap ? want : cap));
@@ -272,6 +282,12 @@ cudaError_t launch_residual_out(const Ctx& c, int M, int D, const __nv_bfloat16*
 
 cudaError_t launch_iota_cu(const Ctx& c, int B, int T, int32_t* cu) {
   iota_cu_kernel<<<1, 256, 0, c.stream>>>(B, T, cu);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_identity_index(const Ctx& c, int B, int T, int32_t* idx, int32_t* cu, int32_t* nk) {
+  identity_index_kernel<<<grid_for(c, (long long)B * T), 256, 0, c.stream>>>(B, T, idx, cu, nk);
   count_launch();
   return cudaGetLastError();
 }

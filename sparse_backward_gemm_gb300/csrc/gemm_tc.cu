@@ -39,8 +39,8 @@ struct TcParams {
   int zero_pad;
   long long c_rows;
   float* partial;    // stream-K: [2 * gridDim.x][BM][BN] f32 partial tiles (null: whole tiles only)
-  int* counters;     // stream-K: per-tile arrival counts, zero on entry and left zero
-  int split_mode;    // 0 whole tiles, 1 stream-K, 2 hybrid (see Split)
+  int* counters;     // stream-K: per-(tile, pair rank) arrival counts, zero on entry and left zero
+  int split_mode;    // 0 whole tiles, 1 stream-K, 2 hybrid, 3 auto (see Split)
   int epi;           // TcEpilogue
   const __nv_bfloat16* aux;
   long long aux_ld;
@@ -72,24 +72,34 @@ constexpr int kTwoStages = 7;
 constexpr uint32_t kTwoStageBytes = BM * BK * 2 + 128 * BK * 2;
 constexpr size_t kTwoSmem = 1024 + kTwoStages * kTwoStageBytes + 256;
 
-// Work split.
-//   whole tiles  (mode 0): tiles round-robin over the CTAs.
+// Work split over the workers: lone CTAs, or CTA pairs (a pair works on one
+// 256-row tile, each CTA on its 128 rows, in step).
+//   whole tiles  (mode 0): tiles round-robin over the workers.
 //   stream-K     (mode 1): the num_tiles * num_kb (tile, k-slice) iterations
-//                are cut into equal contiguous ranges, one per CTA.
+//                are cut into equal contiguous ranges, one per worker.
 //   hybrid       (mode 2): whole tiles round-robin for all but the last full
 //                wave, stream-K over the remaining tiles (between one and two
 //                waves' worth), so the tail wave is as full as the others
 //                while the bulk keeps the round-robin tile order.
-// A tile cut between CTAs is finished by whichever of them arrives last,
-// summing the partial tiles in CTA order (deterministic).
+//   auto         (mode 3): hybrid only where whole tiles would leave the
+//                workers idle much of the time -- the waves' fill below 60%,
+//                or below 90% on a long reduction (>= 128 k-slices, where a
+//                tile's k-loop dwarfs the fix-up) -- else whole tiles.
+//                Decided on the device, where the real tile count is known.
+//                (Measured on the block shapes: a stream-K tail costs more
+//                than a 70%-full last wave on a short reduction.)
+// A tile cut between workers is finished by whichever of them arrives last,
+// summing the partial tiles in worker order (deterministic); in a pair each
+// CTA parks and finishes its own 128 rows.
 struct Split {
   int m_tiles, num_tiles, num_kb;
   int m_units;         // tile rows of the schedule: m_tiles, or pairs of them for a CTA pair
-  int unit0, ustride;  // whole-tile phase: first tile and stride (per CTA, or per CTA pair)
+  int W, wid;          // workers (CTAs or CTA pairs) and this CTA's worker
+  int unit0, ustride;  // whole-tile phase: first tile and stride (per worker)
   int dp_tiles;        // tiles handled whole, round-robin, first
   long long total;     // stream-K iterations (over tiles dp_tiles..num_tiles-1)
   bool sk;
-  int G;               // CTAs sharing the stream-K part: min(grid, total), no empty range
+  int G;               // workers sharing the stream-K part: min(W, total), no empty range
   __device__ long long begin(int c) const { return (long long)c * total / G; }
   // the CTA whose range holds stream-K iteration x
   __device__ int owner(long long x) const { return (int)(((x + 1) * (long long)G - 1) / total); }
@@ -100,10 +110,17 @@ struct Split {
     total = 0;
     sk = false;
     dp_tiles = num_tiles;
-    G = gridDim.x;
+    G = W;
     if (!have_scratch || mode == 0 || num_kb == 0) return;
-    const int grid = gridDim.x;
+    const int grid = W;
     const int waves = num_tiles / grid, rem = num_tiles % grid;
+    if (mode == 3) {
+      if (rem == 0) return;
+      const long long slots = (long long)(waves + 1) * grid;   // whole-tile waves x workers
+      const bool poor = 10LL * num_tiles < 6LL * slots, long_k = num_kb >= 128 && 10LL * num_tiles < 9LL * slots;
+      if (!poor && !long_k) return;
+      mode = 2;
+    }
     if (mode == 2) {
       if (rem == 0) return;
       dp_tiles = waves >= 1 ? (waves - 1) * grid : 0;
@@ -123,9 +140,9 @@ struct SegIter {
   long long it, end;   // stream-K phase (relative iterations)
   __device__ SegIter(const Split& s) : sp(s) {
     tile = sp.unit0;
-    if (sp.sk && (int)blockIdx.x < sp.G) {
-      it = sp.begin(blockIdx.x);
-      end = (long long)(blockIdx.x + 1) * sp.total / sp.G;
+    if (sp.sk && sp.wid < sp.G) {
+      it = sp.begin(sp.wid);
+      end = (long long)(sp.wid + 1) * sp.total / sp.G;
     } else {
       it = end = 0;
     }
@@ -266,9 +283,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   sp.m_units = PAIR ? (sp.m_tiles + 1) / 2 : sp.m_tiles;
   sp.num_tiles = sp.m_units * ((p.N + BN - 1) / BN);
   sp.num_kb = (K + BK - 1) / BK;
-  sp.unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  sp.ustride = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
-  sp.init(PAIR ? 0 : p.split_mode, !PAIR && p.partial != nullptr);
+  sp.W = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  sp.wid = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  sp.unit0 = sp.wid;
+  sp.ustride = sp.W;
+  sp.init(p.split_mode, p.partial != nullptr);
+  // partial tile of worker w for tile t: this CTA's 128 rows, stored as
+  // [BN / 4][BM][4] f32 so that a warp's 32 rows touch 512 contiguous bytes
+  constexpr int R = PAIR ? 2 : 1;
+  auto part_at = [&](int w, int t) -> float* {
+    return p.partial + ((long long)sp.slot(w, t) * R + rank) * (BM * BN);
+  };
   // tile t -> this CTA's output origin
   auto origin = [&](int t, int& m0, int& n0) {
     const int mu = t % sp.m_units;
@@ -473,13 +498,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         release_acc(acc);
       } else {
         // part of a tile: park it, and finish the tile if this CTA is the last
-        float* mine = p.partial + ((long long)sp.slot(blockIdx.x, t) * BM + rl) * BN;
+        float* mine = part_at(sp.wid, t);
         for (int c = 0; c < BN; c += 32) {
           float v[32];
           tmem_ld32(tcol + c, v);
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
-            __stcg(reinterpret_cast<float4*>(mine + c + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+            __stcg(reinterpret_cast<float4*>(mine + ((long long)((c + i) >> 2) * BM + rl) * 4),
+                   make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
         }
         fence_before();
         release_acc(acc);
@@ -488,9 +514,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const long long x0 = (long long)(t - sp.dp_tiles) * sp.num_kb;
         const int c_first = sp.owner(x0), c_last = sp.owner(x0 + sp.num_kb - 1);
         if (et == 0) {
-          const int old = atomicAdd(p.counters + t, 1);
+          int* ctr = p.counters + (long long)t * R + rank;
+          const int old = atomicAdd(ctr, 1);
           const int last = old == c_last - c_first;
-          if (last) p.counters[t] = 0;
+          if (last) *ctr = 0;
           *last_flag = last;
         }
         named_bar(1, 128);
@@ -501,10 +528,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
             for (int cc = c_first; cc <= c_last; ++cc) {
-              const float* src = p.partial + ((long long)sp.slot(cc, t) * BM + rl) * BN + c;
+              const float* src = part_at(cc, t);
 #pragma unroll
               for (int i = 0; i < 32; i += 4) {
-                const float4 w = __ldcg(reinterpret_cast<const float4*>(src + i));
+                const float4 w = __ldcg(reinterpret_cast<const float4*>(src + ((long long)((c + i) >> 2) * BM + rl) * 4));
                 v[i] += w.x; v[i + 1] += w.y; v[i + 2] += w.z; v[i + 3] += w.w;
               }
             }
@@ -593,7 +620,8 @@ cudaError_t launch_variant(const Ctx& c, const TcGemm& g, const CUtensorMap& ma,
   const long long m_tiles = (g.M + BM - 1) / BM, n_tiles = (g.N + BN - 1) / BN;
   if (PAIR) {
     const long long units = (m_tiles + 1) / 2 * n_tiles;
-    const int pairs = static_cast<int>(units < pairs_fit ? (units < 1 ? 1 : units) : pairs_fit);
+    const int pairs = p.partial ? pairs_fit   // stream-K: every pair takes a share
+                                : static_cast<int>(units < pairs_fit ? (units < 1 ? 1 : units) : pairs_fit);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -653,27 +681,27 @@ cudaError_t launch_tc_gemm(const Ctx& c, const TcGemm& g) {
   }
   // dX: both K-major; dW: both MN-major; the forward's Y = X W: A K-major, B MN-major
   if (g.a_mn_major && !g.b_mn_major) return cudaErrorNotSupported;
-  // Work split.  Measured on the block shapes: whole tiles keep the operands'
-  // L2 locality and win except for long reductions over a static K (>= 128
-  // k-slices), where stream-K's even split pays for its fix-up.
-  // COLLIDER_GEMM_STREAMK=0/1/2 forces whole tiles / stream-K / hybrid.
+  // Work split (launches given stream-K scratch): auto -- whole tiles unless
+  // the last wave would run less than 7/8 full, then the tail is cut into
+  // stream-K ranges (decided on the device from the real tile count).
+  // COLLIDER_GEMM_STREAMK=0/1/2/3 forces whole tiles / stream-K / hybrid / auto.
   static const int split_env = [] {
     const char* e = getenv("COLLIDER_GEMM_STREAMK");
     return e ? atoi(e) : -1;
   }();
-  // 2-SM pairs for every whole-tile launch of 256-wide tiles; 128-wide tiles
-  // and stream-K launches run as lone CTAs.  COLLIDER_GEMM_PAIR=0 forces lone
-  // CTAs everywhere.
+  // 2-SM pairs for every launch of 256-wide tiles; 128-wide tiles run as
+  // lone CTAs.  COLLIDER_GEMM_PAIR=0 forces lone CTAs everywhere.
   static const int pair_env = [] {
     const char* e = getenv("COLLIDER_GEMM_PAIR");
     return e ? atoi(e) : -1;
   }();
-  const long long max_tiles = ((long long)(g.M + BM - 1) / BM) * ((g.N + bn - 1) / bn);
-  int split = split_env;
-  if (split < 0) split = (g.dyn != 2 && g.K / BK >= 128) ? 1 : 0;
-  const bool sk = split != 0 && g.partial && g.counters && max_tiles <= g.counter_cap;
-  const bool pair = !sk && pair_env != 0 && bn == 256;
+  const bool pair = pair_env != 0 && bn == 256;
   const int mode = pair ? 2 : 0;
+  // counters the stream-K fix-up needs: one per tile, and per CTA of a pair
+  const long long m_tiles = (g.M + BM - 1) / BM, n_tiles = (g.N + bn - 1) / bn;
+  const long long max_ctrs = (pair ? 2 * ((m_tiles + 1) / 2) : m_tiles) * n_tiles;
+  const int split = split_env >= 0 ? split_env : 3;
+  const bool sk = split != 0 && g.partial && g.counters && max_ctrs <= g.counter_cap;
   CUtensorMap ma, mb;
   // A: K-major [M rows, K] or MN-major [K rows, M]; B: K-major [N rows, K]
   // (half the tile's rows per box for a pair) or MN-major [K rows, N]

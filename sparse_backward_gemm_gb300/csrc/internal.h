@@ -186,10 +186,13 @@ struct AttnArgs {
   float* Dvec;     // scratch f32 [H, M]
   float* lse_k;    // scratch f32 [H, M] (lse gathered to kept order, pre-scaled)
   float2* rope;    // scratch [T, rotary_dim/2] (cos, sin)
+  int* order;      // scratch [attn_order_ints(B, T, H)]: work tickets and dQ accumulation turns
   int M;
   long long cap;   // row capacity of dq, dk, dv (zero padding stops there)
 };
-size_t attn_ws_bytes(int B, int T, int H, int Hkv, int dh);
+// ints of the attention backward's ordering scratch: one work-item ticket and
+// a dQ accumulation turn per (sequence, query head, 64-row query block)
+__host__ __device__ inline size_t attn_order_ints(int B, int T, int H) { return 1 + (size_t)B * H * ((T + 63) / 64); }
 cudaError_t launch_attn_bwd(const Ctx& c, const AttnArgs& a);
 
 // ---- dense forward of one block (attn.cu, fwd.cu) ---------------------------
@@ -246,5 +249,7 @@ cudaError_t launch_residual_out(const Ctx& c, int M, int D, const __nv_bfloat16*
                                 __nv_bfloat16* y);
 // cu[b] = b * T for b <= B
 cudaError_t launch_iota_cu(const Ctx& c, int B, int T, int32_t* cu);
+// the index of "every token kept": idx[i] = i (i < B*T), cu[b] = b*T, *nk = B*T
+cudaError_t launch_identity_index(const Ctx& c, int B, int T, int32_t* idx, int32_t* cu, int32_t* nk);
 
 }  // namespace collider

@@ -109,6 +109,34 @@ __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Ordering between CTAs through a counter in global memory (turns).
+__device__ __forceinline__ int ld_acquire_gpu(const int* a) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+// *a = max(*a, v), with release semantics: everything this thread did before
+// (its completed bulk copies included) is visible to whoever acquires it
+__device__ __forceinline__ void release_turn(int* a, int v) {
+  asm volatile("red.release.gpu.global.max.s32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+// orders generic-proxy accesses against async-proxy (TMA) accesses of global memory
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+// Bounded wait until *turn >= want.  Returns false (and records the site in
+// the status word) when the budget runs out.
+static __device__ __noinline__ bool wait_turn(const int* turn, int want, DevStatus* st, unsigned site) {
+  if (ld_acquire_gpu(turn) >= want) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(turn) >= want) return true;
+    if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+      report_error(st, kErrTimeout, site);
+      return false;
+    }
+  }
+}
+
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -134,6 +162,17 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+// D (+)= A . B with A read from tensor memory (M = 128 lanes, one row per
+// lane, K elements packed two bf16 to a 32-bit column) and B from shared memory
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accum)
       : "memory");
 }
 // arrive on `bar` once every tcgen05 operation this thread issued so far is done
@@ -202,6 +241,17 @@ __device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t* r) {
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
+// 16 consecutive 32-bit columns of this thread's TMEM lane (warp-collective);
+// tmem_wait_st() makes every store issued so far by this thread complete
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // 2^x with the hardware approximation (flushes denormal results to zero)

@@ -165,8 +165,10 @@ def _epilogue(n, roles, arrivers, warps=2):
 
 
 def main64(n, warps=2):
-    """Main pass, head dim 64: two query halves, each with its own S/dP buffer,
-    P/dS tile and group of softmax warps (a named barrier per block)."""
+    """Main pass, head dim 64: two query halves, each with its own S/dP buffer
+    (where its P lands too) and group of softmax warps (a named barrier per
+    block); the dS^T tile and the dQ accumulator are double-buffered by block,
+    so a half waits only for the dQ of two blocks back."""
     mma = [("wait", ("kvready", 0))]
     if n:
         mma += [("wait", ring("qready", 0, 2)), ("sig", (("sfull", 0), 0)), ("sig", (("sfull", 1), 0))]
@@ -176,10 +178,10 @@ def main64(n, warps=2):
         if more:
             mma += [("wait", ring("qready", it + 1, 2)), ("sig", (("sfull", 0), it + 1))]
         mma.append(("wait", (("pfull", 1), it)))
-        if it > 0:
-            mma.append(("wait", ("dqempty", it - 1)))
-        mma += [("sig", ring("qempty", it, 2)), ("sig", ("dqfull", it)),
-                ("sig", (("pempty", 0), it)), ("sig", (("pempty", 1), it))]
+        mma.append(("sig", ring("qempty", it, 2)))
+        if it >= 2:
+            mma.append(("wait", ring("dqempty", it - 2, 2)))
+        mma += [("sig", ring("dqfull", it, 2)), ("sig", ring("dsempty", it, 2))]
         if more:
             mma.append(("sig", (("sfull", 1), it + 1)))
     roles = {"producer": _q_producer(n), "mma": mma}
@@ -190,33 +192,49 @@ def main64(n, warps=2):
             ops = []
             for it in range(n):
                 ops += [("arrive", (("nb", g), it)), ("wait", (("nb", g), it)), ("wait", (("sfull", g), it))]
-                if it > 0:
-                    ops.append(("wait", (("pempty", g), it - 1)))
+                if it >= 2:
+                    ops.append(("wait", ring("dsempty", it - 2, 2)))
                 ops.append(("arrive", (("pfull", g), it)))
             roles[name] = ops
         arrivers[("pfull", g)] = names
         arrivers[("nb", g)] = names
-    _epilogue(n, roles, arrivers)
+    names = [f"epilogue{w}" for w in range(2)]
+    for name in names:
+        ops = []
+        for it in range(n):
+            ops += [("wait", ring("dqfull", it, 2)), ("arrive", ring("dqempty", it, 2)),
+                    ("arrive", (("nb", "epi"), 2 * it)), ("wait", (("nb", "epi"), 2 * it)),
+                    ("arrive", (("nb", "epi"), 2 * it + 1)), ("wait", (("nb", "epi"), 2 * it + 1))]
+        roles[name] = ops
+    for a in (0, 1):
+        arrivers[("dqempty", a)] = names
+    arrivers[("nb", "epi")] = names
     return roles, arrivers
 
 
 def main128(n, warps=2):
-    """Main pass, head dim 128: one S/dP buffer, one P/dS tile, the softmax
-    warps meet at a named barrier per block."""
+    """Main pass, head dim 128: one S/dP buffer (where P and dS land too), the
+    softmax warps meet at a named barrier per block; the next block's S, dP
+    are issued before this block's dQ^T, and the dS^T tile is double-buffered
+    by block for dQ^T."""
     mma = [("wait", ("kvready", 0))]
+    if n:
+        mma += [("wait", ring("qready", 0, 2)), ("sig", ("sfull", 0))]
     for it in range(n):
-        mma += [("wait", ring("qready", it, 2)), ("sig", ("sfull", it)), ("wait", ("pfull", it))]
+        mma += [("wait", ("pfull", it)), ("sig", ring("qempty", it, 2))]
+        if it + 1 < n:
+            mma += [("wait", ring("qready", it + 1, 2)), ("sig", ("sfull", it + 1))]
         if it > 0:
             mma.append(("wait", ("dqempty", it - 1)))
-        mma += [("sig", ring("qempty", it, 2)), ("sig", ("dqfull", it)), ("sig", ("pempty", it))]
+        mma += [("sig", ("dqfull", it)), ("sig", ring("dsempty", it, 2))]
     roles = {"producer": _q_producer(n), "mma": mma}
     names = [f"softmax{w}" for w in range(warps)]
     for name in names:
         ops = []
         for it in range(n):
             ops += [("arrive", (("nb", "soft"), it)), ("wait", (("nb", "soft"), it)), ("wait", ("sfull", it))]
-            if it > 0:
-                ops.append(("wait", ("pempty", it - 1)))
+            if it >= 2:
+                ops.append(("wait", ring("dsempty", it - 2, 2)))
             ops.append(("arrive", ("pfull", it)))
         roles[name] = ops
     arrivers = {"pfull": names, ("nb", "soft"): names}
@@ -254,8 +272,13 @@ def test_single_p_full_barrier_is_unsafe():
 # tcgen05 GEMM (sparse_backward_gemm_gb300/csrc/gemm_tc.cu): an S-stage ring
 # of shared-memory stages, a double-buffered TMEM accumulator, epilogue warps
 # that release it.  `tiles` whole tiles of `kb` k-blocks each.
-def gemm(mode, tiles, kb, S, warps=2):
-    G = tiles * kb
+def gemm(mode, tiles, kb, S, warps=2, segs=None):
+    """segs: k-blocks of each segment (a whole tile, or a stream-K piece of
+    one); default `tiles` segments of `kb`."""
+    segs = [kb] * tiles if segs is None else list(segs)
+    tiles = len(segs)
+    starts = [sum(segs[:i]) for i in range(tiles)]
+    G = sum(segs)
     roles, arrivers = {}, {}
     ctas = ["A"] if mode == 0 else ["A", "B"]
     for c in ctas:
@@ -281,8 +304,8 @@ def gemm(mode, tiles, kb, S, warps=2):
         for t in range(tiles):
             if t >= 2:
                 ops.append(("wait", ring(("tempty", c), t - 2, 2)))
-            for k in range(kb):
-                g = t * kb + k
+            for k in range(segs[t]):
+                g = starts[t] + k
                 ops.append(("wait", ring(("full", c), g, S)))
                 if mode == 0:
                     ops.append(("sig", ring(("empty", c), g, S)))
@@ -312,6 +335,19 @@ def test_gemm_protocols(mode):
             for S in (2, 3, 7):
                 dead, missed, overrun = check(gemm(mode, tiles, kb, S))
                 assert not dead and not missed and not overrun, (mode, tiles, kb, S, dead, missed[:2], overrun[:2])
+
+
+@pytest.mark.parametrize("mode", [0, 2])
+def test_gemm_protocols_with_stream_k_segments(mode):
+    """Stream-K gives a CTA (or pair) segments of unequal length: the same
+    protocol, with a varying number of k-blocks between accumulator hand-offs."""
+    import random
+    rnd = random.Random(5)
+    for _ in range(40):
+        segs = [rnd.randint(1, 6) for _ in range(rnd.randint(1, 5))]
+        for S in (2, 3, 7):
+            dead, missed, overrun = check(gemm(mode, 0, 0, S, segs=segs))
+            assert not dead and not missed and not overrun, (mode, segs, S, dead, missed[:2], overrun[:2])
 
 
 def test_checker_catches_planted_gemm_flaws():

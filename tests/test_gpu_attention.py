@@ -121,3 +121,31 @@ def test_attention_backward_non_causal(B, T, H, Hkv, dh):
         g = gu.host(got).reshape(M, nh, dh)
         assert np.all(g[keep.reshape(-1) == 0] == 0)
         assert gu.rel_err(g, ref) <= 2e-2
+
+
+@pytest.mark.parametrize("B,T,H,Hkv,dh", [(2, 1100, 8, 2, 64), (1, 1300, 6, 2, 128), (1, 900, 4, 4, 64)])
+def test_attention_backward_is_reproducible(B, T, H, Hkv, dh):
+    """dQ sums one tile per key block: the tiles are added in key-block order,
+    so dQ, dK and dV are bit-identical from run to run, on sequences of many
+    key and query blocks (and still match the oracle)."""
+    q, k, v, dO, lse, keep, scale = _case(B, T, H, Hkv, dh, 0.3, "gumbel", seed=17 + T, qk_std=1.5)
+    M = B * T
+    idx, cu, nk = gu.compact(keep)
+    Qd, Kd, Vd, dOd = (gu.bf16(a.reshape(M, -1)) for a in (q, k, v, dO))
+    ws = torch.empty(cl.collider_attn_workspace_size(B, T, H, Hkv, dh), dtype=torch.uint8, device=gu.DEV)
+    runs = []
+    for _ in range(3):
+        out = [torch.full((M, n * dh), float("nan"), dtype=torch.bfloat16, device=gu.DEV) for n in (H, Hkv, Hkv)]
+        cl.collider_attn_bwd(B, T, H, Hkv, dh, 1, scale, dh, 10000.0, Qd, Kd, Vd, None, dOd, H * dh, Hkv * dh,
+                             H * dh, cl.ROWS_FULL, gu.f32(lse), idx, cu, nk, *out, cl.ROWS_FULL, ws)
+        cl.collider_check()
+        runs.append([o.clone() for o in out])
+    for r in runs[1:]:
+        for a, b in zip(runs[0], r):
+            assert torch.equal(a, b)
+    rq, rk, rv = filtered_attention_backward(q, k, v, dO, lse, keep, scale)
+    pos = np.tile(np.arange(T), B)
+    rq = ops.rope_backward(rq, pos, dh, 10000.0)
+    rk = ops.rope_backward(rk, pos, dh, 10000.0)
+    for got, ref, nh in zip(runs[0], (rq, rk, rv), (H, Hkv, Hkv)):
+        assert gu.rel_err(gu.host(got).reshape(M, nh, dh), ref) <= 2e-2

@@ -117,6 +117,63 @@ def test_block_nan_poison_and_determinism():
     assert np.all(b["dx"][km] == 0)
 
 
+def test_block_backward_is_reproducible():
+    """Every output of the block -- dx and the weight gradients below the
+    attention (dw_qkv, dnorm1_w) included -- is bit-identical run to run, on
+    sequences of several key blocks, because every reduction has a fixed order."""
+    s = SMALL["llama"].with_(B=2, T=1100)
+    w = workloads.layer_weights(s)
+    t = workloads.layer_inputs(s)
+    _, saved = ob.block_forward(t["x"], w, s, round_saved=True)
+    L = gu.DeviceLayer(s, w, saved)
+    idx, cu, nk = gu.compact(t["keep"])
+    outs = []
+    for _ in range(3):
+        L.run(gu.bf16(t["dout"]), idx, cu, nk)
+        outs.append(L.results())
+        cl.collider_check()
+    for o in outs[1:]:
+        for k in outs[0]:
+            assert np.array_equal(outs[0][k], o[k]), k
+
+
+@pytest.mark.parametrize("arch", ["llama", "qwen", "phi"])
+def test_dense_call_is_the_all_kept_backward(arch):
+    """idx, cu_kept, n_kept all NULL: the unfiltered dense backward reads FULL
+    rows in place (no gather, no scatter).  It matches the oracle with nothing
+    filtered and is bit-identical to the filtered path run on an all-kept
+    mask (M = 320 or 400 or 300 rows: not whole 128-row tiles)."""
+    s = SMALL[arch].with_(f=0.0)
+    w = workloads.layer_weights(s)
+    t = workloads.layer_inputs(s)
+    keep = np.ones((s.B, s.T), dtype=np.uint8)
+    _, saved = ob.block_forward(t["x"], w, s, round_saved=True)
+    ref = ob.block_backward(t["dout"], saved, w, s, keep)
+    L = gu.DeviceLayer(s, w, saved)
+    dout = gu.bf16(t["dout"])
+    L.run(dout, None, None, None)
+    dense = L.results()
+    cl.collider_check()
+    idx, cu, nk = gu.compact(keep)
+    L.run(dout, idx, cu, nk)
+    masked = L.results()
+    cl.collider_check()
+    for k in ref:
+        assert gu.rel_err(dense[k], ref[k]) <= 2e-2, (k, gu.rel_err(dense[k], ref[k]))
+        assert np.array_equal(dense[k], masked[k]), k
+
+
+def test_dense_call_rejects_a_partial_index():
+    s = SMALL["llama"]
+    w = workloads.layer_weights(s)
+    t = workloads.layer_inputs(s)
+    _, saved = ob.block_forward(t["x"], w, s, round_saved=True)
+    L = gu.DeviceLayer(s, w, saved)
+    idx, cu, nk = gu.compact(t["keep"])
+    with pytest.raises(cl.ColliderError, match="idx/cu_kept/n_kept"):
+        L.run(gu.bf16(t["dout"]), idx, None, None)
+
+
 def test_small_stack():
     ls = SMALL["llama"].with_(B=1, T=192)
     st = workloads.StackShape(seed_base=84000, layer=ls, L=2, V=512)
@@ -171,3 +228,39 @@ def test_loss_only_filtering_baseline():
     for k in ref:
         assert gu.rel_err(got[k], ref[k]) <= 2e-2, k
     assert np.abs(got["dx"][~km]).max() > 0
+
+
+def test_small_stack_dense_call():
+    """The stack's dense call (NULL index) is bit-identical to its filtered path
+    on an all-kept mask, and matches the oracle with nothing filtered."""
+    ls = SMALL["llama"].with_(B=1, T=192, f=0.0)
+    st = workloads.StackShape(seed_base=85000, layer=ls, L=2, V=512)
+    t = workloads.stack_tensors(st)
+    keep = np.ones((ls.B, ls.T), dtype=np.uint8)
+    z, saved = ost.stack_forward(t["ids"], t["E"], t["layers"], t["normf_w"], t["w_lm"], ls, round_saved=True)
+    ref = ost.stack_backward(z, t["targets"], t["ids"], saved, t["layers"], t["normf_w"], t["w_lm"], ls, st.V, keep)
+    layers = [gu.DeviceLayer(ls, t["layers"][l], saved["blocks"][l]) for l in range(st.L)]
+    W = (cl.LayerWeights * st.L)(*[L.weights for L in layers])
+    S = (cl.LayerSaved * st.L)(*[L.saved for L in layers])
+    G = (cl.LayerGrads * st.L)(*[L.grads for L in layers])
+    D, V = ls.D, st.V
+    desc = gu.layer_desc(ls)
+    ws = torch.empty(cl.collider_stack_workspace_size(desc, st.L, V), dtype=torch.uint8, device=gu.DEV)
+    ins = [gu.bf16(z), gu.i32(t["targets"]), gu.i32(t["ids"]), gu.bf16(saved["y"]), gu.bf16(saved["xL"]),
+           gu.f32(saved["rstdf"]), gu.bf16(t["normf_w"]), gu.bf16(t["w_lm"])]
+    res = []
+    for index in ((None, None, None), gu.compact(keep)):
+        outs = [torch.full(shp, float("nan"), device=gu.DEV) for shp in ((D,), (D, V), (V, D))]
+        cl.collider_stack_bwd(desc, st.L, V, W, S, *ins, *index, G, *outs, ws)
+        cl.collider_check()
+        res.append([gu.host(o) for o in outs] + [layers[l].results() for l in range(st.L)])
+    (dnf, dlm, dE), (dnf2, dlm2, dE2) = res[0][:3], res[1][:3]
+    assert np.array_equal(dnf, dnf2) and np.array_equal(dlm, dlm2) and np.array_equal(dE, dE2)
+    assert gu.rel_err(dlm, ref["dw_lm"]) <= 2e-2 and gu.rel_err(dE, ref["dE"]) <= 2e-2
+    for l in range(st.L):
+        a, b = res[0][3 + l], res[1][3 + l]
+        for k, v in ref["blocks"][l].items():
+            if k == "dx":
+                continue
+            assert np.array_equal(a[k], b[k]), (l, k)
+            assert gu.rel_err(a[k], v) <= 2e-2, (l, k)
