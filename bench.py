@@ -613,9 +613,15 @@ def run_ours(args):
             ms2f, _ = timed(b2.masks["filtered"], args.steps, args.warmup, lambda m: b2.step(m, stream))
             ms2u, _ = timed(b2.masks["unfiltered"], args.steps, args.warmup, lambda m: b2.step(m, stream))
             ms2f, ms2u = max_over_ranks([ms2f, ms2u], dev)
+            nk2 = int(b2.keep_np.sum())
+            p2, g2_ms, g2_fl, _ = profile_pass(cl, lambda: b2.step(b2.masks["filtered"], stream), 3, 1, flush, nk2)
             configs[label] = {"tokens_per_s": shp.M * world / (ms2f * 1e-3), "ms_per_step": ms2f,
                               "unfiltered_ms_per_step": ms2u, "speedup_vs_unfiltered": ms2u / ms2f,
-                              "kept_tokens": int(b2.keep_np.sum()), "tokens": shp.M}
+                              "kept_tokens": nk2, "tokens": shp.M,
+                              "gemm_frac": (g2_fl / (g2_ms * 1e-3) / 1e12) / peaks["bf16_tflops"] if g2_ms > 0 else None,
+                              "attention": attn_roofline(p2, 3, attn_flops(shp, b2.keep_np.sum(axis=1).tolist()),
+                                                         peaks["bf16_tflops"], src),
+                              "kernels_ms_per_step": {k: round(v[1] / 3, 4) for k, v in sorted(p2.items())}}
             del b2
             torch.cuda.empty_cache()
         st = workloads.WORKLOADS["tinyllama_stack"]

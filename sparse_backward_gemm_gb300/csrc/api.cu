@@ -576,8 +576,6 @@ struct LayerBufs {
   float* col_part;
   float* sk_partial;     // stream-K scratch of the input-gradient chain's GEMMs
   int* sk_counters;
-  float* sk_partial_w;   // and of the weight-gradient GEMMs (side stream, concurrent)
-  int* sk_counters_w;
   long long sk_cap;
   AttnScratch at;
   int32_t *id_idx, *id_cu, *id_nk;   // the identity index of a dense (every token kept) call
@@ -630,8 +628,6 @@ void layer_carve(Carver& cv, const collider_layer_desc* d, LayerBufs* L) {
   const long long mmax = std::max<long long>((long long)Mp, std::max(D, F));
   L->sk_cap = sk_counter_cap(mmax, std::max<long long>(std::max(Nqkv, Nup), std::max(D, F)));
   L->sk_counters = cv.take<int>(L->sk_cap);
-  L->sk_partial_w = cv.take<float>(kSkPartialFloats);
-  L->sk_counters_w = cv.take<int>(L->sk_cap);
   L->id_idx = cv.take<int32_t>((size_t)d->B * d->T);
   L->id_cu = cv.take<int32_t>((size_t)d->B + 1);
   L->id_nk = cv.take<int32_t>(1);
@@ -710,13 +706,10 @@ cudaError_t join_side(const Ctx& c, Side* S, int k) {
   return e == cudaSuccess ? cudaStreamWaitEvent(c.stream, S->ev[k], 0) : e;
 }
 
-// stream-K scratch shared by the GEMMs of one call that run in stream order:
-// one set for the input-gradient chain, one for the weight-gradient GEMMs
-// (which run concurrently with it on the side stream)
+// stream-K scratch shared by the input-gradient chain's GEMMs of one call
+// (they run in stream order)
 thread_local float* g_sk_partial = nullptr;
 thread_local int* g_sk_counters = nullptr;
-thread_local float* g_sk_partial_w = nullptr;
-thread_local int* g_sk_counters_w = nullptr;
 thread_local long long g_sk_cap = 0;
 
 // C (bf16 or f32, COMPACT [Mk, N]) = A_k [Mk, K] . W^T with W stored [N, K]
@@ -739,12 +732,13 @@ cudaError_t gemm_dx(const Ctx& c, int M, int N, int K, const void* A, const void
 
 // dW [Kin, Nout] f32 = X_k^T dY_k, X_k [Mk, Kin], dY_k [Mk, Nout] (both COMPACT, zero-padded,
 // or -- a dense call -- the caller's M rows: rows = M, the TMA fills past them with zeros)
-// (runs on the side stream, concurrently with the caller's stream: it uses the
-// weight-gradient GEMMs' own stream-K scratch)
+// (runs on the side stream, concurrently with the input-gradient chain, as
+// whole tiles: there a tail wave leaves SMs to the chain's kernels, while
+// stream-K would hold every SM to the end -- measured: the block step was
+// slower with it)
 cudaError_t gemm_dw(const Ctx& c, int M, int Kin, int Nout, const void* Xk, long long ldx, const void* dYk,
                     long long ldy, float* dW, const int32_t* n_kept, long long rows = -1) {
   TcGemm g{};
-  g.partial = g_sk_partial_w; g.counters = g_sk_counters_w; g.counter_cap = g_sk_cap;
   g.M = Kin; g.N = Nout; g.K = M;
   g.A = Xk; g.lda = ldx; g.a_mn_major = 1; g.a_rows = rows > 0 ? rows : pad128(M);
   g.B = dYk; g.ldb = ldy; g.b_mn_major = 1; g.b_rows = rows > 0 ? rows : pad128(M);
@@ -781,8 +775,6 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
   // (the stream-K counters were zeroed by the entry point; kernels leave them zero)
   g_sk_partial = L.sk_partial;
   g_sk_counters = L.sk_counters;
-  g_sk_partial_w = L.sk_partial_w;
-  g_sk_counters_w = L.sk_counters_w;
   g_sk_cap = L.sk_cap;
 
   // row extent of the GEMM / attention operands: COMPACT buffers are padded
@@ -795,48 +787,53 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
     L.o_k = bfp(sv->o);
     L.a_k = bfp(sv->a);
     L.qkv_k = bfp(sv->qkv);
-    if (llama) {
-      L.s_k = bfp(sv->s);
-    } else {
-      // not a gather: gelu(f1) of every row, which the GEMM needs as an operand
-      GatherJob j{static_cast<const char*>(sv->up), reinterpret_cast<char*>(L.s_k), (long long)F * 2,
-                  (long long)F * 2, F * 2, 1};
-      CK(launch_gather(c, &j, 1, M, pad128(M), nullptr, n_kept));
-    }
+    if (llama) L.s_k = bfp(sv->s);
   }
-  // 1. gather the kept rows of dOut and of the saved GEMM operands
+  // 1. gather the kept rows of dOut and of the saved GEMM operands.  The
+  // input-gradient chain reads only dOut and qkv (and the saved rows its row
+  // kernels index directly); s, b, o and a feed only the weight-gradient
+  // GEMMs, so they are gathered on the side stream, beside the chain.
   if (!dense) {
-    GatherJob j[6];
-    int n = 0;
-    j[n++] = GatherJob{static_cast<const char*>(dOut), reinterpret_cast<char*>(L.dout_k), (long long)D * 2,
-                       (long long)D * 2, D * 2, 0};
-    if (llama) {
-      j[n++] = GatherJob{static_cast<const char*>(sv->s), reinterpret_cast<char*>(L.s_k), (long long)F * 2,
-                         (long long)F * 2, F * 2, 0};
-      j[n++] = GatherJob{static_cast<const char*>(sv->b), reinterpret_cast<char*>(L.b_k), (long long)D * 2,
-                         (long long)D * 2, D * 2, 0};
-    } else {
-      j[n++] = GatherJob{static_cast<const char*>(sv->up), reinterpret_cast<char*>(L.s_k), (long long)F * 2,
-                         (long long)F * 2, F * 2, 1};   // gelu(f1)
-    }
-    j[n++] = GatherJob{static_cast<const char*>(sv->o), reinterpret_cast<char*>(L.o_k), (long long)Hd * 2,
-                       (long long)Hd * 2, Hd * 2, 0};
-    j[n++] = GatherJob{static_cast<const char*>(sv->a), reinterpret_cast<char*>(L.a_k), (long long)D * 2,
-                       (long long)D * 2, D * 2, 0};
-    j[n++] = GatherJob{static_cast<const char*>(sv->qkv), reinterpret_cast<char*>(L.qkv_k), (long long)Nqkv * 2,
-                       (long long)Nqkv * 2, Nqkv * 2, 0};
+    GatherJob j[2];
+    j[0] = GatherJob{static_cast<const char*>(dOut), reinterpret_cast<char*>(L.dout_k), (long long)D * 2,
+                     (long long)D * 2, D * 2, 0};
+    j[1] = GatherJob{static_cast<const char*>(sv->qkv), reinterpret_cast<char*>(L.qkv_k), (long long)Nqkv * 2,
+                     (long long)Nqkv * 2, Nqkv * 2, 0};
     if (dout_full) {
-      CK(launch_gather(c, j, n, M, pad128(M), idx, n_kept));
+      CK(launch_gather(c, j, 2, M, pad128(M), idx, n_kept));
     } else {
       CK(launch_gather(c, j, 1, M, pad128(M), nullptr, n_kept));   // COMPACT dOut: copy + zero padding
-      CK(launch_gather(c, j + 1, n - 1, M, pad128(M), idx, n_kept));
+      CK(launch_gather(c, j + 1, 1, M, pad128(M), idx, n_kept));
     }
+  }
+  CK(fork_side(c, side, 0));   // the side stream starts once dOut's kept rows exist
+  {
+    GatherJob j[4];
+    int n = 0;
+    if (llama) {
+      if (!dense) {
+        j[n++] = GatherJob{static_cast<const char*>(sv->s), reinterpret_cast<char*>(L.s_k), (long long)F * 2,
+                           (long long)F * 2, F * 2, 0};
+        j[n++] = GatherJob{static_cast<const char*>(sv->b), reinterpret_cast<char*>(L.b_k), (long long)D * 2,
+                           (long long)D * 2, D * 2, 0};
+      }
+    } else {
+      // gelu(f1) of the kept rows (of every row for a dense call: then not a gather)
+      j[n++] = GatherJob{static_cast<const char*>(sv->up), reinterpret_cast<char*>(L.s_k), (long long)F * 2,
+                         (long long)F * 2, F * 2, 1};
+    }
+    if (!dense) {
+      j[n++] = GatherJob{static_cast<const char*>(sv->o), reinterpret_cast<char*>(L.o_k), (long long)Hd * 2,
+                         (long long)Hd * 2, Hd * 2, 0};
+      j[n++] = GatherJob{static_cast<const char*>(sv->a), reinterpret_cast<char*>(L.a_k), (long long)D * 2,
+                         (long long)D * 2, D * 2, 0};
+    }
+    if (n) CK(launch_gather(cs, j, n, M, pad128(M), dense ? nullptr : idx, n_kept));
   }
 
   // 2. MLP
   const __nv_bfloat16* dres = L.dout_k;   // gradient flowing along the residual into the attention half
   if (llama) {
-    CK(fork_side(c, side, 0));
     CK(gemm_dw(cs, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept, in_rows));     // dW_down = s^T dOut
     CK(gemm_dx(c, M, F, D, L.dout_k, w->w_down, L.ds_k, 1, 0, n_kept, kEpiStore, nullptr, nullptr,
                in_rows));                                                              // ds = dOut W_down^T
@@ -854,7 +851,6 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
     CK(launch_norm_bwd(c, nb));                                                          // dh = dOut + norm2'
     dres = L.dh_k;
   } else {
-    CK(fork_side(c, side, 0));
     CK(gemm_dw(cs, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept, in_rows));     // dW2 = gelu(f1)^T dOut
     CK(gemm_dx(c, M, F, D, L.dout_k, w->w_down, L.ds_k, 1, 0, n_kept, kEpiStore, nullptr, nullptr,
                in_rows));                                                              // df2 = dOut W2^T
@@ -977,7 +973,6 @@ extern "C" collider_status collider_layer_bwd(const collider_layer_desc* d, cons
   // stream-K counters start at zero (every GEMM leaves them zero); zeroed here,
   // on the caller's stream, before any work of this call is forked off it
   CK(cudaMemsetAsync(L.sk_counters, 0, L.sk_cap * sizeof(int), c.stream));
-  CK(cudaMemsetAsync(L.sk_counters_w, 0, L.sk_cap * sizeof(int), c.stream));
   if (dense) {
     CK(launch_identity_index(c, d->B, d->T, L.id_idx, L.id_cu, L.id_nk));
     return layer_bwd_impl(c, d, w, sv, dOut, true, L.id_idx, L.id_cu, L.id_nk, g, true, L, true);
@@ -1204,11 +1199,8 @@ extern "C" collider_status collider_stack_bwd(const collider_layer_desc* d, int 
   const int M = d->B * d->T, D = d->D;
   g_sk_partial = LB.sk_partial;
   g_sk_counters = LB.sk_counters;
-  g_sk_partial_w = LB.sk_partial_w;
-  g_sk_counters_w = LB.sk_counters_w;
   g_sk_cap = LB.sk_cap;
   CK(cudaMemsetAsync(LB.sk_counters, 0, LB.sk_cap * sizeof(int), c.stream));
-  CK(cudaMemsetAsync(LB.sk_counters_w, 0, LB.sk_cap * sizeof(int), c.stream));
   if (dense) {
     CK(launch_identity_index(c, d->B, d->T, LB.id_idx, LB.id_cu, LB.id_nk));
     idx = LB.id_idx;

@@ -206,28 +206,33 @@ __global__ void attn_finalize_kernel(AttnK p, int DH) {
 //                 dV += P_g^T dO_g, dK += dS_g^T Q_g   (M 128 keys, N 64; A
 //                                                       = P^T, dS^T from TMEM)
 //               and per block dQ = dS K                (M 128 queries, N 64)
-//   warps 2-5   query half 0, warps 6-9 query half 1: one key row and the
-//               half's 64 queries per thread: P^T, dS^T from TMEM -> bf16 ->
-//               back into TMEM over the consumed S^T / dP^T columns; dS^T
-//               also to shared (double-buffered by block) for dQ
-//   warps 10-13 one query row per thread: dQ from TMEM -> shared -> TMA
+//   warps 2-9   query half 0, warps 10-17 query half 1: one key row and 32
+//               of the half's 64 queries per thread: P^T, dS^T from TMEM ->
+//               bf16 -> back into TMEM over the consumed S^T / dP^T columns;
+//               dS^T also to shared (double-buffered by block) for dQ
+//   warps 18-21 one query row per thread: dQ from TMEM -> shared -> TMA
 //               reduce-add into the f32 dQ accumulator; at the end dK, dV
 //               likewise into their accumulators
-// TMEM columns: half 0 S^T 0-63 (P^T in 0-31 once formed), dP^T 64-127
-// (dS^T in 64-95); half 1 S^T 128-191, dP^T 192-255; dV 256-319, dK
-// 320-383, dQ 384-447 and 448-511 (double-buffered by block).
+// TMEM columns: half 0 S^T 0-63 (P^T of its queries 0-31 in 0-15, of 32-63
+// in 32-47, once formed), dP^T 64-127 (dS^T likewise); half 1 the same from
+// 128; dV 256-319, dK 320-383, dQ 384-447 and 448-511 (double-buffered by
+// block).
 // P never goes through shared memory and dS has a buffer per block parity,
 // so a softmax half never waits for the previous block's dQ: only for the
 // dQ two blocks back, long done.
 namespace tcattn {
 constexpr int kQ = 128, kK = 128, kD = 64;
 constexpr uint32_t kTile = kQ * kD * 2;                 // 16 KB: 128 rows x 128 bytes
-// dS^T buffers: two (block parity), each two halves of one kTile
-constexpr uint32_t OFF_K = 0, OFF_V = kTile, OFF_Q = 2 * kTile, OFF_DO = 4 * kTile, OFF_DS = 6 * kTile,
-                   OFF_ST = 10 * kTile, OFF_LD = 12 * kTile, OFF_BAR = 12 * kTile + 2048;
+constexpr int kQS = 3;                                  // Q / dO stages
+// Q and dO: kQS stages of one kTile each; dS^T buffers: two (block parity),
+// each two halves of one kTile; staging: one [128 rows x 32 f32] box
+constexpr uint32_t OFF_K = 0, OFF_V = kTile, OFF_Q = 2 * kTile, OFF_DO = OFF_Q + kQS * kTile,
+                   OFF_DS = OFF_DO + kQS * kTile, OFF_ST = OFF_DS + 4 * kTile, OFF_LD = OFF_ST + kTile,
+                   OFF_BAR = OFF_LD + 2048;
 constexpr size_t kSmem = 1024 + OFF_BAR + 256;
+static_assert(kSmem <= 232448, "shared memory");
 constexpr uint32_t TM_S = 0, TM_DV = 256, TM_DK = 320, TM_DQ = 384;
-constexpr int kSoftWarps = 8;                       // two per TMEM lane quadrant
+constexpr int kSoftWarps = 16;                      // four per TMEM lane quadrant
 constexpr int kThreads = 32 * (2 + kSoftWarps + 4);
 }  // namespace tcattn
 
@@ -267,6 +272,17 @@ __device__ __forceinline__ void dq_turn_flush(int*& pending, int j) {
   tc::release_turn(pending, j + 1);
   pending = nullptr;
 }
+// The first half of ordered_dq_add, for a caller that issues its adds in
+// several steps: pass the previous turn on, wait for this one, and return it
+// (the caller stores it in `pending` after its last add is committed).
+__device__ __forceinline__ int* dq_turn_acquire(const MainTc& p, int b, int h, int ib, int j, bool& broken,
+                                                int*& pending, unsigned site) {
+  dq_turn_flush(pending, j);
+  int* turn = p.order + 1 + ((long long)b * p.H + h) * p.nqb_max + ib;
+  if (!broken && !tc::wait_turn(turn, j, p.st, site)) broken = true;
+  tc::fence_proxy_async_global();
+  return turn;
+}
 template <typename Issue>
 __device__ __forceinline__ void ordered_dq_add(const MainTc& p, int b, int h, int ib, int j, bool& broken,
                                                int*& pending, unsigned site, Issue issue) {
@@ -304,14 +320,14 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
   const int n_iter = p.hc * nq_head;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-  // [2] = one per query half (sfull, pfull), per Q/dO stage (qfull, qempty,
-  // qready), or per block parity (dsempty: the dS^T buffer; dqfull, dqempty:
-  // the dQ accumulator)
-  const uint32_t b_kv = smem_u32(bars + 0), b_qfull = smem_u32(bars + 1), b_qempty = smem_u32(bars + 3),
-                 b_sfull = smem_u32(bars + 5), b_pfull = smem_u32(bars + 7), b_dsempty = smem_u32(bars + 9),
-                 b_dqfull = smem_u32(bars + 11), b_dqempty = smem_u32(bars + 13), b_kvready = smem_u32(bars + 15),
-                 b_qready = smem_u32(bars + 16);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+  // [kQS] = one per Q/dO stage (qfull, qempty, qready); [2] = one per query
+  // half (sfull, pfull) or per block parity (dsempty: the dS^T buffer;
+  // dqfull, dqempty: the dQ accumulator)
+  const uint32_t b_kv = smem_u32(bars + 0), b_qfull = smem_u32(bars + 1), b_qempty = smem_u32(bars + 4),
+                 b_sfull = smem_u32(bars + 7), b_pfull = smem_u32(bars + 9), b_dsempty = smem_u32(bars + 11),
+                 b_dqfull = smem_u32(bars + 13), b_dqempty = smem_u32(bars + 15), b_kvready = smem_u32(bars + 17),
+                 b_qready = smem_u32(bars + 18);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 21);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* sL = reinterpret_cast<float*>(sm + OFF_LD);   // [2][128]
   float* sD = sL + 256;                                // [2][128]
@@ -319,9 +335,10 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(b_kv, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kQS; ++s) {
       mbar_init(b_qfull + 8 * s, 1);
       mbar_init(b_qempty + 8 * s, 1);
+      mbar_init(b_qready + 8 * s, 1);
     }
     for (int g = 0; g < 2; ++g) {
       mbar_init(b_sfull + 8 * g, 1);
@@ -331,8 +348,6 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       mbar_init(b_dqempty + 8 * g, 128);
     }
     mbar_init(b_kvready, 1);
-    mbar_init(b_qready, 1);
-    mbar_init(b_qready + 8, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -357,7 +372,7 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
         *reinterpret_cast<uint4*>(sm + off + (from + i / 8) * 128 + (i % 8) * 16) = make_uint4(0, 0, 0, 0);
     };
     auto issue = [&](int it) -> bool {
-      const int st = it & 1, use = it >> 1;
+      const int st = it % kQS, use = it / kQS;
       if (!mbar_wait(b_qempty + 8 * st, (use & 1) ^ 1, abort_flag, p.st, 20)) return false;
       const int h = hk * p.G + hci * p.hc + it % p.hc;
       const int i0 = (nqb - 1 - it / p.hc) * kQ;
@@ -384,14 +399,15 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
     } else {
       ok = false;
     }
-    // Block it+1 is loaded once block it is handed over: the MMA thread asks
-    // for block it+1 before it frees the stage that block it+1 reuses (the dQ
-    // of block it-1 frees it), so the hand-over of block it must not wait on
-    // that stage.
+    // Block it+2 is requested once block it is handed over: its stage is the
+    // one of block it-1, which the MMA thread frees only after it has asked
+    // for block it (S of block it follows the dV, dK of block it-1 that free
+    // it), so the hand-over of block it must not wait on that stage.
     if (lane == 0 && ok && n_iter > 0) ok = issue(0);
+    if (lane == 0 && ok && n_iter > 1) ok = issue(1);
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     for (int it = 0; ok && it < n_iter; ++it) {
-      const int st = it & 1, use = it >> 1;
+      const int st = it % kQS, use = it / kQS;
       if (!mbar_wait(b_qfull + 8 * st, use & 1, &no_abort, p.st, 29)) break;
       const int i0 = (nqb - 1 - it / p.hc) * kQ;
       const int qrows = min(kQ, len - i0);
@@ -403,7 +419,7 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(b_qready + 8 * st);
       int nxt = 1;
-      if (lane == 0 && it + 1 < n_iter) nxt = issue(it + 1) ? 1 : 0;
+      if (lane == 0 && it + 2 < n_iter) nxt = issue(it + 2) ? 1 : 0;
       if (!__shfl_sync(0xffffffffu, nxt, 0)) break;
     }
   } else if (warp == 1) {
@@ -425,12 +441,12 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       const uint64_t d_k = sdesc(sbase + OFF_K, 16, 1024), d_v = sdesc(sbase + OFF_V, 16, 1024);
       const uint64_t d_kmn = sdesc(sbase + OFF_K, 8192, 1024);            // K as the MN-major B of dQ
       const uint64_t d_ds_mn = sdesc(sbase + OFF_DS, kTile, 1024);        // dS^T as the MN-major A of dQ
-      // per Q/dO stage (1 = the second stage, kTile bytes on); per dS buffer and half
+      // per Q/dO stage (stage st is st kTiles on); per dS buffer and half
       const uint64_t d_q0 = sdesc(sbase + OFF_Q, 16, 1024), d_do0 = sdesc(sbase + OFF_DO, 16, 1024);
       const uint64_t d_qmn0 = sdesc(sbase + OFF_Q, 8192, 1024), d_domn0 = sdesc(sbase + OFF_DO, 8192, 1024);
       constexpr uint64_t kTileStep = kTile / 16;   // one tile further on, in descriptor units
       auto sdp = [&](int it, int g) {   // S^T, dP^T of half g: M 128 keys, N 64 queries
-        const int st = it & 1;
+        const int st = it % kQS;
         const uint64_t bq = d_q0 + st * kTileStep + g * (kTileStep / 2),
                        bdo = d_do0 + st * kTileStep + g * (kTileStep / 2);
         const uint32_t ts = tbase + TM_S + g * 128, tdp = ts + 64;
@@ -441,20 +457,20 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
         mma_commit(b_sfull + 8 * g);
       };
       auto dvdk = [&](int it, int g) {  // dV += P^T dO, dK += dS^T Q over the 64 queries of half g
-        const int st = it & 1;
+        const int st = it % kQS;
+        // P^T (dS^T) of this half: queries 0-31 packed in columns 0-15, 32-63
+        // in 32-47 of its S^T (dP^T) columns; a k-step of 16 queries is 8 columns
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
           const int kk = 4 * g + k4;
-          // P^T of this half: 64 queries = 32 columns of packed bf16 pairs, 8 per k-step
-          mma_bf16_ts(tbase + TM_DV, tbase + TM_S + g * 128 + 8 * k4, d_domn0 + st * kTileStep + 128 * kk, id_kv,
-                      (it > 0) || (kk > 0));
+          mma_bf16_ts(tbase + TM_DV, tbase + TM_S + g * 128 + 32 * (k4 >> 1) + 8 * (k4 & 1),
+                      d_domn0 + st * kTileStep + 128 * kk, id_kv, (it > 0) || (kk > 0));
         }
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
           const int kk = 4 * g + k4;
-          // dS^T of this half, packed over the first 32 dP^T columns
-          mma_bf16_ts(tbase + TM_DK, tbase + TM_S + g * 128 + 64 + 8 * k4, d_qmn0 + st * kTileStep + 128 * kk,
-                      id_kv, (it > 0) || (kk > 0));
+          mma_bf16_ts(tbase + TM_DK, tbase + TM_S + g * 128 + 64 + 32 * (k4 >> 1) + 8 * (k4 & 1),
+                      d_qmn0 + st * kTileStep + 128 * kk, id_kv, (it > 0) || (kk > 0));
         }
       };
       bool ok = mbar_wait(b_kvready, 0, abort_flag, p.st, 21);
@@ -467,13 +483,13 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
         }
       }
       for (int it = 0; ok && it < n_iter; ++it) {
-        const int st = it & 1, a = it & 1, use = it >> 1;
+        const int st = it % kQS, a = it & 1, use = it >> 1;
         const bool more = it + 1 < n_iter;
         if (!mbar_wait(b_pfull, it & 1, abort_flag, p.st, 23)) break;
         fence_after();
         dvdk(it, 0);
         if (more) {
-          if (!mbar_wait(b_qready + 8 * ((it + 1) & 1), ((it + 1) >> 1) & 1, abort_flag, p.st, 22)) break;
+          if (!mbar_wait(b_qready + 8 * ((it + 1) % kQS), ((it + 1) / kQS) & 1, abort_flag, p.st, 22)) break;
           fence_after();
           sdp(it + 1, 0);
         }
@@ -493,11 +509,15 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       }
     }
   } else if (warp < 2 + kSoftWarps) {
-    // ---------------- softmax warps: one key row, 64 queries per thread ----------------
-    // Warps 2-5 own query half 0 of every block, warps 6-9 half 1; the two
-    // groups run independently, each on its own TMEM buffer and P/dS tile.
-    const int g = (warp - 2) >> 2;              // query half
-    const int tg = threadIdx.x - 64 - 128 * g;  // 0..127 within the group
+    // ---------------- softmax warps: one key row, 32 queries per thread ----------------
+    // Warps 2-9 own query half 0 of every block, warps 10-17 half 1; within
+    // a half, its first four warps take the half's first 32 queries and the
+    // other four the last 32.  The halves run independently, each on its own
+    // TMEM buffer; the eight warps of a half meet at a named barrier per block.
+    const int w = warp - 2;
+    const int g = w >> 3;                       // query half
+    const int cc = (w >> 2) & 1;                // which 32 queries of the half
+    const int tg = threadIdx.x - 64 - 256 * g;  // 0..255 within the half's group
     const int q = warp & 3;
     const int kr = q * 32 + lane;
     const int key = j0 + kr;
@@ -507,6 +527,7 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
     // after the current one are fetched one iteration early, so the
     // global-load latency hides behind the current block
     auto fetch = [&](int it) -> float {
+      if (tg >= 128) return 0.f;
       const int h = hk * p.G + hci * p.hc + it % p.hc;
       const int i0 = (nqb - 1 - it / p.hc) * kQ;
       const int qq = 64 * g + (tg & 63);
@@ -519,29 +540,31 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       const int i0 = (nqb - 1 - it / p.hc) * kQ;
       const int qrows = min(kQ, len - i0);
       const int buf = it & 1;
-      (tg < 64 ? sL : sD)[buf * 128 + 64 * g + (tg & 63)] = nxt;
+      if (tg < 128) (tg < 64 ? sL : sD)[buf * 128 + 64 * g + (tg & 63)] = nxt;
       if (it + 1 < n_iter) nxt = fetch(it + 1);
-      named_bar(1 + 2 * g, 128);
+      named_bar(1 + 2 * g, 256);
       if (!mbar_wait(b_sfull + 8 * g, it & 1, &no_abort, p.st, 25)) break;
       fence_after();
       const float* L = sL + buf * 128;
       const float* Dd = sD + buf * 128;
-      // a full half-block strictly below the diagonal needs no masking
-      const bool interior = (!p.causal || i0 > j0) && qrows >= 64 * (g + 1) && len - j0 >= kK;
-      bool stop = false;
+      // 32 queries strictly below the diagonal, all inside the sequence, need no masking
+      const bool interior = (!p.causal || i0 > j0) && qrows >= 64 * g + 32 * (cc + 1) && len - j0 >= kK;
+      // dS^T buffer (it & 1) is free once dQ of block it-2 has read it
+      if (it >= 2 && !mbar_wait(b_dsempty + 8 * (it & 1), ((it >> 1) - 1) & 1, &no_abort, p.st, 26)) break;
+      // 16 queries at a time (few registers live: this kernel runs 22 warps)
+      const uint32_t col = TM_S + g * 128 + cc * 32;
       const uint32_t rowoff = g * kTile + kr * 128;
-#pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {          // 32 queries at a time
-        const uint32_t col = TM_S + g * 128 + cc * 32;
-        uint32_t sr[32], dr[32];
-        tmem_ld32_async(tbase + lane_off + col, sr);
-        tmem_ld32_async(tbase + lane_off + col + 64, dr);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t sr[16], dr[16];
+        tmem_ld16_async(tbase + lane_off + col + 16 * hh, sr);
+        tmem_ld16_async(tbase + lane_off + col + 64 + 16 * hh, dr);
         tmem_wait_ld();
-        uint32_t pk[16], dk[16];   // bf16 pairs of P^T and dS^T
+        uint32_t pk[8], dk[8];   // bf16 pairs of P^T and dS^T
         if (interior) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int qi = 64 * g + cc * 32 + 2 * e;
+          for (int e = 0; e < 8; ++e) {
+            const int qi = 64 * g + cc * 32 + 16 * hh + 2 * e;
             const float p0 = exp2_approx(__uint_as_float(sr[2 * e]) * p.scale_log2 - L[qi]);
             const float p1 = exp2_approx(__uint_as_float(sr[2 * e + 1]) * p.scale_log2 - L[qi + 1]);
             pk[e] = pack_bf16x2(p0, p1);
@@ -550,11 +573,11 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
+          for (int e = 0; e < 8; ++e) {
             float pv[2], dv[2];
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-              const int qi = 64 * g + cc * 32 + 2 * e + k;
+              const int qi = 64 * g + cc * 32 + 16 * hh + 2 * e + k;
               const bool valid = kvalid && qi < qrows && (!p.causal || key <= i0 + qi);
               pv[k] = valid ? exp2_approx(__uint_as_float(sr[2 * e + k]) * p.scale_log2 - L[qi]) : 0.f;
               dv[k] = valid ? pv[k] * (__uint_as_float(dr[2 * e + k]) - Dd[qi]) : 0.f;
@@ -563,23 +586,21 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
             dk[e] = pack_bf16x2(dv[0], dv[1]);
           }
         }
-        // P^T and dS^T into TMEM over S^T / dP^T columns this thread has read
-        // already (the chunk cc of 32 queries packs into 16 columns, at 16 cc)
-        tmem_st16(tbase + lane_off + TM_S + g * 128 + 16 * cc, pk);
-        tmem_st16(tbase + lane_off + TM_S + g * 128 + 64 + 16 * cc, dk);
-        // dS^T buffer (it & 1) is free once dQ of block it-2 has read it
-        if (cc == 0 && it >= 2 && !mbar_wait(b_dsempty + 8 * (it & 1), ((it >> 1) - 1) & 1, &no_abort, p.st, 26)) {
-          stop = true;
-          break;
-        }
+        // P^T and dS^T into TMEM over S^T / dP^T columns already read: this
+        // thread's 32 queries (columns 32 cc .. 32 cc + 31 of the half) pack
+        // into the first 16 of those, these 16 queries into 8 at 32 cc + 8 hh
+        // -- columns whose S / dP it loaded in sub-step 0.  The other
+        // sub-group (the same TMEM lanes) reads and writes only its own 32.
+        tmem_st8(tbase + lane_off + TM_S + g * 128 + 32 * cc + 8 * hh, pk);
+        tmem_st8(tbase + lane_off + TM_S + g * 128 + 64 + 32 * cc + 8 * hh, dk);
+        // and dS^T to shared: 16 queries = 32 bytes = two 16-byte chunks of the swizzled row
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t phys = (((cc * 4 + u) ^ (kr & 7)) * 16);
+        for (int u = 0; u < 2; ++u) {
+          const uint32_t phys = (((cc * 4 + 2 * hh + u) ^ (kr & 7)) * 16);
           *reinterpret_cast<uint4*>(sm + OFF_DS + (it & 1) * 2 * kTile + rowoff + phys) =
               make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
         }
       }
-      if (stop) break;
       tmem_wait_st();
       fence_before();
       fence_async_smem();
@@ -600,56 +621,55 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       const int a = it & 1;
       if (!mbar_wait(b_dqfull + 8 * a, (it >> 1) & 1, &no_abort, p.st, 27)) { ok = false; break; }
       fence_after();
-      float v[64];
-      tmem_ld32(tbase + lane_off + TM_DQ + 64 * a, v);
-      tmem_ld32(tbase + lane_off + TM_DQ + 64 * a + 32, v + 32);
-      fence_before();
-      mbar_arrive(b_dqempty + 8 * a);
-      if (t == 0) bulk_wait_read_all();
-      named_bar(2, 128);
-#pragma unroll
-      for (int half = 0; half < 2; ++half)
+      // 32 columns at a time through one staging box (few registers live:
+      // this kernel runs 22 warps; shared memory goes to the Q / dO stages)
+      int* turn = nullptr;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        if (t == 0) bulk_wait_read_all();   // the staging box is free
+        named_bar(2, 128);
+        float v[32];
+        tmem_ld32(tbase + lane_off + TM_DQ + 64 * a + 32 * half, v);
+        if (half == 1) {
+          fence_before();
+          mbar_arrive(b_dqempty + 8 * a);
+        }
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           const uint32_t phys = ((g ^ (r & 7)) * 16);
-          *reinterpret_cast<float4*>(sm + OFF_ST + half * kTile + r * 128 + phys) =
-              make_float4(v[half * 32 + 4 * g], v[half * 32 + 4 * g + 1], v[half * 32 + 4 * g + 2],
-                          v[half * 32 + 4 * g + 3]);
+          *reinterpret_cast<float4*>(sm + OFF_ST + r * 128 + phys) =
+              make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
         }
-      fence_async_smem();
-      named_bar(2, 128);
-      if (t == 0)
-        ordered_dq_add(p, b, h, i0 / kQ, j, chain_broken, dq_pending, 30, [&] {
-          tma_reduce_add_2d(&tmdQ, stage, h * kD, s0 + i0);
-          tma_reduce_add_2d(&tmdQ, stage + kTile, h * kD + 32, s0 + i0);
-        });
+        fence_async_smem();
+        named_bar(2, 128);
+        if (t == 0) {
+          if (half == 0) turn = dq_turn_acquire(p, b, h, i0 / kQ, j, chain_broken, dq_pending, 30);
+          tma_reduce_add_2d(&tmdQ, stage, h * kD + 32 * half, s0 + i0);
+          bulk_commit();
+        }
+      }
+      if (t == 0) dq_pending = turn;
     }
     if (t == 0) dq_turn_flush(dq_pending, j);   // pass the last turn on, even after a failure
     if (ok) {
       // every MMA has completed (the last dQ commit covers them all): drain dK, dV
 #pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        float v[64];
-        const uint32_t col = which == 0 ? TM_DK : TM_DV;
-        tmem_ld32(tbase + lane_off + col, v);
-        tmem_ld32(tbase + lane_off + col + 32, v + 32);
+      for (int pass = 0; pass < 4; ++pass) {   // dK then dV, 32 columns at a time
+        const uint32_t col = (pass < 2 ? TM_DK : TM_DV) + 32 * (pass & 1);
         if (t == 0) bulk_wait_read_all();
         named_bar(2, 128);
+        float v[32];
+        tmem_ld32(tbase + lane_off + col, v);
 #pragma unroll
-        for (int half = 0; half < 2; ++half)
-#pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            const uint32_t phys = ((g ^ (r & 7)) * 16);
-            *reinterpret_cast<float4*>(sm + OFF_ST + half * kTile + r * 128 + phys) =
-                make_float4(v[half * 32 + 4 * g], v[half * 32 + 4 * g + 1], v[half * 32 + 4 * g + 2],
-                            v[half * 32 + 4 * g + 3]);
-          }
+        for (int g = 0; g < 8; ++g) {
+          const uint32_t phys = ((g ^ (r & 7)) * 16);
+          *reinterpret_cast<float4*>(sm + OFF_ST + r * 128 + phys) =
+              make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+        }
         fence_async_smem();
         named_bar(2, 128);
         if (t == 0) {
-          const CUtensorMap* m = which == 0 ? &tmdK : &tmdV;
-          tma_reduce_add_2d(m, stage, hk * kD, s0 + j0);
-          tma_reduce_add_2d(m, stage + kTile, hk * kD + 32, s0 + j0);
+          tma_reduce_add_2d(pass < 2 ? &tmdK : &tmdV, stage, hk * kD + 32 * (pass & 1), s0 + j0);
           bulk_commit();
         }
       }

@@ -131,22 +131,23 @@ def dprep(nj, n_stages, heads, split_pfull=True, warps=2):
     return roles, {b: soft_names for b in bars}
 
 
-def _q_producer(n):
-    """Q / dO ring of two stages behind one K/V load (both main kernels)."""
+def _q_producer(n, stages=2):
+    """Q / dO ring behind one K/V load: block it + stages - 1 is requested once
+    block it is handed over (two stages: head dim 128; three: head dim 64)."""
     prod = [("sig", ("kvready", 0))]
 
     def issue(it):
-        if it >= 2:
-            prod.append(("wait", ring("qempty", it - 2, 2)))
-        prod.append(("sig", ring("qfull", it, 2)))
+        if it >= stages:
+            prod.append(("wait", ring("qempty", it - stages, stages)))
+        prod.append(("sig", ring("qfull", it, stages)))
 
-    if n:
-        issue(0)
+    for it in range(min(stages - 1, n)):
+        issue(it)
     for it in range(n):
-        prod.append(("wait", ring("qfull", it, 2)))
-        prod.append(("sig", ring("qready", it, 2)))
-        if it + 1 < n:
-            issue(it + 1)
+        prod.append(("wait", ring("qfull", it, stages)))
+        prod.append(("sig", ring("qready", it, stages)))
+        if it + stages - 1 < n:
+            issue(it + stages - 1)
     return prod
 
 
@@ -168,23 +169,23 @@ def main64(n, warps=2):
     """Main pass, head dim 64: two query halves, each with its own S/dP buffer
     (where its P lands too) and group of softmax warps (a named barrier per
     block); the dS^T tile and the dQ accumulator are double-buffered by block,
-    so a half waits only for the dQ of two blocks back."""
+    so a half waits only for the dQ of two blocks back; Q / dO have three stages."""
     mma = [("wait", ("kvready", 0))]
     if n:
-        mma += [("wait", ring("qready", 0, 2)), ("sig", (("sfull", 0), 0)), ("sig", (("sfull", 1), 0))]
+        mma += [("wait", ring("qready", 0, 3)), ("sig", (("sfull", 0), 0)), ("sig", (("sfull", 1), 0))]
     for it in range(n):
         more = it + 1 < n
         mma.append(("wait", (("pfull", 0), it)))
         if more:
-            mma += [("wait", ring("qready", it + 1, 2)), ("sig", (("sfull", 0), it + 1))]
+            mma += [("wait", ring("qready", it + 1, 3)), ("sig", (("sfull", 0), it + 1))]
         mma.append(("wait", (("pfull", 1), it)))
-        mma.append(("sig", ring("qempty", it, 2)))
+        mma.append(("sig", ring("qempty", it, 3)))
         if it >= 2:
             mma.append(("wait", ring("dqempty", it - 2, 2)))
         mma += [("sig", ring("dqfull", it, 2)), ("sig", ring("dsempty", it, 2))]
         if more:
             mma.append(("sig", (("sfull", 1), it + 1)))
-    roles = {"producer": _q_producer(n), "mma": mma}
+    roles = {"producer": _q_producer(n, 3), "mma": mma}
     arrivers = {}
     for g in (0, 1):
         names = [f"softmax{g}.{w}" for w in range(warps)]
