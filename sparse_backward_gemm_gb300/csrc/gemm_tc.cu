@@ -681,9 +681,10 @@ cudaError_t launch_tc_gemm(const Ctx& c, const TcGemm& g) {
   }
   // dX: both K-major; dW: both MN-major; the forward's Y = X W: A K-major, B MN-major
   if (g.a_mn_major && !g.b_mn_major) return cudaErrorNotSupported;
-  // Work split (launches given stream-K scratch): auto -- whole tiles unless
-  // the last wave would run less than 7/8 full, then the tail is cut into
-  // stream-K ranges (decided on the device from the real tile count).
+  // Work split (launches given stream-K scratch): the auto rule of Split --
+  // whole tiles unless they would fill the waves below 60% (90% on a
+  // reduction of 128+ k-slices), then a stream-K tail, decided on the device
+  // from the real tile count; long static reductions are stream-K throughout.
   // COLLIDER_GEMM_STREAMK=0/1/2/3 forces whole tiles / stream-K / hybrid / auto.
   static const int split_env = [] {
     const char* e = getenv("COLLIDER_GEMM_STREAMK");
@@ -695,12 +696,17 @@ cudaError_t launch_tc_gemm(const Ctx& c, const TcGemm& g) {
     const char* e = getenv("COLLIDER_GEMM_PAIR");
     return e ? atoi(e) : -1;
   }();
-  const bool pair = pair_env != 0 && bn == 256;
+  // A long static reduction (>= 128 k-slices: the dX of the MLP up-projection)
+  // runs as lone CTAs cut evenly by stream-K: measured against 2-SM pairs with
+  // a stream-K tail, the time was the same and the pairs' tail, walking the
+  // k-ranges of many tiles at once, read 2.1x the DRAM bytes (417 against 195 MB).
+  const bool long_k = g.dyn != 2 && g.K / BK >= 128 && g.partial && g.counters;
+  const bool pair = pair_env != 0 && bn == 256 && !long_k;
   const int mode = pair ? 2 : 0;
   // counters the stream-K fix-up needs: one per tile, and per CTA of a pair
   const long long m_tiles = (g.M + BM - 1) / BM, n_tiles = (g.N + bn - 1) / bn;
   const long long max_ctrs = (pair ? 2 * ((m_tiles + 1) / 2) : m_tiles) * n_tiles;
-  const int split = split_env >= 0 ? split_env : 3;
+  const int split = split_env >= 0 ? split_env : (long_k ? 1 : 3);
   const bool sk = split != 0 && g.partial && g.counters && max_ctrs <= g.counter_cap;
   CUtensorMap ma, mb;
   // A: K-major [M rows, K] or MN-major [K rows, M]; B: K-major [N rows, K]
