@@ -201,7 +201,8 @@ __global__ void attn_finalize_kernel(AttnK p, int DH) {
 // 128 keys, a chunk of hc query heads of the group); items are numbered key
 // block first, so the heavy (early) key blocks start first.
 //   warp 0      TMA: K, V once; Q_i, dO_i per iteration (2 stages)
-//   warp 1      TMEM owner; one lane issues the MMAs, per 64-query half g:
+//   warp 1      TMEM owner; the converged warp waits, one elected lane issues
+//               the MMAs, per 64-query half g:
 //                 S^T = K Q_g^T, dP^T = V dO_g^T       (M 128 keys, N 64 queries)
 //                 dV += P_g^T dO_g, dK += dS_g^T Q_g   (M 128 keys, N 64; A
 //                                                       = P^T, dS^T from TMEM)
@@ -210,30 +211,34 @@ __global__ void attn_finalize_kernel(AttnK p, int DH) {
 //               of the half's 64 queries per thread: P^T, dS^T from TMEM ->
 //               bf16 -> back into TMEM over the consumed S^T / dP^T columns;
 //               dS^T also to shared (double-buffered by block) for dQ
-//   warps 18-21 one query row per thread: dQ from TMEM -> shared -> TMA
-//               reduce-add into the f32 dQ accumulator; at the end dK, dV
-//               likewise into their accumulators
+//   warps 18-21 one query row per thread: dQ from TMEM into two staging
+//               boxes (the TMEM buffer is handed back once read); at the end
+//               dK, dV through the dS^T buffers into their accumulators
+//   warps 22-23 one lane each, even / odd blocks: the dQ reduce-adds, in
+//               key-block order, each turn passed on once its add completed
 // TMEM columns: half 0 S^T 0-63 (P^T of its queries 0-31 in 0-15, of 32-63
 // in 32-47, once formed), dP^T 64-127 (dS^T likewise); half 1 the same from
 // 128; dV 256-319, dK 320-383, dQ 384-447 and 448-511 (double-buffered by
 // block).
-// P never goes through shared memory and dS has a buffer per block parity,
-// so a softmax half never waits for the previous block's dQ: only for the
-// dQ two blocks back, long done.
+// P never goes through shared memory and dS^T has a buffer per block parity,
+// so a softmax half waits only for the dQ of two blocks back.  The dQ adds
+// of consecutive blocks overlap: a reducer waits for its add to complete
+// (the next key block may add only then) while the other adds the next one.
 namespace tcattn {
 constexpr int kQ = 128, kK = 128, kD = 64;
 constexpr uint32_t kTile = kQ * kD * 2;                 // 16 KB: 128 rows x 128 bytes
-constexpr int kQS = 3;                                  // Q / dO stages
+constexpr int kQS = 2;                                  // Q / dO stages
 // Q and dO: kQS stages of one kTile each; dS^T buffers: two (block parity),
-// each two halves of one kTile; staging: one [128 rows x 32 f32] box
+// each two halves of one kTile; dQ staging: two [128 rows x 32 f32] boxes.
+// At the end of the item the dS^T buffers take dK and dV for their adds.
 constexpr uint32_t OFF_K = 0, OFF_V = kTile, OFF_Q = 2 * kTile, OFF_DO = OFF_Q + kQS * kTile,
-                   OFF_DS = OFF_DO + kQS * kTile, OFF_ST = OFF_DS + 4 * kTile, OFF_LD = OFF_ST + kTile,
+                   OFF_DS = OFF_DO + kQS * kTile, OFF_ST = OFF_DS + 4 * kTile, OFF_LD = OFF_ST + 2 * kTile,
                    OFF_BAR = OFF_LD + 2048;
 constexpr size_t kSmem = 1024 + OFF_BAR + 256;
 static_assert(kSmem <= 232448, "shared memory");
 constexpr uint32_t TM_S = 0, TM_DV = 256, TM_DK = 320, TM_DQ = 384;
 constexpr int kSoftWarps = 16;                      // four per TMEM lane quadrant
-constexpr int kThreads = 32 * (2 + kSoftWarps + 4);
+constexpr int kThreads = 32 * (2 + kSoftWarps + 4 + 2);
 }  // namespace tcattn
 
 struct MainTc {
@@ -272,12 +277,10 @@ __device__ __forceinline__ void dq_turn_flush(int*& pending, int j) {
   tc::release_turn(pending, j + 1);
   pending = nullptr;
 }
-// The first half of ordered_dq_add, for a caller that issues its adds in
-// several steps: pass the previous turn on, wait for this one, and return it
-// (the caller stores it in `pending` after its last add is committed).
-__device__ __forceinline__ int* dq_turn_acquire(const MainTc& p, int b, int h, int ib, int j, bool& broken,
-                                                int*& pending, unsigned site) {
-  dq_turn_flush(pending, j);
+// For a caller that passes the turn on itself (dq_turn_flush once its add
+// has completed): wait for this tile's turn and return it.
+__device__ __forceinline__ int* dq_turn_wait(const MainTc& p, int b, int h, int ib, int j, bool& broken,
+                                             unsigned site) {
   int* turn = p.order + 1 + ((long long)b * p.H + h) * p.nqb_max + ib;
   if (!broken && !tc::wait_turn(turn, j, p.st, site)) broken = true;
   tc::fence_proxy_async_global();
@@ -321,12 +324,12 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   // [kQS] = one per Q/dO stage (qfull, qempty, qready); [2] = one per query
-  // half (sfull, pfull) or per block parity (dsempty: the dS^T buffer;
-  // dqfull, dqempty: the dQ accumulator)
+  // half (sfull, pfull) or per block parity (dsempty: the dS^T buffer, handed
+  // back by the epilogue; dqfull, dqempty: the dQ accumulator)
   const uint32_t b_kv = smem_u32(bars + 0), b_qfull = smem_u32(bars + 1), b_qempty = smem_u32(bars + 4),
                  b_sfull = smem_u32(bars + 7), b_pfull = smem_u32(bars + 9), b_dsempty = smem_u32(bars + 11),
                  b_dqfull = smem_u32(bars + 13), b_dqempty = smem_u32(bars + 15), b_kvready = smem_u32(bars + 17),
-                 b_qready = smem_u32(bars + 18);
+                 b_qready = smem_u32(bars + 18), b_staged = smem_u32(bars + 23), b_boxfree = smem_u32(bars + 25);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 21);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* sL = reinterpret_cast<float*>(sm + OFF_LD);   // [2][128]
@@ -348,6 +351,10 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       mbar_init(b_dqempty + 8 * g, 128);
     }
     mbar_init(b_kvready, 1);
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(b_staged + 8 * r, 1);
+      mbar_init(b_boxfree + 8 * r, 1);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -399,12 +406,12 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
     } else {
       ok = false;
     }
-    // Block it+2 is requested once block it is handed over: its stage is the
-    // one of block it-1, which the MMA thread frees only after it has asked
-    // for block it (S of block it follows the dV, dK of block it-1 that free
-    // it), so the hand-over of block it must not wait on that stage.
-    if (lane == 0 && ok && n_iter > 0) ok = issue(0);
-    if (lane == 0 && ok && n_iter > 1) ok = issue(1);
+    // Block it+kQS-1 is requested once block it is handed over: its stage is
+    // the one of block it-1, which the MMA thread frees (after dV, dK of
+    // block it-1) without waiting for any later block, so the hand-over of
+    // block it never waits on that stage.
+    for (int i = 0; i < kQS - 1; ++i)
+      if (lane == 0 && ok && n_iter > i) ok = issue(i);
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     for (int it = 0; ok && it < n_iter; ++it) {
       const int st = it % kQS, use = it / kQS;
@@ -419,19 +426,24 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(b_qready + 8 * st);
       int nxt = 1;
-      if (lane == 0 && it + 2 < n_iter) nxt = issue(it + 2) ? 1 : 0;
+      if (lane == 0 && it + kQS - 1 < n_iter) nxt = issue(it + kQS - 1) ? 1 : 0;
       if (!__shfl_sync(0xffffffffu, nxt, 0)) break;
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
+    {
+      // ---------------- MMA issuer: the converged warp waits, one elected lane issues ----------------
       // Query half g of iteration it has its own S^T / dP^T columns in TMEM
       // (buffer g), where its P^T lands too, so the MMAs of one half run while
       // the softmax warps of the other half work:
       //   S, dP (it, 0) | S, dP (it, 1) | [P(it, 0)] dV, dK (it, 0) | S, dP (it+1, 0)
-      //   | [P(it, 1)] dV, dK (it, 1) | dQ (it) | S, dP (it+1, 1) | ...
+      //   | [P(it, 1)] dV, dK (it, 1) | S, dP (it+1, 1) | dQ (it) | ...
       // MMAs issued by this thread run in issue order, so S (it+1, g) cannot
-      // overwrite P (it, g) before dV (it, g) has read it.
+      // overwrite P (it, g) before dV (it, g) has read it; dQ (it) reads dS^T
+      // from shared memory, so S, dP (it+1, 1) need not wait for it.
+      const bool leader = elect_one();
+      auto wait = [&](uint32_t bar, uint32_t parity, unsigned site) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.st, site)) != 0;
+      };
       constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);
       constexpr uint32_t id_kv = idesc_bf16(128, 64, false, true);
       constexpr uint32_t id_q = idesc_bf16(128, 64, true, true);
@@ -450,6 +462,7 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
         const uint64_t bq = d_q0 + st * kTileStep + g * (kTileStep / 2),
                        bdo = d_do0 + st * kTileStep + g * (kTileStep / 2);
         const uint32_t ts = tbase + TM_S + g * 128, tdp = ts + 64;
+        if (!leader) return;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) mma_bf16(ts, d_k + 2 * kk, bq + 2 * kk, id_s, kk > 0);
 #pragma unroll
@@ -458,6 +471,7 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       };
       auto dvdk = [&](int it, int g) {  // dV += P^T dO, dK += dS^T Q over the 64 queries of half g
         const int st = it % kQS;
+        if (!leader) return;
         // P^T (dS^T) of this half: queries 0-31 packed in columns 0-15, 32-63
         // in 32-47 of its S^T (dP^T) columns; a k-step of 16 queries is 8 columns
 #pragma unroll
@@ -473,9 +487,9 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
                       d_qmn0 + st * kTileStep + 128 * kk, id_kv, (it > 0) || (kk > 0));
         }
       };
-      bool ok = mbar_wait(b_kvready, 0, abort_flag, p.st, 21);
+      bool ok = wait(b_kvready, 0, 21);
       if (ok && n_iter > 0) {
-        ok = mbar_wait(b_qready, 0, abort_flag, p.st, 22);
+        ok = wait(b_qready, 0, 22);
         if (ok) {
           fence_after();
           sdp(0, 0);
@@ -485,26 +499,28 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       for (int it = 0; ok && it < n_iter; ++it) {
         const int st = it % kQS, a = it & 1, use = it >> 1;
         const bool more = it + 1 < n_iter;
-        if (!mbar_wait(b_pfull, it & 1, abort_flag, p.st, 23)) break;
+        if (!wait(b_pfull, it & 1, 23)) break;
         fence_after();
         dvdk(it, 0);
         if (more) {
-          if (!mbar_wait(b_qready + 8 * ((it + 1) % kQS), ((it + 1) / kQS) & 1, abort_flag, p.st, 22)) break;
+          if (!wait(b_qready + 8 * ((it + 1) % kQS), ((it + 1) / kQS) & 1, 22)) break;
           fence_after();
           sdp(it + 1, 0);
         }
-        if (!mbar_wait(b_pfull + 8, it & 1, abort_flag, p.st, 23)) break;
+        if (!wait(b_pfull + 8, it & 1, 23)) break;
         fence_after();
         dvdk(it, 1);
-        mma_commit(b_qempty + 8 * st);   // Q, dO of this block are read for the last time
+        if (leader) mma_commit(b_qempty + 8 * st);   // Q, dO of this block are read for the last time
         // dQ accumulator a was drained of block it-2
-        if (use > 0 && !mbar_wait(b_dqempty + 8 * a, (use - 1) & 1, abort_flag, p.st, 24)) break;
+        if (use > 0 && !wait(b_dqempty + 8 * a, (use - 1) & 1, 24)) break;
         fence_after();
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < kK / 16; ++kk)     // k = keys; dS read MN-major from the dS^T tiles
-          mma_bf16(tbase + TM_DQ + 64 * a, d_ds_mn + 2 * a * kTileStep + 128 * kk, d_kmn + 128 * kk, id_q, kk > 0);
-        mma_commit(b_dqfull + 8 * a);
-        mma_commit(b_dsempty + 8 * a);   // dS^T buffer a is read for the last time
+          for (int kk = 0; kk < kK / 16; ++kk)     // k = keys; dS read MN-major from the dS^T tiles
+            mma_bf16(tbase + TM_DQ + 64 * a, d_ds_mn + 2 * a * kTileStep + 128 * kk, d_kmn + 128 * kk, id_q, kk > 0);
+          mma_commit(b_dqfull + 8 * a);
+          mma_commit(b_dsempty + 8 * a);   // dS^T buffer a is read for the last time
+        }
         if (more) sdp(it + 1, 1);
       }
     }
@@ -606,75 +622,92 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       fence_async_smem();
       mbar_arrive(b_pfull + 8 * g);
     }
-  } else {
+  } else if (warp < 2 + kSoftWarps + 4) {
     // ---------------- dQ / dK / dV epilogue: one row per thread ----------------
     const int t = threadIdx.x - 32 * (2 + kSoftWarps);
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    const uint32_t stage = sbase + OFF_ST;
-    bool ok = true, chain_broken = false;
-    int* dq_pending = nullptr;   // the dQ turn this thread still has to pass on
+    bool ok = true;
+    // one row of 32 f32 into box `box` (128 rows x 128 bytes, 128-byte swizzle)
+    auto stage32 = [&](uint32_t box, const float* v) {
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const uint32_t phys = ((g ^ (r & 7)) * 16);
+        *reinterpret_cast<float4*>(sm + box + r * 128 + phys) =
+            make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+      }
+    };
     for (int it = 0; it < n_iter; ++it) {
       const int h = hk * p.G + hci * p.hc + it % p.hc;
       const int i0 = (nqb - 1 - it / p.hc) * kQ;
       const int a = it & 1;
       if (!mbar_wait(b_dqfull + 8 * a, (it >> 1) & 1, &no_abort, p.st, 27)) { ok = false; break; }
       fence_after();
-      // 32 columns at a time through one staging box (few registers live:
-      // this kernel runs 22 warps; shared memory goes to the Q / dO stages)
-      int* turn = nullptr;
+      // dQ through the two staging boxes (32 columns each); the boxes are free
+      // once the previous block's adds have read them
+      // the boxes are free once the reducer of the previous block saw its adds read them
+      if (it > 0 && !mbar_wait(b_boxfree + 8 * ((it - 1) & 1), ((it - 1) >> 1) & 1, &no_abort, p.st, 31)) {
+        ok = false;
+        break;
+      }
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
-        if (t == 0) bulk_wait_read_all();   // the staging box is free
-        named_bar(2, 128);
         float v[32];
         tmem_ld32(tbase + lane_off + TM_DQ + 64 * a + 32 * half, v);
         if (half == 1) {
           fence_before();
           mbar_arrive(b_dqempty + 8 * a);
         }
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const uint32_t phys = ((g ^ (r & 7)) * 16);
-          *reinterpret_cast<float4*>(sm + OFF_ST + r * 128 + phys) =
-              make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-        }
-        fence_async_smem();
-        named_bar(2, 128);
-        if (t == 0) {
-          if (half == 0) turn = dq_turn_acquire(p, b, h, i0 / kQ, j, chain_broken, dq_pending, 30);
-          tma_reduce_add_2d(&tmdQ, stage, h * kD + 32 * half, s0 + i0);
-          bulk_commit();
-        }
+        stage32(OFF_ST + half * kTile, v);
       }
-      if (t == 0) dq_pending = turn;
+      fence_async_smem();
+      named_bar(2, 128);
+      if (t == 0) mbar_arrive(b_staged + 8 * a);
     }
-    if (t == 0) dq_turn_flush(dq_pending, j);   // pass the last turn on, even after a failure
     if (ok) {
-      // every MMA has completed (the last dQ commit covers them all): drain dK, dV
+      // Every MMA has completed (the last dQ commit covers them all), so the
+      // dS^T buffers are free: dK into buffer 0, dV into buffer 1.
 #pragma unroll 1
       for (int pass = 0; pass < 4; ++pass) {   // dK then dV, 32 columns at a time
         const uint32_t col = (pass < 2 ? TM_DK : TM_DV) + 32 * (pass & 1);
-        if (t == 0) bulk_wait_read_all();
-        named_bar(2, 128);
         float v[32];
         tmem_ld32(tbase + lane_off + col, v);
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const uint32_t phys = ((g ^ (r & 7)) * 16);
-          *reinterpret_cast<float4*>(sm + OFF_ST + r * 128 + phys) =
-              make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-        }
-        fence_async_smem();
-        named_bar(2, 128);
-        if (t == 0) {
-          tma_reduce_add_2d(pass < 2 ? &tmdK : &tmdV, stage, hk * kD + 32 * (pass & 1), s0 + j0);
-          bulk_commit();
-        }
+        stage32(OFF_DS + pass * kTile, v);
+      }
+      fence_async_smem();
+      named_bar(2, 128);
+      if (t == 0) {
+#pragma unroll 1
+        for (int pass = 0; pass < 4; ++pass)
+          tma_reduce_add_2d(pass < 2 ? &tmdK : &tmdV, sbase + OFF_DS + pass * kTile, hk * kD + 32 * (pass & 1),
+                            s0 + j0);
+        bulk_commit();
       }
     }
     if (t == 0) bulk_wait_all();
+  } else if (lane == 0) {
+    // ---------------- dQ reducers: warp 22 even blocks, warp 23 odd ----------------
+    // Each adds its blocks' dQ tiles in key-block order (the tile's turn),
+    // hands the staging boxes back once the adds have read them, and passes
+    // the turn on as soon as its adds have completed: the two reducers
+    // overlap one block's completion with the next block's adds.
+    const int rr = warp - (2 + kSoftWarps + 4);
+    bool broken = false;
+    for (int it = rr; it < n_iter; it += 2) {
+      const int h = hk * p.G + hci * p.hc + it % p.hc;
+      const int i0 = (nqb - 1 - it / p.hc) * kQ;
+      const int a = it & 1;
+      if (!mbar_wait(b_staged + 8 * a, (it >> 1) & 1, abort_flag, p.st, 32)) break;
+      int* turn = dq_turn_wait(p, b, h, i0 / kQ, j, broken, 30);
+      tma_reduce_add_2d(&tmdQ, sbase + OFF_ST, h * kD, s0 + i0);
+      tma_reduce_add_2d(&tmdQ, sbase + OFF_ST + kTile, h * kD + 32, s0 + i0);
+      bulk_commit();
+      bulk_wait_read_all();
+      mbar_arrive(b_boxfree + 8 * a);
+      dq_turn_flush(turn, j);
+    }
+    bulk_wait_all();
   }
   fence_before();
   __syncthreads();

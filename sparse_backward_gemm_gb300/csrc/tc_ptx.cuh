@@ -103,6 +103,8 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// every bulk group this thread committed, except the most recent one, has completed
+__device__ __forceinline__ void bulk_wait_prior() { asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); }
 // make generic-proxy shared-memory writes visible to the async proxy (TMA, tcgen05)
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void named_bar(int id, int threads) {
@@ -135,6 +137,21 @@ static __device__ __noinline__ bool wait_turn(const int* turn, int want, DevStat
       return false;
     }
   }
+}
+
+// One lane of the (converged) warp returns true.  MMA-issuing code runs in
+// a converged warp with the issue itself under this predicate: measured on
+// the attention block's 40-MMA sequence, a lone lane-0 issuer slows from 26
+// to 64 ns per MMA when busy softmax warps share its scheduler, an elected
+// issuer in a converged warp stays at 21 ns.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }

@@ -3,8 +3,8 @@ CPU: the attention kernels (sparse_backward_gemm_gb300/csrc/attn.cu) and the
 GEMM in its two forms (lone CTAs, 2-SM pairs;
 sparse_backward_gemm_gb300/csrc/gemm_tc.cu).
 
-Each role of a kernel (TMA producer, MMA issuer, softmax warps, epilogue
-warps) is written as its sequence of operations on (barrier, phase) events:
+Each role of a kernel (TMA producer, MMA issuer, softmax warps, epilogue and
+reducer warps) is written as its sequence of operations on (barrier, phase) events:
   sig     a single-arrival completion (a TMA transaction, a tcgen05.commit,
           a one-thread arrive)
   arrive  one of several arrivals a phase needs (warps of a group); the
@@ -133,7 +133,7 @@ def dprep(nj, n_stages, heads, split_pfull=True, warps=2):
 
 def _q_producer(n, stages=2):
     """Q / dO ring behind one K/V load: block it + stages - 1 is requested once
-    block it is handed over (two stages: head dim 128; three: head dim 64)."""
+    block it is handed over (both main passes use two stages)."""
     prod = [("sig", ("kvready", 0))]
 
     def issue(it):
@@ -169,23 +169,26 @@ def main64(n, warps=2):
     """Main pass, head dim 64: two query halves, each with its own S/dP buffer
     (where its P lands too) and group of softmax warps (a named barrier per
     block); the dS^T tile and the dQ accumulator are double-buffered by block,
-    so a half waits only for the dQ of two blocks back; Q / dO have three stages."""
+    so a half waits only for the dQ of two blocks back; Q / dO have two stages.
+    The epilogue warps drain dQ into two staging boxes and hand them to the
+    reducer of the block's parity (one thread each), which hands them back
+    once its reduce-add has read them."""
     mma = [("wait", ("kvready", 0))]
     if n:
-        mma += [("wait", ring("qready", 0, 3)), ("sig", (("sfull", 0), 0)), ("sig", (("sfull", 1), 0))]
+        mma += [("wait", ring("qready", 0, 2)), ("sig", (("sfull", 0), 0)), ("sig", (("sfull", 1), 0))]
     for it in range(n):
         more = it + 1 < n
         mma.append(("wait", (("pfull", 0), it)))
         if more:
-            mma += [("wait", ring("qready", it + 1, 3)), ("sig", (("sfull", 0), it + 1))]
+            mma += [("wait", ring("qready", it + 1, 2)), ("sig", (("sfull", 0), it + 1))]
         mma.append(("wait", (("pfull", 1), it)))
-        mma.append(("sig", ring("qempty", it, 3)))
+        mma.append(("sig", ring("qempty", it, 2)))
         if it >= 2:
             mma.append(("wait", ring("dqempty", it - 2, 2)))
         mma += [("sig", ring("dqfull", it, 2)), ("sig", ring("dsempty", it, 2))]
         if more:
             mma.append(("sig", (("sfull", 1), it + 1)))
-    roles = {"producer": _q_producer(n, 3), "mma": mma}
+    roles = {"producer": _q_producer(n, 2), "mma": mma}
     arrivers = {}
     for g in (0, 1):
         names = [f"softmax{g}.{w}" for w in range(warps)]
@@ -203,13 +206,21 @@ def main64(n, warps=2):
     for name in names:
         ops = []
         for it in range(n):
-            ops += [("wait", ring("dqfull", it, 2)), ("arrive", ring("dqempty", it, 2)),
-                    ("arrive", (("nb", "epi"), 2 * it)), ("wait", (("nb", "epi"), 2 * it)),
-                    ("arrive", (("nb", "epi"), 2 * it + 1)), ("wait", (("nb", "epi"), 2 * it + 1))]
+            ops.append(("wait", ring("dqfull", it, 2)))
+            if it > 0:
+                ops.append(("wait", ring("boxfree", it - 1, 2)))
+            ops += [("arrive", ring("dqempty", it, 2)), ("arrive", (("nb", "epi"), it)), ("wait", (("nb", "epi"), it))]
+            if name == "epilogue0":
+                ops.append(("sig", ring("staged", it, 2)))
+        if n:   # dK, dV through the dS^T buffers
+            ops += [("arrive", (("nb", "epi"), n)), ("wait", (("nb", "epi"), n))]
         roles[name] = ops
     for a in (0, 1):
         arrivers[("dqempty", a)] = names
     arrivers[("nb", "epi")] = names
+    for r in (0, 1):
+        roles[f"reducer{r}"] = [op for it in range(r, n, 2)
+                                for op in (("wait", ring("staged", it, 2)), ("sig", ring("boxfree", it, 2)))]
     return roles, arrivers
 
 
