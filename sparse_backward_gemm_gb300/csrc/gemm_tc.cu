@@ -418,39 +418,50 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && (!TWO || rank == 0)) {
+    if (!TWO || rank == 0) {
       // ---------------- MMA issuer (the even CTA of a pair in 2-SM mode) ----------------
+      // The converged warp waits; one elected lane issues the MMAs and commits.
+      const bool leader = elect_one();
+      auto wait = [&](uint32_t bar, uint32_t parity, unsigned site) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.st, site)) != 0;
+      };
       constexpr uint32_t idesc = TWO ? idesc_bf16(2 * BM, BN, A_MN, B_MN) : make_idesc<BN, A_MN, B_MN>();
       int stage = 0;
       uint32_t phase = 0;
       int seg = 0;
       SegIter si(sp);
       int t, k0, k1;
-      while (!*abort_flag && si.next(t, k0, k1)) {
+      while (si.next(t, k0, k1) && !__any_sync(0xffffffffu, *abort_flag != 0)) {
         const int acc = seg & 1;
         const uint32_t aph = (seg >> 1) & 1;
-        if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1u, abort_flag, p.st, 2)) break;
+        if (!wait(tempty0 + 8 * acc, aph ^ 1u, 2)) break;
         fence_after();
         const uint32_t d = tmem_base + acc * BN;
         bool ok = true;
         for (int kb = k0; kb < k1; ++kb) {
-          if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.st, 3)) { ok = false; break; }
+          if (!wait(full0 + 8 * stage, phase, 3)) { ok = false; break; }
           fence_after();
-          const uint32_t sa = smem_u32(smem + stage * kStageBytes), sb = sa + Cfg::kABytes;
+          if (leader) {
+            const uint32_t sa = smem_u32(smem + stage * kStageBytes), sb = sa + Cfg::kABytes;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = A_MN ? sdesc(sa + kk * 2048, 8192, 1024) : sdesc(sa + kk * 32, 16, 1024);
-            const uint64_t bd = B_MN ? sdesc(sb + kk * 2048, 8192, 1024) : sdesc(sb + kk * 32, 16, 1024);
-            if (TWO) mma_bf16_pair(d, ad, bd, idesc, (kb > k0) || (kk > 0));
-            else mma_bf16(d, ad, bd, idesc, (kb > k0) || (kk > 0));
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = A_MN ? sdesc(sa + kk * 2048, 8192, 1024) : sdesc(sa + kk * 32, 16, 1024);
+              const uint64_t bd = B_MN ? sdesc(sb + kk * 2048, 8192, 1024) : sdesc(sb + kk * 32, 16, 1024);
+              if (TWO) mma_bf16_pair(d, ad, bd, idesc, (kb > k0) || (kk > 0));
+              else mma_bf16(d, ad, bd, idesc, (kb > k0) || (kk > 0));
+            }
+            if (TWO) mma_commit_pair_mc(empty0 + 8 * stage, 3);
+            else mma_commit(empty0 + 8 * stage);
           }
-          if (TWO) mma_commit_pair_mc(empty0 + 8 * stage, 3);
-          else mma_commit(empty0 + 8 * stage);
+          __syncwarp();
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        if (TWO) mma_commit_pair_mc(tfull0 + 8 * acc, 3);
-        else mma_commit(tfull0 + 8 * acc);
+        if (leader) {
+          if (TWO) mma_commit_pair_mc(tfull0 + 8 * acc, 3);
+          else mma_commit(tfull0 + 8 * acc);
+        }
+        __syncwarp();
         ++seg;
       }
     }
