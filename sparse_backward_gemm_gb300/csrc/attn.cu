@@ -883,8 +883,12 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
       if (!__shfl_sync(0xffffffffu, nxt, 0)) break;
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
+    {
+      // ---------------- MMA issuer: the converged warp waits, one elected lane issues ----------------
+      const bool leader = elect_one();
+      auto wait = [&](uint32_t bar, uint32_t parity, unsigned site) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.st, site)) != 0;
+      };
       constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);
       constexpr uint32_t id_kv = idesc_bf16(128, 128, false, true);
       constexpr uint32_t id_q = idesc_bf16(128, 64, true, true);
@@ -897,6 +901,7 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
       constexpr uint64_t kQStep = 2 * kQChunk / 16, kKCh = kKChunk / 16, kQCh = kQChunk / 16;
       auto sdp = [&](int it) {   // S^T, dP^T: M 128 keys, N 64 queries
         const int st = it & 1;
+        if (!leader) return;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {   // k = head dims: chunk kk / 4, 32 bytes a step inside it
           const uint64_t ko = (kk >> 2) * kKCh + 2 * (kk & 3), qo = st * kQStep + (kk >> 2) * kQCh + 2 * (kk & 3);
@@ -909,9 +914,9 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
         }
         mma_commit(b_sfull);
       };
-      bool ok = mbar_wait(b_kvready, 0, abort_flag, p.st, 51);
+      bool ok = wait(b_kvready, 0, 51);
       if (ok && n_iter > 0) {
-        ok = mbar_wait(b_qready, 0, abort_flag, p.st, 52);
+        ok = wait(b_qready, 0, 52);
         if (ok) {
           fence_after();
           sdp(0);
@@ -919,33 +924,37 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
       }
       for (int it = 0; ok && it < n_iter; ++it) {
         const int st = it & 1, buf = it & 1;
-        if (!mbar_wait(b_pfull, it & 1, abort_flag, p.st, 53)) break;
+        if (!wait(b_pfull, it & 1, 53)) break;
         fence_after();
         // P^T / dS^T of queries 16 kk .. 16 kk + 15: 8 packed columns, the
         // first 16 of each 32-query group's 32
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < kQ / 16; ++kk)     // k = queries, 16 rows (2 KB) a step
-          mma_bf16_ts(tbase + TM_DV, tbase + TM_S + 32 * (kk >> 1) + 8 * (kk & 1),
-                      d_domn + st * kQStep + 128 * kk, id_kv, (it > 0) || (kk > 0));
+          for (int kk = 0; kk < kQ / 16; ++kk)     // k = queries, 16 rows (2 KB) a step
+            mma_bf16_ts(tbase + TM_DV, tbase + TM_S + 32 * (kk >> 1) + 8 * (kk & 1),
+                        d_domn + st * kQStep + 128 * kk, id_kv, (it > 0) || (kk > 0));
 #pragma unroll
-        for (int kk = 0; kk < kQ / 16; ++kk)
-          mma_bf16_ts(tbase + TM_DK, tbase + TM_DP + 32 * (kk >> 1) + 8 * (kk & 1),
-                      d_qmn + st * kQStep + 128 * kk, id_kv, (it > 0) || (kk > 0));
-        mma_commit(b_qempty + 8 * st);          // Q, dO of this block are read for the last time
+          for (int kk = 0; kk < kQ / 16; ++kk)
+            mma_bf16_ts(tbase + TM_DK, tbase + TM_DP + 32 * (kk >> 1) + 8 * (kk & 1),
+                        d_qmn + st * kQStep + 128 * kk, id_kv, (it > 0) || (kk > 0));
+          mma_commit(b_qempty + 8 * st);          // Q, dO of this block are read for the last time
+        }
         // S, dP of the next block overwrite P, dS of this one, which the MMAs
         // above (issued first, run first) have read
         if (it + 1 < n_iter) {
-          if (!mbar_wait(b_qready + 8 * ((it + 1) & 1), ((it + 1) >> 1) & 1, abort_flag, p.st, 52)) break;
+          if (!wait(b_qready + 8 * ((it + 1) & 1), ((it + 1) >> 1) & 1, 52)) break;
           fence_after();
           sdp(it + 1);
         }
-        if (it > 0 && !mbar_wait(b_dqempty, (it - 1) & 1, abort_flag, p.st, 54)) break;
+        if (it > 0 && !wait(b_dqempty, (it - 1) & 1, 54)) break;
         fence_after();
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < kK / 16; ++kk)     // k = keys, 16 rows (2 KB) a step
-          mma_bf16(tbase + TM_DQ, d_kmn + 128 * kk, d_dsmn + buf * kKCh + 128 * kk, id_q, kk > 0);
-        mma_commit(b_dqfull);
-        mma_commit(b_dsempty + 8 * buf);        // dS^T buffer buf is read for the last time
+          for (int kk = 0; kk < kK / 16; ++kk)     // k = keys, 16 rows (2 KB) a step
+            mma_bf16(tbase + TM_DQ, d_kmn + 128 * kk, d_dsmn + buf * kKCh + 128 * kk, id_q, kk > 0);
+          mma_commit(b_dqfull);
+          mma_commit(b_dsempty + 8 * buf);        // dS^T buffer buf is read for the last time
+        }
       }
     }
   } else if (warp < 2 + kSoftWarps) {
@@ -1288,19 +1297,24 @@ __device__ __forceinline__ void dprep_body(const CUtensorMap& tmQ, const CUtenso
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    {
+      // the converged warp waits, one elected lane issues
+      const bool leader = elect_one();
+      auto wait = [&](uint32_t bar, uint32_t parity, unsigned site) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.st, site)) != 0;
+      };
       constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t id_o = idesc_bf16(128, kD, false, true);
-      bool ok = mbar_wait(b_q, 0, abort_flag, p.st, 41);
+      bool ok = wait(b_q, 0, 41);
       // O'_h += P V_j for the iteration whose P the softmax has finished; the
       // last head of a key block releases its K/V stage
       auto pv = [&](int t) -> bool {
         const int jj = t / HPC, hh = t % HPC;
         const int kst = jj % kKV, pb = t & 1;
-        if (!mbar_wait(b_pfull + 8 * pb, (t >> 1) & 1, abort_flag, p.st, 42)) return false;
+        if (!wait(b_pfull + 8 * pb, (t >> 1) & 1, 42)) return false;
         fence_after();
         const uint32_t sv = sbase + OFF_K + kst * kKVBytes + kCh * kTile;
-        if (MODE != 2) {   // the lse pass only releases the buffers
+        if (MODE != 2 && leader) {   // the lse pass only releases the buffers
 #pragma unroll
           for (int kk = 0; kk < kK / 16; ++kk) {   // V as the MN-major B: head-dim chunks kTile apart
             // P of keys 16 kk .. 16 kk + 15: 8 columns, in the half (kk / 4) of the S buffer
@@ -1308,27 +1322,33 @@ __device__ __forceinline__ void dprep_body(const CUtensorMap& tmQ, const CUtenso
             mma_bf16_ts(tbase + TM_O + hh * kD, pa, sdesc(sv + kk * 2048, kTile, 1024), id_o, (jj > 0) || (kk > 0));
           }
         }
-        if (hh == HPC - 1) mma_commit(b_kvempty + 8 * kst);
-        mma_commit(b_pempty + 8 * pb);
+        if (leader) {
+          if (hh == HPC - 1) mma_commit(b_kvempty + 8 * kst);
+          mma_commit(b_pempty + 8 * pb);
+        }
+        __syncwarp();
         return true;
       };
       for (int it = 0; ok && it < n_it; ++it) {
         const int j = it / HPC, hh = it % HPC;
         const int kst = j % kKV, kuse = j / kKV, sb = it & 1;
         if (hh == 0) {
-          if (!mbar_wait(b_kvready + 8 * kst, kuse & 1, abort_flag, p.st, 43)) { ok = false; break; }
+          if (!wait(b_kvready + 8 * kst, kuse & 1, 43)) { ok = false; break; }
           fence_after();
         }
         const uint32_t sk = sbase + OFF_K + kst * kKVBytes, sq = sbase + OFF_Q + hh * kCh * kTile;
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kTile + (kk & 3) * 32;
-          mma_bf16(tbase + TM_S + sb * 128, sdesc(sq + off, 16, 1024), sdesc(sk + off, 16, 1024), id_s, kk > 0);
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kTile + (kk & 3) * 32;
+            mma_bf16(tbase + TM_S + sb * 128, sdesc(sq + off, 16, 1024), sdesc(sk + off, 16, 1024), id_s, kk > 0);
+          }
+          mma_commit(b_sfull + 8 * sb);
         }
-        mma_commit(b_sfull + 8 * sb);
+        __syncwarp();
         if (it > 0 && !pv(it - 1)) { ok = false; break; }
       }
-      if (ok && n_it > 0 && pv(n_it - 1)) mma_commit(b_ofull);
+      if (ok && n_it > 0 && pv(n_it - 1) && leader) mma_commit(b_ofull);
     }
   } else {
     // softmax: one query row, 64 of the 128 keys of a block per thread
