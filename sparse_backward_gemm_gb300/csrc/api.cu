@@ -570,7 +570,7 @@ namespace {
 
 struct LayerBufs {
   __nv_bfloat16 *dout_k, *s_k, *b_k, *o_k, *a_k, *qkv_k;  // gathered (s_k holds gelu(f1) for phi)
-  __nv_bfloat16 *ds_k, *dgu_k, *dh_k, *do_k, *dqkv_k, *dx_k;
+  __nv_bfloat16 *ds_k, *dgu_k, *dh_k, *do_k, *dqkv_k;
   float *db_k, *da_k;
   float* norm_part;
   float* col_part;
@@ -617,7 +617,6 @@ void layer_carve(Carver& cv, const collider_layer_desc* d, LayerBufs* L) {
   L->dh_k = llama ? cv.take<__nv_bfloat16>(Mp * D) : nullptr;
   L->do_k = cv.take<__nv_bfloat16>(Mp * Hd);
   L->dqkv_k = cv.take<__nv_bfloat16>(Mp * Nqkv);
-  L->dx_k = cv.take<__nv_bfloat16>(Mp * D);
   L->db_k = llama ? cv.take<float>(Mp * D) : nullptr;
   L->da_k = cv.take<float>(Mp * D);
   L->norm_part = cv.take<float>(norm_part_floats((int)Mp, (int)D));
@@ -790,23 +789,27 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
     if (llama) L.s_k = bfp(sv->s);
   }
   // 1. gather the kept rows of dOut and of the saved GEMM operands.  The
-  // input-gradient chain reads only dOut and qkv (and the saved rows its row
-  // kernels index directly); s, b, o and a feed only the weight-gradient
-  // GEMMs, so they are gathered on the side stream, beside the chain.
+  // input-gradient chain starts from dOut alone: qkv is first needed by the
+  // attention, and s, b, o and a feed only the weight-gradient GEMMs, so
+  // these are gathered on the side stream, beside the chain (qkv first; the
+  // chain waits for it before the attention).
   if (!dense) {
-    GatherJob j[2];
-    j[0] = GatherJob{static_cast<const char*>(dOut), reinterpret_cast<char*>(L.dout_k), (long long)D * 2,
-                     (long long)D * 2, D * 2, 0};
-    j[1] = GatherJob{static_cast<const char*>(sv->qkv), reinterpret_cast<char*>(L.qkv_k), (long long)Nqkv * 2,
-                     (long long)Nqkv * 2, Nqkv * 2, 0};
-    if (dout_full) {
-      CK(launch_gather(c, j, 2, M, pad128(M), idx, n_kept));
-    } else {
-      CK(launch_gather(c, j, 1, M, pad128(M), nullptr, n_kept));   // COMPACT dOut: copy + zero padding
-      CK(launch_gather(c, j + 1, 1, M, pad128(M), idx, n_kept));
-    }
+    GatherJob j{static_cast<const char*>(dOut), reinterpret_cast<char*>(L.dout_k), (long long)D * 2,
+                (long long)D * 2, D * 2, 0};
+    // a COMPACT dOut is copied with its zero padding
+    CK(launch_gather(c, &j, 1, M, pad128(M), dout_full ? idx : nullptr, n_kept));
   }
   CK(fork_side(c, side, 0));   // the side stream starts once dOut's kept rows exist
+  if (!dense) {
+    GatherJob j{static_cast<const char*>(sv->qkv), reinterpret_cast<char*>(L.qkv_k), (long long)Nqkv * 2,
+                (long long)Nqkv * 2, Nqkv * 2, 0};
+    CK(launch_gather(cs, &j, 1, M, pad128(M), idx, n_kept));
+    if (side) CK(cudaEventRecord(side->ev[6], cs.stream));
+    // FULL dx: its filtered rows are zero; the norm backward at the end of
+    // the chain writes the kept rows in place
+    if (dx_full)
+      CK(launch_scatter(cs, nullptr, 0, static_cast<char*>(g->dx), (long long)D * 2, D * 2, M, idx, n_kept));
+  }
   {
     GatherJob j[4];
     int n = 0;
@@ -873,6 +876,7 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
   if (d->out_bias && g->db_o) CK(launch_colsum(c, dres, 1, D, M, D, nullptr, n_kept, L.col_part, g->db_o));
 
   // 4. filtered attention backward (+ RoPE backward) straight into dqkv_k
+  if (!dense && side) CK(cudaStreamWaitEvent(c.stream, side->ev[6], 0));   // qkv's kept rows
   {
     AttnArgs a{};
     a.B = d->B; a.T = d->T; a.H = H; a.Hkv = Hkv; a.dh = dh; a.causal = 1;
@@ -896,22 +900,20 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
     CK(launch_colsum(cs, L.dqkv_k, 1, Nqkv, M, Nqkv, nullptr, n_kept, L.col_part, g->db_qkv));
   CK(gemm_dx(c, M, D, Nqkv, L.dqkv_k, w->w_qkv, L.da_k, 0, llama ? 0 : 1, n_kept));  // da (+)= dqkv W_qkv^T
 
-  // 6. input norm backward + residual, then back to FULL rows if asked
-  if (dense) dx_full = false;   // every token kept: the COMPACT rows are the FULL rows
-  __nv_bfloat16* dxk = dx_full ? L.dx_k : static_cast<__nv_bfloat16*>(g->dx);
+  // 6. input norm backward + residual, its rows written where they belong
+  // (FULL dx: at idx, the filtered rows zeroed on the side stream above;
+  // COMPACT dx, or a dense call, whose COMPACT rows are the FULL rows: in order)
   {
     NormBwdArgs nb{};
     nb.layer_norm = llama ? 0 : 1; nb.M = M; nb.D = D;
     nb.dy1 = L.da_k; nb.res = dres; nb.res_ld = D;
     nb.x = static_cast<const __nv_bfloat16*>(sv->x); nb.mean = sv->mean1; nb.rstd = sv->rstd1;
     nb.gamma = static_cast<const __nv_bfloat16*>(w->norm1_w);
-    nb.out = dxk; nb.cap = dx_full ? pad128(M) : M; nb.dgamma = g->dnorm1_w; nb.dbeta = g->dnorm1_b; nb.part = L.norm_part;
+    nb.out = static_cast<__nv_bfloat16*>(g->dx); nb.cap = M; nb.out_full = (dx_full && !dense) ? 1 : 0;
+    nb.dgamma = g->dnorm1_w; nb.dbeta = g->dnorm1_b; nb.part = L.norm_part;
     nb.idx = idx; nb.n_kept = n_kept;
     CK(launch_norm_bwd(c, nb));
   }
-  if (dx_full)
-    CK(launch_scatter(c, reinterpret_cast<const char*>(L.dx_k), (long long)D * 2, static_cast<char*>(g->dx),
-                      (long long)D * 2, D * 2, M, idx, n_kept));
   CK(join_side(c, side, 4));   // the weight gradients are done when the chain is
   if (side) CK(join_hi(c_in.stream, side));
   return COLLIDER_OK;

@@ -48,6 +48,7 @@ constexpr int kMaxGatherJobs = 8;
 // cap: row capacity of every dst (rows n_kept .. min(next multiple of 128, cap) are zeroed).
 cudaError_t launch_gather(const Ctx& c, const GatherJob* jobs, int njobs, int M, long long cap, const int32_t* idx,
                           const int32_t* n_kept);
+// (compact null: only zero the filtered rows of full)
 cudaError_t launch_scatter(const Ctx& c, const char* compact, long long compact_ld, char* full,
                            long long full_ld, int row_bytes, int M, const int32_t* idx,
                            const int32_t* n_kept);
@@ -75,8 +76,9 @@ struct NormBwdArgs {
   const float* mean;    // FULL f32 [M] (LayerNorm)
   const float* rstd;    // FULL f32 [M]
   const __nv_bfloat16* gamma;
-  __nv_bfloat16* out;   // COMPACT bf16 [*, D]
-  long long cap;        // row capacity of out (zero padding stops there)
+  __nv_bfloat16* out;   // COMPACT bf16 [*, D], or FULL [M, D] rows idx[r] when out_full
+  long long cap;        // row capacity of out (zero padding stops there; COMPACT only)
+  int out_full;         // 1: write row r to out row idx[r], no padding (filtered rows are the caller's)
   float* dgamma;
   float* dbeta;         // LayerNorm only
   float* part;          // scratch: norm_part_floats(M, D)

@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(256) scatter_kernel(const char* __restrict__ c
     r = __shfl_sync(0xffffffffu, r, 0);
     bool kept = (r < nk) && (idx[r] == t);
     uint4* d = reinterpret_cast<uint4*>(full + (long long)t * fld);
+    if (kept && !compact) continue;   // zero the filtered rows only
     if (kept) {
       const uint4* s = reinterpret_cast<const uint4*>(compact + (long long)r * cld);
       for (int v = lane; v < vecs; v += 32) d[v] = s[v];
@@ -190,11 +191,11 @@ __device__ __forceinline__ void norm_dy8(const NormBwdArgs& a, long long off, fl
 __global__ void __launch_bounds__(kNormWarps * 32) norm_rows_kernel(NormBwdArgs a, DevStatus* st) {
   const int D = a.D;
   const int nk = *a.n_kept;
-  const int pad = padded_rows(nk, a.cap);
+  const int pad = a.out_full ? nk : padded_rows(nk, a.cap);
   const int lane = threadIdx.x & 31;
   for (int r = blockIdx.x * kNormWarps + (threadIdx.x >> 5); r < pad; r += gridDim.x * kNormWarps) {
-    __nv_bfloat16* orow = a.out + (long long)r * D;
     if (r >= nk) {
+      __nv_bfloat16* orow = a.out + (long long)r * D;
       for (int c = lane * 8; c < D; c += 256) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
       continue;
     }
@@ -203,6 +204,7 @@ __global__ void __launch_bounds__(kNormWarps * 32) norm_rows_kernel(NormBwdArgs 
       if (lane == 0) report_error(st, kErrBadIndex, 200);
       continue;
     }
+    __nv_bfloat16* orow = a.out + (long long)(a.out_full ? t : r) * D;
     const float rstd = a.rstd[t];
     const float mu = a.layer_norm ? a.mean[t] : 0.f;
     const __nv_bfloat16* xr = a.x + (long long)t * D;
