@@ -573,6 +573,7 @@ struct LayerBufs {
   __nv_bfloat16 *ds_k, *dgu_k, *dh_k, *do_k, *dqkv_k;
   float *db_k, *da_k;
   float* norm_part;
+  float* norm_part2;     // the middle norm's partials (reduced on the side stream)
   float* col_part;
   float* sk_partial;     // stream-K scratch of the input-gradient chain's GEMMs
   int* sk_counters;
@@ -620,6 +621,7 @@ void layer_carve(Carver& cv, const collider_layer_desc* d, LayerBufs* L) {
   L->db_k = llama ? cv.take<float>(Mp * D) : nullptr;
   L->da_k = cv.take<float>(Mp * D);
   L->norm_part = cv.take<float>(norm_part_floats((int)Mp, (int)D));
+  L->norm_part2 = llama ? cv.take<float>(norm_part_floats((int)Mp, (int)D)) : nullptr;
   size_t cp = colsum_part_floats((int)Mp, (int)std::max(Nqkv, std::max(Nup, D)));
   L->col_part = cv.take<float>(cp);
   attn_carve(cv, d->B, d->T, d->H, d->Hkv, d->dh, &L->at);
@@ -850,8 +852,10 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
     nb.dy1 = L.db_k; nb.res = L.dout_k; nb.res_ld = D;
     nb.x = static_cast<const __nv_bfloat16*>(sv->h); nb.rstd = sv->rstd2;
     nb.gamma = static_cast<const __nv_bfloat16*>(w->norm2_w);
-    nb.out = L.dh_k; nb.cap = pad128(M); nb.dgamma = g->dnorm2_w; nb.part = L.norm_part; nb.idx = idx; nb.n_kept = n_kept;
-    CK(launch_norm_bwd(c, nb));                                                          // dh = dOut + norm2'
+    nb.out = L.dh_k; nb.cap = pad128(M); nb.dgamma = g->dnorm2_w; nb.part = L.norm_part2; nb.idx = idx; nb.n_kept = n_kept;
+    CK(launch_norm_rows(c, nb));                                                         // dh = dOut + norm2'
+    CK(fork_side(c, side, 7));
+    CK(launch_norm_cols(cs, nb));                                                        // dnorm2_w, beside the chain
     dres = L.dh_k;
   } else {
     CK(gemm_dw(cs, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept, in_rows));     // dW2 = gelu(f1)^T dOut

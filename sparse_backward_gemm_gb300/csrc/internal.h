@@ -87,6 +87,10 @@ struct NormBwdArgs {
 };
 size_t norm_part_floats(int M, int D);
 cudaError_t launch_norm_bwd(const Ctx& c, const NormBwdArgs& a);
+// the two halves of launch_norm_bwd: the input gradient (rows), and dgamma /
+// dbeta (column partials + fixed-order reduction), which only reads dy and x
+cudaError_t launch_norm_rows(const Ctx& c, const NormBwdArgs& a);
+cudaError_t launch_norm_cols(const Ctx& c, const NormBwdArgs& a);
 
 // SwiGLU backward: dgu[r] = [ds*u*sig(g)*(1+g*(1-sig(g))) | ds*silu(g)]
 // ds COMPACT (bf16 or f32) [*, F]; gu FULL bf16 [M, 2F] via idx; dgu COMPACT bf16 [*, 2F].

@@ -497,10 +497,17 @@ size_t norm_part_floats(int M, int D) {
   return (size_t)((M + kNormColRows - 1) / kNormColRows) * 2 * (size_t)D;
 }
 
-cudaError_t launch_norm_bwd(const Ctx& c, const NormBwdArgs& a) {
-  const int nsets = a.layer_norm ? 2 : 1;
+cudaError_t launch_norm_rows(const Ctx& c, const NormBwdArgs& a) {
   prof_begin(c, "norm_bwd");
   norm_rows_kernel<<<grid_rows(c, a.cap, kNormWarps), kNormWarps * 32, 0, c.stream>>>(a, c.st);
+  count_launch(1);
+  prof_end(c);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_norm_cols(const Ctx& c, const NormBwdArgs& a) {
+  const int nsets = a.layer_norm ? 2 : 1;
+  prof_begin(c, "norm_bwd");
   norm_cols_kernel<<<dim3((a.D / 8 + 255) / 256, (unsigned)((a.cap + kNormColRows - 1) / kNormColRows)), 256, 0,
                      c.stream>>>(a);
   // partials are laid out [part][set][D] with set 0 = dgamma, set 1 = dbeta
@@ -510,9 +517,14 @@ cudaError_t launch_norm_bwd(const Ctx& c, const NormBwdArgs& a) {
   if (a.layer_norm)
     colsum_reduce_kernel<<<g, 256, 0, c.stream>>>(a.part + a.D, a.D, (long long)nsets * a.D, kNormColRows,
                                                   a.n_kept, a.dbeta);
-  count_launch(2 + nsets);
+  count_launch(1 + nsets);
   prof_end(c);
   return cudaGetLastError();
+}
+
+cudaError_t launch_norm_bwd(const Ctx& c, const NormBwdArgs& a) {
+  cudaError_t e = launch_norm_rows(c, a);
+  return e == cudaSuccess ? launch_norm_cols(c, a) : e;
 }
 
 cudaError_t launch_swiglu_bwd(const Ctx& c, const void* ds, int ds_is_bf16, int F, const __nv_bfloat16* gu,
