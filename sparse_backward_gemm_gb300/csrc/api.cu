@@ -645,7 +645,7 @@ void layer_carve(Carver& cv, const collider_layer_desc* d, LayerBufs* L) {
 struct Side {
   cudaStream_t s = nullptr;    // weight gradients, default priority
   cudaStream_t hi = nullptr;   // input-gradient chain, highest priority
-  cudaEvent_t ev[10] = {};
+  cudaEvent_t ev[12] = {};
 };
 thread_local Side g_side[64];
 
@@ -790,6 +790,20 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
     L.qkv_k = bfp(sv->qkv);
     if (llama) L.s_k = bfp(sv->s);
   }
+  // the attention's arguments (its preparation runs ahead on the side stream)
+  AttnArgs attn{};
+  attn.B = d->B; attn.T = d->T; attn.H = H; attn.Hkv = Hkv; attn.dh = dh; attn.causal = 1;
+  attn.scale = 1.0f / sqrtf((float)dh);
+  attn.rotary_dim = d->rotary_dim; attn.rope_base = d->rope_base;
+  attn.q = L.qkv_k; attn.k = L.qkv_k + Hd; attn.v = L.qkv_k + Hd + Hkv * dh; attn.dO = L.do_k;
+  attn.q_ld = Nqkv; attn.kv_ld = Nqkv; attn.do_ld = Hd;
+  attn.lse = sv->lse; attn.idx = idx; attn.cu_kept = cu_kept; attn.n_kept = n_kept;
+  attn.dq = L.dqkv_k; attn.dk = L.dqkv_k + Hd; attn.dv = L.dqkv_k + Hd + Hkv * dh;
+  attn.dq_ld = Nqkv; attn.dkv_ld = Nqkv;
+  attn.dq_acc = L.at.dq_acc; attn.Dvec = L.at.Dvec; attn.lse_k = L.at.lse2; attn.rope = L.at.rope; attn.M = M;
+  attn.dk_acc = L.at.dk_acc; attn.dv_acc = L.at.dv_acc; attn.order = L.at.order; attn.in_cap = in_rows;
+  attn.cap = pad128(M);
+
   // 1. gather the kept rows of dOut and of the saved GEMM operands.  The
   // input-gradient chain starts from dOut alone: qkv is first needed by the
   // attention, and s, b, o and a feed only the weight-gradient GEMMs, so
@@ -806,7 +820,14 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
     GatherJob j{static_cast<const char*>(sv->qkv), reinterpret_cast<char*>(L.qkv_k), (long long)Nqkv * 2,
                 (long long)Nqkv * 2, Nqkv * 2, 0};
     CK(launch_gather(cs, &j, 1, M, pad128(M), idx, n_kept));
-    if (side) CK(cudaEventRecord(side->ev[6], cs.stream));
+  }
+  if (side) {
+    AttnArgs prep = attn;
+    prep.stage = 1;
+    CK(launch_attn_bwd(cs, prep));
+    CK(cudaEventRecord(side->ev[6], cs.stream));
+  }
+  if (!dense) {
     // FULL dx: its filtered rows are zero; the norm backward at the end of
     // the chain writes the kept rows in place
     if (dx_full)
@@ -880,22 +901,11 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
   if (d->out_bias && g->db_o) CK(launch_colsum(c, dres, 1, D, M, D, nullptr, n_kept, L.col_part, g->db_o));
 
   // 4. filtered attention backward (+ RoPE backward) straight into dqkv_k
-  if (!dense && side) CK(cudaStreamWaitEvent(c.stream, side->ev[6], 0));   // qkv's kept rows
-  {
-    AttnArgs a{};
-    a.B = d->B; a.T = d->T; a.H = H; a.Hkv = Hkv; a.dh = dh; a.causal = 1;
-    a.scale = 1.0f / sqrtf((float)dh);
-    a.rotary_dim = d->rotary_dim; a.rope_base = d->rope_base;
-    a.q = L.qkv_k; a.k = L.qkv_k + Hd; a.v = L.qkv_k + Hd + Hkv * dh; a.dO = L.do_k;
-    a.q_ld = Nqkv; a.kv_ld = Nqkv; a.do_ld = Hd;
-    a.lse = sv->lse; a.idx = idx; a.cu_kept = cu_kept; a.n_kept = n_kept;
-    a.dq = L.dqkv_k; a.dk = L.dqkv_k + Hd; a.dv = L.dqkv_k + Hd + Hkv * dh;
-    a.dq_ld = Nqkv; a.dkv_ld = Nqkv;
-    a.dq_acc = L.at.dq_acc; a.Dvec = L.at.Dvec; a.lse_k = L.at.lse2; a.rope = L.at.rope; a.M = M;
-    a.dk_acc = L.at.dk_acc; a.dv_acc = L.at.dv_acc; a.order = L.at.order; a.in_cap = in_rows;
-    a.cap = pad128(M);
-    CK(launch_attn_bwd(c, a));
+  if (side) {
+    CK(cudaStreamWaitEvent(c.stream, side->ev[6], 0));   // qkv's kept rows, the attention's preparation
+    attn.stage = 2;
   }
+  CK(launch_attn_bwd(c, attn));
 
   // 5. QKV projection
   CK(fork_side(c, side, 3));
@@ -916,7 +926,9 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
     nb.out = static_cast<__nv_bfloat16*>(g->dx); nb.cap = M; nb.out_full = (dx_full && !dense) ? 1 : 0;
     nb.dgamma = g->dnorm1_w; nb.dbeta = g->dnorm1_b; nb.part = L.norm_part;
     nb.idx = idx; nb.n_kept = n_kept;
-    CK(launch_norm_bwd(c, nb));
+    CK(launch_norm_rows(c, nb));
+    CK(fork_side(c, side, 10));
+    CK(launch_norm_cols(cs, nb));   // dnorm1_w (dnorm1_b), beside the chain
   }
   CK(join_side(c, side, 4));   // the weight gradients are done when the chain is
   if (side) CK(join_hi(c_in.stream, side));

@@ -1610,9 +1610,13 @@ cudaError_t run(const Ctx& c, const AttnK& k, float rope_base, const AttnArgs& a
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) seen[dev] = 1;
   }
-  prof_begin(c, "attn_prep");
-  attn_prep_kernel<<<c.num_sms * 4, 256, 0, c.stream>>>(k, DH, rope_base, const_cast<float2*>(k.rope));
-  prof_end(c);
+  if (a.stage != 2) {
+    prof_begin(c, "attn_prep");
+    attn_prep_kernel<<<c.num_sms * 4, 256, 0, c.stream>>>(k, DH, rope_base, const_cast<float2*>(k.rope));
+    prof_end(c);
+    count_launch(1);
+    if (a.stage == 1) return cudaGetLastError();
+  }
   {
     // work items: (key block, sequence, kv head, chunk of hc query heads).
     // The group's heads are split in at most two chunks: a key block's dK
@@ -1664,7 +1668,7 @@ cudaError_t run(const Ctx& c, const AttnK& k, float rope_base, const AttnArgs& a
   prof_begin(c, "attn_finalize");
   attn_finalize_kernel<<<c.num_sms * 4, 256, 0, c.stream>>>(k, DH);
   prof_end(c);
-  count_launch(4);
+  count_launch(3);
   return cudaGetLastError();
 }
 

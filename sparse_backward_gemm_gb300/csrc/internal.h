@@ -195,6 +195,10 @@ struct AttnArgs {
   int* order;      // scratch [attn_order_ints(B, T, H)]: work tickets and dQ accumulation turns
   int M;
   long long cap;   // row capacity of dq, dk, dv (zero padding stops there)
+  int stage;       // 0: the whole backward; 1: only the preparation (lse in kept
+                   // order, zeroed accumulators and ordering scratch, RoPE table:
+                   // it reads only lse, idx and cu_kept, so it may run ahead on
+                   // another stream); 2: everything after it
 };
 // ints of the attention backward's ordering scratch: one work-item ticket and
 // a dQ accumulation turn per (sequence, query head, 64-row query block)
