@@ -707,17 +707,15 @@ cudaError_t launch_tc_gemm(const Ctx& c, const TcGemm& g) {
     const char* e = getenv("COLLIDER_GEMM_PAIR");
     return e ? atoi(e) : -1;
   }();
-  // A long static reduction (>= 128 k-slices: the dX of the MLP up-projection)
-  // runs as lone CTAs cut evenly by stream-K: measured against 2-SM pairs with
-  // a stream-K tail, the time was the same and the pairs' tail, walking the
-  // k-ranges of many tiles at once, read 2.1x the DRAM bytes (417 against 195 MB).
-  const bool long_k = g.dyn != 2 && g.K / BK >= 128 && g.partial && g.counters;
-  const bool pair = pair_env != 0 && bn == 256 && !long_k;
+  // (A long static reduction -- the dX of the MLP up-projection, 176
+  // k-slices -- also runs as pairs with a stream-K tail: as lone CTAs cut
+  // evenly by stream-K it read half the DRAM bytes but took 168 against 163 us.)
+  const bool pair = pair_env != 0 && bn == 256;
   const int mode = pair ? 2 : 0;
   // counters the stream-K fix-up needs: one per tile, and per CTA of a pair
   const long long m_tiles = (g.M + BM - 1) / BM, n_tiles = (g.N + bn - 1) / bn;
   const long long max_ctrs = (pair ? 2 * ((m_tiles + 1) / 2) : m_tiles) * n_tiles;
-  const int split = split_env >= 0 ? split_env : (long_k ? 1 : 3);
+  const int split = split_env >= 0 ? split_env : 3;
   const bool sk = split != 0 && g.partial && g.counters && max_ctrs <= g.counter_cap;
   CUtensorMap ma, mb;
   // A: K-major [M rows, K] or MN-major [K rows, M]; B: K-major [N rows, K]
