@@ -1149,12 +1149,13 @@ struct DprepCfg {
   static constexpr uint32_t kTile = 16384;                           // 128 rows x 64 columns
   static constexpr int kKV = DH == 64 && HPC == 1 ? 3 : 2;           // K/V stages
   static constexpr uint32_t kKVBytes = 2 * kCh * kTile;              // K and V of one stage
+  static constexpr int kSoftWarps = 16;                              // four per TMEM lane quadrant
+  // OFF_P: the lse pass's per-key-group maxima and sums, [2][HPC][4][128] f32
   static constexpr uint32_t OFF_Q = 0, OFF_K = HPC * kCh * kTile, OFF_P = OFF_K + kKV * kKVBytes,
-                            OFF_BAR = OFF_P + 4 * kTile;
-  static constexpr uint32_t OFF_PART = OFF_BAR + 256;                // [HPC][2][128] f32 partial dot products
-  static constexpr size_t kSmem = 1024 + OFF_PART + HPC * 1024;   // MODE 2 merges in the (unused) P tiles
+                            OFF_BAR = OFF_P + HPC * (kSoftWarps / 4) * 1024;
+  static constexpr uint32_t OFF_PART = OFF_BAR + 256;                // [HPC][4][128] f32 partial dot products
+  static constexpr size_t kSmem = 1024 + OFF_PART + HPC * (kSoftWarps / 4) * 512;
   static constexpr uint32_t TM_S = 0, TM_O = 256;
-  static constexpr int kSoftWarps = 8;                               // two per TMEM lane quadrant
   static constexpr int kThreads = 32 * (2 + kSoftWarps);
   static_assert(kSmem <= 232448, "shared memory");
   static_assert(TM_O + HPC * DH <= 512, "TMEM columns");
@@ -1317,8 +1318,8 @@ __device__ __forceinline__ void dprep_body(const CUtensorMap& tmQ, const CUtenso
         if (MODE != 2 && leader) {   // the lse pass only releases the buffers
 #pragma unroll
           for (int kk = 0; kk < kK / 16; ++kk) {   // V as the MN-major B: head-dim chunks kTile apart
-            // P of keys 16 kk .. 16 kk + 15: 8 columns, in the half (kk / 4) of the S buffer
-            const uint32_t pa = tbase + TM_S + pb * 128 + 64 * (kk >> 2) + 8 * (kk & 3);
+            // P of keys 16 kk .. 16 kk + 15: 8 columns, in the 32-key chunk kk / 2 of the S buffer
+            const uint32_t pa = tbase + TM_S + pb * 128 + 32 * (kk >> 1) + 8 * (kk & 1);
             mma_bf16_ts(tbase + TM_O + hh * kD, pa, sdesc(sv + kk * 2048, kTile, 1024), id_o, (jj > 0) || (kk > 0));
           }
         }
@@ -1351,9 +1352,11 @@ __device__ __forceinline__ void dprep_body(const CUtensorMap& tmQ, const CUtenso
       if (ok && n_it > 0 && pv(n_it - 1) && leader) mma_commit(b_ofull);
     }
   } else {
-    // softmax: one query row, 64 of the 128 keys of a block per thread
+    // softmax: one query row, kKT of the 128 keys of a block per thread
+    // (four warps per TMEM lane quadrant, sub-group `sub` of the row's keys)
+    constexpr int kSubs = kSoftWarps / 4, kKT = kK / kSubs, kDT = kD / kSubs;
     const int q = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int sub = (warp - 2) >> 2;
     const int r = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     float Lh[HPC];
@@ -1367,9 +1370,10 @@ __device__ __forceinline__ void dprep_body(const CUtensorMap& tmQ, const CUtenso
       mrun[hh] = -INFINITY;
       lrun[hh] = 0.f;
     }
-    // with one head, this thread's half of its dO row is loaded now so the
-    // latency hides behind the key loop; with several heads at the end
-    constexpr int kDoVec = HPC == 1 ? kD / 16 : 1;
+    // with one head, this thread's kDT head-dim columns of its dO row are
+    // loaded now so the latency hides behind the key loop; with several
+    // heads at the end
+    constexpr int kDoVec = HPC == 1 ? kDT / 8 : 1;
     uint4 dov[kDoVec];
     if (HPC == 1 && MODE == 0) {
 #pragma unroll
@@ -1377,7 +1381,7 @@ __device__ __forceinline__ void dprep_body(const CUtensorMap& tmQ, const CUtenso
         dov[u] = make_uint4(0, 0, 0, 0);
         if (r < qrows)
           dov[u] = *reinterpret_cast<const uint4*>(p.dO + (long long)(s0 + i0 + r) * p.do_ld + h0 * kD +
-                                                   half * (kD / 2) + 8 * u);
+                                                   sub * kDT + 8 * u);
       }
     }
     bool ok = true;
@@ -1392,18 +1396,19 @@ __device__ __forceinline__ void dprep_body(const CUtensorMap& tmQ, const CUtenso
 #pragma unroll
       for (int x = 1; x < HPC; ++x)
         if (hh == x) L = Lh[x];
-      uint32_t sr[64];
-      tmem_ld32_async(tbase + lane_off + TM_S + st * 128 + half * 64, sr);
-      tmem_ld32_async(tbase + lane_off + TM_S + st * 128 + half * 64 + 32, sr + 32);
+      uint32_t sr[kKT];
+#pragma unroll
+      for (int c = 0; c < kKT / 32; ++c)
+        tmem_ld32_async(tbase + lane_off + TM_S + st * 128 + sub * kKT + 32 * c, sr + 32 * c);
       tmem_wait_ld();
       // a full key block strictly before the query block needs no masking
       const bool interior = (!p.causal || j0 + kK <= i0) && qrows == kQ && len - j0 >= kK;
       if (MODE == 2) {
-        // keys j0 + half * 64 + e of this row, e < 64.  The block maximum is
+        // keys j0 + sub * kKT + e of this row, e < kKT.  The block maximum is
         // taken on the raw scores (scaling by c > 0 is monotone, so max(S) c
         // = max(S c) exactly) and each exponent is one fma; eight independent
         // partial maxima and sums keep the dependency chains short.
-        float sv[64], bm8[8], a8[8];
+        float sv[kKT], bm8[8], a8[8];
 #pragma unroll
         for (int q8 = 0; q8 < 8; ++q8) {
           bm8[q8] = -INFINITY;
@@ -1411,14 +1416,14 @@ __device__ __forceinline__ void dprep_body(const CUtensorMap& tmQ, const CUtenso
         }
         if (interior) {
 #pragma unroll
-          for (int e = 0; e < 64; ++e) {
+          for (int e = 0; e < kKT; ++e) {
             sv[e] = __uint_as_float(sr[e]);
             bm8[e & 7] = fmaxf(bm8[e & 7], sv[e]);
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < 64; ++e) {
-            const int kj = j0 + half * 64 + e;
+          for (int e = 0; e < kKT; ++e) {
+            const int kj = j0 + sub * kKT + e;
             const bool valid = r < qrows && kj < len && (!p.causal || kj <= i0 + r);
             sv[e] = valid ? __uint_as_float(sr[e]) : -INFINITY;
             bm8[e & 7] = fmaxf(bm8[e & 7], sv[e]);
@@ -1433,7 +1438,7 @@ __device__ __forceinline__ void dprep_body(const CUtensorMap& tmQ, const CUtenso
         const float mn = fmaxf(m, bm);
         if (mn != -INFINITY) {
 #pragma unroll
-          for (int e = 0; e < 64; ++e) a8[e & 7] += exp2_approx(fmaf(sv[e], p.scale_log2, -mn));
+          for (int e = 0; e < kKT; ++e) a8[e & 7] += exp2_approx(fmaf(sv[e], p.scale_log2, -mn));
           const float acc = ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
           l = l * exp2_approx(m - mn) + acc;
           m = mn;
@@ -1443,8 +1448,8 @@ __device__ __forceinline__ void dprep_body(const CUtensorMap& tmQ, const CUtenso
           if (hh == x) { mrun[x] = m; lrun[x] = l; }
       }
 #pragma unroll
-      for (int cc = 0; cc < (MODE == 2 ? 0 : 2); ++cc) {
-        const int c = 2 * half + cc;
+      for (int cc = 0; cc < (MODE == 2 ? 0 : kKT / 32); ++cc) {
+        const int c32 = sub * (kKT / 32) + cc;   // 32-key chunk of the block
         float sv[32];
         if (interior) {
 #pragma unroll
@@ -1452,59 +1457,71 @@ __device__ __forceinline__ void dprep_body(const CUtensorMap& tmQ, const CUtenso
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const int kj = j0 + c * 32 + e;
+            const int kj = j0 + c32 * 32 + e;
             const bool valid = r < qrows && kj < len && (!p.causal || kj <= i0 + r);
             sv[e] = valid ? exp2_approx(__uint_as_float(sr[cc * 32 + e]) * p.scale_log2 - L) : 0.f;
           }
         }
-        // these 32 keys' P, packed in pairs: 16 columns of this half's first 32
-        // (every S column of the half is in registers already)
+        // these 32 keys' P, packed in pairs: the first 16 of the chunk's 32
+        // columns (this thread has read all of them already)
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(sv[2 * e], sv[2 * e + 1]);
-        tmem_st16(tbase + lane_off + TM_S + st * 128 + half * 64 + 16 * cc, pk);
+        tmem_st16(tbase + lane_off + TM_S + st * 128 + 32 * c32, pk);
       }
       tmem_wait_st();
       fence_before();
       mbar_arrive(b_pfull + 8 * st);
     }
-    float* part = reinterpret_cast<float*>(sm + OFF_PART);   // [HPC][2][128]
+    float* part = reinterpret_cast<float*>(sm + OFF_PART);   // [HPC][kSubs][128]
+    // this thread's kDT head-dim columns of head hh's O' (or O), 16 at a time
+    auto load_o16 = [&](int hh, int c16, float* o) {
+      uint32_t u[16];
+      tmem_ld16_async(tbase + lane_off + TM_O + hh * kD + sub * kDT + 16 * c16, u);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) o[e] = __uint_as_float(u[e]);
+    };
     if (MODE == 1) {
-      // the attention output: this thread's half of the row's head-dim columns
+      // the attention output: this thread's columns of the row
       if (ok && mbar_wait(b_ofull, 0, &no_abort, p.st, 48)) {
         fence_after();
 #pragma unroll
         for (int hh = 0; hh < HPC; ++hh) {
 #pragma unroll
-          for (int cc = 0; cc < kD / 64; ++cc) {
-            float o[32];
-            const int col = half * (kD / 2) + 32 * cc;
-            tmem_ld32(tbase + lane_off + TM_O + hh * kD + col, o);
+          for (int c16 = 0; c16 < kDT / 16; ++c16) {
+            float o[16];
+            load_o16(hh, c16, o);
             if (r < qrows) {
-              __nv_bfloat16* dst = p.O + (long long)(s0 + i0 + r) * p.o_ld + (h0 + hh) * kD + col;
+              __nv_bfloat16* dst = p.O + (long long)(s0 + i0 + r) * p.o_ld + (h0 + hh) * kD + sub * kDT + 16 * c16;
 #pragma unroll
-              for (int g = 0; g < 4; ++g) *reinterpret_cast<uint4*>(dst + 8 * g) = pack8(o + 8 * g);
+              for (int g = 0; g < 2; ++g) *reinterpret_cast<uint4*>(dst + 8 * g) = pack8(o + 8 * g);
             }
           }
         }
       }
     } else if (MODE == 2) {
-      // merge the two halves of each row: lse2 = max + log2(sum exp2(x - max))
+      // merge the row's key groups: lse2 = max + log2(sum exp2(x - max)),
+      // the groups taken in a fixed order
       if (!(ok && mbar_wait(b_ofull, 0, &no_abort, p.st, 49))) ok = false;
       float* pm = reinterpret_cast<float*>(sm + OFF_P);   // no P tile is written in this pass
-      float* pl = pm + HPC * 256;
+      float* pl = pm + HPC * kSubs * 128;
 #pragma unroll
       for (int hh = 0; hh < HPC; ++hh) {
-        pm[(hh * 2 + half) * 128 + r] = mrun[hh];
-        pl[(hh * 2 + half) * 128 + r] = lrun[hh];
+        pm[(hh * kSubs + sub) * 128 + r] = mrun[hh];
+        pl[(hh * kSubs + sub) * 128 + r] = lrun[hh];
       }
       named_bar(1, 32 * kSoftWarps);
-      if (ok && half == 0 && r < qrows) {
+      if (ok && sub == 0 && r < qrows) {
 #pragma unroll
         for (int hh = 0; hh < HPC; ++hh) {
-          const float m1 = pm[(hh * 2 + 1) * 128 + r], l1 = pl[(hh * 2 + 1) * 128 + r];
-          const float mm = fmaxf(mrun[hh], m1);
-          const float lsum = lrun[hh] * exp2f(mrun[hh] - mm) + l1 * exp2f(m1 - mm);
+          float mm = -INFINITY;
+#pragma unroll
+          for (int x = 0; x < kSubs; ++x) mm = fmaxf(mm, pm[(hh * kSubs + x) * 128 + r]);
+          float lsum = 0.f;
+#pragma unroll
+          for (int x = 0; x < kSubs; ++x)
+            lsum += pl[(hh * kSubs + x) * 128 + r] * exp2f(pm[(hh * kSubs + x) * 128 + r] - mm);
           const float lse2 = mm + log2f(lsum);
           p.lse2_out[(long long)(h0 + hh) * p.M + s0 + i0 + r] = lse2;
           p.lse_out[((long long)b * p.H + h0 + hh) * p.T + i0 + r] = lse2 * kLn2;
@@ -1520,22 +1537,20 @@ __device__ __forceinline__ void dprep_body(const CUtensorMap& tmQ, const CUtenso
       fence_after();
 #pragma unroll
       for (int hh = 0; hh < HPC; ++hh) {
-        // this thread's half of the row: head-dim columns half * kD / 2 ..
 #pragma unroll
-        for (int cc = 0; cc < kD / 64; ++cc) {
-          float o[32];
-          const int col = half * (kD / 2) + 32 * cc;
-          tmem_ld32(tbase + lane_off + TM_O + hh * kD + col, o);
+        for (int c16 = 0; c16 < kDT / 16; ++c16) {
+          float o[16];
+          load_o16(hh, c16, o);
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
+          for (int g = 0; g < 2; ++g) {
             float x[8];
             if (HPC == 1) {
-              unpack8(dov[(4 * cc + g) % kDoVec], x);
+              unpack8(dov[(2 * c16 + g) % kDoVec], x);
             } else {
               uint4 u = make_uint4(0, 0, 0, 0);
               if (r < qrows)
                 u = *reinterpret_cast<const uint4*>(p.dO + (long long)(s0 + i0 + r) * p.do_ld + (h0 + hh) * kD +
-                                                    col + 8 * g);
+                                                    sub * kDT + 16 * c16 + 8 * g);
               unpack8(u, x);
             }
 #pragma unroll
@@ -1548,12 +1563,16 @@ __device__ __forceinline__ void dprep_body(const CUtensorMap& tmQ, const CUtenso
     }
     if (MODE == 0) {
 #pragma unroll
-      for (int hh = 0; hh < HPC; ++hh) part[(hh * 2 + half) * 128 + r] = d[hh];
+      for (int hh = 0; hh < HPC; ++hh) part[(hh * kSubs + sub) * 128 + r] = d[hh];
       named_bar(1, 32 * kSoftWarps);
-      if (ok && half == 0 && r < qrows)
+      if (ok && sub == 0 && r < qrows)
 #pragma unroll
-        for (int hh = 0; hh < HPC; ++hh)
-          p.Dvec[(long long)(h0 + hh) * p.M + s0 + i0 + r] = d[hh] + part[(hh * 2 + 1) * 128 + r];
+        for (int hh = 0; hh < HPC; ++hh) {
+          float dd = d[hh];
+#pragma unroll
+          for (int x = 1; x < kSubs; ++x) dd += part[(hh * kSubs + x) * 128 + r];
+          p.Dvec[(long long)(h0 + hh) * p.M + s0 + i0 + r] = dd;
+        }
     }
   }
   fence_before();
