@@ -344,19 +344,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
   } else if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer ----------------
+    {
+      // ---------------- TMA producer: the converged warp waits, one elected lane issues ----------------
+      const bool leader = elect_one();
+      auto wait = [&](uint32_t bar, uint32_t parity, unsigned site) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.st, site)) != 0;
+      };
+      auto aborted = [&]() { return __any_sync(0xffffffffu, *abort_flag != 0); };
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;   // stages with copies issued, and the phase parity armed
       SegIter si(sp);
       int t, k0, k1;
-      while (!*abort_flag && si.next(t, k0, k1)) {
+      while (si.next(t, k0, k1) && !aborted()) {
         int m0, n0;
         origin(t, m0, n0);
         bool ok = true;
         for (int kb = k0; kb < k1; ++kb) {
-          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.st, 1)) { ok = false; break; }
+          if (!wait(empty0 + 8 * stage, phase ^ 1u, 1)) { ok = false; break; }
           const uint32_t fb = full0 + 8 * stage;
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -364,49 +369,56 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int kx = kb * BK;
           if (TWO) {
             // both CTAs' copies are counted on the even CTA's full barrier
-            if (rank == 0) mbar_expect_tx(fb, 2 * kStageBytes);
-            const uint32_t lb = map_to_rank(fb, 0);
-            if (!A_MN) {
-              tma_load_2d_pair(sa, &tmA, lb, kx, m0);
-            } else {
-              tma_load_2d_pair(sa, &tmA, lb, m0, kx);
-              tma_load_2d_pair(sa + 8192, &tmA, lb, m0 + 64, kx);
-            }
-            if (!B_MN) {
-              tma_load_2d_pair(sb, &tmB, lb, kx, n0 + rank * (BN / 2));
-            } else {
+            if (leader) {
+              if (rank == 0) mbar_expect_tx(fb, 2 * kStageBytes);
+              const uint32_t lb = map_to_rank(fb, 0);
+              if (!A_MN) {
+                tma_load_2d_pair(sa, &tmA, lb, kx, m0);
+              } else {
+                tma_load_2d_pair(sa, &tmA, lb, m0, kx);
+                tma_load_2d_pair(sa + 8192, &tmA, lb, m0 + 64, kx);
+              }
+              if (!B_MN) {
+                tma_load_2d_pair(sb, &tmB, lb, kx, n0 + rank * (BN / 2));
+              } else {
 #pragma unroll
-              for (int j = 0; j < BN / 128; ++j) tma_load_2d_pair(sb + 8192 * j, &tmB, lb, n0 + rank * (BN / 2) + 64 * j, kx);
+                for (int j = 0; j < BN / 128; ++j)
+                  tma_load_2d_pair(sb + 8192 * j, &tmB, lb, n0 + rank * (BN / 2) + 64 * j, kx);
+              }
             }
+            __syncwarp();
             if (++stage == S) { stage = 0; phase ^= 1u; }
             continue;
           }
-          mbar_expect_tx(fb, kStageBytes);
-          if (!A_MN) {
-            tma_load_2d(sa, &tmA, fb, kx, m0);
-          } else {
-            tma_load_2d(sa, &tmA, fb, m0, kx);
-            tma_load_2d(sa + 8192, &tmA, fb, m0 + 64, kx);
-          }
-          if (!B_MN) {
-            tma_load_2d(sb, &tmB, fb, kx, n0);
-          } else {
+          if (leader) {
+            mbar_expect_tx(fb, kStageBytes);
+            if (!A_MN) {
+              tma_load_2d(sa, &tmA, fb, kx, m0);
+            } else {
+              tma_load_2d(sa, &tmA, fb, m0, kx);
+              tma_load_2d(sa + 8192, &tmA, fb, m0 + 64, kx);
+            }
+            if (!B_MN) {
+              tma_load_2d(sb, &tmB, fb, kx, n0);
+            } else {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + 8192 * j, &tmB, fb, n0 + 64 * j, kx);
+              for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + 8192 * j, &tmB, fb, n0 + 64 * j, kx);
+            }
           }
+          __syncwarp();
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
       }
-      if (PAIR && !*abort_flag) {
+      if (PAIR && !aborted()) {
         // both MMAs release every stage (their commits land in this CTA's
         // empty barriers) before this CTA may leave the cluster
         for (int i = 0; i < S; ++i) {
-          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.st, 5)) break;
+          if (!wait(empty0 + 8 * stage, phase ^ 1u, 5)) break;
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
       }
-      if (*abort_flag) {
+      if (aborted() && leader) {
         // another role gave up: let this thread's copies still in flight land
         // (bounded, 10 ms per stage) before the CTA releases its shared memory
         for (int s = 0; s < S; ++s) {
