@@ -565,17 +565,21 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       const float* Dd = sD + buf * 128;
       // 32 queries strictly below the diagonal, all inside the sequence, need no masking
       const bool interior = (!p.causal || i0 > j0) && qrows >= 64 * g + 32 * (cc + 1) && len - j0 >= kK;
-      // dS^T buffer (it & 1) is free once dQ of block it-2 has read it
-      if (it >= 2 && !mbar_wait(b_dsempty + 8 * (it & 1), ((it >> 1) - 1) & 1, &no_abort, p.st, 26)) break;
-      // 16 queries at a time (few registers live: this kernel runs 22 warps)
+      // 16 queries at a time (few registers live: this kernel runs 24 warps)
       const uint32_t col = TM_S + g * 128 + cc * 32;
       const uint32_t rowoff = g * kTile + kr * 128;
+      bool failed = false;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t sr[16], dr[16];
         tmem_ld16_async(tbase + lane_off + col + 16 * hh, sr);
         tmem_ld16_async(tbase + lane_off + col + 64 + 16 * hh, dr);
+        // dS^T buffer (it & 1) is free once dQ of block it-2 has read it
+        // (checked while the first loads are in flight)
+        if (hh == 0 && it >= 2 && !mbar_wait(b_dsempty + 8 * (it & 1), ((it >> 1) - 1) & 1, &no_abort, p.st, 26))
+          failed = true;
         tmem_wait_ld();
+        if (failed) break;
         uint32_t pk[8], dk[8];   // bf16 pairs of P^T and dS^T
         if (interior) {
 #pragma unroll
@@ -617,6 +621,7 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
               make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
         }
       }
+      if (failed) break;
       tmem_wait_st();
       fence_before();
       fence_async_smem();
@@ -830,7 +835,7 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
     };
     auto issue = [&](int it) -> bool {
       const int st = it & 1, use = it >> 1;
-      if (!mbar_wait(b_qempty + 8 * st, (use & 1) ^ 1, abort_flag, p.st, 50)) return false;
+      if (!mbar_wait_call(b_qempty + 8 * st, (use & 1) ^ 1, abort_flag, p.st, 50)) return false;
       const int h = hk * p.G + hci * p.hc + it % p.hc;
       const int i0 = (nqb - 1 - it / p.hc) * kQ;
       mbar_expect_tx(b_qfull + 8 * st, 4 * kQChunk);
@@ -852,7 +857,7 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
         tma_load_2d(sbase + OFF_V + c * kKChunk, &tmV, b_kv, hk * kD + 64 * c, s0 + j0);
       }
     }
-    if (mbar_wait(b_kv, 0, &no_abort, p.st, 58)) {
+    if (mbar_wait_call(b_kv, 0, &no_abort, p.st, 58)) {
       if (krows < kK)
         for (int c = 0; c < 4; ++c) zero_rows(OFF_K + c * kKChunk, kK, krows);   // K chunks then V chunks
       fence_async_smem();
@@ -867,7 +872,7 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     for (int it = 0; ok && it < n_iter; ++it) {
       const int st = it & 1, use = it >> 1;
-      if (!mbar_wait(b_qfull + 8 * st, use & 1, &no_abort, p.st, 59)) break;
+      if (!mbar_wait_call(b_qfull + 8 * st, use & 1, &no_abort, p.st, 59)) break;
       const int i0 = (nqb - 1 - it / p.hc) * kQ;
       const int qrows = min(kQ, len - i0);
       if (qrows < kQ)
@@ -887,7 +892,7 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
       // ---------------- MMA issuer: the converged warp waits, one elected lane issues ----------------
       const bool leader = elect_one();
       auto wait = [&](uint32_t bar, uint32_t parity, unsigned site) {
-        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.st, site)) != 0;
+        return __all_sync(0xffffffffu, mbar_wait_call(bar, parity, abort_flag, p.st, site)) != 0;
       };
       constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);
       constexpr uint32_t id_kv = idesc_bf16(128, 128, false, true);
@@ -985,9 +990,9 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
       if (tg < 64) (tg < 32 ? sL : sD)[buf * 64 + 32 * g + (tg & 31)] = nxt;
       if (it + 1 < n_iter) nxt = fetch(it + 1);
       named_bar(1, 32 * kSoftWarps);
-      if (!mbar_wait(b_sfull, it & 1, &no_abort, p.st, 55)) break;
+      if (!mbar_wait_call(b_sfull, it & 1, &no_abort, p.st, 55)) break;
       // dS^T buffer (it & 1) is free once dQ^T of block it-2 has read it
-      if (it >= 2 && !mbar_wait(b_dsempty + 8 * (it & 1), ((it >> 1) - 1) & 1, &no_abort, p.st, 56)) break;
+      if (it >= 2 && !mbar_wait_call(b_dsempty + 8 * (it & 1), ((it >> 1) - 1) & 1, &no_abort, p.st, 56)) break;
       fence_after();
       const float* L = sL + buf * 64;
       const float* Dd = sD + buf * 64;
@@ -1050,7 +1055,7 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
     for (int it = 0; it < n_iter; ++it) {
       const int h = hk * p.G + hci * p.hc + it % p.hc;
       const int i0 = (nqb - 1 - it / p.hc) * kQ;
-      if (!mbar_wait(b_dqfull, it & 1, &no_abort, p.st, 57)) { ok = false; break; }
+      if (!mbar_wait_call(b_dqfull, it & 1, &no_abort, p.st, 57)) { ok = false; break; }
       fence_after();
       float v[64];                               // dQ[query c][head dim r], c = 0..63
       tmem_ld32(tbase + lane_off + TM_DQ, v);

@@ -37,9 +37,8 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 // Bounded wait for the phase of the given parity.  Returns false when the
 // budget ran out (recorded in the status word, abort flag raised) or another
 // role of this CTA gave up already.
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, DevStatus* st,
-                                       unsigned site) {
-  if (mbar_try(bar, parity)) return true;
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                   DevStatus* st, unsigned site) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try(bar, parity)) return true;
@@ -52,6 +51,16 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, vol
       }
     }
   }
+}
+// the phase already complete is checked inline; only a real wait makes the call
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, DevStatus* st,
+                                          unsigned site) {
+  return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, abort_flag, st, site);
+}
+// the same wait as one out-of-line call (smaller code at each call site)
+static __device__ __noinline__ bool mbar_wait_call(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                   DevStatus* st, unsigned site) {
+  return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, abort_flag, st, site);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
