@@ -582,14 +582,22 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
         if (failed) break;
         uint32_t pk[8], dk[8];   // bf16 pairs of P^T and dS^T
         if (interior) {
+          // lse and D of these 16 queries, four at a time (16-byte shared loads)
+          const float4* L4 = reinterpret_cast<const float4*>(L + 64 * g + cc * 32 + 16 * hh);
+          const float4* D4 = reinterpret_cast<const float4*>(Dd + 64 * g + cc * 32 + 16 * hh);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int qi = 64 * g + cc * 32 + 16 * hh + 2 * e;
-            const float p0 = exp2_approx(__uint_as_float(sr[2 * e]) * p.scale_log2 - L[qi]);
-            const float p1 = exp2_approx(__uint_as_float(sr[2 * e + 1]) * p.scale_log2 - L[qi + 1]);
-            pk[e] = pack_bf16x2(p0, p1);
-            dk[e] = pack_bf16x2(p0 * (__uint_as_float(dr[2 * e]) - Dd[qi]),
-                                p1 * (__uint_as_float(dr[2 * e + 1]) - Dd[qi + 1]));
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const float4 l4 = L4[e4], d4 = D4[e4];
+            const float lq[4] = {l4.x, l4.y, l4.z, l4.w}, dq[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+              const int e = 2 * e4 + e2;
+              const float p0 = exp2_approx(__uint_as_float(sr[2 * e]) * p.scale_log2 - lq[2 * e2]);
+              const float p1 = exp2_approx(__uint_as_float(sr[2 * e + 1]) * p.scale_log2 - lq[2 * e2 + 1]);
+              pk[e] = pack_bf16x2(p0, p1);
+              dk[e] = pack_bf16x2(p0 * (__uint_as_float(dr[2 * e]) - dq[2 * e2]),
+                                  p1 * (__uint_as_float(dr[2 * e + 1]) - dq[2 * e2 + 1]));
+            }
           }
         } else {
 #pragma unroll
