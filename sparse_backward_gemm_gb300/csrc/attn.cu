@@ -766,7 +766,7 @@ constexpr uint32_t OFF_K = 0, OFF_V = 2 * kKChunk, OFF_Q = 4 * kKChunk, OFF_DO =
 constexpr size_t kSmem = 1024 + OFF_BAR + 256;
 constexpr uint32_t TM_S = 0, TM_DP = 64, TM_DV = 128, TM_DK = 256, TM_DQ = 384;
 constexpr int kSoftWarps = 8;                       // two per TMEM lane quadrant
-constexpr int kThreads = 32 * (2 + kSoftWarps + 4);
+constexpr int kThreads = 32 * (2 + kSoftWarps + 4 + 2);
 static_assert(kSmem <= 232448, "shared memory");
 }  // namespace tcattn128
 
@@ -798,7 +798,7 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
   const uint32_t b_kv = smem_u32(bars + 0), b_qfull = smem_u32(bars + 1), b_qempty = smem_u32(bars + 3),
                  b_sfull = smem_u32(bars + 5), b_pfull = smem_u32(bars + 6), b_dsempty = smem_u32(bars + 7),
                  b_dqfull = smem_u32(bars + 9), b_dqempty = smem_u32(bars + 10), b_kvready = smem_u32(bars + 11),
-                 b_qready = smem_u32(bars + 12);
+                 b_qready = smem_u32(bars + 12), b_staged = smem_u32(bars + 16), b_boxfree = smem_u32(bars + 18);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* sL = reinterpret_cast<float*>(sm + OFF_LD);   // [2][64]
@@ -819,6 +819,10 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
     mbar_init(b_dqfull, 1);
     mbar_init(b_dqempty, 128);
     mbar_init(b_kvready, 1);
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(b_staged + 8 * r, 1);
+      mbar_init(b_boxfree + 8 * r, 1);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -1051,18 +1055,15 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
       fence_async_smem();
       mbar_arrive(b_pfull);
     }
-  } else {
+  } else if (warp < 2 + kSoftWarps + 4) {
     // ---------------- dQ / dK / dV epilogue ----------------
     const int t = threadIdx.x - 32 * (2 + kSoftWarps);
     const int q = warp & 3;
     const int r = q * 32 + lane;                // TMEM lane: head dim (dQ^T) or key (dK, dV)
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t stage = sbase + OFF_ST;
-    bool ok = true, chain_broken = false;
-    int* dq_pending = nullptr;   // the dQ turn this thread still has to pass on
+    bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
-      const int h = hk * p.G + hci * p.hc + it % p.hc;
-      const int i0 = (nqb - 1 - it / p.hc) * kQ;
       if (!mbar_wait_call(b_dqfull, it & 1, &no_abort, p.st, 57)) { ok = false; break; }
       fence_after();
       float v[64];                               // dQ[query c][head dim r], c = 0..63
@@ -1070,8 +1071,11 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
       tmem_ld32(tbase + lane_off + TM_DQ + 32, v + 32);
       fence_before();
       mbar_arrive(b_dqempty);
-      if (t == 0) bulk_wait_read_all();
-      named_bar(2, 128);
+      // the boxes are free once the reducer of the previous block saw its adds read them
+      if (it > 0 && !mbar_wait_call(b_boxfree + 8 * ((it - 1) & 1), ((it - 1) >> 1) & 1, &no_abort, p.st, 61)) {
+        ok = false;
+        break;
+      }
       // staging: four 32-column boxes of [64 query rows x 128 bytes]; head dim r
       // sits in box q, column lane
 #pragma unroll
@@ -1081,13 +1085,12 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
       }
       fence_async_smem();
       named_bar(2, 128);
-      if (t == 0)
-        ordered_dq_add(p, b, h, i0 / kQ, j, chain_broken, dq_pending, 60, [&] {
-#pragma unroll
-          for (int bx = 0; bx < 4; ++bx) tma_reduce_add_2d(&tmdQ, stage + bx * 8192, h * kD + 32 * bx, s0 + i0);
-        });
+      if (t == 0) mbar_arrive(b_staged + 8 * (it & 1));
     }
-    if (t == 0) dq_turn_flush(dq_pending, j);   // pass the last turn on, even after a failure
+    // the staging boxes take dK, dV once the last dQ adds have read them
+    if (ok && n_iter > 0 &&
+        !mbar_wait_call(b_boxfree + 8 * ((n_iter - 1) & 1), ((n_iter - 1) >> 1) & 1, &no_abort, p.st, 62))
+      ok = false;
     if (ok) {
       // every MMA has completed (the last dQ commit covers them all): drain
       // dK, dV 64 columns at a time through two [128 x 32] f32 boxes
@@ -1120,6 +1123,27 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
       }
     }
     if (t == 0) bulk_wait_all();
+  } else if (lane == 0) {
+    // ---------------- dQ reducers: warp 14 even blocks, warp 15 odd ----------------
+    // Each adds its blocks' dQ^T tiles in key-block order (the tile's turn),
+    // hands the staging boxes back once the adds have read them, and passes
+    // the turn on as soon as its adds have completed.
+    const int rr = warp - (2 + kSoftWarps + 4);
+    const uint32_t stage = sbase + OFF_ST;
+    bool broken = false;
+    for (int it = rr; it < n_iter; it += 2) {
+      const int h = hk * p.G + hci * p.hc + it % p.hc;
+      const int i0 = (nqb - 1 - it / p.hc) * kQ;
+      if (!mbar_wait_call(b_staged + 8 * (it & 1), (it >> 1) & 1, abort_flag, p.st, 63)) break;
+      int* turn = dq_turn_wait(p, b, h, i0 / kQ, j, broken, 60);
+#pragma unroll
+      for (int bx = 0; bx < 4; ++bx) tma_reduce_add_2d(&tmdQ, stage + bx * 8192, h * kD + 32 * bx, s0 + i0);
+      bulk_commit();
+      bulk_wait_read_all();
+      mbar_arrive(b_boxfree + 8 * (it & 1));
+      dq_turn_flush(turn, j);
+    }
+    bulk_wait_all();
   }
   fence_before();
   __syncthreads();

@@ -151,20 +151,6 @@ def _q_producer(n, stages=2):
     return prod
 
 
-def _epilogue(n, roles, arrivers, warps=2):
-    """dQ drain: wait dQ-full, arrive dQ-empty, two named barriers per block."""
-    names = [f"epilogue{w}" for w in range(warps)]
-    for name in names:
-        ops = []
-        for it in range(n):
-            ops += [("wait", ("dqfull", it)), ("arrive", ("dqempty", it)),
-                    ("arrive", (("nb", "epi"), 2 * it)), ("wait", (("nb", "epi"), 2 * it)),
-                    ("arrive", (("nb", "epi"), 2 * it + 1)), ("wait", (("nb", "epi"), 2 * it + 1))]
-        roles[name] = ops
-    arrivers["dqempty"] = names
-    arrivers[("nb", "epi")] = names
-
-
 def main64(n, warps=2):
     """Main pass, head dim 64: two query halves, each with its own S/dP buffer
     (where its P lands too) and group of softmax warps (a named barrier per
@@ -228,7 +214,8 @@ def main128(n, warps=2):
     """Main pass, head dim 128: one S/dP buffer (where P and dS land too), the
     softmax warps meet at a named barrier per block; the next block's S, dP
     are issued before this block's dQ^T, and the dS^T tile is double-buffered
-    by block for dQ^T."""
+    by block for dQ^T.  dQ^T goes through one staging area to the reducer of
+    the block's parity, as in the head-dim-64 pass."""
     mma = [("wait", ("kvready", 0))]
     if n:
         mma += [("wait", ring("qready", 0, 2)), ("sig", ("sfull", 0))]
@@ -250,7 +237,27 @@ def main128(n, warps=2):
             ops.append(("arrive", ("pfull", it)))
         roles[name] = ops
     arrivers = {"pfull": names, ("nb", "soft"): names}
-    _epilogue(n, roles, arrivers)
+    # epilogue: drain dQ^T, hand the accumulator back, stage it once the
+    # previous block's adds have read the boxes, hand it to the reducer of
+    # the block's parity (one thread each)
+    enames = [f"epilogue{w}" for w in range(2)]
+    for name in enames:
+        ops = []
+        for it in range(n):
+            ops += [("wait", ("dqfull", it)), ("arrive", ("dqempty", it))]
+            if it > 0:
+                ops.append(("wait", ring("boxfree", it - 1, 2)))
+            ops += [("arrive", (("nb", "epi"), it)), ("wait", (("nb", "epi"), it))]
+            if name == "epilogue0":
+                ops.append(("sig", ring("staged", it, 2)))
+        if n:   # dK, dV through the same boxes, once the last adds have read them
+            ops.append(("wait", ring("boxfree", n - 1, 2)))
+        roles[name] = ops
+    arrivers["dqempty"] = enames
+    arrivers[("nb", "epi")] = enames
+    for r in (0, 1):
+        roles[f"reducer{r}"] = [op for it in range(r, n, 2)
+                                for op in (("wait", ring("staged", it, 2)), ("sig", ring("boxfree", it, 2)))]
     return roles, arrivers
 
 
