@@ -436,10 +436,11 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
       // (buffer g), where its P^T lands too, so the MMAs of one half run while
       // the softmax warps of the other half work:
       //   S, dP (it, 0) | S, dP (it, 1) | [P(it, 0)] dV, dK (it, 0) | S, dP (it+1, 0)
-      //   | [P(it, 1)] dV, dK (it, 1) | S, dP (it+1, 1) | dQ (it) | ...
+      //   | [P(it, 1)] dV, dK (it, 1) | dQ (it) | S, dP (it+1, 1) | ...
       // MMAs issued by this thread run in issue order, so S (it+1, g) cannot
-      // overwrite P (it, g) before dV (it, g) has read it; dQ (it) reads dS^T
-      // from shared memory, so S, dP (it+1, 1) need not wait for it.
+      // overwrite P (it, g) before dV (it, g) has read it.  (dQ (it) reads dS^T
+      // from shared memory, so S, dP (it+1, 1) could go first; measured, the
+      // order above was as fast.)
       const bool leader = elect_one();
       auto wait = [&](uint32_t bar, uint32_t parity, unsigned site) {
         return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.st, site)) != 0;
