@@ -716,7 +716,7 @@ def run_case(args):
         ws = torch.empty(cl.collider_linear_workspace_size(cl.BF16, M, K, N), dtype=torch.uint8, device=dev)
         call = lambda: cl.collider_linear_bwd(cl.BF16, M, K, N, X, cl.ROWS_FULL, W, dY, cl.ROWS_FULL, idx, nk, dX,
                                               cl.ROWS_COMPACT, dW, None, ws)
-        flops = {"tc_gemm": 2.0 * int(keep.sum()) * K * N}
+        flops = {"tc_gemm": 4.0 * int(keep.sum()) * K * N}   # dX and dW
     else:
         H, Hkv, dh = s.H, s.Hkv, s.dh
         Q, Kt, V, dO = rnd(M, H * dh), rnd(M, Hkv * dh), rnd(M, Hkv * dh), rnd(M, H * dh)
