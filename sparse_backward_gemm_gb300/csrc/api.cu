@@ -124,6 +124,14 @@ struct Carver {
 
 void count_launch(int n) { g_launches += n; }
 
+bool pdl_allowed() {
+  static const bool on = [] {
+    const char* e = getenv("COLLIDER_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
 void set_last_error(const char* msg) { g_msg = msg; }
 
 void prof_begin(const Ctx& c, const char* name, long long m, long long n, long long k, int dyn) {
@@ -814,6 +822,9 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
                 (long long)D * 2, D * 2, 0};
     // a COMPACT dOut is copied with its zero padding
     CK(launch_gather(c, &j, 1, M, pad128(M), dout_full ? idx : nullptr, n_kept));
+    // from here on each of the chain's kernels follows a kernel of this
+    // library, so it is launched with programmatic stream serialisation
+    c.pdl = pdl_allowed();
   }
   CK(fork_side(c, side, 0));   // the side stream starts once dOut's kept rows exist
   if (!dense) {
@@ -863,6 +874,7 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
     CK(gemm_dw(cs, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept, in_rows));     // dW_down = s^T dOut
     CK(gemm_dx(c, M, F, D, L.dout_k, w->w_down, L.ds_k, 1, 0, n_kept, kEpiStore, nullptr, nullptr,
                in_rows));                                                              // ds = dOut W_down^T
+    c.pdl = pdl_allowed();
     CK(launch_swiglu_bwd(c, L.ds_k, 1, F, static_cast<const __nv_bfloat16*>(sv->up), L.dgu_k, M, pad128(M), idx,
                          n_kept));
     CK(fork_side(c, side, 1));
@@ -882,6 +894,7 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
     CK(gemm_dw(cs, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept, in_rows));     // dW2 = gelu(f1)^T dOut
     CK(gemm_dx(c, M, F, D, L.dout_k, w->w_down, L.ds_k, 1, 0, n_kept, kEpiStore, nullptr, nullptr,
                in_rows));                                                              // df2 = dOut W2^T
+    c.pdl = pdl_allowed();
     if (d->mlp_bias && g->db_down)
       CK(launch_colsum(c, L.dout_k, 1, D, M, D, nullptr, n_kept, L.col_part, g->db_down));
     CK(launch_gelu_bwd(c, L.ds_k, 1, F, static_cast<const __nv_bfloat16*>(sv->up), L.dgu_k, M, pad128(M), idx,
@@ -901,11 +914,15 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
   if (d->out_bias && g->db_o) CK(launch_colsum(c, dres, 1, D, M, D, nullptr, n_kept, L.col_part, g->db_o));
 
   // 4. filtered attention backward (+ RoPE backward) straight into dqkv_k
-  if (side) {
-    CK(cudaStreamWaitEvent(c.stream, side->ev[6], 0));   // qkv's kept rows, the attention's preparation
-    attn.stage = 2;
+  {
+    Ctx ca = c;
+    if (side) {
+      CK(cudaStreamWaitEvent(c.stream, side->ev[6], 0));   // qkv's kept rows, the attention's preparation
+      attn.stage = 2;
+      ca.pdl = false;   // its first kernel follows the wait, not a kernel
+    }
+    CK(launch_attn_bwd(ca, attn));
   }
-  CK(launch_attn_bwd(c, attn));
 
   // 5. QKV projection
   CK(fork_side(c, side, 3));

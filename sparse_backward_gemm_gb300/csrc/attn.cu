@@ -150,6 +150,7 @@ __device__ __forceinline__ void finalize_unit(const float* a, __nv_bfloat16* o, 
 }
 
 __global__ void attn_finalize_kernel(AttnK p, int DH) {
+  grid_dep_wait();
   const int nk = *p.n_kept;
   const int pad = padded_rows(nk, p.cap);
   const int rh = p.rot_half;
@@ -307,6 +308,7 @@ __global__ void __launch_bounds__(tcattn::kThreads, 1)
   using namespace tcattn;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  grid_dep_wait();   // the work ticket, D', lse and the accumulators come from the kernels ahead
   const int item = take_item(p.order);
   const int per_j = p.B * p.Hkv * p.nhc;
   const int j = item / per_j;
@@ -780,6 +782,7 @@ __global__ void __launch_bounds__(tcattn128::kThreads, 1)
   using namespace tcattn128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  grid_dep_wait();   // the work ticket, D', lse and the accumulators come from the kernels ahead
   const int item = take_item(p.order);
   const int per_j = p.B * p.Hkv * p.nhc;
   const int j = item / per_j;
@@ -1227,6 +1230,7 @@ __device__ __forceinline__ void dprep_body(const CUtensorMap& tmQ, const CUtenso
                      TM_O = Cfg::TM_O;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  grid_dep_wait();   // the kept offsets, Q, K, V and dO come from the kernels ahead
   // items: query block descending (most key blocks first), then sequence, head group
   const int ngroups = p.H / HPC;
   const int per_i = p.B * ngroups;
@@ -1704,29 +1708,36 @@ cudaError_t run(const Ctx& c, const AttnK& k, float rope_base, const AttnArgs& a
     dp.scale_log2 = k.scale_log2; dp.cu_kept = k.cu_kept; dp.lse2 = k.lse2; dp.Dvec = k.Dvec; dp.M = k.M;
     dp.dO = k.dO; dp.do_ld = k.do_ld;
     dp.st = c.st;
+    // (programmatic dependent launch: the pre-pass follows the preparation
+    // kernel, or whatever the caller's context allows; the main pass and the
+    // finalisation follow a kernel of this launcher, so they always may)
+    const bool pdl = pdl_allowed();
+    cudaError_t e;
     prof_begin(c, "attn_dprep_tc");
     // four query heads of one kv head per CTA share each K/V block (head dim 64, groups of 4+)
     if (DH == 64 && k.G % 4 == 0)
-      attn_dprep_tc_kernel<64, 4><<<k.B * (k.H / 4) * nkb, DprepCfg<64, 4>::kThreads, DprepCfg<64, 4>::kSmem,
-                                    c.stream>>>(tq_pre, tk, tv, dp);
+      e = launch_k(c, c.pdl || (a.stage != 2 && pdl), attn_dprep_tc_kernel<64, 4>, dim3(k.B * (k.H / 4) * nkb),
+                   dim3(DprepCfg<64, 4>::kThreads), DprepCfg<64, 4>::kSmem, 1, tq_pre, tk, tv, dp);
     else
-      attn_dprep_tc_kernel<DH, 1><<<k.B * k.H * nkb, DprepCfg<DH, 1>::kThreads, DprepCfg<DH, 1>::kSmem, c.stream>>>(
-          tq_pre, tk, tv, dp);
+      e = launch_k(c, c.pdl || (a.stage != 2 && pdl), attn_dprep_tc_kernel<DH, 1>, dim3(k.B * k.H * nkb),
+                   dim3(DprepCfg<DH, 1>::kThreads), DprepCfg<DH, 1>::kSmem, 1, tq_pre, tk, tv, dp);
     prof_end(c);
+    if (e != cudaSuccess) return launched(e);
     prof_begin(c, "attn_main_tc");
     if (DH == 64)
-      attn_main_tc_kernel<<<k.B * k.Hkv * nkb * m.nhc, tcattn::kThreads, tcattn::kSmem, c.stream>>>(
-          tq, tk, tv, tdo, tdq, tdk, tdv, m);
+      e = launch_k(c, pdl, attn_main_tc_kernel, dim3(k.B * k.Hkv * nkb * m.nhc), dim3(tcattn::kThreads),
+                   tcattn::kSmem, 1, tq, tk, tv, tdo, tdq, tdk, tdv, m);
     else
-      attn_main_tc128_kernel<<<k.B * k.Hkv * nkb * m.nhc, tcattn128::kThreads, tcattn128::kSmem, c.stream>>>(
-          tq, tk, tv, tdo, tdq, tdk, tdv, m);
+      e = launch_k(c, pdl, attn_main_tc128_kernel, dim3(k.B * k.Hkv * nkb * m.nhc), dim3(tcattn128::kThreads),
+                   tcattn128::kSmem, 1, tq, tk, tv, tdo, tdq, tdk, tdv, m);
     prof_end(c);
+    if (e != cudaSuccess) return launched(e);
+    prof_begin(c, "attn_finalize");
+    e = launch_k(c, pdl, attn_finalize_kernel, dim3(c.num_sms * 4), dim3(256), 0, 1, k, DH);
+    prof_end(c);
+    count_launch(3);
+    return launched(e);
   }
-  prof_begin(c, "attn_finalize");
-  attn_finalize_kernel<<<c.num_sms * 4, 256, 0, c.stream>>>(k, DH);
-  prof_end(c);
-  count_launch(3);
-  return cudaGetLastError();
 }
 
 template <int DH>

@@ -39,6 +39,23 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 constexpr uint64_t kWaitBudgetNs = 2000000000ull;  // 2 s
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch.  A kernel launched with the programmatic
+// stream-serialisation attribute is scheduled as soon as the kernel ahead of
+// it in the stream has exited, without waiting for that kernel's completion
+// to be processed; it must not touch memory that kernel (or any earlier one)
+// reads or writes before grid_dep_wait() returns, which happens once those
+// grids have completed and their writes are visible.  Every kernel that may
+// be launched so calls it in every CTA before it exits, so the wait reaches
+// back along the whole stream.  No kernel here lets its dependents be
+// scheduled before it exits (griddepcontrol.launch_dependents): measured on
+// the layer backward, the chain's next kernel then parked on SMs that the
+// side stream's persistent weight-gradient GEMMs were waiting for, and the
+// step was 10% slower; scheduled at exit it is 2% faster than without the
+// attribute.  For a kernel launched without the attribute the wait returns
+// at once.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // small math / conversion helpers
 __device__ __forceinline__ float bf2f(__nv_bfloat16 v) { return __bfloat162float(v); }
 __device__ __forceinline__ __nv_bfloat16 f2bf(float v) { return __float2bfloat16_rn(v); }

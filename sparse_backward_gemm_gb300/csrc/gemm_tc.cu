@@ -270,6 +270,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                  tempty0 = smem_u32(bars + 2 * S + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, TWO ? 256 : 128);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+  }
+  if (warp == 1) {
+    if (TWO) tmem_alloc_pair(smem_u32(tmem_slot), Cfg::kTmemCols);
+    else tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+  }
+  fence_before();
+  __syncthreads();
+  if (PAIR) cluster_sync();   // the peer's barriers exist before any copy or commit reaches them
+  fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // Everything above may run before the kernel ahead in the stream has
+  // completed (programmatic dependent launch); the kept count, the operands
+  // and the output are read or written only after it has.
+  grid_dep_wait();
   int M = p.M, K = p.K;
   if (p.dyn) {
     int nk = *p.n_kept;
@@ -300,30 +327,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     m0 = (PAIR ? 2 * mu + rank : mu) * BM;
     n0 = (t / sp.m_units) * BN;
   };
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, TWO ? 256 : 128);
-    }
-    *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
-  }
-  if (warp == 1) {
-    if (TWO) tmem_alloc_pair(smem_u32(tmem_slot), Cfg::kTmemCols);
-    else tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
-  }
-  fence_before();
-  __syncthreads();
-  if (PAIR) cluster_sync();   // the peer's barriers exist before any copy or commit reaches them
-  fence_after();
-  const uint32_t tmem_base = *tmem_slot;
 
   if (sp.num_kb == 0) {
     // empty reduction (nothing kept): the output is zero
@@ -410,6 +413,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if (!ok) break;
       }
+      // this CTA's last operands are on their way: the next kernel in the
+      // stream may be scheduled (it waits for this grid before reading)
       if (PAIR && !aborted()) {
         // both MMAs release every stage (their commits land in this CTA's
         // empty barriers) before this CTA may leave the cluster
@@ -645,19 +650,7 @@ cudaError_t launch_variant(const Ctx& c, const TcGemm& g, const CUtensorMap& ma,
     const long long units = (m_tiles + 1) / 2 * n_tiles;
     const int pairs = p.partial ? pairs_fit   // stream-K: every pair takes a share
                                 : static_cast<int>(units < pairs_fit ? (units < 1 ? 1 : units) : pairs_fit);
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2 * pairs);
-    cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = c.stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, ma, mb, p);
+    return launched(launch_k(c, c.pdl, kern, dim3(2 * pairs), dim3(kTcThreads), kSmemBytes, 2, ma, mb, p));
   }
   const long long tiles = m_tiles * n_tiles;
   int grid;
@@ -667,8 +660,7 @@ cudaError_t launch_variant(const Ctx& c, const TcGemm& g, const CUtensorMap& ma,
     grid = static_cast<int>(tiles < c.num_sms ? tiles : c.num_sms);
   }
   if (grid < 1) grid = 1;
-  kern<<<grid, kTcThreads, kSmemBytes, c.stream>>>(ma, mb, p);
-  return cudaGetLastError();
+  return launched(launch_k(c, c.pdl, kern, dim3(grid), dim3(kTcThreads), kSmemBytes, 1, ma, mb, p));
 }
 
 }  // namespace

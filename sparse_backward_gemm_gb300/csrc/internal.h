@@ -14,7 +14,52 @@ struct Ctx {
   cudaStream_t stream;
   DevStatus* st;   // device status word of the current device
   int num_sms;
+  // launch the next kernel with programmatic stream serialisation (it is
+  // scheduled as the kernel ahead of it exits, and waits for that kernel's
+  // completion with grid_dep_wait).  Set only where the operation ahead in
+  // the stream is a kernel (not an event wait or a copy) that was launched
+  // without the attribute or calls grid_dep_wait in every CTA.
+  bool pdl = false;
 };
+
+// Whether programmatic dependent launch is used at all (COLLIDER_PDL=0 turns
+// it off; read once).
+bool pdl_allowed();
+
+// Launch kernel k on c.stream, with the programmatic stream-serialisation
+// attribute when pdl is set, and a cluster of cluster_x CTAs when > 1.
+template <typename... P, typename... A>
+cudaError_t launch_k(const Ctx& c, bool pdl, void (*k)(P...), dim3 grid, dim3 block, size_t smem, int cluster_x,
+                     A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = c.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<A&&>(args)...);
+}
+
+// The error of a launch made with launch_k, the runtime's last error cleared.
+inline cudaError_t launched(cudaError_t e) {
+  const cudaError_t last = cudaGetLastError();
+  return e != cudaSuccess ? e : last;
+}
 
 // Launch accounting (per host thread) and optional per-kernel event timing.
 void count_launch(int n = 1);

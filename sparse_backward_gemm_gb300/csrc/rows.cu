@@ -50,6 +50,7 @@ struct GatherBatch {
 __global__ void __launch_bounds__(256) gather_kernel(GatherBatch jb, int M, long long cap,
                                                      const int32_t* __restrict__ idx,
                                                      const int32_t* __restrict__ n_kept, DevStatus* st) {
+  grid_dep_wait();
   const GatherJob J = jb.j[blockIdx.y];
   const int nk = *n_kept;
   const int pad = padded_rows(nk, cap);
@@ -189,6 +190,7 @@ __device__ __forceinline__ void norm_dy8(const NormBwdArgs& a, long long off, fl
 }
 
 __global__ void __launch_bounds__(kNormWarps * 32) norm_rows_kernel(NormBwdArgs a, DevStatus* st) {
+  grid_dep_wait();
   const int D = a.D;
   const int nk = *a.n_kept;
   const int pad = a.out_full ? nk : padded_rows(nk, a.cap);
@@ -280,6 +282,7 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const void* __restrict_
                                                          __nv_bfloat16* __restrict__ dgu, int M, long long cap,
                                                          const int32_t* __restrict__ idx,
                                                          const int32_t* __restrict__ n_kept, DevStatus* st) {
+  grid_dep_wait();
   const int nk = *n_kept;
   const int pad = padded_rows(nk, cap);
   const int vpr = F >> 3;   // 8-wide vectors per row
@@ -315,6 +318,7 @@ __global__ void __launch_bounds__(256) gelu_bwd_kernel(const void* __restrict__ 
                                                        __nv_bfloat16* __restrict__ df1, int M, long long cap,
                                                        const int32_t* __restrict__ idx,
                                                        const int32_t* __restrict__ n_kept, DevStatus* st) {
+  grid_dep_wait();
   const int nk = *n_kept;
   const int pad = padded_rows(nk, cap);
   const int vpr = F >> 3;
@@ -461,10 +465,10 @@ cudaError_t launch_gather(const Ctx& c, const GatherJob* jobs, int njobs, int M,
   double bytes = 0;
   for (int i = 0; i < njobs; ++i) bytes += 2.0 * jobs[i].row_bytes;  // per kept row
   prof_begin(c, "gather_rows");
-  gather_kernel<<<grid, 256, 0, c.stream>>>(b, M, cap, idx, n_kept, c.st);
+  const cudaError_t e = launch_k(c, c.pdl, gather_kernel, grid, dim3(256), 0, 1, b, M, cap, idx, n_kept, c.st);
   prof_end(c);
   count_launch();
-  return cudaGetLastError();
+  return launched(e);
 }
 
 cudaError_t launch_scatter(const Ctx& c, const char* compact, long long compact_ld, char* full,
@@ -499,10 +503,11 @@ size_t norm_part_floats(int M, int D) {
 
 cudaError_t launch_norm_rows(const Ctx& c, const NormBwdArgs& a) {
   prof_begin(c, "norm_bwd");
-  norm_rows_kernel<<<grid_rows(c, a.cap, kNormWarps), kNormWarps * 32, 0, c.stream>>>(a, c.st);
+  const cudaError_t e = launch_k(c, c.pdl, norm_rows_kernel, dim3(grid_rows(c, a.cap, kNormWarps)),
+                                 dim3(kNormWarps * 32), 0, 1, a, c.st);
   count_launch(1);
   prof_end(c);
-  return cudaGetLastError();
+  return launched(e);
 }
 
 cudaError_t launch_norm_cols(const Ctx& c, const NormBwdArgs& a) {
@@ -530,21 +535,21 @@ cudaError_t launch_norm_bwd(const Ctx& c, const NormBwdArgs& a) {
 cudaError_t launch_swiglu_bwd(const Ctx& c, const void* ds, int ds_is_bf16, int F, const __nv_bfloat16* gu,
                               __nv_bfloat16* dgu, int M, long long cap, const int32_t* idx, const int32_t* n_kept) {
   prof_begin(c, "swiglu_bwd");
-  swiglu_bwd_kernel<<<grid_rows(c, cap * (F / 8), 256), 256, 0, c.stream>>>(ds, ds_is_bf16, F, gu, dgu, M, cap,
-                                                                            idx, n_kept, c.st);
+  const cudaError_t e = launch_k(c, c.pdl, swiglu_bwd_kernel, dim3(grid_rows(c, cap * (F / 8), 256)), dim3(256), 0,
+                                 1, ds, ds_is_bf16, F, gu, dgu, M, cap, idx, n_kept, c.st);
   prof_end(c);
   count_launch();
-  return cudaGetLastError();
+  return launched(e);
 }
 
 cudaError_t launch_gelu_bwd(const Ctx& c, const void* df2, int df2_is_bf16, int F, const __nv_bfloat16* f1,
                             __nv_bfloat16* df1, int M, long long cap, const int32_t* idx, const int32_t* n_kept) {
   prof_begin(c, "gelu_bwd");
-  gelu_bwd_kernel<<<grid_rows(c, cap * (F / 8), 256), 256, 0, c.stream>>>(df2, df2_is_bf16, F, f1, df1, M, cap,
-                                                                          idx, n_kept, c.st);
+  const cudaError_t e = launch_k(c, c.pdl, gelu_bwd_kernel, dim3(grid_rows(c, cap * (F / 8), 256)), dim3(256), 0, 1,
+                                 df2, df2_is_bf16, F, f1, df1, M, cap, idx, n_kept, c.st);
   prof_end(c);
   count_launch();
-  return cudaGetLastError();
+  return launched(e);
 }
 
 cudaError_t launch_ce_bwd(const Ctx& c, const __nv_bfloat16* logits, const int32_t* targets, int V, int M,
