@@ -722,18 +722,14 @@ thread_local int* g_sk_counters = nullptr;
 thread_local long long g_sk_cap = 0;
 
 // C (bf16 or f32, COMPACT [Mk, N]) = A_k [Mk, K] . W^T with W stored [N, K]
-// (epi: a fused activation backward, reading FULL rows of aux through idx)
 cudaError_t gemm_dx(const Ctx& c, int M, int N, int K, const void* A, const void* W, void* C, int c_bf16,
-                    int accumulate, const int32_t* n_kept, int epi = kEpiStore, const void* aux = nullptr,
-                    const int32_t* idx = nullptr, long long a_rows = -1) {
+                    int accumulate, const int32_t* n_kept, long long a_rows = -1) {
   TcGemm g{};
   g.partial = g_sk_partial; g.counters = g_sk_counters; g.counter_cap = g_sk_cap;
-  g.epi = epi; g.aux = static_cast<const __nv_bfloat16*>(aux); g.idx = idx; g.aux_rows = M;
-  g.aux_ld = epi == kEpiSwiGLU ? 2LL * N : N;
   g.M = M; g.N = N; g.K = K;
   g.A = A; g.lda = K; g.a_mn_major = 0; g.a_rows = a_rows > 0 ? a_rows : pad128(M);
   g.B = W; g.ldb = K; g.b_mn_major = 0; g.b_rows = N;
-  g.C = C; g.ldc = epi == kEpiSwiGLU ? 2LL * N : N; g.c_bf16 = c_bf16; g.accumulate = accumulate; g.zero_pad = 1;
+  g.C = C; g.ldc = N; g.c_bf16 = c_bf16; g.accumulate = accumulate; g.zero_pad = 1;
   g.c_rows = pad128(M);
   g.n_kept = n_kept; g.dyn = 1;
   return launch_tc_gemm(c, g);
@@ -872,8 +868,7 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
   const __nv_bfloat16* dres = L.dout_k;   // gradient flowing along the residual into the attention half
   if (llama) {
     CK(gemm_dw(cs, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept, in_rows));     // dW_down = s^T dOut
-    CK(gemm_dx(c, M, F, D, L.dout_k, w->w_down, L.ds_k, 1, 0, n_kept, kEpiStore, nullptr, nullptr,
-               in_rows));                                                              // ds = dOut W_down^T
+    CK(gemm_dx(c, M, F, D, L.dout_k, w->w_down, L.ds_k, 1, 0, n_kept, in_rows));      // ds = dOut W_down^T
     c.pdl = pdl_allowed();
     CK(launch_swiglu_bwd(c, L.ds_k, 1, F, static_cast<const __nv_bfloat16*>(sv->up), L.dgu_k, M, pad128(M), idx,
                          n_kept));
@@ -892,8 +887,7 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
     dres = L.dh_k;
   } else {
     CK(gemm_dw(cs, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept, in_rows));     // dW2 = gelu(f1)^T dOut
-    CK(gemm_dx(c, M, F, D, L.dout_k, w->w_down, L.ds_k, 1, 0, n_kept, kEpiStore, nullptr, nullptr,
-               in_rows));                                                              // df2 = dOut W2^T
+    CK(gemm_dx(c, M, F, D, L.dout_k, w->w_down, L.ds_k, 1, 0, n_kept, in_rows));      // df2 = dOut W2^T
     c.pdl = pdl_allowed();
     if (d->mlp_bias && g->db_down)
       CK(launch_colsum(c, L.dout_k, 1, D, M, D, nullptr, n_kept, L.col_part, g->db_down));
@@ -909,8 +903,7 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
   // 3. attention output projection
   CK(fork_side(c, side, 2));
   CK(gemm_dw(cs, M, Hd, D, L.o_k, Hd, dres, D, g->dw_o, n_kept, in_rows));            // dW_o = o^T dh
-  CK(gemm_dx(c, M, Hd, D, dres, w->w_o, L.do_k, 1, 0, n_kept, kEpiStore, nullptr, nullptr,
-             in_rows));                                                                // do = dh W_o^T
+  CK(gemm_dx(c, M, Hd, D, dres, w->w_o, L.do_k, 1, 0, n_kept, in_rows));              // do = dh W_o^T
   if (d->out_bias && g->db_o) CK(launch_colsum(c, dres, 1, D, M, D, nullptr, n_kept, L.col_part, g->db_o));
 
   // 4. filtered attention backward (+ RoPE backward) straight into dqkv_k

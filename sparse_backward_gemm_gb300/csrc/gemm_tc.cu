@@ -41,11 +41,6 @@ struct TcParams {
   float* partial;    // stream-K: [2 * gridDim.x][BM][BN] f32 partial tiles (null: whole tiles only)
   int* counters;     // stream-K: per-(tile, pair rank) arrival counts, zero on entry and left zero
   int split_mode;    // 0 whole tiles, 1 stream-K, 2 hybrid, 3 auto (see Split)
-  int epi;           // TcEpilogue
-  const __nv_bfloat16* aux;
-  long long aux_ld;
-  const int32_t* idx;
-  int aux_rows;
   DevStatus* st;
 };
 
@@ -165,60 +160,9 @@ struct SegIter {
   }
 };
 
-__device__ __forceinline__ float sigmoid_dev(float x) { return 1.f / (1.f + __expf(-x)); }
-__device__ __forceinline__ float gelu_tanh_grad_dev(float x) {
-  const float c = 0.7978845608028654f, a = 0.044715f;
-  const float t = tanhf(c * (x + a * x * x * x));
-  return 0.5f * (1.f + t) + 0.5f * x * (1.f - t * t) * c * (1.f + 3.f * a * x * x);
-}
-
 // Store 32 consecutive columns of one output row (bf16 or f32, optional
-// accumulate into C, zero rows past the kept count up to the padding, fused
-// activation backward).
+// accumulate into C, zero rows past the kept count up to the padding).
 __device__ __forceinline__ void store32(const TcParams& p, int row, int col, bool row_ok, float* v) {
-  if (p.epi != kEpiStore) {
-    // activation backward on the kept row: the saved pre-activations are read
-    // through the kept-row index (padding rows stay zero)
-    const int N = p.N;
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.C) + (long long)row * p.ldc + col;
-    float o1[32], o2[32];
-    if (row_ok) {
-      const int t = p.idx[row];
-      const bool in = (unsigned)t < (unsigned)p.aux_rows;
-      if (!in) report_error(p.st, kErrBadIndex, 10);
-      const __nv_bfloat16* a = p.aux + (long long)(in ? t : 0) * p.aux_ld + col;
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        float x[8], u[8];
-        if (col + 8 * g + 8 <= N) {
-          unpack8(*reinterpret_cast<const uint4*>(a + 8 * g), x);
-          if (p.epi == kEpiSwiGLU) unpack8(*reinterpret_cast<const uint4*>(a + N + 8 * g), u);
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float d = in ? v[8 * g + e] : 0.f;
-          if (p.epi == kEpiSwiGLU) {
-            const float sg = sigmoid_dev(x[e]);
-            o1[8 * g + e] = d * u[e] * sg * (1.f + x[e] * (1.f - sg));
-            o2[8 * g + e] = d * x[e] * sg;
-          } else {
-            o1[8 * g + e] = d * gelu_tanh_grad_dev(x[e]);
-          }
-        }
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) o1[i] = o2[i] = 0.f;
-    }
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      if (col + 8 * g + 8 <= N) {
-        *reinterpret_cast<uint4*>(out + 8 * g) = pack8(o1 + 8 * g);
-        if (p.epi == kEpiSwiGLU) *reinterpret_cast<uint4*>(out + N + 8 * g) = pack8(o2 + 8 * g);
-      }
-    }
-    return;
-  }
   if (p.c_bf16) {
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.C) + (long long)row * p.ldc + col;
 #pragma unroll
@@ -731,7 +675,7 @@ cudaError_t launch_tc_gemm(const Ctx& c, const TcGemm& g) {
   if (!ok) return cudaErrorInvalidValue;
   TcParams p{g.M, g.N, g.K, g.dyn, g.n_kept, g.C, g.ldc, g.c_bf16, g.accumulate, g.zero_pad,
              g.c_rows > 0 ? g.c_rows : g.M, sk ? g.partial : nullptr, sk ? g.counters : nullptr,
-             split, g.epi, g.aux, g.aux_ld, g.idx, g.aux_rows, c.st};
+             split, c.st};
   prof_begin(c, "tc_gemm", g.M, g.N, g.K, g.dyn);
   cudaError_t e;
   const int key = (bn == 256 ? 100 : 0) + (g.a_mn_major ? 10 : (g.b_mn_major ? 20 : 0)) + mode;

@@ -184,13 +184,6 @@ cudaError_t launch_simt_gemm(const Ctx& c, const SimtGemm& g);
 // dyn = 2: K is limited by *n_kept (operand rows beyond must be 0 or finite
 // and are multiplied by 0-padded rows of the other operand -- callers keep
 // COMPACT buffers zero-padded to 128 rows).
-// Epilogue applied to the product before it is stored:
-//   kEpiStore   C = result
-//   kEpiSwiGLU  result = ds (SwiGLU output gradient) of COMPACT row r; with
-//               g, u = aux[idx[r]][c], aux[idx[r]][F + c] (bf16 FULL rows, aux_ld):
-//               C[r][c] = ds*u*sig(g)*(1 + g*(1 - sig(g))),  C[r][F + c] = ds*silu(g)
-//   kEpiGelu    result = df2; C[r][c] = df2 * gelu_tanh'(aux[idx[r]][c])
-enum TcEpilogue { kEpiStore = 0, kEpiSwiGLU = 1, kEpiGelu = 2 };
 struct TcGemm {
   int M, N, K;
   const void* A; long long lda; int a_mn_major;  // lda in elements
@@ -207,11 +200,6 @@ struct TcGemm {
   float* partial;
   int* counters;
   long long counter_cap;
-  int epi;                      // TcEpilogue (bf16 C only)
-  const __nv_bfloat16* aux;     // FULL rows read by the fused epilogue
-  long long aux_ld;
-  const int32_t* idx;           // kept-row index list (fused epilogue)
-  int aux_rows;                 // rows of aux (index bound)
 };
 constexpr int kSkMaxCtas = 256;
 constexpr size_t kSkPartialFloats = (size_t)kSkMaxCtas * 2 * 128 * 256;
