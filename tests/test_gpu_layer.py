@@ -117,6 +117,20 @@ def test_block_nan_poison_and_determinism():
     assert np.all(b["dx"][km] == 0)
 
 
+@pytest.mark.parametrize("arch", ["llama", "qwen"])
+def test_block_backward_several_query_blocks(arch):
+    """Sequences of several 128-row query and key blocks (the attention's
+    causal mask then falls inside blocks as well as on whole blocks), element
+    by element against the oracle."""
+    s, w, t, saved, ref = _oracle_case(SMALL[arch].with_(B=2, T=768))
+    L = gu.DeviceLayer(s, w, saved)
+    idx, cu, nk = gu.compact(t["keep"])
+    L.run(gu.bf16(t["dout"]), idx, cu, nk)
+    got = L.results()
+    cl.collider_check()
+    _compare(got, ref, t["keep"])
+
+
 def test_block_backward_is_reproducible():
     """Every output of the block -- dx and the weight gradients below the
     attention (dw_qkv, dnorm1_w) included -- is bit-identical run to run, on
