@@ -264,7 +264,9 @@ typedef struct {
   const void* w_down;
 } collider_layer_weights;
 
-/* Saved forward activations, FULL rows (M = B*T), bf16 unless noted:
+/* Saved forward activations, FULL rows (M = B*T), bf16 unless noted (device
+ * memory; for a filtered collider_layer_bwd call also pinned host memory the
+ * device addresses at the same pointer, see there):
  *   x [M,D] block input; a [M,D] = norm1(x); mean1 f32 [M] (LayerNorm only);
  *   rstd1 f32 [M]; qkv [M,(H+2Hkv)dh] with q and k AFTER RoPE; o [M,H*dh]
  *   attention output; lse f32 [B,H,T].
@@ -320,7 +322,15 @@ typedef struct {
  * gathered, dx is written in place (dout_rows / dx_rows do not matter, the
  * COMPACT rows being the FULL rows); the library writes the identity index
  * into its workspace for the kernels that read one.  Giving only some of the
- * three is COLLIDER_ERR_INVALID_ARG.  Workspace: collider_layer_workspace_size. */
+ * three is COLLIDER_ERR_INVALID_ARG.  Workspace: collider_layer_workspace_size.
+ * Where the inputs may live: a filtered call reads dOut and the saved set only
+ * at the kept rows, with plain loads, so they may also be pinned host memory
+ * (cudaHostAlloc / cudaHostRegister) that the device addresses at the same
+ * pointer under unified addressing: then only the kept rows cross the host
+ * link.  The dense call needs them in device memory, and the weights and
+ * gradients always do.  Any other memory (pageable host memory, or host
+ * memory where device memory is needed) is COLLIDER_ERR_INVALID_ARG, checked
+ * before any launch. */
 size_t collider_layer_workspace_size(const collider_layer_desc* desc);
 collider_status collider_layer_bwd(const collider_layer_desc* desc,
                                    const collider_layer_weights* w,

@@ -966,6 +966,44 @@ collider_status check_layer_ptrs(const collider_layer_desc* d, const collider_la
   return COLLIDER_OK;
 }
 
+// Where the saved set and dOut live: device or managed memory, or pinned host
+// memory that the device addresses at the same pointer (unified addressing).
+// The filtered backward reads those inputs only with plain loads, at the kept
+// rows (through idx), so from host memory only the kept rows cross the host
+// link; the dense call hands whole tensors to TMA and needs device memory.
+// Anything else (pageable host memory) is refused rather than read.  The
+// weights (TMA operands) and the gradients must be device or managed memory.
+collider_status check_input_memory(const collider_layer_weights* w, const collider_layer_saved* sv,
+                                   const void* dOut, const collider_layer_grads* g, bool dense) {
+  const void* ps[] = {sv->x, sv->a, sv->mean1, sv->rstd1, sv->qkv, sv->o, sv->lse, sv->h, sv->b,
+                      sv->rstd2, sv->up, sv->s, dOut,
+                      // from here on: device or managed memory only
+                      w->norm1_w, w->w_qkv, w->w_o, w->norm2_w, w->w_up, w->w_down,
+                      g->dx, g->dnorm1_w, g->dnorm1_b, g->dw_qkv, g->db_qkv, g->dw_o, g->db_o, g->dnorm2_w,
+                      g->dw_up, g->db_up, g->dw_down, g->db_down};
+  constexpr int kHostOk = 13;   // the saved set and dOut
+  for (int i = 0; i < static_cast<int>(sizeof(ps) / sizeof(ps[0])); ++i) {
+    const void* p = ps[i];
+    if (!p) continue;
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(COLLIDER_ERR_INVALID_ARG, "collider_layer_bwd: a pointer the CUDA runtime does not know");
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) continue;
+    if (i < kHostOk && a.type == cudaMemoryTypeHost && a.devicePointer == p) {
+      if (dense)
+        return fail(COLLIDER_ERR_INVALID_ARG, "collider_layer_bwd: the dense call needs its inputs in device memory");
+      continue;
+    }
+    return fail(COLLIDER_ERR_INVALID_ARG,
+                i < kHostOk ? "collider_layer_bwd: inputs must be device memory or pinned host memory the device "
+                              "can address"
+                            : "collider_layer_bwd: weights and gradients must be device memory");
+  }
+  return COLLIDER_OK;
+}
+
 }  // namespace
 
 extern "C" size_t collider_layer_workspace_size(const collider_layer_desc* d) {
@@ -994,6 +1032,8 @@ extern "C" collider_status collider_layer_bwd(const collider_layer_desc* d, cons
     return fail(COLLIDER_ERR_INVALID_ARG, "collider_layer_bwd: needs %zu bytes of 256-aligned workspace", need);
   Ctx c;
   s = make_ctx(stream, &c);
+  if (s != COLLIDER_OK) return s;
+  s = check_input_memory(w, sv, dOut, g, dense);
   if (s != COLLIDER_OK) return s;
   Carver cv{static_cast<char*>(ws), ws_bytes, 0, false};
   LayerBufs L;

@@ -131,6 +131,45 @@ def test_block_backward_several_query_blocks(arch):
     _compare(got, ref, t["keep"])
 
 
+def test_block_backward_reads_pinned_host_inputs():
+    """The filtered call reads dOut and the saved set only at the kept rows,
+    so they may stay in pinned host memory the device addresses directly: the
+    outputs are bit-identical to those from device copies.  The dense call
+    (whole tensors to TMA) and pageable host memory are refused before any
+    launch, with the outputs untouched."""
+    s, w, t, saved, ref = _oracle_case(SMALL["llama"].with_(B=2, T=512))
+    L = gu.DeviceLayer(s, w, saved)
+    idx, cu, nk = gu.compact(t["keep"])
+    dout = gu.bf16(t["dout"])
+    L.run(dout, idx, cu, nk)
+    a = L.results()
+    _compare(a, ref, t["keep"])
+    by_ptr = {x.data_ptr(): x for x in L.keep_alive}
+    fields = [f for f, _ in cl.LayerSaved._fields_]
+    pinned = {f: by_ptr[getattr(L.saved, f)].cpu().pin_memory() for f in fields if getattr(L.saved, f)}
+    hs = cl.LayerSaved(**{f: v.data_ptr() for f, v in pinned.items()})
+    hdout = dout.cpu().pin_memory()
+    for v in L.grads_t.values():
+        v.fill_(float("nan"))
+    L.dx.fill_(float("nan"))
+    cl.collider_layer_bwd(L.desc, L.weights, hs, hdout, cl.ROWS_FULL, idx, cu, nk, L.grads, cl.ROWS_FULL, L.ws)
+    b = L.results()
+    cl.collider_check()
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+    for v in L.grads_t.values():
+        v.fill_(7.0)
+    with pytest.raises(cl.ColliderError):
+        cl.collider_layer_bwd(L.desc, L.weights, hs, hdout, cl.ROWS_FULL, None, None, None, L.grads, cl.ROWS_FULL,
+                              L.ws)
+    with pytest.raises(cl.ColliderError):
+        cl.collider_layer_bwd(L.desc, L.weights, L.saved, dout.cpu(), cl.ROWS_FULL, idx, cu, nk, L.grads,
+                              cl.ROWS_FULL, L.ws)
+    torch.cuda.synchronize()
+    for v in L.grads_t.values():
+        assert torch.all(v == 7.0)
+
+
 def test_block_backward_is_reproducible():
     """Every output of the block -- dx and the weight gradients below the
     attention (dw_qkv, dnorm1_w) included -- is bit-identical run to run, on
