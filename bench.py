@@ -51,9 +51,10 @@ def parse():
                    help="time only the headline block (skip the other block shapes and the stack)")
     p.add_argument("--workload", default=WORKLOAD, choices=sorted(k for k in workloads.WORKLOADS if k.endswith("_layer")),
                    help="block shape for --case gemm / attn")
-    p.add_argument("--case", default="layer", choices=["layer", "gemm", "attn"],
+    p.add_argument("--case", default="layer", choices=["layer", "gemm", "attn", "timeline"],
                    help="layer: the benchmark; gemm / attn: one kernel family on a small input "
-                        "(larger than L2) for profiler captures")
+                        "(larger than L2) for profiler captures; timeline: every launch of one "
+                        "filtered block step of --workload on its stream, with start and end times")
     return p.parse_args()
 
 
@@ -747,10 +748,46 @@ def run_case(args):
     print(json.dumps({"case": args.case, "kernels": res}))
 
 
+def run_timeline(args):
+    """One filtered block step as it runs (weight-gradient side stream and all):
+    each launch's stream, the time its launch reached the head of that stream,
+    its end, and its duration, from the library's per-launch events.  The
+    events recorded between launches can keep a kernel from being launched
+    before the one ahead of it has completed, so the step runs a little longer
+    than in the timed region."""
+    import torch
+    import sparse_backward_gemm_gb300 as cl
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    s = workloads.WORKLOADS[args.workload]
+    blk = Block(cl, s, dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        blk.step(blk.masks["filtered"], stream)
+    cl.collider_check(stream)
+    for rep in range(args.steps):
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        cl.collider_profile_enable(1)
+        blk.step(blk.masks["filtered"], stream)
+        torch.cuda.synchronize()
+        cl.collider_profile_enable(0)
+        print(f"# {args.workload}, step {rep}: launch, stream, kernel, M x N x K (GEMMs), start us, end us, us")
+        for i in range(cl.collider_profile_count()):
+            name, (m, n, k, dyn), ms = cl.collider_profile_get(i)
+            t0, t1, si = cl.collider_profile_get_span(i)
+            shape = f"{m}x{n}x{k}" if name == "tc_gemm" else "-"
+            print(f"{i:3d} {si} {name:16s} {shape:18s} {t0 * 1e3:8.1f} {t1 * 1e3:8.1f} {ms * 1e3:7.1f}")
+    cl.collider_check(stream)
+
+
 if __name__ == "__main__":
     a = parse()
     if a.impl == "reference":
         run_reference(a)
+    elif a.case == "timeline":
+        run_timeline(a)
     elif a.case != "layer":
         run_case(a)
     else:

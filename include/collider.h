@@ -104,6 +104,11 @@ long long collider_launch_count(int reset);
 int collider_profile_enable(int on);
 int collider_profile_count(void);
 int collider_profile_get(int i, const char** name, long long* mnk_dyn, float* ms);
+/* Record i on a timeline: the milliseconds from record 0's first event to
+ * record i's two events (the launch reaching the head of its stream, and the
+ * kernel done), and its stream, numbered 0, 1, ... in the order the records'
+ * streams first appear.  Waits for the events.  -1 for an index out of range. */
+int collider_profile_get_span(int i, float* start_ms, float* end_ms, int* stream_index);
 
 /* ------------------------------------------------------------------------ */
 /* a1. Compaction  (abstract: the dimension-reduced GEMM runs over the kept  */

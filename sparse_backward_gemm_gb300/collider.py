@@ -19,7 +19,7 @@ __all__ = [
     "ARCH_LLAMA", "ARCH_PHI", "NORM_RMS", "NORM_LAYER", "ACT_SWIGLU", "ACT_GELU_TANH",
     "LayerDesc", "LayerWeights", "LayerSaved", "LayerGrads", "LayerParams", "LayerActs", "EXPORTED",
     "collider_last_error", "collider_check", "collider_selftest_wait_timeout", "collider_launch_count",
-    "collider_profile_enable", "collider_profile_count", "collider_profile_get",
+    "collider_profile_enable", "collider_profile_count", "collider_profile_get", "collider_profile_get_span",
     "collider_select_keep", "collider_compact_workspace_size", "collider_compact", "collider_compact_noalloc",
     "collider_gather_rows",
     "collider_scatter_rows", "collider_linear_workspace_size", "collider_linear_bwd",
@@ -88,6 +88,7 @@ _SIGS = {
     "collider_profile_enable": (I, [I]),
     "collider_profile_count": (I, []),
     "collider_profile_get": (I, [I, C.POINTER(C.c_char_p), C.POINTER(C.c_longlong), C.POINTER(C.c_float)]),
+    "collider_profile_get_span": (I, [I, C.POINTER(C.c_float), C.POINTER(C.c_float), C.POINTER(C.c_int)]),
     "collider_select_keep": (I, [P, I, I, I, P, P]),
     "collider_compact_workspace_size": (SZ, [I, I]),
     "collider_compact": (I, [P, I, I, P, P, P, P, SZ, P]),
@@ -184,6 +185,14 @@ def collider_profile_enable(on: int) -> None:
 
 def collider_profile_count() -> int:
     return lib().collider_profile_count()
+
+
+def collider_profile_get_span(i: int):
+    """Returns (start_ms, end_ms, stream_index) of profile record i on the timeline of record 0."""
+    a, b, k = C.c_float(), C.c_float(), C.c_int()
+    if lib().collider_profile_get_span(i, C.byref(a), C.byref(b), C.byref(k)) != 0:
+        raise IndexError(i)
+    return a.value, b.value, k.value
 
 
 def collider_profile_get(i: int):

@@ -31,6 +31,7 @@ struct ProfRec {
   long long m, n, k;
   int dyn;
   cudaEvent_t e0, e1;
+  cudaStream_t stream;
 };
 thread_local bool g_prof_on = false;
 thread_local std::vector<ProfRec> g_prof;
@@ -136,7 +137,7 @@ void set_last_error(const char* msg) { g_msg = msg; }
 
 void prof_begin(const Ctx& c, const char* name, long long m, long long n, long long k, int dyn) {
   if (!g_prof_on) return;
-  ProfRec r{name, m, n, k, dyn, next_event(), next_event()};
+  ProfRec r{name, m, n, k, dyn, next_event(), next_event(), c.stream};
   if (r.e0) cudaEventRecord(r.e0, c.stream);
   g_prof.push_back(r);
   g_prof_stream = c.stream;
@@ -217,6 +218,26 @@ extern "C" int collider_profile_count(void) { return static_cast<int>(g_prof.siz
 
 // Record i: kernel name, GEMM extents (0 for other kernels), and elapsed ms.
 // Synchronises the recorded events.
+extern "C" int collider_profile_get_span(int i, float* start_ms, float* end_ms, int* stream_index) {
+  if (i < 0 || i >= static_cast<int>(g_prof.size())) return -1;
+  const ProfRec& r = g_prof[i];
+  const ProfRec& z = g_prof[0];
+  if (start_ms) *start_ms = -1.f;
+  if (end_ms) *end_ms = -1.f;
+  if (r.e1 && cudaEventSynchronize(r.e1) == cudaSuccess && z.e0) {
+    if (start_ms && r.e0) cudaEventElapsedTime(start_ms, z.e0, r.e0);
+    if (end_ms) cudaEventElapsedTime(end_ms, z.e0, r.e1);
+  }
+  if (stream_index) {
+    // distinct streams numbered in the order of their first record
+    std::vector<cudaStream_t> seen;
+    for (int j = 0; j <= i; ++j)
+      if (std::find(seen.begin(), seen.end(), g_prof[j].stream) == seen.end()) seen.push_back(g_prof[j].stream);
+    *stream_index = static_cast<int>(std::find(seen.begin(), seen.end(), r.stream) - seen.begin());
+  }
+  return 0;
+}
+
 extern "C" int collider_profile_get(int i, const char** name, long long* mnk_dyn, float* ms) {
   if (i < 0 || i >= static_cast<int>(g_prof.size())) return -1;
   const ProfRec& r = g_prof[i];
@@ -881,8 +902,10 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
     nb.x = static_cast<const __nv_bfloat16*>(sv->h); nb.rstd = sv->rstd2;
     nb.gamma = static_cast<const __nv_bfloat16*>(w->norm2_w);
     nb.out = L.dh_k; nb.cap = pad128(M); nb.dgamma = g->dnorm2_w; nb.part = L.norm_part2; nb.idx = idx; nb.n_kept = n_kept;
-    CK(launch_norm_rows(c, nb));                                                         // dh = dOut + norm2'
+    // the column pass needs only what the row pass reads, so it is forked
+    // before it and the two run side by side
     CK(fork_side(c, side, 7));
+    CK(launch_norm_rows(c, nb));                                                         // dh = dOut + norm2'
     CK(launch_norm_cols(cs, nb));                                                        // dnorm2_w, beside the chain
     dres = L.dh_k;
   } else {
@@ -936,8 +959,8 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
     nb.out = static_cast<__nv_bfloat16*>(g->dx); nb.cap = M; nb.out_full = (dx_full && !dense) ? 1 : 0;
     nb.dgamma = g->dnorm1_w; nb.dbeta = g->dnorm1_b; nb.part = L.norm_part;
     nb.idx = idx; nb.n_kept = n_kept;
+    CK(fork_side(c, side, 10));   // (the column pass needs only what the row pass reads)
     CK(launch_norm_rows(c, nb));
-    CK(fork_side(c, side, 10));
     CK(launch_norm_cols(cs, nb));   // dnorm1_w (dnorm1_b), beside the chain
   }
   CK(join_side(c, side, 4));   // the weight gradients are done when the chain is
