@@ -263,14 +263,13 @@ __device__ __forceinline__ int take_item(int* ticket) {
   return s_item;
 }
 
-// Adds this key block's dQ tile of (sequence b, head h, query block ib) into
-// the f32 accumulator in key-block order, so the sum is the same every run:
-// wait until the key blocks before this one (0 .. j-1) have added theirs,
-// then issue the TMA reduce-add(s).  The turn is passed on lazily: the next
-// call (or dq_turn_flush at the end) waits for this add to complete and then
-// releases it, so the issuing thread never stalls on its own add.  A wait
-// that runs out is recorded (COLLIDER_ERR_TIMEOUT) and the chain goes on
-// unordered rather than stall.  One thread; `pending` carries the turn to pass.
+// Key-block-ordered dQ accumulation.  The dQ tile of (sequence b, head h,
+// query block ib) is added into the f32 accumulator by key block 0, 1, ... in
+// turn, so the sum is the same every run.  The reducer thread of key block j
+// waits for the tile's turn counter to reach j (dq_turn_wait), issues its TMA
+// reduce-add, and once that add has completed passes the turn on to j + 1
+// (dq_turn_flush).  A wait that runs out is recorded (COLLIDER_ERR_TIMEOUT)
+// and the chain goes on unordered rather than stall.
 __device__ __forceinline__ void dq_turn_flush(int*& pending, int j) {
   if (!pending) return;
   tc::bulk_wait_all();              // the previous add has completed
@@ -278,25 +277,12 @@ __device__ __forceinline__ void dq_turn_flush(int*& pending, int j) {
   tc::release_turn(pending, j + 1);
   pending = nullptr;
 }
-// For a caller that passes the turn on itself (dq_turn_flush once its add
-// has completed): wait for this tile's turn and return it.
 __device__ __forceinline__ int* dq_turn_wait(const MainTc& p, int b, int h, int ib, int j, bool& broken,
                                              unsigned site) {
   int* turn = p.order + 1 + ((long long)b * p.H + h) * p.nqb_max + ib;
   if (!broken && !tc::wait_turn(turn, j, p.st, site)) broken = true;
   tc::fence_proxy_async_global();
   return turn;
-}
-template <typename Issue>
-__device__ __forceinline__ void ordered_dq_add(const MainTc& p, int b, int h, int ib, int j, bool& broken,
-                                               int*& pending, unsigned site, Issue issue) {
-  dq_turn_flush(pending, j);
-  int* turn = p.order + 1 + ((long long)b * p.H + h) * p.nqb_max + ib;
-  if (!broken && !tc::wait_turn(turn, j, p.st, site)) broken = true;
-  tc::fence_proxy_async_global();
-  issue();
-  tc::bulk_commit();
-  pending = turn;
 }
 
 __global__ void __launch_bounds__(tcattn::kThreads, 1)

@@ -57,8 +57,6 @@ __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.w
 
 // ---------------------------------------------------------------------------
 // small math / conversion helpers
-__device__ __forceinline__ float bf2f(__nv_bfloat16 v) { return __bfloat162float(v); }
-__device__ __forceinline__ __nv_bfloat16 f2bf(float v) { return __float2bfloat16_rn(v); }
 
 __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);

@@ -112,8 +112,6 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-// every bulk group this thread committed, except the most recent one, has completed
-__device__ __forceinline__ void bulk_wait_prior() { asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); }
 // make generic-proxy shared-memory writes visible to the async proxy (TMA, tcgen05)
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void named_bar(int id, int threads) {
