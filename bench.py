@@ -38,6 +38,7 @@ import workloads  # noqa: E402
 
 METRIC = "filtered-backward tokens/s, TFLOP/s vs bf16 TC peak, speedup vs unfiltered"
 WORKLOAD = "tinyllama_layer"
+SAVED = "lean"   # --saved
 
 
 def parse():
@@ -51,6 +52,9 @@ def parse():
                    help="time only the headline block (skip the other block shapes and the stack)")
     p.add_argument("--workload", default=WORKLOAD, choices=sorted(k for k in workloads.WORKLOADS if k.endswith("_layer")),
                    help="block shape for --case gemm / attn")
+    p.add_argument("--saved", default="lean", choices=["lean", "full"],
+                   help="saved set the filtered backward is given (Llama-style blocks): lean leaves out "
+                        "a, b and s, which it recomputes for the kept rows; full passes them")
     p.add_argument("--case", default="layer", choices=["layer", "gemm", "attn", "timeline"],
                    help="layer: the benchmark; gemm / attn: one kernel family on a small input "
                         "(larger than L2) for profiler captures; timeline: every launch of one "
@@ -63,6 +67,8 @@ def config_dict(s, l2):
                         f"d_model {s.D}, heads {s.H}/{s.Hkv}x{s.dh}, SwiGLU {s.F}, "
                         f"{int(s.f * 100)}% tokens filtered per sequence (Gumbel scores)",
             "global_batch": s.B, "seq_len": s.T, "filtered_fraction": s.f, "parallelism": "replicas",
+            "saved_set": ("lean: a, b, s recomputed for the kept rows" if SAVED == "lean" and s.arch == "llama"
+                          else "full"),
             "l2": l2}
 
 
@@ -181,6 +187,11 @@ class Block:
         self.weights = cl.LayerWeights(**{k: self.W[k].data_ptr() for k in
                                           ("norm1_w", "w_qkv", "w_o", "norm2_w", "w_up", "w_down") if k in self.W})
         self.sv = cl.LayerSaved(**{k: v.data_ptr() for k, v in self.saved.items()})
+        # what the filtered backward is given: without a, b and s (Llama-style
+        # blocks; recomputed for the kept rows) unless --saved full
+        lean = SAVED == "lean" and s.arch == "llama"
+        self.saved_filtered = {k: v for k, v in self.saved.items() if not (lean and k in ("a", "b", "s"))}
+        self.sv_filtered = cl.LayerSaved(**{k: v.data_ptr() for k, v in self.saved_filtered.items()})
         self.G = grad_buffers(s, dev)
         self.dx = torch.empty(s.M, s.D, dtype=torch.bfloat16, device=dev)
         self.grads = cl.LayerGrads(dx=self.dx.data_ptr(), **{k: v.data_ptr() for k, v in self.G.items()})
@@ -196,9 +207,10 @@ class Block:
         if mask is not None:
             cl.collider_compact(mask, s.B, s.T, self.idx, self.cu, self.nk, None, stream)
             index = (self.idx, self.cu, self.nk)
-        cl.collider_layer_bwd(self.desc, self.weights, self.sv if sv is None else sv,
-                              self.dout if dout is None else dout, cl.ROWS_FULL, *index,
-                              self.grads, cl.ROWS_FULL, self.ws, stream)
+        if sv is None:
+            sv = self.sv if mask is None else self.sv_filtered
+        cl.collider_layer_bwd(self.desc, self.weights, sv, self.dout if dout is None else dout, cl.ROWS_FULL,
+                              *index, self.grads, cl.ROWS_FULL, self.ws, stream)
 
 
 class Stack:
@@ -240,6 +252,11 @@ class Stack:
                                                               ("norm1_w", "w_qkv", "w_o", "norm2_w", "w_up", "w_down")})
                                           for W in self.Ws])
         self.Sc = (cl.LayerSaved * L)(*[cl.LayerSaved(**{k: v.data_ptr() for k, v in sv.items()}) for sv in self.saved])
+        # the filtered call's saved sets: without a, b and s unless --saved full
+        lean = SAVED == "lean"
+        self.Sc_filtered = (cl.LayerSaved * L)(*[cl.LayerSaved(**{k: v.data_ptr() for k, v in sv.items()
+                                                                  if not (lean and k in ("a", "b", "s"))})
+                                                 for sv in self.saved])
         self.G = [grad_buffers(ls, dev) for _ in range(L)]
         self.Gc = (cl.LayerGrads * L)(*[cl.LayerGrads(dx=None, **{k: v.data_ptr() for k, v in g.items()})
                                         for g in self.G])
@@ -261,7 +278,8 @@ class Stack:
         if mask is not None:
             cl.collider_compact(mask, ls.B, ls.T, self.idx, self.cu, self.nk, None, stream)
             index = (self.idx, self.cu, self.nk)
-        cl.collider_stack_bwd(self.desc, st.L, st.V, self.Wc, self.Sc, self.z, self.targets, self.ids, self.y,
+        cl.collider_stack_bwd(self.desc, st.L, st.V, self.Wc, self.Sc if mask is None else self.Sc_filtered,
+                              self.z, self.targets, self.ids, self.y,
                               self.xL, self.rstdf, self.nf, self.wlm, *index, self.Gc, self.dnf,
                               self.dlm, self.dE, self.ws, stream)
 
@@ -509,13 +527,14 @@ def run_ours(args):
     step_ms_prof = sum(v[1] for v in per.values()) / args.steps
 
     # ---- end to end through the C ABI with host buffers ------------------
-    # Every step copies its inputs (saved activations, dOut, keep-mask) from
-    # pinned host memory and its outputs (weight gradients, dx) back.  The
+    # Every step copies its inputs (the saved set the filtered call is given,
+    # dOut, keep-mask) from pinned host memory and its outputs (weight
+    # gradients, dx) back.  The
     # copies are pipelined the way a training loop prefetches: the inputs of
     # step i+1 go up on a copy stream while step i computes (two device input
     # sets), and step i's outputs come down on a third stream while step i+1
     # computes (two device output sets).  All copies sit inside the timed region.
-    host_in = {k: v.cpu().pin_memory() for k, v in saved.items()}
+    host_in = {k: v.cpu().pin_memory() for k, v in blk.saved_filtered.items()}
     host_dout = dout.cpu().pin_memory()
     host_mask = masks["filtered"].cpu().pin_memory()
     host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in G.items()}
@@ -525,7 +544,7 @@ def run_ours(args):
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
     sets = []
     for _ in range(2):
-        din = {k: torch.empty_like(v) for k, v in saved.items()}
+        din = {k: torch.empty_like(v) for k, v in blk.saved_filtered.items()}
         dgr = {k: torch.empty_like(v) for k, v in G.items()}
         ddx = torch.empty_like(dx)
         sets.append(dict(
@@ -784,6 +803,7 @@ def run_timeline(args):
 
 if __name__ == "__main__":
     a = parse()
+    SAVED = a.saved
     if a.impl == "reference":
         run_reference(a)
     elif a.case == "timeline":

@@ -277,7 +277,13 @@ typedef struct {
  *   attention output; lse f32 [B,H,T].
  *   LLAMA: h [M,D] = x + attn; b [M,D] = norm2(h); rstd2 f32 [M];
  *          up [M,2F] = [g | u]; s [M,F] = silu(g)*u.
- *   PHI:   up [M,F] = fc1 output before GELU; h, b, rstd2, s unused. */
+ *   PHI:   up [M,F] = fc1 output before GELU; h, b, rstd2, s unused.
+ * LLAMA: a, b and s may be NULL in a filtered call: the backward then
+ * recomputes them for the kept rows from x and rstd1 (a = norm1(x)), h and
+ * rstd2 (b), and up (s), with the same roundings as collider_layer_fwd, so
+ * the gradients are bit-identical to those from that forward's a, b and s.
+ * This shrinks what a training loop keeps (or uploads) by 2D + F values a
+ * token.  The dense call (NULL index) needs all three. */
 typedef struct {
   const void* x;
   const void* a;

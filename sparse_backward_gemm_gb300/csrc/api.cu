@@ -865,12 +865,13 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
     GatherJob j[4];
     int n = 0;
     if (llama) {
-      if (!dense) {
+      // (a saved set without s or b: the SwiGLU and norm2 backward recompute them below)
+      if (!dense && sv->s)
         j[n++] = GatherJob{static_cast<const char*>(sv->s), reinterpret_cast<char*>(L.s_k), (long long)F * 2,
                            (long long)F * 2, F * 2, 0};
+      if (!dense && sv->b)
         j[n++] = GatherJob{static_cast<const char*>(sv->b), reinterpret_cast<char*>(L.b_k), (long long)D * 2,
                            (long long)D * 2, D * 2, 0};
-      }
     } else {
       // gelu(f1) of the kept rows (of every row for a dense call: then not a gather)
       j[n++] = GatherJob{static_cast<const char*>(sv->up), reinterpret_cast<char*>(L.s_k), (long long)F * 2,
@@ -879,8 +880,13 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
     if (!dense) {
       j[n++] = GatherJob{static_cast<const char*>(sv->o), reinterpret_cast<char*>(L.o_k), (long long)Hd * 2,
                          (long long)Hd * 2, Hd * 2, 0};
-      j[n++] = GatherJob{static_cast<const char*>(sv->a), reinterpret_cast<char*>(L.a_k), (long long)D * 2,
-                         (long long)D * 2, D * 2, 0};
+      if (sv->a) {
+        j[n++] = GatherJob{static_cast<const char*>(sv->a), reinterpret_cast<char*>(L.a_k), (long long)D * 2,
+                           (long long)D * 2, D * 2, 0};
+      } else {   // RMSNorm: a = norm1(x), recomputed from x, rstd1 and norm1_w
+        j[n++] = GatherJob{static_cast<const char*>(sv->x), reinterpret_cast<char*>(L.a_k), (long long)D * 2,
+                           (long long)D * 2, D * 2, 2, sv->rstd1, static_cast<const __nv_bfloat16*>(w->norm1_w)};
+      }
     }
     if (n) CK(launch_gather(cs, j, n, M, pad128(M), dense ? nullptr : idx, n_kept));
   }
@@ -888,13 +894,18 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
   // 2. MLP
   const __nv_bfloat16* dres = L.dout_k;   // gradient flowing along the residual into the attention half
   if (llama) {
-    CK(gemm_dw(cs, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept, in_rows));     // dW_down = s^T dOut
+    // s_k and b_k come from the gathers above, or are recomputed by the
+    // SwiGLU backward and the norm2 row pass (saved set without s, b); the
+    // weight-gradient GEMMs that read them wait for those kernels then
+    const bool s_re = !dense && !sv->s, b_re = !dense && !sv->b;
+    if (!s_re) CK(gemm_dw(cs, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept, in_rows));   // dW_down = s^T dOut
     CK(gemm_dx(c, M, F, D, L.dout_k, w->w_down, L.ds_k, 1, 0, n_kept, in_rows));      // ds = dOut W_down^T
     c.pdl = pdl_allowed();
     CK(launch_swiglu_bwd(c, L.ds_k, 1, F, static_cast<const __nv_bfloat16*>(sv->up), L.dgu_k, M, pad128(M), idx,
-                         n_kept));
+                         n_kept, s_re ? L.s_k : nullptr));
     CK(fork_side(c, side, 1));
-    CK(gemm_dw(cs, M, D, Nup, L.b_k, D, L.dgu_k, Nup, g->dw_up, n_kept, in_rows));    // dW_up = b^T dgu
+    if (s_re) CK(gemm_dw(cs, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept, in_rows));
+    if (!b_re) CK(gemm_dw(cs, M, D, Nup, L.b_k, D, L.dgu_k, Nup, g->dw_up, n_kept, in_rows));  // dW_up = b^T dgu
     CK(gemm_dx(c, M, D, Nup, L.dgu_k, w->w_up, L.db_k, 0, 0, n_kept));                // db = dgu W_up^T
     NormBwdArgs nb{};
     nb.layer_norm = 0; nb.M = M; nb.D = D;
@@ -902,11 +913,16 @@ collider_status layer_bwd_impl(const Ctx& c_in, const collider_layer_desc* d, co
     nb.x = static_cast<const __nv_bfloat16*>(sv->h); nb.rstd = sv->rstd2;
     nb.gamma = static_cast<const __nv_bfloat16*>(w->norm2_w);
     nb.out = L.dh_k; nb.cap = pad128(M); nb.dgamma = g->dnorm2_w; nb.part = L.norm_part2; nb.idx = idx; nb.n_kept = n_kept;
+    nb.xn_out = b_re ? L.b_k : nullptr;   // b = norm2(h), recomputed
     // the column pass needs only what the row pass reads, so it is forked
     // before it and the two run side by side
     CK(fork_side(c, side, 7));
     CK(launch_norm_rows(c, nb));                                                         // dh = dOut + norm2'
     CK(launch_norm_cols(cs, nb));                                                        // dnorm2_w, beside the chain
+    if (b_re) {
+      CK(fork_side(c, side, 11));
+      CK(gemm_dw(cs, M, D, Nup, L.b_k, D, L.dgu_k, Nup, g->dw_up, n_kept, in_rows));
+    }
     dres = L.dh_k;
   } else {
     CK(gemm_dw(cs, M, F, D, L.s_k, F, L.dout_k, D, g->dw_down, n_kept, in_rows));     // dW2 = gelu(f1)^T dOut
@@ -972,15 +988,16 @@ collider_status check_layer_ptrs(const collider_layer_desc* d, const collider_la
                                  const collider_layer_saved* sv, const collider_layer_grads* g, bool need_dx) {
   if (!w || !sv || !g) return fail(COLLIDER_ERR_INVALID_ARG, "null weights/saved/grads struct");
   const bool llama = d->arch == COLLIDER_ARCH_LLAMA;
-  const void* req[] = {w->norm1_w, w->w_qkv, w->w_o, w->w_up, w->w_down, sv->x, sv->a, sv->rstd1, sv->qkv,
+  const void* req[] = {w->norm1_w, w->w_qkv, w->w_o, w->w_up, w->w_down, sv->x, sv->rstd1, sv->qkv,
                        sv->o, sv->lse, sv->up, g->dnorm1_w, g->dw_qkv, g->dw_o, g->dw_up, g->dw_down};
   for (const void* p : req)
     if (!p) return fail(COLLIDER_ERR_INVALID_ARG, "a required weight/saved/gradient pointer is null");
   if (need_dx && !g->dx) return fail(COLLIDER_ERR_INVALID_ARG, "grads->dx is null");
-  if (llama && (!w->norm2_w || !sv->h || !sv->b || !sv->rstd2 || !sv->s || !g->dnorm2_w))
-    return fail(COLLIDER_ERR_INVALID_ARG, "llama block needs norm2_w, h, b, rstd2, s and dnorm2_w");
-  if (!llama && (!sv->mean1 || !g->dnorm1_b))
-    return fail(COLLIDER_ERR_INVALID_ARG, "phi block needs mean1 and dnorm1_b");
+  // (llama: a, b and s may be NULL -- recomputed -- except in a dense call, checked there)
+  if (llama && (!w->norm2_w || !sv->h || !sv->rstd2 || !g->dnorm2_w))
+    return fail(COLLIDER_ERR_INVALID_ARG, "llama block needs norm2_w, h, rstd2 and dnorm2_w");
+  if (!llama && (!sv->a || !sv->mean1 || !g->dnorm1_b))
+    return fail(COLLIDER_ERR_INVALID_ARG, "phi block needs a, mean1 and dnorm1_b");
   const void* al[] = {w->norm1_w, w->w_qkv, w->w_o, w->w_up, w->w_down, w->norm2_w, sv->x, sv->a, sv->qkv,
                       sv->o, sv->h, sv->b, sv->up, sv->s, g->dx, g->dw_qkv, g->dw_o, g->dw_up, g->dw_down,
                       g->dnorm1_w, g->dnorm1_b, g->dnorm2_w, g->db_qkv, g->db_o, g->db_up, g->db_down};
@@ -1050,6 +1067,8 @@ extern "C" collider_status collider_layer_bwd(const collider_layer_desc* d, cons
                 "collider_layer_bwd: null or misaligned dOut, or only some of idx/cu_kept/n_kept given");
   s = check_layer_ptrs(d, w, sv, g, true);
   if (s != COLLIDER_OK) return s;
+  if (dense && d->arch == COLLIDER_ARCH_LLAMA && (!sv->a || !sv->b || !sv->s))
+    return fail(COLLIDER_ERR_INVALID_ARG, "collider_layer_bwd: the dense call reads a, b and s in place: none may be NULL");
   const size_t need = collider_layer_workspace_size(d);
   if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255))
     return fail(COLLIDER_ERR_INVALID_ARG, "collider_layer_bwd: needs %zu bytes of 256-aligned workspace", need);
@@ -1275,6 +1294,8 @@ extern "C" collider_status collider_stack_bwd(const collider_layer_desc* d, int 
   for (int l = 0; l < nL; ++l) {
     s = check_layer_ptrs(d, &w[l], &sv[l], &grads[l], false);
     if (s != COLLIDER_OK) return s;
+    if (dense && (!sv[l].a || !sv[l].b || !sv[l].s))
+      return fail(COLLIDER_ERR_INVALID_ARG, "collider_stack_bwd: the dense call reads a, b and s in place: none may be NULL");
   }
   const size_t need = collider_stack_workspace_size(d, nL, V);
   if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255))

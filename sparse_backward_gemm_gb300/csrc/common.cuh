@@ -56,6 +56,19 @@ constexpr uint64_t kWaitBudgetNs = 2000000000ull;  // 2 s
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
+// The forward's elementwise outputs that the backward may recompute instead of
+// reading them from the saved set (SwiGLU's s = silu(g) u, an RMSNorm output).
+// Forward and backward both call these, every rounding spelled out (no
+// contraction into a fused multiply-add the compiler might choose differently
+// at the two sites), so a recomputed value is the forward's bit for bit.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.f, expf(-g))), u);
+}
+__device__ __forceinline__ float norm_affine(float v, float mean, float rstd, float gamma, float beta) {
+  return __fmaf_rn(__fmul_rn(__fsub_rn(v, mean), rstd), gamma, beta);
+}
+
+// ---------------------------------------------------------------------------
 // small math / conversion helpers
 
 __device__ __forceinline__ void unpack8(const uint4& u, float* f) {

@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kNormThreads) norm_fwd_kernel(NormFwdArgs a) {
       unpack8(*reinterpret_cast<const uint4*>(a.gamma + 8 * ch), g);
       if (a.layer_norm) unpack8(*reinterpret_cast<const uint4*>(a.beta + 8 * ch), bt);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = (v[u][e] - mean) * rstd * g[e] + (a.layer_norm ? bt[e] : 0.f);
+      for (int e = 0; e < 8; ++e) o[e] = norm_affine(v[u][e], mean, rstd, g[e], a.layer_norm ? bt[e] : 0.f);
       *reinterpret_cast<uint4*>(a.out + (long long)row * a.D + 8 * ch) = pack8(o);
     }
   }
@@ -128,7 +128,7 @@ __global__ void swiglu_fwd_kernel(int M, int F, const __nv_bfloat16* up, __nv_bf
     unpack8(*reinterpret_cast<const uint4*>(in + c), g);
     unpack8(*reinterpret_cast<const uint4*>(in + F + c), u);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] = g[i] / (1.f + expf(-g[i])) * u[i];
+    for (int i = 0; i < 8; ++i) o[i] = silu_mul(g[i], u[i]);
     *reinterpret_cast<uint4*>(act + (long long)row * F + c) = pack8(o);
   }
 }
@@ -161,7 +161,7 @@ __global__ void act_fwd_kernel(int gelu, int M, int F, const float* acc, const _
       for (int i = 0; i < 8; ++i) u[i] = bf16_round(u[i] + (bias ? ub[i] : 0.f));
       *reinterpret_cast<uint4*>(up + (long long)row * Nup + F + c) = pack8(u);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = g[i] / (1.f + expf(-g[i])) * u[i];
+      for (int i = 0; i < 8; ++i) o[i] = silu_mul(g[i], u[i]);
     }
     *reinterpret_cast<uint4*>(act + (long long)row * F + c) = pack8(o);
   }

@@ -86,7 +86,11 @@ struct GatherJob {
   long long src_ld;   // bytes
   long long dst_ld;   // bytes
   int row_bytes;      // multiple of 16
-  int op;             // 0 copy, 1 gelu_tanh(bf16 row) -> bf16
+  int op;             // 0 copy, 1 gelu_tanh(bf16 row) -> bf16, 2 RMSNorm output of a bf16 row (below)
+  // op 2: dst = bf16(src * rstd[t] * gamma), the forward's norm_affine with
+  // mean 0 and no bias (t: the FULL row read)
+  const float* rstd;
+  const __nv_bfloat16* gamma;
 };
 constexpr int kMaxGatherJobs = 8;
 // idx may be null: identity (copy the first n_kept rows, zero the padding).
@@ -122,6 +126,8 @@ struct NormBwdArgs {
   const float* rstd;    // FULL f32 [M]
   const __nv_bfloat16* gamma;
   __nv_bfloat16* out;   // COMPACT bf16 [*, D], or FULL [M, D] rows idx[r] when out_full
+  __nv_bfloat16* xn_out;   // optional COMPACT bf16 [*, D]: the forward's norm output of each kept row
+                           // (RMSNorm: norm_affine(x, 0, rstd, gamma, 0)), padding rows zero
   long long cap;        // row capacity of out (zero padding stops there; COMPACT only)
   int out_full;         // 1: write row r to out row idx[r], no padding (filtered rows are the caller's)
   float* dgamma;
@@ -138,10 +144,11 @@ cudaError_t launch_norm_rows(const Ctx& c, const NormBwdArgs& a);
 cudaError_t launch_norm_cols(const Ctx& c, const NormBwdArgs& a);
 
 // SwiGLU backward: dgu[r] = [ds*u*sig(g)*(1+g*(1-sig(g))) | ds*silu(g)]
-// ds COMPACT (bf16 or f32) [*, F]; gu FULL bf16 [M, 2F] via idx; dgu COMPACT bf16 [*, 2F].
+// ds COMPACT (bf16 or f32) [*, F]; gu FULL bf16 [M, 2F] via idx; dgu COMPACT bf16 [*, 2F];
+// s_out (optional) COMPACT bf16 [*, F]: the forward's s = silu_mul(g, u) of each kept row.
 cudaError_t launch_swiglu_bwd(const Ctx& c, const void* ds, int ds_is_bf16, int F,
                               const __nv_bfloat16* gu, __nv_bfloat16* dgu, int M, long long cap,
-                              const int32_t* idx, const int32_t* n_kept);
+                              const int32_t* idx, const int32_t* n_kept, __nv_bfloat16* s_out = nullptr);
 // GELU-tanh backward: df1[r] = df2[r] * gelu'(f1[idx[r]]); df2 COMPACT, f1 FULL.
 cudaError_t launch_gelu_bwd(const Ctx& c, const void* df2, int df2_is_bf16, int F,
                             const __nv_bfloat16* f1, __nv_bfloat16* df1, int M, long long cap,

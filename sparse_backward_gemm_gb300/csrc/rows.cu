@@ -67,6 +67,19 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherBatch jb, int M, long
       }
       const uint4* s = reinterpret_cast<const uint4*>(J.src + (long long)t * J.src_ld);
       int v = lane;
+      if (J.op == 2) {
+        // the forward's RMSNorm output of row t, recomputed
+        const float rs = J.rstd[t];
+        for (; v < vecs; v += 32) {
+          float x[8], g[8], o[8];
+          unpack8(s[v], x);
+          unpack8(reinterpret_cast<const uint4*>(J.gamma)[v], g);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = norm_affine(x[e], 0.f, rs, g[e], 0.f);
+          d[v] = pack8(o);
+        }
+        continue;
+      }
       // four 16-byte loads in flight per lane before their stores
       for (; v + 96 < vecs; v += 128) {
         uint4 x0 = s[v], x1 = s[v + 32], x2 = s[v + 64], x3 = s[v + 96];
@@ -198,7 +211,10 @@ __global__ void __launch_bounds__(kNormWarps * 32) norm_rows_kernel(NormBwdArgs 
   for (int r = blockIdx.x * kNormWarps + (threadIdx.x >> 5); r < pad; r += gridDim.x * kNormWarps) {
     if (r >= nk) {
       __nv_bfloat16* orow = a.out + (long long)r * D;
-      for (int c = lane * 8; c < D; c += 256) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+      for (int c = lane * 8; c < D; c += 256) {
+        *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+        if (a.xn_out) *reinterpret_cast<uint4*>(a.xn_out + (long long)r * D + c) = make_uint4(0, 0, 0, 0);
+      }
       continue;
     }
     const int t = a.idx[r];
@@ -239,6 +255,12 @@ __global__ void __launch_bounds__(kNormWarps * 32) norm_rows_kernel(NormBwdArgs 
 #pragma unroll
       for (int k = 0; k < 8; ++k) o[k] += rstd * (dy[k] * gm[k] - (xv[k] - mu) * rstd * s_gx - s_g);
       *reinterpret_cast<uint4*>(orow + c) = pack8(o);
+      if (a.xn_out) {
+        float xn[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) xn[k] = norm_affine(xv[k], mu, rstd, gm[k], 0.f);
+        *reinterpret_cast<uint4*>(a.xn_out + (long long)r * D + c) = pack8(xn);
+      }
     }
   }
 }
@@ -281,7 +303,8 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const void* __restrict_
                                                          const __nv_bfloat16* __restrict__ gu,
                                                          __nv_bfloat16* __restrict__ dgu, int M, long long cap,
                                                          const int32_t* __restrict__ idx,
-                                                         const int32_t* __restrict__ n_kept, DevStatus* st) {
+                                                         const int32_t* __restrict__ n_kept, DevStatus* st,
+                                                         __nv_bfloat16* __restrict__ s_out) {
   grid_dep_wait();
   const int nk = *n_kept;
   const int pad = padded_rows(nk, cap);
@@ -294,6 +317,7 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const void* __restrict_
     if (r >= nk) {
       *reinterpret_cast<uint4*>(o + c) = make_uint4(0, 0, 0, 0);
       *reinterpret_cast<uint4*>(o + F + c) = make_uint4(0, 0, 0, 0);
+      if (s_out) *reinterpret_cast<uint4*>(s_out + (long long)r * F + c) = make_uint4(0, 0, 0, 0);
       continue;
     }
     const int t = idx[r];
@@ -310,6 +334,13 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const void* __restrict_
     }
     *reinterpret_cast<uint4*>(o + c) = pack8(dg);
     *reinterpret_cast<uint4*>(o + F + c) = pack8(du);
+    if (s_out) {
+      // the forward's s = silu(g) u of this kept row, recomputed
+      float sv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sv[i] = silu_mul(g[i], u[i]);
+      *reinterpret_cast<uint4*>(s_out + (long long)r * F + c) = pack8(sv);
+    }
   }
 }
 
@@ -533,10 +564,11 @@ cudaError_t launch_norm_bwd(const Ctx& c, const NormBwdArgs& a) {
 }
 
 cudaError_t launch_swiglu_bwd(const Ctx& c, const void* ds, int ds_is_bf16, int F, const __nv_bfloat16* gu,
-                              __nv_bfloat16* dgu, int M, long long cap, const int32_t* idx, const int32_t* n_kept) {
+                              __nv_bfloat16* dgu, int M, long long cap, const int32_t* idx, const int32_t* n_kept,
+                              __nv_bfloat16* s_out) {
   prof_begin(c, "swiglu_bwd");
   const cudaError_t e = launch_k(c, c.pdl, swiglu_bwd_kernel, dim3(grid_rows(c, cap * (F / 8), 256)), dim3(256), 0,
-                                 1, ds, ds_is_bf16, F, gu, dgu, M, cap, idx, n_kept, c.st);
+                                 1, ds, ds_is_bf16, F, gu, dgu, M, cap, idx, n_kept, c.st, s_out);
   prof_end(c);
   count_launch();
   return launched(e);

@@ -145,6 +145,43 @@ def test_forward_feeds_backward(arch):
         assert gu.rel_err(got[k], ref[k]) <= BF16_TOL, (k, gu.rel_err(got[k], ref[k]))
 
 
+@pytest.mark.parametrize("arch", ["llama", "qwen"])
+def test_backward_recomputes_a_b_s_exactly(arch):
+    """A filtered backward given a saved set without a, b and s recomputes them
+    for the kept rows with the forward's roundings: every gradient is
+    bit-identical to the one from the forward's own a, b and s.  The dense
+    call, which reads them in place, refuses such a saved set."""
+    s = SMALL[arch].with_(T=640)
+    w = workloads.layer_weights(s)
+    t = workloads.layer_inputs(s)
+    _, sv_ref = ob.block_forward(t["x"], w, s, round_saved=True)
+    ref = ob.block_backward(t["dout"], sv_ref, w, s, t["keep"])
+    F = DeviceForward(s, w)
+    x_t = gu.bf16(t["x"])
+    F.run(x_t)
+    L = gu.DeviceLayer(s, w, sv_ref)
+    full = F.saved_struct(x_t)
+    L.saved = full
+    idx, cu, nk = gu.compact(t["keep"])
+    dout = gu.bf16(t["dout"])
+    L.run(dout, idx, cu, nk)
+    a = L.results()
+    part = cl.LayerSaved(**{f: getattr(full, f) for f, _ in cl.LayerSaved._fields_})
+    part.a = part.b = part.s = None
+    L.saved = part
+    for v in L.grads_t.values():
+        v.fill_(float("nan"))
+    L.dx.fill_(float("nan"))
+    L.run(dout, idx, cu, nk)
+    b = L.results()
+    cl.collider_check()
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+        assert gu.rel_err(b[k], ref[k]) <= BF16_TOL, (k, gu.rel_err(b[k], ref[k]))
+    with pytest.raises(cl.ColliderError):
+        L.run(dout, None, None, None)
+
+
 FULL = ["tinyllama_layer", "qwen25_layer", "phi15_layer"]
 
 

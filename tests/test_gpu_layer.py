@@ -131,6 +131,21 @@ def test_block_backward_several_query_blocks(arch):
     _compare(got, ref, t["keep"])
 
 
+@pytest.mark.parametrize("arch", ["llama", "qwen"])
+def test_block_backward_without_a_b_s(arch):
+    """A saved set without a, b and s: the backward recomputes them for the
+    kept rows (from x, h and up); element by element against the oracle, on
+    sequences of several query and key blocks."""
+    s, w, t, saved, ref = _oracle_case(SMALL[arch].with_(B=2, T=512))
+    L = gu.DeviceLayer(s, w, saved)
+    L.saved.a = L.saved.b = L.saved.s = None
+    idx, cu, nk = gu.compact(t["keep"])
+    L.run(gu.bf16(t["dout"]), idx, cu, nk)
+    got = L.results()
+    cl.collider_check()
+    _compare(got, ref, t["keep"])
+
+
 def test_block_backward_reads_pinned_host_inputs():
     """The filtered call reads dOut and the saved set only at the kept rows,
     so they may stay in pinned host memory the device addresses directly: the
