@@ -55,7 +55,7 @@ extern "C" {
 typedef enum {
   COLLIDER_OK = 0,
   COLLIDER_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, workspace too small */
-  COLLIDER_ERR_UNSUPPORTED = 2, /* shape or option this build does not handle */
+  COLLIDER_ERR_UNSUPPORTED = 2, /* shape or option the library does not handle */
   COLLIDER_ERR_CUDA = 3,        /* a CUDA call failed (incl. an earlier asynchronous error) */
   COLLIDER_ERR_TIMEOUT = 4      /* a bounded in-kernel wait ran out (see collider_check) */
 } collider_status;
