@@ -242,7 +242,10 @@ def test_dense_call_rejects_a_partial_index():
         L.run(gu.bf16(t["dout"]), idx, None, None)
 
 
-def test_small_stack():
+@pytest.mark.parametrize("lean", [False, True])
+def test_small_stack(lean):
+    """A two-block stack against the oracle's stack backward; lean: every
+    block's saved set without a, b and s (recomputed for the kept rows)."""
     ls = SMALL["llama"].with_(B=1, T=192)
     st = workloads.StackShape(seed_base=84000, layer=ls, L=2, V=512)
     t = workloads.stack_tensors(st)
@@ -250,6 +253,9 @@ def test_small_stack():
     ref = ost.stack_backward(z, t["targets"], t["ids"], saved, t["layers"], t["normf_w"], t["w_lm"], ls, st.V,
                              t["keep"])
     layers = [gu.DeviceLayer(ls, t["layers"][l], saved["blocks"][l]) for l in range(st.L)]
+    if lean:
+        for L in layers:
+            L.saved.a = L.saved.b = L.saved.s = None
     W = (cl.LayerWeights * st.L)(*[L.weights for L in layers])
     S = (cl.LayerSaved * st.L)(*[L.saved for L in layers])
     G = (cl.LayerGrads * st.L)(*[L.grads for L in layers])
