@@ -90,6 +90,42 @@ def test_forward_argument_errors_need_no_gpu(lib):
     assert e.value.status == lib.ERR_UNSUPPORTED
 
 
+def test_layer_backward_saved_set_errors_need_no_gpu(lib):
+    """A Llama block's saved set may leave out a, b and s (recomputed), but not
+    h or rstd2, and not a, b or s in a dense call (which reads them in place);
+    a Phi block needs a.  All refused before any CUDA call."""
+    import workloads
+    s = workloads.WORKLOADS["tinyllama_layer"]
+    d = lib.LayerDesc(arch=lib.ARCH_LLAMA, B=s.B, T=s.T, D=s.D, H=s.H, Hkv=s.Hkv, dh=s.dh, F=s.F,
+                      rotary_dim=s.rotary_dim, rope_base=s.rope_base, norm=lib.NORM_RMS, eps=s.eps,
+                      act=lib.ACT_SWIGLU)
+    fake = 1 << 20   # never dereferenced: validation fails first
+    w = lib.LayerWeights(**{f: fake for f, _ in lib.LayerWeights._fields_})
+    g = lib.LayerGrads(**{f: fake for f, _ in lib.LayerGrads._fields_})
+    sv = lib.LayerSaved(**{f: fake for f, _ in lib.LayerSaved._fields_})
+    sv.mean1 = None
+    sv.a = sv.b = sv.s = None
+    with pytest.raises(lib.ColliderError) as e:      # dense call without a, b, s
+        lib.collider_layer_bwd(d, w, sv, fake, lib.ROWS_FULL, None, None, None, g, lib.ROWS_FULL, None, stream=0)
+    assert e.value.status == lib.ERR_INVALID_ARG and "dense" in str(e.value)
+    with pytest.raises(lib.ColliderError) as e:      # filtered: a, b, s may be absent; the workspace is next
+        lib.collider_layer_bwd(d, w, sv, fake, lib.ROWS_FULL, fake, fake, fake, g, lib.ROWS_FULL, None, stream=0)
+    assert e.value.status == lib.ERR_INVALID_ARG and "workspace" in str(e.value)
+    sv.h = None
+    with pytest.raises(lib.ColliderError) as e:      # h is needed
+        lib.collider_layer_bwd(d, w, sv, fake, lib.ROWS_FULL, fake, fake, fake, g, lib.ROWS_FULL, None, stream=0)
+    assert e.value.status == lib.ERR_INVALID_ARG and "h" in str(e.value)
+    p = workloads.WORKLOADS["phi15_layer"]
+    dp = lib.LayerDesc(arch=lib.ARCH_PHI, B=p.B, T=p.T, D=p.D, H=p.H, Hkv=p.Hkv, dh=p.dh, F=p.F,
+                       rotary_dim=p.rotary_dim, rope_base=p.rope_base, norm=lib.NORM_LAYER, eps=p.eps,
+                       act=lib.ACT_GELU_TANH)
+    svp = lib.LayerSaved(**{f: fake for f, _ in lib.LayerSaved._fields_})
+    svp.a = None
+    with pytest.raises(lib.ColliderError) as e:      # a Phi block needs a
+        lib.collider_layer_bwd(dp, w, svp, fake, lib.ROWS_FULL, fake, fake, fake, g, lib.ROWS_FULL, None, stream=0)
+    assert e.value.status == lib.ERR_INVALID_ARG and "phi" in str(e.value)
+
+
 def test_binding_has_no_fallback(lib):
     src = open(os.path.join(ROOT, "sparse_backward_gemm_gb300", "collider.py")).read()
     assert "oracle" not in src and "numpy" not in src
